@@ -1,0 +1,173 @@
+"""The oracle: a plain, slow, single-threaded CPU statement of the INT4
+group-quantized paged KV cache (quantize-on-append, dequantize, decode
+attention in fp64).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product path
+never does, and this package imports nothing from the product.
+
+The arithmetic lives in ``kvq_oracle.c`` (see its header for the cited
+passages and the layout it restates).  This module only marshals numpy arrays
+into that library through ctypes.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+(worked examples, closed forms, invariants and brute force); none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The oracle library.  KVQ_ORACLE_LIB may name another build of the same source
+    (the planted-mistake tests use it to load deliberately broken copies)."""
+    global _lib
+    if _lib is None:
+        path = os.environ.get("KVQ_ORACLE_LIB") or _build.build()
+        L = C.CDLL(path)
+        L.kvq_oracle_f32_to_f16.argtypes = [C.c_float]
+        L.kvq_oracle_f32_to_f16.restype = C.c_uint16
+        L.kvq_oracle_f16_to_f64.argtypes = [C.c_uint16]
+        L.kvq_oracle_f16_to_f64.restype = C.c_double
+        L.kvq_oracle_f32_to_f16_array.argtypes = [C.c_void_p, C.c_void_p, C.c_size_t]
+        L.kvq_oracle_f32_to_f16_array.restype = None
+        L.kvq_oracle_f16_to_f64_array.argtypes = [C.c_void_p, C.c_void_p, C.c_size_t]
+        L.kvq_oracle_f16_to_f64_array.restype = None
+        L.kvq_oracle_block_bytes.argtypes = [C.c_int] * 4
+        L.kvq_oracle_block_bytes.restype = C.c_size_t
+        L.kvq_oracle_fp16_kv_bytes.argtypes = [C.c_int, C.c_int, C.c_int, C.c_double]
+        L.kvq_oracle_fp16_kv_bytes.restype = C.c_double
+        L.kvq_oracle_quantize_group.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
+        L.kvq_oracle_quantize_group.restype = None
+        L.kvq_oracle_quantize_append.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
+                                                 C.c_void_p] + [C.c_int] * 8
+        L.kvq_oracle_quantize_append.restype = C.c_int
+        L.kvq_oracle_dequantize.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_int,
+                                            C.c_void_p, C.c_void_p, C.c_int] + [C.c_int] * 6
+        L.kvq_oracle_dequantize.restype = C.c_int
+        L.kvq_oracle_decode_attention.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
+                                                  C.c_int, C.c_int, C.c_double, C.c_void_p] + [C.c_int] * 6
+        L.kvq_oracle_decode_attention.restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle buffers must be C-contiguous"
+    return a.ctypes.data
+
+
+def f32_to_f16_bits(x: float) -> int:
+    return int(lib().kvq_oracle_f32_to_f16(float(x)))
+
+
+def f16_bits_to_f64(h: int) -> float:
+    return float(lib().kvq_oracle_f16_to_f64(int(h)))
+
+
+def f32_to_f16_array(x: np.ndarray) -> np.ndarray:
+    """fp32 array -> fp16 bit patterns (uint16), round to nearest even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().kvq_oracle_f32_to_f16_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def f16_to_f64_array(h: np.ndarray) -> np.ndarray:
+    """fp16 bit patterns (uint16) -> float64 values."""
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.float64)
+    lib().kvq_oracle_f16_to_f64_array(_ptr(h), _ptr(out), h.size)
+    return out
+
+
+def block_bytes(head_dim: int, page_size: int, group_k: int, group_v: int) -> int:
+    return int(lib().kvq_oracle_block_bytes(head_dim, page_size, group_k, group_v))
+
+
+def fp16_kv_bytes(layers: int, kv_heads: int, head_dim: int, tokens: float) -> float:
+    return float(lib().kvq_oracle_fp16_kv_bytes(layers, kv_heads, head_dim, float(tokens)))
+
+
+def quantize_group(x_f16: np.ndarray) -> tuple[np.ndarray, int]:
+    """One group of fp16 values -> (int8 codes in [-7, 7], fp16 scale bits)."""
+    x = np.ascontiguousarray(x_f16, dtype=np.float16)
+    codes = np.zeros(x.size, dtype=np.int8)
+    s = np.zeros(1, dtype=np.uint16)
+    lib().kvq_oracle_quantize_group(_ptr(x), int(x.size), _ptr(codes), _ptr(s))
+    return codes, int(s[0])
+
+
+class Layout:
+    """Cache geometry (kv heads, head_dim, page size, K/V group sizes, pages)."""
+
+    def __init__(self, num_kv_heads: int, head_dim: int, page_size: int, group_k: int, group_v: int,
+                 num_pages: int):
+        self.Hkv, self.d, self.P = num_kv_heads, head_dim, page_size
+        self.Gk, self.Gv, self.num_pages = group_k, group_v, num_pages
+
+    @property
+    def geom(self) -> list[int]:
+        return [self.Hkv, self.d, self.P, self.Gk, self.Gv, self.num_pages]
+
+    @property
+    def block_bytes(self) -> int:
+        return block_bytes(self.d, self.P, self.Gk, self.Gv)
+
+    @property
+    def pool_bytes(self) -> int:
+        return self.num_pages * self.Hkv * self.block_bytes
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+def quantize_append(L: Layout, pool: np.ndarray, k: np.ndarray, v: np.ndarray, block_table: np.ndarray,
+                    start_pos: np.ndarray) -> None:
+    """In-place quantize-on-append into the uint8 pool.  k, v: fp16 [B, n_new, Hkv, d]."""
+    k = np.ascontiguousarray(k, dtype=np.float16)
+    v = np.ascontiguousarray(v, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sp = np.ascontiguousarray(start_pos, dtype=np.int32)
+    B, n_new = k.shape[0], k.shape[1]
+    assert pool.dtype == np.uint8 and pool.size >= L.pool_bytes
+    rc = lib().kvq_oracle_quantize_append(_ptr(pool), _ptr(k), _ptr(v), _ptr(bt), int(bt.shape[1]), _ptr(sp),
+                                          B, n_new, *L.geom)
+    _check(rc, "quantize_append")
+
+
+def dequantize(L: Layout, pool: np.ndarray, block_table: np.ndarray, b: int, start: int, n: int,
+               out_fp16: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """Positions [start, start+n) of sequence b -> (K, V) each [n, Hkv, d] (fp32, or fp16)."""
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    dt = np.float16 if out_fp16 else np.float32
+    ok = np.zeros((n, L.Hkv, L.d), dtype=dt)
+    ov = np.zeros((n, L.Hkv, L.d), dtype=dt)
+    rc = lib().kvq_oracle_dequantize(_ptr(pool), _ptr(bt), int(bt.shape[1]), b, start, n, _ptr(ok), _ptr(ov),
+                                     1 if out_fp16 else 0, *L.geom)
+    _check(rc, "dequantize")
+    return ok, ov
+
+
+def decode_attention(L: Layout, pool: np.ndarray, q: np.ndarray, block_table: np.ndarray, seq_lens: np.ndarray,
+                     softmax_scale: float) -> np.ndarray:
+    """fp64 decode attention over the quantized cache.  q: fp16 [B, Hq, d] -> fp64 [B, Hq, d]."""
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, _ = q.shape
+    out = np.zeros((B, Hq, L.d), dtype=np.float64)
+    rc = lib().kvq_oracle_decode_attention(_ptr(pool), _ptr(q), _ptr(bt), int(bt.shape[1]), _ptr(sl), B, Hq,
+                                           float(softmax_scale), _ptr(out), *L.geom)
+    _check(rc, "decode_attention")
+    return out

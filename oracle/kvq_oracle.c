@@ -1,0 +1,343 @@
+/*
+ * kvq_oracle.c -- the oracle: a plain, slow, single-threaded CPU statement of
+ * what the INT4 group-quantized paged KV cache computes.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this file's library.  The product path
+ * (the CUDA library and its Python binding) never includes, links or calls
+ * anything here, and nothing here includes the product's headers: the layout
+ * below is restated from the specification in prose, not shared code.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [Q] "4-bit KV cache compression" (lpnh.cn/news/2042373), section 2.1
+ *      "symmetric uniform quantization, one scale per group":
+ *      amax = max |x| over a group, scale = amax / 7, an all-zero group takes
+ *      scale 1, q = round(x / scale) clamped to [-7, 7], dequant = q * scale.
+ *      Section 2.2: storage bits per element 4 + 16/G; K grouped at 64 and V
+ *      at 128 along the last (head) dimension.
+ *  [M] "AI inference tuning: KV Cache optimisation and memory management"
+ *      (bxzpzcl.cn/news/2871434), section 3.1 (KVCacheManager: fixed pages of
+ *      page_size tokens, ceil(n / page_size) pages per request) and section
+ *      3.2 (scaled dot-product attention with scale = head_dim^-0.5, softmax,
+ *      then weights @ V; GQA repeats each KV head over n_rep = Hq / Hkv
+ *      consecutive query heads).
+ *  [S] "LLM long-context inference: managing the KV cache with an INT4 state
+ *      machine" (pwwt.cn/news/4219524), section 2 (KV bytes per token
+ *      2 * layers * heads * head_dim * dtype_size) and section 5 step 5
+ *      (the inference layer reads INT4 directly and dequantizes inside the
+ *      operator).
+ *
+ * Conventions the pages leave open, fixed by the workload statement:
+ *  - the scale is computed as fp32 amax / 7.0f and then rounded to fp16
+ *    (round-to-nearest-even); the zero test is made on that fp16 value;
+ *  - codes are clamp(rne(fp32(x) / fp32(scale16)), -7, 7), the division an
+ *    IEEE fp32 division, the rounding half-to-even;
+ *  - a code c is stored as the nibble c + 8; byte j of a row holds the code of
+ *    element 2j in its low nibble and element 2j+1 in its high nibble.
+ *
+ * Paged layout (one block per (page, kv-head); block index page*Hkv + h):
+ *    K codes   P rows x d/2 bytes        (row = token slot in the page)
+ *    V codes   P rows x d/2 bytes
+ *    K scales  P rows x d/Gk fp16, little-endian
+ *    V scales  P rows x d/Gv fp16
+ *    zero padding up to a multiple of 16 bytes.
+ * Token position t of sequence b lives in page block_table[b*max_blocks + t/P],
+ * slot t % P.
+ *
+ * Build: gcc -O2 -std=c11 -fno-fast-math -ffp-contract=off -shared -fPIC.
+ * Contraction is off so every fp32 operation rounds exactly once.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_ERANGE 2
+
+/* ------------------------------------------------------------------------ */
+/* IEEE-754 binary16 <-> binary32 / binary64, written from the format's      */
+/* definition: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.     */
+/* ------------------------------------------------------------------------ */
+
+/* Round v / 2^s to an integer, ties to even (s >= 1). */
+static uint64_t shift_right_rne(uint64_t v, int s) {
+    if (s >= 64) return 0;
+    uint64_t q = v >> s;
+    uint64_t rem = v & ((((uint64_t)1) << s) - 1);
+    uint64_t half = ((uint64_t)1) << (s - 1);
+    if (rem > half || (rem == half && (q & 1))) q += 1;
+    return q;
+}
+
+uint16_t kvq_oracle_f32_to_f16(float f) {
+    uint32_t x;
+    memcpy(&x, &f, sizeof x);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    uint32_t ax = x & 0x7fffffffu;
+    if (ax >= 0x7f800000u) /* infinity or NaN */
+        return (uint16_t)(sign | 0x7c00u | (ax > 0x7f800000u ? 0x0200u : 0u));
+    if (ax < 0x00800000u) /* fp32 zero or subnormal: below 2^-126, far under half the smallest fp16 subnormal */
+        return sign;
+    int e = (int)(ax >> 23) - 127;              /* value = M * 2^(e-23) */
+    uint64_t M = (uint64_t)((ax & 0x7fffffu) | 0x800000u);
+    if (e >= -14) {
+        /* normal fp16 candidate: keep 11 significant bits */
+        uint64_t m16 = shift_right_rne(M, 13);
+        if (m16 == 2048) { m16 = 1024; e += 1; }
+        if (e > 15) return (uint16_t)(sign | 0x7c00u);
+        return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(m16 - 1024));
+    }
+    /* subnormal fp16: value / 2^-24 = M * 2^(e+1), rounded to an integer k in [0, 1024] */
+    int s = -(e + 1);
+    uint64_t k = shift_right_rne(M, s);
+    return (uint16_t)(sign | (uint16_t)k); /* k == 1024 is exactly the smallest normal */
+}
+
+double kvq_oracle_f16_to_f64(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int ex = (h >> 10) & 0x1f;
+    int fr = h & 0x3ff;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)fr, -24);
+    else if (ex == 31)
+        v = fr ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + fr), ex - 25);
+    return sign ? -v : v;
+}
+
+float kvq_oracle_f16_to_f32(uint16_t h) { return (float)kvq_oracle_f16_to_f64(h); }
+
+/* Array forms of the two conversions (used to check them against other implementations in bulk). */
+void kvq_oracle_f32_to_f16_array(const float *x, uint16_t *out, size_t n) {
+    for (size_t i = 0; i < n; ++i) out[i] = kvq_oracle_f32_to_f16(x[i]);
+}
+void kvq_oracle_f16_to_f64_array(const uint16_t *h, double *out, size_t n) {
+    for (size_t i = 0; i < n; ++i) out[i] = kvq_oracle_f16_to_f64(h[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sizes                                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of one (page, kv-head) block, per the layout in the file header. */
+size_t kvq_oracle_block_bytes(int head_dim, int page_size, int group_k, int group_v) {
+    size_t codes = (size_t)page_size * (size_t)head_dim;                 /* K and V: P*d/2 each */
+    size_t scales = 2u * (size_t)page_size * (size_t)(head_dim / group_k + head_dim / group_v);
+    size_t raw = codes + scales;
+    return (raw + 15u) / 16u * 16u;
+}
+
+/* FP16 KV bytes: 2 (K and V) * layers * kv_heads * head_dim * tokens * 2 bytes
+ * ([S] section 2; [Q] section 1.2 with S*B tokens). */
+double kvq_oracle_fp16_kv_bytes(int layers, int kv_heads, int head_dim, double tokens) {
+    return 2.0 * layers * kv_heads * head_dim * tokens * 2.0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantization of one group ([Q] section 2.1)                                */
+/* ------------------------------------------------------------------------ */
+
+/* x: G fp16 values.  codes: G signed codes in [-7, 7].  *scale16: fp16 bits. */
+void kvq_oracle_quantize_group(const uint16_t *x, int G, int8_t *codes, uint16_t *scale16) {
+    float amax = 0.0f;
+    for (int i = 0; i < G; ++i) {
+        float a = fabsf(kvq_oracle_f16_to_f32(x[i]));
+        if (a > amax) amax = a;
+    }
+    float s32 = amax / 7.0f;
+    uint16_t s16 = kvq_oracle_f32_to_f16(s32);
+    if ((s16 & 0x7fffu) == 0) s16 = 0x3c00u; /* an all-zero group (or a scale that rounds to zero) gets 1 */
+    float s = kvq_oracle_f16_to_f32(s16);
+    for (int i = 0; i < G; ++i) {
+        float q = kvq_oracle_f16_to_f32(x[i]) / s;
+        float r = nearbyintf(q); /* default rounding mode: to nearest, ties to even */
+        if (r > 7.0f) r = 7.0f;
+        if (r < -7.0f) r = -7.0f;
+        codes[i] = (int8_t)r;
+    }
+    *scale16 = s16;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged pool access                                                          */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int Hkv, d, P, Gk, Gv, num_pages;
+    size_t block;
+} layout_t;
+
+static int make_layout(layout_t *L, int Hkv, int d, int P, int Gk, int Gv, int num_pages) {
+    if (Hkv <= 0 || d <= 0 || P <= 0 || Gk <= 0 || Gv <= 0 || num_pages <= 0) return ORACLE_EINVAL;
+    if (d % 2 || d % Gk || d % Gv) return ORACLE_EINVAL;
+    L->Hkv = Hkv; L->d = d; L->P = P; L->Gk = Gk; L->Gv = Gv; L->num_pages = num_pages;
+    L->block = kvq_oracle_block_bytes(d, P, Gk, Gv);
+    return ORACLE_OK;
+}
+
+static uint8_t *block_ptr(const layout_t *L, uint8_t *pool, int page, int h) {
+    return pool + ((size_t)page * (size_t)L->Hkv + (size_t)h) * L->block;
+}
+static uint8_t *k_codes_row(const layout_t *L, uint8_t *blk, int slot) { return blk + (size_t)slot * (size_t)(L->d / 2); }
+static uint8_t *v_codes_row(const layout_t *L, uint8_t *blk, int slot) {
+    return blk + (size_t)L->P * (size_t)(L->d / 2) + (size_t)slot * (size_t)(L->d / 2);
+}
+static uint8_t *k_scales_row(const layout_t *L, uint8_t *blk, int slot) {
+    return blk + (size_t)L->P * (size_t)L->d + (size_t)slot * (size_t)(L->d / L->Gk) * 2u;
+}
+static uint8_t *v_scales_row(const layout_t *L, uint8_t *blk, int slot) {
+    return blk + (size_t)L->P * (size_t)L->d + (size_t)L->P * (size_t)(L->d / L->Gk) * 2u +
+           (size_t)slot * (size_t)(L->d / L->Gv) * 2u;
+}
+
+static void put_u16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)(v & 0xff); p[1] = (uint8_t)(v >> 8); }
+static uint16_t get_u16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* Quantize one row of d fp16 values in groups of G; write codes (d/2 bytes) and scales (d/G fp16). */
+static void quantize_row(const uint16_t *x, int d, int G, uint8_t *codes_row, uint8_t *scales_row) {
+    int8_t c[256];
+    for (int g0 = 0; g0 < d; g0 += G) {
+        uint16_t s16;
+        kvq_oracle_quantize_group(x + g0, G, c + g0, &s16);
+        put_u16(scales_row + (size_t)(g0 / G) * 2u, s16);
+    }
+    for (int j = 0; j < d / 2; ++j) {
+        unsigned lo = (unsigned)(c[2 * j] + 8);
+        unsigned hi = (unsigned)(c[2 * j + 1] + 8);
+        codes_row[j] = (uint8_t)(lo | (hi << 4));
+    }
+}
+
+/* Dequantize one row: element i = (nibble_i - 8) * scale[i / G], exact in fp32. */
+static void dequant_row(const uint8_t *codes_row, const uint8_t *scales_row, int d, int G, float *out) {
+    for (int i = 0; i < d; ++i) {
+        uint8_t byte = codes_row[i / 2];
+        int nib = (i & 1) ? (byte >> 4) : (byte & 0x0f);
+        float s = kvq_oracle_f16_to_f32(get_u16(scales_row + (size_t)(i / G) * 2u));
+        out[i] = (float)(nib - 8) * s;
+    }
+}
+
+/*
+ * Quantize-on-append.  k, v: fp16 [B, n_new, Hkv, d] contiguous.  For every b
+ * and every t < n_new the token is written at position start_pos[b] + t.
+ * Returns ORACLE_ERANGE (and writes nothing further) if a position falls
+ * outside the block table or a page id is outside [0, num_pages).
+ */
+int kvq_oracle_quantize_append(uint8_t *pool, const uint16_t *k, const uint16_t *v,
+                               const int32_t *block_table, int max_blocks, const int32_t *start_pos,
+                               int B, int n_new, int Hkv, int d, int P, int Gk, int Gv, int num_pages) {
+    layout_t L;
+    if (make_layout(&L, Hkv, d, P, Gk, Gv, num_pages) || d > 256 || B < 0 || n_new < 0) return ORACLE_EINVAL;
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < n_new; ++t) {
+            long pos = (long)start_pos[b] + t;
+            if (pos < 0 || pos / P >= max_blocks) return ORACLE_ERANGE;
+            int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(pos / P)];
+            if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+            int slot = (int)(pos % P);
+            for (int h = 0; h < Hkv; ++h) {
+                size_t off = (((size_t)b * (size_t)n_new + (size_t)t) * (size_t)Hkv + (size_t)h) * (size_t)d;
+                uint8_t *blk = block_ptr(&L, pool, page, h);
+                quantize_row(k + off, d, Gk, k_codes_row(&L, blk, slot), k_scales_row(&L, blk, slot));
+                quantize_row(v + off, d, Gv, v_codes_row(&L, blk, slot), v_scales_row(&L, blk, slot));
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Dequantize positions [start, start+n) of sequence b into out_k, out_v laid
+ * out [n, Hkv, d].  out_fp16 != 0: fp16 bits (RNE of the exact fp32 product);
+ * otherwise fp32.
+ */
+int kvq_oracle_dequantize(const uint8_t *pool, const int32_t *block_table, int max_blocks, int b, int start,
+                          int n, void *out_k, void *out_v, int out_fp16,
+                          int Hkv, int d, int P, int Gk, int Gv, int num_pages) {
+    layout_t L;
+    if (make_layout(&L, Hkv, d, P, Gk, Gv, num_pages) || d > 256 || start < 0 || n < 0) return ORACLE_EINVAL;
+    float rk[256], rv[256];
+    for (int t = 0; t < n; ++t) {
+        long pos = (long)start + t;
+        if (pos / P >= max_blocks) return ORACLE_ERANGE;
+        int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(pos / P)];
+        if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+        int slot = (int)(pos % P);
+        for (int h = 0; h < Hkv; ++h) {
+            uint8_t *blk = block_ptr(&L, (uint8_t *)pool, page, h);
+            dequant_row(k_codes_row(&L, blk, slot), k_scales_row(&L, blk, slot), d, Gk, rk);
+            dequant_row(v_codes_row(&L, blk, slot), v_scales_row(&L, blk, slot), d, Gv, rv);
+            size_t off = ((size_t)t * (size_t)Hkv + (size_t)h) * (size_t)d;
+            for (int i = 0; i < d; ++i) {
+                if (out_fp16) {
+                    ((uint16_t *)out_k)[off + i] = kvq_oracle_f32_to_f16(rk[i]);
+                    ((uint16_t *)out_v)[off + i] = kvq_oracle_f32_to_f16(rv[i]);
+                } else {
+                    ((float *)out_k)[off + i] = rk[i];
+                    ((float *)out_v)[off + i] = rv[i];
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Decode attention over the quantized cache, in fp64 ([M] section 3.2 with the
+ * dequantization of [Q] section 2.1 inside, as [S] section 5 step 5 puts it).
+ * q: fp16 [B, Hq, d].  Query head hq reads KV head hq / (Hq / Hkv).  Sequence
+ * b attends to positions 0 .. seq_lens[b]-1 (the appended token included).
+ * out: fp64 [B, Hq, d].  A sequence of length 0 yields zeros.
+ */
+int kvq_oracle_decode_attention(const uint8_t *pool, const uint16_t *q, const int32_t *block_table,
+                                int max_blocks, const int32_t *seq_lens, int B, int Hq, double softmax_scale,
+                                double *out, int Hkv, int d, int P, int Gk, int Gv, int num_pages) {
+    layout_t L;
+    if (make_layout(&L, Hkv, d, P, Gk, Gv, num_pages) || d > 256 || Hq <= 0 || Hq % Hkv) return ORACLE_EINVAL;
+    int n_rep = Hq / Hkv;
+    float rk[256], rv[256];
+    for (int b = 0; b < B; ++b) {
+        int len = seq_lens[b];
+        if (len < 0 || (len + P - 1) / P > max_blocks) return ORACLE_ERANGE;
+        for (int hq = 0; hq < Hq; ++hq) {
+            int h = hq / n_rep;
+            const uint16_t *qrow = q + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            double *o = out + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            for (int i = 0; i < d; ++i) o[i] = 0.0;
+            if (len == 0) continue;
+            /* pass 1: logits and their maximum */
+            double zmax = -INFINITY;
+            for (int t = 0; t < len; ++t) {
+                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+                if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+                uint8_t *blk = block_ptr(&L, (uint8_t *)pool, page, h);
+                dequant_row(k_codes_row(&L, blk, t % P), k_scales_row(&L, blk, t % P), d, Gk, rk);
+                double z = 0.0;
+                for (int i = 0; i < d; ++i) z += kvq_oracle_f16_to_f64(qrow[i]) * (double)rk[i];
+                z *= softmax_scale;
+                if (z > zmax) zmax = z;
+            }
+            /* pass 2: softmax weights and the weighted sum of values */
+            double l = 0.0;
+            for (int t = 0; t < len; ++t) {
+                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+                uint8_t *blk = block_ptr(&L, (uint8_t *)pool, page, h);
+                dequant_row(k_codes_row(&L, blk, t % P), k_scales_row(&L, blk, t % P), d, Gk, rk);
+                dequant_row(v_codes_row(&L, blk, t % P), v_scales_row(&L, blk, t % P), d, Gv, rv);
+                double z = 0.0;
+                for (int i = 0; i < d; ++i) z += kvq_oracle_f16_to_f64(qrow[i]) * (double)rk[i];
+                z *= softmax_scale;
+                double p = exp(z - zmax);
+                l += p;
+                for (int i = 0; i < d; ++i) o[i] += p * (double)rv[i];
+            }
+            for (int i = 0; i < d; ++i) o[i] /= l;
+        }
+    }
+    return ORACLE_OK;
+}

@@ -1,0 +1,69 @@
+"""Planted mistakes: each case copies the oracle's C source, plants one plausible
+mistake (a wrong rounding, a dropped term, a swapped index, a wrong sign or
+offset), compiles the copy on the CPU and runs the pin suite against it.  Every
+planted mistake must make at least one pin fail; a survivor means the pins do
+not constrain that part of the oracle."""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "kvq_oracle.c")
+PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
+
+# (name, text in the oracle, replacement): each text occurs exactly once
+MUTANTS = [
+    ("round_half_up", "float r = nearbyintf(q);", "float r = floorf(q + 0.5f);"),
+    ("scale_not_rounded_to_fp16", "float s = kvq_oracle_f16_to_f32(s16);", "float s = (amax > 0.0f) ? s32 : 1.0f;"),
+    ("divide_by_8", "float s32 = amax / 7.0f;", "float s32 = amax / 8.0f;"),
+    ("zero_rule_before_rounding", "if ((s16 & 0x7fffu) == 0) s16 = 0x3c00u;", "if (amax == 0.0f) s16 = 0x3c00u;"),
+    ("clamp_to_minus_8", "if (r < -7.0f) r = -7.0f;", "if (r < -8.0f) r = -8.0f;"),
+    ("nibbles_swapped", "codes_row[j] = (uint8_t)(lo | (hi << 4));", "codes_row[j] = (uint8_t)(hi | (lo << 4));"),
+    ("offset_7", "unsigned lo = (unsigned)(c[2 * j] + 8);", "unsigned lo = (unsigned)(c[2 * j] + 7);"),
+    ("dequant_wrong_group", "float s = kvq_oracle_f16_to_f32(get_u16(scales_row + (size_t)(i / G) * 2u));",
+     "float s = kvq_oracle_f16_to_f32(get_u16(scales_row + (size_t)((i / G) ^ 1) % (size_t)(d / G) * 2u));"),
+    ("gqa_modulo_map", "int h = hq / n_rep;", "int h = hq % Hkv;"),
+    ("no_max_subtraction", "double p = exp(z - zmax);", "double p = exp(z);"),
+    ("softmax_scale_dropped_in_pass2", "        z *= softmax_scale;\n                double p",
+     "        double p"),
+    ("page_slot_swapped", "uint8_t *blk = block_ptr(&L, pool, page, h);\n                quantize_row",
+     "uint8_t *blk = block_ptr(&L, pool, page, (h + 1) % Hkv);\n                quantize_row"),
+    ("v_scales_overlap_k_scales", "return blk + (size_t)L->P * (size_t)L->d + (size_t)L->P * (size_t)(L->d / L->Gk) * 2u +",
+     "return blk + (size_t)L->P * (size_t)L->d + (size_t)(L->d / L->Gk) * 2u +"),
+    ("f16_ties_away", "if (rem > half || (rem == half && (q & 1))) q += 1;", "if (rem >= half) q += 1;"),
+    ("f16_subnormal_off_by_one", "int s = -(e + 1);", "int s = -e;"),
+    ("last_token_dropped", "for (int t = 0; t < len; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk",
+     "for (int t = 0; t < len - 1; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk"),
+]
+
+
+def _run_mutant(name, old, new, tmp):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"{name}: anchor occurs {src.count(old)} times"
+    mdir = os.path.join(tmp, name)
+    os.makedirs(mdir, exist_ok=True)
+    msrc = os.path.join(mdir, "kvq_oracle.c")
+    with open(msrc, "w") as f:
+        f.write(src.replace(old, new))
+    lib = os.path.join(mdir, "libkvq_oracle.so")
+    sys.path.insert(0, ROOT)
+    from oracle import build as obuild
+    obuild.build(msrc, lib, force=True)
+    env = dict(os.environ, KVQ_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", PINS, "-x", "-q", "-p", "no:cacheprovider"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return name, r.returncode, r.stdout[-400:]
+
+
+def test_every_planted_mistake_is_caught(tmp_path):
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
+        results = list(ex.map(lambda m: _run_mutant(*m, str(tmp_path)), MUTANTS))
+    survivors = [(n, out) for n, rc, out in results if rc == 0]
+    assert not survivors, f"planted mistakes the pins missed: {survivors}"
+    # and the unmodified oracle passes the same suite (rc 0) -- run in-process elsewhere
+    assert all(rc == 1 for _, rc, _ in results), [(n, rc, out) for n, rc, out in results if rc != 1]

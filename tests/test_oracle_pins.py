@@ -1,0 +1,477 @@
+"""Pins for the oracle: checks against what the pages and the mathematics fix,
+never against a retyping of the oracle's own formulas.
+
+ - fp16 conversion: exhaustive and randomized agreement with numpy's float16
+   (an independent implementation of IEEE-754 binary16 rounding).
+ - sizes: the bits-per-element table of "4-bit KV cache compression"
+   (lpnh.cn/news/2042373) section 2.2 and the FP16 KV size figures of its
+   section 1.2 and of "LLM long-context inference: managing the KV cache with an
+   INT4 state machine" (pwwt.cn/news/4219524) sections 2 and 6.2.
+ - quantization: hand-worked examples (tests/golden/quantize_examples.txt),
+   brute-force nearest-code search, the error bound |x - x^| <= s/2, the
+   max-code invariant and sign symmetry.
+ - layout: a hand-worked byte map (tests/golden/layout_example.txt).
+ - attention: special cases with closed forms (one token, equal keys, one
+   dominant logit, zero softmax scale), brute force against numpy/scipy
+   softmax attention on tiny inputs, GQA = MHA on repeated KV heads ("AI
+   inference tuning: KV Cache optimisation..." section 3.2), page-table
+   permutation invariance and exact scaling by powers of two.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ----------------------------------------------------------------------------
+# fp16 conversions
+# ----------------------------------------------------------------------------
+
+def test_f16_to_f64_exhaustive():
+    h = np.arange(65536, dtype=np.uint16)
+    ours = oracle.f16_to_f64_array(h)
+    ref = h.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_f32_to_f16_midpoints_and_random():
+    rng = np.random.default_rng(0)
+    # every finite fp16 value, its exact fp32 image, and the midpoints to its neighbours
+    h = np.arange(0, 0x7c00, dtype=np.uint16)
+    v = h.view(np.float16).astype(np.float64)
+    nxt = np.append(v[1:], 65520.0)  # 65520 is the midpoint rounding to infinity
+    mids = ((v + nxt) / 2).astype(np.float32)  # exactly representable in fp32
+    vals = np.concatenate([v.astype(np.float32), mids, np.nextafter(mids, np.float32(0)),
+                           np.nextafter(mids, np.float32(np.inf))])
+    rand_bits = rng.integers(0, 2 ** 32, size=2_000_000, dtype=np.uint64).astype(np.uint32)
+    rand = rand_bits.view(np.float32)
+    rand = rand[np.isfinite(rand)]
+    small = (rng.standard_normal(500_000) * 10.0 ** rng.uniform(-9, 5, 500_000)).astype(np.float32)
+    allv = np.concatenate([vals, -vals, rand, small, np.array([65519.996, 65520.0, 1e-8, 2.0 ** -25,
+                                                               2.0 ** -25 * 1.0000001], dtype=np.float32)])
+    ours = oracle.f32_to_f16_array(allv)
+    with np.errstate(over="ignore"):
+        ref = allv.astype(np.float16).view(np.uint16)
+    bad = np.nonzero(ours != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first {allv[bad[:5]]}: {ours[bad[:5]]} vs {ref[bad[:5]]}"
+
+
+# ----------------------------------------------------------------------------
+# sizes
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("G,bits,ratio", [(32, 4.5, 3.56), (64, 4.25, 3.76), (128, 4.125, 3.88)])
+def test_bits_per_element_table(G, bits, ratio):
+    """Section 2.2 of the 4-bit compression page: 4 + 16/G bits per element."""
+    d, P = 128, 16
+    blk = oracle.block_bytes(d, P, G, G)
+    got_bits = 8.0 * blk / (2 * P * d)  # K and V elements of one page and head
+    assert got_bits == bits
+    assert round(16.0 / got_bits, 2) == ratio
+
+
+def test_block_bytes_default_k64_v128():
+    # K at 64 and V at 128: 2048 code bytes + 16*(2+1)*2 scale bytes; a 16-byte multiple
+    assert oracle.block_bytes(128, 16, 64, 128) == 2144
+    assert oracle.block_bytes(128, 16, 64, 128) % 16 == 0
+
+
+def test_fp16_kv_size_figures():
+    GiB = 1024 ** 3
+    # 32 layers x 32 heads x 128: 512 KB per token; 10k tokens about 5 GB, 100k about 50 GB
+    assert oracle.fp16_kv_bytes(32, 32, 128, 1) == 512 * 1024
+    assert 4.5e9 < oracle.fp16_kv_bytes(32, 32, 128, 10_000) < 5.5e9
+    assert 45e9 < oracle.fp16_kv_bytes(32, 32, 128, 100_000) < 55e9
+    # the 7B MHA table: 2048x1 -> 1 GB, 4096x4 -> 8 GB, 8192x8 -> 32 GB
+    assert oracle.fp16_kv_bytes(32, 32, 128, 2048 * 1) == 1 * GiB
+    assert oracle.fp16_kv_bytes(32, 32, 128, 4096 * 4) == 8 * GiB
+    assert oracle.fp16_kv_bytes(32, 32, 128, 8192 * 8) == 32 * GiB
+    # GQA 8B with 8 KV heads: 128 KB per token, 32K x batch 4 -> 16 GB
+    assert oracle.fp16_kv_bytes(32, 8, 128, 1) == 128 * 1024
+    assert oracle.fp16_kv_bytes(32, 8, 128, 32768 * 4) == 16 * GiB
+    # the cache_memory estimator of section 6.2: FP16 2/4/8/16 GiB, 4 bits 0.5/1/2/4 GiB at 4K..32K
+    for seq, gib in [(4096, 2.0), (8192, 4.0), (16384, 8.0), (32768, 16.0)]:
+        assert oracle.fp16_kv_bytes(32, 32, 128, seq) / GiB == gib
+        assert oracle.fp16_kv_bytes(32, 32, 128, seq) / 4 / GiB == gib / 4
+
+
+# ----------------------------------------------------------------------------
+# quantization: golden worked examples
+# ----------------------------------------------------------------------------
+
+def _parse_value(tok: str) -> np.float16:
+    if tok.startswith("h0x"):
+        return np.array([int(tok[1:], 16)], dtype=np.uint16).view(np.float16)[0]
+    return np.float16(float(tok))
+
+
+def load_quantize_cases():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "quantize_examples.txt")) as f:
+        for raw in f:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            if key == "case":
+                cur = {"name": rest, "x": {}, "codes": {}, "bytes": None}
+                cases.append(cur)
+            elif key == "G":
+                cur["G"] = int(rest)
+            elif key == "x":
+                for tok in rest.split():
+                    i, v = tok.split(":")
+                    cur["x"][int(i)] = _parse_value(v)
+            elif key == "scale":
+                cur["scale"] = int(rest, 16)
+            elif key == "codes":
+                for tok in rest.split():
+                    i, c = tok.split(":")
+                    cur["codes"][int(i)] = int(c)
+            elif key == "bytes":
+                cur["bytes"] = [int(t, 16) for t in rest.split()]
+    return cases
+
+
+QCASES = load_quantize_cases()
+
+
+@pytest.mark.parametrize("case", QCASES, ids=[c["name"] for c in QCASES])
+def test_quantize_golden(case):
+    G = case["G"]
+    x = np.zeros(G, dtype=np.float16)
+    for i, v in case["x"].items():
+        x[i] = v
+    codes, scale = oracle.quantize_group(x)
+    assert scale == case["scale"], f"scale {scale:#06x} != {case['scale']:#06x}"
+    want = np.zeros(G, dtype=np.int8)
+    for i, c in case["codes"].items():
+        want[i] = c
+    assert np.array_equal(codes, want), f"codes {codes} != {want}"
+    if case["bytes"] is not None:
+        # pack through the pool writer: one token, one head, d = G, K and V groups = G
+        L = oracle.Layout(1, G, 16, G, G, 1)
+        pool = np.zeros(L.pool_bytes, dtype=np.uint8)
+        k = x.reshape(1, 1, 1, G)
+        oracle.quantize_append(L, pool, k, k, np.zeros((1, 1), np.int32), np.zeros(1, np.int32))
+        nb = len(case["bytes"])
+        assert list(pool[:nb]) == case["bytes"]
+
+
+def test_quantize_golden_covers_cases():
+    assert len(QCASES) >= 12
+
+
+# ----------------------------------------------------------------------------
+# quantization: brute force and invariants on random groups
+# ----------------------------------------------------------------------------
+
+def _random_groups(n, G, seed):
+    """fp16 groups with magnitudes from 1e-7 to 6e4, some with x20 outliers, a few exact zeros."""
+    rng = np.random.default_rng(seed)
+    mag = 10.0 ** rng.uniform(-7, 4.5, size=(n, 1))
+    x = rng.standard_normal((n, G)) * mag
+    out = rng.random((n, G)) < 0.05
+    x = np.where(out, x * 20, x)
+    x = np.clip(x, -65504, 65504).astype(np.float16)
+    x[rng.random((n, G)) < 0.02] = 0
+    x[: max(1, n // 50)] = 0  # some all-zero groups
+    return x
+
+
+@pytest.mark.parametrize("G", [32, 64, 128])
+def test_quantize_brute_force_nearest_code(G):
+    """The code is the integer in [-7, 7] nearest to fp32(x / s), ties to even: found by exhaustive search."""
+    groups = _random_groups(400, G, seed=G)
+    ks = np.arange(-7, 8, dtype=np.float64)
+    for x in groups:
+        codes, sbits = oracle.quantize_group(x)
+        s = np.float32(np.array([sbits], np.uint16).view(np.float16)[0])
+        qf = (x.astype(np.float32) / s).astype(np.float64)  # IEEE fp32 quotient
+        dist = np.abs(qf[:, None] - ks[None, :])
+        best = dist.min(axis=1, keepdims=True)
+        cand = np.where(dist == best, ks[None, :], np.nan)
+        # tie: prefer the even integer
+        even = np.where(np.isnan(cand), np.nan, np.where(cand % 2 == 0, cand, np.nan))
+        even_max = np.max(np.where(np.isnan(even), -np.inf, even), axis=1)
+        cand_max = np.max(np.where(np.isnan(cand), -np.inf, cand), axis=1)
+        pick = np.where(np.isfinite(even_max), even_max, cand_max)
+        assert np.array_equal(codes.astype(np.float64), pick)
+
+
+@pytest.mark.parametrize("G", [32, 64, 128])
+def test_quantize_scale_is_fp16_of_fp32_amax_over_7(G):
+    groups = _random_groups(400, G, seed=100 + G)
+    for x in groups:
+        _, sbits = oracle.quantize_group(x)
+        amax = np.float32(np.max(np.abs(x.astype(np.float32))))
+        s_ref = np.float16(amax / np.float32(7.0))  # numpy: IEEE fp32 division, fp16 RNE
+        if s_ref == 0:
+            s_ref = np.float16(1.0)
+        assert sbits == int(np.array([s_ref]).view(np.uint16)[0])
+
+
+@pytest.mark.parametrize("G", [32, 64, 128])
+def test_quantize_invariants(G):
+    groups = _random_groups(600, G, seed=200 + G)
+    for x in groups:
+        codes, sbits = oracle.quantize_group(x)
+        s = float(np.array([sbits], np.uint16).view(np.float16)[0])
+        assert codes.min() >= -7 and codes.max() <= 7
+        xf = x.astype(np.float64)
+        xhat = codes.astype(np.float64) * s
+        nonzero = np.any(xf != 0)
+        if s >= 2.0 ** -14 and nonzero:  # a normal fp16 scale
+            assert np.all(np.abs(xf - xhat) <= s / 2 * (1 + 2.0 ** -20))
+            # amax / s lies within 7 * (1 +- 2^-11), so the largest |code| is exactly 7
+            assert np.abs(codes).max() == 7
+        if not nonzero:
+            assert sbits == 0x3C00 and np.all(codes == 0)
+        # sign symmetry: quantize(-x) = -quantize(x), same scale
+        c2, s2 = oracle.quantize_group(-x)
+        assert s2 == sbits and np.array_equal(c2, -codes)
+
+
+def test_dequantize_roundtrip_exact_on_grid():
+    """Values that are exact multiples k*s with max |k| = 7 come back exactly (closed form)."""
+    rng = np.random.default_rng(7)
+    L = oracle.Layout(2, 64, 16, 32, 64, 4)
+    for s in [1.0, 0.5, 0.25, 2.0 ** -6, 3.0, 96.0]:
+        ks = rng.integers(-7, 8, size=(1, 5, 2, 64))
+        ks[..., 0] = 7
+        ks[..., 32] = -7
+        x = (ks * s).astype(np.float16)
+        assert np.array_equal(x.astype(np.float64), ks * s)
+        pool = np.zeros(L.pool_bytes, np.uint8)
+        bt = np.array([[3, 1, 0, 2]], np.int32)
+        oracle.quantize_append(L, pool, x, x, bt, np.array([9], np.int32))
+        dk, dv = oracle.dequantize(L, pool, bt, 0, 9, 5)
+        assert np.array_equal(dk, x[0].astype(np.float32))
+        assert np.array_equal(dv, x[0].astype(np.float32))
+        hk, hv = oracle.dequantize(L, pool, bt, 0, 9, 5, out_fp16=True)
+        assert np.array_equal(hk, x[0]) and np.array_equal(hv, x[0])
+
+
+@pytest.mark.parametrize("Gk,Gv", [(32, 64), (64, 128), (32, 32)])
+def test_dequantize_error_bound_per_group(Gk, Gv):
+    """Each element comes back within half its own group's step amax_g / 7 (computed here from
+    the input), with groups of very different magnitude side by side."""
+    d = 128
+    L = oracle.Layout(2, d, 16, Gk, Gv, 6)
+    rng = np.random.default_rng(Gk + Gv)
+    n = 23
+    mags = 10.0 ** rng.uniform(-3, 3, size=(1, n, 2, d // 16)).repeat(16, axis=3)
+    x = (rng.standard_normal((1, n, 2, d)) * mags).astype(np.float16)
+    bt = np.array([[5, 0, 3]], np.int32)
+    pool = np.zeros(L.pool_bytes, np.uint8)
+    oracle.quantize_append(L, pool, x, x, bt, np.array([3], np.int32))
+    dk, dv = oracle.dequantize(L, pool, bt, 0, 3, n)
+    xf = x[0].astype(np.float64)
+    for deq, G in [(dk, Gk), (dv, Gv)]:
+        amax = np.abs(xf).reshape(n, 2, d // G, G).max(axis=3, keepdims=True)
+        step = (amax / 7.0) * (1 + 2.0 ** -10)  # the fp16 scale is within 2^-11 of amax/7
+        err = np.abs(xf - deq.astype(np.float64)).reshape(n, 2, d // G, G)
+        assert np.all(err <= step / 2 * (1 + 2.0 ** -20) + 1e-30)
+
+
+# ----------------------------------------------------------------------------
+# layout
+# ----------------------------------------------------------------------------
+
+def _parse_expect(toks):
+    out = []
+    for t in toks:
+        if "*" in t:
+            b, n = t.split("*")
+            out += [int(b, 16)] * int(n)
+        else:
+            out.append(int(t, 16))
+    return out
+
+
+def test_layout_golden():
+    spec = {"expect": []}
+    with open(os.path.join(GOLDEN, "layout_example.txt")) as f:
+        for raw in f:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *toks = line.split()
+            if key == "expect":
+                spec["expect"].append((int(toks[0]), _parse_expect(toks[1:])))
+            else:
+                spec[key] = toks
+    Hkv, d, P, Gk, Gv, npg = map(int, spec["geometry"])
+    L = oracle.Layout(Hkv, d, P, Gk, Gv, npg)
+    assert L.block_bytes == int(spec["block_bytes"][0])
+    k = np.zeros((1, 1, Hkv, d), np.float16)
+    v = np.zeros((1, 1, Hkv, d), np.float16)
+    for arr, key in [(k, "k"), (v, "v")]:
+        for t in spec[key]:
+            h, i, val = t.split(":")
+            arr[0, 0, int(h), int(i)] = float(val)
+    pool = np.full(L.pool_bytes, 0xA5, np.uint8)
+    bt = np.array([list(map(int, spec["block_table"]))], np.int32)
+    oracle.quantize_append(L, pool, k, v, bt, np.array([int(spec["start_pos"][0])], np.int32))
+    touched = np.zeros(pool.size, bool)
+    for off, bs in spec["expect"]:
+        assert list(pool[off:off + len(bs)]) == bs, f"bytes at {off}"
+        touched[off:off + len(bs)] = True
+    assert np.all(pool[~touched] == 0xA5)
+
+
+# ----------------------------------------------------------------------------
+# attention
+# ----------------------------------------------------------------------------
+
+def _build_cache(L, B, lens, seed, permute=True, outliers=True, extra_pages=0):
+    """Quantize seeded K/V histories of the given lengths into a pool; return (pool, bt, k, v)."""
+    P = L.P
+    pages = [(n + P - 1) // P for n in lens]
+    maxb = max(pages)
+    total = sum(pages)
+    assert total + extra_pages <= L.num_pages
+    order = W.permutation(seed + 11, L.num_pages).numpy() if permute else np.arange(L.num_pages, dtype=np.int32)
+    bt = np.full((B, maxb), -1, np.int32)
+    kk = 0
+    for b in range(B):
+        bt[b, :pages[b]] = order[kk:kk + pages[b]]
+        kk += pages[b]
+    n = max(lens)
+    oidx = W.outlier_channels(L.Hkv, L.d, seed=seed + 13) if outliers else None
+    k = W.kv_tensor(seed, (B, n, L.Hkv, L.d), 20.0 if outliers else 0.0, oidx).numpy()
+    v = W.kv_tensor(seed + 1, (B, n, L.Hkv, L.d)).numpy()
+    pool = np.zeros(L.pool_bytes, np.uint8)
+    for b in range(B):
+        if lens[b]:
+            oracle.quantize_append(L, pool, k[b:b + 1, :lens[b]], v[b:b + 1, :lens[b]], bt[b:b + 1],
+                                   np.array([0], np.int32))
+    return pool, bt, k, v
+
+
+def _reference_attention(L, pool, bt, q, lens, scale):
+    """numpy/scipy softmax attention over the oracle's dequantized cache (GQA by repetition)."""
+    B, Hq, d = q.shape
+    r = Hq // L.Hkv
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        if lens[b] == 0:
+            continue
+        dk, dv = oracle.dequantize(L, pool, bt, b, 0, lens[b])
+        for hq in range(Hq):
+            kh = dk[:, hq // r, :].astype(np.float64)
+            vh = dv[:, hq // r, :].astype(np.float64)
+            s = (kh @ q[b, hq].astype(np.float64)) * scale
+            out[b, hq] = scipy.special.softmax(s) @ vh
+    return out
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv", [([1, 15], 4, 2), ([16, 17], 4, 4), ([40, 33], 8, 2), ([5, 0], 2, 2)])
+def test_attention_brute_force(lens, Hq, Hkv):
+    L = oracle.Layout(Hkv, 64, 16, 32, 64, 16)
+    pool, bt, _, _ = _build_cache(L, len(lens), lens, seed=21)
+    q = W.kv_tensor(W.SEED_Q, (1, len(lens), Hq, 64)).numpy()[0]
+    scale = 64 ** -0.5
+    got = oracle.decode_attention(L, pool, q, bt, np.array(lens, np.int32), scale)
+    ref = _reference_attention(L, pool, bt, q, lens, scale)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert np.all(got[b] == 0)
+
+
+def test_attention_single_token_returns_its_value():
+    L = oracle.Layout(2, 64, 16, 32, 64, 4)
+    pool, bt, _, _ = _build_cache(L, 1, [1], seed=31)
+    q = W.kv_tensor(W.SEED_Q, (1, 1, 4, 64)).numpy()[0]
+    got = oracle.decode_attention(L, pool, q, bt, np.array([1], np.int32), 0.125)
+    _, dv = oracle.dequantize(L, pool, bt, 0, 0, 1)
+    for hq in range(4):
+        assert np.array_equal(got[0, hq], dv[0, hq // 2].astype(np.float64))
+
+
+def test_attention_equal_keys_gives_mean_value():
+    L = oracle.Layout(1, 64, 16, 32, 64, 4)
+    n = 37
+    k = np.repeat(W.kv_tensor(1, (1, 1, 1, 64)).numpy(), n, axis=1)
+    v = W.kv_tensor(2, (1, n, 1, 64)).numpy()
+    pool = np.zeros(L.pool_bytes, np.uint8)
+    bt = np.array([[2, 0, 3]], np.int32)
+    oracle.quantize_append(L, pool, k, v, bt, np.array([0], np.int32))
+    q = W.kv_tensor(3, (1, 1, 1, 64)).numpy()[0]
+    got = oracle.decode_attention(L, pool, q, bt, np.array([n], np.int32), 0.3)
+    _, dv = oracle.dequantize(L, pool, bt, 0, 0, n)
+    np.testing.assert_allclose(got[0, 0], dv[:, 0].astype(np.float64).mean(axis=0), rtol=1e-13, atol=1e-13)
+    # zero softmax scale makes any keys uniform too
+    pool2, bt2, _, _ = _build_cache(L, 1, [n], seed=41)
+    got0 = oracle.decode_attention(L, pool2, q, bt2, np.array([n], np.int32), 0.0)
+    _, dv2 = oracle.dequantize(L, pool2, bt2, 0, 0, n)
+    np.testing.assert_allclose(got0[0, 0], dv2[:, 0].astype(np.float64).mean(axis=0), rtol=1e-13, atol=1e-13)
+
+
+def test_attention_dominant_logit_selects_value():
+    L = oracle.Layout(1, 64, 16, 32, 64, 4)
+    n = 20
+    k = np.zeros((1, n, 1, 64), np.float16)
+    k[0, :, 0, 0] = 0.0
+    k[0, 13, 0, 0] = 7.0     # one key aligned with q
+    v = W.kv_tensor(2, (1, n, 1, 64)).numpy()
+    pool = np.zeros(L.pool_bytes, np.uint8)
+    bt = np.array([[1, 3]], np.int32)
+    oracle.quantize_append(L, pool, k, v, bt, np.array([0], np.int32))
+    q = np.zeros((1, 1, 64), np.float16)
+    q[0, 0, 0] = 1000.0
+    # logit 7000 against 0: exp(7000) overflows fp64, so the maximum must be subtracted first
+    got = oracle.decode_attention(L, pool, q, bt, np.array([n], np.int32), 1.0)
+    _, dv = oracle.dequantize(L, pool, bt, 0, 0, n)
+    np.testing.assert_allclose(got[0, 0], dv[13, 0].astype(np.float64), rtol=0, atol=1e-300)
+
+
+def test_attention_gqa_equals_mha_on_repeated_heads():
+    """Query head h reads KV head h // r: the same as MHA over KV heads repeated r times (section 3.2)."""
+    r, Hkv, d = 4, 2, 64
+    Lg = oracle.Layout(Hkv, d, 16, 32, 64, 8)
+    Lm = oracle.Layout(Hkv * r, d, 16, 32, 64, 8)
+    n = 45
+    k = W.kv_tensor(1, (1, n, Hkv, d), 20.0, W.outlier_channels(Hkv, d)).numpy()
+    v = W.kv_tensor(2, (1, n, Hkv, d)).numpy()
+    bt = np.array([[4, 0, 6]], np.int32)
+    pg, pm = np.zeros(Lg.pool_bytes, np.uint8), np.zeros(Lm.pool_bytes, np.uint8)
+    oracle.quantize_append(Lg, pg, k, v, bt, np.array([0], np.int32))
+    oracle.quantize_append(Lm, pm, np.repeat(k, r, axis=2), np.repeat(v, r, axis=2), bt, np.array([0], np.int32))
+    q = W.kv_tensor(3, (1, 1, Hkv * r, d)).numpy()[0]
+    og = oracle.decode_attention(Lg, pg, q, bt, np.array([n], np.int32), d ** -0.5)
+    om = oracle.decode_attention(Lm, pm, q, bt, np.array([n], np.int32), d ** -0.5)
+    assert np.array_equal(og, om)
+
+
+def test_attention_page_permutation_invariance_and_pow2_scaling():
+    L = oracle.Layout(2, 64, 16, 32, 64, 12)
+    n = 70
+    k = W.kv_tensor(1, (1, n, 2, 64), 20.0, W.outlier_channels(2, 64)).numpy()
+    v = W.kv_tensor(2, (1, n, 2, 64)).numpy()
+    q = W.kv_tensor(3, (1, 1, 4, 64)).numpy()[0]
+    outs = []
+    for bt in (np.array([[0, 1, 2, 3, 4]], np.int32), np.array([[11, 3, 7, 0, 5]], np.int32)):
+        pool = np.zeros(L.pool_bytes, np.uint8)
+        oracle.quantize_append(L, pool, k, v, bt, np.array([0], np.int32))
+        outs.append(oracle.decode_attention(L, pool, q, bt, np.array([n], np.int32), 0.125))
+    assert np.array_equal(outs[0], outs[1])
+    # V x 2 doubles every V scale and keeps the codes, so the output doubles exactly
+    pool = np.zeros(L.pool_bytes, np.uint8)
+    bt = np.array([[11, 3, 7, 0, 5]], np.int32)
+    oracle.quantize_append(L, pool, k, (v.astype(np.float32) * 2).astype(np.float16), bt, np.array([0], np.int32))
+    out2 = oracle.decode_attention(L, pool, q, bt, np.array([n], np.int32), 0.125)
+    assert np.array_equal(out2, 2 * outs[1])
