@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Benchmark of the INT4 group-quantized paged KV cache decode step on GB300.
+
+A step is one pass of the whole hot path over one batch: quantize-on-append of one
+new token per sequence (K and V), then decode attention of every query head over the
+packed paged cache (split-KV kernel + combine).  Default workload: Llama-7B-shaped
+MHA layer, batch 8, 32 query = 32 KV heads, head_dim 128, context 8192 (+1 appended
+token), 16-token pages in a seeded random permutation, K grouped at 64 and V at 128.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvq|reference] [--workload NAME]
+
+Prints one JSON line (rank 0).  `value` is whole-job HBM throughput: algorithmic bytes
+of all ranks' steps / max-over-ranks time, with algorithmic bytes = the packed cache
+the decode reads (head_dim + 2*(d/Gk + d/Gv) bytes per token per KV head) plus the
+append's fp16 read and packed write.  `--impl reference` times the oracle (plain
+single-threaded C, fp64 attention) on the host cores on a bounded sample of the same
+workload, in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "INT4-KV paged decode attention: HBM GB/s vs peak, tokens/s; quantize GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--workload", default="llama7b", help="llama7b (default), gqa8b, ragged, longctx, tiny")
+    ap.add_argument("--group", type=int, default=None, help="K and V group size for the longctx sweep")
+    ap.add_argument("--graph-steps", type=int, default=200, help="steps captured per CUDA graph")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def make_workload(name: str, group: int | None):
+    import workloads as W
+    if name == "longctx":
+        return W.longctx(group or 64)
+    wl = W.ALL[name]()
+    return wl.with_groups(group) if group else wl
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu), "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"unavailable": "nvidia-smi could not be started"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"unavailable": "no samples"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median([x for x in sm if x == x] or [float("nan")]),
+                "sm_max_mhz": max(num(r[2]) for r in rows), "samples": len(rows),
+                "power_w_max": max(num(r[3]) for r in rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """A bounded slice of the workload for the oracle: sequence 0, the first `heads` KV
+    heads (all their query heads) and the first `tokens` positions; one step appends the
+    token at position tokens-1 and attends over `tokens` positions."""
+
+    def __init__(self, wl, heads: int, tokens: int):
+        import numpy as np
+        import oracle
+        import workloads as W
+        self.np, self.oracle = np, oracle
+        self.wl, self.heads, self.tokens = wl, heads, tokens
+        k = W.kv_tensor(W.SEED_K, (1, tokens, wl.Hkv, wl.d), 20.0, W.outlier_channels(wl.Hkv, wl.d))
+        v = W.kv_tensor(W.SEED_V, (1, tokens, wl.Hkv, wl.d))
+        self.k = np.ascontiguousarray(k[:, :, :heads].numpy())
+        self.v = np.ascontiguousarray(v[:, :, :heads].numpy())
+        q = W.kv_tensor(W.SEED_Q, (1, 1, wl.Hq, wl.d))[0].numpy()
+        self.q = np.ascontiguousarray(q[:, :heads * wl.r])
+        npg = (tokens + wl.P - 1) // wl.P
+        self.L = oracle.Layout(heads, wl.d, wl.P, wl.Gk, wl.Gv, npg)
+        self.bt = np.arange(npg, dtype=np.int32).reshape(1, -1)
+        self.pool = np.zeros(self.L.pool_bytes, np.uint8)
+        if tokens > 1:
+            oracle.quantize_append(self.L, self.pool, self.k[:, :tokens - 1], self.v[:, :tokens - 1], self.bt,
+                                   np.zeros(1, np.int32))
+
+    def step(self):
+        np = self.np
+        t = self.tokens - 1
+        self.oracle.quantize_append(self.L, self.pool, self.k[:, t:t + 1], self.v[:, t:t + 1], self.bt,
+                                    np.array([t], np.int32))
+        return self.oracle.decode_attention(self.L, self.pool, self.q, self.bt, np.array([self.tokens], np.int32),
+                                            self.wl.d ** -0.5)
+
+    def bytes(self) -> int:
+        wl = self.wl
+        per = wl.packed_bytes_per_token_head()
+        return self.heads * self.tokens * per + self.heads * (2 * wl.d * 2 + per)
+
+    def describe(self) -> str:
+        wl = self.wl
+        return (f"{wl.name}: sequence 0, {self.heads} of {wl.Hkv} KV heads ({self.heads * wl.r} query heads), "
+                f"{self.tokens} of {wl.seq_lens[0]} positions; append 1 token + fp64 decode attention")
+
+
+def plan_oracle_sample(wl, seconds_per_step: float) -> "OracleSample":
+    """Size a sample so one oracle step takes about seconds_per_step on this host."""
+    probe_tokens = min(wl.seq_lens[0], 512)
+    probe = OracleSample(wl, 1, probe_tokens)
+    t0 = time.perf_counter()
+    probe.step()
+    per_head_token = max((time.perf_counter() - t0) / probe_tokens, 1e-9)
+    budget_ht = max(1.0, seconds_per_step / per_head_token)
+    tokens = wl.seq_lens[0]
+    heads = int(max(1, min(wl.Hkv, budget_ht // tokens)))
+    if heads == 1:
+        tokens = int(max(16, min(tokens, budget_ht)))
+    return OracleSample(wl, heads, tokens)
+
+
+def time_oracle(wl, budget_s: float) -> dict:
+    """The oracle as it stands, single-threaded, on a sample of about budget_s seconds."""
+    smp = plan_oracle_sample(wl, min(budget_s, 4.0))
+    reps, t_total = 0, 0.0
+    while t_total < budget_s or reps == 0:
+        t0 = time.perf_counter()
+        smp.step()
+        t_total += time.perf_counter() - t0
+        reps += 1
+    per = t_total / reps
+    return {"value": smp.bytes() / per / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": smp.describe() + f"; {reps} repetitions, {per * 1e3:.1f} ms each",
+            "seconds_per_step": per}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def run_kvq(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    import int4_group_quantized_kvq_gb300 as kvq
+    import workloads as W
+    from int4_group_quantized_kvq_gb300.cache import PagedKVCache
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = make_workload(args.workload, args.group)
+    K, Wm = args.steps, args.warmup
+    if Wm < 3:
+        raise SystemExit("--warmup must be at least 3")
+
+    # ---- inputs (seeded, synthetic, generated on the GPU) ----
+    n_tok = max(wl.seq_lens)
+    oidx = W.outlier_channels(wl.Hkv, wl.d)
+    k_all = W.kv_tensor(W.SEED_K, (wl.B, n_tok, wl.Hkv, wl.d), 20.0, oidx, device=dev)
+    v_all = W.kv_tensor(W.SEED_V, (wl.B, n_tok, wl.Hkv, wl.d), device=dev)
+    q = W.kv_tensor(W.SEED_Q, (1, wl.B, wl.Hq, wl.d), device=dev)[0].contiguous()
+    cfg = kvq.config(wl.Hkv, wl.d, wl.P, wl.Gk, wl.Gv, wl.num_pages)
+    bt = wl.block_table()
+    pool_bytes = kvq.kvq_pool_bytes(cfg)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20)
+    n_pools = max(2, math.ceil(3 * l2 / pool_bytes))
+
+    caches = [PagedKVCache(cfg, bt, wl.Hq, wl.max_len, device=dev)]
+    # prefill the first pool: each sequence's history (timed as the quantize throughput)
+    same_ctx = len(set(wl.ctx)) == 1
+    zero = torch.zeros(wl.B if same_ctx else 1, dtype=torch.int32, device=dev)
+    hist = [(k_all[:, :wl.ctx[0]].contiguous(), v_all[:, :wl.ctx[0]].contiguous())] if same_ctx else \
+        [(k_all[b:b + 1, :c].contiguous(), v_all[b:b + 1, :c].contiguous()) for b, c in enumerate(wl.ctx)]
+
+    def prefill(cache):
+        if same_ctx:
+            cache.append(hist[0][0], hist[0][1], zero)
+        else:
+            for b, (kb, vb) in enumerate(hist):
+                kvq.kvq_quantize_append(cfg, cache.pool, kb, vb, cache.block_table[b:b + 1], zero,
+                                        status=cache.status)
+
+    prefill(caches[0])
+    torch.cuda.synchronize()
+    qt = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        prefill(caches[0])
+        e1.record()
+        torch.cuda.synchronize()
+        qt.append(e0.elapsed_time(e1) * 1e-3)
+    tok_hist = sum(wl.ctx)
+    q_bytes = wl.Hkv * tok_hist * (2 * wl.d * 2 + wl.packed_bytes_per_token_head())
+    quantize = {"gbs": q_bytes / min(qt) / 1e9, "tokens": tok_hist, "bytes": q_bytes,
+                "what": "prefill quantize of the whole history: fp16 K+V read, packed codes+scales written"}
+    for _ in range(n_pools - 1):
+        caches.append(PagedKVCache(cfg, bt, wl.Hq, wl.max_len, device=dev, pool=caches[0].pool.clone()))
+
+    pos = torch.tensor(wl.ctx, dtype=torch.int32, device=dev)
+    idx = pos.long().view(-1, 1, 1, 1).expand(-1, 1, wl.Hkv, wl.d)
+    k_new = torch.gather(k_all, 1, idx).contiguous()
+    v_new = torch.gather(v_all, 1, idx).contiguous()
+    del k_all, v_all, hist
+    torch.cuda.empty_cache()
+    seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
+    out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.float32, device=dev)
+
+    step_bytes = wl.decode_bytes() + wl.append_bytes()
+    stream = torch.cuda.Stream(device=dev)
+
+    # ---- warm-up (eager) ----
+    with torch.cuda.stream(stream):
+        for i in range(Wm):
+            caches[i % n_pools].decode_step(q, k_new, v_new, pos, seq_lens, out, stream=stream)
+    stream.synchronize()
+
+    # ---- capture G steps (rotating pools) with events around each decode attention call ----
+    G = max(g for g in range(1, min(K, args.graph_steps) + 1) if K % g == 0)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(G)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            c = caches[i % n_pools]
+            c.append(k_new, v_new, pos, stream=stream)
+            ev[i][0].record(stream)
+            c.attend(q, seq_lens, out, stream=stream)
+            ev[i][1].record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            graph.replay()
+    stream.synchronize()
+
+    # ---- timed region ----
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(K // G):
+            graph.replay()
+        t_end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    t_local = t_start.elapsed_time(t_end) * 1e-3
+    decode_s = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e-3  # last replay's G launches
+    flags = max(c.flags() for c in caches)
+    if world > 1:
+        t = torch.tensor([t_local], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    else:
+        t_max = t_local
+    step_s = t_max / K
+
+    # ---- end to end through the public API from pinned host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        q_h = q.cpu().pin_memory()
+        k_h = k_new.cpu().pin_memory()
+        v_h = v_new.cpu().pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        bufs = (torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(out))
+        for i in range(Wm):
+            caches[i % n_pools].decode_step_host(q_h, k_h, v_h, out_h, pos, seq_lens, bufs, stream=stream)
+        stream.synchronize()
+        n_e2e = K
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            caches[i % n_pools].decode_step_host(q_h, k_h, v_h, out_h, pos, seq_lens, bufs, stream=stream)
+        stream.synchronize()
+        t_e2e = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        h2d = q.numel() * 2 + k_new.numel() * 2 + v_new.numel() * 2
+        d2h = out.numel() * 4
+        e2e = {"value": world * n_e2e * step_bytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": t_e2e / n_e2e * 1e3,
+               "how": "PagedKVCache.decode_step_host: pinned H2D of q/K/V, append + attend, D2H of out, "
+                      "wall clock over all steps with a stream sync at the end"}
+
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    achieved = wl.decode_bytes() / decode_s / 1e9
+    res = {
+        "metric": METRIC,
+        "value": world * step_bytes / step_s / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": step_s * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "dtype_detail": "INT4 codes + fp16 group scales stored; f16 x f16 -> f32 tensor-core MMA; fp32 softmax; "
+                        "fp32 output",
+        "data": "synthetic",
+        "config": {
+            "workload": wl.name,
+            "description": wl.description,
+            "batch": wl.B, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.d,
+            "context": wl.ctx[0] if len(set(wl.ctx)) == 1 else f"{min(wl.ctx)}..{max(wl.ctx)}",
+            "attended_tokens": sum(wl.seq_lens), "page_size": wl.P, "group_k": wl.Gk, "group_v": wl.Gv,
+            "step": "quantize-append 1 token per sequence + decode attention (split-KV + combine)",
+            "bytes_per_step": step_bytes,
+            "l2": f"inputs larger than L2: {n_pools} rotated pool copies of {pool_bytes / 1e6:.1f} MB "
+                  f"against a {l2 / 1e6:.0f} MB L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "timing": f"CUDA graphs of {G} steps replayed {K // G} times, CUDA events on the launch stream",
+        },
+        "tokens_per_s": world * wl.B / step_s,
+        "decode_us": decode_s * 1e6,
+        "quantize": quantize,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"],
+            "traffic": None,
+            "kernel": "kvq_decode_attention (split-KV decode + combine), packed bytes of the cache per call",
+            "peak_source": peaks["source"],
+        },
+        "e2e": e2e,
+        "gpu_launches": 3 * K,
+        "status_flags": flags,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = time_oracle(wl, args.cpu_seconds)
+        res["cpu_baseline"].pop("seconds_per_step", None)
+    return res
+
+
+def run_reference(args, world, rank):
+    """The oracle on the host cores, on a bounded sample per step of the same workload."""
+    if rank != 0:
+        return None
+    wl = make_workload(args.workload, args.group)
+    K, Wm = args.steps, args.warmup
+    per_step = max(0.002, min(2.0, 150.0 / (K + Wm)))
+    smp = plan_oracle_sample(wl, per_step)
+    for _ in range(Wm):
+        smp.step()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        smp.step()
+    t = time.perf_counter() - t0
+    value = K * smp.bytes() / t / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": t / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "sample": smp.describe()},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": smp.describe()},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "kvq" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, world, rank)
+        else:
+            res = run_kvq(args, world, rank, local)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

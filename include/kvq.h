@@ -1,0 +1,172 @@
+/*
+ * kvq.h -- C ABI of the INT4 group-quantized paged KV cache for NVIDIA GB300 (sm_103a).
+ *
+ * The library implements two operations and an inverse:
+ *   quantize-on-append  symmetric per-group INT4 quantization of new K/V rows into
+ *                       fixed-size pages ("4-bit KV cache compression",
+ *                       lpnh.cn/news/2042373, section 2.1; pages as in "AI inference
+ *                       tuning: KV Cache optimisation and memory management",
+ *                       bxzpzcl.cn/news/2871434, section 3.1);
+ *   decode attention    one query token per sequence attends to every cached token,
+ *                       reading the packed cache and dequantizing inside the kernel
+ *                       (scaled dot-product attention as in section 3.2 of the same
+ *                       KV-cache optimisation page; "dequantize inside the operator" as
+ *                       in "LLM long-context inference: managing the KV cache with an
+ *                       INT4 state machine", pwwt.cn/news/4219524, section 5 step 5);
+ *   dequantize          the inverse map code * scale (section 2.1 of the 4-bit page).
+ *
+ * Conventions
+ *   - Every pointer argument except `cfg` and host outputs is a DEVICE pointer on the
+ *     current CUDA device.  The caller owns and allocates all memory; the library
+ *     allocates nothing and keeps no state except a per-thread error string.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream).
+ *     Buffers must stay valid until the stream reaches the call.
+ *   - Return value: KVQ_OK or an error code; kvq_last_error() describes the last
+ *     failure on the calling thread.  Argument errors are detected on the host before
+ *     anything is launched.  Bad device-side data (a page id outside [0, num_pages),
+ *     a position beyond the block table) is never dereferenced: the offending row is
+ *     skipped (quantize) or read from page 0 instead (decode, dequantize) and a flag
+ *     bit is OR-ed into a device status word; see kvq_read_status().
+ *
+ * Storage format (the "pool")
+ *   The pool is num_pages * num_kv_heads blocks of kvq_block_bytes(cfg) bytes; block
+ *   (page, h) starts at byte (page * num_kv_heads + h) * kvq_block_bytes(cfg).  A block
+ *   holds, in order, for its P = page_size token slots:
+ *     K codes   P rows of head_dim/2 bytes
+ *     V codes   P rows of head_dim/2 bytes
+ *     K scales  P rows of head_dim/group_k fp16 (little-endian)
+ *     V scales  P rows of head_dim/group_v fp16
+ *     zero padding to a multiple of 16 bytes.
+ *   A code c in [-7, 7] is stored as the nibble c + 8; byte j of a row holds element
+ *   2j in its low nibble and element 2j+1 in its high nibble.  Token position t of
+ *   sequence b lives in page block_table[b * max_blocks + t / P], slot t % P.
+ *   Storage is 4 + 16/G bits per element (4.5 / 4.25 / 4.125 for G = 32 / 64 / 128),
+ *   the figure of section 2.2 of the 4-bit page.
+ *
+ * Quantization (section 2.1 of the 4-bit page, with the rounding made exact):
+ *   scale = fp16_rne(fp32(amax) / 7.0f) over each group of G consecutive elements
+ *   along head_dim; a scale that is zero after rounding becomes 1.0;
+ *   code  = clamp(round_half_even(fp32(x) / fp32(scale)), -7, 7), an IEEE division.
+ *   Codes and scales are bit-exact functions of the fp16 input.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *kvq_stream_t;
+
+/* Cache geometry, shared by all calls on one pool. */
+typedef struct {
+    int32_t num_kv_heads; /* KV heads per layer (Hkv), >= 1                          */
+    int32_t head_dim;     /* d: 64, 128 or 256 (decode attention: 128)                */
+    int32_t page_size;    /* tokens per page: 16, 32 or 64                            */
+    int32_t group_k;      /* K quantization group along head_dim: 32, 64 or 128 (<= d) */
+    int32_t group_v;      /* V quantization group: 32, 64 or 128 (<= d)               */
+    int32_t num_pages;    /* pages in the pool, >= 1                                  */
+} kvq_cache_config;
+
+enum {
+    KVQ_OK = 0,
+    KVQ_EINVAL = 1,       /* null or misaligned pointer, negative size, Hq % Hkv != 0  */
+    KVQ_EUNSUPPORTED = 2, /* a geometry outside the supported set above                */
+    KVQ_EWORKSPACE = 3,   /* workspace smaller than kvq_decode_workspace_bytes()       */
+    KVQ_ECUDA = 4         /* a CUDA runtime error (launch failure, bad device, ...)    */
+};
+
+/* Bits OR-ed into a device status word (they stay set until the caller clears them). */
+#define KVQ_FLAG_BAD_PAGE 0x1u     /* a block-table entry outside [0, num_pages)          */
+#define KVQ_FLAG_BAD_POSITION 0x2u /* a position or length beyond max_blocks * page_size  */
+#define KVQ_FLAG_WAIT_TIMEOUT 0x4u /* an asynchronous copy did not complete in time       */
+
+/* Bytes of one (page, kv-head) block; 0 if cfg is invalid.  Pure host computation. */
+size_t kvq_block_bytes(const kvq_cache_config *cfg);
+
+/* Bytes of the whole pool: num_pages * num_kv_heads * kvq_block_bytes(cfg). */
+size_t kvq_pool_bytes(const kvq_cache_config *cfg);
+
+/*
+ * Quantize-on-append (section 2.1 of the 4-bit page; pages as in section 3.1 of the
+ * KV-cache optimisation page).
+ *   pool         device, kvq_pool_bytes(cfg) bytes, 16-byte aligned; written in place.
+ *   k, v         device fp16 [batch, n_new, num_kv_heads, head_dim], contiguous,
+ *                16-byte aligned: the new K and V rows.
+ *   block_table  device int32 [batch, max_blocks] page ids.
+ *   start_pos    device int32 [batch]: token t of sequence b goes to position
+ *                start_pos[b] + t.
+ *   status       device uint32 status word or NULL; flag bits are OR-ed into it.
+ * A row whose position or page is out of range is skipped and flagged.
+ * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED or KVQ_ECUDA.
+ */
+int kvq_quantize_append(const kvq_cache_config *cfg, void *pool, const void *k, const void *v,
+                        const int32_t *block_table, int32_t max_blocks, const int32_t *start_pos,
+                        int32_t batch, int32_t n_new, uint32_t *status, kvq_stream_t stream);
+
+/*
+ * Workspace bytes kvq_decode_attention needs for this shape on the current device
+ * (it depends on the device's SM count).  0 if the arguments are invalid.
+ */
+size_t kvq_decode_workspace_bytes(const kvq_cache_config *cfg, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_len);
+
+/*
+ * Decode attention over the packed cache (section 3.2 of the KV-cache optimisation
+ * page: scores = q . k * softmax_scale, softmax over all cached positions, weights
+ * applied to V; query head hq reads KV head hq / (num_q_heads / num_kv_heads)).
+ * K and V are dequantized inside the kernel (section 5 step 5 of the state-machine
+ * page); q . k, the softmax and P . V accumulate in fp32.
+ *   pool          device, as written by kvq_quantize_append.
+ *   q             device fp16 [batch, num_q_heads, head_dim], 16-byte aligned.
+ *   block_table   device int32 [batch, max_blocks].
+ *   seq_lens      device int32 [batch]: positions 0 .. seq_lens[b]-1 are attended to
+ *                 (the newly appended token included).  A length of 0 gives zeros.
+ *   max_len       host bound on every seq_lens[b] (sizes the workspace).
+ *   out           device fp32 [batch, num_q_heads, head_dim], 16-byte aligned.
+ *   workspace     device, >= kvq_decode_workspace_bytes(...) bytes, 256-byte aligned.
+ *                 Its first 4 bytes are the status word (zero it once after
+ *                 allocating); the rest is scratch for split-KV partial results.
+ * num_q_heads must be a multiple of num_kv_heads with a ratio of at most 8.
+ * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE or KVQ_ECUDA.
+ */
+int kvq_decode_attention(const kvq_cache_config *cfg, const void *pool, const void *q,
+                         const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                         int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                         float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * Dequantize positions [start, start + n) of sequence b (section 2.1 of the 4-bit
+ * page: value = code * scale, exact in fp32).
+ *   out_k, out_v  device [n, num_kv_heads, head_dim]; out_dtype 0 = fp16 (the fp32
+ *                 value rounded to nearest even), 1 = fp32.
+ *   status        device uint32 status word or NULL.
+ * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED or KVQ_ECUDA.
+ */
+int kvq_dequantize(const kvq_cache_config *cfg, const void *pool, const int32_t *block_table,
+                   int32_t max_blocks, int32_t b, int32_t start, int32_t n, void *out_k, void *out_v,
+                   int32_t out_dtype, uint32_t *status, kvq_stream_t stream);
+
+/*
+ * Copy a device status word (a `status` argument, or the first 4 bytes of a decode
+ * workspace) to *flags after the stream has reached this point (synchronizes the
+ * stream).  Returns KVQ_OK, KVQ_EINVAL or KVQ_ECUDA.
+ */
+int kvq_read_status(const void *status_word, uint32_t *flags, kvq_stream_t stream);
+
+/* The calling thread's last error message ("" if none).  Never NULL. */
+const char *kvq_last_error(void);
+
+/* Library version string. */
+const char *kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

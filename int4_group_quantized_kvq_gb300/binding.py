@@ -1,0 +1,187 @@
+"""ctypes binding of libkvq.so: the C ABI of include/kvq.h under the same names.
+
+Argument marshalling only: every function checks that the torch tensors it is
+handed have the dtype, device and layout the C ABI expects, passes raw pointers
+and the current CUDA stream, and turns a non-zero status into an exception.  All
+computation happens in the library's CUDA kernels; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvq.so")
+
+KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE, KVQ_ECUDA = 0, 1, 2, 3, 4
+KVQ_FLAG_BAD_PAGE, KVQ_FLAG_BAD_POSITION, KVQ_FLAG_WAIT_TIMEOUT = 0x1, 0x2, 0x4
+
+ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
+               "kvq_decode_attention", "kvq_dequantize", "kvq_read_status", "kvq_last_error", "kvq_version")
+
+
+class KvqError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"kvq error {code}: {msg}")
+        self.code = code
+
+
+class CacheConfig(C.Structure):
+    """kvq_cache_config: num_kv_heads, head_dim, page_size, group_k, group_v, num_pages."""
+
+    _fields_ = [("num_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("page_size", C.c_int32),
+                ("group_k", C.c_int32), ("group_v", C.c_int32), ("num_pages", C.c_int32)]
+
+    def __repr__(self) -> str:
+        return (f"CacheConfig(Hkv={self.num_kv_heads}, d={self.head_dim}, P={self.page_size}, "
+                f"Gk={self.group_k}, Gv={self.group_v}, pages={self.num_pages})")
+
+
+_lib: C.CDLL | None = None
+
+
+def lib() -> C.CDLL:
+    """Load libkvq.so.  Raises if it has not been built: there is no other implementation."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                              f"g.build()'` (nvcc, sm_103a)")
+        L = C.CDLL(LIB_PATH)
+        P, I32, SZ = C.c_void_p, C.c_int32, C.c_size_t
+        cfgp = C.POINTER(CacheConfig)
+        L.kvq_block_bytes.argtypes = [cfgp]
+        L.kvq_block_bytes.restype = SZ
+        L.kvq_pool_bytes.argtypes = [cfgp]
+        L.kvq_pool_bytes.restype = SZ
+        L.kvq_quantize_append.argtypes = [cfgp, P, P, P, P, I32, P, I32, I32, P, P]
+        L.kvq_quantize_append.restype = C.c_int
+        L.kvq_decode_workspace_bytes.argtypes = [cfgp, I32, I32, I32]
+        L.kvq_decode_workspace_bytes.restype = SZ
+        L.kvq_decode_attention.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
+        L.kvq_decode_attention.restype = C.c_int
+        L.kvq_dequantize.argtypes = [cfgp, P, P, I32, I32, I32, I32, P, P, I32, P, P]
+        L.kvq_dequantize.restype = C.c_int
+        L.kvq_read_status.argtypes = [P, C.POINTER(C.c_uint32), P]
+        L.kvq_read_status.restype = C.c_int
+        L.kvq_last_error.argtypes = []
+        L.kvq_last_error.restype = C.c_char_p
+        L.kvq_version.argtypes = []
+        L.kvq_version.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def kvq_last_error() -> str:
+    return lib().kvq_last_error().decode()
+
+
+def kvq_version() -> str:
+    return lib().kvq_version().decode()
+
+
+def _check(rc: int) -> None:
+    if rc != KVQ_OK:
+        raise KvqError(rc, kvq_last_error())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype | None = None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def config(num_kv_heads: int, head_dim: int, page_size: int = 16, group_k: int = 64, group_v: int = 128,
+           num_pages: int = 1) -> CacheConfig:
+    return CacheConfig(num_kv_heads, head_dim, page_size, group_k, group_v, num_pages)
+
+
+def kvq_block_bytes(cfg: CacheConfig) -> int:
+    n = lib().kvq_block_bytes(C.byref(cfg))
+    if n == 0:
+        raise KvqError(KVQ_EINVAL, kvq_last_error())
+    return int(n)
+
+
+def kvq_pool_bytes(cfg: CacheConfig) -> int:
+    n = lib().kvq_pool_bytes(C.byref(cfg))
+    if n == 0:
+        raise KvqError(KVQ_EINVAL, kvq_last_error())
+    return int(n)
+
+
+def kvq_quantize_append(cfg: CacheConfig, pool: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        block_table: torch.Tensor, start_pos: torch.Tensor, status: torch.Tensor | None = None,
+                        stream=None) -> None:
+    """k, v: fp16 [B, n_new, Hkv, d]; block_table int32 [B, max_blocks]; start_pos int32 [B]."""
+    if k.shape != v.shape or k.dim() != 4:
+        raise ValueError("k and v must both be [B, n_new, Hkv, d]")
+    B, n_new = int(k.shape[0]), int(k.shape[1])
+    rc = lib().kvq_quantize_append(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(k, "k", torch.float16), _dev(v, "v", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(start_pos, "start_pos", torch.int32), B, n_new,
+        None if status is None else _dev(status, "status"), _stream(stream))
+    _check(rc)
+
+
+def kvq_decode_workspace_bytes(cfg: CacheConfig, batch: int, num_q_heads: int, max_len: int) -> int:
+    n = lib().kvq_decode_workspace_bytes(C.byref(cfg), batch, num_q_heads, max_len)
+    if n == 0:
+        raise KvqError(KVQ_EUNSUPPORTED, kvq_last_error())
+    return int(n)
+
+
+def kvq_decode_attention(cfg: CacheConfig, pool: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
+                         seq_lens: torch.Tensor, max_len: int, softmax_scale: float, out: torch.Tensor,
+                         workspace: torch.Tensor, stream=None) -> None:
+    """q: fp16 [B, Hq, d]; out: fp32 [B, Hq, d]; seq_lens int32 [B]; workspace uint8 (first 4 bytes: status)."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_decode_attention(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(q, "q", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
+        _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(rc)
+
+
+def kvq_dequantize(cfg: CacheConfig, pool: torch.Tensor, block_table: torch.Tensor, b: int, start: int, n: int,
+                   out_k: torch.Tensor, out_v: torch.Tensor, status: torch.Tensor | None = None,
+                   stream=None) -> None:
+    """out_k, out_v: [n, Hkv, d] fp16 or fp32 (both the same dtype)."""
+    if out_k.dtype != out_v.dtype or out_k.dtype not in (torch.float16, torch.float32):
+        raise ValueError("out_k and out_v must both be fp16 or both fp32")
+    out_dtype = 1 if out_k.dtype == torch.float32 else 0
+    rc = lib().kvq_dequantize(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(block_table, "block_table", torch.int32),
+        int(block_table.shape[1]), b, start, n, _dev(out_k, "out_k"), _dev(out_v, "out_v"), out_dtype,
+        None if status is None else _dev(status, "status"), _stream(stream))
+    _check(rc)
+
+
+def kvq_read_status(status_word: torch.Tensor, stream=None) -> int:
+    """Flags of a status word (a uint32 status tensor or a decode workspace); synchronizes the stream."""
+    flags = C.c_uint32(0)
+    _check(lib().kvq_read_status(_dev(status_word, "status_word"), C.byref(flags), _stream(stream)))
+    return int(flags.value)
+
+
+def new_workspace(cfg: CacheConfig, batch: int, num_q_heads: int, max_len: int, device="cuda") -> torch.Tensor:
+    """A zeroed decode workspace of the size the library asks for (allocated by torch, not the library)."""
+    n = kvq_decode_workspace_bytes(cfg, batch, num_q_heads, max_len)
+    return torch.zeros(n, dtype=torch.uint8, device=device)

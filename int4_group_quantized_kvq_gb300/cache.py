@@ -1,0 +1,72 @@
+"""One layer's INT4 paged KV cache on the GPU and its decode step.
+
+A thin holder of device buffers (torch allocates them; the library allocates
+nothing) around the two C ABI calls a decode step makes:
+
+    quantize-on-append of the new token's K/V  ->  kvq_quantize_append
+    decode attention over the packed cache      ->  kvq_decode_attention
+
+``decode_step_host`` is the same step driven from pinned host buffers: the new
+token's q/K/V are copied in and the output copied back on the same stream.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import binding as B
+
+
+class PagedKVCache:
+    def __init__(self, cfg: B.CacheConfig, block_table: torch.Tensor, num_q_heads: int, max_len: int,
+                 device="cuda", pool: torch.Tensor | None = None):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.block_table = block_table.to(self.device, torch.int32).contiguous()
+        self.batch = int(self.block_table.shape[0])
+        self.num_q_heads = int(num_q_heads)
+        self.max_len = int(max_len)
+        nbytes = B.kvq_pool_bytes(cfg)
+        if pool is None:
+            pool = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        if pool.numel() < nbytes:
+            raise ValueError(f"pool has {pool.numel()} bytes, needs {nbytes}")
+        self.pool = pool
+        self.workspace = B.new_workspace(cfg, self.batch, self.num_q_heads, self.max_len, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.softmax_scale = 1.0 / math.sqrt(cfg.head_dim)
+
+    def append(self, k: torch.Tensor, v: torch.Tensor, start_pos: torch.Tensor, stream=None) -> None:
+        """Quantize k, v [B, n, Hkv, d] fp16 into positions start_pos[b] .. start_pos[b] + n - 1."""
+        B.kvq_quantize_append(self.cfg, self.pool, k, v, self.block_table, start_pos, status=self.status,
+                              stream=stream)
+
+    def attend(self, q: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+        """Decode attention of q [B, Hq, d] fp16 over positions 0 .. seq_lens[b]-1 into out (fp32)."""
+        B.kvq_decode_attention(self.cfg, self.pool, q, self.block_table, seq_lens, self.max_len,
+                               self.softmax_scale, out, self.workspace, stream=stream)
+
+    def decode_step(self, q, k_new, v_new, append_pos, seq_lens, out, stream=None) -> None:
+        """Append one token per sequence at append_pos, then attend over seq_lens (which include it)."""
+        self.append(k_new, v_new, append_pos, stream)
+        self.attend(q, seq_lens, out, stream)
+
+    def decode_step_host(self, q_h, k_h, v_h, out_h, append_pos, seq_lens, dev_bufs, stream=None) -> None:
+        """The decode step from pinned host buffers: H2D of q/K/V, the two calls, D2H of out.
+
+        dev_bufs = (q, k_new, v_new, out) device tensors of matching shapes, reused across steps.
+        All copies are asynchronous on the step's stream.
+        """
+        s = torch.cuda.current_stream() if stream is None else stream
+        q, k, v, out = dev_bufs
+        with torch.cuda.stream(s):
+            q.copy_(q_h, non_blocking=True)
+            k.copy_(k_h, non_blocking=True)
+            v.copy_(v_h, non_blocking=True)
+            self.decode_step(q, k, v, append_pos, seq_lens, out, stream=s)
+            out_h.copy_(out, non_blocking=True)
+
+    def flags(self) -> int:
+        """Status flags of the last calls (synchronizes)."""
+        return B.kvq_read_status(self.status) | B.kvq_read_status(self.workspace)

@@ -1,0 +1,79 @@
+// decode_plan.cu -- sizing of the persistent split-KV grid and of its workspace.
+//
+// The grid is W warps (4 per CTA).  W is the number of warps the device can keep
+// resident (SMs x resident CTAs x 4), reduced for small problems so that a warp gets
+// at least two pages; every warp receives an equal contiguous slice of the flattened
+// (sequence, kv head, page) units.  Each warp writes at most one partial per
+// (sequence, kv head) segment its slice touches.  Partial index = warp + segment is
+// unique: if warp w touches segment s and warp w-1 touches segment s+1, warp w-1 would
+// hold a later unit than warp w, which contiguous ordered slices rule out.  So the
+// workspace holds W + B * Hkv partials, each r (query heads per KV head) x (2 + d) floats.
+#include <algorithm>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+
+cudaError_t decode_run_gk32(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_gk64(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_gk128(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+int decode_occupancy_gk32(const DecodeArgs& a, size_t smem);
+int decode_occupancy_gk64(const DecodeArgs& a, size_t smem);
+int decode_occupancy_gk128(const DecodeArgs& a, size_t smem);
+
+namespace {
+constexpr int kWarpsPerCta = 4;
+constexpr size_t kRingTargetBytes = 13 * 1024;  // per warp: ~6 pages of 2144 bytes in flight
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+}  // namespace
+
+cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
+    if (a.L.d != 128) return cudaErrorInvalidValue;
+    if (a.L.P % 16 != 0) return cudaErrorInvalidValue;
+    const int r = a.Hq / a.Hkv;
+    if (r < 1 || r > 8) return cudaErrorInvalidValue;
+    int stages = static_cast<int>(kRingTargetBytes / static_cast<size_t>(a.L.bytes));
+    stages = std::max(2, std::min(8, stages));
+    const size_t smem = static_cast<size_t>(kWarpsPerCta) * stages * a.L.bytes +
+                        static_cast<size_t>(kWarpsPerCta) * stages * 8 + static_cast<size_t>(a.B + 1) * 4;
+    int occ = 0;
+    switch (a.L.Gk) {
+        case 32: occ = decode_occupancy_gk32(a, smem); break;
+        case 64: occ = decode_occupancy_gk64(a, smem); break;
+        case 128: occ = decode_occupancy_gk128(a, smem); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (occ <= 0) return cudaErrorInvalidConfiguration;
+    int dev = 0, sms = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    const long long w_max = static_cast<long long>(sms) * occ * kWarpsPerCta;
+    const long long pages_max = (static_cast<long long>(std::max(a.max_len, 0)) + a.L.P - 1) / a.L.P;
+    const long long u_max = static_cast<long long>(a.Hkv) * a.B * pages_max;
+    long long w = std::min(w_max, std::max<long long>(kWarpsPerCta, (u_max + 1) / 2));
+    w = round_up(static_cast<size_t>(w), kWarpsPerCta);
+    plan->warps = static_cast<int32_t>(w);
+    plan->ctas = static_cast<int32_t>(w / kWarpsPerCta);
+    plan->stages = stages;
+    plan->smem_bytes = smem;
+    const size_t pieces = static_cast<size_t>(w) + static_cast<size_t>(a.B) * a.Hkv;
+    plan->ws_ml_offset = kAlign;  // the first 256 bytes hold the status word
+    plan->ws_o_offset = plan->ws_ml_offset + round_up(pieces * r * 2 * sizeof(float), kAlign);
+    plan->ws_bytes = plan->ws_o_offset + round_up(pieces * r * a.L.d * sizeof(float), kAlign);
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
+    switch (a.L.Gk) {
+        case 32: return decode_run_gk32(a, plan, stream);
+        case 64: return decode_run_gk64(a, plan, stream);
+        case 128: return decode_run_gk128(a, plan, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace kvq

@@ -1,0 +1,212 @@
+// kvq_api.cu -- the extern "C" boundary: argument validation, geometry checks,
+// dispatch to the kernels and error reporting.  No allocation, no hidden state
+// except a per-thread error string.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok() {
+    g_err[0] = '\0';
+    return KVQ_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool is_pow2_in(int x, int lo, int hi) { return x >= lo && x <= hi && (x & (x - 1)) == 0; }
+
+// Geometry shared by every call.  Returns KVQ_OK or an error (with the message set).
+int check_cfg(const kvq_cache_config* c) {
+    if (!c) return fail(KVQ_EINVAL, "cfg is NULL");
+    if (c->num_kv_heads < 1) return fail(KVQ_EINVAL, "num_kv_heads %d < 1", c->num_kv_heads);
+    if (c->num_pages < 1) return fail(KVQ_EINVAL, "num_pages %d < 1", c->num_pages);
+    if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256)
+        return fail(KVQ_EUNSUPPORTED, "head_dim %d not in {64, 128, 256}", c->head_dim);
+    if (!is_pow2_in(c->page_size, 16, 64)) return fail(KVQ_EUNSUPPORTED, "page_size %d not in {16, 32, 64}", c->page_size);
+    if (!is_pow2_in(c->group_k, 32, 128) || c->group_k > c->head_dim)
+        return fail(KVQ_EUNSUPPORTED, "group_k %d not in {32, 64, 128} or > head_dim", c->group_k);
+    if (!is_pow2_in(c->group_v, 32, 128) || c->group_v > c->head_dim)
+        return fail(KVQ_EUNSUPPORTED, "group_v %d not in {32, 64, 128} or > head_dim", c->group_v);
+    const size_t blocks = static_cast<size_t>(c->num_pages) * c->num_kv_heads;
+    if (blocks * kvq::block_layout(*c).bytes > (static_cast<size_t>(1) << 46))
+        return fail(KVQ_EINVAL, "pool larger than 64 TiB");
+    return KVQ_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(KVQ_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvq_block_bytes(const kvq_cache_config* cfg) {
+    if (check_cfg(cfg) != KVQ_OK) return 0;
+    return static_cast<size_t>(kvq::block_layout(*cfg).bytes);
+}
+
+size_t kvq_pool_bytes(const kvq_cache_config* cfg) {
+    if (check_cfg(cfg) != KVQ_OK) return 0;
+    return static_cast<size_t>(cfg->num_pages) * cfg->num_kv_heads * kvq::block_layout(*cfg).bytes;
+}
+
+int kvq_quantize_append(const kvq_cache_config* cfg, void* pool, const void* k, const void* v,
+                        const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
+                        int32_t n_new, uint32_t* status, kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || n_new < 0) return fail(KVQ_EINVAL, "batch %d / n_new %d negative", batch, n_new);
+    if (batch == 0 || n_new == 0) return ok();
+    if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
+    if (!pool || !k || !v || !block_table || !start_pos) return fail(KVQ_EINVAL, "NULL device pointer");
+    if (!aligned(pool, 16) || !aligned(k, 16) || !aligned(v, 16))
+        return fail(KVQ_EINVAL, "pool, k and v must be 16-byte aligned");
+    if (!aligned(block_table, 4) || !aligned(start_pos, 4) || (status && !aligned(status, 4)))
+        return fail(KVQ_EINVAL, "int32/uint32 arguments must be 4-byte aligned");
+    kvq::QuantizeArgs a;
+    a.pool = static_cast<uint8_t*>(pool);
+    a.k = static_cast<const __half*>(k);
+    a.v = static_cast<const __half*>(v);
+    a.block_table = block_table;
+    a.start_pos = start_pos;
+    a.status = status;
+    a.max_blocks = max_blocks;
+    a.B = batch;
+    a.n_new = n_new;
+    a.Hkv = cfg->num_kv_heads;
+    a.num_pages = cfg->num_pages;
+    a.L = kvq::block_layout(*cfg);
+    cudaError_t e = kvq::launch_quantize_append(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_quantize_append launch");
+    return ok();
+}
+
+size_t kvq_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_len) {
+    if (check_cfg(cfg) != KVQ_OK) return 0;
+    if (batch < 1 || num_q_heads < 1 || max_len < 0 || num_q_heads % cfg->num_kv_heads) {
+        fail(KVQ_EINVAL, "invalid batch / num_q_heads / max_len");
+        return 0;
+    }
+    kvq::DecodeArgs a{};
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hkv = cfg->num_kv_heads;
+    a.max_len = max_len;
+    a.L = kvq::block_layout(*cfg);
+    kvq::DecodePlan plan;
+    cudaError_t e = kvq::plan_decode(a, &plan);
+    if (e != cudaSuccess) {
+        fail(e == cudaErrorInvalidValue ? KVQ_EUNSUPPORTED : KVQ_ECUDA, "no decode kernel for this shape: %s",
+             cudaGetErrorString(e));
+        return 0;
+    }
+    ok();
+    return plan.ws_bytes;
+}
+
+int kvq_decode_attention(const kvq_cache_config* cfg, const void* pool, const void* q, const int32_t* block_table,
+                         int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                         int32_t max_len, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                         kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || num_q_heads < 1 || max_len < 0)
+        return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
+    if (num_q_heads % cfg->num_kv_heads)
+        return fail(KVQ_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, cfg->num_kv_heads);
+    if (num_q_heads / cfg->num_kv_heads > 8)
+        return fail(KVQ_EUNSUPPORTED, "query heads per KV head %d > 8", num_q_heads / cfg->num_kv_heads);
+    if (cfg->head_dim != 128) return fail(KVQ_EUNSUPPORTED, "decode attention supports head_dim 128");
+    if (batch > 4096) return fail(KVQ_EUNSUPPORTED, "batch %d > 4096", batch);
+    if (batch == 0) return ok();
+    if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
+    if (!pool || !q || !block_table || !seq_lens || !out || !workspace) return fail(KVQ_EINVAL, "NULL device pointer");
+    if (!aligned(pool, 16) || !aligned(q, 16) || !aligned(out, 16))
+        return fail(KVQ_EINVAL, "pool, q and out must be 16-byte aligned");
+    if (!aligned(workspace, 256)) return fail(KVQ_EINVAL, "workspace must be 256-byte aligned");
+    if (!aligned(block_table, 4) || !aligned(seq_lens, 4)) return fail(KVQ_EINVAL, "int32 arguments must be aligned");
+    kvq::DecodeArgs a;
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.q = static_cast<const __half*>(q);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.workspace = static_cast<uint8_t*>(workspace);
+    a.max_blocks = max_blocks;
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hkv = cfg->num_kv_heads;
+    a.num_pages = cfg->num_pages;
+    a.max_len = max_len;
+    a.softmax_scale = softmax_scale;
+    a.L = kvq::block_layout(*cfg);
+    kvq::DecodePlan plan;
+    cudaError_t e = kvq::plan_decode(a, &plan);
+    if (e == cudaErrorInvalidValue) return fail(KVQ_EUNSUPPORTED, "no decode kernel for this shape");
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention plan");
+    if (workspace_bytes < plan.ws_bytes)
+        return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, plan.ws_bytes);
+    e = kvq::launch_decode(a, plan, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention launch");
+    return ok();
+}
+
+int kvq_dequantize(const kvq_cache_config* cfg, const void* pool, const int32_t* block_table, int32_t max_blocks,
+                   int32_t b, int32_t start, int32_t n, void* out_k, void* out_v, int32_t out_dtype, uint32_t* status,
+                   kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (b < 0 || start < 0 || n < 0) return fail(KVQ_EINVAL, "b %d, start %d, n %d", b, start, n);
+    if (out_dtype != 0 && out_dtype != 1) return fail(KVQ_EINVAL, "out_dtype %d not 0 (fp16) or 1 (fp32)", out_dtype);
+    if (n == 0) return ok();
+    if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
+    if (!pool || !block_table || !out_k || !out_v) return fail(KVQ_EINVAL, "NULL device pointer");
+    if (!aligned(pool, 16) || !aligned(out_k, 16) || !aligned(out_v, 16))
+        return fail(KVQ_EINVAL, "pool, out_k and out_v must be 16-byte aligned");
+    kvq::DequantArgs a;
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.block_table = block_table;
+    a.out_k = out_k;
+    a.out_v = out_v;
+    a.status = status;
+    a.max_blocks = max_blocks;
+    a.b = b;
+    a.start = start;
+    a.n = n;
+    a.Hkv = cfg->num_kv_heads;
+    a.num_pages = cfg->num_pages;
+    a.out_fp32 = out_dtype;
+    a.L = kvq::block_layout(*cfg);
+    cudaError_t e = kvq::launch_dequantize(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_dequantize launch");
+    return ok();
+}
+
+int kvq_read_status(const void* status_word, uint32_t* flags, kvq_stream_t stream) {
+    if (!status_word || !flags) return fail(KVQ_EINVAL, "NULL pointer");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(flags, status_word, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_read_status");
+    return ok();
+}
+
+const char* kvq_last_error(void) { return g_err; }
+
+const char* kvq_version(void) { return "kvq 0.1 (sm_103a)"; }
+
+}  // extern "C"

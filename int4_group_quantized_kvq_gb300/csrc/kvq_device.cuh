@@ -1,0 +1,145 @@
+// kvq_device.cuh -- device-side helpers shared by the kernels: inline PTX for the
+// bulk-copy engine, mbarriers, the f16 tensor-core MMA and the INT4 nibble unpack.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// ---------------------------------------------------------------------------
+// Status flags (device side).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void raise_flag(uint32_t* status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers and 1-D bulk copies (TMA engine).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make mbarrier initialisation visible to the asynchronous proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before later
+// asynchronous-proxy writes (a stage is refilled only after it has been read).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bulk copy global -> shared, completion signalled on `bar` as transaction bytes.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of the mbarrier to complete, giving up after `limit_ns`.
+// Returns true on completion.  Never spins without bound.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Packed f16 arithmetic and the nibble unpack.
+//
+// A nibble n in [0, 15] ORed into the mantissa of the fp16 value 1024 (0x6400)
+// gives exactly 1024 + n; subtracting 1032 leaves the signed code n - 8.  A nibble
+// sitting four bits higher gives 1024 + 16 n, and (1024 + 16 n) / 16 - 72 = n - 8.
+// Both results are exact in fp16.  Each helper handles the two 16-bit halves of a
+// 32-bit word at once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
+    uint32_t d;  // (a & mask) | orv
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(orv));
+    return d;
+}
+
+// Codes of the nibbles at bits [0,4) and [16,20) of w, as an f16x2 (low, high).
+__device__ __forceinline__ uint32_t unpack_lo(uint32_t w) {
+    return h2_sub(lop3_and_or(w, 0x000F000Fu, 0x64006400u), 0x64086408u);  // - 1032
+}
+// Codes of the nibbles at bits [4,8) and [20,24) of w, as an f16x2 (low, high).
+__device__ __forceinline__ uint32_t unpack_hi(uint32_t w) {
+    return h2_fma(lop3_and_or(w, 0x00F000F0u, 0x64006400u), 0x2C002C00u /* 1/16 */, 0xD480D480u /* -72 */);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// D += A * B, m16n8k16, A/B f16, accumulate f32 (tensor cores).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^x (hardware approximation, relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+}  // namespace kvq

@@ -1,0 +1,86 @@
+// kvq_internal.h -- launchers shared between the kernel files and the C ABI layer.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// Byte offsets of the four sections of a (page, kv-head) block.
+struct BlockLayout {
+    int32_t d, P, Gk, Gv;
+    int32_t v_codes;   // P * d / 2
+    int32_t k_scales;  // P * d
+    int32_t v_scales;  // P * d + P * (d / Gk) * 2
+    int32_t bytes;     // padded to 16
+};
+
+inline BlockLayout block_layout(const kvq_cache_config& c) {
+    BlockLayout L;
+    L.d = c.head_dim;
+    L.P = c.page_size;
+    L.Gk = c.group_k;
+    L.Gv = c.group_v;
+    L.v_codes = c.page_size * c.head_dim / 2;
+    L.k_scales = c.page_size * c.head_dim;
+    L.v_scales = L.k_scales + c.page_size * (c.head_dim / c.group_k) * 2;
+    const int32_t raw = L.v_scales + c.page_size * (c.head_dim / c.group_v) * 2;
+    L.bytes = (raw + 15) / 16 * 16;
+    return L;
+}
+
+struct QuantizeArgs {
+    uint8_t* pool;
+    const __half* k;
+    const __half* v;
+    const int32_t* block_table;
+    const int32_t* start_pos;
+    uint32_t* status;
+    int32_t max_blocks, B, n_new, Hkv, num_pages;
+    BlockLayout L;
+};
+cudaError_t launch_quantize_append(const QuantizeArgs& a, cudaStream_t stream);
+
+struct DequantArgs {
+    const uint8_t* pool;
+    const int32_t* block_table;
+    void* out_k;
+    void* out_v;
+    uint32_t* status;
+    int32_t max_blocks, b, start, n, Hkv, num_pages, out_fp32;
+    BlockLayout L;
+};
+cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t stream);
+
+// Decode attention: the persistent split-KV kernel plus the combine pass.
+struct DecodePlan {
+    int32_t warps;        // W: total consumer warps of the persistent grid (multiple of 4)
+    int32_t ctas;         // W / 4
+    int32_t stages;       // bulk-copy ring depth per warp
+    size_t smem_bytes;    // dynamic shared memory per CTA
+    size_t ws_ml_offset;  // byte offset of the (m, l) partials in the workspace
+    size_t ws_o_offset;   // byte offset of the o partials
+    size_t ws_bytes;      // total workspace bytes
+};
+
+struct DecodeArgs {
+    const uint8_t* pool;
+    const __half* q;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    float* out;
+    uint8_t* workspace;
+    int32_t max_blocks, B, Hq, Hkv, num_pages, max_len;
+    float softmax_scale;
+    BlockLayout L;
+};
+
+// Returns cudaErrorInvalidValue for a geometry no kernel instance covers.
+cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan);
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+
+}  // namespace kvq

@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI library (no GPU needed): it builds, loads, exports
+every function include/kvq.h declares, sizes blocks like the oracle, and rejects bad
+arguments on the host before touching the device."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def built():
+    from int4_group_quantized_kvq_gb300 import _build
+    return _build.build()
+
+
+def header_functions() -> set[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", text))
+
+
+def test_header_declares_the_abi():
+    names = header_functions()
+    assert {"kvq_quantize_append", "kvq_decode_attention", "kvq_dequantize", "kvq_block_bytes",
+            "kvq_decode_workspace_bytes", "kvq_read_status", "kvq_last_error"} <= names
+
+
+def test_library_exports_every_declared_symbol(built):
+    out = subprocess.run(["nm", "-D", "--defined-only", built], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (kvq_[a-z_]+)\b", out))
+    missing = header_functions() - exported
+    assert not missing, f"declared but not exported: {missing}"
+    lib = C.CDLL(built)
+    for name in header_functions():
+        assert hasattr(lib, name)
+
+
+def test_binding_names_match_header(built):
+    import int4_group_quantized_kvq_gb300 as kvq
+    assert set(kvq.ABI_SYMBOLS) == header_functions()
+    for name in kvq.ABI_SYMBOLS:
+        assert callable(getattr(kvq, name))
+
+
+@pytest.mark.parametrize("d,P,Gk,Gv", [(128, 16, 64, 128), (128, 16, 32, 32), (128, 16, 128, 128),
+                                       (64, 16, 32, 64), (256, 64, 128, 32), (128, 32, 64, 64)])
+def test_block_bytes_agree_with_oracle(built, d, P, Gk, Gv):
+    import int4_group_quantized_kvq_gb300 as kvq
+    import oracle
+    cfg = kvq.config(8, d, P, Gk, Gv, 10)
+    assert kvq.kvq_block_bytes(cfg) == oracle.block_bytes(d, P, Gk, Gv)
+    assert kvq.kvq_pool_bytes(cfg) == 10 * 8 * oracle.block_bytes(d, P, Gk, Gv)
+
+
+@pytest.mark.parametrize("field,value,code", [("head_dim", 96, 2), ("page_size", 24, 2), ("group_k", 16, 2),
+                                              ("group_v", 256, 2), ("num_kv_heads", 0, 1), ("num_pages", 0, 1)])
+def test_bad_geometry_rejected_on_host(built, field, value, code):
+    import int4_group_quantized_kvq_gb300 as kvq
+    cfg = kvq.config(8, 128, 16, 64, 128, 10)
+    setattr(cfg, field, value)
+    assert kvq.lib().kvq_block_bytes(C.byref(cfg)) == 0
+    rc = kvq.lib().kvq_quantize_append(C.byref(cfg), None, None, None, None, 1, None, 1, 1, None, None)
+    assert rc == code
+    assert kvq.kvq_last_error()
+
+
+def test_null_and_misaligned_pointers_rejected_on_host(built):
+    import int4_group_quantized_kvq_gb300 as kvq
+    L = kvq.lib()
+    cfg = kvq.config(8, 128, 16, 64, 128, 10)
+    assert L.kvq_quantize_append(C.byref(cfg), None, None, None, None, 4, None, 2, 1, None, None) == kvq.KVQ_EINVAL
+    assert L.kvq_quantize_append(C.byref(cfg), 0x1008, 0x2000, 0x3000, 0x4000, 4, 0x5000, 2, 1, None,
+                                 None) == kvq.KVQ_EINVAL  # pool not 16-byte aligned
+    assert "aligned" in kvq.kvq_last_error()
+    # nothing to do is not an error
+    assert L.kvq_quantize_append(C.byref(cfg), None, None, None, None, 4, None, 0, 1, None, None) == kvq.KVQ_OK
+    # decode: ratio > 8, head_dim 64, misaligned workspace
+    assert L.kvq_decode_attention(C.byref(cfg), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 72, 10, 1.0, 0x5000,
+                                  0x6000, 1 << 20, None) == kvq.KVQ_EUNSUPPORTED
+    cfg64 = kvq.config(8, 64, 16, 32, 64, 10)
+    assert L.kvq_decode_attention(C.byref(cfg64), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 8, 10, 1.0, 0x5000,
+                                  0x6000, 1 << 20, None) == kvq.KVQ_EUNSUPPORTED
+    assert L.kvq_decode_attention(C.byref(cfg), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 8, 10, 1.0, 0x5000,
+                                  0x6010, 1 << 20, None) == kvq.KVQ_EINVAL
+    assert L.kvq_decode_attention(C.byref(cfg), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 12, 10, 1.0, 0x5000,
+                                  0x6000, 1 << 20, None) == kvq.KVQ_EINVAL  # 12 % 8 != 0
+    assert L.kvq_dequantize(C.byref(cfg), 0x1000, 0x2000, 4, 0, 0, 4, 0x3000, 0x4000, 2, None,
+                            None) == kvq.KVQ_EINVAL  # out_dtype
+    assert L.kvq_read_status(None, None, None) == kvq.KVQ_EINVAL
+
+
+def test_version_string(built):
+    import int4_group_quantized_kvq_gb300 as kvq
+    assert "sm_103a" in kvq.kvq_version()
