@@ -45,8 +45,10 @@ def parse_args():
     ap.add_argument("--workload", default="llama7b", help="llama7b (default), gqa8b, ragged, longctx, tiny")
     ap.add_argument("--group", type=int, default=None, help="K and V group size for the longctx sweep")
     ap.add_argument("--graph-steps", type=int, default=200, help="steps captured per CUDA graph")
+    ap.add_argument("--eager", action="store_true", help="launch every step from Python instead of graphs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-quality", action="store_true", help="skip the dequantization quality report")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
     return ap.parse_args()
 
@@ -216,6 +218,47 @@ def time_oracle(wl, budget_s: float) -> dict:
 
 
 # ---------------------------------------------------------------------------
+# dequantization quality against the fp16 input
+# ---------------------------------------------------------------------------
+
+def quality_report(dev, tokens: int = 4096, heads: int = 32, d: int = 128) -> dict:
+    """Per group size G in {32, 64, 128} (K and V both grouped at G): quantize seeded fp16 rows
+    through the library, dequantize them back (fp32, exact), and compare with the fp16 input
+    row by row (a row = one token of one head, d values).  K carries the x20 outlier channels.
+    The group step s is read back from the dequantized values (max |x^| over a nonzero group
+    is exactly 7 s)."""
+    import torch
+
+    import int4_group_quantized_kvq_gb300 as kvq
+    import workloads as W
+    k = W.kv_tensor(W.SEED_K, (1, tokens, heads, d), 20.0, W.outlier_channels(heads, d), device=dev)
+    v = W.kv_tensor(W.SEED_V, (1, tokens, heads, d), device=dev)
+    P = 16
+    npg = tokens // P
+    bt = torch.arange(npg, dtype=torch.int32, device=dev).view(1, -1)
+    rep = {}
+    for G in (32, 64, 128):
+        cfg = kvq.config(heads, d, P, G, G, npg)
+        pool = torch.zeros(kvq.kvq_pool_bytes(cfg), dtype=torch.uint8, device=dev)
+        kvq.kvq_quantize_append(cfg, pool, k, v, bt, torch.zeros(1, dtype=torch.int32, device=dev))
+        dk = torch.empty((tokens, heads, d), dtype=torch.float32, device=dev)
+        dv = torch.empty_like(dk)
+        kvq.kvq_dequantize(cfg, pool, bt, 0, 0, tokens, dk, dv)
+        out = {}
+        for name, x, xh in (("K", k[0].float(), dk), ("V", v[0].float(), dv)):
+            cos = torch.nn.functional.cosine_similarity(x.reshape(-1, d), xh.reshape(-1, d), dim=1)
+            err = (x - xh).abs()
+            step = xh.abs().reshape(tokens, heads, d // G, G).amax(-1, keepdim=True) / 7.0
+            ratio = (err.reshape(tokens, heads, d // G, G) / step.clamp_min(1e-30)).amax()
+            out[name] = {"cos_mean": float(cos.mean()), "cos_min": float(cos.min()),
+                         "max_abs_err": float(err.max()), "max_err_over_scale": float(ratio),
+                         "mse": float((err ** 2).mean())}
+        rep[f"G{G}"] = out
+    rep["rows"] = f"{tokens} tokens x {heads} heads, d={d}, N(0,1) fp16; K with 4 x20 outlier channels per head"
+    return rep
+
+
+# ---------------------------------------------------------------------------
 # the CUDA path
 # ---------------------------------------------------------------------------
 
@@ -296,23 +339,32 @@ def run_kvq(args, world, rank, local):
             caches[i % n_pools].decode_step(q, k_new, v_new, pos, seq_lens, out, stream=stream)
     stream.synchronize()
 
-    # ---- capture G steps (rotating pools) with events around each decode attention call ----
-    G = max(g for g in range(1, min(K, args.graph_steps) + 1) if K % g == 0)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(G)]
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(G):
-            c = caches[i % n_pools]
-            c.append(k_new, v_new, pos, stream=stream)
-            ev[i][0].record(stream)
-            c.attend(q, seq_lens, out, stream=stream)
-            ev[i][1].record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            graph.replay()
-    stream.synchronize()
+    # ---- the timed steps: CUDA graphs of G steps (rotating pools) with events recorded as graph
+    # nodes around each decode attention call; eager launches if this torch cannot record
+    # events inside a graph ----
+    def timing_event():
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True), True
+        except TypeError:
+            return torch.cuda.Event(enable_timing=True), False
 
-    # ---- timed region ----
+    use_graph = not args.eager and timing_event()[1]
+    G = max(g for g in range(1, min(K, args.graph_steps) + 1) if K % g == 0) if use_graph else K
+    ev = [(timing_event()[0], timing_event()[0]) for _ in range(G)]
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(G):
+                c = caches[i % n_pools]
+                c.append(k_new, v_new, pos, stream=stream)
+                ev[i][0].record(stream)
+                c.attend(q, seq_lens, out, stream=stream)
+                ev[i][1].record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                graph.replay()
+        stream.synchronize()
+
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -322,8 +374,16 @@ def run_kvq(args, world, rank, local):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for _ in range(K // G):
-            graph.replay()
+        if use_graph:
+            for _ in range(K // G):
+                graph.replay()
+        else:
+            for i in range(K):
+                c = caches[i % n_pools]
+                c.append(k_new, v_new, pos, stream=stream)
+                ev[i][0].record(stream)
+                c.attend(q, seq_lens, out, stream=stream)
+                ev[i][1].record(stream)
         t_end.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
@@ -331,7 +391,7 @@ def run_kvq(args, world, rank, local):
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     t_local = t_start.elapsed_time(t_end) * 1e-3
-    decode_s = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e-3  # last replay's G launches
+    decode_s = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e-3  # (last replay's) decode calls
     flags = max(c.flags() for c in caches)
     if world > 1:
         t = torch.tensor([t_local], dtype=torch.float64, device=dev)
@@ -401,7 +461,8 @@ def run_kvq(args, world, rank, local):
             "l2": f"inputs larger than L2: {n_pools} rotated pool copies of {pool_bytes / 1e6:.1f} MB "
                   f"against a {l2 / 1e6:.0f} MB L2",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "timing": f"CUDA graphs of {G} steps replayed {K // G} times, CUDA events on the launch stream",
+            "timing": (f"CUDA graphs of {G} steps replayed {K // G} times" if use_graph else "eager launches")
+            + ", CUDA events on the launch stream",
         },
         "tokens_per_s": world * wl.B / step_s,
         "decode_us": decode_s * 1e6,
@@ -421,6 +482,8 @@ def run_kvq(args, world, rank, local):
         "status_flags": flags,
         "clocks": clocks,
     }
+    if not args.no_quality:
+        res["quality"] = quality_report(dev)
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = time_oracle(wl, args.cpu_seconds)
         res["cpu_baseline"].pop("seconds_per_step", None)
