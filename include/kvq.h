@@ -18,7 +18,8 @@
  * Conventions
  *   - Every pointer argument except `cfg` and host outputs is a DEVICE pointer on the
  *     current CUDA device.  The caller owns and allocates all memory; the library
- *     allocates nothing and keeps no state except a per-thread error string.
+ *     allocates nothing and keeps no state except a per-thread error string (and the
+ *     built-in scratch array of kvq_decode_attention_noalloc, described there).
  *   - Every call is asynchronous on `stream` (NULL = the legacy default stream).
  *     Buffers must stay valid until the stream reaches the call.
  *   - Return value: KVQ_OK or an error code; kvq_last_error() describes the last
@@ -139,6 +140,29 @@ int kvq_decode_attention(const kvq_cache_config *cfg, const void *pool, const vo
                          const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
                          int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
                          float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * Decode attention that allocates nothing, for callers that cannot provide a
+ * workspace: a plugin inside a host engine that owns no device allocator, an
+ * embedded or real-time runtime with a fixed memory budget that forbids allocation
+ * while serving, code on an out-of-memory path.  (No passage of the pages has a
+ * counterpart; this is an interface variant of kvq_decode_attention.)
+ * Same computation and arguments as kvq_decode_attention, without the workspace:
+ * the scratch lives in an 8 MiB array built into the library, which every GPU that
+ * loads the library holds until the process exits.  No cudaMalloc, cudaFree or other
+ * allocating call is made.
+ *   status   device uint32 or NULL: receives this call's status flags.
+ * The first call on a device looks up the array's address on that device; make that
+ * first call before any stream capture.  All calls on a device share the array, so
+ * calls whose work overlaps on the GPU (other streams or threads) race: serialize them.
+ * A shape that needs more scratch than 8 MiB (see kvq_decode_workspace_bytes) is
+ * rejected with KVQ_EWORKSPACE before anything is launched.
+ * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE or KVQ_ECUDA.
+ */
+int kvq_decode_attention_noalloc(const kvq_cache_config *cfg, const void *pool, const void *q,
+                                 const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                                 int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                                 float *out, uint32_t *status, kvq_stream_t stream);
 
 /*
  * Dequantize positions [start, start + n) of sequence b (section 2.1 of the 4-bit

@@ -21,6 +21,7 @@ from .binding import (  # noqa: F401
     config,
     kvq_block_bytes,
     kvq_decode_attention,
+    kvq_decode_attention_noalloc,
     kvq_decode_workspace_bytes,
     kvq_dequantize,
     kvq_last_error,

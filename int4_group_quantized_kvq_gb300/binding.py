@@ -19,7 +19,8 @@ KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE, KVQ_ECUDA = 0, 1, 2, 3, 4
 KVQ_FLAG_BAD_PAGE, KVQ_FLAG_BAD_POSITION, KVQ_FLAG_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 
 ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
-               "kvq_decode_attention", "kvq_dequantize", "kvq_read_status", "kvq_last_error", "kvq_version")
+               "kvq_decode_attention", "kvq_dequantize", "kvq_read_status", "kvq_last_error", "kvq_version",
+               "kvq_decode_attention_noalloc")
 
 
 class KvqError(RuntimeError):
@@ -62,6 +63,8 @@ def lib() -> C.CDLL:
         L.kvq_decode_workspace_bytes.restype = SZ
         L.kvq_decode_attention.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
         L.kvq_decode_attention.restype = C.c_int
+        L.kvq_decode_attention_noalloc.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, P]
+        L.kvq_decode_attention_noalloc.restype = C.c_int
         L.kvq_dequantize.argtypes = [cfgp, P, P, I32, I32, I32, I32, P, P, I32, P, P]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_read_status.argtypes = [P, C.POINTER(C.c_uint32), P]
@@ -157,6 +160,20 @@ def kvq_decode_attention(cfg: CacheConfig, pool: torch.Tensor, q: torch.Tensor, 
         _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
         _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
         _stream(stream))
+    _check(rc)
+
+
+def kvq_decode_attention_noalloc(cfg: CacheConfig, pool: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
+                                 seq_lens: torch.Tensor, max_len: int, softmax_scale: float, out: torch.Tensor,
+                                 status: torch.Tensor | None = None, stream=None) -> None:
+    """kvq_decode_attention for callers that cannot allocate: no workspace argument; the
+    library's built-in scratch (8 MiB) is used.  Calls that overlap on the GPU race on it."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_decode_attention_noalloc(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(q, "q", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
+        _dev(out, "out", torch.float32), None if status is None else _dev(status, "status"), _stream(stream))
     _check(rc)
 
 

@@ -5,6 +5,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 
 #include "kvq.h"
 #include "kvq_internal.h"
@@ -210,3 +211,110 @@ const char* kvq_last_error(void) { return g_err; }
 const char* kvq_version(void) { return "kvq 0.1 (sm_103a)"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode attention without any allocation.
+//
+// Some callers cannot hand the library a workspace.  A plugin inside a host
+// engine may own no device allocator.  An embedded or real-time runtime may run
+// with a fixed memory budget and forbid allocation once serving starts.  Code on
+// an out-of-memory path cannot ask for more memory.  For them this entry point
+// keeps its scratch in one array compiled into the library
+// (kNoAllocScratchBytes = 8 MiB, held on every GPU that loads the library until
+// the process exits) and never calls cudaMalloc, cudaFree or any allocating
+// routine.
+//
+// The first call on a device looks up that device's address of the array
+// (cudaGetSymbolAddress, with the device current); make that first call before
+// any stream capture.  Every call on a device uses the same array, and the array
+// keeps what the last call left in it.  Calls whose work overlaps on the GPU
+// (other streams, other threads) race on it: serialize them.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(8) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once per device).
+cudaError_t noalloc_scratch(void** ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (dev >= 0 && dev < kMaxDevices && g_noalloc_ptr[dev]) {
+        *ptr = g_noalloc_ptr[dev];
+        return cudaSuccess;
+    }
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) g_noalloc_ptr[dev] = p;
+    *ptr = p;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int kvq_decode_attention_noalloc(const kvq_cache_config* cfg, const void* pool, const void* q,
+                                            const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                                            int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                                            float* out, uint32_t* status, kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || num_q_heads < 1 || max_len < 0)
+        return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
+    if (num_q_heads % cfg->num_kv_heads)
+        return fail(KVQ_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, cfg->num_kv_heads);
+    if (num_q_heads / cfg->num_kv_heads > 8)
+        return fail(KVQ_EUNSUPPORTED, "query heads per KV head %d > 8", num_q_heads / cfg->num_kv_heads);
+    if (cfg->head_dim != 128) return fail(KVQ_EUNSUPPORTED, "decode attention supports head_dim 128");
+    if (batch > 4096) return fail(KVQ_EUNSUPPORTED, "batch %d > 4096", batch);
+    if (batch == 0) return ok();
+    if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
+    if (!pool || !q || !block_table || !seq_lens || !out) return fail(KVQ_EINVAL, "NULL device pointer");
+    if (!aligned(pool, 16) || !aligned(q, 16) || !aligned(out, 16))
+        return fail(KVQ_EINVAL, "pool, q and out must be 16-byte aligned");
+    if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || (status && !aligned(status, 4)))
+        return fail(KVQ_EINVAL, "int32/uint32 arguments must be 4-byte aligned");
+    kvq::DecodeArgs a;
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.q = static_cast<const __half*>(q);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.max_blocks = max_blocks;
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hkv = cfg->num_kv_heads;
+    a.num_pages = cfg->num_pages;
+    a.max_len = max_len;
+    a.softmax_scale = softmax_scale;
+    a.L = kvq::block_layout(*cfg);
+    kvq::DecodePlan plan;
+    cudaError_t e = kvq::plan_decode(a, &plan);
+    if (e == cudaErrorInvalidValue) return fail(KVQ_EUNSUPPORTED, "no decode kernel for this shape");
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention_noalloc plan");
+    if (plan.ws_bytes > kNoAllocScratchBytes)
+        return fail(KVQ_EWORKSPACE,
+                    "this shape needs %zu bytes of scratch; the built-in scratch of kvq_decode_attention_noalloc "
+                    "holds %zu bytes (use kvq_decode_attention with a workspace)",
+                    plan.ws_bytes, kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention_noalloc scratch lookup");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the status word starts each call at zero; the partial results need no clearing
+    e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention_noalloc status clear");
+    a.workspace = static_cast<uint8_t*>(scratch);
+    e = kvq::launch_decode(a, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention_noalloc launch");
+    if (status) {
+        e = cudaMemcpyAsync(status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention_noalloc status copy");
+    }
+    return ok();
+}
