@@ -456,7 +456,7 @@ def run_kvq(args, world, rank, local):
             "batch": wl.B, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.d,
             "context": wl.ctx[0] if len(set(wl.ctx)) == 1 else f"{min(wl.ctx)}..{max(wl.ctx)}",
             "attended_tokens": sum(wl.seq_lens), "page_size": wl.P, "group_k": wl.Gk, "group_v": wl.Gv,
-            "step": "quantize-append 1 token per sequence + decode attention (split-KV + combine)",
+            "step": "quantize-append 1 token per sequence + decode attention (split-KV, fused combine)",
             "bytes_per_step": step_bytes,
             "l2": f"inputs larger than L2: {n_pools} rotated pool copies of {pool_bytes / 1e6:.1f} MB "
                   f"against a {l2 / 1e6:.0f} MB L2",
@@ -474,11 +474,11 @@ def run_kvq(args, world, rank, local):
             "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"],
             "traffic": None,
-            "kernel": "kvq_decode_attention (split-KV decode + combine), packed bytes of the cache per call",
+            "kernel": "decode_splitkv_kernel (kvq_decode_attention), packed bytes of the cache per call",
             "peak_source": peaks["source"],
         },
         "e2e": e2e,
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,  # quantize-append + decode (split combine fused in) per step
         "status_flags": flags,
         "clocks": clocks,
     }

@@ -86,6 +86,9 @@ enum {
 #define KVQ_FLAG_BAD_PAGE 0x1u     /* a block-table entry outside [0, num_pages)          */
 #define KVQ_FLAG_BAD_POSITION 0x2u /* a position or length beyond max_blocks * page_size  */
 #define KVQ_FLAG_WAIT_TIMEOUT 0x4u /* an asynchronous copy did not complete in time       */
+#define KVQ_FLAG_STALE_WORKSPACE 0x8u /* a split counter was not zero when the call began:
+                                         the workspace was not zeroed, or was last used for
+                                         another shape (the outputs of the call are unreliable) */
 
 /* Bytes of one (page, kv-head) block; 0 if cfg is invalid.  Pure host computation. */
 size_t kvq_block_bytes(const kvq_cache_config *cfg);
@@ -131,8 +134,12 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_config *cfg, int32_t batch, in
  *   max_len       host bound on every seq_lens[b] (sizes the workspace).
  *   out           device fp32 [batch, num_q_heads, head_dim], 16-byte aligned.
  *   workspace     device, >= kvq_decode_workspace_bytes(...) bytes, 256-byte aligned.
- *                 Its first 4 bytes are the status word (zero it once after
- *                 allocating); the rest is scratch for split-KV partial results.
+ *                 Its first 4 bytes are the status word; the rest holds split-KV
+ *                 partial results and one counter per (sequence, kv head).  Zero the
+ *                 whole workspace after allocating it.  The counters return to zero at
+ *                 the end of every call, so the workspace can serve any number of calls
+ *                 of the same (cfg, batch, num_q_heads, max_len); zero it again before
+ *                 using it for another shape.
  * num_q_heads must be a multiple of num_kv_heads with a ratio of at most 8.
  * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE or KVQ_ECUDA.
  */

@@ -56,14 +56,18 @@ struct DequantArgs {
 };
 cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t stream);
 
-// Decode attention: the persistent split-KV kernel plus the combine pass.
+// Decode attention: the persistent split-KV kernel with the split combine fused in.
 struct DecodePlan {
     int32_t warps;        // W: total consumer warps of the persistent grid (multiple of 4)
     int32_t ctas;         // W / 4
     int32_t stages;       // bulk-copy ring depth per warp
     size_t smem_bytes;    // dynamic shared memory per CTA
-    size_t ws_ml_offset;  // byte offset of the (m, l) partials in the workspace
-    size_t ws_o_offset;   // byte offset of the o partials
+    size_t ws_cnt_offset;  // per-(sequence, kv head) split counters
+    size_t ws_gcnt_offset; // per-group counters of long segments
+    size_t ws_ml_offset;   // (m, l) partials
+    size_t ws_o_offset;    // o partials
+    size_t ws_gml_offset;  // level-2 (m, l) partials of long segments
+    size_t ws_go_offset;   // level-2 o partials
     size_t ws_bytes;      // total workspace bytes
 };
 

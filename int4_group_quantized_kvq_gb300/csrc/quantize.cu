@@ -22,6 +22,9 @@ namespace {
 
 template <int D>
 __global__ void __launch_bounds__(256) quantize_append_kernel(QuantizeArgs a) {
+    // a decode launched behind this kernel may start its own set-up now; it waits for
+    // this grid to finish before it reads the pool
+    asm volatile("griddepcontrol.launch_dependents;");
     constexpr int LPR = D / 8;            // lanes per row
     constexpr int TEAMS = 32 / LPR;       // row jobs per warp at a time
     const int lane = threadIdx.x & 31;
