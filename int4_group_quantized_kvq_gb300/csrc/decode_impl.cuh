@@ -12,39 +12,47 @@
 // cache compression" section 1.3 on Flash attention).
 //
 // Design for GB300 (sm_103a):
-//  * Work is the flattened list of (sequence, kv head, page) units.  A persistent grid
-//    of W warps (SM count x resident CTAs x 4) gives every warp an equal contiguous
-//    slice, so ragged lengths and small batches still keep every SM busy.
-//  * Each warp owns a ring of `stages` page buffers in shared memory, filled by 1-D
+//  * A unit of work is one page of HK consecutive kv heads of one sequence: HK = 4 when
+//    every query head has its own kv head (Hq == Hkv) and pages hold 16 tokens, else
+//    HK = 1 and the unit serves the r = Hq / Hkv query heads that share the kv head.  The HK blocks of a unit are
+//    adjacent in the pool (block index page * Hkv + head), so one bulk copy moves them.
+//    Either way a unit feeds 4 (or 8) query heads, the "slots" of the MMA tiles below.
+//  * A persistent grid of CTAs (SM count x resident CTAs) gives every CTA an equal
+//    contiguous slice of the flattened (sequence, head group, page) units, so ragged
+//    lengths and small batches keep every SM busy.  The CTA's four warps take the units
+//    of its slice in turn (warp k: units k, k + 4, ...), so they move through the same
+//    (sequence, head group) segments together.
+//  * Each warp owns a ring of `stages` unit buffers in shared memory, filled by 1-D
 //    bulk copies (the TMA engine, cp.async.bulk) that complete on per-stage mbarriers.
-//    A (page, head) block is contiguous (2144 bytes at d=128, P=16), so one copy moves
-//    a whole page of K codes, V codes and scales.  Waits are bounded in time.
+//    Waits are bounded in time.
 //  * The arithmetic runs on the tensor cores (mma.sync m16n8k16, f16 inputs, f32
-//    accumulate), which keeps the per-element ALU work near one instruction: nibbles
-//    become exact f16 integers in two instructions per pair, and the MMA does the
-//    multiply-accumulate.  For a 16-token chunk:
+//    accumulate): nibbles become exact f16 integers in two instructions per pair and
+//    the MMA does the multiply-accumulate.  For a 16-token chunk of one kv head:
 //      scores  S[token, col] = K[token, :] . Qcol  with M = 16 tokens, N = 8 columns,
-//              K-dim = head_dim.  Column (head, k-group) carries q masked to that group,
-//              so each group's partial dot product comes out separately and is scaled
-//              by its own fp16 scale afterwards (codes and q are exact in f16; products
-//              and sums are fp32).
+//              K-dim = head_dim.  Column (slot, k-group) carries the slot's q masked to
+//              that group, so each group's partial dot product comes out separately
+//              and is scaled by its own fp16 scale afterwards (codes and q are exact in
+//              f16; products and sums are fp32).  With HK = 4 each kv head's chunk has
+//              its own accumulator and a thread keeps the one of its slot's head.
 //      output  O^T[d, col] += V^T[d, token] . W[token, col] with M = 16 dims, N = 8
-//              columns (head, hi|lo), K-dim = 16 tokens.  W = p * v_scale is split into
+//              columns (slot, hi|lo), K-dim = 16 tokens.  W = p * v_scale is split into
 //              an f16 high part and an f16 remainder, two columns of the same MMA, which
-//              keeps about 22 bits of the weight.  M-tiles never straddle a V group.
-//    The score fragment of thread (g, c) holds tokens g, g+8 of head c (+4), and the
-//    output fragment holds head c (+4) too, so the softmax rescale is thread-local;
-//    only the weights are exchanged (four shuffles per chunk and V group).
-//    Chunks are taken two at a time (two 16-token pages, or two chunks of a larger
+//              keeps about 22 bits of the weight.  With HK = 4 the columns of the other
+//              heads' slots are zeroed for each head's MMA.  M-tiles never straddle a
+//              V group.
+//    The score fragment of thread (g, c) holds tokens g, g+8 of slot c (+4), and the
+//    output fragment holds slot c (+4) too, so the softmax rescale is thread-local;
+//    only the weights are exchanged (four shuffles per chunk and V group).  With HK = 1
+//    chunks are taken two at a time (two 16-token pages, or two chunks of a larger
 //    page): the two score chains interleave and one softmax reduction covers both.
-//  * Split combine, fused: a warp that finishes its part of a (sequence, kv head)
-//    segment writes a partial (running max, running sum, unnormalised output), then
-//    bumps a counter (fence + atomic add, never waiting on other warps; the result is
-//    looked at one segment later so the round trip overlaps streaming).  The warp that
-//    counted last merges: all partials of a segment spread over at most 32 warps, or,
-//    for longer segments, its group of 32 partials into a level-2 partial, the last
-//    group then merging those.  Counters return to zero for the next call.  A segment
-//    covered by one warp is written directly from registers.
+//  * Split combine, fused.  At the end of each segment the four warps of a CTA merge
+//    their parts in shared memory (each writes its part into the ring stage it has just
+//    consumed, whose refill waits for the merge).  A segment inside one CTA's slice is
+//    written out directly; otherwise the CTA writes a partial (running max, running
+//    sum, unnormalised output) and bumps the segment's counter (fence + atomic add; the
+//    result is looked at when the CTA next reaches a segment end, so the round trip
+//    overlaps streaming).  The CTA that counted last merges all partials of the
+//    segment with its 128 threads, and sets the counter back to zero for the next call.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -60,16 +68,18 @@ namespace kvq {
 namespace decode {
 
 constexpr int kWarps = 4;                         // warps per CTA
-constexpr int kMergeFanIn = 32;                   // longest segment (in warps) merged in-kernel
-
-// Per-warp values needed only at segment ends, kept in shared memory rather than in
-// registers (the hot loop needs every register it can get).
-struct WarpCtx {
-    long long U, W, wid;
-    int pend_kind, pend_b, pend_h, pend_gi, pend_target;
-    int pad;
-};
 constexpr uint64_t kWaitLimitNs = 250000000ull;   // a page copy that takes 250 ms has failed
+
+// CTA-wide bookkeeping in shared memory.
+struct CtaCtl {
+    int buf[kWarps];     // ring stage holding warp w's part at a segment end (-1: none)
+    int pend_valid;      // a partial of segment (pend_b, pend_hg) has been counted ...
+    int pend_b, pend_hg;
+    int pend_target;     // ... out of pend_target, and the count came back as pend_arrived
+    int pend_arrived;
+    int pad[7];
+};
+static_assert(sizeof(CtaCtl) % 16 == 0, "keeps the prefix array aligned");
 
 struct KParams {
     const uint8_t* pool;
@@ -77,14 +87,12 @@ struct KParams {
     const int32_t* block_table;
     const int32_t* seq_lens;
     float* out;
-    float* ws_ml;       // level-1 partials (one per warp and segment it touches): (max, sum)
-    float* ws_o;        //   ... and unnormalised outputs
-    float* ws_gml;      // level-2 partials (one per group of 32 warps of a long segment)
-    float* ws_go;
+    float* ws_ml;       // CTA partials (one per CTA and segment it touches): (max, sum) per slot
+    float* ws_o;        //   ... and unnormalised outputs per slot
     int32_t* counters;  // per segment; zero between calls
-    int32_t* gcounters; // per group of a long segment; zero between calls
     uint32_t* status;
-    int32_t B, Hq, Hkv, r, P, num_pages, max_blocks, block_bytes, stages;
+    int32_t B, Hq, Hkv, Hg, r, ns;  // Hg = Hkv / HK head groups; ns = HK * r query heads per unit
+    int32_t P, num_pages, max_blocks, block_bytes, unit_bytes, stages;
     int32_t v_codes, k_scales, v_scales;
     float scale_log2;  // softmax_scale * log2(e)
 };
@@ -117,199 +125,124 @@ __device__ __forceinline__ void page_prefix(const KParams& p, int32_t* pre, int 
     if (lane == 0) pre[p.B] = carry;
 }
 
-// Sequence index b containing unit u (largest b with Hkv * pre[b] <= u).
-__device__ __forceinline__ int find_seq(const int32_t* pre, int B, int Hkv, long long u) {
+// Sequence index b containing unit u (largest b with Hg * pre[b] <= u).
+__device__ __forceinline__ int find_seq(const int32_t* pre, int B, int Hg, long long u) {
     int lo = 0, hi = B - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<long long>(Hkv) * pre[mid] <= u) lo = mid;
+        if (static_cast<long long>(Hg) * pre[mid] <= u) lo = mid;
         else hi = mid - 1;
     }
     return lo;
 }
 
-// Global address of the block of unit u, validating the page id.
-__device__ __forceinline__ const uint8_t* unit_block(const KParams& p, const int32_t* pre, long long u) {
-    const int b = find_seq(pre, p.B, p.Hkv, u);
-    const long long rem = u - static_cast<long long>(p.Hkv) * pre[b];
+// Global address of the HK blocks of unit u, validating the page id.
+__device__ __forceinline__ const uint8_t* unit_block(const KParams& p, const int32_t* pre, long long u, int HK) {
+    const int b = find_seq(pre, p.B, p.Hg, u);
+    const long long rem = u - static_cast<long long>(p.Hg) * pre[b];
     const int np = pre[b + 1] - pre[b];
-    const int h = static_cast<int>(rem / np);
-    const int pg = static_cast<int>(rem - static_cast<long long>(h) * np);
+    const int hg = static_cast<int>(rem / np);
+    const int pg = static_cast<int>(rem - static_cast<long long>(hg) * np);
     int page = p.block_table[static_cast<long long>(b) * p.max_blocks + pg];
     if (page < 0 || page >= p.num_pages) {
         raise_flag(p.status, KVQ_FLAG_BAD_PAGE);
         page = 0;
     }
-    return p.pool + (static_cast<long long>(page) * p.Hkv + h) * p.block_bytes;
+    return p.pool + (static_cast<long long>(page) * p.Hkv + static_cast<long long>(hg) * HK) * p.block_bytes;
 }
 
-// First unit of warp w's slice of U units split over W warps.
+// First unit of slice w of U units split over W slices.
 __device__ __forceinline__ long long slice_start(long long w, long long U, long long W) { return w * U / W; }
 
-// The warp whose slice contains unit u (the largest w with slice_start(w) <= u).
+// The slice containing unit u (the largest w with slice_start(w) <= u).
 __device__ __forceinline__ long long slice_of(long long u, long long U, long long W) { return ((u + 1) * W - 1) / U; }
 
-// What a warp ending its part of segment (b, h) needs to know: the warps sharing the
-// segment (n), whether it alone holds it, and which counter stands for its partial (the
-// segment's, or that of its group of 32 when n > kMergeFanIn) with how many partials.
-struct SegEnd {
-    int n;            // warps whose slices touch the segment
-    int alone;        // 1: this warp holds the whole segment
-    int kind;         // 1: segment counter, 2: group counter
-    int gi;           // group index within the segment (kind 2)
-    int target;       // partials the counter stands for
-    long long cidx;   // counter index (segment, or group's first partial slot)
-};
-
-static __device__ __noinline__ SegEnd segment_end(const int32_t* pre, int b, int h, int Hkv, long long U, long long W,
-                                           long long wid, int lane) {
-    SegEnd e;
-    const int np = pre[b + 1] - pre[b];
-    const long long seg = static_cast<long long>(b) * Hkv + h;
-    const long long a_unit = static_cast<long long>(Hkv) * pre[b] + static_cast<long long>(h) * np;
-    const long long wf = slice_of(a_unit, U, W);
-    const long long wl = slice_of(a_unit + np - 1, U, W);
-    const bool dense = U >= W;  // every slice non-empty
-    e.n = static_cast<int>(wl - wf + 1);
-    e.gi = e.n > kMergeFanIn ? static_cast<int>((wid - wf) / 32) : 0;
-    const long long c0 = e.n > kMergeFanIn ? wf + 32LL * e.gi : wf;
-    const long long c1 = e.n > kMergeFanIn ? (c0 + 31 < wl ? c0 + 31 : wl) : wl;
-    int pieces = static_cast<int>(c1 - c0 + 1);
-    if (!dense) {
-        pieces = 0;
-        for (long long w0 = c0; w0 <= c1; w0 += 32) {
-            const long long w = w0 + lane;
-            pieces += __popc(__ballot_sync(0xffffffffu, w <= c1 && slice_start(w, U, W) < slice_start(w + 1, U, W)));
-        }
-    }
-    e.alone = (e.n == 1 || (!dense && e.n <= kMergeFanIn && pieces == 1)) ? 1 : 0;
-    e.kind = e.n > kMergeFanIn ? 2 : 1;
-    e.target = pieces;
-    e.cidx = e.n > kMergeFanIn ? c0 + seg : seg;
-    return e;
+// Slot of the CTA partial that CTA k writes for segment seg, or -1 when CTA k's slice is
+// empty.  k + seg is unique: if CTA k touches segment s and CTA k - 1 touches s + 1,
+// CTA k - 1 would hold a later unit than CTA k, which ordered slices rule out.
+__device__ __forceinline__ long long piece_index(long long k, long long seg, long long U, long long C) {
+    return (U >= C || slice_start(k, U, C) < slice_start(k + 1, U, C)) ? k + seg : -1;
 }
 
-// Merge n partials (max, sum, unnormalised output) of one segment, read through index(k)
-// (partial k's slot; -1 = empty), for each of the r query heads.  The result goes to the
-// normalised output of (b, h) when final, else to the level-2 slot `dst`.  Lane i takes
-// partials i, i + 32, ... for the maxima and sums; the outputs are folded 4 dimensions
-// per lane with 8 loads in flight.
-template <int D, typename Index>
-__device__ __forceinline__ void merge_partials(const KParams& p, const float* src_ml, const float* src_o, int n,
-                                               Index index, bool final_out, long long dst, int b, int h, int lane) {
-    for (int j = 0; j < p.r; ++j) {
+// Merge the CTA partials of segment (b, hg), spread over the slices of CTAs cf..cl, into
+// the normalised output; run by all threads of the CTA that counted last.  Warp w takes
+// slots w and w + 4, lane l dimensions 4l .. 4l + 3; partials are read 16 at a time.
+template <int D>
+__device__ __noinline__ void merge_segment(const KParams& p, int b, int hg, long long cf, long long cl,
+                                           long long U, long long C) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long seg = static_cast<long long>(b) * p.Hg + hg;
+    const int n = static_cast<int>(cl - cf + 1);
+    __threadfence();  // the partials counted before this CTA are visible
+    for (int sl = warp; sl < p.ns; sl += kWarps) {
         float M = -INFINITY;
-        for (int k0 = 0; k0 < n; k0 += 32) {
-            const long long ix = k0 + lane < n ? index(k0 + lane) : -1;
-            if (ix >= 0) M = fmaxf(M, __ldcg(src_ml + (ix * p.r + j) * 2));
+        for (int k = lane; k < n; k += 32) {
+            const long long ix = piece_index(cf + k, seg, U, C);
+            if (ix >= 0) M = fmaxf(M, __ldcg(p.ws_ml + (ix * p.ns + sl) * 2));
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float Lsum = 0.f;
+        float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const long long stride4 = static_cast<long long>(p.r) * D / 4;
-        for (int k0 = 0; k0 < n; k0 += 32) {
-            const long long ix = k0 + lane < n ? index(k0 + lane) : -1;
-            float f = 0.f;
-            if (ix >= 0) {
-                const float2 ml = __ldcg(reinterpret_cast<const float2*>(src_ml + (ix * p.r + j) * 2));
-                f = fast_exp2(ml.x - M);
-                Lsum = fmaf(f, ml.y, Lsum);
-            }
-            const int cnt = n - k0 < 32 ? n - k0 : 32;
-            for (int i0 = 0; i0 < cnt; i0 += 8) {
-                float4 ov[8];
-                float fi[8];
+        for (int k0 = 0; k0 < n; k0 += 16) {
+            float2 ml[16];
+            float4 ov[16];
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    fi[kk] = __shfl_sync(0xffffffffu, f, (i0 + kk) & 31);
-                    const long long ik = __shfl_sync(0xffffffffu, ix, (i0 + kk) & 31);
-                    ov[kk] = (i0 + kk < cnt && fi[kk] != 0.f)
-                                 ? __ldcg(reinterpret_cast<const float4*>(src_o + (ik * p.r + j) * D) + lane)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                    (void)stride4;
-                }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const float gk = (i0 + kk < cnt) ? fi[kk] : 0.f;
-                    acc.x = fmaf(gk, ov[kk].x, acc.x);
-                    acc.y = fmaf(gk, ov[kk].y, acc.y);
-                    acc.z = fmaf(gk, ov[kk].z, acc.z);
-                    acc.w = fmaf(gk, ov[kk].w, acc.w);
+            for (int kk = 0; kk < 16; ++kk) {
+                const long long ix = k0 + kk < n ? piece_index(cf + k0 + kk, seg, U, C) : -1;
+                if (ix >= 0) {
+                    ml[kk] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (ix * p.ns + sl) * 2));
+                    ov[kk] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (ix * p.ns + sl) * D) + lane);
+                } else {
+                    ml[kk] = make_float2(-INFINITY, 0.f);
+                    ov[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
-        }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
-        if (final_out) {
-            const float inv = 1.f / Lsum;
-            float4* o4 = reinterpret_cast<float4*>(p.out + (static_cast<long long>(b) * p.Hq + h * p.r + j) * D) + lane;
-            *o4 = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        } else {
-            if (lane == 0) *reinterpret_cast<float2*>(p.ws_gml + (dst * p.r + j) * 2) = make_float2(M, Lsum);
-            reinterpret_cast<float4*>(p.ws_go + (dst * p.r + j) * D)[lane] = acc;
+            for (int kk = 0; kk < 16; ++kk) {
+                const float f = fast_exp2(ml[kk].x - M);
+                L = fmaf(f, ml[kk].y, L);
+                acc.x = fmaf(f, ov[kk].x, acc.x);
+                acc.y = fmaf(f, ov[kk].y, acc.y);
+                acc.z = fmaf(f, ov[kk].z, acc.z);
+                acc.w = fmaf(f, ov[kk].w, acc.w);
+            }
         }
+        const float inv = 1.f / L;
+        const int hq = hg * p.ns + sl;
+        reinterpret_cast<float4*>(p.out + (static_cast<long long>(b) * p.Hq + hq) * D)[lane] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
+    if (threadIdx.x == 0) p.counters[seg] = 0;
 }
 
-// A warp that was last to count a partial merges what its counter stood for.  kind 1:
-// the <= 32 warps of a short segment -> output.  kind 2: one group of up to 32 warps of a
-// long segment -> level-2 partial; the group that is counted last at the segment level
-// then merges the group partials -> output.  Counters return to zero once used.
-template <int D>
-__device__ __noinline__ void merge_after_count(const KParams& p, int kind, int b, int h, int gi, long long U,
-                                               long long W, const int32_t* pre, int lane) {
-    const int np = pre[b + 1] - pre[b];
-    const long long seg = static_cast<long long>(b) * p.Hkv + h;
-    const long long a_unit = static_cast<long long>(p.Hkv) * pre[b] + static_cast<long long>(h) * np;
-    const long long wf = slice_of(a_unit, U, W);
-    const long long wl = slice_of(a_unit + np - 1, U, W);
-    const int n = static_cast<int>(wl - wf + 1);
-    const bool dense = U >= W;
-    auto slice_ix = [&](long long w) -> long long {
-        return (dense || slice_start(w, U, W) < slice_start(w + 1, U, W)) ? w + seg : -1;
-    };
-    __threadfence();  // the partials counted before this warp are visible
-    if (kind == 1) {
-        merge_partials<D>(p, p.ws_ml, p.ws_o, n, [&](int k) { return slice_ix(wf + k); }, true, 0, b, h, lane);
-        if (lane == 0) p.counters[seg] = 0;
-        return;
-    }
-    const long long gs = wf + 32LL * gi;
-    const int gn = static_cast<int>(wl - gs + 1 < 32 ? wl - gs + 1 : 32);
-    merge_partials<D>(p, p.ws_ml, p.ws_o, gn, [&](int k) { return slice_ix(gs + k); }, false, gs + seg, b, h,
-                      lane);
-    if (lane == 0) p.gcounters[gs + seg] = 0;
-    // count this group at the segment level; groups holding no non-empty slice never count
-    const int ng = (n + 31) / 32;
-    auto group_live = [&](int k) {
-        if (dense) return true;
-        const long long g0 = wf + 32LL * k, g1 = g0 + 31 < wl ? g0 + 31 : wl;
-        return slice_start(g0, U, W) < slice_start(g1 + 1, U, W);
-    };
-    int live = 0;
-    for (int k0 = 0; k0 < ng; k0 += 32) live += __popc(__ballot_sync(0xffffffffu, k0 + lane < ng && group_live(k0 + lane)));
-    __threadfence();
-    __syncwarp();
-    int arrived = 0;
-    if (lane == 0) arrived = atomicAdd(p.counters + seg, 1);
-    arrived = __shfl_sync(0xffffffffu, arrived, 0);
-    if (arrived >= live && lane == 0) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
-    if (arrived != live - 1) return;
-    __threadfence();
-    merge_partials<D>(p, p.ws_gml, p.ws_go, ng,
-                      [&](int k) { return group_live(k) ? wf + 32LL * k + seg : -1LL; }, true, 0, b, h, lane);
-    if (lane == 0) p.counters[seg] = 0;
+// Number of non-empty CTA slices among cf..cl (all of them when no slice is empty).
+__device__ __forceinline__ int pieces_between(long long cf, long long cl, long long U, long long C) {
+    if (U >= C) return static_cast<int>(cl - cf + 1);
+    int n = 0;
+    for (long long k = cf; k <= cl; ++k) n += slice_start(k, U, C) < slice_start(k + 1, U, C) ? 1 : 0;
+    return n;
 }
 
-// Resident CTAs the register budget is tuned for (3 gives up to 168 registers, enough
-// for the single-head-slot fragments without spilling).
-template <int GK, int HS>
-constexpr int min_ctas() { return HS == 1 ? 3 : 2; }
+// The chunks of one step: chunk X is chunk chk[X] of the unit buffer blk[X] and holds
+// sequence positions t0[X] .. t0[X] + 15; a chunk with !live[X] is masked out whole.
+template <int TG>
+struct Step {
+    const uint8_t* blk[TG];
+    int chk[TG];
+    int t0[TG];
+    bool live[TG];
+};
 
-template <int D, int GK, int GV, int HS>
-__global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitkv_kernel(KParams p) {
+// Resident CTAs per SM the register budget is tuned for (3 gives up to 168 registers).
+template <int HK, int HS>
+constexpr int min_ctas() { return 2; }
+
+template <int D, int GK, int GV, int HK, int HS>
+__global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitkv_kernel(KParams p) {
     static_assert(D == 128, "the fragment mapping below is written for head_dim 128");
+    static_assert(HK == 1 || HS == 1, "several kv heads per unit only with one query head each");
     constexpr int NGK = D / GK;               // K groups per row
     constexpr int NGV = D / GV;               // V groups per row
     constexpr int KW = D / 32;                // K code words per thread per token row
@@ -318,9 +251,10 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitk
     constexpr int VB = GV / 16;               // V code bytes per thread per group per row
     constexpr int MT = D / 16;                // output m-tiles
     constexpr int ROW = D / 2;                // bytes of one token's codes
+    constexpr int TG = HK == 1 ? 2 : 1;       // 16-token chunks per step
     static_assert(NGV * VB == MT, "m-tiles cover head_dim");
 
-    // let the combine pass launch now; it waits for this grid before reading anything
+    // a kernel launched behind this one may start its set-up; it waits for this grid
     asm volatile("griddepcontrol.launch_dependents;");
 
     extern __shared__ __align__(128) uint8_t smem[];
@@ -329,37 +263,35 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitk
     const int g = lane >> 2;   // fragment row group
     const int c = lane & 3;    // thread in group
     const int stages = p.stages;
-    const int bytes = p.block_bytes;
-    const size_t ring_bytes = static_cast<size_t>(kWarps) * stages * bytes;
-    uint8_t* ring = smem + static_cast<size_t>(warp) * stages * bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_bytes) + warp * stages;
-    WarpCtx* ctx_all = reinterpret_cast<WarpCtx*>(smem + ring_bytes + kWarps * stages * sizeof(uint64_t));
-    volatile WarpCtx* ctx = ctx_all + warp;
-    int32_t* pre = reinterpret_cast<int32_t*>(ctx_all + kWarps);
+    const int ubytes = p.unit_bytes;
+    const int bbytes = p.block_bytes;
+    const size_t ring_all = static_cast<size_t>(kWarps) * stages * ubytes;
+    uint8_t* ring = smem + static_cast<size_t>(warp) * stages * ubytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_all) + warp * stages;
+    CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + ring_all + kWarps * stages * sizeof(uint64_t));
+    int32_t* pre = reinterpret_cast<int32_t*>(ctl + 1);
 
     // every input may come from the kernel ahead of this one on the stream
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (warp == 0) page_prefix(p, pre, lane);
+    if (threadIdx.x == 0) ctl->pend_valid = 0;
     __syncthreads();
 
-    const long long U = static_cast<long long>(p.Hkv) * pre[p.B];
-    const long long W = static_cast<long long>(gridDim.x) * kWarps;
-    const long long wid = static_cast<long long>(blockIdx.x) * kWarps + warp;
-    const long long u0 = slice_start(wid, U, W);
-    const long long u1 = slice_start(wid + 1, U, W);
+    const long long U = static_cast<long long>(p.Hg) * pre[p.B];
+    const long long C = gridDim.x;
+    const long long cta = blockIdx.x;
     // sequences with no positions get zeros (no slice visits them)
-    for (long long bb = wid; bb < p.B; bb += W) {
+    for (long long bb = cta * kWarps + warp; bb < p.B; bb += C * kWarps) {
         if (pre[bb + 1] == pre[bb]) {
             float4* z4 = reinterpret_cast<float4*>(p.out + bb * p.Hq * D);
             for (int i = lane; i < p.Hq * D / 4; i += 32) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    if (u0 >= u1) return;
-    const int n_units = static_cast<int>(u1 - u0);
-    ctx->U = U;
-    ctx->W = W;
-    ctx->wid = wid;
-    ctx->pend_kind = 0;
+    const long long c0 = slice_start(cta, U, C);
+    const long long c1 = slice_start(cta + 1, U, C);
+    if (c0 >= c1) return;  // the whole CTA leaves together
+    const int span = static_cast<int>(c1 - c0);
+    const int nm = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;  // this warp's units
 
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t ring0 = smem_u32(ring);
@@ -369,104 +301,120 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitk
     }
     __syncwarp();
 
-    // ---- producer: lane l holds the block address of unit wbase + l; the next window's
-    // addresses are looked up one window ahead so their block-table loads overlap work ----
+    // ---- producer: lane l holds the block address of this warp's unit wbase + l; the next
+    // window's addresses are looked up one window ahead so their loads overlap work ----
+    auto unit_of = [&](int i) { return c0 + warp + static_cast<long long>(kWarps) * i; };
     int wbase = 0;
     unsigned long long waddr =
-        lane < n_units ? reinterpret_cast<unsigned long long>(unit_block(p, pre, u0 + lane)) : 0ull;
+        lane < nm ? reinterpret_cast<unsigned long long>(unit_block(p, pre, unit_of(lane), HK)) : 0ull;
     unsigned long long wnext =
-        32 + lane < n_units ? reinterpret_cast<unsigned long long>(unit_block(p, pre, u0 + 32 + lane)) : 0ull;
-    auto issue = [&](int i, int st) {  // unit u0 + i into stage st; i increases call by call
+        32 + lane < nm ? reinterpret_cast<unsigned long long>(unit_block(p, pre, unit_of(32 + lane), HK)) : 0ull;
+    int issued = 0;
+    auto issue = [&](int i, int st) {  // this warp's unit i into stage st; i increases call by call
         if (i - wbase >= 32) {
             wbase += 32;
             waddr = wnext;
-            wnext = wbase + 32 + lane < n_units
-                        ? reinterpret_cast<unsigned long long>(unit_block(p, pre, u0 + wbase + 32 + lane))
+            wnext = wbase + 32 + lane < nm
+                        ? reinterpret_cast<unsigned long long>(unit_block(p, pre, unit_of(wbase + 32 + lane), HK))
                         : 0ull;
         }
         const unsigned long long src = __shfl_sync(0xffffffffu, waddr, i - wbase);
         if (lane == 0) {
             const uint32_t bar = bar0 + 8 * st;
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(ring0 + st * bytes, reinterpret_cast<const void*>(src), bytes, bar);
+            mbar_arrive_expect_tx(bar, ubytes);
+            bulk_g2s(ring0 + st * ubytes, reinterpret_cast<const void*>(src), ubytes, bar);
         }
+        ++issued;
     };
-
-    // ---- consumer cursor ----
-    int b = find_seq(pre, p.B, p.Hkv, u0);
-    int np = pre[b + 1] - pre[b];
-    int h = static_cast<int>((u0 - static_cast<long long>(p.Hkv) * pre[b]) / np);
-    int pg = static_cast<int>(u0 - static_cast<long long>(p.Hkv) * pre[b] - static_cast<long long>(h) * np);
-    int Leff = 0;
-    bool seg_start = true;
-
-    const int pro = n_units < stages ? n_units : stages;
-    for (int k = 0; k < pro; ++k) issue(k, k);
+    {
+        const int pro = nm < stages ? nm : stages;
+        for (int k = 0; k < pro; ++k) issue(k, k);
+    }
 
     uint32_t qb[KSTEPS][NTQ][2];
     float m[HS], l[HS];
     float o[MT][HS][4];
+    int Leff = 0;
 
-    // per-thread byte offsets inside a page buffer (chunk 0)
+    // the kv head (within the unit) of this thread's score slot, and of its B-fragment
+    // column (HK > 1 only when every slot is its own kv head)
+    const int a_row = HK == 1 ? 0 : c;
+    const int a_col = HK == 1 ? 0 : (g >> 1);
+    // per-thread byte offsets inside a unit buffer (chunk 0)
     const int k_off = g * ROW + c * (D / 8);
-    const int ks_off = p.k_scales + g * NGK * 2;
-    const int vs_off = p.v_scales + g * NGV * 2;
+    const int ks_off = a_row * bbytes + p.k_scales + g * NGK * 2;
+    const int vs_off = a_row * bbytes + p.v_scales + g * NGV * 2;
     const int v_off = p.v_codes + c * ROW + g * VB;
     const int src0 = 4 * c + (g >> 1);
     const int src1 = 4 * (c + 4) + (g >> 1);
     const bool want_lo = (g & 1) != 0;
 
-    // Two 16-token chunks, X = 0 and X = 1, processed together: chunk X is chunk chk[X]
-    // of the page buffer blk[X] and holds sequence positions t0[X] .. t0[X] + 15.  With
-    // MASKED, positions at or past Leff (and all of chunk 1 when !liveB) are excluded;
-    // without it every position is valid.  The two score MMA chains are independent and
-    // interleave; the softmax reduction covers all 32 positions at once.
-    auto process_pair = [&](auto masked, const uint8_t* blkA, int chA, int t0A, const uint8_t* blkB, int chB,
-                            int t0B, bool liveB) {
+    // One step: TG 16-token chunks, chunk X being chunk chk[X] of the unit buffer blk[X]
+    // and holding sequence positions t0[X] .. t0[X] + 15, each over the HK kv heads of the
+    // unit.  With MASKED, positions at or past Leff (and all of chunk X when !live[X]) are
+    // excluded; without it every position is valid.
+    auto process = [&](auto masked, const Step<TG>& in) {
         constexpr bool MASKED = decltype(masked)::value;
-        const uint8_t* blk[2] = {blkA, blkB};
-        const int chk[2] = {chA, chB};
-        bool vg[2], vg8[2];
+        const uint8_t* const* blk = in.blk;
+        const int* chk = in.chk;
+        const int* t0 = in.t0;
+        const bool* live = in.live;
+        bool vg[TG], vg8[TG];
         if (MASKED) {
-            vg[0] = t0A + g < Leff;
-            vg8[0] = t0A + g + 8 < Leff;
-            vg[1] = liveB && t0B + g < Leff;
-            vg8[1] = liveB && t0B + g + 8 < Leff;
-        }
-
-        // -------- scores: S = K . Q (per k-group columns), one MMA chain per chunk --------
-        uint32_t kg[2][KW], kg8[2][KW];
 #pragma unroll
-        for (int X = 0; X < 2; ++X) {
-            const uint8_t* kb = blk[X] + chk[X] * 16 * ROW + k_off;
-            const uint4 x0 = *reinterpret_cast<const uint4*>(kb);
-            const uint4 x1 = *reinterpret_cast<const uint4*>(kb + 8 * ROW);
-            kg[X][0] = x0.x; kg[X][1] = x0.y; kg[X][2] = x0.z; kg[X][3] = x0.w;
-            kg8[X][0] = x1.x; kg8[X][1] = x1.y; kg8[X][2] = x1.z; kg8[X][3] = x1.w;
-        }
-        float acc[2][NTQ][4];
-#pragma unroll
-        for (int X = 0; X < 2; ++X)
-#pragma unroll
-            for (int t = 0; t < NTQ; ++t) acc[X][t][0] = acc[X][t][1] = acc[X][t][2] = acc[X][t][3] = 0.f;
-#pragma unroll
-        for (int wi = 0; wi < KW; ++wi) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-#pragma unroll
-                for (int X = 0; X < 2; ++X) {
-                    const uint32_t x = kg[X][wi] >> (8 * e);
-                    const uint32_t y = kg8[X][wi] >> (8 * e);
-                    const uint32_t a0 = unpack_lo(x), a1 = unpack_lo(y), a2 = unpack_hi(x), a3 = unpack_hi(y);
-#pragma unroll
-                    for (int t = 0; t < NTQ; ++t)
-                        mma_f16_16816(acc[X][t], a0, a1, a2, a3, qb[2 * wi + e][t][0], qb[2 * wi + e][t][1]);
-                }
+            for (int X = 0; X < TG; ++X) {
+                vg[X] = live[X] && t0[X] + g < Leff;
+                vg8[X] = live[X] && t0[X] + g + 8 < Leff;
             }
         }
-        float z[2][HS][2];
+
+        // -------- scores: S = K . Q (per k-group columns), one MMA chain per chunk and head --------
+        float acc[TG][HK][NTQ][4];
+        {
+            uint32_t kg[TG][HK][KW], kg8[TG][HK][KW];
 #pragma unroll
-        for (int X = 0; X < 2; ++X) {
+            for (int X = 0; X < TG; ++X)
+#pragma unroll
+                for (int a = 0; a < HK; ++a) {
+                    const uint8_t* kb = blk[X] + a * bbytes + chk[X] * 16 * ROW + k_off;
+                    const uint4 x0 = *reinterpret_cast<const uint4*>(kb);
+                    const uint4 x1 = *reinterpret_cast<const uint4*>(kb + 8 * ROW);
+                    kg[X][a][0] = x0.x; kg[X][a][1] = x0.y; kg[X][a][2] = x0.z; kg[X][a][3] = x0.w;
+                    kg8[X][a][0] = x1.x; kg8[X][a][1] = x1.y; kg8[X][a][2] = x1.z; kg8[X][a][3] = x1.w;
+#pragma unroll
+                    for (int t = 0; t < NTQ; ++t)
+                        acc[X][a][t][0] = acc[X][a][t][1] = acc[X][a][t][2] = acc[X][a][t][3] = 0.f;
+                }
+#pragma unroll
+            for (int wi = 0; wi < KW; ++wi)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                    for (int X = 0; X < TG; ++X)
+#pragma unroll
+                        for (int a = 0; a < HK; ++a) {
+                            const uint32_t x = kg[X][a][wi] >> (8 * e);
+                            const uint32_t y = kg8[X][a][wi] >> (8 * e);
+                            const uint32_t a0 = unpack_lo(x), a1 = unpack_lo(y), a2 = unpack_hi(x), a3 = unpack_hi(y);
+#pragma unroll
+                            for (int t = 0; t < NTQ; ++t)
+                                mma_f16_16816(acc[X][a][t], a0, a1, a2, a3, qb[2 * wi + e][t][0], qb[2 * wi + e][t][1]);
+                        }
+        }
+        float z[TG][HS][2];
+#pragma unroll
+        for (int X = 0; X < TG; ++X) {
+            // this thread's slot lives in the accumulator of kv head a_row
+            float sacc[NTQ][4];
+#pragma unroll
+            for (int t = 0; t < NTQ; ++t)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float v = acc[X][0][t][k];
+#pragma unroll
+                    for (int a = 1; a < HK; ++a) v = a_row == a ? acc[X][a][t][k] : v;
+                    sacc[t][k] = v;
+                }
             const __half* s0 = reinterpret_cast<const __half*>(blk[X] + chk[X] * 16 * NGK * 2 + ks_off);
             const __half* s1 = s0 + 8 * NGK;
             float skg[NGK], skg8[NGK];
@@ -481,8 +429,8 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitk
 #pragma unroll
                 for (int R = 0; R < NGK; ++R) {
                     const int pi = s * NGK + R;
-                    z0 = fmaf(skg[R], acc[X][pi >> 1][pi & 1], z0);
-                    z1 = fmaf(skg8[R], acc[X][pi >> 1][2 + (pi & 1)], z1);
+                    z0 = fmaf(skg[R], sacc[pi >> 1][pi & 1], z0);
+                    z1 = fmaf(skg8[R], sacc[pi >> 1][2 + (pi & 1)], z1);
                 }
                 z[X][s][0] = z0 * p.scale_log2;
                 z[X][s][1] = z1 * p.scale_log2;
@@ -493,12 +441,14 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitk
             }
         }
 
-        // -------- online softmax over the 32 positions (per head, lanes with the same c) --------
+        // -------- online softmax over the step's positions (per slot, lanes with the same c) --------
         float mn[HS];
         bool grow = false;
 #pragma unroll
         for (int s = 0; s < HS; ++s) {
-            float cm = fmaxf(fmaxf(z[0][s][0], z[0][s][1]), fmaxf(z[1][s][0], z[1][s][1]));
+            float cm = fmaxf(z[0][s][0], z[0][s][1]);
+#pragma unroll
+            for (int X = 1; X < TG; ++X) cm = fmaxf(cm, fmaxf(z[X][s][0], z[X][s][1]));
             cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
             cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
             cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
@@ -516,12 +466,12 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitk
                     for (int e = 0; e < 4; ++e) o[mt][s][e] *= alpha;
             }
         }
-        float pr[2][HS][2];
+        float pr[TG][HS][2];
 #pragma unroll
         for (int s = 0; s < HS; ++s) {
             m[s] = mn[s];
 #pragma unroll
-            for (int X = 0; X < 2; ++X) {
+            for (int X = 0; X < TG; ++X) {
                 pr[X][s][0] = fast_exp2(z[X][s][0] - mn[s]);
                 pr[X][s][1] = fast_exp2(z[X][s][1] - mn[s]);
                 l[s] += pr[X][s][0] + pr[X][s][1];
@@ -529,9 +479,9 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitk
         }
 
         // -------- weights W = p * v_scale as f16 hi + lo, moved into B fragments --------
-        uint32_t bv[2][HS][NGV][2];
+        uint32_t bv[TG][HS][NGV][2];
 #pragma unroll
-        for (int X = 0; X < 2; ++X) {
+        for (int X = 0; X < TG; ++X) {
             const __half* s0 = reinterpret_cast<const __half*>(blk[X] + chk[X] * 16 * NGV * 2 + vs_off);
             const __half* s1 = s0 + 8 * NGV;
             float svg[NGV], svg8[NGV];
@@ -563,161 +513,102 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitk
             }
         }
 
-        // -------- output: O^T += V^T . W, both chunks --------
+        // -------- output: O^T += V^T . W, every chunk and kv head --------
 #pragma unroll
-        for (int R = 0; R < NGV; ++R) {
-            uint32_t va[2][(VB + 3) / 4], vb[2][(VB + 3) / 4], vc[2][(VB + 3) / 4], vd[2][(VB + 3) / 4];
+        for (int X = 0; X < TG; ++X)
 #pragma unroll
-            for (int X = 0; X < 2; ++X) {
-                const uint8_t* vcodes = blk[X] + chk[X] * 16 * ROW + v_off + R * (GV / 2);
-                if constexpr (VB == 8) {
-                    const uint2 ta = *reinterpret_cast<const uint2*>(vcodes);
-                    const uint2 tb = *reinterpret_cast<const uint2*>(vcodes + 8 * ROW);
-                    const uint2 tc = *reinterpret_cast<const uint2*>(vcodes + 4 * ROW);
-                    const uint2 td = *reinterpret_cast<const uint2*>(vcodes + 12 * ROW);
-                    va[X][0] = ta.x; va[X][1] = ta.y; vb[X][0] = tb.x; vb[X][1] = tb.y;
-                    vc[X][0] = tc.x; vc[X][1] = tc.y; vd[X][0] = td.x; vd[X][1] = td.y;
-                } else if constexpr (VB == 4) {
-                    va[X][0] = *reinterpret_cast<const uint32_t*>(vcodes);
-                    vb[X][0] = *reinterpret_cast<const uint32_t*>(vcodes + 8 * ROW);
-                    vc[X][0] = *reinterpret_cast<const uint32_t*>(vcodes + 4 * ROW);
-                    vd[X][0] = *reinterpret_cast<const uint32_t*>(vcodes + 12 * ROW);
-                } else {
-                    va[X][0] = *reinterpret_cast<const uint16_t*>(vcodes);
-                    vb[X][0] = *reinterpret_cast<const uint16_t*>(vcodes + 8 * ROW);
-                    vc[X][0] = *reinterpret_cast<const uint16_t*>(vcodes + 4 * ROW);
-                    vd[X][0] = *reinterpret_cast<const uint16_t*>(vcodes + 12 * ROW);
-                }
-            }
+            for (int a = 0; a < HK; ++a)
 #pragma unroll
-            for (int jb = 0; jb < VB; jb += 2) {
-                const int wi = jb / 4;
-                const uint32_t bb = static_cast<uint32_t>(jb % 4);
-                const uint32_t sel = bb | ((bb + 1) << 4) | ((bb + 4) << 8) | ((bb + 5) << 12);
-                const int mt0 = R * VB + jb;
+                for (int R = 0; R < NGV; ++R) {
+                    // B fragment of kv head a: the columns of other heads' slots are zero
+                    uint32_t b0[HS], b1[HS];
 #pragma unroll
-                for (int X = 0; X < 2; ++X) {
-                    const uint32_t yac = prmt(va[X][wi], vb[X][wi], sel);  // tokens c, c+8
-                    const uint32_t ybd = prmt(vc[X][wi], vd[X][wi], sel);  // tokens c+4, c+12
-                    {
-                        const uint32_t a0 = unpack_lo(yac), a1 = unpack_hi(yac);
-                        const uint32_t a2 = unpack_lo(ybd), a3 = unpack_hi(ybd);
-#pragma unroll
-                        for (int s = 0; s < HS; ++s)
-                            mma_f16_16816(o[mt0][s], a0, a1, a2, a3, bv[X][s][R][0], bv[X][s][R][1]);
+                    for (int s = 0; s < HS; ++s) {
+                        b0[s] = (HK == 1 || a_col == a) ? bv[X][s][R][0] : 0u;
+                        b1[s] = (HK == 1 || a_col == a) ? bv[X][s][R][1] : 0u;
                     }
-                    {
-                        const uint32_t y1 = yac >> 8, y2 = ybd >> 8;
-                        const uint32_t a0 = unpack_lo(y1), a1 = unpack_hi(y1);
-                        const uint32_t a2 = unpack_lo(y2), a3 = unpack_hi(y2);
-#pragma unroll
-                        for (int s = 0; s < HS; ++s)
-                            mma_f16_16816(o[mt0 + 1][s], a0, a1, a2, a3, bv[X][s][R][0], bv[X][s][R][1]);
+                    uint32_t va[(VB + 3) / 4], vb[(VB + 3) / 4], vc[(VB + 3) / 4], vd[(VB + 3) / 4];
+                    const uint8_t* vcodes = blk[X] + a * bbytes + chk[X] * 16 * ROW + v_off + R * (GV / 2);
+                    if constexpr (VB == 8) {
+                        const uint2 ta = *reinterpret_cast<const uint2*>(vcodes);
+                        const uint2 tb = *reinterpret_cast<const uint2*>(vcodes + 8 * ROW);
+                        const uint2 tc = *reinterpret_cast<const uint2*>(vcodes + 4 * ROW);
+                        const uint2 td = *reinterpret_cast<const uint2*>(vcodes + 12 * ROW);
+                        va[0] = ta.x; va[1] = ta.y; vb[0] = tb.x; vb[1] = tb.y;
+                        vc[0] = tc.x; vc[1] = tc.y; vd[0] = td.x; vd[1] = td.y;
+                    } else if constexpr (VB == 4) {
+                        va[0] = *reinterpret_cast<const uint32_t*>(vcodes);
+                        vb[0] = *reinterpret_cast<const uint32_t*>(vcodes + 8 * ROW);
+                        vc[0] = *reinterpret_cast<const uint32_t*>(vcodes + 4 * ROW);
+                        vd[0] = *reinterpret_cast<const uint32_t*>(vcodes + 12 * ROW);
+                    } else {
+                        va[0] = *reinterpret_cast<const uint16_t*>(vcodes);
+                        vb[0] = *reinterpret_cast<const uint16_t*>(vcodes + 8 * ROW);
+                        vc[0] = *reinterpret_cast<const uint16_t*>(vcodes + 4 * ROW);
+                        vd[0] = *reinterpret_cast<const uint16_t*>(vcodes + 12 * ROW);
                     }
-                }
-            }
-        }
-    };
-
-    // Counting a partial is deferred: the atomic add is issued at the end of a segment and
-    // its result looked at when the next segment ends (or the slice does), so the round
-    // trip overlaps streaming.  pend_kind 0 = nothing pending.
-    int pend_arrived = 0;
-    auto resolve = [&]() {
-        const int kind = ctx->pend_kind;
-        if (kind == 0) return;
-        const int arrived = __shfl_sync(0xffffffffu, pend_arrived, 0);
-        const int target = ctx->pend_target;
-        if (arrived >= target && lane == 0) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
-        if (arrived == target - 1)
-            merge_after_count<D>(p, kind, ctx->pend_b, ctx->pend_h, ctx->pend_gi, ctx->U, ctx->W, pre, lane);
-        __syncwarp();
-        ctx->pend_kind = 0;
-    };
-
-    // End of this warp's part of segment (b, h): write it, or hand over a partial.
-    auto flush = [&]() {
-        const SegEnd e = segment_end(pre, b, h, p.Hkv, ctx->U, ctx->W, ctx->wid, lane);
-        const long long seg = static_cast<long long>(b) * p.Hkv + h;
-        float lt[HS];
 #pragma unroll
-        for (int s = 0; s < HS; ++s) {
-            lt[s] = l[s];
-            lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 4);
-            lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 8);
-            lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 16);
-        }
-        if (e.alone) {
-            // the whole segment is in this warp's registers: normalise and write
+                    for (int jb = 0; jb < VB; jb += 2) {
+                        const int wi = jb / 4;
+                        const uint32_t bb = static_cast<uint32_t>(jb % 4);
+                        const uint32_t sel = bb | ((bb + 1) << 4) | ((bb + 4) << 8) | ((bb + 5) << 12);
+                        const int mt0 = R * VB + jb;
+                        const uint32_t yac = prmt(va[wi], vb[wi], sel);  // tokens c, c+8
+                        const uint32_t ybd = prmt(vc[wi], vd[wi], sel);  // tokens c+4, c+12
+                        {
+                            const uint32_t a0 = unpack_lo(yac), a1 = unpack_hi(yac);
+                            const uint32_t a2 = unpack_lo(ybd), a3 = unpack_hi(ybd);
 #pragma unroll
-            for (int s = 0; s < HS; ++s) {
-                const int j = c + 4 * s;
-                if (j < p.r) {
-                    const float inv = 1.f / lt[s];
-                    float* od = p.out + (static_cast<long long>(b) * p.Hq + h * p.r + j) * D;
-#pragma unroll
-                    for (int R = 0; R < NGV; ++R)
-#pragma unroll
-                        for (int jb = 0; jb < VB; ++jb) {
-                            const int mt = R * VB + jb;
-                            const int dd = 2 * (R * (GV / 2) + g * VB + jb);
-                            *reinterpret_cast<float2*>(od + dd) = make_float2((o[mt][s][0] + o[mt][s][1]) * inv,
-                                                                             (o[mt][s][2] + o[mt][s][3]) * inv);
+                            for (int s = 0; s < HS; ++s) mma_f16_16816(o[mt0][s], a0, a1, a2, a3, b0[s], b1[s]);
                         }
-                }
-            }
-            return;
-        }
-        const long long piece = ctx->wid + seg;
+                        {
+                            const uint32_t y1 = yac >> 8, y2 = ybd >> 8;
+                            const uint32_t a0 = unpack_lo(y1), a1 = unpack_hi(y1);
+                            const uint32_t a2 = unpack_lo(y2), a3 = unpack_hi(y2);
 #pragma unroll
-        for (int s = 0; s < HS; ++s) {
-            const int j = c + 4 * s;
-            if (j < p.r) {
-                if (g == 0) *reinterpret_cast<float2*>(p.ws_ml + (piece * p.r + j) * 2) = make_float2(m[s], lt[s]);
-                float* od = p.ws_o + (piece * p.r + j) * D;
-#pragma unroll
-                for (int R = 0; R < NGV; ++R)
-#pragma unroll
-                    for (int jb = 0; jb < VB; ++jb) {
-                        const int mt = R * VB + jb;
-                        const int dd = 2 * (R * (GV / 2) + g * VB + jb);
-                        *reinterpret_cast<float2*>(od + dd) =
-                            make_float2(o[mt][s][0] + o[mt][s][1], o[mt][s][2] + o[mt][s][3]);
+                            for (int s = 0; s < HS; ++s) mma_f16_16816(o[mt0 + 1][s], a0, a1, a2, a3, b0[s], b1[s]);
+                        }
                     }
-            }
-        }
-        resolve();  // the previous segment's count has had time to come back
-        __threadfence();  // publish this partial before counting it
-        __syncwarp();
-        if (lane == 0) {
-            pend_arrived = atomicAdd((e.kind == 2 ? p.gcounters : p.counters) + e.cidx, 1);
-            ctx->pend_kind = e.kind;
-            ctx->pend_b = b;
-            ctx->pend_h = h;
-            ctx->pend_gi = e.gi;
-            ctx->pend_target = e.target;
-        }
-        __syncwarp();
+                }
     };
 
+    // ---- walk the segments this CTA's slice touches ----
+    int b = find_seq(pre, p.B, p.Hg, c0);
+    int np = pre[b + 1] - pre[b];
+    int hg = static_cast<int>((c0 - static_cast<long long>(p.Hg) * pre[b]) / np);
+    long long sfirst = static_cast<long long>(p.Hg) * pre[b] + static_cast<long long>(hg) * np;
+    int consumed = 0;     // this warp's units taken out of the ring
     int cst = 0;          // stage of the next unit to consume
     uint32_t cpar = 0;    // its phase parity
+    bool failed = false;  // a copy did not arrive in time: stop waiting, keep the barriers
+    int f_st = 0, f_out = 0;  // where consumption stopped, and the copies still in flight then
+    uint32_t f_par = 0;
+    int pend_arrived = 0; // thread 0: what the last counting atomic returned
     const bool p16 = p.P == 16;
 
-    for (int i = 0; i < n_units;) {
-        if (seg_start) {
-            // new (sequence, kv head): q fragments and a fresh softmax state
+    while (sfirst < c1) {
+        const long long ua = sfirst > c0 ? sfirst : c0;
+        const long long ue = sfirst + np < c1 ? sfirst + np : c1;
+        const long long fu = ua + (((c0 + warp - ua) % kWarps) + kWarps) % kWarps;  // my first unit here
+        const int cnt = fu < ue ? static_cast<int>((ue - fu + kWarps - 1) / kWarps) : 0;
+        const int pg0 = static_cast<int>(fu - sfirst);
+        int last_st = -1;   // stage of the last unit consumed in this segment
+        int held[2] = {-1, -1}, held_i[2] = {0, 0};  // stages whose refill waits for the merge
+
+        if (cnt > 0) {
+            // new (sequence, head group): q fragments and a fresh softmax state
             int L = p.seq_lens[b];
             L = L < 0 ? 0 : L;
             Leff = min(L, p.max_blocks * p.P);
+            const int hq0 = hg * p.ns;
 #pragma unroll
             for (int t = 0; t < NTQ; ++t) {
                 const int pi = 2 * t + (g & 1);
                 const int sigma = pi / NGK;
                 const int R = pi % NGK;
                 const int j = (g >> 1) + 4 * sigma;
-                const bool colv = sigma < HS && j < p.r;
-                const __half* qrow = p.q + (static_cast<long long>(b) * p.Hq + h * p.r + (colv ? j : 0)) * D;
+                const bool colv = sigma < HS && j < p.ns;
+                const __half* qrow = p.q + (static_cast<long long>(b) * p.Hq + hq0 + (colv ? j : 0)) * D;
 #pragma unroll
                 for (int wi = 0; wi < KW; ++wi) {
                     const int dbase = c * (D / 4) + 8 * wi;
@@ -729,104 +620,256 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<GK, HS>()) decode_splitk
                     qb[2 * wi + 1][t][1] = prmt(w4.y, w4.w, 0x7632u);
                 }
             }
+        }
 #pragma unroll
-            for (int s = 0; s < HS; ++s) {
-                m[s] = -INFINITY;
-                l[s] = 0.f;
+        for (int s = 0; s < HS; ++s) {
+            m[s] = -INFINITY;
+            l[s] = 0.f;
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[mt][s][e] = 0.f;
-            }
-            seg_start = false;
+                for (int e = 0; e < 4; ++e) o[mt][s][e] = 0.f;
         }
 
-        // 16-token pages: two pages of the same segment per iteration when there are two;
-        // larger pages: one page, its chunks two at a time.
-        const int n = (p16 && i + 1 < n_units && pg + 1 < np) ? 2 : 1;
-        int st1 = cst;
-        uint32_t par1 = cpar;
-        bool ok = mbar_wait(bar0 + 8 * cst, cpar, kWaitLimitNs);
-        if (n == 2) {
-            if (++st1 == stages) {
+        for (int j = 0; j < cnt;) {
+            // HK = 1 with 16-token pages: two units per step when there are two
+            const int n = (HK == 1 && p16 && j + 1 < cnt) ? 2 : 1;
+            int st1 = cst;
+            uint32_t par1 = cpar;
+            if (n == 2 && ++st1 == stages) {
                 st1 = 0;
                 par1 ^= 1u;
             }
-            ok = ok && mbar_wait(bar0 + 8 * st1, par1, kWaitLimitNs);
-        }
-        if (!__all_sync(0xffffffffu, ok)) {
-            // give up on this slice: flag it, then let the copies already issued land
-            if (lane == 0) raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
-            const int pending = n_units - i < stages ? n_units - i : stages;
-            int st = cst;
-            uint32_t par = cpar;
-            for (int k = 0; k < pending; ++k) {
-                mbar_wait(bar0 + 8 * st, par, kWaitLimitNs);
-                if (++st == stages) {
-                    st = 0;
-                    par ^= 1u;
+            if (!failed) {
+                bool ok = mbar_wait(bar0 + 8 * cst, cpar, kWaitLimitNs);
+                if (n == 2) ok = ok && mbar_wait(bar0 + 8 * st1, par1, kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    if (lane == 0) raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
+                    failed = true;
+                    f_st = cst;
+                    f_par = cpar;
+                    f_out = issued - consumed;
                 }
             }
-            return;
-        }
-        const uint8_t* blkA = ring + cst * bytes;
-        const uint8_t* blkB = ring + st1 * bytes;
-        if (p16) {
-            const int t0 = pg * 16;
-            if (n == 2 && t0 + 32 <= Leff)
-                process_pair(std::false_type{}, blkA, 0, t0, blkB, 0, t0 + 16, true);
-            else
-                process_pair(std::true_type{}, blkA, 0, t0, blkB, 0, t0 + 16, n == 2);
-        } else {
-            for (int chunk = 0; chunk < p.P / 16; chunk += 2) {
-                const int t0 = pg * p.P + chunk * 16;
-                if (t0 >= Leff) break;
-                if (t0 + 32 <= Leff)
-                    process_pair(std::false_type{}, blkA, chunk, t0, blkA, chunk + 1, t0 + 16, true);
-                else
-                    process_pair(std::true_type{}, blkA, chunk, t0, blkA, chunk + 1, t0 + 16, true);
+            if (!failed) {
+                const uint8_t* blkA = ring + cst * ubytes;
+                const uint8_t* blkB = ring + st1 * ubytes;
+                const int pg = pg0 + kWarps * j;
+                if constexpr (HK == 1) {
+                    if (p16) {
+                        const int t0A = pg * 16, t0B = (pg + kWarps) * 16;
+                        const Step<TG> st = {{blkA, blkB}, {0, 0}, {t0A, t0B}, {true, n == 2}};
+                        if (n == 2 && t0B + 16 <= Leff) process(std::false_type{}, st);
+                        else process(std::true_type{}, st);
+                    } else {
+                        for (int chunk = 0; chunk < p.P / 16; chunk += 2) {
+                            const int t0 = pg * p.P + chunk * 16;
+                            if (t0 >= Leff) break;
+                            // an odd last chunk pairs with a re-read of itself, masked out
+                            const bool two = chunk + 1 < p.P / 16;
+                            const Step<TG> st = {{blkA, blkA}, {chunk, two ? chunk + 1 : chunk}, {t0, t0 + 16}, {true, two}};
+                            if (two && t0 + 32 <= Leff) process(std::false_type{}, st);
+                            else process(std::true_type{}, st);
+                        }
+                    }
+                } else {
+                    for (int chunk = 0; chunk < p.P / 16; ++chunk) {
+                        const int t0 = pg * p.P + chunk * 16;
+                        if (t0 >= Leff) break;
+                        const Step<TG> st = {{blkA}, {chunk}, {t0}, {true}};
+                        if (t0 + 16 <= Leff) process(std::false_type{}, st);
+                        else process(std::true_type{}, st);
+                    }
+                }
             }
+
+            // ---- release the stages and refill them with the units `stages` ahead; the
+            // segment's last stage(s) are refilled after the merge below ----
+            const bool last = j + n == cnt;
+            last_st = n == 2 ? st1 : cst;
+            if (!failed) {
+                __syncwarp();
+                if (lane == 0) fence_proxy_async_smem();
+                if (!last) {
+                    if (consumed + stages < nm) issue(consumed + stages, cst);
+                    if (n == 2 && consumed + 1 + stages < nm) issue(consumed + 1 + stages, st1);
+                } else {
+                    held[0] = cst;
+                    held_i[0] = consumed + stages;
+                    if (n == 2) {
+                        held[1] = st1;
+                        held_i[1] = consumed + 1 + stages;
+                    }
+                }
+            }
+            consumed += n;
+            cst = st1;
+            cpar = par1;
+            if (++cst == stages) {
+                cst = 0;
+                cpar ^= 1u;
+            }
+            j += n;
         }
 
-        // ---- release the stages and refill them with the pages `stages` units ahead ----
-        __syncwarp();
-        if (lane == 0) fence_proxy_async_smem();
-        if (i + stages < n_units) issue(i + stages, cst);
-        if (n == 2 && i + 1 + stages < n_units) issue(i + 1 + stages, st1);
-        cst = st1;
-        cpar = par1;
-        if (++cst == stages) {
-            cst = 0;
-            cpar ^= 1u;
+        // ---- segment end: the four warps merge their parts in shared memory ----
+        const long long seg = static_cast<long long>(b) * p.Hg + hg;
+        const long long cf = slice_of(sfirst, U, C);
+        const long long cl = slice_of(sfirst + np - 1, U, C);
+        const bool whole = cf == cl;
+        const bool mine = cnt > 0 && !failed;
+        float lt[HS];
+#pragma unroll
+        for (int s = 0; s < HS; ++s) {
+            lt[s] = l[s];
+            lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 4);
+            lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 8);
+            lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 16);
         }
-        i += n;
-
-        // ---- end of a segment or of this warp's slice ----
-        pg += n;
-        const bool seg_end = (pg == np);
-        if (seg_end || i == n_units) flush();
-        if (seg_end) {
-            pg = 0;
-            if (++h == p.Hkv) {
-                h = 0;
-                do {
-                    ++b;
-                } while (b < p.B && pre[b + 1] == pre[b]);
+        if (lane == 0) ctl->buf[warp] = mine ? last_st : -1;
+        if (threadIdx.x == 0 && ctl->pend_valid) ctl->pend_arrived = pend_arrived;
+        float* mybuf = reinterpret_cast<float*>(ring + (mine ? last_st : 0) * ubytes);
+        bool pend_seen = false;
+#pragma unroll
+        for (int s = 0; s < HS; ++s) {
+            if (mine) {
+                // o (hi + lo columns summed) of slot c + 4s as [4][D], then (max, sum) pairs
+#pragma unroll
+                for (int R = 0; R < NGV; ++R)
+#pragma unroll
+                    for (int jb = 0; jb < VB; ++jb) {
+                        const int mt = R * VB + jb;
+                        const int dd = 2 * (R * (GV / 2) + g * VB + jb);
+                        *reinterpret_cast<float2*>(mybuf + c * D + dd) =
+                            make_float2(o[mt][s][0] + o[mt][s][1], o[mt][s][2] + o[mt][s][3]);
+                    }
+                if (g == 0) *reinterpret_cast<float2*>(mybuf + 4 * D + 2 * c) = make_float2(m[s], lt[s]);
+                fence_proxy_async_smem();  // the stage is refilled by the bulk copy engine later
             }
-            if (b < p.B) np = pre[b + 1] - pre[b];
-            seg_start = true;
+            __syncthreads();
+            // the pending record is only rewritten after this segment end's last barrier
+            if (s == 0) pend_seen = ctl->pend_valid != 0;
+            const int sl = warp + 4 * s;
+            if (sl < p.ns) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const int bs = ctl->buf[w];
+                    if (bs >= 0) {
+                        const float* wb = reinterpret_cast<const float*>(smem + (static_cast<size_t>(w) * stages + bs) * ubytes);
+                        M = fmaxf(M, wb[4 * D + 2 * warp]);
+                    }
+                }
+                float Ls = 0.f;
+                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const int bs = ctl->buf[w];
+                    if (bs >= 0) {
+                        const float* wb = reinterpret_cast<const float*>(smem + (static_cast<size_t>(w) * stages + bs) * ubytes);
+                        const float2 ml = *reinterpret_cast<const float2*>(wb + 4 * D + 2 * warp);
+                        const float4 ov = *reinterpret_cast<const float4*>(wb + warp * D + 4 * lane);
+                        const float f = fast_exp2(ml.x - M);
+                        Ls = fmaf(f, ml.y, Ls);
+                        O.x = fmaf(f, ov.x, O.x);
+                        O.y = fmaf(f, ov.y, O.y);
+                        O.z = fmaf(f, ov.z, O.z);
+                        O.w = fmaf(f, ov.w, O.w);
+                    }
+                }
+                const int hq = hg * p.ns + sl;
+                if (whole) {
+                    const float inv = 1.f / Ls;
+                    reinterpret_cast<float4*>(p.out + (static_cast<long long>(b) * p.Hq + hq) * D)[lane] =
+                        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+                } else {
+                    const long long piece = cta + seg;
+                    if (lane == 0) *reinterpret_cast<float2*>(p.ws_ml + (piece * p.ns + sl) * 2) = make_float2(M, Ls);
+                    reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + sl) * D)[lane] = O;
+                    __threadfence();  // publish the partial before it is counted
+                }
+            }
+            __syncthreads();
+        }
+        // the stages held for the merge can be refilled now
+        if (mine) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                if (held[k] >= 0 && held_i[k] < nm) issue(held_i[k], held[k]);
+        }
+
+        // ---- the previous count has had time to come back: merge if this CTA was last ----
+        if (pend_seen) {
+            const int arrived = ctl->pend_arrived;
+            const int target = ctl->pend_target;
+            if (arrived >= target && threadIdx.x == 0) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
+            if (arrived == target - 1) {
+                const int pb = ctl->pend_b, ph = ctl->pend_hg;
+                const int pnp = pre[pb + 1] - pre[pb];
+                const long long pf = static_cast<long long>(p.Hg) * pre[pb] + static_cast<long long>(ph) * pnp;
+                merge_segment<D>(p, pb, ph, slice_of(pf, U, C), slice_of(pf + pnp - 1, U, C), U, C);
+            }
+            __syncthreads();  // everyone has read the pending record
+            if (threadIdx.x == 0) ctl->pend_valid = 0;
+        }
+        // ---- count this CTA's partial; the result is looked at later ----
+        if (!whole && threadIdx.x == 0) {
+            pend_arrived = atomicAdd(p.counters + seg, 1);
+            ctl->pend_valid = 1;
+            ctl->pend_b = b;
+            ctl->pend_hg = hg;
+            ctl->pend_target = pieces_between(cf, cl, U, C);
+        }
+
+        // ---- next segment ----
+        sfirst += np;
+        if (++hg == p.Hg) {
+            hg = 0;
+            do {
+                ++b;
+            } while (b < p.B && pre[b + 1] == pre[b]);
+        }
+        if (b < p.B) np = pre[b + 1] - pre[b];
+        else break;
+    }
+
+    // ---- the last count ----
+    __syncthreads();
+    if (threadIdx.x == 0 && ctl->pend_valid) ctl->pend_arrived = pend_arrived;
+    __syncthreads();
+    if (ctl->pend_valid) {
+        const int arrived = ctl->pend_arrived;
+        const int target = ctl->pend_target;
+        if (arrived >= target && threadIdx.x == 0) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
+        if (arrived == target - 1) {
+            const int pb = ctl->pend_b, ph = ctl->pend_hg;
+            const int pnp = pre[pb + 1] - pre[pb];
+            const long long pf = static_cast<long long>(p.Hg) * pre[pb] + static_cast<long long>(ph) * pnp;
+            merge_segment<D>(p, pb, ph, slice_of(pf, U, C), slice_of(pf + pnp - 1, U, C), U, C);
         }
     }
-    resolve();
+
+    // ---- after a failed wait: let the copies already issued land before leaving ----
+    if (failed) {
+        int st = f_st;
+        uint32_t par = f_par;
+        for (int k = 0; k < f_out; ++k) {
+            mbar_wait(bar0 + 8 * st, par, kWaitLimitNs);
+            if (++st == stages) {
+                st = 0;
+                par ^= 1u;
+            }
+        }
+    }
 }
 
 // Raise the kernel's dynamic shared-memory limit once to the largest size asked for,
 // so repeated calls (and calls under stream capture) only launch.
-template <int D, int GK, int GV, int HS>
+template <int D, int GK, int GV, int HK, int HS>
 cudaError_t ensure_smem_attr(size_t smem) {
     static std::atomic<long long> granted{-1};
     if (static_cast<long long>(smem) <= granted.load(std::memory_order_acquire)) return cudaSuccess;
-    const cudaError_t err = cudaFuncSetAttribute(decode_splitkv_kernel<D, GK, GV, HS>,
+    const cudaError_t err = cudaFuncSetAttribute(decode_splitkv_kernel<D, GK, GV, HK, HS>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) cudaGetLastError();  // a refused size must not linger as the last error
     if (err == cudaSuccess) {
@@ -839,7 +882,7 @@ cudaError_t ensure_smem_attr(size_t smem) {
 
 // Resident CTAs per SM for a given shared-memory size, memoised per size (a few sizes
 // per shape are asked for; the slots fill once and later calls only read them).
-template <int D, int GK, int GV, int HS>
+template <int D, int GK, int GV, int HK, int HS>
 int occupancy(size_t smem) {
     constexpr int kSlots = 32;
     static std::atomic<long long> memo[kSlots];  // (smem << 8) | ctas, 0 = empty
@@ -848,10 +891,10 @@ int occupancy(size_t smem) {
         if (m == 0) break;
         if ((m >> 8) == static_cast<long long>(smem)) return static_cast<int>(m & 0xff);
     }
-    if (ensure_smem_attr<D, GK, GV, HS>(smem) != cudaSuccess) return 0;
+    if (ensure_smem_attr<D, GK, GV, HK, HS>(smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HS>, kWarps * 32, smem) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HK, HS>, kWarps * 32,
+                                                      smem) != cudaSuccess)
         return 0;
     const long long entry = (static_cast<long long>(smem) << 8) | (n & 0xff);
     for (int i = 0; i < kSlots; ++i) {
@@ -861,7 +904,7 @@ int occupancy(size_t smem) {
     return n;
 }
 
-template <int D, int GK, int GV, int HS>
+template <int D, int GK, int GV, int HK, int HS>
 cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     KParams p;
     p.pool = a.pool;
@@ -871,25 +914,25 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     p.out = a.out;
     p.ws_ml = reinterpret_cast<float*>(a.workspace + plan.ws_ml_offset);
     p.ws_o = reinterpret_cast<float*>(a.workspace + plan.ws_o_offset);
-    p.ws_gml = reinterpret_cast<float*>(a.workspace + plan.ws_gml_offset);
-    p.ws_go = reinterpret_cast<float*>(a.workspace + plan.ws_go_offset);
     p.counters = reinterpret_cast<int32_t*>(a.workspace + plan.ws_cnt_offset);
-    p.gcounters = reinterpret_cast<int32_t*>(a.workspace + plan.ws_gcnt_offset);
     p.status = reinterpret_cast<uint32_t*>(a.workspace);
     p.B = a.B;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
+    p.Hg = a.Hkv / HK;
     p.r = a.Hq / a.Hkv;
+    p.ns = HK * p.r;
     p.P = a.L.P;
     p.num_pages = a.num_pages;
     p.max_blocks = a.max_blocks;
     p.block_bytes = a.L.bytes;
+    p.unit_bytes = a.L.bytes * HK;
     p.stages = plan.stages;
     p.v_codes = a.L.v_codes;
     p.k_scales = a.L.k_scales;
     p.v_scales = a.L.v_scales;
     p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
-    cudaError_t err = ensure_smem_attr<D, GK, GV, HS>(plan.smem_bytes);
+    cudaError_t err = ensure_smem_attr<D, GK, GV, HK, HS>(plan.smem_bytes);
     if (err != cudaSuccess) return err;
     // The launch may start before the kernel ahead of it on the stream finishes
     // (programmatic dependent launch); the kernel waits with griddepcontrol.wait before
@@ -904,7 +947,7 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, GK, GV, HS>, p);
+    err = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, GK, GV, HK, HS>, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -915,37 +958,35 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
 cudaError_t decode_run_gk32(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_gk64(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_gk128(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
-int decode_occupancy_gk32(const DecodeArgs& a, size_t smem);
-int decode_occupancy_gk64(const DecodeArgs& a, size_t smem);
-int decode_occupancy_gk128(const DecodeArgs& a, size_t smem);
+int decode_occupancy_gk32(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_gk64(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_gk128(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 
 }  // namespace kvq
 
-// Instantiates the dispatch for one K group size GK_ over GV in {32, 64, 128}, HS in {1, 2}.
+// Instantiates the dispatch for one K group size GK_ over GV in {32, 64, 128} and the
+// three unit shapes (HK, HS) in {(1, 1), (1, 2), (4, 1)}.
+#define KVQ_DECODE_DISPATCH(GK_, CALL, FAIL)                                                         \
+    switch (a.L.Gv * 16 + plan.hk * 4 + plan.hs) {                                                   \
+        case 32 * 16 + 4 + 1: return CALL(128, GK_, 32, 1, 1);                                       \
+        case 32 * 16 + 4 + 2: return CALL(128, GK_, 32, 1, 2);                                       \
+        case 32 * 16 + 16 + 1: return CALL(128, GK_, 32, 4, 1);                                      \
+        case 64 * 16 + 4 + 1: return CALL(128, GK_, 64, 1, 1);                                       \
+        case 64 * 16 + 4 + 2: return CALL(128, GK_, 64, 1, 2);                                       \
+        case 64 * 16 + 16 + 1: return CALL(128, GK_, 64, 4, 1);                                      \
+        case 128 * 16 + 4 + 1: return CALL(128, GK_, 128, 1, 1);                                     \
+        case 128 * 16 + 4 + 2: return CALL(128, GK_, 128, 1, 2);                                     \
+        case 128 * 16 + 16 + 1: return CALL(128, GK_, 128, 4, 1);                                    \
+        default: return FAIL;                                                                        \
+    }
+#define KVQ_DECODE_RUN(D_, GK_, GV_, HK_, HS_) decode::run<D_, GK_, GV_, HK_, HS_>(a, plan, s)
+#define KVQ_DECODE_OCC(D_, GK_, GV_, HK_, HS_) decode::occupancy<D_, GK_, GV_, HK_, HS_>(smem)
 #define KVQ_DECODE_TU(GK_)                                                                           \
     namespace kvq {                                                                                  \
     cudaError_t decode_run_gk##GK_(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {    \
-        const int hs = (a.Hq / a.Hkv) > 4 ? 2 : 1;                                                   \
-        switch (a.L.Gv * 4 + hs) {                                                                   \
-            case 32 * 4 + 1: return decode::run<128, GK_, 32, 1>(a, plan, s);                        \
-            case 32 * 4 + 2: return decode::run<128, GK_, 32, 2>(a, plan, s);                        \
-            case 64 * 4 + 1: return decode::run<128, GK_, 64, 1>(a, plan, s);                        \
-            case 64 * 4 + 2: return decode::run<128, GK_, 64, 2>(a, plan, s);                        \
-            case 128 * 4 + 1: return decode::run<128, GK_, 128, 1>(a, plan, s);                      \
-            case 128 * 4 + 2: return decode::run<128, GK_, 128, 2>(a, plan, s);                      \
-            default: return cudaErrorInvalidValue;                                                   \
-        }                                                                                            \
+        KVQ_DECODE_DISPATCH(GK_, KVQ_DECODE_RUN, cudaErrorInvalidValue)                              \
     }                                                                                                \
-    int decode_occupancy_gk##GK_(const DecodeArgs& a, size_t smem) {                                 \
-        const int hs = (a.Hq / a.Hkv) > 4 ? 2 : 1;                                                   \
-        switch (a.L.Gv * 4 + hs) {                                                                   \
-            case 32 * 4 + 1: return decode::occupancy<128, GK_, 32, 1>(smem);                        \
-            case 32 * 4 + 2: return decode::occupancy<128, GK_, 32, 2>(smem);                        \
-            case 64 * 4 + 1: return decode::occupancy<128, GK_, 64, 1>(smem);                        \
-            case 64 * 4 + 2: return decode::occupancy<128, GK_, 64, 2>(smem);                        \
-            case 128 * 4 + 1: return decode::occupancy<128, GK_, 128, 1>(smem);                      \
-            case 128 * 4 + 2: return decode::occupancy<128, GK_, 128, 2>(smem);                      \
-            default: return 0;                                                                       \
-        }                                                                                            \
+    int decode_occupancy_gk##GK_(const DecodeArgs& a, const DecodePlan& plan, size_t smem) {         \
+        KVQ_DECODE_DISPATCH(GK_, KVQ_DECODE_OCC, 0)                                                  \
     }                                                                                                \
     }

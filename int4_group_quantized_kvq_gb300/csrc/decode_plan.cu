@@ -1,18 +1,16 @@
 // decode_plan.cu -- sizing of the persistent split-KV grid and of its workspace.
 //
-// The grid is W warps (4 per CTA).  W is the number of warps the device can keep
-// resident (SMs x resident CTAs x 4), reduced for small problems so that a warp gets
-// at least two pages; every warp receives an equal contiguous slice of the flattened
-// (sequence, kv head, page) units.  Each warp writes at most one partial per
-// (sequence, kv head) segment its slice touches.  Partial index = warp + segment is
-// unique: if warp w touches segment s and warp w-1 touches segment s+1, warp w-1 would
-// hold a later unit than warp w, which contiguous ordered slices rule out.  So the
-// workspace holds W + B * Hkv partials, each r (query heads per KV head) x (2 + d) floats,
-// plus one split counter per (sequence, KV head) and, for segments spread over more than
-// 32 warps, a second level: one counter and one partial per group of 32 warps (indexed
-// by the group's first partial, so the same W + B * Hkv slots suffice).  The counters
-// must be zero when a call starts; each is reset by the warp that consumes it, so they
-// stay zero from one call to the next while the workspace serves the same shape.
+// A unit of work is one page of HK consecutive kv heads: HK = 4 when every query head
+// has its own kv head, Hkv is a multiple of 4 and pages hold 16 tokens, else HK = 1.  The grid is C CTAs of 4
+// warps: C is the number of CTAs the device keeps resident (SMs x resident CTAs),
+// reduced for small problems so that a CTA gets at least eight units; every CTA
+// receives an equal contiguous slice of the flattened (sequence, head group, page)
+// units.  Each CTA writes at most one partial per segment (sequence, head group) its
+// slice touches, at index CTA + segment, which is unique (see piece_index in the
+// kernel).  So the workspace holds C + B * Hg partials of ns = HK * r query heads, each
+// (max, sum) plus d floats, and one split counter per segment.  The counters must be
+// zero when a call starts; each is reset by the CTA that consumes it, so they stay
+// zero from one call to the next while the workspace serves the same shape.
 #include <algorithm>
 
 #include "kvq_internal.h"
@@ -22,14 +20,16 @@ namespace kvq {
 cudaError_t decode_run_gk32(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_gk64(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_gk128(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
-int decode_occupancy_gk32(const DecodeArgs& a, size_t smem);
-int decode_occupancy_gk64(const DecodeArgs& a, size_t smem);
-int decode_occupancy_gk128(const DecodeArgs& a, size_t smem);
+int decode_occupancy_gk32(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_gk64(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_gk128(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 
 namespace {
 constexpr int kWarpsPerCta = 4;
-constexpr int kMaxStages = 8;  // deepest page ring per warp
-constexpr size_t kWarpCtxBytes = 64;  // per-warp shared context of the decode kernel
+constexpr int kMaxStages = 8;           // deepest unit ring per warp
+constexpr size_t kMaxRingBytes = 8 * 2144;  // per warp: deeper rings gain nothing
+constexpr size_t kCtlBytes = 64;        // CTA bookkeeping of the decode kernel
+constexpr int kMinUnitsPerCta = 8;
 constexpr size_t kAlign = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -40,17 +40,27 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     if (a.L.P % 16 != 0) return cudaErrorInvalidValue;
     const int r = a.Hq / a.Hkv;
     if (r < 1 || r > 8) return cudaErrorInvalidValue;
-    // Resident CTAs are limited by registers; give each warp as deep a ring of page
-    // buffers as the shared memory left at that occupancy allows (up to 8 stages).
+    // four kv heads per unit for 16-token pages (a 4-block unit then stays near the size
+    // of one larger page); larger pages are big enough copies on their own
+    plan->hk = (r == 1 && a.Hkv % 4 == 0 && a.L.P == 16) ? 4 : 1;
+    plan->hs = (plan->hk == 1 && r > 4) ? 2 : 1;
+    const int hg = a.Hkv / plan->hk;
+    const int ns = plan->hk * r;
+    const size_t unit = static_cast<size_t>(a.L.bytes) * plan->hk;
+    // the CTA merge stages a warp's part (4 slots x (d + 2) floats) in a unit buffer
+    if (unit < static_cast<size_t>(4 * (a.L.d + 2)) * sizeof(float)) return cudaErrorInvalidValue;
+
+    // Resident CTAs are limited by registers; give each warp as deep a ring of unit
+    // buffers as the shared memory left at that occupancy allows.
     auto smem_for = [&](int st) {
-        return static_cast<size_t>(kWarpsPerCta) * st * a.L.bytes + static_cast<size_t>(kWarpsPerCta) * st * 8 +
-               static_cast<size_t>(kWarpsPerCta) * kWarpCtxBytes + static_cast<size_t>(a.B + 1) * 4;
+        return static_cast<size_t>(kWarpsPerCta) * st * unit + static_cast<size_t>(kWarpsPerCta) * st * 8 +
+               kCtlBytes + round_up(static_cast<size_t>(a.B + 1) * 4, 16);
     };
     auto occ_for = [&](size_t smem) {
         switch (a.L.Gk) {
-            case 32: return decode_occupancy_gk32(a, smem);
-            case 64: return decode_occupancy_gk64(a, smem);
-            case 128: return decode_occupancy_gk128(a, smem);
+            case 32: return decode_occupancy_gk32(a, *plan, smem);
+            case 64: return decode_occupancy_gk64(a, *plan, smem);
+            case 128: return decode_occupancy_gk128(a, *plan, smem);
             default: return 0;
         }
     };
@@ -63,36 +73,29 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     if (err != cudaSuccess) return err;
     int stages = 2;
     if (smem_for(stages) > static_cast<size_t>(smem_max)) return cudaErrorInvalidConfiguration;
-    int occ = occ_for(smem_for(stages));
+    const int occ = occ_for(smem_for(stages));
     if (occ <= 0) return a.L.Gk == 32 || a.L.Gk == 64 || a.L.Gk == 128 ? cudaErrorInvalidConfiguration
                                                                     : cudaErrorInvalidValue;
     for (int st = kMaxStages; st > 2; --st) {
+        if (static_cast<size_t>(st) * unit > std::max(kMaxRingBytes, 3 * unit)) continue;
         if (smem_for(st) <= static_cast<size_t>(smem_max) && occ_for(smem_for(st)) >= occ) {
             stages = st;
             break;
         }
     }
-    const size_t smem = smem_for(stages);
-    const long long w_max = static_cast<long long>(sms) * occ * kWarpsPerCta;
+    const long long c_max = static_cast<long long>(sms) * occ;
     const long long pages_max = (static_cast<long long>(std::max(a.max_len, 0)) + a.L.P - 1) / a.L.P;
-    const long long u_max = static_cast<long long>(a.Hkv) * a.B * pages_max;
-    long long w = std::min(w_max, std::max<long long>(kWarpsPerCta, (u_max + 1) / 2));
-    w = round_up(static_cast<size_t>(w), kWarpsPerCta);
-    plan->warps = static_cast<int32_t>(w);
-    plan->ctas = static_cast<int32_t>(w / kWarpsPerCta);
+    const long long u_max = static_cast<long long>(hg) * a.B * pages_max;
+    const long long ctas = std::min(c_max, std::max<long long>(1, u_max / kMinUnitsPerCta));
+    plan->ctas = static_cast<int32_t>(ctas);
     plan->stages = stages;
-    plan->smem_bytes = smem;
-    const size_t pieces = static_cast<size_t>(w) + static_cast<size_t>(a.B) * a.Hkv;
-    const size_t segs = static_cast<size_t>(a.B) * a.Hkv;
-    const size_t part_ml = round_up(pieces * r * 2 * sizeof(float), kAlign);
-    const size_t part_o = round_up(pieces * r * a.L.d * sizeof(float), kAlign);
+    plan->smem_bytes = smem_for(stages);
+    const size_t pieces = static_cast<size_t>(ctas) + static_cast<size_t>(a.B) * hg;
+    const size_t segs = static_cast<size_t>(a.B) * hg;
     plan->ws_cnt_offset = kAlign;  // the first 256 bytes hold the status word
-    plan->ws_gcnt_offset = plan->ws_cnt_offset + round_up(segs * sizeof(int32_t), kAlign);
-    plan->ws_ml_offset = plan->ws_gcnt_offset + round_up(pieces * sizeof(int32_t), kAlign);
-    plan->ws_o_offset = plan->ws_ml_offset + part_ml;
-    plan->ws_gml_offset = plan->ws_o_offset + part_o;
-    plan->ws_go_offset = plan->ws_gml_offset + part_ml;
-    plan->ws_bytes = plan->ws_go_offset + part_o;
+    plan->ws_ml_offset = plan->ws_cnt_offset + round_up(segs * sizeof(int32_t), kAlign);
+    plan->ws_o_offset = plan->ws_ml_offset + round_up(pieces * ns * 2 * sizeof(float), kAlign);
+    plan->ws_bytes = plan->ws_o_offset + round_up(pieces * ns * a.L.d * sizeof(float), kAlign);
     return cudaSuccess;
 }
 

@@ -58,16 +58,14 @@ cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t stream);
 
 // Decode attention: the persistent split-KV kernel with the split combine fused in.
 struct DecodePlan {
-    int32_t warps;        // W: total consumer warps of the persistent grid (multiple of 4)
-    int32_t ctas;         // W / 4
-    int32_t stages;       // bulk-copy ring depth per warp
+    int32_t hk;           // kv heads per unit of work (4 when Hq == Hkv, Hkv % 4 == 0, P == 16; else 1)
+    int32_t hs;           // query-head slots per score thread: 1 (up to 4 per unit) or 2 (up to 8)
+    int32_t ctas;         // CTAs of the persistent grid (4 warps each)
+    int32_t stages;       // bulk-copy ring depth per warp, in units
     size_t smem_bytes;    // dynamic shared memory per CTA
-    size_t ws_cnt_offset;  // per-(sequence, kv head) split counters
-    size_t ws_gcnt_offset; // per-group counters of long segments
-    size_t ws_ml_offset;   // (m, l) partials
-    size_t ws_o_offset;    // o partials
-    size_t ws_gml_offset;  // level-2 (m, l) partials of long segments
-    size_t ws_go_offset;   // level-2 o partials
+    size_t ws_cnt_offset; // per-(sequence, head group) split counters
+    size_t ws_ml_offset;  // (max, sum) of the CTA partials
+    size_t ws_o_offset;   // unnormalised outputs of the CTA partials
     size_t ws_bytes;      // total workspace bytes
 };
 

@@ -28,14 +28,17 @@ def test_groups(kvq, Gk, Gv):
     _run(kvq, Case(3, 8, 8, 128, [300, 129, 17], Gk=Gk, Gv=Gv, seed=Gk + Gv))
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (12, 4), (16, 4), (32, 8), (16, 2), (8, 1), (24, 4)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (12, 4), (16, 4), (32, 8), (16, 2), (8, 1), (24, 4), (6, 6),
+                                     (2, 2), (12, 12)])
 def test_gqa_ratios(kvq, Hq, Hkv):
     _run(kvq, Case(2, Hq, Hkv, 128, [211, 64], seed=Hq * 7 + Hkv))
 
 
 @pytest.mark.parametrize("P", [16, 32, 64])
-def test_page_sizes(kvq, P):
-    _run(kvq, Case(3, 8, 4, 128, [1, P + 1, 5 * P - 3], P=P, seed=P))
+@pytest.mark.parametrize("Hq,Hkv", [(8, 4), (8, 8)])
+def test_page_sizes(kvq, P, Hq, Hkv):
+    # (8, 8) takes four kv heads per unit of work, (8, 4) one
+    _run(kvq, Case(3, Hq, Hkv, 128, [1, P + 1, 5 * P - 3], P=P, seed=P + Hkv))
 
 
 def test_edge_lengths(kvq):
@@ -56,9 +59,10 @@ def test_many_sequences_ragged(kvq):
     _run(kvq, Case(33, 8, 2, 128, lens, seed=8))
 
 
-def test_long_single_sequence(kvq):
-    # one sequence spread over many warps: exercises the combine of many partials
-    _run(kvq, Case(1, 32, 8, 128, [6000], seed=10))
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (16, 16), (16, 2)])
+def test_long_single_sequence(kvq, Hq, Hkv):
+    # one sequence spread over many CTAs: exercises the combine of many partials
+    _run(kvq, Case(1, Hq, Hkv, 128, [6000], seed=10 + Hkv))
 
 
 def test_contiguous_pages_and_no_outliers(kvq):
