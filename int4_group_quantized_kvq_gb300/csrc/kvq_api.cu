@@ -79,6 +79,8 @@ int kvq_quantize_append(const kvq_cache_config* cfg, void* pool, const void* k, 
         return fail(KVQ_EINVAL, "pool, k and v must be 16-byte aligned");
     if (!aligned(block_table, 4) || !aligned(start_pos, 4) || (status && !aligned(status, 4)))
         return fail(KVQ_EINVAL, "int32/uint32 arguments must be 4-byte aligned");
+    if (static_cast<int64_t>(batch) * n_new * cfg->num_kv_heads >= (int64_t{1} << 30))
+        return fail(KVQ_EINVAL, "batch * n_new * num_kv_heads must be below 2^30 per call");
     kvq::QuantizeArgs a;
     a.pool = static_cast<uint8_t*>(pool);
     a.k = static_cast<const __half*>(k);
@@ -91,6 +93,15 @@ int kvq_quantize_append(const kvq_cache_config* cfg, void* pool, const void* k, 
     a.n_new = n_new;
     a.Hkv = cfg->num_kv_heads;
     a.num_pages = cfg->num_pages;
+    a.rows = static_cast<uint32_t>(batch) * static_cast<uint32_t>(n_new) * static_cast<uint32_t>(cfg->num_kv_heads);
+    a.div_h = kvq::make_fastdiv(static_cast<uint32_t>(cfg->num_kv_heads));
+    a.div_n = kvq::make_fastdiv(static_cast<uint32_t>(n_new));
+    a.lg_p = 0;
+    while ((1 << a.lg_p) < cfg->page_size) ++a.lg_p;
+    a.lg_lanes_k = 0;
+    while ((8 << a.lg_lanes_k) < cfg->group_k) ++a.lg_lanes_k;
+    a.lg_lanes_v = 0;
+    while ((8 << a.lg_lanes_v) < cfg->group_v) ++a.lg_lanes_v;
     a.L = kvq::block_layout(*cfg);
     cudaError_t e = kvq::launch_quantize_append(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "kvq_quantize_append launch");

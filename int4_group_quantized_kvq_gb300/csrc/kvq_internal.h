@@ -33,6 +33,26 @@ inline BlockLayout block_layout(const kvq_cache_config& c) {
     return L;
 }
 
+// Division of 32-bit n < 2^31 by a fixed divisor d >= 1 as a multiply-high, add and
+// shift: with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (umulhi(n, m) + n) >> l, and the sum stays below 2^32 because n < 2^31.
+struct FastDiv {
+    uint32_t d, m, l;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.l = 0;
+    while ((1ull << f.l) < d) ++f.l;
+    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.l) - d)) / d + 1);
+    return f;
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+    return (__umulhi(n, f.m) + n) >> f.l;
+}
+#endif
+
 struct QuantizeArgs {
     uint8_t* pool;
     const __half* k;
@@ -41,6 +61,10 @@ struct QuantizeArgs {
     const int32_t* start_pos;
     uint32_t* status;
     int32_t max_blocks, B, n_new, Hkv, num_pages;
+    uint32_t rows;          // B * n_new * Hkv (< 2^30)
+    FastDiv div_h, div_n;   // by Hkv, by n_new
+    int32_t lg_p;           // log2 page_size
+    int32_t lg_lanes_k, lg_lanes_v;  // log2 of group_k / 8 and group_v / 8 (lanes of 8 values per group)
     BlockLayout L;
 };
 cudaError_t launch_quantize_append(const QuantizeArgs& a, cudaStream_t stream);

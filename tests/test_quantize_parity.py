@@ -60,6 +60,65 @@ def test_quantize_append_bitexact(kvq, d, P, Gk, Gv):
     assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
 
 
+@pytest.mark.parametrize("B,n,H", [(5, 13, 6), (1, 300, 3), (7, 1, 5)])
+def test_quantize_append_odd_shapes(kvq, B, n, H):
+    """Row counts, token counts and head counts that are not powers of two."""
+    d, P, Gk, Gv = 128, 16, 64, 128
+    per = (n + 2 * P) // P
+    npg = B * per + 1
+    L = oracle.Layout(H, d, P, Gk, Gv, npg)
+    x_k = _hard_inputs((B, n, H, d), seed=B * 100 + n + H)
+    x_v = _hard_inputs((B, n, H, d), seed=B * 100 + n + H + 1)
+    bt = W.permutation(B + n, npg).numpy()[:B * per].reshape(B, per).astype(np.int32)
+    start = (np.arange(B, dtype=np.int32) * 3) % P
+    ref = np.full(L.pool_bytes, 0x3C, np.uint8)
+    oracle.quantize_append(L, ref, x_k, x_v, bt, start)
+    _, pool = _gpu_pool(kvq, L, 0x3C, x_k, x_v, bt, start)
+    assert np.array_equal(pool.cpu().numpy(), ref)
+
+
+def _tie_rows(rng):
+    """fp16 groups of 64 built around a known scale s: one element 7 s (so the group's scale
+    is exactly s), every half-integer multiple (k + 1/2) s for k in -7..6 (exact ties),
+    the fp16 neighbours of each tie, and random values in [-7 s, 7 s].  The scales cover
+    every 7-bit mantissa over exponents -20..6 and the subnormals m * 2^-24 with 7 m < 1024."""
+    scales = [(64 + j) * 2.0 ** e for e in range(-20, 7) for j in range(64)]
+    scales += [m * 2.0 ** -24 for m in range(1, 147)]
+    groups = []
+    for sc in scales:
+        s16 = np.float16(sc)
+        assert float(s16) == sc and float(np.float16(7 * sc)) == 7 * sc
+        ties = np.array([(k + 0.5) * sc for k in range(-7, 7)], np.float16)
+        up = np.nextafter(ties, np.float16(np.inf))
+        down = np.nextafter(ties, np.float16(-np.inf))
+        rnd = (rng.uniform(-7, 7, 21) * sc).astype(np.float16)
+        g = np.concatenate([[np.float16(7 * sc)], ties, up, down, rnd]).astype(np.float16)
+        assert g.size == 64 and np.max(np.abs(g.astype(np.float64))) == 7 * sc
+        groups.append(rng.permutation(g))
+    return np.stack(groups)
+
+
+def test_quantize_rounding_ties_bitexact(kvq):
+    """Codes at and next to every half-integer multiple of the scale, for ~1900 scales."""
+    rng = np.random.default_rng(77)
+    g = _tie_rows(rng)                      # [n_groups, 64]
+    H, d, P = 4, 128, 16
+    n_rows = -(-g.shape[0] // 2)
+    n = -(-n_rows // H)
+    pad = np.zeros((n * H * 2 - g.shape[0], 64), np.float16)
+    rows = np.concatenate([g, pad]).reshape(1, n, H, d)
+    per = -(-n // P)
+    L = oracle.Layout(H, d, P, 64, 64, per)
+    bt = np.arange(per, dtype=np.int32).reshape(1, per)
+    start = np.zeros(1, np.int32)
+    ref = np.full(L.pool_bytes, 0xA5, np.uint8)
+    oracle.quantize_append(L, ref, rows, rows[:, ::-1].copy(), bt, start)
+    _, pool = _gpu_pool(kvq, L, 0xA5, rows, rows[:, ::-1].copy(), bt, start)
+    got = pool.cpu().numpy()
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
+
+
 def test_quantize_append_single_token_steps(kvq):
     """The decode step: one token per sequence at a time, positions advancing across pages."""
     B, H, d, P = 4, 8, 128, 16
