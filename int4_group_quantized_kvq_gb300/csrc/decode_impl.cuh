@@ -166,9 +166,10 @@ __device__ __forceinline__ long long piece_index(long long k, long long seg, lon
 
 // Merge the CTA partials of segment (b, hg), spread over the slices of CTAs cf..cl, into
 // the normalised output; run by all threads of the CTA that counted last.  Warp w takes
-// slots w and w + 4, lane l dimensions 4l .. 4l + 3; partials are read 16 at a time.
+// slots w and w + 4, lane l dimensions 4l .. 4l + 3; partials are read 8 at a time (the
+// merge is inlined and kept small so that the kernel fits three CTAs per SM).
 template <int D>
-__device__ __noinline__ void merge_segment(const KParams& p, int b, int hg, long long cf, long long cl,
+__device__ __forceinline__ void merge_segment(const KParams& p, int b, int hg, long long cf, long long cl,
                                            long long U, long long C) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -185,11 +186,11 @@ __device__ __noinline__ void merge_segment(const KParams& p, int b, int hg, long
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k0 = 0; k0 < n; k0 += 16) {
-            float2 ml[16];
-            float4 ov[16];
+        for (int k0 = 0; k0 < n; k0 += 8) {
+            float2 ml[8];
+            float4 ov[8];
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
+            for (int kk = 0; kk < 8; ++kk) {
                 const long long ix = k0 + kk < n ? piece_index(cf + k0 + kk, seg, U, C) : -1;
                 if (ix >= 0) {
                     ml[kk] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (ix * p.ns + sl) * 2));
@@ -200,7 +201,7 @@ __device__ __noinline__ void merge_segment(const KParams& p, int b, int hg, long
                 }
             }
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
+            for (int kk = 0; kk < 8; ++kk) {
                 const float f = fast_exp2(ml[kk].x - M);
                 L = fmaf(f, ml[kk].y, L);
                 acc.x = fmaf(f, ov[kk].x, acc.x);
@@ -235,9 +236,10 @@ struct Step {
     bool live[TG];
 };
 
-// Resident CTAs per SM the register budget is tuned for (3 gives up to 168 registers).
+// Resident CTAs per SM the register budget is tuned for: 3 (up to 168 registers) when a
+// thread carries one slot, 2 when it carries two (whose fragments need more).
 template <int HK, int HS>
-constexpr int min_ctas() { return 2; }
+constexpr int min_ctas() { return HS == 1 ? 3 : 2; }
 
 template <int D, int GK, int GV, int HK, int HS>
 __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitkv_kernel(KParams p) {
