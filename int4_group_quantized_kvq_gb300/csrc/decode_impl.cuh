@@ -67,19 +67,29 @@
 namespace kvq {
 namespace decode {
 
-constexpr int kWarps = 4;                         // warps per CTA
+constexpr int kMaxWarps = 16;                     // most warps per CTA
 constexpr uint64_t kWaitLimitNs = 250000000ull;   // a page copy that takes 250 ms has failed
+
+// Warps per CTA, and resident CTAs per SM the register budget is tuned for: 3 (up to 168
+// registers) when a thread carries one query-head slot, 2 when it carries two.
+template <int HS>
+constexpr int cta_warps() { return 4; }
+template <int HS>
+constexpr int min_ctas() { return HS == 1 ? 3 : 2; }
 
 // CTA-wide bookkeeping in shared memory.
 struct CtaCtl {
-    int buf[kWarps];     // ring stage holding warp w's part at a segment end (-1: none)
+    int buf[kMaxWarps];  // ring stage holding warp w's part at a segment end (-1: none)
     int pend_valid;      // a partial of segment (pend_b, pend_hg) has been counted ...
     int pend_b, pend_hg;
     int pend_target;     // ... out of pend_target, and the count came back as pend_arrived
     int pend_arrived;
-    int pad[7];
+    int pad[3];
+    uint64_t qbar[2];    // completion of the bulk copies of q rows into the two q buffers
+    uint64_t pad2[2];
 };
-static_assert(sizeof(CtaCtl) % 16 == 0, "keeps the prefix array aligned");
+static_assert(sizeof(CtaCtl) == 128, "the planner reserves 128 bytes");
+constexpr int kQBufBytes = 2 * 8 * 128 * 2;  // two buffers of up to 8 query-head rows of d = 128 fp16
 
 struct KParams {
     const uint8_t* pool;
@@ -97,8 +107,9 @@ struct KParams {
     float scale_log2;  // softmax_scale * log2(e)
 };
 
-// Exclusive prefix sums of pages per sequence into pre[0..B]; run by one warp.
-__device__ __forceinline__ void page_prefix(const KParams& p, int32_t* pre, int lane) {
+// Exclusive prefix sums of pages per sequence into pre[0..B], and the lengths (negative
+// ones as 0) into lens[0..B-1]; run by one warp.
+__device__ __forceinline__ void page_prefix(const KParams& p, int32_t* pre, int32_t* lens, int lane) {
     int carry = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int b = b0 + lane;
@@ -106,6 +117,7 @@ __device__ __forceinline__ void page_prefix(const KParams& p, int32_t* pre, int 
         if (b < p.B) {
             int L = p.seq_lens[b];
             L = L < 0 ? 0 : L;
+            lens[b] = L;
             long long npl = (static_cast<long long>(L) + p.P - 1) / p.P;
             if (npl > p.max_blocks) {
                 raise_flag(p.status, KVQ_FLAG_BAD_POSITION);
@@ -176,7 +188,8 @@ __device__ __forceinline__ void merge_segment(const KParams& p, int b, int hg, l
     const long long seg = static_cast<long long>(b) * p.Hg + hg;
     const int n = static_cast<int>(cl - cf + 1);
     __threadfence();  // the partials counted before this CTA are visible
-    for (int sl = warp; sl < p.ns; sl += kWarps) {
+    const int nw = blockDim.x >> 5;
+    for (int sl = warp; sl < p.ns; sl += nw) {
         float M = -INFINITY;
         for (int k = lane; k < n; k += 32) {
             const long long ix = piece_index(cf + k, seg, U, C);
@@ -236,13 +249,8 @@ struct Step {
     bool live[TG];
 };
 
-// Resident CTAs per SM the register budget is tuned for: 3 (up to 168 registers) when a
-// thread carries one slot, 2 when it carries two (whose fragments need more).
-template <int HK, int HS>
-constexpr int min_ctas() { return HS == 1 ? 3 : 2; }
-
 template <int D, int GK, int GV, int HK, int HS>
-__global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitkv_kernel(KParams p) {
+__global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_splitkv_kernel(KParams p) {
     static_assert(D == 128, "the fragment mapping below is written for head_dim 128");
     static_assert(HK == 1 || HS == 1, "several kv heads per unit only with one query head each");
     constexpr int NGK = D / GK;               // K groups per row
@@ -254,6 +262,7 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
     constexpr int MT = D / 16;                // output m-tiles
     constexpr int ROW = D / 2;                // bytes of one token's codes
     constexpr int TG = HK == 1 ? 2 : 1;       // 16-token chunks per step
+    constexpr int kWarps = cta_warps<HS>();   // warps per CTA
     static_assert(NGV * VB == MT, "m-tiles cover head_dim");
 
     // a kernel launched behind this one may start its set-up; it waits for this grid
@@ -271,12 +280,20 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
     uint8_t* ring = smem + static_cast<size_t>(warp) * stages * ubytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_all) + warp * stages;
     CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + ring_all + kWarps * stages * sizeof(uint64_t));
-    int32_t* pre = reinterpret_cast<int32_t*>(ctl + 1);
+    __half* qbuf = reinterpret_cast<__half*>(ctl + 1);  // [2][8][D]
+    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(qbuf) + kQBufBytes);
+    int32_t* lens = pre + p.B + 1;
+    const uint32_t qbar0 = smem_u32(&ctl->qbar[0]);
 
     // every input may come from the kernel ahead of this one on the stream
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (warp == 0) page_prefix(p, pre, lane);
-    if (threadIdx.x == 0) ctl->pend_valid = 0;
+    if (warp == 0) page_prefix(p, pre, lens, lane);
+    if (threadIdx.x == 0) {
+        ctl->pend_valid = 0;
+        mbar_init(qbar0, 1);
+        mbar_init(qbar0 + 8, 1);
+        fence_mbar_init();
+    }
     __syncthreads();
 
     const long long U = static_cast<long long>(p.Hg) * pre[p.B];
@@ -588,6 +605,28 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
     int pend_arrived = 0; // thread 0: what the last counting atomic returned
     const bool p16 = p.P == 16;
 
+    // q rows of a segment go to shared memory by a bulk copy issued one segment ahead
+    // (thread 0); segment k of this CTA uses buffer k & 1 at phase (k >> 1) & 1
+    const uint32_t q_bytes = static_cast<uint32_t>(p.ns) * D * 2;
+    auto issue_q = [&](int sb, int shg, int k) {
+        const uint32_t bar = qbar0 + 8 * (k & 1);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, q_bytes);
+        bulk_g2s(smem_u32(qbuf + (k & 1) * 8 * D), p.q + (static_cast<long long>(sb) * p.Hq + shg * p.ns) * D, q_bytes,
+                 bar);
+    };
+    // the segment after (sb, shg), skipping sequences without positions; sb == B when none
+    auto next_seg = [&](int& sb, int& shg) {
+        if (++shg == p.Hg) {
+            shg = 0;
+            do {
+                ++sb;
+            } while (sb < p.B && pre[sb + 1] == pre[sb]);
+        }
+    };
+    if (threadIdx.x == 0) issue_q(b, hg, 0);
+    int segk = 0;  // segments of this CTA started so far
+
     while (sfirst < c1) {
         const long long ua = sfirst > c0 ? sfirst : c0;
         const long long ue = sfirst + np < c1 ? sfirst + np : c1;
@@ -597,12 +636,23 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
         int last_st = -1;   // stage of the last unit consumed in this segment
         int held[2] = {-1, -1}, held_i[2] = {0, 0};  // stages whose refill waits for the merge
 
+        // the next segment's q rows start moving now
+        if (threadIdx.x == 0 && sfirst + np < c1) {
+            int nb = b, nhg = hg;
+            next_seg(nb, nhg);
+            issue_q(nb, nhg, segk + 1);
+        }
         if (cnt > 0) {
             // new (sequence, head group): q fragments and a fresh softmax state
-            int L = p.seq_lens[b];
-            L = L < 0 ? 0 : L;
-            Leff = min(L, p.max_blocks * p.P);
-            const int hq0 = hg * p.ns;
+            Leff = min(lens[b], p.max_blocks * p.P);
+            if (!failed && !__all_sync(0xffffffffu, mbar_wait(qbar0 + 8 * (segk & 1), (segk >> 1) & 1, kWaitLimitNs))) {
+                if (lane == 0) raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
+                failed = true;
+                f_st = cst;
+                f_par = cpar;
+                f_out = issued - consumed;
+            }
+            const __half* qseg = qbuf + (segk & 1) * 8 * D;
 #pragma unroll
             for (int t = 0; t < NTQ; ++t) {
                 const int pi = 2 * t + (g & 1);
@@ -610,7 +660,7 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
                 const int R = pi % NGK;
                 const int j = (g >> 1) + 4 * sigma;
                 const bool colv = sigma < HS && j < p.ns;
-                const __half* qrow = p.q + (static_cast<long long>(b) * p.Hq + hq0 + (colv ? j : 0)) * D;
+                const __half* qrow = qseg + (colv ? j : 0) * D;
 #pragma unroll
                 for (int wi = 0; wi < KW; ++wi) {
                     const int dbase = c * (D / 4) + 8 * wi;
@@ -751,8 +801,8 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
             __syncthreads();
             // the pending record is only rewritten after this segment end's last barrier
             if (s == 0) pend_seen = ctl->pend_valid != 0;
-            const int sl = warp + 4 * s;
-            if (sl < p.ns) {
+            const int sl = warp + 4 * s;  // warps 0..3 merge the four slots of this round
+            if (warp < 4 && sl < p.ns) {
                 float M = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) {
@@ -788,7 +838,6 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
                     const long long piece = cta + seg;
                     if (lane == 0) *reinterpret_cast<float2*>(p.ws_ml + (piece * p.ns + sl) * 2) = make_float2(M, Ls);
                     reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + sl) * D)[lane] = O;
-                    __threadfence();  // publish the partial before it is counted
                 }
             }
             __syncthreads();
@@ -816,6 +865,9 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
         }
         // ---- count this CTA's partial; the result is looked at later ----
         if (!whole && threadIdx.x == 0) {
+            // the CTA's partial, written by several threads before the barrier above, is
+            // published by this thread's fence ahead of the count
+            __threadfence();
             pend_arrived = atomicAdd(p.counters + seg, 1);
             ctl->pend_valid = 1;
             ctl->pend_b = b;
@@ -824,6 +876,7 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
         }
 
         // ---- next segment ----
+        ++segk;
         sfirst += np;
         if (++hg == p.Hg) {
             hg = 0;
@@ -851,6 +904,12 @@ __global__ void __launch_bounds__(kWarps * 32, min_ctas<HK, HS>()) decode_splitk
         }
     }
 
+    // ---- no q copy may still be landing when the CTA leaves (they all have, unless a
+    // wait failed) ----
+    if (threadIdx.x == 0) {
+        for (int k = segk - 2; k < segk; ++k)
+            if (k >= 0) mbar_wait(qbar0 + 8 * (k & 1), (k >> 1) & 1, kWaitLimitNs);
+    }
     // ---- after a failed wait: let the copies already issued land before leaving ----
     if (failed) {
         int st = f_st;
@@ -895,7 +954,7 @@ int occupancy(size_t smem) {
     }
     if (ensure_smem_attr<D, GK, GV, HK, HS>(smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HK, HS>, kWarps * 32,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HK, HS>, cta_warps<HS>() * 32,
                                                       smem) != cudaSuccess)
         return 0;
     const long long entry = (static_cast<long long>(smem) << 8) | (n & 0xff);
@@ -944,7 +1003,7 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.ctas));
-    cfg.blockDim = dim3(kWarps * 32);
+    cfg.blockDim = dim3(cta_warps<HS>() * 32);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;

@@ -1,9 +1,10 @@
 // decode_plan.cu -- sizing of the persistent split-KV grid and of its workspace.
 //
 // A unit of work is one page of HK consecutive kv heads: HK = 4 when every query head
-// has its own kv head, Hkv is a multiple of 4 and pages hold 16 tokens, else HK = 1.  The grid is C CTAs of 4
-// warps: C is the number of CTAs the device keeps resident (SMs x resident CTAs),
-// reduced for small problems so that a CTA gets at least eight units; every CTA
+// has its own kv head, Hkv is a multiple of 4 and pages hold 16 tokens, else HK = 1.
+// The grid is C CTAs of 4 warps: C is the number of CTAs the device keeps resident (SMs
+// x resident CTAs), reduced for small problems so that a warp gets at least two units;
+// every CTA
 // receives an equal contiguous slice of the flattened (sequence, head group, page)
 // units.  Each CTA writes at most one partial per segment (sequence, head group) its
 // slice touches, at index CTA + segment, which is unique (see piece_index in the
@@ -25,11 +26,10 @@ int decode_occupancy_gk64(const DecodeArgs& a, const DecodePlan& plan, size_t sm
 int decode_occupancy_gk128(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 
 namespace {
-constexpr int kWarpsPerCta = 4;
 constexpr int kMaxStages = 8;           // deepest unit ring per warp
 constexpr size_t kMaxRingBytes = 8 * 2144;  // per warp: deeper rings gain nothing
-constexpr size_t kCtlBytes = 64;        // CTA bookkeeping of the decode kernel
-constexpr int kMinUnitsPerCta = 8;
+constexpr size_t kCtlBytes = 128 + 2 * 8 * 128 * 2;  // CTA bookkeeping and the two q buffers
+constexpr int kMinUnitsPerWarp = 2;
 constexpr size_t kAlign = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -45,6 +45,7 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     plan->hk = (r == 1 && a.Hkv % 4 == 0 && a.L.P == 16) ? 4 : 1;
     plan->hs = (plan->hk == 1 && r > 4) ? 2 : 1;
     const int hg = a.Hkv / plan->hk;
+    const int kWarpsPerCta = 4;  // the kernel's CTA size
     const int ns = plan->hk * r;
     const size_t unit = static_cast<size_t>(a.L.bytes) * plan->hk;
     // the CTA merge stages a warp's part (4 slots x (d + 2) floats) in a unit buffer
@@ -54,7 +55,7 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     // buffers as the shared memory left at that occupancy allows.
     auto smem_for = [&](int st) {
         return static_cast<size_t>(kWarpsPerCta) * st * unit + static_cast<size_t>(kWarpsPerCta) * st * 8 +
-               kCtlBytes + round_up(static_cast<size_t>(a.B + 1) * 4, 16);
+               kCtlBytes + round_up(static_cast<size_t>(2 * a.B + 1) * 4, 16);
     };
     auto occ_for = [&](size_t smem) {
         switch (a.L.Gk) {
@@ -86,7 +87,7 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     const long long c_max = static_cast<long long>(sms) * occ;
     const long long pages_max = (static_cast<long long>(std::max(a.max_len, 0)) + a.L.P - 1) / a.L.P;
     const long long u_max = static_cast<long long>(hg) * a.B * pages_max;
-    const long long ctas = std::min(c_max, std::max<long long>(1, u_max / kMinUnitsPerCta));
+    const long long ctas = std::min(c_max, std::max<long long>(1, u_max / (kMinUnitsPerWarp * kWarpsPerCta)));
     plan->ctas = static_cast<int32_t>(ctas);
     plan->stages = stages;
     plan->smem_bytes = smem_for(stages);
