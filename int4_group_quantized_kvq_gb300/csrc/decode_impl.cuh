@@ -84,9 +84,10 @@ struct CtaCtl {
     int pend_b, pend_hg;
     int pend_target;     // ... out of pend_target, and the count came back as pend_arrived
     int pend_arrived;
-    int pad[3];
+    int ndm;             // segments this CTA counted last and merges after streaming (<= 2:
+    int dm_b[2], dm_hg[2];  // only the first and the last segment of a slice are shared)
+    int pad;
     uint64_t qbar[2];    // completion of the bulk copies of q rows into the two q buffers
-    uint64_t pad2[2];
 };
 static_assert(sizeof(CtaCtl) == 128, "the planner reserves 128 bytes");
 constexpr int kQBufBytes = 2 * 8 * 128 * 2;  // two buffers of up to 8 query-head rows of d = 128 fp16
@@ -178,57 +179,77 @@ __device__ __forceinline__ long long piece_index(long long k, long long seg, lon
 
 // Merge the CTA partials of segment (b, hg), spread over the slices of CTAs cf..cl, into
 // the normalised output; run by all threads of the CTA that counted last.  Warp w takes
-// slots w and w + 4, lane l dimensions 4l .. 4l + 3; partials are read 8 at a time (the
-// merge is inlined and kept small so that the kernel fits three CTAs per SM).
-template <int D>
-__device__ __forceinline__ void merge_segment(const KParams& p, int b, int hg, long long cf, long long cl,
-                                           long long U, long long C) {
+// slots w and w + 4, lane l dimensions 4l .. 4l + 3.  First the lanes find the largest
+// running maximum M among the partials (lane k reads partials k, k + 32, ...), then the
+// outputs are folded NB partials at a time with weights 2^(m_k - M), into four
+// independent accumulators so that consecutive partials do not wait on each other.
+template <int D, int NB>
+__device__ __forceinline__ void merge_partials(const KParams& p, int b, int hg, long long cf, long long cl,
+                                               long long U, long long C) {
+    static_assert(NB % 4 == 0, "four accumulators");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const long long seg = static_cast<long long>(b) * p.Hg + hg;
     const int n = static_cast<int>(cl - cf + 1);
+    const bool dense = U >= C;  // every CTA slice is non-empty: partial k sits at cf + k + seg
     __threadfence();  // the partials counted before this CTA are visible
     const int nw = blockDim.x >> 5;
     for (int sl = warp; sl < p.ns; sl += nw) {
+        const float* ml0 = p.ws_ml + ((cf + seg) * p.ns + sl) * 2;
+        const float* o0 = p.ws_o + ((cf + seg) * p.ns + sl) * D + 4 * lane;
+        const long long stride_ml = static_cast<long long>(p.ns) * 2;
+        const long long stride_o = static_cast<long long>(p.ns) * D;
+        auto present = [&](int k) { return dense || piece_index(cf + k, seg, U, C) >= 0; };
         float M = -INFINITY;
-        for (int k = lane; k < n; k += 32) {
-            const long long ix = piece_index(cf + k, seg, U, C);
-            if (ix >= 0) M = fmaxf(M, __ldcg(p.ws_ml + (ix * p.ns + sl) * 2));
-        }
+        for (int k = lane; k < n; k += 32)
+            if (present(k)) M = fmaxf(M, __ldcg(ml0 + k * stride_ml));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k0 = 0; k0 < n; k0 += 8) {
-            float2 ml[8];
-            float4 ov[8];
+        float4 acc[4];
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const long long ix = k0 + kk < n ? piece_index(cf + k0 + kk, seg, U, C) : -1;
-                if (ix >= 0) {
-                    ml[kk] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (ix * p.ns + sl) * 2));
-                    ov[kk] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (ix * p.ns + sl) * D) + lane);
+        for (int a = 0; a < 4; ++a) acc[a] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k0 = 0; k0 < n; k0 += NB) {
+            float2 ml[NB];
+            float4 ov[NB];
+#pragma unroll
+            for (int kk = 0; kk < NB; ++kk) {
+                const int k = k0 + kk;
+                if (k < n && present(k)) {
+                    ml[kk] = __ldcg(reinterpret_cast<const float2*>(ml0 + k * stride_ml));
+                    ov[kk] = __ldcg(reinterpret_cast<const float4*>(o0 + k * stride_o));
                 } else {
                     ml[kk] = make_float2(-INFINITY, 0.f);
                     ov[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < NB; ++kk) {
                 const float f = fast_exp2(ml[kk].x - M);
                 L = fmaf(f, ml[kk].y, L);
-                acc.x = fmaf(f, ov[kk].x, acc.x);
-                acc.y = fmaf(f, ov[kk].y, acc.y);
-                acc.z = fmaf(f, ov[kk].z, acc.z);
-                acc.w = fmaf(f, ov[kk].w, acc.w);
+                float4& A = acc[kk & 3];
+                A.x = fmaf(f, ov[kk].x, A.x);
+                A.y = fmaf(f, ov[kk].y, A.y);
+                A.z = fmaf(f, ov[kk].z, A.z);
+                A.w = fmaf(f, ov[kk].w, A.w);
             }
         }
         const float inv = 1.f / L;
         const int hq = hg * p.ns + sl;
         reinterpret_cast<float4*>(p.out + (static_cast<long long>(b) * p.Hq + hq) * D)[lane] =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            make_float4((acc[0].x + acc[1].x + acc[2].x + acc[3].x) * inv,
+                        (acc[0].y + acc[1].y + acc[2].y + acc[3].y) * inv,
+                        (acc[0].z + acc[1].z + acc[2].z + acc[3].z) * inv,
+                        (acc[0].w + acc[1].w + acc[2].w + acc[3].w) * inv);
     }
     if (threadIdx.x == 0) p.counters[seg] = 0;
+}
+
+// The merge, run after the CTA has streamed its slice (every register is free then).
+template <int D>
+__device__ __noinline__ void merge_segment_final(const KParams& p, int b, int hg, long long cf, long long cl,
+                                                 long long U, long long C) {
+    merge_partials<D, 16>(p, b, hg, cf, cl, U, C);
 }
 
 // Number of non-empty CTA slices among cf..cl (all of them when no slice is empty).
@@ -290,6 +311,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     if (warp == 0) page_prefix(p, pre, lens, lane);
     if (threadIdx.x == 0) {
         ctl->pend_valid = 0;
+        ctl->ndm = 0;
         mbar_init(qbar0, 1);
         mbar_init(qbar0 + 8, 1);
         fence_mbar_init();
@@ -329,6 +351,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     unsigned long long wnext =
         32 + lane < nm ? reinterpret_cast<unsigned long long>(unit_block(p, pre, unit_of(32 + lane), HK)) : 0ull;
     int issued = 0;
+    const uint64_t l2_stream = l2_policy_evict_first();  // pages are read once per call
     auto issue = [&](int i, int st) {  // this warp's unit i into stage st; i increases call by call
         if (i - wbase >= 32) {
             wbase += 32;
@@ -341,7 +364,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         if (lane == 0) {
             const uint32_t bar = bar0 + 8 * st;
             mbar_arrive_expect_tx(bar, ubytes);
-            bulk_g2s(ring0 + st * ubytes, reinterpret_cast<const void*>(src), ubytes, bar);
+            bulk_g2s_hint(ring0 + st * ubytes, reinterpret_cast<const void*>(src), ubytes, bar, l2_stream);
         }
         ++issued;
     };
@@ -853,12 +876,13 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         if (pend_seen) {
             const int arrived = ctl->pend_arrived;
             const int target = ctl->pend_target;
-            if (arrived >= target && threadIdx.x == 0) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
-            if (arrived == target - 1) {
-                const int pb = ctl->pend_b, ph = ctl->pend_hg;
-                const int pnp = pre[pb + 1] - pre[pb];
-                const long long pf = static_cast<long long>(p.Hg) * pre[pb] + static_cast<long long>(ph) * pnp;
-                merge_segment<D>(p, pb, ph, slice_of(pf, U, C), slice_of(pf + pnp - 1, U, C), U, C);
+            if (threadIdx.x == 0) {
+                if (arrived >= target) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
+                if (arrived == target - 1 && ctl->ndm < 2) {  // this CTA merges the segment later
+                    ctl->dm_b[ctl->ndm] = ctl->pend_b;
+                    ctl->dm_hg[ctl->ndm] = ctl->pend_hg;
+                    ++ctl->ndm;
+                }
             }
             __syncthreads();  // everyone has read the pending record
             if (threadIdx.x == 0) ctl->pend_valid = 0;
@@ -888,20 +912,24 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         else break;
     }
 
-    // ---- the last count ----
+    // ---- the last count, then the merges of the segments this CTA counted last ----
     __syncthreads();
-    if (threadIdx.x == 0 && ctl->pend_valid) ctl->pend_arrived = pend_arrived;
-    __syncthreads();
-    if (ctl->pend_valid) {
-        const int arrived = ctl->pend_arrived;
+    if (threadIdx.x == 0 && ctl->pend_valid) {
+        const int arrived = pend_arrived;
         const int target = ctl->pend_target;
-        if (arrived >= target && threadIdx.x == 0) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
-        if (arrived == target - 1) {
-            const int pb = ctl->pend_b, ph = ctl->pend_hg;
-            const int pnp = pre[pb + 1] - pre[pb];
-            const long long pf = static_cast<long long>(p.Hg) * pre[pb] + static_cast<long long>(ph) * pnp;
-            merge_segment<D>(p, pb, ph, slice_of(pf, U, C), slice_of(pf + pnp - 1, U, C), U, C);
+        if (arrived >= target) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
+        if (arrived == target - 1 && ctl->ndm < 2) {
+            ctl->dm_b[ctl->ndm] = ctl->pend_b;
+            ctl->dm_hg[ctl->ndm] = ctl->pend_hg;
+            ++ctl->ndm;
         }
+    }
+    __syncthreads();
+    for (int k = 0; k < ctl->ndm; ++k) {
+        const int pb = ctl->dm_b[k], ph = ctl->dm_hg[k];
+        const int pnp = pre[pb + 1] - pre[pb];
+        const long long pf = static_cast<long long>(p.Hg) * pre[pb] + static_cast<long long>(ph) * pnp;
+        merge_segment_final<D>(p, pb, ph, slice_of(pf, U, C), slice_of(pf + pnp - 1, U, C), U, C);
     }
 
     // ---- no q copy may still be landing when the CTA leaves (they all have, unless a
