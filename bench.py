@@ -70,6 +70,34 @@ def load_peaks() -> dict:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
+KERNEL_SOURCES = ("int4_group_quantized_kvq_gb300/csrc/decode_impl.cuh",
+                  "int4_group_quantized_kvq_gb300/csrc/kvq_device.cuh",
+                  "int4_group_quantized_kvq_gb300/csrc/decode_plan.cu")
+
+
+def measured_traffic(workload: str) -> int | None:
+    """DRAM bytes of one decode launch from the committed ncu record, or None when the kernel
+    sources changed since the capture or the record is for another workload."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+    try:
+        rec = {}
+        for line in open(path):
+            line = line.strip()
+            if line and not line.startswith("#") and "=" in line:
+                k, v = line.split("=", 1)
+                rec[k.strip()] = v.strip()
+        h = hashlib.sha256()
+        for f in KERNEL_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        if rec.get("kernel_source_sha256") == h.hexdigest() and rec.get("workload") == workload:
+            return int(rec["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
 def make_workload(name: str, group: int | None):
     import workloads as W
     if name == "longctx":
@@ -473,7 +501,7 @@ def run_kvq(args, world, rank, local):
             "peak": peaks["hbm_gbs"],
             "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"],
-            "traffic": None,
+            "traffic": measured_traffic(wl.name),
             "kernel": "decode_splitkv_kernel (kvq_decode_attention), packed bytes of the cache per call",
             "peak_source": peaks["source"],
         },
