@@ -141,12 +141,44 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_config *cfg, int32_t batch, in
  *                 of the same (cfg, batch, num_q_heads, max_len); zero it again before
  *                 using it for another shape.
  * num_q_heads must be a multiple of num_kv_heads with a ratio of at most 8.
+ * Launch overlap: the kernel is launched with programmatic dependent launch.  While the
+ * kernel ahead of it on the stream is still running (only possible when that kernel
+ * has signalled its dependents early, which this library's kernels do), it may already
+ * read q, block_table and seq_lens; it reads the pool and touches out and the
+ * workspace only after that kernel has finished.  This library's kernels never write
+ * q, block_table or seq_lens.
  * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE or KVQ_ECUDA.
  */
 int kvq_decode_attention(const kvq_cache_config *cfg, const void *pool, const void *q,
                          const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
                          int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
                          float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * One decode step in one launch: quantize-on-append of one new token per sequence
+ * (exactly as kvq_quantize_append with n_new = 1), then decode attention (exactly as
+ * kvq_decode_attention) over the updated cache.  The warp that streams the page taking
+ * a sequence's new token quantizes the token itself, writes it to the pool and uses
+ * it; an append into a page the attention does not reach is written by the grid's
+ * other warps.  (The two steps are the pages' decode step, section 1.1 of the 4-bit
+ * page: append the token, then attend.)
+ *   pool          device, kvq_pool_bytes(cfg) bytes, 16-byte aligned; written in place.
+ *   k_new, v_new  device fp16 [batch, num_kv_heads, head_dim], contiguous, 16-byte
+ *                 aligned: the new token's K and V rows.
+ *   append_pos    device int32 [batch]: the new token of sequence b goes to position
+ *                 append_pos[b]; a negative position appends nothing for b.
+ *   other arguments as in kvq_decode_attention.  seq_lens[b] normally is
+ *                 append_pos[b] + 1, so the new token is attended to.
+ * A position outside the block table or a bad page id skips that append and sets a
+ * flag in the workspace status word.  Two sequences appending into the same slot
+ * leave either one.
+ * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE or KVQ_ECUDA.
+ */
+int kvq_decode_step(const kvq_cache_config *cfg, void *pool, const void *k_new, const void *v_new,
+                    const int32_t *append_pos, const void *q, const int32_t *block_table, int32_t max_blocks,
+                    const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len,
+                    float softmax_scale, float *out, void *workspace, size_t workspace_bytes,
+                    kvq_stream_t stream);
 
 /*
  * Decode attention that allocates nothing, for callers that cannot provide a

@@ -20,7 +20,7 @@ KVQ_FLAG_BAD_PAGE, KVQ_FLAG_BAD_POSITION, KVQ_FLAG_WAIT_TIMEOUT, KVQ_FLAG_STALE_
 
 ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
                "kvq_decode_attention", "kvq_dequantize", "kvq_read_status", "kvq_last_error", "kvq_version",
-               "kvq_decode_attention_noalloc")
+               "kvq_decode_attention_noalloc", "kvq_decode_step")
 
 
 class KvqError(RuntimeError):
@@ -65,6 +65,8 @@ def lib() -> C.CDLL:
         L.kvq_decode_attention.restype = C.c_int
         L.kvq_decode_attention_noalloc.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, P]
         L.kvq_decode_attention_noalloc.restype = C.c_int
+        L.kvq_decode_step.argtypes = [cfgp, P, P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
+        L.kvq_decode_step.restype = C.c_int
         L.kvq_dequantize.argtypes = [cfgp, P, P, I32, I32, I32, I32, P, P, I32, P, P]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_read_status.argtypes = [P, C.POINTER(C.c_uint32), P]
@@ -157,6 +159,24 @@ def kvq_decode_attention(cfg: CacheConfig, pool: torch.Tensor, q: torch.Tensor, 
     rc = lib().kvq_decode_attention(
         C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(q, "q", torch.float16),
         _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
+        _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(rc)
+
+
+def kvq_decode_step(cfg: CacheConfig, pool: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                    append_pos: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                    max_len: int, softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                    stream=None) -> None:
+    """One decode step in one launch: append k_new, v_new (fp16 [B, Hkv, d], or [B, 1, Hkv, d]) at
+    append_pos (int32 [B], negative: none), then attend q (fp16 [B, Hq, d]) over seq_lens into out
+    (fp32 [B, Hq, d])."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_decode_step(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(k_new, "k_new", torch.float16),
+        _dev(v_new, "v_new", torch.float16), _dev(append_pos, "append_pos", torch.int32),
+        _dev(q, "q", torch.float16), _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
         _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
         _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
         _stream(stream))

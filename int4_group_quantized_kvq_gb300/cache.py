@@ -1,10 +1,11 @@
 """One layer's INT4 paged KV cache on the GPU and its decode step.
 
 A thin holder of device buffers (torch allocates them; the library allocates
-nothing) around the two C ABI calls a decode step makes:
+nothing) around the C ABI calls of a decode step:
 
     quantize-on-append of the new token's K/V  ->  kvq_quantize_append
     decode attention over the packed cache      ->  kvq_decode_attention
+    both in one launch                          ->  kvq_decode_step
 
 ``decode_step_host`` is the same step driven from pinned host buffers: the new
 token's q/K/V are copied in and the output copied back on the same stream.
@@ -48,7 +49,13 @@ class PagedKVCache:
                                self.softmax_scale, out, self.workspace, stream=stream)
 
     def decode_step(self, q, k_new, v_new, append_pos, seq_lens, out, stream=None) -> None:
-        """Append one token per sequence at append_pos, then attend over seq_lens (which include it)."""
+        """Append one token per sequence at append_pos, then attend over seq_lens (which include it):
+        one launch of kvq_decode_step."""
+        B.kvq_decode_step(self.cfg, self.pool, k_new, v_new, append_pos, q, self.block_table, seq_lens, self.max_len,
+                          self.softmax_scale, out, self.workspace, stream=stream)
+
+    def decode_step_two_calls(self, q, k_new, v_new, append_pos, seq_lens, out, stream=None) -> None:
+        """The same step as two calls: kvq_quantize_append, then kvq_decode_attention."""
         self.append(k_new, v_new, append_pos, stream)
         self.attend(q, seq_lens, out, stream)
 

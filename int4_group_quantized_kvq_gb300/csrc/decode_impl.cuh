@@ -63,6 +63,7 @@
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_quant.cuh"
 
 namespace kvq {
 namespace decode {
@@ -106,11 +107,19 @@ struct KParams {
     int32_t P, num_pages, max_blocks, block_bytes, unit_bytes, stages;
     int32_t v_codes, k_scales, v_scales;
     float scale_log2;  // softmax_scale * log2(e)
+    // fused append (decode step): one token per sequence, K and V rows [B, Hkv, D] fp16,
+    // quantized into the pool at position append_pos[b] (< 0: none).  k_new == nullptr: none.
+    const __half* k_new;
+    const __half* v_new;
+    const int32_t* append_pos;
+    uint8_t* pool_w;
+    int32_t lg_p, lg_lk, lg_lv;  // log2 of P, of the K and of the V group width in 8-value lanes
 };
 
-// Exclusive prefix sums of pages per sequence into pre[0..B], and the lengths (negative
-// ones as 0) into lens[0..B-1]; run by one warp.
-__device__ __forceinline__ void page_prefix(const KParams& p, int32_t* pre, int32_t* lens, int lane) {
+// Exclusive prefix sums of pages per sequence into pre[0..B], the lengths (negative ones
+// as 0) into lens[0..B-1] and the append positions (-1: none) into aps[0..B-1]; run by
+// one warp.
+__device__ __forceinline__ void page_prefix(const KParams& p, int32_t* pre, int32_t* lens, int32_t* aps, int lane) {
     int carry = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int b = b0 + lane;
@@ -119,6 +128,7 @@ __device__ __forceinline__ void page_prefix(const KParams& p, int32_t* pre, int3
             int L = p.seq_lens[b];
             L = L < 0 ? 0 : L;
             lens[b] = L;
+            aps[b] = p.k_new != nullptr ? p.append_pos[b] : -1;
             long long npl = (static_cast<long long>(L) + p.P - 1) / p.P;
             if (npl > p.max_blocks) {
                 raise_flag(p.status, KVQ_FLAG_BAD_POSITION);
@@ -270,6 +280,49 @@ struct Step {
     bool live[TG];
 };
 
+// Fused append of the decode step: quantize the new token's K and V rows of sequence sb,
+// head group shg (its HK heads) into page index pgu of the sequence, in the pool and,
+// when the page is staged in shared memory at sblk, in that copy too.  All lanes call
+// this: lanes 0..15 take the K row, 16..31 the V row, 8 values each (the same arithmetic
+// and bytes as the quantize-append kernel).  Out of line: it runs once per segment at
+// most, and inlined into the streaming loop its code would crowd the instruction cache.
+template <int D, int HK>
+__device__ __noinline__ void append_rows(const KParams& p, const int32_t* aps, uint8_t* sblk, int sb, int shg,
+                                         int pgu) {
+    const int lane = threadIdx.x & 31;
+    const int page = p.block_table[static_cast<long long>(sb) * p.max_blocks + pgu];
+    const bool pvalid = page >= 0 && page < p.num_pages;  // else flagged where the page is looked up
+    const int slot = aps[sb] & ((1 << p.lg_p) - 1);
+    const int half = lane >> 4;
+    const int tl = lane & 15;
+    const int lg = half ? p.lg_lv : p.lg_lk;
+    const int ng = D >> (lg + 3);
+    const int code_off = (half ? p.v_codes : 0) + slot * (D / 2) + tl * 4;
+    const int scale_off = (half ? p.v_scales : p.k_scales) + slot * ng * 2 + (tl >> lg) * 2;
+    const bool writes_scale = (tl & ((1 << lg) - 1)) == 0;
+    for (int a = 0; a < HK; ++a) {
+        const int h = shg * HK + a;
+        const uint4 raw = *reinterpret_cast<const uint4*>((half ? p.v_new : p.k_new) +
+                                                          (static_cast<long long>(sb) * p.Hkv + h) * D + tl * 8);
+        __half s16;
+        const uint32_t word = quant_lane8<D / 8>(raw, lg, s16);
+        if (pvalid) {
+            uint8_t* gb = p.pool_w + (static_cast<long long>(page) * p.Hkv + h) * p.block_bytes;
+            *reinterpret_cast<uint32_t*>(gb + code_off) = word;
+            if (writes_scale) *reinterpret_cast<__half*>(gb + scale_off) = s16;
+            if (sblk != nullptr) {
+                uint8_t* sa = sblk + a * p.block_bytes;
+                *reinterpret_cast<uint32_t*>(sa + code_off) = word;
+                if (writes_scale) *reinterpret_cast<__half*>(sa + scale_off) = s16;
+            }
+        }
+    }
+    if (sblk != nullptr) {
+        fence_proxy_async_smem();  // the stage is refilled by the bulk copy engine later
+        __syncwarp();
+    }
+}
+
 template <int D, int GK, int GV, int HK, int HS>
 __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_splitkv_kernel(KParams p) {
     static_assert(D == 128, "the fragment mapping below is written for head_dim 128");
@@ -287,6 +340,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     static_assert(NGV * VB == MT, "m-tiles cover head_dim");
 
     // a kernel launched behind this one may start its set-up; it waits for this grid
+    // before it reads what this grid writes
     asm volatile("griddepcontrol.launch_dependents;");
 
     extern __shared__ __align__(128) uint8_t smem[];
@@ -304,11 +358,13 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     __half* qbuf = reinterpret_cast<__half*>(ctl + 1);  // [2][8][D]
     int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(qbuf) + kQBufBytes);
     int32_t* lens = pre + p.B + 1;
+    int32_t* aps = lens + p.B;
     const uint32_t qbar0 = smem_u32(&ctl->qbar[0]);
 
-    // every input may come from the kernel ahead of this one on the stream
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (warp == 0) page_prefix(p, pre, lens, lane);
+    // Until griddepcontrol.wait below, the kernel ahead of this one on the stream may still be
+    // running.  Only the read-only inputs are read before it: seq_lens, the block table and
+    // q.  The pool (written by quantize-append), the output and the workspace come after.
+    if (warp == 0) page_prefix(p, pre, lens, aps, lane);
     if (threadIdx.x == 0) {
         ctl->pend_valid = 0;
         ctl->ndm = 0;
@@ -321,16 +377,49 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     const long long U = static_cast<long long>(p.Hg) * pre[p.B];
     const long long C = gridDim.x;
     const long long cta = blockIdx.x;
-    // sequences with no positions get zeros (no slice visits them)
-    for (long long bb = cta * kWarps + warp; bb < p.B; bb += C * kWarps) {
-        if (pre[bb + 1] == pre[bb]) {
-            float4* z4 = reinterpret_cast<float4*>(p.out + bb * p.Hq * D);
-            for (int i = lane; i < p.Hq * D / 4; i += 32) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
     const long long c0 = slice_start(cta, U, C);
     const long long c1 = slice_start(cta + 1, U, C);
-    if (c0 >= c1) return;  // the whole CTA leaves together
+
+    // Appends whose page this call does not attend (or positions out of the table) are
+    // handled here, spread over all warps of the grid; the others by the warp that streams
+    // the page, which also patches its staged copy before using it.
+    auto orphan_appends = [&]() {
+        if (p.k_new == nullptr) return;
+        const long long W = C * kWarps;
+        const long long nseg = static_cast<long long>(p.B) * p.Hg;
+        for (long long t = cta * kWarps + warp; t < nseg; t += W) {
+            const int sb = static_cast<int>(t / p.Hg);
+            const int shg = static_cast<int>(t - static_cast<long long>(sb) * p.Hg);
+            const int apos = aps[sb];
+            if (apos < 0) continue;
+            const long long apg = static_cast<long long>(apos) >> p.lg_p;
+            if (apg >= p.max_blocks) {
+                if (lane == 0 && shg == 0) raise_flag(p.status, KVQ_FLAG_BAD_POSITION);
+                continue;
+            }
+            if (apg < pre[sb + 1] - pre[sb]) continue;  // streamed by this call
+            const int page = p.block_table[static_cast<long long>(sb) * p.max_blocks + apg];
+            if (page < 0 || page >= p.num_pages) {
+                if (lane == 0) raise_flag(p.status, KVQ_FLAG_BAD_PAGE);
+                continue;
+            }
+            append_rows<D, HK>(p, aps, nullptr, sb, shg, static_cast<int>(apg));
+        }
+    };
+
+    if (c0 >= c1) {
+        // no units: only the zeros of empty sequences and appends nobody streams, after the
+        // kernel ahead has finished
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        orphan_appends();
+        for (long long bb = cta * kWarps + warp; bb < p.B; bb += C * kWarps) {
+            if (pre[bb + 1] == pre[bb]) {
+                float4* z4 = reinterpret_cast<float4*>(p.out + bb * p.Hq * D);
+                for (int i = lane; i < p.Hq * D / 4; i += 32) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        return;  // the whole CTA leaves together
+    }
     const int span = static_cast<int>(c1 - c0);
     const int nm = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;  // this warp's units
 
@@ -368,6 +457,28 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         }
         ++issued;
     };
+    // the first segment's q rows (read-only input) can move before the wait
+    {
+        int b0 = find_seq(pre, p.B, p.Hg, c0);
+        const int np0 = pre[b0 + 1] - pre[b0];
+        const int hg0 = static_cast<int>((c0 - static_cast<long long>(p.Hg) * pre[b0]) / np0);
+        if (threadIdx.x == 0) {
+            const uint32_t qbytes0 = static_cast<uint32_t>(p.ns) * D * 2;
+            mbar_arrive_expect_tx(qbar0, qbytes0);
+            bulk_g2s(smem_u32(qbuf), p.q + (static_cast<long long>(b0) * p.Hq + hg0 * p.ns) * D, qbytes0, qbar0);
+        }
+    }
+
+    // ---- from here on the pool, the output and the workspace are used ----
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    orphan_appends();
+    // sequences with no positions get zeros (no slice visits them)
+    for (long long bb = cta * kWarps + warp; bb < p.B; bb += C * kWarps) {
+        if (pre[bb + 1] == pre[bb]) {
+            float4* z4 = reinterpret_cast<float4*>(p.out + bb * p.Hq * D);
+            for (int i = lane; i < p.Hq * D / 4; i += 32) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
     {
         const int pro = nm < stages ? nm : stages;
         for (int k = 0; k < pro; ++k) issue(k, k);
@@ -647,8 +758,8 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
             } while (sb < p.B && pre[sb + 1] == pre[sb]);
         }
     };
-    if (threadIdx.x == 0) issue_q(b, hg, 0);
-    int segk = 0;  // segments of this CTA started so far
+    int segk = 0;  // segments of this CTA started so far (segment 0's q copy is already issued)
+    int apg_seg = -1;  // page index (within the segment's sequence) of its append, if streamed here
 
     while (sfirst < c1) {
         const long long ua = sfirst > c0 ? sfirst : c0;
@@ -668,6 +779,8 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         if (cnt > 0) {
             // new (sequence, head group): q fragments and a fresh softmax state
             Leff = min(lens[b], p.max_blocks * p.P);
+            apg_seg = -1;
+            if (aps[b] >= 0 && (aps[b] >> p.lg_p) < np) apg_seg = aps[b] >> p.lg_p;
             if (!failed && !__all_sync(0xffffffffu, mbar_wait(qbar0 + 8 * (segk & 1), (segk >> 1) & 1, kWaitLimitNs))) {
                 if (lane == 0) raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
                 failed = true;
@@ -730,6 +843,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                 const uint8_t* blkA = ring + cst * ubytes;
                 const uint8_t* blkB = ring + st1 * ubytes;
                 const int pg = pg0 + kWarps * j;
+                // the page taking this step's appended token is patched before it is used
+                if (apg_seg >= 0 && (pg == apg_seg || (n == 2 && pg + kWarps == apg_seg)))
+                    append_rows<D, HK>(p, aps, ring + (pg == apg_seg ? cst : st1) * ubytes, b, hg, apg_seg);
                 if constexpr (HK == 1) {
                     if (p16) {
                         const int t0A = pg * 16, t0B = (pg + kWarps) * 16;
@@ -1021,6 +1137,16 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     p.k_scales = a.L.k_scales;
     p.v_scales = a.L.v_scales;
     p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+    p.k_new = a.k_new;
+    p.v_new = a.v_new;
+    p.append_pos = a.append_pos;
+    p.pool_w = a.pool_w;
+    p.lg_p = 0;
+    while ((1 << p.lg_p) < a.L.P) ++p.lg_p;
+    p.lg_lk = 0;
+    while ((8 << p.lg_lk) < a.L.Gk) ++p.lg_lk;
+    p.lg_lv = 0;
+    while ((8 << p.lg_lv) < a.L.Gv) ++p.lg_lv;
     cudaError_t err = ensure_smem_attr<D, GK, GV, HK, HS>(plan.smem_bytes);
     if (err != cudaSuccess) return err;
     // The launch may start before the kernel ahead of it on the stream finishes

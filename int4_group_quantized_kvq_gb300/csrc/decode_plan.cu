@@ -55,7 +55,7 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     // buffers as the shared memory left at that occupancy allows.
     auto smem_for = [&](int st) {
         return static_cast<size_t>(kWarpsPerCta) * st * unit + static_cast<size_t>(kWarpsPerCta) * st * 8 +
-               kCtlBytes + round_up(static_cast<size_t>(2 * a.B + 1) * 4, 16);
+               kCtlBytes + round_up(static_cast<size_t>(3 * a.B + 1) * 4, 16);
     };
     auto occ_for = [&](size_t smem) {
         switch (a.L.Gk) {

@@ -178,6 +178,58 @@ int kvq_decode_attention(const kvq_cache_config* cfg, const void* pool, const vo
     return ok();
 }
 
+int kvq_decode_step(const kvq_cache_config* cfg, void* pool, const void* k_new, const void* v_new,
+                    const int32_t* append_pos, const void* q, const int32_t* block_table, int32_t max_blocks,
+                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                    float* out, void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || num_q_heads < 1 || max_len < 0)
+        return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
+    if (num_q_heads % cfg->num_kv_heads)
+        return fail(KVQ_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, cfg->num_kv_heads);
+    if (num_q_heads / cfg->num_kv_heads > 8)
+        return fail(KVQ_EUNSUPPORTED, "query heads per KV head %d > 8", num_q_heads / cfg->num_kv_heads);
+    if (cfg->head_dim != 128) return fail(KVQ_EUNSUPPORTED, "the decode step supports head_dim 128");
+    if (batch > 4096) return fail(KVQ_EUNSUPPORTED, "batch %d > 4096", batch);
+    if (batch == 0) return ok();
+    if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
+    if (!pool || !k_new || !v_new || !append_pos || !q || !block_table || !seq_lens || !out || !workspace)
+        return fail(KVQ_EINVAL, "NULL device pointer");
+    if (!aligned(pool, 16) || !aligned(q, 16) || !aligned(out, 16) || !aligned(k_new, 16) || !aligned(v_new, 16))
+        return fail(KVQ_EINVAL, "pool, k_new, v_new, q and out must be 16-byte aligned");
+    if (!aligned(workspace, 256)) return fail(KVQ_EINVAL, "workspace must be 256-byte aligned");
+    if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(append_pos, 4))
+        return fail(KVQ_EINVAL, "int32 arguments must be aligned");
+    kvq::DecodeArgs a;
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.q = static_cast<const __half*>(q);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.workspace = static_cast<uint8_t*>(workspace);
+    a.max_blocks = max_blocks;
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hkv = cfg->num_kv_heads;
+    a.num_pages = cfg->num_pages;
+    a.max_len = max_len;
+    a.softmax_scale = softmax_scale;
+    a.L = kvq::block_layout(*cfg);
+    a.k_new = static_cast<const __half*>(k_new);
+    a.v_new = static_cast<const __half*>(v_new);
+    a.append_pos = append_pos;
+    a.pool_w = static_cast<uint8_t*>(pool);
+    kvq::DecodePlan plan;
+    cudaError_t e = kvq::plan_decode(a, &plan);
+    if (e == cudaErrorInvalidValue) return fail(KVQ_EUNSUPPORTED, "no decode kernel for this shape");
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step plan");
+    if (workspace_bytes < plan.ws_bytes)
+        return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, plan.ws_bytes);
+    e = kvq::launch_decode(a, plan, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step launch");
+    return ok();
+}
+
 int kvq_dequantize(const kvq_cache_config* cfg, const void* pool, const int32_t* block_table, int32_t max_blocks,
                    int32_t b, int32_t start, int32_t n, void* out_k, void* out_v, int32_t out_dtype, uint32_t* status,
                    kvq_stream_t stream) {

@@ -103,6 +103,11 @@ struct DecodeArgs {
     int32_t max_blocks, B, Hq, Hkv, num_pages, max_len;
     float softmax_scale;
     BlockLayout L;
+    // the decode step's fused append of one token per sequence (k_new == nullptr: none)
+    const __half* k_new = nullptr;
+    const __half* v_new = nullptr;
+    const int32_t* append_pos = nullptr;
+    uint8_t* pool_w = nullptr;
 };
 
 // Returns cudaErrorInvalidValue for a geometry no kernel instance covers.

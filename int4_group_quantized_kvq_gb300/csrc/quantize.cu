@@ -5,106 +5,29 @@
 // elements along head_dim, scale = amax / 7 (an all-zero group gets 1), code =
 // round(x / scale) clamped to [-7, 7].  Here scale = fp16_rne(fp32(amax) / 7.0f), the
 // zero test is on that fp16 value, and code = round_half_even(fp32(x) / fp32(scale)),
-// computed exactly without a per-element division (quant_code below), so codes and
-// scales are bit-exact functions of the input.
+// computed exactly without a per-element division (kvq_quant.cuh, shared with the decode
+// step's fused append), so codes and scales are bit-exact functions of the input.
 #include <cuda_fp16.h>
 
 #include <atomic>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_quant.cuh"
 
 namespace kvq {
 namespace {
-
-// round_half_even(fp32(x) / s) without a division per element.  x and s are fp16
-// values (s > 0), so the quotient q = x / s is either exactly a half-integer or more
-// than 2^-13 away from every half-integer: with x = X 2^a and s = S 2^b (integers
-// X, S < 2048), q - (k + 1/2) = (2 X 2^(a-b) - (2k + 1) S) / (2 S), whose numerator is
-// a nonzero multiple of min(1, 2^(a-b)), and 2^(a-b) > S / 4096 whenever |q| >= 1/2.
-// The fp32 quotient the definition rounds is therefore on the same side of every
-// half-integer as q.  y = x * rs, with rs within 2 ulp of 1/s, is within 2^-18 of q for
-// |q| < 16 (the quotient never reaches 16 for finite input: the fp16 scale is at least
-// two thirds of amax / 7), so rounding y gives the same code unless y is within 2^-10
-// of a half-integer h; there the sign of x - h s, exact in one fma because h s has at
-// most 15 significant bits, decides, with ties to even.
-__device__ __forceinline__ int exact_code(float x, float s, float y) {
-    const float h = floorf(y) + 0.5f;    // the half-integer next to y (when y is near one)
-    const float r = fmaf(-h, s, x);      // sign of x - h s, exact
-    const int lo = __float2int_rd(h);
-    return r > 0.f ? lo + 1 : (r < 0.f ? lo : lo + (lo & 1));
-}
-
-// The 8 codes of one lane as nibbles (code + 8, low nibble first) of a 32-bit word.
-__device__ __forceinline__ uint32_t quant8(const float (&x)[8], float s, bool plain) {
-    int c[8];
-    if (plain) {
-        // an infinite scale or a NaN input: the plain conversion of the IEEE quotient
-        // (a NaN quotient converts to 0)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) c[i] = __float2int_rn(__fdiv_rn(x[i], s));
-    } else {
-        float rs;
-        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rs) : "f"(s));
-        constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer, ties to even
-        bool near = false;
-        float y[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            y[i] = x[i] * rs;
-            const float m = y[i] + kMagic;
-            c[i] = __float_as_int(m) - 0x4B400000;
-            near |= fabsf(y[i] - (m - kMagic)) > 0.4990234375f;
-        }
-        if (near) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (fabsf(y[i] - rintf(y[i])) > 0.4990234375f) c[i] = exact_code(x[i], s, y[i]);
-        }
-    }
-    uint32_t word = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) word |= static_cast<uint32_t>(max(-7, min(7, c[i])) + 8) << (4 * i);
-    return word;
-}
 
 // Quantize one row job (a K or V row of one (sequence, token, kv head)) held as 8
 // values per lane, and store its codes and scales.  Every lane of the warp calls this
 // together (the group maximum is a shuffle reduction); `active` marks real jobs.
 template <int D>
 __device__ __forceinline__ void quantize_row(const QuantizeArgs& a, uint4 raw, uint32_t job, bool active, int tl) {
-    constexpr int LPR = D / 8;  // lanes per row
     const int is_v = static_cast<int>(job & 1u);
     const int lg = is_v ? a.lg_lanes_v : a.lg_lanes_k;  // log2 of the lanes per group
-    float x[8];
-    {
-        const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(h2[i]);
-            x[2 * i] = f.x;
-            x[2 * i + 1] = f.y;
-        }
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    // group maximum over the group's lanes (groups are aligned within the team).  The K
-    // and V teams of a warp have different group widths, so every lane runs the same
-    // shuffles and only folds in partners inside its own group.
-#pragma unroll
-    for (int off = 1; off < LPR; off <<= 1) {
-        const float other = __shfl_xor_sync(0xffffffffu, amax, off);
-        if (off < (1 << lg)) amax = fmaxf(amax, other);
-    }
+    __half s16;
+    const uint32_t word = quant_lane8<D / 8>(raw, lg, s16);
     if (!active) return;
-    __half s16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
-    if ((__half_as_ushort(s16) & 0x7fffu) == 0) s16 = __ushort_as_half(0x3c00u);
-    const float s = __half2float(s16);
-    bool nan = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) nan |= x[i] != x[i];
-    const uint32_t word = quant8(x, s, nan || isinf(s));
 
     // destination: row = (b * n_new + t) * Hkv + h -> position, page, slot
     const uint32_t row = job >> 1;
@@ -140,9 +63,12 @@ __device__ __forceinline__ void quantize_row(const QuantizeArgs& a, uint4 raw, u
 // grid-strided over a grid of one wave of resident CTAs.
 template <int D, int U>
 __global__ void __launch_bounds__(256) quantize_append_kernel(QuantizeArgs a) {
-    // a decode launched behind this kernel may start its own set-up now; it waits for
-    // this grid to finish before it reads the pool
+    // A decode launched behind this kernel may start its own set-up now; it waits for this
+    // grid to finish before it reads the pool.  This kernel itself may start before the
+    // kernel ahead of it (a decode that reads the pool) has finished: it waits for it
+    // before anything else.
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int LPR = D / 8;            // lanes per row
     constexpr int TEAMS = 32 / LPR;       // row jobs per warp at a time
     const int lane = threadIdx.x & 31;
@@ -198,7 +124,20 @@ cudaError_t launch_q(const QuantizeArgs& a, cudaStream_t stream) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long cap = static_cast<long long>(sms > 0 ? sms : 1) * quantize_ctas_per_sm<D, U>();
     if (blocks > cap) blocks = cap;
-    quantize_append_kernel<D, U><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(a);
+    // programmatic dependent launch: the CTAs may become resident while the kernel ahead
+    // drains; the kernel waits for it with griddepcontrol.wait before touching memory
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, quantize_append_kernel<D, U>, a);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

@@ -1,0 +1,171 @@
+"""The decode step in one launch (kvq_decode_step): append one token per sequence, then
+attend.  Checked against the oracle on the same bytes:
+  - the whole pool after the step is bit-exact with the oracle's quantize-append of the
+    new tokens (same fill byte everywhere else, so a stray write shows up);
+  - the attention output is within the tolerances of tests/kvq_testlib.py, against the
+    oracle's fp64 attention over the updated pool;
+  - the step equals the two-call path (kvq_quantize_append, then kvq_decode_attention)
+    bit for bit, pool and output.
+Cases cover four-head and one-head units, 8 query heads per kv head, page sizes 16/32/64,
+every group size pair, ragged batches, one long sequence over many CTAs, appends into a
+page the attention does not reach, sequences without an append, and bad positions."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import cuda_available
+from kvq_testlib import Case, assert_attention_close
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not cuda_available(), reason="needs a CUDA GPU")]
+
+
+def _setup(case: Case, append_pos, fill):
+    """Oracle pool with each sequence's history below its append position (or its whole length
+    when it appends nothing), and the new rows k_new / v_new [B, Hkv, d]."""
+    L = case.layout
+    pool = np.full(L.pool_bytes, fill, np.uint8)
+    bt = case.block_table.numpy()
+    hist = [ap if ap >= 0 else n for ap, n in zip(append_pos, case.lens)]
+    for b in range(case.B):
+        n = min(hist[b], case.k.shape[1])
+        if n > 0:
+            oracle.quantize_append(L, pool, case.k[b:b + 1, :n].numpy(), case.v[b:b + 1, :n].numpy(), bt[b:b + 1],
+                                   np.zeros(1, np.int32))
+    src = [min(max(ap, 0), case.k.shape[1] - 1) for ap in append_pos]
+    k_new = np.stack([case.k[b, src[b]].numpy() for b in range(case.B)]).astype(np.float16)
+    v_new = np.stack([case.v[b, src[b]].numpy() for b in range(case.B)]).astype(np.float16)
+    return pool, k_new, v_new
+
+
+def _oracle_step(case: Case, pool, k_new, v_new, append_pos, seq_lens):
+    L = case.layout
+    ref = pool.copy()
+    bt = case.block_table.numpy()
+    max_pos = bt.shape[1] * case.P
+    for b in range(case.B):
+        ap = append_pos[b]
+        if 0 <= ap < max_pos and 0 <= bt[b, ap // case.P] < case.num_pages:
+            oracle.quantize_append(L, ref, k_new[b:b + 1, None], v_new[b:b + 1, None], bt[b:b + 1],
+                                   np.array([ap], np.int32))
+    out = oracle.decode_attention(L, ref, case.q.numpy(), bt, np.array(seq_lens, np.int32), case.scale)
+    return ref, out
+
+
+def _gpu_step(kvq, case: Case, pool, k_new, v_new, append_pos, seq_lens, two_calls=False):
+    cfg = case.cfg(kvq)
+    pool_g = torch.from_numpy(pool.copy()).cuda()
+    kg = torch.from_numpy(k_new).cuda()
+    vg = torch.from_numpy(v_new).cuda()
+    ap = torch.tensor(append_pos, dtype=torch.int32, device="cuda")
+    q = case.q.cuda()
+    bt = case.block_table.cuda()
+    sl = torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
+    ml = max(max(seq_lens), 1)
+    out = torch.full((case.B, case.Hq, case.d), float("nan"), dtype=torch.float32, device="cuda")
+    ws = kvq.new_workspace(cfg, case.B, case.Hq, ml, device="cuda")
+    if two_calls:
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kvq.kvq_quantize_append(cfg, pool_g, kg[:, None], vg[:, None], bt, ap, status=status)
+        kvq.kvq_decode_attention(cfg, pool_g, q, bt, sl, ml, case.scale, out, ws)
+        flags = kvq.kvq_read_status(ws) | kvq.kvq_read_status(status)
+    else:
+        kvq.kvq_decode_step(cfg, pool_g, kg, vg, ap, q, bt, sl, ml, case.scale, out, ws)
+        flags = kvq.kvq_read_status(ws)
+    return pool_g.cpu().numpy(), out.cpu().numpy(), flags
+
+
+def _run(kvq, case: Case, append_pos=None, seq_lens=None, fill=0xC3, expect_flags=0, compare_two_calls=True):
+    append_pos = [n - 1 for n in case.lens] if append_pos is None else list(append_pos)
+    seq_lens = list(case.lens) if seq_lens is None else list(seq_lens)
+    pool, k_new, v_new = _setup(case, append_pos, fill)
+    ref_pool, ref_out = _oracle_step(case, pool, k_new, v_new, append_pos, seq_lens)
+    got_pool, got_out, flags = _gpu_step(kvq, case, pool, k_new, v_new, append_pos, seq_lens)
+    assert flags == expect_flags, f"status flags {flags:#x}, expected {expect_flags:#x}"
+    diff = np.nonzero(got_pool != ref_pool)[0]
+    assert diff.size == 0, f"{diff.size} pool bytes differ, first at {diff[:8]}"
+    stats = assert_attention_close(got_out, ref_out, what=f"B{case.B} Hq{case.Hq} Hkv{case.Hkv} P{case.P}")
+    if compare_two_calls:
+        pool2, out2, _ = _gpu_step(kvq, case, pool, k_new, v_new, append_pos, seq_lens, two_calls=True)
+        assert np.array_equal(pool2, got_pool), "pool differs from the two-call path"
+        assert np.array_equal(out2, got_out), "output differs from the two-call path"
+    return stats
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (32, 8), (16, 2), (12, 4), (6, 6)])
+def test_step_head_ratios(kvq, Hq, Hkv):
+    _run(kvq, Case(3, Hq, Hkv, 128, [300, 129, 17], seed=Hq + 3 * Hkv))
+
+
+@pytest.mark.parametrize("P", [16, 32, 64])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4)])
+def test_step_page_sizes(kvq, P, Hq, Hkv):
+    _run(kvq, Case(3, Hq, Hkv, 128, [1, P + 1, 5 * P - 3], P=P, seed=P + Hkv))
+
+
+@pytest.mark.parametrize("Gk,Gv", [(64, 128), (32, 32), (128, 128), (32, 128), (128, 32)])
+def test_step_groups(kvq, Gk, Gv):
+    _run(kvq, Case(2, 8, 8, 128, [211, 40], Gk=Gk, Gv=Gv, seed=Gk + Gv))
+
+
+def test_step_ragged_batch(kvq):
+    rng = np.random.default_rng(21)
+    lens = rng.integers(1, 700, size=33).tolist()
+    _run(kvq, Case(33, 8, 2, 128, lens, seed=21))
+
+
+def test_step_long_single_sequence(kvq):
+    _run(kvq, Case(1, 32, 32, 128, [6000], seed=22))
+
+
+def test_step_append_beyond_attended_pages(kvq):
+    # sequence 0 appends at 99 (page 6) but attends 60 positions (pages 0..3): the append is
+    # written by the grid, not by the warp streaming the page; sequence 1 is the usual step
+    case = Case(2, 8, 8, 128, [100, 50], seed=23)
+    _run(kvq, case, append_pos=[99, 49], seq_lens=[60, 50])
+
+
+def test_step_without_append_and_empty(kvq):
+    # sequence 0 appends nothing; sequence 1 has no history and appends its first token;
+    # sequence 2 neither appends nor attends (zeros)
+    case = Case(3, 8, 4, 128, [40, 1, 5], seed=24)
+    _run(kvq, case, append_pos=[-1, 0, -1], seq_lens=[40, 1, 0])
+
+
+def test_step_bad_position_flagged(kvq):
+    case = Case(2, 8, 8, 128, [64, 33], seed=25)
+    max_pos = case.block_table.shape[1] * case.P
+    # sequence 0 appends past its block table: skipped and flagged; sequence 1 is normal
+    _run(kvq, case, append_pos=[max_pos + 5, 32], seq_lens=[64, 33], expect_flags=kvq.KVQ_FLAG_BAD_POSITION,
+         compare_two_calls=False)
+
+
+def test_step_repeated_steps_match_oracle(kvq):
+    """Several steps in a row on the same pool, positions advancing across a page boundary."""
+    case = Case(2, 16, 4, 128, [40, 70], seed=26)
+    L = case.layout
+    cfg = case.cfg(kvq)
+    bt = case.block_table.numpy()
+    hist = [30, 60]
+    pool = np.full(L.pool_bytes, 0x11, np.uint8)
+    for b in range(2):
+        oracle.quantize_append(L, pool, case.k[b:b + 1, :hist[b]].numpy(), case.v[b:b + 1, :hist[b]].numpy(),
+                               bt[b:b + 1], np.zeros(1, np.int32))
+    pool_g = torch.from_numpy(pool.copy()).cuda()
+    btg = case.block_table.cuda()
+    ws = kvq.new_workspace(cfg, 2, case.Hq, 70, device="cuda")
+    out = torch.empty((2, case.Hq, 128), dtype=torch.float32, device="cuda")
+    for step in range(10):
+        ap = [hist[0] + step, hist[1] + step]
+        sl = [a + 1 for a in ap]
+        k_new = np.stack([case.k[b, ap[b]].numpy() for b in range(2)]).astype(np.float16)
+        v_new = np.stack([case.v[b, ap[b]].numpy() for b in range(2)]).astype(np.float16)
+        pool, ref_out = _oracle_step(case, pool, k_new, v_new, ap, sl)
+        kvq.kvq_decode_step(cfg, pool_g, torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda(),
+                            torch.tensor(ap, dtype=torch.int32, device="cuda"), case.q.cuda(), btg,
+                            torch.tensor(sl, dtype=torch.int32, device="cuda"), 70, case.scale, out, ws)
+        assert np.array_equal(pool_g.cpu().numpy(), pool), f"step {step}: pool differs"
+        assert_attention_close(out.cpu().numpy(), ref_out, what=f"step {step}")
+    assert kvq.kvq_read_status(ws) == 0
