@@ -443,32 +443,32 @@ def run_kvq(args, world, rank, local):
     # ---- end to end through the public API from pinned host buffers ----
     e2e = None
     if not args.no_e2e:
-        q_h = q.cpu().pin_memory()
-        k_h = k_new.cpu().pin_memory()
-        v_h = v_new.cpu().pin_memory()
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        bufs = (torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(out))
+        from int4_group_quantized_kvq_gb300.cache import HostStaging
+        st = HostStaging(wl.B, wl.Hq, wl.Hkv, wl.d, device=dev)
+        st.q_host.copy_(q.cpu())
+        st.k_host.copy_(k_new.reshape(st.k_host.shape).cpu())
+        st.v_host.copy_(v_new.reshape(st.v_host.shape).cpu())
         for i in range(Wm):
-            caches[i % n_pools].decode_step_host(q_h, k_h, v_h, out_h, pos, seq_lens, bufs, stream=stream)
+            caches[i % n_pools].decode_step_host(st, pos, seq_lens, stream=stream)
         stream.synchronize()
         n_e2e = K
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
         for i in range(n_e2e):
-            caches[i % n_pools].decode_step_host(q_h, k_h, v_h, out_h, pos, seq_lens, bufs, stream=stream)
+            caches[i % n_pools].decode_step_host(st, pos, seq_lens, stream=stream)
         stream.synchronize()
         t_e2e = time.perf_counter() - t0
         if world > 1:
             t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             t_e2e = float(t.item())
-        h2d = q.numel() * 2 + k_new.numel() * 2 + v_new.numel() * 2
-        d2h = out.numel() * 4
+        h2d = st.host.numel() * 2
+        d2h = st.out_host.numel() * 4
         e2e = {"value": world * n_e2e * step_bytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": t_e2e / n_e2e * 1e3,
-               "how": "PagedKVCache.decode_step_host: pinned H2D of q/K/V, append + attend, D2H of out, "
-                      "wall clock over all steps with a stream sync at the end"}
+               "how": "PagedKVCache.decode_step_host: one pinned H2D copy of q/K/V, the step (one launch), "
+                      "one D2H copy of out, wall clock over all steps with a stream sync at the end"}
 
     if rank != 0:
         return None

@@ -7,8 +7,9 @@ nothing) around the C ABI calls of a decode step:
     decode attention over the packed cache      ->  kvq_decode_attention
     both in one launch                          ->  kvq_decode_step
 
-``decode_step_host`` is the same step driven from pinned host buffers: the new
-token's q/K/V are copied in and the output copied back on the same stream.
+``decode_step_host`` is the same step driven from pinned host buffers (``HostStaging``):
+the step's q, K and V are copied in with one transfer and the output copied back, on
+the same stream.
 """
 from __future__ import annotations
 
@@ -59,21 +60,39 @@ class PagedKVCache:
         self.append(k_new, v_new, append_pos, stream)
         self.attend(q, seq_lens, out, stream)
 
-    def decode_step_host(self, q_h, k_h, v_h, out_h, append_pos, seq_lens, dev_bufs, stream=None) -> None:
-        """The decode step from pinned host buffers: H2D of q/K/V, the two calls, D2H of out.
-
-        dev_bufs = (q, k_new, v_new, out) device tensors of matching shapes, reused across steps.
-        All copies are asynchronous on the step's stream.
-        """
+    def decode_step_host(self, staging: "HostStaging", append_pos, seq_lens, stream=None) -> None:
+        """The decode step from pinned host memory: one H2D copy of the step's q, K and V (staged
+        back to back), the step (one launch), one D2H copy of the output.  All asynchronous on
+        the step's stream."""
         s = torch.cuda.current_stream() if stream is None else stream
-        q, k, v, out = dev_bufs
         with torch.cuda.stream(s):
-            q.copy_(q_h, non_blocking=True)
-            k.copy_(k_h, non_blocking=True)
-            v.copy_(v_h, non_blocking=True)
-            self.decode_step(q, k, v, append_pos, seq_lens, out, stream=s)
-            out_h.copy_(out, non_blocking=True)
+            staging.dev.copy_(staging.host, non_blocking=True)
+            self.decode_step(staging.q, staging.k_new, staging.v_new, append_pos, seq_lens, staging.out, stream=s)
+            staging.out_host.copy_(staging.out, non_blocking=True)
 
     def flags(self) -> int:
         """Status flags of the last calls (synchronizes)."""
         return B.kvq_read_status(self.status) | B.kvq_read_status(self.workspace)
+
+
+class HostStaging:
+    """Pinned host buffers and their device twins for one decode step: q [B, Hq, d], k_new and
+    v_new [B, Hkv, d] fp16 back to back (so a step copies its inputs in one transfer), and the
+    fp32 output [B, Hq, d].  Fill `q_host`, `k_host`, `v_host` on the host; read `out_host`
+    after the stream has passed the step."""
+
+    def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, device="cuda"):
+        nq = batch * num_q_heads * head_dim
+        nk = batch * num_kv_heads * head_dim
+        self.host = torch.empty(nq + 2 * nk, dtype=torch.float16).pin_memory()
+        self.dev = torch.empty(nq + 2 * nk, dtype=torch.float16, device=device)
+        shq = (batch, num_q_heads, head_dim)
+        shk = (batch, num_kv_heads, head_dim)
+        self.q_host = self.host[:nq].view(shq)
+        self.k_host = self.host[nq:nq + nk].view(shk)
+        self.v_host = self.host[nq + nk:].view(shk)
+        self.q = self.dev[:nq].view(shq)
+        self.k_new = self.dev[nq:nq + nk].view(shk)
+        self.v_new = self.dev[nq + nk:].view(shk)
+        self.out = torch.empty(shq, dtype=torch.float32, device=device)
+        self.out_host = torch.empty(shq, dtype=torch.float32).pin_memory()

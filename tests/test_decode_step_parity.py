@@ -169,3 +169,30 @@ def test_step_repeated_steps_match_oracle(kvq):
         assert np.array_equal(pool_g.cpu().numpy(), pool), f"step {step}: pool differs"
         assert_attention_close(out.cpu().numpy(), ref_out, what=f"step {step}")
     assert kvq.kvq_read_status(ws) == 0
+
+
+def test_step_from_host_staging_matches_device_step(kvq):
+    """PagedKVCache.decode_step_host (one pinned H2D copy, the step, one D2H copy) gives the
+    device step's pool and output bit for bit."""
+    from int4_group_quantized_kvq_gb300.cache import HostStaging, PagedKVCache
+    case = Case(3, 16, 4, 128, [90, 33, 200], seed=27)
+    append_pos = [n - 1 for n in case.lens]
+    pool, k_new, v_new = _setup(case, append_pos, 0x00)
+    cfg = case.cfg(kvq)
+    ap = torch.tensor(append_pos, dtype=torch.int32, device="cuda")
+    sl = torch.tensor(case.lens, dtype=torch.int32, device="cuda")
+    c1 = PagedKVCache(cfg, case.block_table, case.Hq, max(case.lens), device="cuda",
+                      pool=torch.from_numpy(pool.copy()).cuda())
+    c2 = PagedKVCache(cfg, case.block_table, case.Hq, max(case.lens), device="cuda",
+                      pool=torch.from_numpy(pool.copy()).cuda())
+    out1 = torch.empty((case.B, case.Hq, case.d), dtype=torch.float32, device="cuda")
+    c1.decode_step(case.q.cuda(), torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda(), ap, sl, out1)
+    st = HostStaging(case.B, case.Hq, case.Hkv, case.d, device="cuda")
+    st.q_host.copy_(case.q)
+    st.k_host.copy_(torch.from_numpy(k_new))
+    st.v_host.copy_(torch.from_numpy(v_new))
+    c2.decode_step_host(st, ap, sl)
+    torch.cuda.synchronize()
+    assert torch.equal(c1.pool, c2.pool)
+    assert torch.equal(out1.cpu(), st.out_host)
+    assert c1.flags() == 0 and c2.flags() == 0
