@@ -520,7 +520,7 @@ def run_kvq(args, world, rank, local):
             "peak_source": peaks["source"],
         },
         "e2e": e2e,
-        "gpu_launches": K,  # one kvq_decode_step launch per step (append and split combine fused in)
+        "gpu_launches": 2 * K,  # per step: the decode grid (append fused in) and the combine grid
         "status_flags": flags,
         "clocks": clocks,
     }

@@ -86,9 +86,8 @@ enum {
 #define KVQ_FLAG_BAD_PAGE 0x1u     /* a block-table entry outside [0, num_pages)          */
 #define KVQ_FLAG_BAD_POSITION 0x2u /* a position or length beyond max_blocks * page_size  */
 #define KVQ_FLAG_WAIT_TIMEOUT 0x4u /* an asynchronous copy did not complete in time       */
-#define KVQ_FLAG_STALE_WORKSPACE 0x8u /* a split counter was not zero when the call began:
-                                         the workspace was not zeroed, or was last used for
-                                         another shape (the outputs of the call are unreliable) */
+#define KVQ_FLAG_STALE_WORKSPACE 0x8u /* reserved: no longer raised (the decode workspace
+                                         carries no state from one call to the next) */
 
 /* Bytes of one (page, kv-head) block; 0 if cfg is invalid.  Pure host computation. */
 size_t kvq_block_bytes(const kvq_cache_config *cfg);
@@ -134,19 +133,20 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_config *cfg, int32_t batch, in
  *   max_len       host bound on every seq_lens[b] (sizes the workspace).
  *   out           device fp32 [batch, num_q_heads, head_dim], 16-byte aligned.
  *   workspace     device, >= kvq_decode_workspace_bytes(...) bytes, 256-byte aligned.
- *                 Its first 4 bytes are the status word; the rest holds split-KV
- *                 partial results and one counter per (sequence, kv head).  Zero the
- *                 whole workspace after allocating it.  The counters return to zero at
- *                 the end of every call, so the workspace can serve any number of calls
- *                 of the same (cfg, batch, num_q_heads, max_len); zero it again before
- *                 using it for another shape.
+ *                 Its first 4 bytes are the status word (zero it before the first call
+ *                 to read flags); the rest holds the split-KV partial results of the
+ *                 call, written before they are read, so it needs no initialisation and
+ *                 can serve any call whose shape needs no more bytes.
  * num_q_heads must be a multiple of num_kv_heads with a ratio of at most 8.
- * Launch overlap: the kernel is launched with programmatic dependent launch.  While the
- * kernel ahead of it on the stream is still running (only possible when that kernel
- * has signalled its dependents early, which this library's kernels do), it may already
- * read q, block_table and seq_lens; it reads the pool and touches out and the
- * workspace only after that kernel has finished.  This library's kernels never write
- * q, block_table or seq_lens.
+ * Two kernels run: the decode grid, which leaves one partial result per warp and
+ * segment in the workspace, and a combine grid that merges them into out.
+ * Launch overlap: both are launched with programmatic dependent launch.  While the
+ * kernel ahead of the decode grid on the stream is still running (only possible when
+ * that kernel has signalled its dependents early, which this library's kernels do),
+ * the decode grid may already read q, block_table and seq_lens; it reads the pool and
+ * touches the workspace only after that kernel has finished, and out is written by
+ * the combine grid after the decode grid has finished.  This library's kernels never
+ * write q, block_table or seq_lens.
  * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE or KVQ_ECUDA.
  */
 int kvq_decode_attention(const kvq_cache_config *cfg, const void *pool, const void *q,

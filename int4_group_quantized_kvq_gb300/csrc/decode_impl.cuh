@@ -21,7 +21,7 @@
 //    contiguous slice of the flattened (sequence, head group, page) units, so ragged
 //    lengths and small batches keep every SM busy.  The CTA's four warps take the units
 //    of its slice in turn (warp k: units k, k + 4, ...), so they move through the same
-//    (sequence, head group) segments together.
+//    (sequence, head group) segments at about the same time.
 //  * Each warp owns a ring of `stages` unit buffers in shared memory, filled by 1-D
 //    bulk copies (the TMA engine, cp.async.bulk) that complete on per-stage mbarriers.
 //    Waits are bounded in time.
@@ -45,14 +45,15 @@
 //    only the weights are exchanged (four shuffles per chunk and V group).  With HK = 1
 //    chunks are taken two at a time (two 16-token pages, or two chunks of a larger
 //    page): the two score chains interleave and one softmax reduction covers both.
-//  * Split combine, fused.  At the end of each segment the four warps of a CTA merge
-//    their parts in shared memory (each writes its part into the ring stage it has just
-//    consumed, whose refill waits for the merge).  A segment inside one CTA's slice is
-//    written out directly; otherwise the CTA writes a partial (running max, running
-//    sum, unnormalised output) and bumps the segment's counter (fence + atomic add; the
-//    result is looked at when the CTA next reaches a segment end, so the round trip
-//    overlaps streaming).  The CTA that counted last merges all partials of the
-//    segment with its 128 threads, and sets the counter back to zero for the next call.
+//  * Split combine.  At the end of each segment (sequence, head group) every warp writes
+//    its own partial (running max, running sum and unnormalised output per slot) to the
+//    workspace, staged through the ring stage it has just consumed; no warp waits for
+//    another, and nothing is counted or fenced on the streaming path, so a warp that
+//    finishes its part of a segment early keeps its copies in flight.  A second, small
+//    kernel, launched behind this one with programmatic dependent launch, merges the
+//    partials of each (sequence, query head) row and writes the output.  The two q
+//    buffers of a CTA are reused once every warp has taken its fragments out (an
+//    mbarrier with one arrival per warp), the only point where warps of a CTA meet.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -68,7 +69,6 @@
 namespace kvq {
 namespace decode {
 
-constexpr int kMaxWarps = 16;                     // most warps per CTA
 constexpr uint64_t kWaitLimitNs = 250000000ull;   // a page copy that takes 250 ms has failed
 
 // Warps per CTA, and resident CTAs per SM the register budget is tuned for: 3 (up to 168
@@ -80,15 +80,9 @@ constexpr int min_ctas() { return HS == 1 ? 3 : 2; }
 
 // CTA-wide bookkeeping in shared memory.
 struct CtaCtl {
-    int buf[kMaxWarps];  // ring stage holding warp w's part at a segment end (-1: none)
-    int pend_valid;      // a partial of segment (pend_b, pend_hg) has been counted ...
-    int pend_b, pend_hg;
-    int pend_target;     // ... out of pend_target, and the count came back as pend_arrived
-    int pend_arrived;
-    int ndm;             // segments this CTA counted last and merges after streaming (<= 2:
-    int dm_b[2], dm_hg[2];  // only the first and the last segment of a slice are shared)
-    int pad;
     uint64_t qbar[2];    // completion of the bulk copies of q rows into the two q buffers
+    uint64_t qfree[2];   // every warp has taken its q fragments out of the buffer
+    uint64_t pad[12];
 };
 static_assert(sizeof(CtaCtl) == 128, "the planner reserves 128 bytes");
 constexpr int kQBufBytes = 2 * 8 * 128 * 2;  // two buffers of up to 8 query-head rows of d = 128 fp16
@@ -98,10 +92,9 @@ struct KParams {
     const __half* q;
     const int32_t* block_table;
     const int32_t* seq_lens;
-    float* out;
-    float* ws_ml;       // CTA partials (one per CTA and segment it touches): (max, sum) per slot
+    float* ws_ml;       // warp partials (one per warp and segment its CTA touches): (max, sum) per slot
     float* ws_o;        //   ... and unnormalised outputs per slot
-    int32_t* counters;  // per segment; zero between calls
+    int32_t* ws_pre;    // the pages prefix pre[0..B], for the combine kernel
     uint32_t* status;
     int32_t B, Hq, Hkv, Hg, r, ns;  // Hg = Hkv / HK head groups; ns = HK * r query heads per unit
     int32_t P, num_pages, max_blocks, block_bytes, unit_bytes, stages;
@@ -115,6 +108,12 @@ struct KParams {
     uint8_t* pool_w;
     int32_t lg_p, lg_lk, lg_lv;  // log2 of P, of the K and of the V group width in 8-value lanes
 };
+
+// Pages sequence b spans for a length of L positions (negative: 0), at most max_blocks.
+__device__ __forceinline__ int seq_pages(int L, int P, int max_blocks) {
+    const long long n = (static_cast<long long>(L < 0 ? 0 : L) + P - 1) / P;
+    return static_cast<int>(n < max_blocks ? n : max_blocks);
+}
 
 // Exclusive prefix sums of pages per sequence into pre[0..B], the lengths (negative ones
 // as 0) into lens[0..B-1] and the append positions (-1: none) into aps[0..B-1]; run by
@@ -179,96 +178,6 @@ __device__ __forceinline__ long long slice_start(long long w, long long U, long 
 
 // The slice containing unit u (the largest w with slice_start(w) <= u).
 __device__ __forceinline__ long long slice_of(long long u, long long U, long long W) { return ((u + 1) * W - 1) / U; }
-
-// Slot of the CTA partial that CTA k writes for segment seg, or -1 when CTA k's slice is
-// empty.  k + seg is unique: if CTA k touches segment s and CTA k - 1 touches s + 1,
-// CTA k - 1 would hold a later unit than CTA k, which ordered slices rule out.
-__device__ __forceinline__ long long piece_index(long long k, long long seg, long long U, long long C) {
-    return (U >= C || slice_start(k, U, C) < slice_start(k + 1, U, C)) ? k + seg : -1;
-}
-
-// Merge the CTA partials of segment (b, hg), spread over the slices of CTAs cf..cl, into
-// the normalised output; run by all threads of the CTA that counted last.  Warp w takes
-// slots w and w + 4, lane l dimensions 4l .. 4l + 3.  First the lanes find the largest
-// running maximum M among the partials (lane k reads partials k, k + 32, ...), then the
-// outputs are folded NB partials at a time with weights 2^(m_k - M), into four
-// independent accumulators so that consecutive partials do not wait on each other.
-template <int D, int NB>
-__device__ __forceinline__ void merge_partials(const KParams& p, int b, int hg, long long cf, long long cl,
-                                               long long U, long long C) {
-    static_assert(NB % 4 == 0, "four accumulators");
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const long long seg = static_cast<long long>(b) * p.Hg + hg;
-    const int n = static_cast<int>(cl - cf + 1);
-    const bool dense = U >= C;  // every CTA slice is non-empty: partial k sits at cf + k + seg
-    __threadfence();  // the partials counted before this CTA are visible
-    const int nw = blockDim.x >> 5;
-    for (int sl = warp; sl < p.ns; sl += nw) {
-        const float* ml0 = p.ws_ml + ((cf + seg) * p.ns + sl) * 2;
-        const float* o0 = p.ws_o + ((cf + seg) * p.ns + sl) * D + 4 * lane;
-        const long long stride_ml = static_cast<long long>(p.ns) * 2;
-        const long long stride_o = static_cast<long long>(p.ns) * D;
-        auto present = [&](int k) { return dense || piece_index(cf + k, seg, U, C) >= 0; };
-        float M = -INFINITY;
-        for (int k = lane; k < n; k += 32)
-            if (present(k)) M = fmaxf(M, __ldcg(ml0 + k * stride_ml));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float L = 0.f;
-        float4 acc[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) acc[a] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k0 = 0; k0 < n; k0 += NB) {
-            float2 ml[NB];
-            float4 ov[NB];
-#pragma unroll
-            for (int kk = 0; kk < NB; ++kk) {
-                const int k = k0 + kk;
-                if (k < n && present(k)) {
-                    ml[kk] = __ldcg(reinterpret_cast<const float2*>(ml0 + k * stride_ml));
-                    ov[kk] = __ldcg(reinterpret_cast<const float4*>(o0 + k * stride_o));
-                } else {
-                    ml[kk] = make_float2(-INFINITY, 0.f);
-                    ov[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-            for (int kk = 0; kk < NB; ++kk) {
-                const float f = fast_exp2(ml[kk].x - M);
-                L = fmaf(f, ml[kk].y, L);
-                float4& A = acc[kk & 3];
-                A.x = fmaf(f, ov[kk].x, A.x);
-                A.y = fmaf(f, ov[kk].y, A.y);
-                A.z = fmaf(f, ov[kk].z, A.z);
-                A.w = fmaf(f, ov[kk].w, A.w);
-            }
-        }
-        const float inv = 1.f / L;
-        const int hq = hg * p.ns + sl;
-        reinterpret_cast<float4*>(p.out + (static_cast<long long>(b) * p.Hq + hq) * D)[lane] =
-            make_float4((acc[0].x + acc[1].x + acc[2].x + acc[3].x) * inv,
-                        (acc[0].y + acc[1].y + acc[2].y + acc[3].y) * inv,
-                        (acc[0].z + acc[1].z + acc[2].z + acc[3].z) * inv,
-                        (acc[0].w + acc[1].w + acc[2].w + acc[3].w) * inv);
-    }
-    if (threadIdx.x == 0) p.counters[seg] = 0;
-}
-
-// The merge, run after the CTA has streamed its slice (every register is free then).
-template <int D>
-__device__ __noinline__ void merge_segment_final(const KParams& p, int b, int hg, long long cf, long long cl,
-                                                 long long U, long long C) {
-    merge_partials<D, 16>(p, b, hg, cf, cl, U, C);
-}
-
-// Number of non-empty CTA slices among cf..cl (all of them when no slice is empty).
-__device__ __forceinline__ int pieces_between(long long cf, long long cl, long long U, long long C) {
-    if (U >= C) return static_cast<int>(cl - cf + 1);
-    int n = 0;
-    for (long long k = cf; k <= cl; ++k) n += slice_start(k, U, C) < slice_start(k + 1, U, C) ? 1 : 0;
-    return n;
-}
 
 // The chunks of one step: chunk X is chunk chk[X] of the unit buffer blk[X] and holds
 // sequence positions t0[X] .. t0[X] + 15; a chunk with !live[X] is masked out whole.
@@ -365,11 +274,12 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     // running.  Only the read-only inputs are read before it: seq_lens, the block table and
     // q.  The pool (written by quantize-append), the output and the workspace come after.
     if (warp == 0) page_prefix(p, pre, lens, aps, lane);
+    const uint32_t qfree0 = smem_u32(&ctl->qfree[0]);
     if (threadIdx.x == 0) {
-        ctl->pend_valid = 0;
-        ctl->ndm = 0;
         mbar_init(qbar0, 1);
         mbar_init(qbar0 + 8, 1);
+        mbar_init(qfree0, kWarps);
+        mbar_init(qfree0 + 8, kWarps);
         fence_mbar_init();
     }
     __syncthreads();
@@ -407,17 +317,16 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         }
     };
 
+    // the combine kernel finds each segment's partials from the pages prefix
+    auto publish_prefix = [&]() {
+        if (cta == 0 && warp == 0)
+            for (int i = lane; i <= p.B; i += 32) p.ws_pre[i] = pre[i];
+    };
     if (c0 >= c1) {
-        // no units: only the zeros of empty sequences and appends nobody streams, after the
-        // kernel ahead has finished
+        // no units: only appends nobody streams, after the kernel ahead has finished
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        publish_prefix();
         orphan_appends();
-        for (long long bb = cta * kWarps + warp; bb < p.B; bb += C * kWarps) {
-            if (pre[bb + 1] == pre[bb]) {
-                float4* z4 = reinterpret_cast<float4*>(p.out + bb * p.Hq * D);
-                for (int i = lane; i < p.Hq * D / 4; i += 32) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
         return;  // the whole CTA leaves together
     }
     const int span = static_cast<int>(c1 - c0);
@@ -471,14 +380,8 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
 
     // ---- from here on the pool, the output and the workspace are used ----
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    publish_prefix();
     orphan_appends();
-    // sequences with no positions get zeros (no slice visits them)
-    for (long long bb = cta * kWarps + warp; bb < p.B; bb += C * kWarps) {
-        if (pre[bb + 1] == pre[bb]) {
-            float4* z4 = reinterpret_cast<float4*>(p.out + bb * p.Hq * D);
-            for (int i = lane; i < p.Hq * D / 4; i += 32) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
     {
         const int pro = nm < stages ? nm : stages;
         for (int k = 0; k < pro; ++k) issue(k, k);
@@ -736,7 +639,6 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     bool failed = false;  // a copy did not arrive in time: stop waiting, keep the barriers
     int f_st = 0, f_out = 0;  // where consumption stopped, and the copies still in flight then
     uint32_t f_par = 0;
-    int pend_arrived = 0; // thread 0: what the last counting atomic returned
     const bool p16 = p.P == 16;
 
     // q rows of a segment go to shared memory by a bulk copy issued one segment ahead
@@ -768,12 +670,15 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         const int cnt = fu < ue ? static_cast<int>((ue - fu + kWarps - 1) / kWarps) : 0;
         const int pg0 = static_cast<int>(fu - sfirst);
         int last_st = -1;   // stage of the last unit consumed in this segment
-        int held[2] = {-1, -1}, held_i[2] = {0, 0};  // stages whose refill waits for the merge
+        int held[2] = {-1, -1}, held_i[2] = {0, 0};  // stages whose refill waits for the partial
 
-        // the next segment's q rows start moving now
+        // the next segment's q rows start moving now, into the buffer of segment segk - 1
+        // once every warp has taken its fragments out of it
         if (threadIdx.x == 0 && sfirst + np < c1) {
             int nb = b, nhg = hg;
             next_seg(nb, nhg);
+            if (segk >= 1 && !mbar_wait(qfree0 + 8 * ((segk - 1) & 1), ((segk - 1) >> 1) & 1, kWaitLimitNs))
+                raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
             issue_q(nb, nhg, segk + 1);
         }
         if (cnt > 0) {
@@ -809,6 +714,10 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                 }
             }
         }
+        // this warp is done with the segment's q buffer (a warp with units here has waited
+        // for its copy, so the buffer is only reused after the copy has landed)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qfree0 + 8 * (segk & 1));
 #pragma unroll
         for (int s = 0; s < HS; ++s) {
             m[s] = -INFINITY;
@@ -903,116 +812,57 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
             j += n;
         }
 
-        // ---- segment end: the four warps merge their parts in shared memory ----
-        const long long seg = static_cast<long long>(b) * p.Hg + hg;
-        const long long cf = slice_of(sfirst, U, C);
-        const long long cl = slice_of(sfirst + np - 1, U, C);
-        const bool whole = cf == cl;
-        const bool mine = cnt > 0 && !failed;
-        float lt[HS];
+        // ---- segment end: this warp's part of the segment goes out as one partial ----
+        // (running max and sum per slot, unnormalised output per slot), at index
+        // kWarps * (CTA + segment) + warp; the combine kernel merges them.  No other warp
+        // is waited for, so a warp that reaches the end early keeps streaming.
+        {
+            const long long seg = static_cast<long long>(b) * p.Hg + hg;
+            const long long piece = static_cast<long long>(kWarps) * (cta + seg) + warp;
+            float lt[HS];
 #pragma unroll
-        for (int s = 0; s < HS; ++s) {
-            lt[s] = l[s];
-            lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 4);
-            lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 8);
-            lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 16);
-        }
-        if (lane == 0) ctl->buf[warp] = mine ? last_st : -1;
-        if (threadIdx.x == 0 && ctl->pend_valid) ctl->pend_arrived = pend_arrived;
-        float* mybuf = reinterpret_cast<float*>(ring + (mine ? last_st : 0) * ubytes);
-        bool pend_seen = false;
-#pragma unroll
-        for (int s = 0; s < HS; ++s) {
-            if (mine) {
-                // o (hi + lo columns summed) of slot c + 4s as [4][D], then (max, sum) pairs
-#pragma unroll
-                for (int R = 0; R < NGV; ++R)
-#pragma unroll
-                    for (int jb = 0; jb < VB; ++jb) {
-                        const int mt = R * VB + jb;
-                        const int dd = 2 * (R * (GV / 2) + g * VB + jb);
-                        *reinterpret_cast<float2*>(mybuf + c * D + dd) =
-                            make_float2(o[mt][s][0] + o[mt][s][1], o[mt][s][2] + o[mt][s][3]);
-                    }
-                if (g == 0) *reinterpret_cast<float2*>(mybuf + 4 * D + 2 * c) = make_float2(m[s], lt[s]);
-                fence_proxy_async_smem();  // the stage is refilled by the bulk copy engine later
+            for (int s = 0; s < HS; ++s) {
+                lt[s] = l[s];
+                lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 4);
+                lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 8);
+                lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 16);
             }
-            __syncthreads();
-            // the pending record is only rewritten after this segment end's last barrier
-            if (s == 0) pend_seen = ctl->pend_valid != 0;
-            const int sl = warp + 4 * s;  // warps 0..3 merge the four slots of this round
-            if (warp < 4 && sl < p.ns) {
-                float M = -INFINITY;
+            if (cnt > 0 && !failed) {
+                // staged through the ring stage just consumed ([4][D] floats per round of
+                // four slots), then written out in rows of 512 bytes
+                float* sbuf = reinterpret_cast<float*>(ring + last_st * ubytes);
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const int bs = ctl->buf[w];
-                    if (bs >= 0) {
-                        const float* wb = reinterpret_cast<const float*>(smem + (static_cast<size_t>(w) * stages + bs) * ubytes);
-                        M = fmaxf(M, wb[4 * D + 2 * warp]);
-                    }
-                }
-                float Ls = 0.f;
-                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int s = 0; s < HS; ++s) {
+                    const int nsr = min(4, p.ns - 4 * s);  // slots in this round
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const int bs = ctl->buf[w];
-                    if (bs >= 0) {
-                        const float* wb = reinterpret_cast<const float*>(smem + (static_cast<size_t>(w) * stages + bs) * ubytes);
-                        const float2 ml = *reinterpret_cast<const float2*>(wb + 4 * D + 2 * warp);
-                        const float4 ov = *reinterpret_cast<const float4*>(wb + warp * D + 4 * lane);
-                        const float f = fast_exp2(ml.x - M);
-                        Ls = fmaf(f, ml.y, Ls);
-                        O.x = fmaf(f, ov.x, O.x);
-                        O.y = fmaf(f, ov.y, O.y);
-                        O.z = fmaf(f, ov.z, O.z);
-                        O.w = fmaf(f, ov.w, O.w);
-                    }
+                    for (int R = 0; R < NGV; ++R)
+#pragma unroll
+                        for (int jb = 0; jb < VB; ++jb) {
+                            const int mt = R * VB + jb;
+                            const int dd = 2 * (R * (GV / 2) + g * VB + jb);
+                            *reinterpret_cast<float2*>(sbuf + c * D + dd) =
+                                make_float2(o[mt][s][0] + o[mt][s][1], o[mt][s][2] + o[mt][s][3]);
+                        }
+                    __syncwarp();
+                    for (int k = 0; k < nsr; ++k)
+                        reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + 4 * s + k) * D)[lane] =
+                            reinterpret_cast<const float4*>(sbuf + k * D)[lane];
+                    if (g == 0 && c < nsr)
+                        *reinterpret_cast<float2*>(p.ws_ml + (piece * p.ns + 4 * s + c) * 2) = make_float2(m[s], lt[s]);
+                    __syncwarp();
                 }
-                const int hq = hg * p.ns + sl;
-                if (whole) {
-                    const float inv = 1.f / Ls;
-                    reinterpret_cast<float4*>(p.out + (static_cast<long long>(b) * p.Hq + hq) * D)[lane] =
-                        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
-                } else {
-                    const long long piece = cta + seg;
-                    if (lane == 0) *reinterpret_cast<float2*>(p.ws_ml + (piece * p.ns + sl) * 2) = make_float2(M, Ls);
-                    reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + sl) * D)[lane] = O;
-                }
+                fence_proxy_async_smem();  // the stage is refilled by the bulk copy engine next
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    if (held[k] >= 0 && held_i[k] < nm) issue(held_i[k], held[k]);
+            } else {
+                // no units of this segment here (or a failed wait): an empty partial
+                if (lane < p.ns)
+                    *reinterpret_cast<float2*>(p.ws_ml + (piece * p.ns + lane) * 2) = make_float2(-INFINITY, 0.f);
+                for (int k = 0; k < p.ns; ++k)
+                    reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + k) * D)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            __syncthreads();
-        }
-        // the stages held for the merge can be refilled now
-        if (mine) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                if (held[k] >= 0 && held_i[k] < nm) issue(held_i[k], held[k]);
-        }
-
-        // ---- the previous count has had time to come back: merge if this CTA was last ----
-        if (pend_seen) {
-            const int arrived = ctl->pend_arrived;
-            const int target = ctl->pend_target;
-            if (threadIdx.x == 0) {
-                if (arrived >= target) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
-                if (arrived == target - 1 && ctl->ndm < 2) {  // this CTA merges the segment later
-                    ctl->dm_b[ctl->ndm] = ctl->pend_b;
-                    ctl->dm_hg[ctl->ndm] = ctl->pend_hg;
-                    ++ctl->ndm;
-                }
-            }
-            __syncthreads();  // everyone has read the pending record
-            if (threadIdx.x == 0) ctl->pend_valid = 0;
-        }
-        // ---- count this CTA's partial; the result is looked at later ----
-        if (!whole && threadIdx.x == 0) {
-            // the CTA's partial, written by several threads before the barrier above, is
-            // published by this thread's fence ahead of the count
-            __threadfence();
-            pend_arrived = atomicAdd(p.counters + seg, 1);
-            ctl->pend_valid = 1;
-            ctl->pend_b = b;
-            ctl->pend_hg = hg;
-            ctl->pend_target = pieces_between(cf, cl, U, C);
         }
 
         // ---- next segment ----
@@ -1026,26 +876,6 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         }
         if (b < p.B) np = pre[b + 1] - pre[b];
         else break;
-    }
-
-    // ---- the last count, then the merges of the segments this CTA counted last ----
-    __syncthreads();
-    if (threadIdx.x == 0 && ctl->pend_valid) {
-        const int arrived = pend_arrived;
-        const int target = ctl->pend_target;
-        if (arrived >= target) raise_flag(p.status, KVQ_FLAG_STALE_WORKSPACE);
-        if (arrived == target - 1 && ctl->ndm < 2) {
-            ctl->dm_b[ctl->ndm] = ctl->pend_b;
-            ctl->dm_hg[ctl->ndm] = ctl->pend_hg;
-            ++ctl->ndm;
-        }
-    }
-    __syncthreads();
-    for (int k = 0; k < ctl->ndm; ++k) {
-        const int pb = ctl->dm_b[k], ph = ctl->dm_hg[k];
-        const int pnp = pre[pb + 1] - pre[pb];
-        const long long pf = static_cast<long long>(p.Hg) * pre[pb] + static_cast<long long>(ph) * pnp;
-        merge_segment_final<D>(p, pb, ph, slice_of(pf, U, C), slice_of(pf + pnp - 1, U, C), U, C);
     }
 
     // ---- no q copy may still be landing when the CTA leaves (they all have, unless a
@@ -1065,6 +895,182 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                 par ^= 1u;
             }
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Combine: the warp partials of each (sequence, query head) row into its output.
+// ---------------------------------------------------------------------------
+struct CParams {
+    const float* ws_ml;
+    const float* ws_o;
+    const int32_t* ws_pre;
+    const int32_t* seq_lens;
+    float* out;
+    int32_t B, Hq, Hg, ns;
+    int32_t P, max_blocks;
+    int32_t C;  // CTAs of the decode grid
+    int32_t W;  // warps per decode CTA: partials per CTA and segment
+};
+
+constexpr int kCombineMaxWarps = 16;
+constexpr int kCombineBatch = 8;      // partials loaded together by a warp
+constexpr int kCombineLocalB = 256;   // up to this batch the row metadata is computed before the wait
+
+// One CTA per output row (b, hq).  The row's partials sit at W * (cf + seg) + j for
+// j < W * (cl - cf + 1), where CTAs cf..cl hold the units of segment seg = (b, hq / ns);
+// when some CTA slices are empty (fewer units than CTAs) their partials do not exist.
+// Warp w of the CTA takes partials w, w + nw, ..., eight at a time, keeping a running
+// maximum M and sum L and an unnormalised output (lane l: dimensions 4l .. 4l + 3); the
+// warps' results are then merged with weights 2^(M_w - max M).  Sequences without
+// positions have no partials and get zeros.  This is the split-KV combine of flash
+// decoding: out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
+template <int D>
+__global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams p) {
+    static_assert(D == 128, "one float4 per lane");
+    // the next decode call may start its set-up; it waits for this grid before it
+    // touches the workspace
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ float s_m[kCombineMaxWarps], s_l[kCombineMaxWarps];
+    __shared__ float4 s_o[kCombineMaxWarps][D / 4];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const int b = static_cast<int>(blockIdx.x / p.Hq);
+    const int hq = static_cast<int>(blockIdx.x - static_cast<long long>(b) * p.Hq);
+    const int hg = hq / p.ns;
+    const int sl = hq - hg * p.ns;
+
+    // The row's pages prefix: for small batches from seq_lens (a read-only input) while
+    // the decode grid still runs; else from the prefix the decode grid publishes.
+    __shared__ int s_red[2][kCombineMaxWarps];
+    int pb = 0, np = 0, tot = 0;
+    const bool local = p.B <= kCombineLocalB;
+    if (local) {
+        int before = 0, all = 0;
+        for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+            const int n_i = seq_pages(p.seq_lens[i], p.P, p.max_blocks);
+            all += n_i;
+            if (i < b) before += n_i;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            before += __shfl_xor_sync(0xffffffffu, before, off);
+            all += __shfl_xor_sync(0xffffffffu, all, off);
+        }
+        if (lane == 0) {
+            s_red[0][warp] = before;
+            s_red[1][warp] = all;
+        }
+        __syncthreads();
+        for (int w = 0; w < nw; ++w) {
+            pb += s_red[0][w];
+            tot += s_red[1][w];
+        }
+        np = seq_pages(p.seq_lens[b], p.P, p.max_blocks);
+    }
+    auto row_range = [&](int pb_, int np_, int tot_, long long& cf_, long long& base_, long long& U_) {
+        U_ = static_cast<long long>(p.Hg) * tot_;
+        const long long sf = static_cast<long long>(p.Hg) * pb_ + static_cast<long long>(hg) * np_;
+        cf_ = slice_of(sf, U_, p.C);
+        const long long cl = slice_of(sf + np_ - 1, U_, p.C);
+        base_ = static_cast<long long>(p.W) * (cf_ + static_cast<long long>(b) * p.Hg + hg);
+        return p.W * static_cast<int>(cl - cf_ + 1);
+    };
+    int n = 0;
+    long long cf = 0, base = 0, U = 1;
+    if (local && np > 0) n = row_range(pb, np, tot, cf, base, U);
+
+    // the partials (and the published prefix) are written by the decode grid ahead of this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!local) {
+        pb = __ldcg(p.ws_pre + b);
+        np = __ldcg(p.ws_pre + b + 1) - pb;
+        tot = __ldcg(p.ws_pre + p.B);
+        if (np > 0) n = row_range(pb, np, tot, cf, base, U);
+    }
+    const bool dense = U >= p.C;  // every CTA slice holds units
+    const long long stride_ml = static_cast<long long>(p.ns) * 2;
+    const long long stride_o = static_cast<long long>(p.ns) * D;
+    const float* ml0 = p.ws_ml + (base * p.ns + sl) * 2;
+    const float* o0 = p.ws_o + (base * p.ns + sl) * D + 4 * lane;
+
+    float M = -INFINITY, L = 0.f;
+    float4 acc[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) acc[a] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = warp; j0 < n; j0 += kCombineBatch * nw) {
+        float2 ml[kCombineBatch];
+        float4 ov[kCombineBatch];
+#pragma unroll
+        for (int kk = 0; kk < kCombineBatch; ++kk) {
+            const int j = j0 + kk * nw;
+            bool have = j < n;
+            if (have && !dense) {
+                const long long k = cf + j / p.W;
+                have = slice_start(k, U, p.C) < slice_start(k + 1, U, p.C);
+            }
+            if (have) {
+                ml[kk] = __ldcg(reinterpret_cast<const float2*>(ml0 + j * stride_ml));
+                ov[kk] = __ldcg(reinterpret_cast<const float4*>(o0 + j * stride_o));
+            } else {
+                ml[kk] = make_float2(-INFINITY, 0.f);
+                ov[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float mb = M;
+#pragma unroll
+        for (int kk = 0; kk < kCombineBatch; ++kk) mb = fmaxf(mb, ml[kk].x);
+        if (mb == -INFINITY) continue;  // only empty partials so far
+        if (mb > M) {  // a larger running maximum: rescale what has been summed
+            const float f = fast_exp2(M - mb);
+            L *= f;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                acc[a].x *= f;
+                acc[a].y *= f;
+                acc[a].z *= f;
+                acc[a].w *= f;
+            }
+            M = mb;
+        }
+#pragma unroll
+        for (int kk = 0; kk < kCombineBatch; ++kk) {
+            const float f = fast_exp2(ml[kk].x - M);
+            L = fmaf(f, ml[kk].y, L);
+            float4& A = acc[kk & 3];
+            A.x = fmaf(f, ov[kk].x, A.x);
+            A.y = fmaf(f, ov[kk].y, A.y);
+            A.z = fmaf(f, ov[kk].z, A.z);
+            A.w = fmaf(f, ov[kk].w, A.w);
+        }
+    }
+    if (lane == 0) {
+        s_m[warp] = M;
+        s_l[warp] = L;
+    }
+    s_o[warp][lane] = make_float4(acc[0].x + acc[1].x + acc[2].x + acc[3].x, acc[0].y + acc[1].y + acc[2].y + acc[3].y,
+                                  acc[0].z + acc[1].z + acc[2].z + acc[3].z, acc[0].w + acc[1].w + acc[2].w + acc[3].w);
+    __syncthreads();
+    if (warp == 0) {
+        float Mx = -INFINITY;
+        for (int w = 0; w < nw; ++w) Mx = fmaxf(Mx, s_m[w]);
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        float Ls = 0.f;
+        if (Mx != -INFINITY) {
+            for (int w = 0; w < nw; ++w) {
+                const float f = fast_exp2(s_m[w] - Mx);
+                const float4 ow = s_o[w][lane];
+                Ls = fmaf(f, s_l[w], Ls);
+                O.x = fmaf(f, ow.x, O.x);
+                O.y = fmaf(f, ow.y, O.y);
+                O.z = fmaf(f, ow.z, O.z);
+                O.w = fmaf(f, ow.w, O.w);
+            }
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        reinterpret_cast<float4*>(p.out + (static_cast<long long>(b) * p.Hq + hq) * D)[lane] =
+            make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
     }
 }
 
@@ -1116,10 +1122,9 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     p.q = a.q;
     p.block_table = a.block_table;
     p.seq_lens = a.seq_lens;
-    p.out = a.out;
     p.ws_ml = reinterpret_cast<float*>(a.workspace + plan.ws_ml_offset);
     p.ws_o = reinterpret_cast<float*>(a.workspace + plan.ws_o_offset);
-    p.counters = reinterpret_cast<int32_t*>(a.workspace + plan.ws_cnt_offset);
+    p.ws_pre = reinterpret_cast<int32_t*>(a.workspace + plan.ws_pre_offset);
     p.status = reinterpret_cast<uint32_t*>(a.workspace);
     p.B = a.B;
     p.Hq = a.Hq;

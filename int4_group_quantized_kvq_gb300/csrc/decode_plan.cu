@@ -4,14 +4,15 @@
 // has its own kv head, Hkv is a multiple of 4 and pages hold 16 tokens, else HK = 1.
 // The grid is C CTAs of 4 warps: C is the number of CTAs the device keeps resident (SMs
 // x resident CTAs), reduced for small problems so that a warp gets at least two units;
-// every CTA
-// receives an equal contiguous slice of the flattened (sequence, head group, page)
-// units.  Each CTA writes at most one partial per segment (sequence, head group) its
-// slice touches, at index CTA + segment, which is unique (see piece_index in the
-// kernel).  So the workspace holds C + B * Hg partials of ns = HK * r query heads, each
-// (max, sum) plus d floats, and one split counter per segment.  The counters must be
-// zero when a call starts; each is reset by the CTA that consumes it, so they stay
-// zero from one call to the next while the workspace serves the same shape.
+// every CTA receives an equal contiguous slice of the flattened (sequence, head group,
+// page) units.  Each warp writes one partial per segment (sequence, head group) its
+// CTA's slice touches, at index 4 * (CTA + segment) + warp, which is unique (CTA +
+// segment is: if CTA k touches segment s and CTA k - 1 touches s + 1, CTA k - 1 would
+// hold a later unit than CTA k, which ordered slices rule out).  So the workspace holds
+// 4 * (C + B * Hg) partials of ns = HK * r query heads, each (max, sum) plus d floats,
+// and the pages prefix the decode grid publishes for the combine kernel, which runs
+// next with one CTA per (sequence, query head) row.  Nothing in the workspace carries
+// over from one call to the next.
 #include <algorithm>
 
 #include "kvq_internal.h"
@@ -24,6 +25,7 @@ cudaError_t decode_run_gk128(const DecodeArgs& a, const DecodePlan& plan, cudaSt
 int decode_occupancy_gk32(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk64(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk128(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+cudaError_t launch_combine(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 
 namespace {
 constexpr int kMaxStages = 8;           // deepest unit ring per warp
@@ -89,24 +91,34 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     const long long u_max = static_cast<long long>(hg) * a.B * pages_max;
     const long long ctas = std::min(c_max, std::max<long long>(1, u_max / (kMinUnitsPerWarp * kWarpsPerCta)));
     plan->ctas = static_cast<int32_t>(ctas);
+    // Combine CTA size from the most partials a row can have: a segment of pages_max
+    // units spans about pages_max / (u_max / ctas) + 2 CTA slices, 4 partials each; a
+    // warp folds 8 partials per round trip, so give it about 8 of them.
+    {
+        const long long per_cta = std::max<long long>(1, u_max / ctas);
+        const long long parts = kWarpsPerCta * (pages_max / per_cta + 2);
+        plan->combine_warps = parts <= 32 ? 4 : (parts <= 64 ? 8 : 16);
+    }
     plan->stages = stages;
     plan->smem_bytes = smem_for(stages);
-    const size_t pieces = static_cast<size_t>(ctas) + static_cast<size_t>(a.B) * hg;
-    const size_t segs = static_cast<size_t>(a.B) * hg;
-    plan->ws_cnt_offset = kAlign;  // the first 256 bytes hold the status word
-    plan->ws_ml_offset = plan->ws_cnt_offset + round_up(segs * sizeof(int32_t), kAlign);
+    const size_t pieces = static_cast<size_t>(kWarpsPerCta) * (static_cast<size_t>(ctas) + static_cast<size_t>(a.B) * hg);
+    plan->ws_pre_offset = kAlign;  // the first 256 bytes hold the status word
+    plan->ws_ml_offset = plan->ws_pre_offset + round_up((static_cast<size_t>(a.B) + 1) * sizeof(int32_t), kAlign);
     plan->ws_o_offset = plan->ws_ml_offset + round_up(pieces * ns * 2 * sizeof(float), kAlign);
     plan->ws_bytes = plan->ws_o_offset + round_up(pieces * ns * a.L.d * sizeof(float), kAlign);
     return cudaSuccess;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
+    cudaError_t e;
     switch (a.L.Gk) {
-        case 32: return decode_run_gk32(a, plan, stream);
-        case 64: return decode_run_gk64(a, plan, stream);
-        case 128: return decode_run_gk128(a, plan, stream);
+        case 32: e = decode_run_gk32(a, plan, stream); break;
+        case 64: e = decode_run_gk64(a, plan, stream); break;
+        case 128: e = decode_run_gk128(a, plan, stream); break;
         default: return cudaErrorInvalidValue;
     }
+    if (e != cudaSuccess) return e;
+    return launch_combine(a, plan, stream);
 }
 
 }  // namespace kvq

@@ -369,9 +369,8 @@ extern "C" int kvq_decode_attention_noalloc(const kvq_cache_config* cfg, const v
     e = noalloc_scratch(&scratch);
     if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention_noalloc scratch lookup");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // The status word and the split counters must start each call at zero.  The array
-    // serves every shape, so a counter slot of this call may hold a partial result of an
-    // earlier call with another shape: clear both (the partial results need no clearing).
+    // The status word must start each call at zero (the partial results and the pages
+    // prefix behind it are written before they are read).
     e = cudaMemsetAsync(scratch, 0, plan.ws_ml_offset, s);
     if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention_noalloc scratch clear");
     a.workspace = static_cast<uint8_t*>(scratch);

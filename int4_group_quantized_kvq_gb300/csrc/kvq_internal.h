@@ -87,9 +87,10 @@ struct DecodePlan {
     int32_t ctas;         // CTAs of the persistent grid (4 warps each)
     int32_t stages;       // bulk-copy ring depth per warp, in units
     size_t smem_bytes;    // dynamic shared memory per CTA
-    size_t ws_cnt_offset; // per-(sequence, head group) split counters
-    size_t ws_ml_offset;  // (max, sum) of the CTA partials
-    size_t ws_o_offset;   // unnormalised outputs of the CTA partials
+    int32_t combine_warps; // warps per CTA of the combine kernel (one CTA per output row)
+    size_t ws_pre_offset; // pages prefix per sequence, published by the decode grid
+    size_t ws_ml_offset;  // (max, sum) of the warp partials
+    size_t ws_o_offset;   // unnormalised outputs of the warp partials
     size_t ws_bytes;      // total workspace bytes
 };
 

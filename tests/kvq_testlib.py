@@ -84,7 +84,7 @@ class Case:
                                        np.array(self.lens, np.int32), self.scale)
 
 
-def gpu_decode(kvq, case: Case, pool_gpu: torch.Tensor, max_len: int | None = None):
+def gpu_decode(kvq, case: Case, pool_gpu: torch.Tensor, max_len: int | None = None, ws: torch.Tensor | None = None):
     cfg = case.cfg(kvq)
     dev = pool_gpu.device
     q = case.q.to(dev)
@@ -92,7 +92,8 @@ def gpu_decode(kvq, case: Case, pool_gpu: torch.Tensor, max_len: int | None = No
     sl = torch.tensor(case.lens, dtype=torch.int32, device=dev)
     ml = max(case.lens) if max_len is None else max_len
     out = torch.full((case.B, case.Hq, case.d), float("nan"), dtype=torch.float32, device=dev)
-    ws = kvq.new_workspace(cfg, case.B, case.Hq, ml, device=dev)
+    if ws is None:
+        ws = kvq.new_workspace(cfg, case.B, case.Hq, ml, device=dev)
     kvq.kvq_decode_attention(cfg, pool_gpu, q, bt, sl, ml, case.scale, out, ws)
     flags = kvq.kvq_read_status(ws)
     return out.cpu().numpy(), flags

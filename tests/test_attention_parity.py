@@ -102,3 +102,28 @@ def test_repeated_calls_are_deterministic(kvq):
     a, _ = gpu_decode(kvq, case, pool)
     b, _ = gpu_decode(kvq, case, pool)
     assert np.array_equal(a, b)
+
+
+def test_large_batch_published_prefix(kvq):
+    # more than 256 sequences: the combine reads the pages prefix the decode grid publishes
+    # instead of summing seq_lens itself; empty sequences among them get zeros
+    rng = np.random.default_rng(19)
+    lens = rng.integers(0, 90, size=300).tolist()
+    lens[:3] = [0, 1, 17]
+    _run(kvq, Case(300, 4, 2, 128, lens, seed=19))
+
+
+def test_workspace_reused_across_shapes_without_clearing(kvq):
+    # nothing in the workspace carries over between calls: one buffer, filled with garbage
+    # once, serves calls of three shapes in turn
+    cases = [Case(6, 16, 4, 128, [900, 17, 400, 1, 256, 333], seed=20), Case(2, 8, 8, 128, [70, 300], seed=21),
+             Case(1, 32, 8, 128, [5000], seed=22)]
+    nbytes = max(kvq.kvq_decode_workspace_bytes(c.cfg(kvq), c.B, c.Hq, max(c.lens)) for c in cases)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    ws[:256].zero_()  # the status word
+    for case in cases:
+        pool_np = case.oracle_pool()
+        ref = case.oracle_attention(pool_np)
+        got, flags = gpu_decode(kvq, case, torch.from_numpy(pool_np).cuda(), ws=ws)
+        assert flags == 0
+        assert_attention_close(got, ref, what=f"reused workspace B{case.B}")
