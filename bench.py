@@ -467,7 +467,8 @@ def run_kvq(args, world, rank, local):
         d2h = st.out_host.numel() * 4
         e2e = {"value": world * n_e2e * step_bytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": t_e2e / n_e2e * 1e3,
-               "how": "PagedKVCache.decode_step_host: one pinned H2D copy of q/K/V, the step (one launch), "
+               "how": "PagedKVCache.decode_step_host: one pinned H2D copy of q/K/V, the step (decode and combine "
+                      "launches), "
                       "one D2H copy of out, wall clock over all steps with a stream sync at the end"}
 
     if rank != 0:
@@ -495,8 +496,8 @@ def run_kvq(args, world, rank, local):
             "batch": wl.B, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.d,
             "context": wl.ctx[0] if len(set(wl.ctx)) == 1 else f"{min(wl.ctx)}..{max(wl.ctx)}",
             "attended_tokens": sum(wl.seq_lens), "page_size": wl.P, "group_k": wl.Gk, "group_v": wl.Gv,
-            "step": "quantize-append 1 token per sequence + decode attention, one kvq_decode_step launch "
-                    "(split-KV, fused append and combine)",
+            "step": "quantize-append 1 token per sequence + decode attention, one kvq_decode_step call: "
+                    "the split-KV decode grid with the append fused in, then the combine grid",
             "bytes_per_step": step_bytes,
             "l2": f"inputs larger than L2: {n_pools} rotated pool copies of {pool_bytes / 1e6:.1f} MB "
                   f"against a {l2 / 1e6:.0f} MB L2",

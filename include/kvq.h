@@ -155,7 +155,7 @@ int kvq_decode_attention(const kvq_cache_config *cfg, const void *pool, const vo
                          float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
 
 /*
- * One decode step in one launch: quantize-on-append of one new token per sequence
+ * One decode step in one call: quantize-on-append of one new token per sequence
  * (exactly as kvq_quantize_append with n_new = 1), then decode attention (exactly as
  * kvq_decode_attention) over the updated cache.  The warp that streams the page taking
  * a sequence's new token quantizes the token itself, writes it to the pool and uses

@@ -169,7 +169,7 @@ def kvq_decode_step(cfg: CacheConfig, pool: torch.Tensor, k_new: torch.Tensor, v
                     append_pos: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
                     max_len: int, softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
                     stream=None) -> None:
-    """One decode step in one launch: append k_new, v_new (fp16 [B, Hkv, d], or [B, 1, Hkv, d]) at
+    """One decode step in one call (the append fused into the decode grid): append k_new, v_new (fp16 [B, Hkv, d], or [B, 1, Hkv, d]) at
     append_pos (int32 [B], negative: none), then attend q (fp16 [B, Hq, d]) over seq_lens into out
     (fp32 [B, Hq, d])."""
     B, Hq = int(q.shape[0]), int(q.shape[1])

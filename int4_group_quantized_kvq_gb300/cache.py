@@ -5,7 +5,7 @@ nothing) around the C ABI calls of a decode step:
 
     quantize-on-append of the new token's K/V  ->  kvq_quantize_append
     decode attention over the packed cache      ->  kvq_decode_attention
-    both in one launch                          ->  kvq_decode_step
+    both in one call (append fused in)          ->  kvq_decode_step
 
 ``decode_step_host`` is the same step driven from pinned host buffers (``HostStaging``):
 the step's q, K and V are copied in with one transfer and the output copied back, on
@@ -51,7 +51,7 @@ class PagedKVCache:
 
     def decode_step(self, q, k_new, v_new, append_pos, seq_lens, out, stream=None) -> None:
         """Append one token per sequence at append_pos, then attend over seq_lens (which include it):
-        one launch of kvq_decode_step."""
+        one kvq_decode_step call."""
         B.kvq_decode_step(self.cfg, self.pool, k_new, v_new, append_pos, q, self.block_table, seq_lens, self.max_len,
                           self.softmax_scale, out, self.workspace, stream=stream)
 
@@ -62,8 +62,8 @@ class PagedKVCache:
 
     def decode_step_host(self, staging: "HostStaging", append_pos, seq_lens, stream=None) -> None:
         """The decode step from pinned host memory: one H2D copy of the step's q, K and V (staged
-        back to back), the step (one launch), one D2H copy of the output.  All asynchronous on
-        the step's stream."""
+        back to back), the step (the decode and combine launches), one D2H copy of the output.
+        All asynchronous on the step's stream."""
         s = torch.cuda.current_stream() if stream is None else stream
         with torch.cuda.stream(s):
             staging.dev.copy_(staging.host, non_blocking=True)
