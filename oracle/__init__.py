@@ -56,6 +56,10 @@ def lib() -> C.CDLL:
         L.kvq_oracle_decode_attention.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
                                                   C.c_int, C.c_int, C.c_double, C.c_void_p] + [C.c_int] * 6
         L.kvq_oracle_decode_attention.restype = C.c_int
+        L.kvq_oracle_decode_attention_window.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
+                                                         C.c_int, C.c_int, C.c_double, C.c_int, C.c_int,
+                                                         C.c_void_p] + [C.c_int] * 6
+        L.kvq_oracle_decode_attention_window.restype = C.c_int
         _lib = L
     return _lib
 
@@ -170,4 +174,20 @@ def decode_attention(L: Layout, pool: np.ndarray, q: np.ndarray, block_table: np
     rc = lib().kvq_oracle_decode_attention(_ptr(pool), _ptr(q), _ptr(bt), int(bt.shape[1]), _ptr(sl), B, Hq,
                                            float(softmax_scale), _ptr(out), *L.geom)
     _check(rc, "decode_attention")
+    return out
+
+
+def decode_attention_window(L: Layout, pool: np.ndarray, q: np.ndarray, block_table: np.ndarray,
+                            seq_lens: np.ndarray, softmax_scale: float, window: int, sinks: int) -> np.ndarray:
+    """fp64 decode attention over the quantized cache, restricted to the last `window` positions and
+    the first `sinks` ("AI inference tuning: KV Cache optimisation and memory management" section 3.2,
+    SlidingWindowAttention).  window <= 0: no window.  q: fp16 [B, Hq, d] -> fp64 [B, Hq, d]."""
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, _ = q.shape
+    out = np.zeros((B, Hq, L.d), dtype=np.float64)
+    rc = lib().kvq_oracle_decode_attention_window(_ptr(pool), _ptr(q), _ptr(bt), int(bt.shape[1]), _ptr(sl), B, Hq,
+                                                  float(softmax_scale), int(window), int(sinks), _ptr(out), *L.geom)
+    _check(rc, "decode_attention_window")
     return out

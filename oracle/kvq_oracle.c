@@ -341,3 +341,69 @@ int kvq_oracle_decode_attention(const uint8_t *pool, const uint16_t *q, const in
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention with a sliding window and sink tokens ([M] section 3.2, */
+/* SlidingWindowAttention): query position i sees keys max(0, i - W + 1)     */
+/* .. i and, when S > 0, the first S positions 0 .. S-1.  The decode query   */
+/* is the last position i = len - 1, so the visible keys are                 */
+/* [max(0, len - W), len) together with [0, min(S, len)).  window <= 0       */
+/* means no window (every position is visible, as in plain decode            */
+/* attention); sinks <= 0 means none.                                        */
+/* ------------------------------------------------------------------------ */
+static int visible_pos(int t, int len, int window, int sinks) {
+    if (window <= 0) return 1;
+    if (t >= len - window) return 1;
+    return sinks > 0 && t < sinks;
+}
+
+int kvq_oracle_decode_attention_window(const uint8_t *pool, const uint16_t *q, const int32_t *block_table,
+                                       int max_blocks, const int32_t *seq_lens, int B, int Hq, double softmax_scale,
+                                       int window, int sinks, double *out, int Hkv, int d, int P, int Gk, int Gv,
+                                       int num_pages) {
+    layout_t L;
+    if (make_layout(&L, Hkv, d, P, Gk, Gv, num_pages) || d > 256 || Hq <= 0 || Hq % Hkv) return ORACLE_EINVAL;
+    int n_rep = Hq / Hkv;
+    float rk[256], rv[256];
+    for (int b = 0; b < B; ++b) {
+        int len = seq_lens[b];
+        if (len < 0 || (len + P - 1) / P > max_blocks) return ORACLE_ERANGE;
+        for (int hq = 0; hq < Hq; ++hq) {
+            int kv = hq / n_rep;
+            const uint16_t *qrow = q + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            double *o = out + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            for (int i = 0; i < d; ++i) o[i] = 0.0;
+            if (len == 0) continue;
+            /* pass 1: logits of the visible positions and their maximum */
+            double zmax = -INFINITY;
+            for (int t = 0; t < len; ++t) {
+                if (!visible_pos(t, len, window, sinks)) continue;
+                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+                if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+                uint8_t *blk = block_ptr(&L, (uint8_t *)pool, page, kv);
+                dequant_row(k_codes_row(&L, blk, t % P), k_scales_row(&L, blk, t % P), d, Gk, rk);
+                double z = 0.0;
+                for (int i = 0; i < d; ++i) z += kvq_oracle_f16_to_f64(qrow[i]) * (double)rk[i];
+                z *= softmax_scale;
+                if (z > zmax) zmax = z;
+            }
+            /* pass 2: softmax weights over the visible positions and the weighted sum of values */
+            double l = 0.0;
+            for (int t = 0; t < len; ++t) {
+                if (!visible_pos(t, len, window, sinks)) continue;
+                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+                uint8_t *blk = block_ptr(&L, (uint8_t *)pool, page, kv);
+                dequant_row(k_codes_row(&L, blk, t % P), k_scales_row(&L, blk, t % P), d, Gk, rk);
+                dequant_row(v_codes_row(&L, blk, t % P), v_scales_row(&L, blk, t % P), d, Gv, rv);
+                double z = 0.0;
+                for (int i = 0; i < d; ++i) z += kvq_oracle_f16_to_f64(qrow[i]) * (double)rk[i];
+                z *= softmax_scale;
+                double w = exp(z - zmax);
+                l += w;
+                for (int i = 0; i < d; ++i) o[i] += w * (double)rv[i];
+            }
+            for (int i = 0; i < d; ++i) o[i] /= l;
+        }
+    }
+    return ORACLE_OK;
+}

@@ -37,6 +37,11 @@ MUTANTS = [
      "return blk + (size_t)L->P * (size_t)L->d + (size_t)(L->d / L->Gk) * 2u +"),
     ("f16_ties_away", "if (rem > half || (rem == half && (q & 1))) q += 1;", "if (rem >= half) q += 1;"),
     ("f16_subnormal_off_by_one", "int s = -(e + 1);", "int s = -e;"),
+    ("window_start_off_by_one", "if (t >= len - window) return 1;", "if (t > len - window) return 1;"),
+    ("window_sinks_inclusive", "return sinks > 0 && t < sinks;", "return sinks > 0 && t <= sinks;"),
+    ("window_sinks_ignored", "return sinks > 0 && t < sinks;", "return 0;"),
+    ("window_gqa_modulo_map", "int kv = hq / n_rep;", "int kv = hq % Hkv;"),
+    ("window_no_max_subtraction", "double w = exp(z - zmax);", "double w = exp(z);"),
     ("last_token_dropped", "for (int t = 0; t < len; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk",
      "for (int t = 0; t < len - 1; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk"),
 ]

@@ -475,3 +475,80 @@ def test_attention_page_permutation_invariance_and_pow2_scaling():
     oracle.quantize_append(L, pool, k, (v.astype(np.float32) * 2).astype(np.float16), bt, np.array([0], np.int32))
     out2 = oracle.decode_attention(L, pool, q, bt, np.array([n], np.int32), 0.125)
     assert np.array_equal(out2, 2 * outs[1])
+
+
+# ----------------------------------------------------------------------------
+# sliding window with sink tokens ("AI inference tuning: KV Cache optimisation and
+# memory management" section 3.2): the decode query at position L-1 sees keys
+# [max(0, L - W), L) and the first S positions
+# ----------------------------------------------------------------------------
+
+def _window_visible(n, window, sinks):
+    """Visible key positions of query row i = n - 1, from the page's mask construction."""
+    i = n - 1
+    mask = np.zeros(n, bool)
+    mask[max(0, i - window + 1):i + 1] = True
+    if sinks > 0:
+        mask[:sinks] = True
+    return np.nonzero(mask)[0]
+
+
+@pytest.mark.parametrize("window,sinks", [(1, 0), (5, 0), (5, 3), (17, 4), (16, 16), (3, 40), (40, 0), (100, 2)])
+def test_window_equals_full_attention_on_compacted_cache(window, sinks):
+    # the windowed result equals plain decode attention over a cache that holds only the
+    # visible rows (re-quantized row by row: the codes are the same), in the same order
+    L = oracle.Layout(2, 64, 16, 32, 64, 32)
+    lens = [40, 23, 7]
+    pool, bt, k, v = _build_cache(L, len(lens), lens, seed=51)
+    q = W.kv_tensor(W.SEED_Q + 50, (1, len(lens), 8, 64)).numpy()[0]
+    scale = 0.3
+    got = oracle.decode_attention_window(L, pool, q, bt, np.array(lens, np.int32), scale, window, sinks)
+    for b, n in enumerate(lens):
+        vis = _window_visible(n, window, sinks)
+        pages = (len(vis) + L.P - 1) // L.P
+        bt1 = np.arange(pages, dtype=np.int32)[None, :]
+        pool1 = np.zeros(L.pool_bytes, np.uint8)
+        oracle.quantize_append(L, pool1, k[b:b + 1, vis], v[b:b + 1, vis], bt1, np.array([0], np.int32))
+        ref = oracle.decode_attention(L, pool1, q[b:b + 1], bt1, np.array([len(vis)], np.int32), scale)
+        assert np.array_equal(got[b], ref[0]), (b, window, sinks)
+
+
+def test_window_covering_everything_is_plain_attention():
+    L = oracle.Layout(2, 64, 16, 32, 64, 16)
+    lens = [1, 33, 17, 0]
+    pool, bt, _, _ = _build_cache(L, len(lens), lens, seed=52)
+    q = W.kv_tensor(W.SEED_Q + 51, (1, len(lens), 4, 64)).numpy()[0]
+    full = oracle.decode_attention(L, pool, q, bt, np.array(lens, np.int32), 0.125)
+    for window, sinks in [(0, 0), (0, 5), (33, 0), (1000, 4), (-1, 2)]:
+        got = oracle.decode_attention_window(L, pool, q, bt, np.array(lens, np.int32), 0.125, window, sinks)
+        assert np.array_equal(got, full), (window, sinks)
+
+
+def test_window_of_one_returns_the_last_value_row():
+    L = oracle.Layout(2, 64, 16, 32, 64, 16)
+    lens = [29, 1, 16]
+    pool, bt, _, _ = _build_cache(L, len(lens), lens, seed=53)
+    q = W.kv_tensor(W.SEED_Q + 52, (1, len(lens), 4, 64)).numpy()[0]
+    got = oracle.decode_attention_window(L, pool, q, bt, np.array(lens, np.int32), 0.125, 1, 0)
+    for b, n in enumerate(lens):
+        _, dv = oracle.dequantize(L, pool, bt, b, n - 1, 1)
+        for hq in range(4):
+            assert np.array_equal(got[b, hq], dv[0, hq // 2].astype(np.float64))
+
+
+@pytest.mark.parametrize("window,sinks", [(4, 2), (9, 0), (2, 6), (30, 30)])
+def test_window_brute_force(window, sinks):
+    # numpy softmax over the page's mask, against the oracle, on tiny inputs with large logits
+    L = oracle.Layout(2, 64, 16, 32, 64, 16)
+    lens = [26, 11]
+    pool, bt, _, _ = _build_cache(L, len(lens), lens, seed=54)
+    q = W.kv_tensor(W.SEED_Q + 53, (1, len(lens), 4, 64)).numpy()[0]
+    scale = 40.0  # logits far past exp's range: the maximum has to be subtracted
+    got = oracle.decode_attention_window(L, pool, q, bt, np.array(lens, np.int32), scale, window, sinks)
+    for b, n in enumerate(lens):
+        dk, dv = oracle.dequantize(L, pool, bt, b, 0, n)
+        vis = _window_visible(n, window, sinks)
+        for hq in range(4):
+            s = (dk[vis, hq // 2, :].astype(np.float64) @ q[b, hq].astype(np.float64)) * scale
+            ref = scipy.special.softmax(s) @ dv[vis, hq // 2, :].astype(np.float64)
+            np.testing.assert_allclose(got[b, hq], ref, rtol=1e-10, atol=1e-10)
