@@ -181,6 +181,32 @@ int kvq_decode_step(const kvq_cache_config *cfg, void *pool, const void *k_new, 
                     kvq_stream_t stream);
 
 /*
+ * Decode attention and the decode step with a sliding window and sink tokens
+ * (SlidingWindowAttention, section 3.2 of the KV-cache optimisation page): the query,
+ * at the last position L - 1 of its sequence, attends to positions
+ * [max(0, L - window), L) and to the first `sinks` positions [0, min(sinks, L)).
+ *   window   >= 0; 0 means no window (every position, as in kvq_decode_attention).
+ *   sinks    >= 0; positions kept from the start of the sequence besides the window.
+ * Pages wholly outside both ranges are not read.  Every other argument is as in
+ * kvq_decode_attention / kvq_decode_step; a workspace of kvq_decode_workspace_bytes()
+ * for the same (cfg, batch, num_q_heads, max_len) is large enough for any window.
+ * The step appends the new token whether or not it falls in the window (it always
+ * does when append_pos[b] = seq_lens[b] - 1).
+ * Returns KVQ_OK, KVQ_EINVAL (also for a negative window or sinks), KVQ_EUNSUPPORTED,
+ * KVQ_EWORKSPACE or KVQ_ECUDA.
+ */
+int kvq_decode_attention_window(const kvq_cache_config *cfg, const void *pool, const void *q,
+                                const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                                int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                                int32_t window, int32_t sinks, float *out, void *workspace,
+                                size_t workspace_bytes, kvq_stream_t stream);
+int kvq_decode_step_window(const kvq_cache_config *cfg, void *pool, const void *k_new, const void *v_new,
+                           const int32_t *append_pos, const void *q, const int32_t *block_table,
+                           int32_t max_blocks, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                           int32_t max_len, float softmax_scale, int32_t window, int32_t sinks, float *out,
+                           void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
  * Decode attention that allocates nothing, for callers that cannot provide a
  * workspace: a plugin inside a host engine that owns no device allocator, an
  * embedded or real-time runtime with a fixed memory budget that forbids allocation

@@ -22,7 +22,9 @@ from .binding import (  # noqa: F401
     kvq_block_bytes,
     kvq_decode_attention,
     kvq_decode_attention_noalloc,
+    kvq_decode_attention_window,
     kvq_decode_step,
+    kvq_decode_step_window,
     kvq_decode_workspace_bytes,
     kvq_dequantize,
     kvq_last_error,

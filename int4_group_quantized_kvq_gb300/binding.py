@@ -20,7 +20,8 @@ KVQ_FLAG_BAD_PAGE, KVQ_FLAG_BAD_POSITION, KVQ_FLAG_WAIT_TIMEOUT, KVQ_FLAG_STALE_
 
 ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
                "kvq_decode_attention", "kvq_dequantize", "kvq_read_status", "kvq_last_error", "kvq_version",
-               "kvq_decode_attention_noalloc", "kvq_decode_step")
+               "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_attention_window",
+               "kvq_decode_step_window")
 
 
 class KvqError(RuntimeError):
@@ -67,6 +68,12 @@ def lib() -> C.CDLL:
         L.kvq_decode_attention_noalloc.restype = C.c_int
         L.kvq_decode_step.argtypes = [cfgp, P, P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
         L.kvq_decode_step.restype = C.c_int
+        L.kvq_decode_attention_window.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, I32, I32, P, P,
+                                                  SZ, P]
+        L.kvq_decode_attention_window.restype = C.c_int
+        L.kvq_decode_step_window.argtypes = [cfgp, P, P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, I32, I32, P,
+                                             P, SZ, P]
+        L.kvq_decode_step_window.restype = C.c_int
         L.kvq_dequantize.argtypes = [cfgp, P, P, I32, I32, I32, I32, P, P, I32, P, P]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_read_status.argtypes = [P, C.POINTER(C.c_uint32), P]
@@ -178,6 +185,36 @@ def kvq_decode_step(cfg: CacheConfig, pool: torch.Tensor, k_new: torch.Tensor, v
         _dev(v_new, "v_new", torch.float16), _dev(append_pos, "append_pos", torch.int32),
         _dev(q, "q", torch.float16), _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
         _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
+        _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(rc)
+
+
+def kvq_decode_attention_window(cfg: CacheConfig, pool: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
+                                seq_lens: torch.Tensor, max_len: int, softmax_scale: float, window: int, sinks: int,
+                                out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """kvq_decode_attention over the last `window` positions (0: all) and the first `sinks`."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_decode_attention_window(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(q, "q", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale), int(window), int(sinks),
+        _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(rc)
+
+
+def kvq_decode_step_window(cfg: CacheConfig, pool: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                           append_pos: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
+                           seq_lens: torch.Tensor, max_len: int, softmax_scale: float, window: int, sinks: int,
+                           out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """kvq_decode_step attending to the last `window` positions (0: all) and the first `sinks`."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_decode_step_window(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(k_new, "k_new", torch.float16),
+        _dev(v_new, "v_new", torch.float16), _dev(append_pos, "append_pos", torch.int32),
+        _dev(q, "q", torch.float16), _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale), int(window), int(sinks),
         _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
         _stream(stream))
     _check(rc)

@@ -7,6 +7,9 @@ nothing) around the C ABI calls of a decode step:
     decode attention over the packed cache      ->  kvq_decode_attention
     both in one call (append fused in)          ->  kvq_decode_step
 
+With ``window > 0`` the attention is restricted to the last ``window`` positions and
+the first ``sinks`` (``kvq_decode_attention_window`` / ``kvq_decode_step_window``).
+
 ``decode_step_host`` is the same step driven from pinned host buffers (``HostStaging``):
 the step's q, K and V are copied in with one transfer and the output copied back, on
 the same stream.
@@ -22,8 +25,10 @@ from . import binding as B
 
 class PagedKVCache:
     def __init__(self, cfg: B.CacheConfig, block_table: torch.Tensor, num_q_heads: int, max_len: int,
-                 device="cuda", pool: torch.Tensor | None = None):
+                 device="cuda", pool: torch.Tensor | None = None, window: int = 0, sinks: int = 0):
         self.cfg = cfg
+        self.window = int(window)
+        self.sinks = int(sinks)
         self.device = torch.device(device)
         self.block_table = block_table.to(self.device, torch.int32).contiguous()
         self.batch = int(self.block_table.shape[0])
@@ -46,14 +51,24 @@ class PagedKVCache:
 
     def attend(self, q: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor, stream=None) -> None:
         """Decode attention of q [B, Hq, d] fp16 over positions 0 .. seq_lens[b]-1 into out (fp32)."""
-        B.kvq_decode_attention(self.cfg, self.pool, q, self.block_table, seq_lens, self.max_len,
-                               self.softmax_scale, out, self.workspace, stream=stream)
+        if self.window > 0:
+            B.kvq_decode_attention_window(self.cfg, self.pool, q, self.block_table, seq_lens, self.max_len,
+                                          self.softmax_scale, self.window, self.sinks, out, self.workspace,
+                                          stream=stream)
+        else:
+            B.kvq_decode_attention(self.cfg, self.pool, q, self.block_table, seq_lens, self.max_len,
+                                   self.softmax_scale, out, self.workspace, stream=stream)
 
     def decode_step(self, q, k_new, v_new, append_pos, seq_lens, out, stream=None) -> None:
         """Append one token per sequence at append_pos, then attend over seq_lens (which include it):
         one kvq_decode_step call."""
-        B.kvq_decode_step(self.cfg, self.pool, k_new, v_new, append_pos, q, self.block_table, seq_lens, self.max_len,
-                          self.softmax_scale, out, self.workspace, stream=stream)
+        if self.window > 0:
+            B.kvq_decode_step_window(self.cfg, self.pool, k_new, v_new, append_pos, q, self.block_table, seq_lens,
+                                     self.max_len, self.softmax_scale, self.window, self.sinks, out, self.workspace,
+                                     stream=stream)
+        else:
+            B.kvq_decode_step(self.cfg, self.pool, k_new, v_new, append_pos, q, self.block_table, seq_lens,
+                              self.max_len, self.softmax_scale, out, self.workspace, stream=stream)
 
     def decode_step_two_calls(self, q, k_new, v_new, append_pos, seq_lens, out, stream=None) -> None:
         """The same step as two calls: kvq_quantize_append, then kvq_decode_attention."""

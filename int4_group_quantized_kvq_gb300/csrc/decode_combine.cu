@@ -12,7 +12,11 @@ cudaError_t launch_combine(const DecodeArgs& a, const DecodePlan& plan, cudaStre
     p.seq_lens = a.seq_lens;
     p.out = a.out;
     p.P = a.L.P;
+    p.lg_p = 0;
+    while ((1 << p.lg_p) < a.L.P) ++p.lg_p;
     p.max_blocks = a.max_blocks;
+    p.window = a.window;
+    p.sinks = a.sinks;
     p.B = a.B;
     p.Hq = a.Hq;
     p.Hg = a.Hkv / plan.hk;

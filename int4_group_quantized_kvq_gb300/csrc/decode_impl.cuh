@@ -107,12 +107,59 @@ struct KParams {
     const int32_t* append_pos;
     uint8_t* pool_w;
     int32_t lg_p, lg_lk, lg_lv;  // log2 of P, of the K and of the V group width in 8-value lanes
+    // sliding window with sink tokens: the last `window` positions (window <= 0: all) and
+    // the first `sinks` are attended
+    int32_t window, sinks;
 };
 
-// Pages sequence b spans for a length of L positions (negative: 0), at most max_blocks.
-__device__ __forceinline__ int seq_pages(int L, int P, int max_blocks) {
-    const long long n = (static_cast<long long>(L < 0 ? 0 : L) + P - 1) / P;
-    return static_cast<int>(n < max_blocks ? n : max_blocks);
+// a / b for a >= 0, b > 0, with 32-bit division when both fit (the usual case).
+__device__ __forceinline__ long long div_nn(long long a, long long b) {
+    if (((a | b) >> 32) == 0) return static_cast<long long>(static_cast<unsigned>(a) / static_cast<unsigned>(b));
+    return a / b;
+}
+
+// The positions a sequence of L positions attends to ("AI inference tuning: KV Cache
+// optimisation and memory management" section 3.2, SlidingWindowAttention, for the query at
+// the last position): L is clamped to [0, max_blocks * P]; positions t < L with t >= wlo or
+// t < sinks.  Its pages are listed in order: the sink pages [0, sp), then the window pages
+// [wlo / P, ceil(L / P)), one run when they meet.  List index j is page j + (j >= gs ? gd : 0).
+struct SeqSpan {
+    int L;    // positions (clamped)
+    int wlo;  // first window position; 0 when every position is attended
+    int gs;   // list index at which the window pages resume after a gap (np: no gap)
+    int gd;   // pages skipped by the gap
+    int np;   // pages listed
+};
+// P = 2^lg_p.
+__device__ __forceinline__ SeqSpan seq_span(int L, int lg_p, int max_blocks, int window, int sinks) {
+    const int P = 1 << lg_p;
+    long long Lc = L < 0 ? 0 : L;
+    if (Lc > (static_cast<long long>(max_blocks) << lg_p)) Lc = static_cast<long long>(max_blocks) << lg_p;
+    SeqSpan sp;
+    sp.L = static_cast<int>(Lc);
+    const int npl = (sp.L + P - 1) >> lg_p;
+    sp.wlo = 0;
+    sp.gs = npl;
+    sp.gd = 0;
+    sp.np = npl;
+    if (window > 0 && sp.L > window) {
+        sp.wlo = sp.L - window;
+        const int sk = sinks > 0 ? (sinks < sp.L ? sinks : sp.L) : 0;
+        const int s_pages = (sk + P - 1) >> lg_p;
+        const int w_first = sp.wlo >> lg_p;
+        if (w_first > s_pages) {
+            sp.gs = s_pages;
+            sp.gd = w_first - s_pages;
+            sp.np = s_pages + (npl - w_first);
+        }
+    }
+    return sp;
+}
+// Page of list index j, and list index of page r (-1 when r is not attended).
+__device__ __forceinline__ int span_page(const SeqSpan& sp, int j) { return j + (j >= sp.gs ? sp.gd : 0); }
+__device__ __forceinline__ int span_index(const SeqSpan& sp, int r) {
+    if (r < sp.gs) return r;
+    return (r >= sp.gs + sp.gd && r < sp.np + sp.gd) ? r - sp.gd : -1;
 }
 
 // Exclusive prefix sums of pages per sequence into pre[0..B], the lengths (negative ones
@@ -128,12 +175,13 @@ __device__ __forceinline__ void page_prefix(const KParams& p, int32_t* pre, int3
             L = L < 0 ? 0 : L;
             lens[b] = L;
             aps[b] = p.k_new != nullptr ? p.append_pos[b] : -1;
-            long long npl = (static_cast<long long>(L) + p.P - 1) / p.P;
-            if (npl > p.max_blocks) {
-                raise_flag(p.status, KVQ_FLAG_BAD_POSITION);
-                npl = p.max_blocks;
+            if (((static_cast<long long>(L) + p.P - 1) >> p.lg_p) > p.max_blocks) raise_flag(p.status, KVQ_FLAG_BAD_POSITION);
+            if (p.window > 0) {
+                np = seq_span(L, p.lg_p, p.max_blocks, p.window, p.sinks).np;
+            } else {
+                const long long npl = (static_cast<long long>(L) + p.P - 1) >> p.lg_p;
+                np = static_cast<int>(npl < p.max_blocks ? npl : p.max_blocks);
             }
-            np = static_cast<int>(npl);
         }
         int x = np;
 #pragma unroll
@@ -159,12 +207,15 @@ __device__ __forceinline__ int find_seq(const int32_t* pre, int B, int Hg, long 
 }
 
 // Global address of the HK blocks of unit u, validating the page id.
-__device__ __forceinline__ const uint8_t* unit_block(const KParams& p, const int32_t* pre, long long u, int HK) {
+template <bool WIN>
+__device__ __forceinline__ const uint8_t* unit_block(const KParams& p, const int32_t* pre, const int32_t* lens,
+                                                     long long u, int HK) {
     const int b = find_seq(pre, p.B, p.Hg, u);
     const long long rem = u - static_cast<long long>(p.Hg) * pre[b];
     const int np = pre[b + 1] - pre[b];
     const int hg = static_cast<int>(rem / np);
-    const int pg = static_cast<int>(rem - static_cast<long long>(hg) * np);
+    int pg = static_cast<int>(rem - static_cast<long long>(hg) * np);
+    if (WIN) pg = span_page(seq_span(lens[b], p.lg_p, p.max_blocks, p.window, p.sinks), pg);
     int page = p.block_table[static_cast<long long>(b) * p.max_blocks + pg];
     if (page < 0 || page >= p.num_pages) {
         raise_flag(p.status, KVQ_FLAG_BAD_PAGE);
@@ -174,10 +225,10 @@ __device__ __forceinline__ const uint8_t* unit_block(const KParams& p, const int
 }
 
 // First unit of slice w of U units split over W slices.
-__device__ __forceinline__ long long slice_start(long long w, long long U, long long W) { return w * U / W; }
+__device__ __forceinline__ long long slice_start(long long w, long long U, long long W) { return div_nn(w * U, W); }
 
 // The slice containing unit u (the largest w with slice_start(w) <= u).
-__device__ __forceinline__ long long slice_of(long long u, long long U, long long W) { return ((u + 1) * W - 1) / U; }
+__device__ __forceinline__ long long slice_of(long long u, long long U, long long W) { return div_nn((u + 1) * W - 1, U); }
 
 // The chunks of one step: chunk X is chunk chk[X] of the unit buffer blk[X] and holds
 // sequence positions t0[X] .. t0[X] + 15; a chunk with !live[X] is masked out whole.
@@ -232,7 +283,7 @@ __device__ __noinline__ void append_rows(const KParams& p, const int32_t* aps, u
     }
 }
 
-template <int D, int GK, int GV, int HK, int HS>
+template <int D, int GK, int GV, int HK, int HS, bool WIN>
 __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_splitkv_kernel(KParams p) {
     static_assert(D == 128, "the fragment mapping below is written for head_dim 128");
     static_assert(HK == 1 || HS == 1, "several kv heads per unit only with one query head each");
@@ -307,7 +358,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                 if (lane == 0 && shg == 0) raise_flag(p.status, KVQ_FLAG_BAD_POSITION);
                 continue;
             }
-            if (apg < pre[sb + 1] - pre[sb]) continue;  // streamed by this call
+            if (WIN ? span_index(seq_span(lens[sb], p.lg_p, p.max_blocks, p.window, p.sinks), static_cast<int>(apg)) >= 0
+                    : apg < pre[sb + 1] - pre[sb])
+                continue;  // streamed by this call
             const int page = p.block_table[static_cast<long long>(sb) * p.max_blocks + apg];
             if (page < 0 || page >= p.num_pages) {
                 if (lane == 0) raise_flag(p.status, KVQ_FLAG_BAD_PAGE);
@@ -345,9 +398,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     auto unit_of = [&](int i) { return c0 + warp + static_cast<long long>(kWarps) * i; };
     int wbase = 0;
     unsigned long long waddr =
-        lane < nm ? reinterpret_cast<unsigned long long>(unit_block(p, pre, unit_of(lane), HK)) : 0ull;
+        lane < nm ? reinterpret_cast<unsigned long long>(unit_block<WIN>(p, pre, lens, unit_of(lane), HK)) : 0ull;
     unsigned long long wnext =
-        32 + lane < nm ? reinterpret_cast<unsigned long long>(unit_block(p, pre, unit_of(32 + lane), HK)) : 0ull;
+        32 + lane < nm ? reinterpret_cast<unsigned long long>(unit_block<WIN>(p, pre, lens, unit_of(32 + lane), HK)) : 0ull;
     int issued = 0;
     const uint64_t l2_stream = l2_policy_evict_first();  // pages are read once per call
     auto issue = [&](int i, int st) {  // this warp's unit i into stage st; i increases call by call
@@ -355,7 +408,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
             wbase += 32;
             waddr = wnext;
             wnext = wbase + 32 + lane < nm
-                        ? reinterpret_cast<unsigned long long>(unit_block(p, pre, unit_of(wbase + 32 + lane), HK))
+                        ? reinterpret_cast<unsigned long long>(unit_block<WIN>(p, pre, lens, unit_of(wbase + 32 + lane), HK))
                         : 0ull;
         }
         const unsigned long long src = __shfl_sync(0xffffffffu, waddr, i - wbase);
@@ -370,7 +423,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     {
         int b0 = find_seq(pre, p.B, p.Hg, c0);
         const int np0 = pre[b0 + 1] - pre[b0];
-        const int hg0 = static_cast<int>((c0 - static_cast<long long>(p.Hg) * pre[b0]) / np0);
+        const int hg0 = static_cast<int>(div_nn(c0 - static_cast<long long>(p.Hg) * pre[b0], np0));
         if (threadIdx.x == 0) {
             const uint32_t qbytes0 = static_cast<uint32_t>(p.ns) * D * 2;
             mbar_arrive_expect_tx(qbar0, qbytes0);
@@ -390,7 +443,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     uint32_t qb[KSTEPS][NTQ][2];
     float m[HS], l[HS];
     float o[MT][HS][4];
-    int Leff = 0;
+    int Leff = 0;  // positions of the segment's sequence (clamped to its block table)
+    int wlo = 0;   // its first window position (0: all attended)
+    SeqSpan sspan{};  // attended positions and listed pages of the segment's sequence
 
     // the kv head (within the unit) of this thread's score slot, and of its B-fragment
     // column (HK > 1 only when every slot is its own kv head)
@@ -419,8 +474,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         if (MASKED) {
 #pragma unroll
             for (int X = 0; X < TG; ++X) {
-                vg[X] = live[X] && t0[X] + g < Leff;
-                vg8[X] = live[X] && t0[X] + g + 8 < Leff;
+                const int ta = t0[X] + g, tb = ta + 8;
+                vg[X] = live[X] && ta < Leff && (!WIN || ta >= wlo || ta < p.sinks);
+                vg8[X] = live[X] && tb < Leff && (!WIN || tb >= wlo || tb < p.sinks);
             }
         }
 
@@ -631,7 +687,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     // ---- walk the segments this CTA's slice touches ----
     int b = find_seq(pre, p.B, p.Hg, c0);
     int np = pre[b + 1] - pre[b];
-    int hg = static_cast<int>((c0 - static_cast<long long>(p.Hg) * pre[b]) / np);
+    int hg = static_cast<int>(div_nn(c0 - static_cast<long long>(p.Hg) * pre[b], np));
     long long sfirst = static_cast<long long>(p.Hg) * pre[b] + static_cast<long long>(hg) * np;
     int consumed = 0;     // this warp's units taken out of the ring
     int cst = 0;          // stage of the next unit to consume
@@ -683,9 +739,16 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         }
         if (cnt > 0) {
             // new (sequence, head group): q fragments and a fresh softmax state
-            Leff = min(lens[b], p.max_blocks * p.P);
+            if constexpr (WIN) {
+                sspan = seq_span(lens[b], p.lg_p, p.max_blocks, p.window, p.sinks);
+                Leff = sspan.L;
+                wlo = sspan.wlo;
+            } else {
+                Leff = min(lens[b], p.max_blocks * p.P);
+            }
             apg_seg = -1;
-            if (aps[b] >= 0 && (aps[b] >> p.lg_p) < np) apg_seg = aps[b] >> p.lg_p;
+            if (aps[b] >= 0 && (WIN ? span_index(sspan, aps[b] >> p.lg_p) >= 0 : (aps[b] >> p.lg_p) < np))
+                apg_seg = aps[b] >> p.lg_p;
             if (!failed && !__all_sync(0xffffffffu, mbar_wait(qbar0 + 8 * (segk & 1), (segk >> 1) & 1, kWaitLimitNs))) {
                 if (lane == 0) raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
                 failed = true;
@@ -752,32 +815,42 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                 const uint8_t* blkA = ring + cst * ubytes;
                 const uint8_t* blkB = ring + st1 * ubytes;
                 const int pg = pg0 + kWarps * j;
+                // pages of the two units (list indices past a window gap skip it)
+                const int rA = WIN ? span_page(sspan, pg) : pg;
+                const int rB = WIN ? span_page(sspan, pg + kWarps) : pg + kWarps;
                 // the page taking this step's appended token is patched before it is used
-                if (apg_seg >= 0 && (pg == apg_seg || (n == 2 && pg + kWarps == apg_seg)))
-                    append_rows<D, HK>(p, aps, ring + (pg == apg_seg ? cst : st1) * ubytes, b, hg, apg_seg);
+                if (apg_seg >= 0 && (rA == apg_seg || (n == 2 && rB == apg_seg)))
+                    append_rows<D, HK>(p, aps, ring + (rA == apg_seg ? cst : st1) * ubytes, b, hg, apg_seg);
+                // every position of [t, t + w) attended, and some of it attended
+                auto all_in = [&](int t, int w) { return t + w <= Leff && (!WIN || t >= wlo || t + w <= p.sinks); };
+                auto any_in = [&](int t, int w) { return !WIN || (min(t + w, Leff) > wlo || t < p.sinks); };
                 if constexpr (HK == 1) {
                     if (p16) {
-                        const int t0A = pg * 16, t0B = (pg + kWarps) * 16;
+                        const int t0A = rA * 16, t0B = rB * 16;
                         const Step<TG> st = {{blkA, blkB}, {0, 0}, {t0A, t0B}, {true, n == 2}};
-                        if (n == 2 && t0B + 16 <= Leff) process(std::false_type{}, st);
+                        // (without a window, page B comes after page A, so B whole implies A whole)
+                        if (n == 2 && (WIN ? all_in(t0A, 16) && all_in(t0B, 16) : t0B + 16 <= Leff))
+                            process(std::false_type{}, st);
                         else process(std::true_type{}, st);
                     } else {
                         for (int chunk = 0; chunk < p.P / 16; chunk += 2) {
-                            const int t0 = pg * p.P + chunk * 16;
+                            const int t0 = rA * p.P + chunk * 16;
                             if (t0 >= Leff) break;
                             // an odd last chunk pairs with a re-read of itself, masked out
                             const bool two = chunk + 1 < p.P / 16;
+                            if (!any_in(t0, two ? 32 : 16)) continue;  // wholly before the window
                             const Step<TG> st = {{blkA, blkA}, {chunk, two ? chunk + 1 : chunk}, {t0, t0 + 16}, {true, two}};
-                            if (two && t0 + 32 <= Leff) process(std::false_type{}, st);
+                            if (two && all_in(t0, 32)) process(std::false_type{}, st);
                             else process(std::true_type{}, st);
                         }
                     }
                 } else {
                     for (int chunk = 0; chunk < p.P / 16; ++chunk) {
-                        const int t0 = pg * p.P + chunk * 16;
+                        const int t0 = rA * p.P + chunk * 16;
                         if (t0 >= Leff) break;
+                        if (!any_in(t0, 16)) continue;  // wholly before the window
                         const Step<TG> st = {{blkA}, {chunk}, {t0}, {true}};
-                        if (t0 + 16 <= Leff) process(std::false_type{}, st);
+                        if (all_in(t0, 16)) process(std::false_type{}, st);
                         else process(std::true_type{}, st);
                     }
                 }
@@ -908,7 +981,8 @@ struct CParams {
     const int32_t* seq_lens;
     float* out;
     int32_t B, Hq, Hg, ns;
-    int32_t P, max_blocks;
+    int32_t P, lg_p, max_blocks;
+    int32_t window, sinks;  // as in KParams
     int32_t C;  // CTAs of the decode grid
     int32_t W;  // warps per decode CTA: partials per CTA and segment
 };
@@ -949,7 +1023,7 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
     if (local) {
         int before = 0, all = 0;
         for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
-            const int n_i = seq_pages(p.seq_lens[i], p.P, p.max_blocks);
+            const int n_i = seq_span(p.seq_lens[i], p.lg_p, p.max_blocks, p.window, p.sinks).np;
             all += n_i;
             if (i < b) before += n_i;
         }
@@ -967,7 +1041,7 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
             pb += s_red[0][w];
             tot += s_red[1][w];
         }
-        np = seq_pages(p.seq_lens[b], p.P, p.max_blocks);
+        np = seq_span(p.seq_lens[b], p.lg_p, p.max_blocks, p.window, p.sinks).np;
     }
     auto row_range = [&](int pb_, int np_, int tot_, long long& cf_, long long& base_, long long& U_) {
         U_ = static_cast<long long>(p.Hg) * tot_;
@@ -1076,11 +1150,11 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
 
 // Raise the kernel's dynamic shared-memory limit once to the largest size asked for,
 // so repeated calls (and calls under stream capture) only launch.
-template <int D, int GK, int GV, int HK, int HS>
+template <int D, int GK, int GV, int HK, int HS, bool WIN>
 cudaError_t ensure_smem_attr(size_t smem) {
     static std::atomic<long long> granted{-1};
     if (static_cast<long long>(smem) <= granted.load(std::memory_order_acquire)) return cudaSuccess;
-    const cudaError_t err = cudaFuncSetAttribute(decode_splitkv_kernel<D, GK, GV, HK, HS>,
+    const cudaError_t err = cudaFuncSetAttribute(decode_splitkv_kernel<D, GK, GV, HK, HS, WIN>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) cudaGetLastError();  // a refused size must not linger as the last error
     if (err == cudaSuccess) {
@@ -1093,7 +1167,7 @@ cudaError_t ensure_smem_attr(size_t smem) {
 
 // Resident CTAs per SM for a given shared-memory size, memoised per size (a few sizes
 // per shape are asked for; the slots fill once and later calls only read them).
-template <int D, int GK, int GV, int HK, int HS>
+template <int D, int GK, int GV, int HK, int HS, bool WIN>
 int occupancy(size_t smem) {
     constexpr int kSlots = 32;
     static std::atomic<long long> memo[kSlots];  // (smem << 8) | ctas, 0 = empty
@@ -1102,9 +1176,9 @@ int occupancy(size_t smem) {
         if (m == 0) break;
         if ((m >> 8) == static_cast<long long>(smem)) return static_cast<int>(m & 0xff);
     }
-    if (ensure_smem_attr<D, GK, GV, HK, HS>(smem) != cudaSuccess) return 0;
+    if (ensure_smem_attr<D, GK, GV, HK, HS, WIN>(smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HK, HS>, cta_warps<HS>() * 32,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN>, cta_warps<HS>() * 32,
                                                       smem) != cudaSuccess)
         return 0;
     const long long entry = (static_cast<long long>(smem) << 8) | (n & 0xff);
@@ -1115,7 +1189,7 @@ int occupancy(size_t smem) {
     return n;
 }
 
-template <int D, int GK, int GV, int HK, int HS>
+template <int D, int GK, int GV, int HK, int HS, bool WIN>
 cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     KParams p;
     p.pool = a.pool;
@@ -1146,13 +1220,15 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     p.v_new = a.v_new;
     p.append_pos = a.append_pos;
     p.pool_w = a.pool_w;
+    p.window = a.window;
+    p.sinks = a.sinks;
     p.lg_p = 0;
     while ((1 << p.lg_p) < a.L.P) ++p.lg_p;
     p.lg_lk = 0;
     while ((8 << p.lg_lk) < a.L.Gk) ++p.lg_lk;
     p.lg_lv = 0;
     while ((8 << p.lg_lv) < a.L.Gv) ++p.lg_lv;
-    cudaError_t err = ensure_smem_attr<D, GK, GV, HK, HS>(plan.smem_bytes);
+    cudaError_t err = ensure_smem_attr<D, GK, GV, HK, HS, WIN>(plan.smem_bytes);
     if (err != cudaSuccess) return err;
     // The launch may start before the kernel ahead of it on the stream finishes
     // (programmatic dependent launch); the kernel waits with griddepcontrol.wait before
@@ -1167,46 +1243,53 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, GK, GV, HK, HS>, p);
+    err = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN>, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
 }  // namespace decode
 
-// Per-K-group dispatch entry points, one per translation unit.
+// Per-K-group dispatch entry points, one per translation unit (the _win ones serve calls
+// with a sliding window).
 cudaError_t decode_run_gk32(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_gk64(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_gk128(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 int decode_occupancy_gk32(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk64(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk128(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+cudaError_t decode_run_gk32_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_gk64_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_gk128_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+int decode_occupancy_gk32_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_gk64_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_gk128_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 
 }  // namespace kvq
 
 // Instantiates the dispatch for one K group size GK_ over GV in {32, 64, 128} and the
-// three unit shapes (HK, HS) in {(1, 1), (1, 2), (4, 1)}.
-#define KVQ_DECODE_DISPATCH(GK_, CALL, FAIL)                                                         \
+// three unit shapes (HK, HS) in {(1, 1), (1, 2), (4, 1)}; W_ selects the window instances.
+#define KVQ_DECODE_DISPATCH(GK_, W_, CALL, FAIL)                                                     \
     switch (a.L.Gv * 16 + plan.hk * 4 + plan.hs) {                                                   \
-        case 32 * 16 + 4 + 1: return CALL(128, GK_, 32, 1, 1);                                       \
-        case 32 * 16 + 4 + 2: return CALL(128, GK_, 32, 1, 2);                                       \
-        case 32 * 16 + 16 + 1: return CALL(128, GK_, 32, 4, 1);                                      \
-        case 64 * 16 + 4 + 1: return CALL(128, GK_, 64, 1, 1);                                       \
-        case 64 * 16 + 4 + 2: return CALL(128, GK_, 64, 1, 2);                                       \
-        case 64 * 16 + 16 + 1: return CALL(128, GK_, 64, 4, 1);                                      \
-        case 128 * 16 + 4 + 1: return CALL(128, GK_, 128, 1, 1);                                     \
-        case 128 * 16 + 4 + 2: return CALL(128, GK_, 128, 1, 2);                                     \
-        case 128 * 16 + 16 + 1: return CALL(128, GK_, 128, 4, 1);                                    \
+        case 32 * 16 + 4 + 1: return CALL(128, GK_, 32, 1, 1, W_);                                   \
+        case 32 * 16 + 4 + 2: return CALL(128, GK_, 32, 1, 2, W_);                                   \
+        case 32 * 16 + 16 + 1: return CALL(128, GK_, 32, 4, 1, W_);                                  \
+        case 64 * 16 + 4 + 1: return CALL(128, GK_, 64, 1, 1, W_);                                   \
+        case 64 * 16 + 4 + 2: return CALL(128, GK_, 64, 1, 2, W_);                                   \
+        case 64 * 16 + 16 + 1: return CALL(128, GK_, 64, 4, 1, W_);                                  \
+        case 128 * 16 + 4 + 1: return CALL(128, GK_, 128, 1, 1, W_);                                 \
+        case 128 * 16 + 4 + 2: return CALL(128, GK_, 128, 1, 2, W_);                                 \
+        case 128 * 16 + 16 + 1: return CALL(128, GK_, 128, 4, 1, W_);                                \
         default: return FAIL;                                                                        \
     }
-#define KVQ_DECODE_RUN(D_, GK_, GV_, HK_, HS_) decode::run<D_, GK_, GV_, HK_, HS_>(a, plan, s)
-#define KVQ_DECODE_OCC(D_, GK_, GV_, HK_, HS_) decode::occupancy<D_, GK_, GV_, HK_, HS_>(smem)
-#define KVQ_DECODE_TU(GK_)                                                                           \
+#define KVQ_DECODE_RUN(D_, GK_, GV_, HK_, HS_, W_) decode::run<D_, GK_, GV_, HK_, HS_, W_>(a, plan, s)
+#define KVQ_DECODE_OCC(D_, GK_, GV_, HK_, HS_, W_) decode::occupancy<D_, GK_, GV_, HK_, HS_, W_>(smem)
+#define KVQ_DECODE_TU(GK_, W_, RUN_NAME, OCC_NAME)                                                   \
     namespace kvq {                                                                                  \
-    cudaError_t decode_run_gk##GK_(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {    \
-        KVQ_DECODE_DISPATCH(GK_, KVQ_DECODE_RUN, cudaErrorInvalidValue)                              \
+    cudaError_t RUN_NAME(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {              \
+        KVQ_DECODE_DISPATCH(GK_, W_, KVQ_DECODE_RUN, cudaErrorInvalidValue)                          \
     }                                                                                                \
-    int decode_occupancy_gk##GK_(const DecodeArgs& a, const DecodePlan& plan, size_t smem) {         \
-        KVQ_DECODE_DISPATCH(GK_, KVQ_DECODE_OCC, 0)                                                  \
+    int OCC_NAME(const DecodeArgs& a, const DecodePlan& plan, size_t smem) {                         \
+        KVQ_DECODE_DISPATCH(GK_, W_, KVQ_DECODE_OCC, 0)                                              \
     }                                                                                                \
     }

@@ -25,6 +25,12 @@ cudaError_t decode_run_gk128(const DecodeArgs& a, const DecodePlan& plan, cudaSt
 int decode_occupancy_gk32(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk64(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk128(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+cudaError_t decode_run_gk32_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_gk64_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_gk128_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+int decode_occupancy_gk32_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_gk64_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_gk128_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 cudaError_t launch_combine(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 
 namespace {
@@ -60,10 +66,11 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
                kCtlBytes + round_up(static_cast<size_t>(3 * a.B + 1) * 4, 16);
     };
     auto occ_for = [&](size_t smem) {
+        const bool w = a.window > 0;
         switch (a.L.Gk) {
-            case 32: return decode_occupancy_gk32(a, *plan, smem);
-            case 64: return decode_occupancy_gk64(a, *plan, smem);
-            case 128: return decode_occupancy_gk128(a, *plan, smem);
+            case 32: return w ? decode_occupancy_gk32_win(a, *plan, smem) : decode_occupancy_gk32(a, *plan, smem);
+            case 64: return w ? decode_occupancy_gk64_win(a, *plan, smem) : decode_occupancy_gk64(a, *plan, smem);
+            case 128: return w ? decode_occupancy_gk128_win(a, *plan, smem) : decode_occupancy_gk128(a, *plan, smem);
             default: return 0;
         }
     };
@@ -87,7 +94,11 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
         }
     }
     const long long c_max = static_cast<long long>(sms) * occ;
-    const long long pages_max = (static_cast<long long>(std::max(a.max_len, 0)) + a.L.P - 1) / a.L.P;
+    long long pages_max = (static_cast<long long>(std::max(a.max_len, 0)) + a.L.P - 1) / a.L.P;
+    if (a.window > 0) {  // a sequence lists its sink pages and at most window / P + 1 window pages
+        const long long sink_pages = (std::min<long long>(std::max(a.sinks, 0), std::max(a.max_len, 0)) + a.L.P - 1) / a.L.P;
+        pages_max = std::min(pages_max, sink_pages + a.window / a.L.P + 2);
+    }
     const long long u_max = static_cast<long long>(hg) * a.B * pages_max;
     const long long ctas = std::min(c_max, std::max<long long>(1, u_max / (kMinUnitsPerWarp * kWarpsPerCta)));
     plan->ctas = static_cast<int32_t>(ctas);
@@ -111,10 +122,11 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     cudaError_t e;
+    const bool w = a.window > 0;
     switch (a.L.Gk) {
-        case 32: e = decode_run_gk32(a, plan, stream); break;
-        case 64: e = decode_run_gk64(a, plan, stream); break;
-        case 128: e = decode_run_gk128(a, plan, stream); break;
+        case 32: e = w ? decode_run_gk32_win(a, plan, stream) : decode_run_gk32(a, plan, stream); break;
+        case 64: e = w ? decode_run_gk64_win(a, plan, stream) : decode_run_gk64(a, plan, stream); break;
+        case 128: e = w ? decode_run_gk128_win(a, plan, stream) : decode_run_gk128(a, plan, stream); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;

@@ -132,13 +132,15 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, in
     return plan.ws_bytes;
 }
 
-int kvq_decode_attention(const kvq_cache_config* cfg, const void* pool, const void* q, const int32_t* block_table,
-                         int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
-                         int32_t max_len, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
-                         kvq_stream_t stream) {
+namespace {
+int decode_attention_impl(const kvq_cache_config* cfg, const void* pool, const void* q, const int32_t* block_table,
+                          int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                          int32_t max_len, float softmax_scale, int32_t window, int32_t sinks, float* out,
+                          void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
     if (int e = check_cfg(cfg)) return e;
     if (batch < 0 || num_q_heads < 1 || max_len < 0)
         return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
+    if (window < 0 || sinks < 0) return fail(KVQ_EINVAL, "window %d, sinks %d", window, sinks);
     if (num_q_heads % cfg->num_kv_heads)
         return fail(KVQ_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, cfg->num_kv_heads);
     if (num_q_heads / cfg->num_kv_heads > 8)
@@ -166,6 +168,8 @@ int kvq_decode_attention(const kvq_cache_config* cfg, const void* pool, const vo
     a.num_pages = cfg->num_pages;
     a.max_len = max_len;
     a.softmax_scale = softmax_scale;
+    a.window = window;
+    a.sinks = sinks;
     a.L = kvq::block_layout(*cfg);
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
@@ -178,13 +182,15 @@ int kvq_decode_attention(const kvq_cache_config* cfg, const void* pool, const vo
     return ok();
 }
 
-int kvq_decode_step(const kvq_cache_config* cfg, void* pool, const void* k_new, const void* v_new,
-                    const int32_t* append_pos, const void* q, const int32_t* block_table, int32_t max_blocks,
-                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
-                    float* out, void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+int decode_step_impl(const kvq_cache_config* cfg, void* pool, const void* k_new, const void* v_new,
+                     const int32_t* append_pos, const void* q, const int32_t* block_table, int32_t max_blocks,
+                     const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                     int32_t window, int32_t sinks, float* out, void* workspace, size_t workspace_bytes,
+                     kvq_stream_t stream) {
     if (int e = check_cfg(cfg)) return e;
     if (batch < 0 || num_q_heads < 1 || max_len < 0)
         return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
+    if (window < 0 || sinks < 0) return fail(KVQ_EINVAL, "window %d, sinks %d", window, sinks);
     if (num_q_heads % cfg->num_kv_heads)
         return fail(KVQ_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, cfg->num_kv_heads);
     if (num_q_heads / cfg->num_kv_heads > 8)
@@ -219,6 +225,8 @@ int kvq_decode_step(const kvq_cache_config* cfg, void* pool, const void* k_new, 
     a.v_new = static_cast<const __half*>(v_new);
     a.append_pos = append_pos;
     a.pool_w = static_cast<uint8_t*>(pool);
+    a.window = window;
+    a.sinks = sinks;
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
     if (e == cudaErrorInvalidValue) return fail(KVQ_EUNSUPPORTED, "no decode kernel for this shape");
@@ -228,6 +236,42 @@ int kvq_decode_step(const kvq_cache_config* cfg, void* pool, const void* k_new, 
     e = kvq::launch_decode(a, plan, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step launch");
     return ok();
+}
+}  // namespace
+
+int kvq_decode_attention(const kvq_cache_config* cfg, const void* pool, const void* q, const int32_t* block_table,
+                         int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                         int32_t max_len, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                         kvq_stream_t stream) {
+    return decode_attention_impl(cfg, pool, q, block_table, max_blocks, seq_lens, batch, num_q_heads, max_len,
+                                 softmax_scale, 0, 0, out, workspace, workspace_bytes, stream);
+}
+
+int kvq_decode_attention_window(const kvq_cache_config* cfg, const void* pool, const void* q,
+                                const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                                int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                                int32_t window, int32_t sinks, float* out, void* workspace, size_t workspace_bytes,
+                                kvq_stream_t stream) {
+    return decode_attention_impl(cfg, pool, q, block_table, max_blocks, seq_lens, batch, num_q_heads, max_len,
+                                 softmax_scale, window, sinks, out, workspace, workspace_bytes, stream);
+}
+
+int kvq_decode_step(const kvq_cache_config* cfg, void* pool, const void* k_new, const void* v_new,
+                    const int32_t* append_pos, const void* q, const int32_t* block_table, int32_t max_blocks,
+                    const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                    float* out, void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+    return decode_step_impl(cfg, pool, k_new, v_new, append_pos, q, block_table, max_blocks, seq_lens, batch,
+                            num_q_heads, max_len, softmax_scale, 0, 0, out, workspace, workspace_bytes, stream);
+}
+
+int kvq_decode_step_window(const kvq_cache_config* cfg, void* pool, const void* k_new, const void* v_new,
+                           const int32_t* append_pos, const void* q, const int32_t* block_table, int32_t max_blocks,
+                           const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len,
+                           float softmax_scale, int32_t window, int32_t sinks, float* out, void* workspace,
+                           size_t workspace_bytes, kvq_stream_t stream) {
+    return decode_step_impl(cfg, pool, k_new, v_new, append_pos, q, block_table, max_blocks, seq_lens, batch,
+                            num_q_heads, max_len, softmax_scale, window, sinks, out, workspace, workspace_bytes,
+                            stream);
 }
 
 int kvq_dequantize(const kvq_cache_config* cfg, const void* pool, const int32_t* block_table, int32_t max_blocks,

@@ -109,6 +109,9 @@ struct DecodeArgs {
     const __half* v_new = nullptr;
     const int32_t* append_pos = nullptr;
     uint8_t* pool_w = nullptr;
+    // sliding window with sink tokens: the last `window` positions (0: all) and the first `sinks`
+    int32_t window = 0;
+    int32_t sinks = 0;
 };
 
 // Returns cudaErrorInvalidValue for a geometry no kernel instance covers.
