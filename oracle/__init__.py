@@ -60,6 +60,15 @@ def lib() -> C.CDLL:
                                                          C.c_int, C.c_int, C.c_double, C.c_int, C.c_int,
                                                          C.c_void_p] + [C.c_int] * 6
         L.kvq_oracle_decode_attention_window.restype = C.c_int
+        L.kvq_oracle_fp16_block_bytes.argtypes = [C.c_int, C.c_int]
+        L.kvq_oracle_fp16_block_bytes.restype = C.c_size_t
+        L.kvq_oracle_fp16_append.argtypes = [C.c_void_p] * 4 + [C.c_int, C.c_void_p] + [C.c_int] * 6
+        L.kvq_oracle_fp16_append.restype = C.c_int
+        L.kvq_oracle_dequantize_to_fp16_pool.argtypes = [C.c_void_p] * 3 + [C.c_int, C.c_void_p] + [C.c_int] * 7
+        L.kvq_oracle_dequantize_to_fp16_pool.restype = C.c_int
+        L.kvq_oracle_fp16_decode_attention.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
+                                                       C.c_int, C.c_int, C.c_double, C.c_void_p] + [C.c_int] * 4
+        L.kvq_oracle_fp16_decode_attention.restype = C.c_int
         _lib = L
     return _lib
 
@@ -190,4 +199,54 @@ def decode_attention_window(L: Layout, pool: np.ndarray, q: np.ndarray, block_ta
     rc = lib().kvq_oracle_decode_attention_window(_ptr(pool), _ptr(q), _ptr(bt), int(bt.shape[1]), _ptr(sl), B, Hq,
                                                   float(softmax_scale), int(window), int(sinks), _ptr(out), *L.geom)
     _check(rc, "decode_attention_window")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The FP16 cache of the latency comparison ("LLM long-context inference: managing the KV
+# cache with an INT4 state machine" section 7.4): same pages, K then V rows in fp16.
+# ---------------------------------------------------------------------------
+
+def fp16_block_bytes(head_dim: int, page_size: int) -> int:
+    return int(lib().kvq_oracle_fp16_block_bytes(head_dim, page_size))
+
+
+def fp16_pool_bytes(L: Layout) -> int:
+    return L.num_pages * L.Hkv * fp16_block_bytes(L.d, L.P)
+
+
+def fp16_append(L: Layout, pool16: np.ndarray, k: np.ndarray, v: np.ndarray, block_table: np.ndarray,
+                start_pos: np.ndarray) -> None:
+    """fp16 rows k, v [B, n_new, Hkv, d] into the FP16 pool at start_pos[b] + t."""
+    k = np.ascontiguousarray(k, dtype=np.float16)
+    v = np.ascontiguousarray(v, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sp = np.ascontiguousarray(start_pos, dtype=np.int32)
+    B, n = k.shape[0], k.shape[1]
+    rc = lib().kvq_oracle_fp16_append(_ptr(pool16), _ptr(k), _ptr(v), _ptr(bt), int(bt.shape[1]), _ptr(sp), B, n,
+                                      L.Hkv, L.d, L.P, L.num_pages)
+    _check(rc, "fp16_append")
+
+
+def dequantize_to_fp16_pool(L: Layout, pool: np.ndarray, pool16: np.ndarray, block_table: np.ndarray,
+                            seq_lens: np.ndarray) -> None:
+    """Every attended position of the INT4 pool, dequantized (fp16 RNE) into the FP16 pool."""
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    rc = lib().kvq_oracle_dequantize_to_fp16_pool(_ptr(pool), _ptr(pool16), _ptr(bt), int(bt.shape[1]), _ptr(sl),
+                                                  int(sl.shape[0]), *L.geom)
+    _check(rc, "dequantize_to_fp16_pool")
+
+
+def fp16_decode_attention(L: Layout, pool16: np.ndarray, q: np.ndarray, block_table: np.ndarray,
+                          seq_lens: np.ndarray, softmax_scale: float) -> np.ndarray:
+    """fp64 decode attention over the FP16 cache.  q: fp16 [B, Hq, d] -> fp64 [B, Hq, d]."""
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, _ = q.shape
+    out = np.zeros((B, Hq, L.d), dtype=np.float64)
+    rc = lib().kvq_oracle_fp16_decode_attention(_ptr(pool16), _ptr(q), _ptr(bt), int(bt.shape[1]), _ptr(sl), B, Hq,
+                                                float(softmax_scale), _ptr(out), L.Hkv, L.d, L.P, L.num_pages)
+    _check(rc, "fp16_decode_attention")
     return out

@@ -407,3 +407,121 @@ int kvq_oracle_decode_attention_window(const uint8_t *pool, const uint16_t *q, c
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The FP16 cache of the latency comparison ([S] section 7.4: FP16 baseline, */
+/* INT4 dequantized first and then attended, INT4 dequantized inside the     */
+/* operator).  Pages as in [M] section 3.1: one block per (page, kv-head),   */
+/* block index page*Hkv + h, holding K rows P x d fp16 and then V rows        */
+/* P x d fp16 (little-endian), 4*P*d bytes.                                  */
+/* ------------------------------------------------------------------------ */
+size_t kvq_oracle_fp16_block_bytes(int head_dim, int page_size) {
+    if (head_dim <= 0 || page_size <= 0) return 0;
+    return (size_t)4 * (size_t)page_size * (size_t)head_dim;
+}
+
+static uint8_t *fp16_row(uint8_t *pool16, int Hkv, int d, int P, int page, int h, int is_v, int slot) {
+    size_t blk = ((size_t)page * (size_t)Hkv + (size_t)h) * ((size_t)4 * (size_t)P * (size_t)d);
+    return pool16 + blk + ((size_t)is_v * (size_t)P + (size_t)slot) * (size_t)d * 2u;
+}
+
+/* Store fp16 K and V rows [B, n_new, Hkv, d] at positions start_pos[b] + t. */
+int kvq_oracle_fp16_append(uint8_t *pool16, const uint16_t *k, const uint16_t *v, const int32_t *block_table,
+                           int max_blocks, const int32_t *start_pos, int B, int n_new, int Hkv, int d, int P,
+                           int num_pages) {
+    if (Hkv <= 0 || d <= 0 || P <= 0 || B < 0 || n_new < 0) return ORACLE_EINVAL;
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < n_new; ++t) {
+            long pos = (long)start_pos[b] + t;
+            if (pos < 0 || pos / P >= max_blocks) return ORACLE_ERANGE;
+            int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(pos / P)];
+            if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+            int slot = (int)(pos % P);
+            for (int h = 0; h < Hkv; ++h) {
+                size_t src = (((size_t)b * (size_t)n_new + (size_t)t) * (size_t)Hkv + (size_t)h) * (size_t)d;
+                uint8_t *kr = fp16_row(pool16, Hkv, d, P, page, h, 0, slot);
+                uint8_t *vr = fp16_row(pool16, Hkv, d, P, page, h, 1, slot);
+                for (int i = 0; i < d; ++i) {
+                    put_u16(kr + 2 * i, k[src + i]);
+                    put_u16(vr + 2 * i, v[src + i]);
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Dequantize every position 0 .. seq_lens[b]-1 of the INT4 pool into the FP16
+   pool, at the same page ids and slots: each value is the fp16 RNE of
+   (nibble - 8) * scale ([Q] section 2.1). */
+int kvq_oracle_dequantize_to_fp16_pool(const uint8_t *pool, uint8_t *pool16, const int32_t *block_table,
+                                       int max_blocks, const int32_t *seq_lens, int B, int Hkv, int d, int P,
+                                       int Gk, int Gv, int num_pages) {
+    layout_t L;
+    if (make_layout(&L, Hkv, d, P, Gk, Gv, num_pages) || d > 256) return ORACLE_EINVAL;
+    float rk[256], rv[256];
+    for (int b = 0; b < B; ++b) {
+        int len = seq_lens[b];
+        if (len < 0 || (len + P - 1) / P > max_blocks) return ORACLE_ERANGE;
+        for (int t = 0; t < len; ++t) {
+            int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+            if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+            for (int h = 0; h < Hkv; ++h) {
+                uint8_t *blk = block_ptr(&L, (uint8_t *)pool, page, h);
+                dequant_row(k_codes_row(&L, blk, t % P), k_scales_row(&L, blk, t % P), d, Gk, rk);
+                dequant_row(v_codes_row(&L, blk, t % P), v_scales_row(&L, blk, t % P), d, Gv, rv);
+                uint8_t *kr = fp16_row(pool16, Hkv, d, P, page, h, 0, t % P);
+                uint8_t *vr = fp16_row(pool16, Hkv, d, P, page, h, 1, t % P);
+                for (int i = 0; i < d; ++i) {
+                    put_u16(kr + 2 * i, kvq_oracle_f32_to_f16(rk[i]));
+                    put_u16(vr + 2 * i, kvq_oracle_f32_to_f16(rv[i]));
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Decode attention over the FP16 cache, in fp64 ([M] section 3.2): as
+   kvq_oracle_decode_attention with the K and V rows read as fp16. */
+int kvq_oracle_fp16_decode_attention(const uint8_t *pool16, const uint16_t *q, const int32_t *block_table,
+                                     int max_blocks, const int32_t *seq_lens, int B, int Hq, double softmax_scale,
+                                     double *out, int Hkv, int d, int P, int num_pages) {
+    if (Hkv <= 0 || d <= 0 || P <= 0 || Hq <= 0 || Hq % Hkv) return ORACLE_EINVAL;
+    int rep = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        int len = seq_lens[b];
+        if (len < 0 || (len + P - 1) / P > max_blocks) return ORACLE_ERANGE;
+        for (int hq = 0; hq < Hq; ++hq) {
+            int kvh = hq / rep;
+            const uint16_t *qrow = q + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            double *o = out + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            for (int i = 0; i < d; ++i) o[i] = 0.0;
+            if (len == 0) continue;
+            double zmax = -INFINITY;
+            for (int t = 0; t < len; ++t) {
+                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+                if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+                const uint8_t *kr = fp16_row((uint8_t *)pool16, Hkv, d, P, page, kvh, 0, t % P);
+                double z = 0.0;
+                for (int i = 0; i < d; ++i) z += kvq_oracle_f16_to_f64(qrow[i]) * kvq_oracle_f16_to_f64(get_u16(kr + 2 * i));
+                z *= softmax_scale;
+                if (z > zmax) zmax = z;
+            }
+            double lsum = 0.0;
+            for (int t = 0; t < len; ++t) {
+                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+                const uint8_t *kr = fp16_row((uint8_t *)pool16, Hkv, d, P, page, kvh, 0, t % P);
+                const uint8_t *vr = fp16_row((uint8_t *)pool16, Hkv, d, P, page, kvh, 1, t % P);
+                double z = 0.0;
+                for (int i = 0; i < d; ++i) z += kvq_oracle_f16_to_f64(qrow[i]) * kvq_oracle_f16_to_f64(get_u16(kr + 2 * i));
+                z *= softmax_scale;
+                double wz = exp(z - zmax);
+                lsum += wz;
+                for (int i = 0; i < d; ++i) o[i] += wz * kvq_oracle_f16_to_f64(get_u16(vr + 2 * i));
+            }
+            for (int i = 0; i < d; ++i) o[i] /= lsum;
+        }
+    }
+    return ORACLE_OK;
+}

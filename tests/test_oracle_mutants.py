@@ -42,6 +42,15 @@ MUTANTS = [
     ("window_sinks_ignored", "return sinks > 0 && t < sinks;", "return 0;"),
     ("window_gqa_modulo_map", "int kv = hq / n_rep;", "int kv = hq % Hkv;"),
     ("window_no_max_subtraction", "double w = exp(z - zmax);", "double w = exp(z);"),
+    ("fp16_k_v_swapped", "uint8_t *kr = fp16_row(pool16, Hkv, d, P, page, h, 0, slot);",
+     "uint8_t *kr = fp16_row(pool16, Hkv, d, P, page, h, 1, slot);"),
+    ("fp16_block_stride_2pd", "size_t blk = ((size_t)page * (size_t)Hkv + (size_t)h) * ((size_t)4 * (size_t)P * (size_t)d);",
+     "size_t blk = ((size_t)page * (size_t)Hkv + (size_t)h) * ((size_t)2 * (size_t)P * (size_t)d);"),
+    ("fp16_gqa_modulo", "int kvh = hq / rep;", "int kvh = hq % Hkv;"),
+    ("fp16_dequant_truncated", "put_u16(kr + 2 * i, kvq_oracle_f32_to_f16(rk[i]));",
+     "put_u16(kr + 2 * i, (uint16_t)(kvq_oracle_f32_to_f16(rk[i]) & 0xfffeu));"),
+    ("fp16_attention_scale_dropped", "        z *= softmax_scale;\n                double wz",
+     "        double wz"),
     ("last_token_dropped", "for (int t = 0; t < len; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk",
      "for (int t = 0; t < len - 1; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk"),
 ]

@@ -552,3 +552,109 @@ def test_window_brute_force(window, sinks):
             s = (dk[vis, hq // 2, :].astype(np.float64) @ q[b, hq].astype(np.float64)) * scale
             ref = scipy.special.softmax(s) @ dv[vis, hq // 2, :].astype(np.float64)
             np.testing.assert_allclose(got[b, hq], ref, rtol=1e-10, atol=1e-10)
+
+
+# ----------------------------------------------------------------------------
+# the FP16 cache of the latency comparison ("LLM long-context inference: managing
+# the KV cache with an INT4 state machine" section 7.4)
+# ----------------------------------------------------------------------------
+
+def _fp16_blocks(L, pool16):
+    """The FP16 pool as [page, kv head, K|V, slot, d] fp16 (the layout of the oracle's header)."""
+    return pool16.view(np.float16).reshape(L.num_pages, L.Hkv, 2, L.P, L.d)
+
+
+def test_fp16_append_places_rows_by_page_table():
+    L = oracle.Layout(3, 64, 16, 32, 64, 12)
+    lens = [37, 5]
+    pages = [(n + 15) // 16 for n in lens]
+    order = W.permutation(61, L.num_pages).numpy()
+    bt = np.full((2, max(pages)), -1, np.int32)
+    bt[0, :pages[0]] = order[:pages[0]]
+    bt[1, :pages[1]] = order[pages[0]:pages[0] + pages[1]]
+    k = W.kv_tensor(61, (2, 37, 3, 64)).numpy()
+    v = W.kv_tensor(62, (2, 37, 3, 64)).numpy()
+    pool16 = np.zeros(oracle.fp16_pool_bytes(L), np.uint8)
+    assert oracle.fp16_block_bytes(64, 16) == 4 * 16 * 64
+    for b in range(2):
+        oracle.fp16_append(L, pool16, k[b:b + 1, :lens[b]], v[b:b + 1, :lens[b]], bt[b:b + 1], np.array([0], np.int32))
+    blocks = _fp16_blocks(L, pool16)
+    for b in range(2):
+        for t in range(lens[b]):
+            pg, sl = bt[b, t // 16], t % 16
+            assert np.array_equal(blocks[pg, :, 0, sl], k[b, t])
+            assert np.array_equal(blocks[pg, :, 1, sl], v[b, t])
+
+
+def test_fp16_decode_attention_brute_force():
+    L = oracle.Layout(2, 64, 16, 32, 64, 16)
+    lens = [40, 1, 17]
+    pool16 = np.zeros(oracle.fp16_pool_bytes(L), np.uint8)
+    bt = np.arange(9, dtype=np.int32).reshape(3, 3)[:, :3]
+    bt = np.array([[4, 0, 8], [2, -1, -1], [7, 5, -1]], np.int32)
+    k = W.kv_tensor(63, (3, 40, 2, 64), 20.0, W.outlier_channels(2, 64, seed=3)).numpy()
+    v = W.kv_tensor(64, (3, 40, 2, 64)).numpy()
+    for b in range(3):
+        oracle.fp16_append(L, pool16, k[b:b + 1, :lens[b]], v[b:b + 1, :lens[b]], bt[b:b + 1], np.array([0], np.int32))
+    q = W.kv_tensor(65, (1, 3, 8, 64)).numpy()[0]
+    got = oracle.fp16_decode_attention(L, pool16, q, bt, np.array(lens, np.int32), 0.2)
+    for b in range(3):
+        for hq in range(8):
+            kh = k[b, :lens[b], hq // 4].astype(np.float64)
+            s_ = (kh @ q[b, hq].astype(np.float64)) * 0.2
+            ref = scipy.special.softmax(s_) @ v[b, :lens[b], hq // 4].astype(np.float64)
+            np.testing.assert_allclose(got[b, hq], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_dequantize_to_fp16_pool_matches_dequantize():
+    L = oracle.Layout(2, 64, 16, 32, 64, 16)
+    lens = [33, 16, 7]
+    pool, bt, _, _ = _build_cache(L, len(lens), lens, seed=66)
+    pool16 = np.zeros(oracle.fp16_pool_bytes(L), np.uint8)
+    oracle.dequantize_to_fp16_pool(L, pool, pool16, bt, np.array(lens, np.int32))
+    blocks = _fp16_blocks(L, pool16)
+    for b, n in enumerate(lens):
+        dk, dv = oracle.dequantize(L, pool, bt, b, 0, n, out_fp16=True)
+        for t in range(n):
+            assert np.array_equal(blocks[bt[b, t // 16], :, 0, t % 16], dk[t])
+            assert np.array_equal(blocks[bt[b, t // 16], :, 1, t % 16], dv[t])
+
+
+def test_fp16_attention_equals_int4_attention_when_dequant_is_exact():
+    # every group's amax is 7 * 2^k, so every scale is a power of two and every
+    # dequantized value is exact in fp16: attention over the FP16 pool built by
+    # dequantize_to_fp16_pool must equal the INT4 attention bit for bit
+    L = oracle.Layout(2, 64, 16, 32, 64, 12)
+    lens = [45, 19]
+    rng = np.random.default_rng(67)
+    n = max(lens)
+    k = rng.standard_normal((2, n, 2, 64)).astype(np.float16)
+    v = rng.standard_normal((2, n, 2, 64)).astype(np.float16)
+    for x, G in ((k, 32), (v, 64)):
+        g = x.reshape(2, n, 2, 64 // G, G)
+        e = rng.integers(-2, 3, size=g.shape[:-1])
+        g[...] = np.clip(g, -0.9, 0.9) * (7.0 * 2.0 ** e)[..., None] / 0.9 * 0.5
+        g[..., 0] = (7.0 * 2.0 ** e).astype(np.float16)
+    pool = np.zeros(L.pool_bytes, np.uint8)
+    bt = np.array([[3, 9, 0], [5, 1, -1]], np.int32)
+    for b in range(2):
+        oracle.quantize_append(L, pool, k[b:b + 1, :lens[b]], v[b:b + 1, :lens[b]], bt[b:b + 1], np.array([0], np.int32))
+    pool16 = np.zeros(oracle.fp16_pool_bytes(L), np.uint8)
+    oracle.dequantize_to_fp16_pool(L, pool, pool16, bt, np.array(lens, np.int32))
+    q = W.kv_tensor(68, (1, 2, 4, 64)).numpy()[0]
+    a = oracle.decode_attention(L, pool, q, bt, np.array(lens, np.int32), 0.125)
+    b_ = oracle.fp16_decode_attention(L, pool16, q, bt, np.array(lens, np.int32), 0.125)
+    assert np.array_equal(a, b_)
+
+
+def test_fp16_single_token_returns_its_value():
+    L = oracle.Layout(1, 64, 16, 32, 64, 2)
+    pool16 = np.zeros(oracle.fp16_pool_bytes(L), np.uint8)
+    k = W.kv_tensor(69, (1, 1, 1, 64)).numpy()
+    v = W.kv_tensor(70, (1, 1, 1, 64)).numpy()
+    bt = np.array([[1]], np.int32)
+    oracle.fp16_append(L, pool16, k, v, bt, np.array([0], np.int32))
+    q = W.kv_tensor(71, (1, 1, 2, 64)).numpy()[0]
+    got = oracle.fp16_decode_attention(L, pool16, q, bt, np.array([1], np.int32), 0.125)
+    assert np.array_equal(got[0, 0], v[0, 0, 0].astype(np.float64))
+    assert np.array_equal(got[0, 1], v[0, 0, 0].astype(np.float64))
