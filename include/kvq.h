@@ -207,6 +207,38 @@ int kvq_decode_step_window(const kvq_cache_config *cfg, void *pool, const void *
                            void *workspace, size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * The FP16 cache of the latency comparison (section 7.4 of the INT4 state-machine page:
+ * FP16 attention; INT4 dequantized first and then attended; INT4 dequantized inside the
+ * operator).  Same pages and block table as the INT4 cache, same cfg (the group sizes
+ * are not used): block (page, kv head) at (page * Hkv + h) * 4 * P * d bytes holds K
+ * rows P x d fp16, then V rows P x d fp16.
+ *
+ * kvq_fp16_pool_bytes: num_pages * Hkv * 4 * P * d; 0 if cfg is invalid.
+ * kvq_fp16_append: as kvq_quantize_append, storing the fp16 rows unchanged.
+ * kvq_dequantize_to_fp16_pool: every position 0 .. seq_lens[b]-1 of the INT4 pool,
+ *   dequantized ((nibble - 8) * scale, rounded to fp16 nearest-even), into the FP16 pool
+ *   at the same page and slot.  max_len >= every seq_lens[b] (sizes the grid); batch at
+ *   most 65535.  Pages or positions out of range are skipped and flagged in *status.
+ * kvq_fp16_decode_workspace_bytes / kvq_fp16_decode_attention: as the INT4 calls of the
+ *   same names, over the FP16 pool (head_dim 128, page sizes 16/32/64, up to 8 query
+ *   heads per kv head).  The workspace sizes differ from the INT4 ones.
+ * Return codes as for the INT4 calls.
+ */
+size_t kvq_fp16_pool_bytes(const kvq_cache_config *cfg);
+int kvq_fp16_append(const kvq_cache_config *cfg, void *pool16, const void *k, const void *v,
+                    const int32_t *block_table, int32_t max_blocks, const int32_t *start_pos, int32_t batch,
+                    int32_t n_new, uint32_t *status, kvq_stream_t stream);
+int kvq_dequantize_to_fp16_pool(const kvq_cache_config *cfg, const void *pool, void *pool16,
+                                const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                                int32_t batch, int32_t max_len, uint32_t *status, kvq_stream_t stream);
+size_t kvq_fp16_decode_workspace_bytes(const kvq_cache_config *cfg, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_len);
+int kvq_fp16_decode_attention(const kvq_cache_config *cfg, const void *pool16, const void *q,
+                              const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                              int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                              float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
  * Decode attention that allocates nothing, for callers that cannot provide a
  * workspace: a plugin inside a host engine that owns no device allocator, an
  * embedded or real-time runtime with a fixed memory budget that forbids allocation

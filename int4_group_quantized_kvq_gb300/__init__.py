@@ -26,6 +26,12 @@ from .binding import (  # noqa: F401
     kvq_decode_step,
     kvq_decode_step_window,
     kvq_decode_workspace_bytes,
+    kvq_dequantize_to_fp16_pool,
+    kvq_fp16_append,
+    kvq_fp16_decode_attention,
+    kvq_fp16_decode_workspace_bytes,
+    kvq_fp16_pool_bytes,
+    new_fp16_workspace,
     kvq_dequantize,
     kvq_last_error,
     kvq_pool_bytes,

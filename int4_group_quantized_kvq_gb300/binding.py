@@ -21,7 +21,8 @@ KVQ_FLAG_BAD_PAGE, KVQ_FLAG_BAD_POSITION, KVQ_FLAG_WAIT_TIMEOUT, KVQ_FLAG_STALE_
 ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
                "kvq_decode_attention", "kvq_dequantize", "kvq_read_status", "kvq_last_error", "kvq_version",
                "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_attention_window",
-               "kvq_decode_step_window")
+               "kvq_decode_step_window", "kvq_fp16_pool_bytes", "kvq_fp16_append", "kvq_dequantize_to_fp16_pool",
+               "kvq_fp16_decode_workspace_bytes", "kvq_fp16_decode_attention")
 
 
 class KvqError(RuntimeError):
@@ -74,6 +75,16 @@ def lib() -> C.CDLL:
         L.kvq_decode_step_window.argtypes = [cfgp, P, P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, I32, I32, P,
                                              P, SZ, P]
         L.kvq_decode_step_window.restype = C.c_int
+        L.kvq_fp16_pool_bytes.argtypes = [cfgp]
+        L.kvq_fp16_pool_bytes.restype = SZ
+        L.kvq_fp16_append.argtypes = [cfgp, P, P, P, P, I32, P, I32, I32, P, P]
+        L.kvq_fp16_append.restype = C.c_int
+        L.kvq_dequantize_to_fp16_pool.argtypes = [cfgp, P, P, P, I32, P, I32, I32, P, P]
+        L.kvq_dequantize_to_fp16_pool.restype = C.c_int
+        L.kvq_fp16_decode_workspace_bytes.argtypes = [cfgp, I32, I32, I32]
+        L.kvq_fp16_decode_workspace_bytes.restype = SZ
+        L.kvq_fp16_decode_attention.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
+        L.kvq_fp16_decode_attention.restype = C.c_int
         L.kvq_dequantize.argtypes = [cfgp, P, P, I32, I32, I32, I32, P, P, I32, P, P]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_read_status.argtypes = [P, C.POINTER(C.c_uint32), P]
@@ -259,3 +270,62 @@ def new_workspace(cfg: CacheConfig, batch: int, num_q_heads: int, max_len: int, 
     """A zeroed decode workspace of the size the library asks for (allocated by torch, not the library)."""
     n = kvq_decode_workspace_bytes(cfg, batch, num_q_heads, max_len)
     return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------
+# The FP16 cache of the latency comparison (same pages; K then V rows in fp16).
+# ---------------------------------------------------------------------------
+
+def kvq_fp16_pool_bytes(cfg: CacheConfig) -> int:
+    return int(lib().kvq_fp16_pool_bytes(C.byref(cfg)))
+
+
+def kvq_fp16_append(cfg: CacheConfig, pool16: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                    block_table: torch.Tensor, start_pos: torch.Tensor, status: torch.Tensor | None = None,
+                    stream=None) -> None:
+    """fp16 rows k, v [B, n_new, Hkv, d] into the FP16 pool at start_pos[b] + t."""
+    B, n = int(k.shape[0]), int(k.shape[1])
+    rc = lib().kvq_fp16_append(
+        C.byref(cfg), _dev(pool16, "pool16", torch.uint8), _dev(k, "k", torch.float16), _dev(v, "v", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(start_pos, "start_pos", torch.int32), B, n, None if status is None else _dev(status, "status"),
+        _stream(stream))
+    _check(rc)
+
+
+def kvq_dequantize_to_fp16_pool(cfg: CacheConfig, pool: torch.Tensor, pool16: torch.Tensor,
+                                block_table: torch.Tensor, seq_lens: torch.Tensor, max_len: int,
+                                status: torch.Tensor | None = None, stream=None) -> None:
+    """Every attended position of the INT4 pool, dequantized to fp16, into the FP16 pool."""
+    rc = lib().kvq_dequantize_to_fp16_pool(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(pool16, "pool16", torch.uint8),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), int(seq_lens.shape[0]), int(max_len),
+        None if status is None else _dev(status, "status"), _stream(stream))
+    _check(rc)
+
+
+def kvq_fp16_decode_workspace_bytes(cfg: CacheConfig, batch: int, num_q_heads: int, max_len: int) -> int:
+    n = int(lib().kvq_fp16_decode_workspace_bytes(C.byref(cfg), batch, num_q_heads, max_len))
+    if n == 0:
+        raise KvqError(KVQ_EINVAL, kvq_last_error())
+    return n
+
+
+def new_fp16_workspace(cfg: CacheConfig, batch: int, num_q_heads: int, max_len: int, device="cuda") -> torch.Tensor:
+    return torch.zeros(kvq_fp16_decode_workspace_bytes(cfg, batch, num_q_heads, max_len), dtype=torch.uint8,
+                       device=device)
+
+
+def kvq_fp16_decode_attention(cfg: CacheConfig, pool16: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
+                              seq_lens: torch.Tensor, max_len: int, softmax_scale: float, out: torch.Tensor,
+                              workspace: torch.Tensor, stream=None) -> None:
+    """Decode attention over the FP16 cache; arguments as kvq_decode_attention."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_fp16_decode_attention(
+        C.byref(cfg), _dev(pool16, "pool16", torch.uint8), _dev(q, "q", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
+        _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(rc)

@@ -32,6 +32,8 @@ int decode_occupancy_gk32_win(const DecodeArgs& a, const DecodePlan& plan, size_
 int decode_occupancy_gk64_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk128_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 cudaError_t launch_combine(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_fp16(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+int decode_occupancy_fp16(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 
 namespace {
 constexpr int kMaxStages = 8;           // deepest unit ring per warp
@@ -50,13 +52,14 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     if (r < 1 || r > 8) return cudaErrorInvalidValue;
     // four kv heads per unit for 16-token pages (a 4-block unit then stays near the size
     // of one larger page); larger pages are big enough copies on their own
-    plan->hk = (r == 1 && a.Hkv % 4 == 0 && a.L.P == 16) ? 4 : 1;
+    plan->hk = (!a.fp16 && r == 1 && a.Hkv % 4 == 0 && a.L.P == 16) ? 4 : 1;
     plan->hs = (plan->hk == 1 && r > 4) ? 2 : 1;
     const int hg = a.Hkv / plan->hk;
     const int kWarpsPerCta = 4;  // the kernel's CTA size
     const int ns = plan->hk * r;
-    const size_t unit = static_cast<size_t>(a.L.bytes) * plan->hk;
-    // the CTA merge stages a warp's part (4 slots x (d + 2) floats) in a unit buffer
+    // the FP16 cache's unit is one page of one kv head: K and V rows, P x d fp16 each
+    const size_t unit = a.fp16 ? static_cast<size_t>(4) * a.L.P * a.L.d : static_cast<size_t>(a.L.bytes) * plan->hk;
+    // a warp stages its partial (4 slots x d floats) in a unit buffer
     if (unit < static_cast<size_t>(4 * (a.L.d + 2)) * sizeof(float)) return cudaErrorInvalidValue;
 
     // Resident CTAs are limited by registers; give each warp as deep a ring of unit
@@ -66,6 +69,7 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
                kCtlBytes + round_up(static_cast<size_t>(3 * a.B + 1) * 4, 16);
     };
     auto occ_for = [&](size_t smem) {
+        if (a.fp16) return decode_occupancy_fp16(a, *plan, smem);
         const bool w = a.window > 0;
         switch (a.L.Gk) {
             case 32: return w ? decode_occupancy_gk32_win(a, *plan, smem) : decode_occupancy_gk32(a, *plan, smem);
@@ -82,6 +86,9 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     err = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (err != cudaSuccess) return err;
     int stages = 2;
+    // a 64-token FP16 page (32 KB) leaves room for one stage per warp only: its copy is
+    // then not overlapped with the arithmetic
+    if (a.fp16 && smem_for(stages) > static_cast<size_t>(smem_max)) stages = 1;
     if (smem_for(stages) > static_cast<size_t>(smem_max)) return cudaErrorInvalidConfiguration;
     const int occ = occ_for(smem_for(stages));
     if (occ <= 0) return a.L.Gk == 32 || a.L.Gk == 64 || a.L.Gk == 128 ? cudaErrorInvalidConfiguration
@@ -123,6 +130,11 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     cudaError_t e;
     const bool w = a.window > 0;
+    if (a.fp16) {
+        e = decode_run_fp16(a, plan, stream);
+        if (e != cudaSuccess) return e;
+        return launch_combine(a, plan, stream);
+    }
     switch (a.L.Gk) {
         case 32: e = w ? decode_run_gk32_win(a, plan, stream) : decode_run_gk32(a, plan, stream); break;
         case 64: e = w ? decode_run_gk64_win(a, plan, stream) : decode_run_gk64(a, plan, stream); break;

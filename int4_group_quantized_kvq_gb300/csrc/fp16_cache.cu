@@ -1,0 +1,122 @@
+// fp16_cache.cu -- the FP16 paged cache of the latency comparison ("LLM long-context
+// inference: managing the KV cache with an INT4 state machine", section 7.4): its append,
+// and the dequantization of the INT4 cache into it (the "dequantize first, then attend"
+// arm).  Block (page, kv head) at (page * Hkv + h) * 4 * P * d bytes: K rows P x d fp16,
+// then V rows P x d fp16.
+//
+// Both kernels move 16-byte pieces: one thread per 8 elements of one row.
+#include <cuda_fp16.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+__device__ __forceinline__ uint8_t* fp16_row(uint8_t* pool16, int Hkv, int d, int P, long long page, int h, int is_v,
+                                             int slot) {
+    return pool16 + (page * Hkv + h) * (4LL * P * d) + (static_cast<long long>(is_v) * P + slot) * d * 2;
+}
+
+// rows k, v [B, n_new, Hkv, d] fp16 -> the FP16 pool at start_pos[b] + t
+__global__ void __launch_bounds__(256) fp16_append_kernel(Fp16AppendArgs a) {
+    const int words = a.d / 8;
+    const long long total = 2LL * a.B * a.n_new * a.Hkv * words;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int w = static_cast<int>(i % words);
+        const long long r = i / words;  // ((b * n_new + t) * Hkv + h) * 2 + is_v
+        const int is_v = static_cast<int>(r & 1);
+        const long long row = r >> 1;
+        const int h = static_cast<int>(row % a.Hkv);
+        const long long bt_ = row / a.Hkv;
+        const int t = static_cast<int>(bt_ % a.n_new);
+        const int b = static_cast<int>(bt_ / a.n_new);
+        const long long pos = static_cast<long long>(a.start_pos[b]) + t;
+        const long long pidx = pos >= 0 ? pos / a.P : -1;
+        if (pidx < 0 || pidx >= a.max_blocks) {
+            if (w == 0 && is_v == 0) raise_flag(a.status, KVQ_FLAG_BAD_POSITION);
+            continue;
+        }
+        const int page = a.block_table[static_cast<long long>(b) * a.max_blocks + pidx];
+        if (page < 0 || page >= a.num_pages) {
+            if (w == 0 && is_v == 0) raise_flag(a.status, KVQ_FLAG_BAD_PAGE);
+            continue;
+        }
+        const uint4 src = reinterpret_cast<const uint4*>((is_v ? a.v : a.k) + row * a.d)[w];
+        uint8_t* dst = fp16_row(a.pool16, a.Hkv, a.d, a.P, page, h, is_v, static_cast<int>(pos % a.P));
+        reinterpret_cast<uint4*>(dst)[w] = src;
+    }
+}
+
+// positions 0 .. seq_lens[b]-1 of the INT4 pool -> the FP16 pool, same pages and slots.
+// One CTA per (page index j, sequence b) covers the Hkv blocks of that page; each value
+// is (nibble - 8) * scale, exact in fp32, rounded to fp16 (nearest even).
+__global__ void __launch_bounds__(256) dequantize_to_fp16_kernel(Fp16DequantArgs a) {
+    const int b = blockIdx.y;
+    const long long j = blockIdx.x;
+    int len = a.seq_lens[b];
+    len = len < 0 ? 0 : len;
+    const long long need = (static_cast<long long>(len) + a.L.P - 1) / a.L.P;
+    if (j >= need) return;
+    if (j >= a.max_blocks) {
+        if (threadIdx.x == 0) raise_flag(a.status, KVQ_FLAG_BAD_POSITION);
+        return;
+    }
+    const int page = a.block_table[static_cast<long long>(b) * a.max_blocks + j];
+    if (page < 0 || page >= a.num_pages) {
+        if (threadIdx.x == 0) raise_flag(a.status, KVQ_FLAG_BAD_PAGE);
+        return;
+    }
+    const int d = a.L.d;
+    const int words = d / 8;
+    const long long rows_here = static_cast<long long>(len) - j * a.L.P;  // positions in this page
+    const int slots = rows_here < a.L.P ? static_cast<int>(rows_here) : a.L.P;
+    const int total = a.Hkv * 2 * slots * words;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int w = i % words;
+        const int r = i / words;  // (h * 2 + is_v) * slots + slot
+        const int slot = r % slots;
+        const int is_v = (r / slots) & 1;
+        const int h = r / (2 * slots);
+        const uint8_t* blk = a.pool + (static_cast<long long>(page) * a.Hkv + h) * a.L.bytes;
+        const int G = is_v ? a.L.Gv : a.L.Gk;
+        const uint32_t word = reinterpret_cast<const uint32_t*>(blk + (is_v ? a.L.v_codes : 0) + slot * (d / 2))[w];
+        const float s = __half2float(
+            reinterpret_cast<const __half*>(blk + (is_v ? a.L.v_scales : a.L.k_scales) + slot * (d / G) * 2)[(w * 8) / G]);
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = static_cast<float>(static_cast<int>((word >> (4 * k)) & 0xFu) - 8) * s;
+        uint4 pk;
+        pk.x = pack_h2(v[0], v[1]);
+        pk.y = pack_h2(v[2], v[3]);
+        pk.z = pack_h2(v[4], v[5]);
+        pk.w = pack_h2(v[6], v[7]);
+        reinterpret_cast<uint4*>(fp16_row(a.pool16, a.Hkv, d, a.L.P, page, h, is_v, slot))[w] = pk;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fp16_append(const Fp16AppendArgs& a, cudaStream_t stream) {
+    const long long total = 2LL * a.B * a.n_new * a.Hkv * (a.d / 8);
+    if (total == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long want = (total + 255) / 256;
+    const long long grid = want < 8LL * sms ? want : 8LL * sms;
+    fp16_append_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize_to_fp16(const Fp16DequantArgs& a, long long max_pages, cudaStream_t stream) {
+    if (max_pages <= 0 || a.B <= 0) return cudaSuccess;
+    if (max_pages > 0x7fffffffLL || a.B > 65535) return cudaErrorInvalidValue;
+    dequantize_to_fp16_kernel<<<dim3(static_cast<unsigned>(max_pages), static_cast<unsigned>(a.B)), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -108,8 +108,9 @@ int kvq_quantize_append(const kvq_cache_config* cfg, void* pool, const void* k, 
     return ok();
 }
 
-size_t kvq_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
-                                  int32_t max_len) {
+namespace {
+size_t workspace_bytes_impl(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads, int32_t max_len,
+                            bool fp16) {
     if (check_cfg(cfg) != KVQ_OK) return 0;
     if (batch < 1 || num_q_heads < 1 || max_len < 0 || num_q_heads % cfg->num_kv_heads) {
         fail(KVQ_EINVAL, "invalid batch / num_q_heads / max_len");
@@ -120,6 +121,7 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, in
     a.Hq = num_q_heads;
     a.Hkv = cfg->num_kv_heads;
     a.max_len = max_len;
+    a.fp16 = fp16;
     a.L = kvq::block_layout(*cfg);
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
@@ -131,12 +133,23 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, in
     ok();
     return plan.ws_bytes;
 }
+}  // namespace
+
+size_t kvq_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_len) {
+    return workspace_bytes_impl(cfg, batch, num_q_heads, max_len, false);
+}
+
+size_t kvq_fp16_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_len) {
+    return workspace_bytes_impl(cfg, batch, num_q_heads, max_len, true);
+}
 
 namespace {
 int decode_attention_impl(const kvq_cache_config* cfg, const void* pool, const void* q, const int32_t* block_table,
                           int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
                           int32_t max_len, float softmax_scale, int32_t window, int32_t sinks, float* out,
-                          void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+                          void* workspace, size_t workspace_bytes, kvq_stream_t stream, bool fp16 = false) {
     if (int e = check_cfg(cfg)) return e;
     if (batch < 0 || num_q_heads < 1 || max_len < 0)
         return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
@@ -170,6 +183,7 @@ int decode_attention_impl(const kvq_cache_config* cfg, const void* pool, const v
     a.softmax_scale = softmax_scale;
     a.window = window;
     a.sinks = sinks;
+    a.fp16 = fp16;
     a.L = kvq::block_layout(*cfg);
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
@@ -256,6 +270,14 @@ int kvq_decode_attention_window(const kvq_cache_config* cfg, const void* pool, c
                                  softmax_scale, window, sinks, out, workspace, workspace_bytes, stream);
 }
 
+int kvq_fp16_decode_attention(const kvq_cache_config* cfg, const void* pool16, const void* q,
+                              const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                              int32_t num_q_heads, int32_t max_len, float softmax_scale, float* out, void* workspace,
+                              size_t workspace_bytes, kvq_stream_t stream) {
+    return decode_attention_impl(cfg, pool16, q, block_table, max_blocks, seq_lens, batch, num_q_heads, max_len,
+                                 softmax_scale, 0, 0, out, workspace, workspace_bytes, stream, true);
+}
+
 int kvq_decode_step(const kvq_cache_config* cfg, void* pool, const void* k_new, const void* v_new,
                     const int32_t* append_pos, const void* q, const int32_t* block_table, int32_t max_blocks,
                     const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
@@ -301,6 +323,71 @@ int kvq_dequantize(const kvq_cache_config* cfg, const void* pool, const int32_t*
     a.L = kvq::block_layout(*cfg);
     cudaError_t e = kvq::launch_dequantize(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "kvq_dequantize launch");
+    return ok();
+}
+
+size_t kvq_fp16_pool_bytes(const kvq_cache_config* cfg) {
+    if (check_cfg(cfg) != KVQ_OK) return 0;
+    return static_cast<size_t>(cfg->num_pages) * cfg->num_kv_heads * 4u * cfg->page_size * cfg->head_dim;
+}
+
+int kvq_fp16_append(const kvq_cache_config* cfg, void* pool16, const void* k, const void* v,
+                    const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
+                    int32_t n_new, uint32_t* status, kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || n_new < 0) return fail(KVQ_EINVAL, "batch %d / n_new %d negative", batch, n_new);
+    if (batch == 0 || n_new == 0) return ok();
+    if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
+    if (!pool16 || !k || !v || !block_table || !start_pos) return fail(KVQ_EINVAL, "NULL device pointer");
+    if (!aligned(pool16, 16) || !aligned(k, 16) || !aligned(v, 16))
+        return fail(KVQ_EINVAL, "pool16, k and v must be 16-byte aligned");
+    if (!aligned(block_table, 4) || !aligned(start_pos, 4) || (status && !aligned(status, 4)))
+        return fail(KVQ_EINVAL, "int32/uint32 arguments must be 4-byte aligned");
+    kvq::Fp16AppendArgs a;
+    a.pool16 = static_cast<uint8_t*>(pool16);
+    a.k = static_cast<const __half*>(k);
+    a.v = static_cast<const __half*>(v);
+    a.block_table = block_table;
+    a.start_pos = start_pos;
+    a.status = status;
+    a.max_blocks = max_blocks;
+    a.B = batch;
+    a.n_new = n_new;
+    a.Hkv = cfg->num_kv_heads;
+    a.d = cfg->head_dim;
+    a.P = cfg->page_size;
+    a.num_pages = cfg->num_pages;
+    cudaError_t e = kvq::launch_fp16_append(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_fp16_append launch");
+    return ok();
+}
+
+int kvq_dequantize_to_fp16_pool(const kvq_cache_config* cfg, const void* pool, void* pool16,
+                                const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                                int32_t batch, int32_t max_len, uint32_t* status, kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || max_len < 0) return fail(KVQ_EINVAL, "batch %d / max_len %d negative", batch, max_len);
+    if (batch > 65535) return fail(KVQ_EUNSUPPORTED, "batch %d > 65535", batch);
+    if (batch == 0 || max_len == 0) return ok();
+    if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
+    if (!pool || !pool16 || !block_table || !seq_lens) return fail(KVQ_EINVAL, "NULL device pointer");
+    if (!aligned(pool, 16) || !aligned(pool16, 16)) return fail(KVQ_EINVAL, "pool and pool16 must be 16-byte aligned");
+    if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || (status && !aligned(status, 4)))
+        return fail(KVQ_EINVAL, "int32/uint32 arguments must be 4-byte aligned");
+    kvq::Fp16DequantArgs a;
+    a.pool = static_cast<const uint8_t*>(pool);
+    a.pool16 = static_cast<uint8_t*>(pool16);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.status = status;
+    a.max_blocks = max_blocks;
+    a.B = batch;
+    a.Hkv = cfg->num_kv_heads;
+    a.num_pages = cfg->num_pages;
+    a.L = kvq::block_layout(*cfg);
+    const long long max_pages = (static_cast<long long>(max_len) + cfg->page_size - 1) / cfg->page_size;
+    cudaError_t e = kvq::launch_dequantize_to_fp16(a, max_pages, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_dequantize_to_fp16_pool launch");
     return ok();
 }
 

@@ -112,7 +112,32 @@ struct DecodeArgs {
     // sliding window with sink tokens: the last `window` positions (0: all) and the first `sinks`
     int32_t window = 0;
     int32_t sinks = 0;
+    // attention over the FP16 cache instead of the INT4 one (the comparison's baseline)
+    bool fp16 = false;
 };
+
+// The FP16 cache of the latency comparison: block (page, kv head) holds K rows P x d fp16,
+// then V rows P x d fp16.
+struct Fp16AppendArgs {
+    uint8_t* pool16;
+    const __half* k;
+    const __half* v;
+    const int32_t* block_table;
+    const int32_t* start_pos;
+    uint32_t* status;
+    int32_t max_blocks, B, n_new, Hkv, d, P, num_pages;
+};
+struct Fp16DequantArgs {
+    const uint8_t* pool;
+    uint8_t* pool16;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    uint32_t* status;
+    int32_t max_blocks, B, Hkv, num_pages;
+    BlockLayout L;
+};
+cudaError_t launch_fp16_append(const Fp16AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_dequantize_to_fp16(const Fp16DequantArgs& a, long long max_pages, cudaStream_t stream);
 
 // Returns cudaErrorInvalidValue for a geometry no kernel instance covers.
 cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan);

@@ -23,7 +23,7 @@ def built():
 def header_functions() -> set[str]:
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", text))
+    return set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", text))
 
 
 def test_header_declares_the_abi():
@@ -34,7 +34,7 @@ def test_header_declares_the_abi():
 
 def test_library_exports_every_declared_symbol(built):
     out = subprocess.run(["nm", "-D", "--defined-only", built], capture_output=True, text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (kvq_[a-z_]+)\b", out))
+    exported = set(re.findall(r"\bT (kvq_[a-z0-9_]+)\b", out))
     missing = header_functions() - exported
     assert not missing, f"declared but not exported: {missing}"
     lib = C.CDLL(built)
