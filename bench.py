@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--graph-steps", type=int, default=200, help="steps captured per CUDA graph")
     ap.add_argument("--eager", action="store_true", help="launch every step from Python instead of graphs")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--compare", action="store_true",
+                    help="also time the latency comparison: FP16 cache, INT4 dequantized then attended, INT4 fused")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-quality", action="store_true", help="skip the dequantization quality report")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
@@ -333,6 +335,15 @@ def run_kvq(args, world, rank, local):
                                         status=cache.status)
 
     prefill(caches[0])
+    # the comparison's FP16 cache holds the same fp16 history
+    pool16 = None
+    if getattr(args, "compare", False):
+        pool16 = torch.zeros(kvq.kvq_fp16_pool_bytes(cfg), dtype=torch.uint8, device=dev)
+        if same_ctx:
+            kvq.kvq_fp16_append(cfg, pool16, hist[0][0], hist[0][1], caches[0].block_table, zero)
+        else:
+            for b, (kb, vb) in enumerate(hist):
+                kvq.kvq_fp16_append(cfg, pool16, kb, vb, caches[0].block_table[b:b + 1], zero)
     torch.cuda.synchronize()
     qt = []
     for _ in range(3):
@@ -353,6 +364,8 @@ def run_kvq(args, world, rank, local):
     idx = pos.long().view(-1, 1, 1, 1).expand(-1, 1, wl.Hkv, wl.d)
     k_new = torch.gather(k_all, 1, idx).contiguous()
     v_new = torch.gather(v_all, 1, idx).contiguous()
+    if pool16 is not None:  # the new token, as the INT4 step appends it
+        kvq.kvq_fp16_append(cfg, pool16, k_new, v_new, caches[0].block_table, pos)
     del k_all, v_all, hist
     torch.cuda.empty_cache()
     seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
@@ -430,6 +443,64 @@ def run_kvq(args, world, rank, local):
         d1.record(stream)
     stream.synchronize()
     decode_s = d0.elapsed_time(d1) * 1e-3 / (n_rep * D)
+
+    # ---- the latency comparison ("LLM long-context inference: managing the KV cache with an
+    # INT4 state machine" section 7.4): FP16 attention; INT4 dequantized to an FP16 pool and
+    # then attended; INT4 dequantized inside the operator (decode_s above).  Same workload,
+    # same timing (a graph of D back-to-back calls, replayed) ----
+    comparison = None
+    if pool16 is not None:
+        cfg16 = cfg
+        ws16 = kvq.new_fp16_workspace(cfg16, wl.B, wl.Hq, wl.max_len, device=dev)
+        deq16 = torch.empty_like(pool16)
+        out16 = torch.empty_like(out)
+        bt0 = caches[0].block_table
+        scale = 1.0 / math.sqrt(wl.d)
+
+        def fp16_attend():
+            kvq.kvq_fp16_decode_attention(cfg16, pool16, q, bt0, seq_lens, wl.max_len, scale, out16, ws16,
+                                          stream=stream)
+
+        def deq_then_attend():
+            kvq.kvq_dequantize_to_fp16_pool(cfg16, caches[0].pool, deq16, bt0, seq_lens, wl.max_len, stream=stream)
+            kvq.kvq_fp16_decode_attention(cfg16, deq16, q, bt0, seq_lens, wl.max_len, scale, out16, ws16,
+                                          stream=stream)
+
+        def per_call(fn, calls=50, reps=4):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                fn()
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(calls):
+                    fn()
+            with torch.cuda.stream(stream):
+                g.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            stream.synchronize()
+            return e0.elapsed_time(e1) * 1e-3 / (calls * reps)
+
+        t16 = per_call(fp16_attend)
+        tdq = per_call(deq_then_attend)
+        fp16_bytes = 4 * wl.d * sum(wl.seq_lens) * wl.Hkv
+        comparison = {
+            "what": "decode attention latency on the bench workload: FP16 cache; INT4 dequantized to an FP16 pool "
+                    "then attended; INT4 dequantized inside the operator (back-to-back calls in CUDA graphs)",
+            "fp16_us": t16 * 1e6, "fp16_gbs": fp16_bytes / t16 / 1e9,
+            "int4_dequant_then_attend_us": tdq * 1e6,
+            "int4_fused_us": decode_s * 1e6,
+            "fp16_bytes": fp16_bytes, "int4_bytes": wl.decode_bytes(),
+            "fused_speedup_vs_fp16": t16 / decode_s, "fused_speedup_vs_dequant_then_attend": tdq / decode_s,
+        }
+        if rank == 0:
+            print(f"[compare] fp16 {t16 * 1e6:.1f} us ({fp16_bytes / t16 / 1e9:.0f} GB/s), dequant+attend "
+                  f"{tdq * 1e6:.1f} us, int4 fused {decode_s * 1e6:.1f} us", file=sys.stderr)
     # the step leaves the output of the last decode step in `out` for e2e and checks
     flags = max(c.flags() for c in caches)
     if world > 1:
@@ -525,6 +596,8 @@ def run_kvq(args, world, rank, local):
         "status_flags": flags,
         "clocks": clocks,
     }
+    if comparison is not None:
+        res["comparison"] = comparison
     if not args.no_quality:
         res["quality"] = quality_report(dev)
     if world == 1 and not args.no_cpu_baseline:
