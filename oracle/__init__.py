@@ -69,6 +69,10 @@ def lib() -> C.CDLL:
         L.kvq_oracle_fp16_decode_attention.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
                                                        C.c_int, C.c_int, C.c_double, C.c_void_p] + [C.c_int] * 4
         L.kvq_oracle_fp16_decode_attention.restype = C.c_int
+        L.kvq_oracle_mixed_decode_attention.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
+                                                        C.c_int, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                                        C.c_double, C.c_void_p] + [C.c_int] * 7
+        L.kvq_oracle_mixed_decode_attention.restype = C.c_int
         _lib = L
     return _lib
 
@@ -249,4 +253,23 @@ def fp16_decode_attention(L: Layout, pool16: np.ndarray, q: np.ndarray, block_ta
     rc = lib().kvq_oracle_fp16_decode_attention(_ptr(pool16), _ptr(q), _ptr(bt), int(bt.shape[1]), _ptr(sl), B, Hq,
                                                 float(softmax_scale), _ptr(out), L.Hkv, L.d, L.P, L.num_pages)
     _check(rc, "fp16_decode_attention")
+    return out
+
+
+def mixed_decode_attention(L: Layout, pool: np.ndarray, block_table: np.ndarray, pool16: np.ndarray,
+                           block_table16: np.ndarray, num_pages16: int, q: np.ndarray, seq_lens: np.ndarray,
+                           residual: int, softmax_scale: float) -> np.ndarray:
+    """fp64 decode attention with the last `residual` positions read from the FP16 pool and the
+    older ones from the INT4 pool ("LLM long-context inference: managing the KV cache with an
+    INT4 state machine" section 8.3).  q: fp16 [B, Hq, d] -> fp64 [B, Hq, d]."""
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    bt16 = np.ascontiguousarray(block_table16, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, _ = q.shape
+    out = np.zeros((B, Hq, L.d), dtype=np.float64)
+    rc = lib().kvq_oracle_mixed_decode_attention(_ptr(pool), _ptr(bt), int(bt.shape[1]), _ptr(pool16), _ptr(bt16),
+                                                 int(bt16.shape[1]), _ptr(q), _ptr(sl), B, Hq, int(residual),
+                                                 float(softmax_scale), _ptr(out), *L.geom, int(num_pages16))
+    _check(rc, "mixed_decode_attention")
     return out

@@ -525,3 +525,68 @@ int kvq_oracle_fp16_decode_attention(const uint8_t *pool16, const uint16_t *q, c
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Mixed precision ([S] section 8.3, item 1: quantize the KV of old tokens   */
+/* to INT4 first and keep recent tokens in FP16): for a sequence of len      */
+/* positions, position t < len - residual is read from the INT4 pool, and    */
+/* t >= len - residual from the FP16 pool (same page table layout each, own  */
+/* block tables).  Plain decode attention over all len positions, in fp64.   */
+/* ------------------------------------------------------------------------ */
+int kvq_oracle_mixed_decode_attention(const uint8_t *pool, const int32_t *block_table, int max_blocks,
+                                      const uint8_t *pool16, const int32_t *block_table16, int max_blocks16,
+                                      const uint16_t *q, const int32_t *seq_lens, int B, int Hq, int residual,
+                                      double softmax_scale, double *out, int Hkv, int d, int P, int Gk, int Gv,
+                                      int num_pages, int num_pages16) {
+    layout_t L;
+    if (make_layout(&L, Hkv, d, P, Gk, Gv, num_pages) || d > 256 || Hq <= 0 || Hq % Hkv || residual < 0)
+        return ORACLE_EINVAL;
+    int grp = Hq / Hkv;
+    float rk[256], rv[256];
+    for (int b = 0; b < B; ++b) {
+        int len = seq_lens[b];
+        if (len < 0) return ORACLE_ERANGE;
+        int split = len - residual > 0 ? len - residual : 0;  /* first FP16 position */
+        if ((split + P - 1) / P > max_blocks || (len + P - 1) / P > max_blocks16) return ORACLE_ERANGE;
+        for (int hq = 0; hq < Hq; ++hq) {
+            int hk = hq / grp;
+            const uint16_t *qrow = q + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            double *o = out + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            for (int i = 0; i < d; ++i) o[i] = 0.0;
+            if (len == 0) continue;
+            double zmax = -INFINITY, lsum = 0.0;
+            for (int pass = 0; pass < 2; ++pass) {
+                for (int t = 0; t < len; ++t) {
+                    double z = 0.0;
+                    const uint8_t *vrow16 = 0;
+                    if (t < split) {
+                        int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+                        if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+                        uint8_t *blk = block_ptr(&L, (uint8_t *)pool, page, hk);
+                        dequant_row(k_codes_row(&L, blk, t % P), k_scales_row(&L, blk, t % P), d, Gk, rk);
+                        dequant_row(v_codes_row(&L, blk, t % P), v_scales_row(&L, blk, t % P), d, Gv, rv);
+                        for (int i = 0; i < d; ++i) z += kvq_oracle_f16_to_f64(qrow[i]) * (double)rk[i];
+                    } else {
+                        int page = block_table16[(size_t)b * (size_t)max_blocks16 + (size_t)(t / P)];
+                        if (page < 0 || page >= num_pages16) return ORACLE_ERANGE;
+                        const uint8_t *kr = fp16_row((uint8_t *)pool16, Hkv, d, P, page, hk, 0, t % P);
+                        vrow16 = fp16_row((uint8_t *)pool16, Hkv, d, P, page, hk, 1, t % P);
+                        for (int i = 0; i < d; ++i)
+                            z += kvq_oracle_f16_to_f64(qrow[i]) * kvq_oracle_f16_to_f64(get_u16(kr + 2 * i));
+                    }
+                    z *= softmax_scale;
+                    if (pass == 0) {
+                        if (z > zmax) zmax = z;
+                        continue;
+                    }
+                    double e = exp(z - zmax);
+                    lsum += e;
+                    for (int i = 0; i < d; ++i)
+                        o[i] += e * (vrow16 ? kvq_oracle_f16_to_f64(get_u16(vrow16 + 2 * i)) : (double)rv[i]);
+                }
+            }
+            for (int i = 0; i < d; ++i) o[i] /= lsum;
+        }
+    }
+    return ORACLE_OK;
+}

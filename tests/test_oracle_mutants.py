@@ -51,6 +51,10 @@ MUTANTS = [
      "put_u16(kr + 2 * i, (uint16_t)(kvq_oracle_f32_to_f16(rk[i]) & 0xfffeu));"),
     ("fp16_attention_scale_dropped", "        z *= softmax_scale;\n                double wz",
      "        double wz"),
+    ("mixed_split_off_by_one", "                    if (t < split) {", "                    if (t <= split) {"),
+    ("mixed_fp16_part_from_int4_table",
+     "int page = block_table16[(size_t)b * (size_t)max_blocks16 + (size_t)(t / P)];",
+     "int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];"),
     ("last_token_dropped", "for (int t = 0; t < len; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk",
      "for (int t = 0; t < len - 1; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk"),
 ]

@@ -658,3 +658,58 @@ def test_fp16_single_token_returns_its_value():
     got = oracle.fp16_decode_attention(L, pool16, q, bt, np.array([1], np.int32), 0.125)
     assert np.array_equal(got[0, 0], v[0, 0, 0].astype(np.float64))
     assert np.array_equal(got[0, 1], v[0, 0, 0].astype(np.float64))
+
+
+# ----------------------------------------------------------------------------
+# mixed precision ("LLM long-context inference: managing the KV cache with an INT4
+# state machine" section 8.3): positions before len - residual from the INT4 pool,
+# the last `residual` from the FP16 pool
+# ----------------------------------------------------------------------------
+
+def _mixed_setup(seed, lens, Hkv=2, d=64, P=16):
+    L = oracle.Layout(Hkv, d, P, 32, 64, 24)
+    pool, bt, k, v = _build_cache(L, len(lens), lens, seed=seed)
+    # the FP16 pool: its own pages and block table, holding every position
+    n16 = 20
+    pool16 = np.zeros(n16 * Hkv * oracle.fp16_block_bytes(d, P), np.uint8)
+    L16 = oracle.Layout(Hkv, d, P, 32, 64, n16)
+    pages = [(n + P - 1) // P for n in lens]
+    order = W.permutation(seed + 77, n16).numpy()
+    bt16 = np.full((len(lens), max(pages)), -1, np.int32)
+    kk = 0
+    for b, n in enumerate(pages):
+        bt16[b, :n] = order[kk:kk + n]
+        kk += n
+    for b, n in enumerate(lens):
+        if n:
+            oracle.fp16_append(L16, pool16, k[b:b + 1, :n], v[b:b + 1, :n], bt16[b:b + 1], np.array([0], np.int32))
+    q = W.kv_tensor(seed + 5, (1, len(lens), 2 * Hkv, d)).numpy()[0]
+    return L, L16, pool, bt, pool16, bt16, n16, k, v, q
+
+
+def test_mixed_residual_zero_is_int4_attention_and_large_residual_is_fp16():
+    lens = [37, 16, 1, 0]
+    L, L16, pool, bt, pool16, bt16, n16, _, _, q = _mixed_setup(91, lens)
+    sl = np.array(lens, np.int32)
+    int4 = oracle.decode_attention(L, pool, q, bt, sl, 0.2)
+    fp16 = oracle.fp16_decode_attention(L16, pool16, q, bt16, sl, 0.2)
+    assert np.array_equal(oracle.mixed_decode_attention(L, pool, bt, pool16, bt16, n16, q, sl, 0, 0.2), int4)
+    for r in (37, 100):
+        assert np.array_equal(oracle.mixed_decode_attention(L, pool, bt, pool16, bt16, n16, q, sl, r, 0.2), fp16)
+
+
+@pytest.mark.parametrize("residual", [1, 5, 16, 20, 36])
+def test_mixed_brute_force(residual):
+    lens = [37, 23]
+    L, L16, pool, bt, pool16, bt16, n16, k, v, q = _mixed_setup(92 + residual, lens)
+    scale = 25.0  # large logits: the maximum must be subtracted
+    got = oracle.mixed_decode_attention(L, pool, bt, pool16, bt16, n16, q, np.array(lens, np.int32), residual, scale)
+    for b, n in enumerate(lens):
+        split = max(n - residual, 0)
+        dk, dv = oracle.dequantize(L, pool, bt, b, 0, n)
+        kk = np.concatenate([dk[:split].astype(np.float64), k[b, split:n].astype(np.float64)])
+        vv = np.concatenate([dv[:split].astype(np.float64), v[b, split:n].astype(np.float64)])
+        for hq in range(4):
+            s_ = (kk[:, hq // 2] @ q[b, hq].astype(np.float64)) * scale
+            ref = scipy.special.softmax(s_) @ vv[:, hq // 2]
+            np.testing.assert_allclose(got[b, hq], ref, rtol=1e-10, atol=1e-10)
