@@ -239,6 +239,31 @@ int kvq_fp16_decode_attention(const kvq_cache_config *cfg, const void *pool16, c
                               float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * Mixed-precision decode attention (section 8.3 of the INT4 state-machine page: quantize
+ * the KV of old tokens to INT4 first, keep recent tokens in FP16).  For sequence b of
+ * L = seq_lens[b] positions, positions [0, L - residual) are read from the INT4 pool
+ * (block_table, max_blocks) and [max(0, L - residual), L) from the FP16 pool
+ * (block_table16, max_blocks16, num_pages16 pages; the layout of kvq_fp16_append).  Both
+ * tables are indexed by the page number t / page_size of position t; block_table16 only
+ * needs valid entries for the pages that hold the last residual positions.  The result
+ * is plain decode attention over all L positions (kvq_decode_attention's conventions).
+ *   residual  >= 0; 0 is kvq_decode_attention over the INT4 pool alone.
+ *   workspace >= kvq_mixed_decode_workspace_bytes(cfg, batch, num_q_heads, max_len,
+ *             residual) bytes, 256-byte aligned; its first word is the status word.
+ * Three kernels run: the INT4 grid, the FP16 grid, and a combine of both grids'
+ * partials.
+ * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE or KVQ_ECUDA.
+ */
+size_t kvq_mixed_decode_workspace_bytes(const kvq_cache_config *cfg, int32_t batch, int32_t num_q_heads,
+                                        int32_t max_len, int32_t residual);
+int kvq_mixed_decode_attention(const kvq_cache_config *cfg, const void *pool, const int32_t *block_table,
+                               int32_t max_blocks, const void *pool16, const int32_t *block_table16,
+                               int32_t max_blocks16, int32_t num_pages16, const void *q, const int32_t *seq_lens,
+                               int32_t batch, int32_t num_q_heads, int32_t max_len, int32_t residual,
+                               float softmax_scale, float *out, void *workspace, size_t workspace_bytes,
+                               kvq_stream_t stream);
+
+/*
  * Decode attention that allocates nothing, for callers that cannot provide a
  * workspace: a plugin inside a host engine that owns no device allocator, an
  * embedded or real-time runtime with a fixed memory budget that forbids allocation

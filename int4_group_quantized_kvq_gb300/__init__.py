@@ -31,6 +31,8 @@ from .binding import (  # noqa: F401
     kvq_fp16_decode_attention,
     kvq_fp16_decode_workspace_bytes,
     kvq_fp16_pool_bytes,
+    kvq_mixed_decode_attention,
+    kvq_mixed_decode_workspace_bytes,
     new_fp16_workspace,
     kvq_dequantize,
     kvq_last_error,

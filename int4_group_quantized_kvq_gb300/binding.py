@@ -22,7 +22,8 @@ ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_
                "kvq_decode_attention", "kvq_dequantize", "kvq_read_status", "kvq_last_error", "kvq_version",
                "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_attention_window",
                "kvq_decode_step_window", "kvq_fp16_pool_bytes", "kvq_fp16_append", "kvq_dequantize_to_fp16_pool",
-               "kvq_fp16_decode_workspace_bytes", "kvq_fp16_decode_attention")
+               "kvq_fp16_decode_workspace_bytes", "kvq_fp16_decode_attention", "kvq_mixed_decode_workspace_bytes",
+               "kvq_mixed_decode_attention")
 
 
 class KvqError(RuntimeError):
@@ -85,6 +86,11 @@ def lib() -> C.CDLL:
         L.kvq_fp16_decode_workspace_bytes.restype = SZ
         L.kvq_fp16_decode_attention.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
         L.kvq_fp16_decode_attention.restype = C.c_int
+        L.kvq_mixed_decode_workspace_bytes.argtypes = [cfgp, I32, I32, I32, I32]
+        L.kvq_mixed_decode_workspace_bytes.restype = SZ
+        L.kvq_mixed_decode_attention.argtypes = [cfgp, P, P, I32, P, P, I32, I32, P, P, I32, I32, I32, I32, C.c_float,
+                                                 P, P, SZ, P]
+        L.kvq_mixed_decode_attention.restype = C.c_int
         L.kvq_dequantize.argtypes = [cfgp, P, P, I32, I32, I32, I32, P, P, I32, P, P]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_read_status.argtypes = [P, C.POINTER(C.c_uint32), P]
@@ -328,4 +334,29 @@ def kvq_fp16_decode_attention(cfg: CacheConfig, pool16: torch.Tensor, q: torch.T
         _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
         _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
         _stream(stream))
+    _check(rc)
+
+
+def kvq_mixed_decode_workspace_bytes(cfg: CacheConfig, batch: int, num_q_heads: int, max_len: int,
+                                     residual: int) -> int:
+    n = int(lib().kvq_mixed_decode_workspace_bytes(C.byref(cfg), batch, num_q_heads, max_len, residual))
+    if n == 0:
+        raise KvqError(KVQ_EINVAL, kvq_last_error())
+    return n
+
+
+def kvq_mixed_decode_attention(cfg: CacheConfig, pool: torch.Tensor, block_table: torch.Tensor,
+                               pool16: torch.Tensor, block_table16: torch.Tensor, num_pages16: int, q: torch.Tensor,
+                               seq_lens: torch.Tensor, max_len: int, residual: int, softmax_scale: float,
+                               out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Decode attention with the last `residual` positions read from the FP16 pool and the
+    older ones from the INT4 pool."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_mixed_decode_attention(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(block_table, "block_table", torch.int32),
+        int(block_table.shape[1]), _dev(pool16, "pool16", torch.uint8),
+        _dev(block_table16, "block_table16", torch.int32), int(block_table16.shape[1]), int(num_pages16),
+        _dev(q, "q", torch.float16), _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), int(residual),
+        float(softmax_scale), _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), _stream(stream))
     _check(rc)

@@ -8,11 +8,11 @@ namespace kvq {
 namespace decode {
 namespace {
 
-template <int R>
+template <int R, bool WIN>
 cudaError_t fp16_smem_attr(size_t smem) {
     static std::atomic<long long> granted{-1};
     if (static_cast<long long>(smem) <= granted.load(std::memory_order_acquire)) return cudaSuccess;
-    const cudaError_t err = cudaFuncSetAttribute(decode_fp16_kernel<128, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t err = cudaFuncSetAttribute(decode_fp16_kernel<128, R, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -24,18 +24,18 @@ cudaError_t fp16_smem_attr(size_t smem) {
     return cudaSuccess;
 }
 
-template <int R>
+template <int R, bool WIN>
 int fp16_occupancy(size_t smem) {
-    if (fp16_smem_attr<R>(smem) != cudaSuccess) return 0;
+    if (fp16_smem_attr<R, WIN>(smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_fp16_kernel<128, R>, 128, smem) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_fp16_kernel<128, R, WIN>, 128, smem) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-template <int R>
+template <int R, bool WIN>
 cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     KParams p{};
     p.pool = a.pool;
@@ -45,7 +45,10 @@ cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s
     p.ws_ml = reinterpret_cast<float*>(a.workspace + plan.ws_ml_offset);
     p.ws_o = reinterpret_cast<float*>(a.workspace + plan.ws_o_offset);
     p.ws_pre = reinterpret_cast<int32_t*>(a.workspace + plan.ws_pre_offset);
-    p.status = reinterpret_cast<uint32_t*>(a.workspace);
+    p.status = a.status ? a.status : reinterpret_cast<uint32_t*>(a.workspace);
+    p.len_sub = a.len_sub;
+    p.window = a.window;
+    p.sinks = a.sinks;
     p.B = a.B;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
@@ -61,7 +64,7 @@ cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s
     p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
     p.lg_p = 0;
     while ((1 << p.lg_p) < a.L.P) ++p.lg_p;
-    cudaError_t err = fp16_smem_attr<R>(plan.smem_bytes);
+    cudaError_t err = fp16_smem_attr<R, WIN>(plan.smem_bytes);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -73,7 +76,7 @@ cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, decode_fp16_kernel<128, R>, p);
+    err = cudaLaunchKernelEx(&cfg, decode_fp16_kernel<128, R, WIN>, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -81,24 +84,34 @@ cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s
 }  // namespace
 }  // namespace decode
 
-// query heads per kv head r in 1..8, rounded up to 1, 2, 4 or 8
-cudaError_t decode_run_fp16(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {
+// query heads per kv head r in 1..8, rounded up to 1, 2, 4 or 8; window instances when a
+// window is given
+template <bool WIN>
+cudaError_t run_r(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {
     const int r = a.Hq / a.Hkv;
-    if (r <= 1) return decode::fp16_run<1>(a, plan, s);
-    if (r <= 2) return decode::fp16_run<2>(a, plan, s);
-    if (r <= 4) return decode::fp16_run<4>(a, plan, s);
-    if (r <= 8) return decode::fp16_run<8>(a, plan, s);
+    if (r <= 1) return decode::fp16_run<1, WIN>(a, plan, s);
+    if (r <= 2) return decode::fp16_run<2, WIN>(a, plan, s);
+    if (r <= 4) return decode::fp16_run<4, WIN>(a, plan, s);
+    if (r <= 8) return decode::fp16_run<8, WIN>(a, plan, s);
     return cudaErrorInvalidValue;
+}
+template <bool WIN>
+int occ_r(const DecodeArgs& a, size_t smem) {
+    const int r = a.Hq / a.Hkv;
+    if (r <= 1) return decode::fp16_occupancy<1, WIN>(smem);
+    if (r <= 2) return decode::fp16_occupancy<2, WIN>(smem);
+    if (r <= 4) return decode::fp16_occupancy<4, WIN>(smem);
+    if (r <= 8) return decode::fp16_occupancy<8, WIN>(smem);
+    return 0;
+}
+
+cudaError_t decode_run_fp16(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {
+    return a.window > 0 ? run_r<true>(a, plan, s) : run_r<false>(a, plan, s);
 }
 
 int decode_occupancy_fp16(const DecodeArgs& a, const DecodePlan& plan, size_t smem) {
     (void)plan;
-    const int r = a.Hq / a.Hkv;
-    if (r <= 1) return decode::fp16_occupancy<1>(smem);
-    if (r <= 2) return decode::fp16_occupancy<2>(smem);
-    if (r <= 4) return decode::fp16_occupancy<4>(smem);
-    if (r <= 8) return decode::fp16_occupancy<8>(smem);
-    return 0;
+    return a.window > 0 ? occ_r<true>(a, smem) : occ_r<false>(a, smem);
 }
 
 }  // namespace kvq

@@ -26,8 +26,9 @@
 namespace kvq {
 namespace decode {
 
-// R: query heads per kv head, rounded up to 1, 2, 4 or 8.
-template <int D, int R>
+// R: query heads per kv head, rounded up to 1, 2, 4 or 8.  WIN: the sequences list only
+// their window and sink pages (p.window > 0), as in decode_splitkv_kernel.
+template <int D, int R, bool WIN>
 __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
     static_assert(D == 128, "four dimensions per lane");
     constexpr int kWarps = 4;
@@ -93,9 +94,9 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
     auto unit_of = [&](int i) { return c0 + warp + static_cast<long long>(kWarps) * i; };
     int wbase = 0;
     unsigned long long waddr =
-        lane < nm ? reinterpret_cast<unsigned long long>(unit_block<false>(p, pre, lens, unit_of(lane), 1)) : 0ull;
+        lane < nm ? reinterpret_cast<unsigned long long>(unit_block<WIN>(p, pre, lens, unit_of(lane), 1)) : 0ull;
     unsigned long long wnext =
-        32 + lane < nm ? reinterpret_cast<unsigned long long>(unit_block<false>(p, pre, lens, unit_of(32 + lane), 1))
+        32 + lane < nm ? reinterpret_cast<unsigned long long>(unit_block<WIN>(p, pre, lens, unit_of(32 + lane), 1))
                        : 0ull;
     int issued = 0;
     const uint64_t l2_stream = l2_policy_evict_first();
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
             wbase += 32;
             waddr = wnext;
             wnext = wbase + 32 + lane < nm
-                        ? reinterpret_cast<unsigned long long>(unit_block<false>(p, pre, lens, unit_of(wbase + 32 + lane), 1))
+                        ? reinterpret_cast<unsigned long long>(unit_block<WIN>(p, pre, lens, unit_of(wbase + 32 + lane), 1))
                         : 0ull;
         }
         const unsigned long long src = __shfl_sync(0xffffffffu, waddr, i - wbase);
@@ -167,7 +168,9 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
         const long long fu = ua + (((c0 + warp - ua) % kWarps) + kWarps) % kWarps;
         const int cnt = fu < ue ? static_cast<int>((ue - fu + kWarps - 1) / kWarps) : 0;
         const int pg0 = static_cast<int>(fu - sfirst);
-        const int Leff = min(lens[b], p.max_blocks * p.P);
+        const SeqSpan sspan = seq_span(lens[b], p.lg_p, p.max_blocks, WIN ? p.window : 0, WIN ? p.sinks : 0);
+        const int Leff = sspan.L;
+        const int wlo = sspan.wlo;  // 0 without a window
 
         if (threadIdx.x == 0 && sfirst + np < c1) {
             int nb = b, nhg = hg;
@@ -208,9 +211,13 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
                 const __half* kb = reinterpret_cast<const __half*>(ring + cst * ubytes);
                 const __half* vb = kb + p.P * D;
                 const int pg = pg0 + kWarps * j;
+                const int rp = WIN ? span_page(sspan, pg) : pg;  // the page (past a window gap)
                 for (int t0 = 0; t0 < p.P; t0 += T) {
-                    const int tpos = pg * p.P + t0;
+                    const int tpos = rp * p.P + t0;
                     if (tpos >= Leff) break;
+                    // a step wholly outside the window and the sinks is skipped, so every
+                    // processed step holds an attended token
+                    if (WIN && !(min(tpos + T, Leff) > wlo || tpos < p.sinks)) continue;
                     // partial dot products of this lane's 4 dimensions, T tokens, R heads
                     float a[R][T];
 #pragma unroll
@@ -242,7 +249,8 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
                     }
                     // online softmax per head on the token this lane holds
                     const int tau = lane >> TSH;
-                    const bool valid = tpos + tau < Leff;
+                    const int tt = tpos + tau;
+                    const bool valid = tt < Leff && (!WIN || tt >= wlo || tt < p.sinks);
                     float pw[R];
 #pragma unroll
                     for (int s = 0; s < R; ++s) {

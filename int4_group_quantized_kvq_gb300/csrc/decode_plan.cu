@@ -127,20 +127,19 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     return cudaSuccess;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
-    cudaError_t e;
+cudaError_t launch_decode_grid(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
+    if (a.fp16) return decode_run_fp16(a, plan, stream);
     const bool w = a.window > 0;
-    if (a.fp16) {
-        e = decode_run_fp16(a, plan, stream);
-        if (e != cudaSuccess) return e;
-        return launch_combine(a, plan, stream);
-    }
     switch (a.L.Gk) {
-        case 32: e = w ? decode_run_gk32_win(a, plan, stream) : decode_run_gk32(a, plan, stream); break;
-        case 64: e = w ? decode_run_gk64_win(a, plan, stream) : decode_run_gk64(a, plan, stream); break;
-        case 128: e = w ? decode_run_gk128_win(a, plan, stream) : decode_run_gk128(a, plan, stream); break;
+        case 32: return w ? decode_run_gk32_win(a, plan, stream) : decode_run_gk32(a, plan, stream);
+        case 64: return w ? decode_run_gk64_win(a, plan, stream) : decode_run_gk64(a, plan, stream);
+        case 128: return w ? decode_run_gk128_win(a, plan, stream) : decode_run_gk128(a, plan, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
+    cudaError_t e = launch_decode_grid(a, plan, stream);
     if (e != cudaSuccess) return e;
     return launch_combine(a, plan, stream);
 }

@@ -391,6 +391,118 @@ int kvq_dequantize_to_fp16_pool(const kvq_cache_config* cfg, const void* pool, v
     return ok();
 }
 
+namespace {
+// The two grids of the mixed-precision decode: INT4 over positions [0, L - residual),
+// FP16 over [L - residual, L); their workspaces back to back, one status word.
+struct MixedPlan {
+    kvq::DecodeArgs a4, a16;
+    kvq::DecodePlan p4, p16;
+    size_t off16, bytes;
+};
+cudaError_t plan_mixed(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads, int32_t max_len,
+                       int32_t residual, MixedPlan* m) {
+    kvq::DecodeArgs a{};
+    a.B = batch;
+    a.Hq = num_q_heads;
+    a.Hkv = cfg->num_kv_heads;
+    a.max_len = max_len;
+    a.L = kvq::block_layout(*cfg);
+    m->a4 = a;
+    m->a4.len_sub = residual;
+    m->a16 = a;
+    m->a16.fp16 = true;
+    m->a16.window = residual;
+    cudaError_t e = kvq::plan_decode(m->a4, &m->p4);
+    if (e != cudaSuccess) return e;
+    e = kvq::plan_decode(m->a16, &m->p16);
+    if (e != cudaSuccess) return e;
+    m->off16 = (m->p4.ws_bytes + 255) / 256 * 256;
+    m->bytes = m->off16 + m->p16.ws_bytes;
+    return cudaSuccess;
+}
+}  // namespace
+
+size_t kvq_mixed_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
+                                        int32_t max_len, int32_t residual) {
+    if (check_cfg(cfg) != KVQ_OK) return 0;
+    if (batch < 1 || num_q_heads < 1 || max_len < 0 || residual < 0 || num_q_heads % cfg->num_kv_heads) {
+        fail(KVQ_EINVAL, "invalid batch / num_q_heads / max_len / residual");
+        return 0;
+    }
+    if (residual == 0) return kvq_decode_workspace_bytes(cfg, batch, num_q_heads, max_len);
+    MixedPlan m;
+    cudaError_t e = plan_mixed(cfg, batch, num_q_heads, max_len, residual, &m);
+    if (e != cudaSuccess) {
+        fail(e == cudaErrorInvalidValue ? KVQ_EUNSUPPORTED : KVQ_ECUDA, "no decode kernel for this shape: %s",
+             cudaGetErrorString(e));
+        return 0;
+    }
+    ok();
+    return m.bytes;
+}
+
+int kvq_mixed_decode_attention(const kvq_cache_config* cfg, const void* pool, const int32_t* block_table,
+                               int32_t max_blocks, const void* pool16, const int32_t* block_table16,
+                               int32_t max_blocks16, int32_t num_pages16, const void* q, const int32_t* seq_lens,
+                               int32_t batch, int32_t num_q_heads, int32_t max_len, int32_t residual,
+                               float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                               kvq_stream_t stream) {
+    if (residual < 0) return fail(KVQ_EINVAL, "residual %d < 0", residual);
+    if (residual == 0)
+        return kvq_decode_attention(cfg, pool, q, block_table, max_blocks, seq_lens, batch, num_q_heads, max_len,
+                                    softmax_scale, out, workspace, workspace_bytes, stream);
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || num_q_heads < 1 || max_len < 0)
+        return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
+    if (num_q_heads % cfg->num_kv_heads)
+        return fail(KVQ_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, cfg->num_kv_heads);
+    if (num_q_heads / cfg->num_kv_heads > 8)
+        return fail(KVQ_EUNSUPPORTED, "query heads per KV head %d > 8", num_q_heads / cfg->num_kv_heads);
+    if (cfg->head_dim != 128) return fail(KVQ_EUNSUPPORTED, "decode attention supports head_dim 128");
+    if (batch > 4096) return fail(KVQ_EUNSUPPORTED, "batch %d > 4096", batch);
+    if (batch == 0) return ok();
+    if (max_blocks < 1 || max_blocks16 < 1 || num_pages16 < 1)
+        return fail(KVQ_EINVAL, "max_blocks %d, max_blocks16 %d, num_pages16 %d", max_blocks, max_blocks16,
+                    num_pages16);
+    if (!pool || !pool16 || !q || !block_table || !block_table16 || !seq_lens || !out || !workspace)
+        return fail(KVQ_EINVAL, "NULL device pointer");
+    if (!aligned(pool, 16) || !aligned(pool16, 16) || !aligned(q, 16) || !aligned(out, 16))
+        return fail(KVQ_EINVAL, "pools, q and out must be 16-byte aligned");
+    if (!aligned(workspace, 256)) return fail(KVQ_EINVAL, "workspace must be 256-byte aligned");
+    if (!aligned(block_table, 4) || !aligned(block_table16, 4) || !aligned(seq_lens, 4))
+        return fail(KVQ_EINVAL, "int32 arguments must be aligned");
+    MixedPlan m;
+    cudaError_t e = plan_mixed(cfg, batch, num_q_heads, max_len, residual, &m);
+    if (e == cudaErrorInvalidValue) return fail(KVQ_EUNSUPPORTED, "no decode kernel for this shape");
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_mixed_decode_attention plan");
+    if (workspace_bytes < m.bytes)
+        return fail(KVQ_EWORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, m.bytes);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    for (kvq::DecodeArgs* a : {&m.a4, &m.a16}) {
+        a->q = static_cast<const __half*>(q);
+        a->seq_lens = seq_lens;
+        a->out = out;
+        a->num_pages = cfg->num_pages;
+        a->softmax_scale = softmax_scale;
+        a->status = reinterpret_cast<uint32_t*>(ws);
+    }
+    m.a4.pool = static_cast<const uint8_t*>(pool);
+    m.a4.block_table = block_table;
+    m.a4.max_blocks = max_blocks;
+    m.a4.workspace = ws;
+    m.a16.pool = static_cast<const uint8_t*>(pool16);
+    m.a16.block_table = block_table16;
+    m.a16.max_blocks = max_blocks16;
+    m.a16.num_pages = num_pages16;
+    m.a16.workspace = ws + m.off16;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = kvq::launch_decode_grid(m.a4, m.p4, s);
+    if (e == cudaSuccess) e = kvq::launch_decode_grid(m.a16, m.p16, s);
+    if (e == cudaSuccess) e = kvq::launch_combine2(m.a4, m.p4, m.a16, m.p16, s);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_mixed_decode_attention launch");
+    return ok();
+}
+
 int kvq_read_status(const void* status_word, uint32_t* flags, kvq_stream_t stream) {
     if (!status_word || !flags) return fail(KVQ_EINVAL, "NULL pointer");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -114,6 +114,10 @@ struct DecodeArgs {
     int32_t sinks = 0;
     // attention over the FP16 cache instead of the INT4 one (the comparison's baseline)
     bool fp16 = false;
+    // attend seq_lens[b] - len_sub positions (the INT4 part of the mixed-precision decode)
+    int32_t len_sub = 0;
+    // status word (nullptr: the first word of the workspace)
+    uint32_t* status = nullptr;
 };
 
 // The FP16 cache of the latency comparison: block (page, kv head) holds K rows P x d fp16,
@@ -142,5 +146,10 @@ cudaError_t launch_dequantize_to_fp16(const Fp16DequantArgs& a, long long max_pa
 // Returns cudaErrorInvalidValue for a geometry no kernel instance covers.
 cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan);
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+// the decode grid alone (its partials stay in the workspace), and the combine of two grids'
+// partials (the mixed-precision decode)
+cudaError_t launch_decode_grid(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+cudaError_t launch_combine2(const DecodeArgs& a0, const DecodePlan& plan0, const DecodeArgs& a1,
+                            const DecodePlan& plan1, cudaStream_t stream);
 
 }  // namespace kvq
