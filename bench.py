@@ -486,8 +486,17 @@ def run_kvq(args, world, rank, local):
             stream.synchronize()
             return e0.elapsed_time(e1) * 1e-3 / (calls * reps)
 
+        R = 128  # the mixed arm: the last 128 positions in FP16, the older ones in INT4
+        wsm = torch.zeros(kvq.kvq_mixed_decode_workspace_bytes(cfg16, wl.B, wl.Hq, wl.max_len, R), dtype=torch.uint8,
+                          device=dev)
+
+        def mixed_attend():
+            kvq.kvq_mixed_decode_attention(cfg16, caches[0].pool, bt0, pool16, bt0, cfg16.num_pages, q, seq_lens,
+                                           wl.max_len, R, scale, out16, wsm, stream=stream)
+
         t16 = per_call(fp16_attend)
         tdq = per_call(deq_then_attend)
+        tmx = per_call(mixed_attend)
         fp16_bytes = 4 * wl.d * sum(wl.seq_lens) * wl.Hkv
         comparison = {
             "what": "decode attention latency on the bench workload: FP16 cache; INT4 dequantized to an FP16 pool "
@@ -495,12 +504,14 @@ def run_kvq(args, world, rank, local):
             "fp16_us": t16 * 1e6, "fp16_gbs": fp16_bytes / t16 / 1e9,
             "int4_dequant_then_attend_us": tdq * 1e6,
             "int4_fused_us": decode_s * 1e6,
+            "mixed_int4_fp16_last128_us": tmx * 1e6,
             "fp16_bytes": fp16_bytes, "int4_bytes": wl.decode_bytes(),
             "fused_speedup_vs_fp16": t16 / decode_s, "fused_speedup_vs_dequant_then_attend": tdq / decode_s,
         }
         if rank == 0:
             print(f"[compare] fp16 {t16 * 1e6:.1f} us ({fp16_bytes / t16 / 1e9:.0f} GB/s), dequant+attend "
-                  f"{tdq * 1e6:.1f} us, int4 fused {decode_s * 1e6:.1f} us", file=sys.stderr)
+                  f"{tdq * 1e6:.1f} us, int4 fused {decode_s * 1e6:.1f} us, mixed (last {R} fp16) {tmx * 1e6:.1f} us",
+                  file=sys.stderr)
     # the step leaves the output of the last decode step in `out` for e2e and checks
     flags = max(c.flags() for c in caches)
     if world > 1:
