@@ -73,6 +73,18 @@ def lib() -> C.CDLL:
                                                         C.c_int, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                                         C.c_double, C.c_void_p] + [C.c_int] * 7
         L.kvq_oracle_mixed_decode_attention.restype = C.c_int
+        L.kvq_oracle_int8_block_bytes.argtypes = [C.c_int, C.c_int]
+        L.kvq_oracle_int8_block_bytes.restype = C.c_size_t
+        L.kvq_oracle_int8_quantize_row.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
+        L.kvq_oracle_int8_quantize_row.restype = None
+        L.kvq_oracle_int8_quantize_append.argtypes = [C.c_void_p] * 4 + [C.c_int, C.c_void_p] + [C.c_int] * 6
+        L.kvq_oracle_int8_quantize_append.restype = C.c_int
+        L.kvq_oracle_int8_dequantize.argtypes = [C.c_void_p, C.c_void_p] + [C.c_int] * 4 + [C.c_void_p] * 2 + \
+            [C.c_int] * 4
+        L.kvq_oracle_int8_dequantize.restype = C.c_int
+        L.kvq_oracle_int8_decode_attention.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
+                                                       C.c_int, C.c_int, C.c_double, C.c_void_p] + [C.c_int] * 4
+        L.kvq_oracle_int8_decode_attention.restype = C.c_int
         _lib = L
     return _lib
 
@@ -272,4 +284,61 @@ def mixed_decode_attention(L: Layout, pool: np.ndarray, block_table: np.ndarray,
                                                  int(bt16.shape[1]), _ptr(q), _ptr(sl), B, Hq, int(residual),
                                                  float(softmax_scale), _ptr(out), *L.geom, int(num_pages16))
     _check(rc, "mixed_decode_attention")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# INT8 per-row codec ("AI inference tuning: KV Cache optimisation and memory management"
+# section 3.1, KVCacheQuantizer): one fp32 scale per (token, kv head) row.
+# ---------------------------------------------------------------------------
+
+def int8_block_bytes(head_dim: int, page_size: int) -> int:
+    return int(lib().kvq_oracle_int8_block_bytes(head_dim, page_size))
+
+
+def int8_pool_bytes(L: Layout) -> int:
+    return L.num_pages * L.Hkv * int8_block_bytes(L.d, L.P)
+
+
+def int8_quantize_row(x_f16: np.ndarray) -> tuple[np.ndarray, float]:
+    """One fp16 row -> (int8 codes, fp32 scale)."""
+    x = np.ascontiguousarray(x_f16, dtype=np.float16)
+    codes = np.zeros(x.size, np.int8)
+    s = np.zeros(1, np.float32)
+    lib().kvq_oracle_int8_quantize_row(_ptr(x), int(x.size), _ptr(codes), _ptr(s))
+    return codes, float(s[0])
+
+
+def int8_quantize_append(L: Layout, pool8: np.ndarray, k: np.ndarray, v: np.ndarray, block_table: np.ndarray,
+                         start_pos: np.ndarray) -> None:
+    k = np.ascontiguousarray(k, dtype=np.float16)
+    v = np.ascontiguousarray(v, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sp = np.ascontiguousarray(start_pos, dtype=np.int32)
+    rc = lib().kvq_oracle_int8_quantize_append(_ptr(pool8), _ptr(k), _ptr(v), _ptr(bt), int(bt.shape[1]), _ptr(sp),
+                                               int(k.shape[0]), int(k.shape[1]), L.Hkv, L.d, L.P, L.num_pages)
+    _check(rc, "int8_quantize_append")
+
+
+def int8_dequantize(L: Layout, pool8: np.ndarray, block_table: np.ndarray, b: int, start: int,
+                    n: int) -> tuple[np.ndarray, np.ndarray]:
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    ok = np.zeros((n, L.Hkv, L.d), np.float32)
+    ov = np.zeros((n, L.Hkv, L.d), np.float32)
+    rc = lib().kvq_oracle_int8_dequantize(_ptr(pool8), _ptr(bt), int(bt.shape[1]), b, start, n, _ptr(ok), _ptr(ov),
+                                          L.Hkv, L.d, L.P, L.num_pages)
+    _check(rc, "int8_dequantize")
+    return ok, ov
+
+
+def int8_decode_attention(L: Layout, pool8: np.ndarray, q: np.ndarray, block_table: np.ndarray,
+                          seq_lens: np.ndarray, softmax_scale: float) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, _ = q.shape
+    out = np.zeros((B, Hq, L.d), dtype=np.float64)
+    rc = lib().kvq_oracle_int8_decode_attention(_ptr(pool8), _ptr(q), _ptr(bt), int(bt.shape[1]), _ptr(sl), B, Hq,
+                                                float(softmax_scale), _ptr(out), L.Hkv, L.d, L.P, L.num_pages)
+    _check(rc, "int8_decode_attention")
     return out

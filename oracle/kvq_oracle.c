@@ -590,3 +590,153 @@ int kvq_oracle_mixed_decode_attention(const uint8_t *pool, const int32_t *block_
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* INT8 per-row codec ([M] section 3.1, KVCacheQuantizer.quantize_int8 /    */
+/* dequantize_int8): one scale per row (token, kv head) over head_dim,       */
+/* scale = amax / 127 clamped below at 1e-8, code = round(x / scale)         */
+/* clamped to [-128, 127], value = code * scale.  The page computes in the   */
+/* input's dtype; here every step is fp32 (amax is exact from fp16; the      */
+/* division and the product round once to nearest), the rounding is         */
+/* half-to-even, and the scale is stored as fp32.                           */
+/* Block (page, kv head), index page*Hkv + h, 2*P*d + 8*P bytes: K codes     */
+/* P x d int8, V codes P x d int8, K scales P fp32, V scales P fp32 (little- */
+/* endian).                                                                  */
+/* ------------------------------------------------------------------------ */
+size_t kvq_oracle_int8_block_bytes(int head_dim, int page_size) {
+    if (head_dim <= 0 || page_size <= 0) return 0;
+    return (size_t)2 * (size_t)page_size * (size_t)head_dim + (size_t)8 * (size_t)page_size;
+}
+
+static uint8_t *int8_block(uint8_t *pool8, int Hkv, int d, int P, int page, int h) {
+    return pool8 + ((size_t)page * (size_t)Hkv + (size_t)h) * kvq_oracle_int8_block_bytes(d, P);
+}
+
+static void put_f32(uint8_t *p, float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    p[0] = (uint8_t)u; p[1] = (uint8_t)(u >> 8); p[2] = (uint8_t)(u >> 16); p[3] = (uint8_t)(u >> 24);
+}
+static float get_f32(const uint8_t *p) {
+    uint32_t u = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* one row of d fp16 values -> d int8 codes and the fp32 scale */
+void kvq_oracle_int8_quantize_row(const uint16_t *x, int d, int8_t *codes, float *scale_out) {
+    float amax = 0.0f;
+    for (int i = 0; i < d; ++i) {
+        float a = fabsf(kvq_oracle_f16_to_f32(x[i]));
+        if (a > amax) amax = a;
+    }
+    float s = amax / 127.0f;
+    if (s < 1e-8f) s = 1e-8f;
+    for (int i = 0; i < d; ++i) {
+        float r = nearbyintf(kvq_oracle_f16_to_f32(x[i]) / s);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -128.0f) r = -128.0f;
+        codes[i] = (int8_t)r;
+    }
+    *scale_out = s;
+}
+
+int kvq_oracle_int8_quantize_append(uint8_t *pool8, const uint16_t *k, const uint16_t *v, const int32_t *block_table,
+                                    int max_blocks, const int32_t *start_pos, int B, int n_new, int Hkv, int d, int P,
+                                    int num_pages) {
+    if (Hkv <= 0 || d <= 0 || d > 256 || P <= 0 || B < 0 || n_new < 0) return ORACLE_EINVAL;
+    int8_t codes[256];
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < n_new; ++t) {
+            long pos = (long)start_pos[b] + t;
+            if (pos < 0 || pos / P >= max_blocks) return ORACLE_ERANGE;
+            int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(pos / P)];
+            if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+            int slot = (int)(pos % P);
+            for (int h = 0; h < Hkv; ++h) {
+                size_t src = (((size_t)b * (size_t)n_new + (size_t)t) * (size_t)Hkv + (size_t)h) * (size_t)d;
+                uint8_t *blk = int8_block(pool8, Hkv, d, P, page, h);
+                float sk, sv;
+                kvq_oracle_int8_quantize_row(k + src, d, codes, &sk);
+                memcpy(blk + (size_t)slot * (size_t)d, codes, (size_t)d);
+                kvq_oracle_int8_quantize_row(v + src, d, codes, &sv);
+                memcpy(blk + (size_t)P * (size_t)d + (size_t)slot * (size_t)d, codes, (size_t)d);
+                put_f32(blk + (size_t)2 * (size_t)P * (size_t)d + (size_t)4 * (size_t)slot, sk);
+                put_f32(blk + (size_t)2 * (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot), sv);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Dequantize positions [start, start+n) of sequence b: value = fp32(code * scale). */
+int kvq_oracle_int8_dequantize(const uint8_t *pool8, const int32_t *block_table, int max_blocks, int b, int start,
+                               int n, float *out_k, float *out_v, int Hkv, int d, int P, int num_pages) {
+    if (Hkv <= 0 || d <= 0 || P <= 0 || start < 0 || n < 0) return ORACLE_EINVAL;
+    for (int t = 0; t < n; ++t) {
+        long pos = (long)start + t;
+        if (pos / P >= max_blocks) return ORACLE_ERANGE;
+        int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(pos / P)];
+        if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+        int slot = (int)(pos % P);
+        for (int h = 0; h < Hkv; ++h) {
+            const uint8_t *blk = int8_block((uint8_t *)pool8, Hkv, d, P, page, h);
+            float sk = get_f32(blk + (size_t)2 * (size_t)P * (size_t)d + (size_t)4 * (size_t)slot);
+            float sv = get_f32(blk + (size_t)2 * (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot));
+            size_t off = ((size_t)t * (size_t)Hkv + (size_t)h) * (size_t)d;
+            for (int i = 0; i < d; ++i) {
+                out_k[off + i] = (float)(int8_t)blk[(size_t)slot * (size_t)d + (size_t)i] * sk;
+                out_v[off + i] = (float)(int8_t)blk[((size_t)P + (size_t)slot) * (size_t)d + (size_t)i] * sv;
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Decode attention over the INT8 cache, in fp64 ([M] section 3.2) over the dequantized rows. */
+int kvq_oracle_int8_decode_attention(const uint8_t *pool8, const uint16_t *q, const int32_t *block_table,
+                                     int max_blocks, const int32_t *seq_lens, int B, int Hq, double softmax_scale,
+                                     double *out, int Hkv, int d, int P, int num_pages) {
+    if (Hkv <= 0 || d <= 0 || d > 256 || P <= 0 || Hq <= 0 || Hq % Hkv) return ORACLE_EINVAL;
+    int per = Hq / Hkv;
+    float rk[256], rv[256];
+    for (int b = 0; b < B; ++b) {
+        int len = seq_lens[b];
+        if (len < 0 || (len + P - 1) / P > max_blocks) return ORACLE_ERANGE;
+        for (int hq = 0; hq < Hq; ++hq) {
+            int kh = hq / per;
+            const uint16_t *qrow = q + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            double *o = out + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            for (int i = 0; i < d; ++i) o[i] = 0.0;
+            if (len == 0) continue;
+            double top = -INFINITY, den = 0.0;
+            for (int pass = 0; pass < 2; ++pass) {
+                for (int t = 0; t < len; ++t) {
+                    int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+                    if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+                    const uint8_t *blk = int8_block((uint8_t *)pool8, Hkv, d, P, page, kh);
+                    int slot = t % P;
+                    float sk = get_f32(blk + (size_t)2 * (size_t)P * (size_t)d + (size_t)4 * (size_t)slot);
+                    float sv = get_f32(blk + (size_t)2 * (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot));
+                    for (int i = 0; i < d; ++i) {
+                        rk[i] = (float)(int8_t)blk[(size_t)slot * (size_t)d + (size_t)i] * sk;
+                        rv[i] = (float)(int8_t)blk[((size_t)P + (size_t)slot) * (size_t)d + (size_t)i] * sv;
+                    }
+                    double z = 0.0;
+                    for (int i = 0; i < d; ++i) z += kvq_oracle_f16_to_f64(qrow[i]) * (double)rk[i];
+                    z *= softmax_scale;
+                    if (pass == 0) {
+                        if (z > top) top = z;
+                        continue;
+                    }
+                    double e = exp(z - top);
+                    den += e;
+                    for (int i = 0; i < d; ++i) o[i] += e * (double)rv[i];
+                }
+            }
+            for (int i = 0; i < d; ++i) o[i] /= den;
+        }
+    }
+    return ORACLE_OK;
+}

@@ -55,6 +55,14 @@ MUTANTS = [
     ("mixed_fp16_part_from_int4_table",
      "int page = block_table16[(size_t)b * (size_t)max_blocks16 + (size_t)(t / P)];",
      "int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];"),
+    ("int8_divide_by_128", "float s = amax / 127.0f;", "float s = amax / 128.0f;"),
+    # (the INT8 clamp at -128 cannot bind: with scale = amax / 127 every |x / scale| <= 127,
+    # so moving it to -127 changes nothing and is not planted)
+    ("int8_ties_away", "float r = nearbyintf(kvq_oracle_f16_to_f32(x[i]) / s);",
+     "float r = roundf(kvq_oracle_f16_to_f32(x[i]) / s);"),
+    ("int8_k_scale_for_v", "float sv = get_f32(blk + (size_t)2 * (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot));\n            size_t off",
+     "float sv = get_f32(blk + (size_t)2 * (size_t)P * (size_t)d + (size_t)4 * (size_t)slot);\n            size_t off"),
+    ("int8_attention_gqa_modulo", "int kh = hq / per;", "int kh = hq % Hkv;"),
     ("last_token_dropped", "for (int t = 0; t < len; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk",
      "for (int t = 0; t < len - 1; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk"),
 ]

@@ -713,3 +713,105 @@ def test_mixed_brute_force(residual):
             s_ = (kk[:, hq // 2] @ q[b, hq].astype(np.float64)) * scale
             ref = scipy.special.softmax(s_) @ vv[:, hq // 2]
             np.testing.assert_allclose(got[b, hq], ref, rtol=1e-10, atol=1e-10)
+
+
+# ----------------------------------------------------------------------------
+# INT8 per-row codec ("AI inference tuning: KV Cache optimisation and memory
+# management" section 3.1, KVCacheQuantizer.quantize_int8)
+# ----------------------------------------------------------------------------
+
+def test_int8_worked_examples():
+    # amax 127: the scale is exactly 1 and the codes are the values rounded, ties to even
+    x = np.zeros(64, np.float16)
+    x[:6] = [127.0, -127.0, 2.5, 3.5, -2.5, 0.49]
+    codes, s = oracle.int8_quantize_row(x)
+    assert s == 1.0
+    assert codes[:6].tolist() == [127, -127, 2, 4, -2, 0]
+    # an all-zero row takes the floor scale 1e-8 and zero codes
+    codes, s = oracle.int8_quantize_row(np.zeros(64, np.float16))
+    assert s == float(np.float32(1e-8)) and not codes.any()
+    # a single nonzero value maps to +-127
+    x = np.zeros(64, np.float16)
+    x[7] = -0.3
+    codes, s = oracle.int8_quantize_row(x)
+    assert codes[7] == -127 and np.count_nonzero(codes) == 1
+
+
+def test_int8_codes_are_nearest_within_range():
+    rng = np.random.default_rng(101)
+    for _ in range(200):
+        x = (rng.standard_normal(128) * rng.uniform(0.01, 50)).astype(np.float16)
+        codes, s = oracle.int8_quantize_row(x)
+        amax = float(np.abs(x.astype(np.float64)).max())
+        assert abs(s - amax / 127) <= 2 ** -23 * s  # the fp32 quotient
+        assert codes.min() >= -128 and codes.max() <= 127
+        assert np.abs(codes).max() == 127
+        # brute force: every code is the integer nearest to x / s (f64), except where the
+        # quotient lies within fp32 rounding (the definition divides in fp32) of a tie
+        y = x.astype(np.float64) / s
+        cand = np.arange(-128, 128)
+        best = cand[np.argmin(np.abs(y[:, None] - cand[None, :]), axis=1)]
+        tie = np.abs(np.abs(y - np.floor(y)) - 0.5) < 2.0 ** -22 * np.maximum(np.abs(y), 1.0)
+        assert np.array_equal(codes[~tie], best[~tie])
+        # half a step, plus the fp32 rounding of a quotient up to 127
+        assert np.all(np.abs(x.astype(np.float64) - codes * np.float64(s)) <= s * (0.5 + 127 * 2.0 ** -23))
+
+
+def test_int8_layout_and_dequantize():
+    L = oracle.Layout(2, 64, 16, 32, 64, 6)
+    assert oracle.int8_block_bytes(64, 16) == 2 * 16 * 64 + 8 * 16
+    k = W.kv_tensor(111, (1, 20, 2, 64)).numpy()
+    v = W.kv_tensor(112, (1, 20, 2, 64)).numpy()
+    bt = np.array([[4, 1]], np.int32)
+    pool8 = np.zeros(oracle.int8_pool_bytes(L), np.uint8)
+    oracle.int8_quantize_append(L, pool8, k, v, bt, np.array([0], np.int32))
+    blocks = pool8.reshape(L.num_pages, L.Hkv, -1)
+    dk, dv = oracle.int8_dequantize(L, pool8, bt, 0, 0, 20)
+    for t in range(20):
+        for h in range(2):
+            blk = blocks[bt[0, t // 16], h]
+            ck, sk = oracle.int8_quantize_row(k[0, t, h])
+            cv, sv = oracle.int8_quantize_row(v[0, t, h])
+            assert np.array_equal(blk[(t % 16) * 64:(t % 16 + 1) * 64].view(np.int8), ck)
+            assert np.array_equal(blk[(16 + t % 16) * 64:(17 + t % 16) * 64].view(np.int8), cv)
+            assert blk[2048 + 4 * (t % 16):2052 + 4 * (t % 16)].view(np.float32)[0] == np.float32(sk)
+            assert blk[2048 + 64 + 4 * (t % 16):2052 + 64 + 4 * (t % 16)].view(np.float32)[0] == np.float32(sv)
+            assert np.array_equal(dk[t, h], ck.astype(np.float32) * np.float32(sk))
+            assert np.array_equal(dv[t, h], cv.astype(np.float32) * np.float32(sv))
+
+
+def test_int8_attention_brute_force_and_exact_case():
+    L = oracle.Layout(2, 64, 16, 32, 64, 8)
+    lens = [30, 9]
+    bt = np.array([[3, 0], [6, -1]], np.int32)
+    k = W.kv_tensor(113, (2, 30, 2, 64), 20.0, W.outlier_channels(2, 64, seed=9)).numpy()
+    v = W.kv_tensor(114, (2, 30, 2, 64)).numpy()
+    pool8 = np.zeros(oracle.int8_pool_bytes(L), np.uint8)
+    for b in range(2):
+        oracle.int8_quantize_append(L, pool8, k[b:b + 1, :lens[b]], v[b:b + 1, :lens[b]], bt[b:b + 1],
+                                    np.array([0], np.int32))
+    q = W.kv_tensor(115, (1, 2, 4, 64)).numpy()[0]
+    got = oracle.int8_decode_attention(L, pool8, q, bt, np.array(lens, np.int32), 30.0)
+    for b in range(2):
+        dk, dv = oracle.int8_dequantize(L, pool8, bt, b, 0, lens[b])
+        for hq in range(4):
+            s_ = (dk[:, hq // 2].astype(np.float64) @ q[b, hq].astype(np.float64)) * 30.0
+            ref = scipy.special.softmax(s_) @ dv[:, hq // 2].astype(np.float64)
+            np.testing.assert_allclose(got[b, hq], ref, rtol=1e-10, atol=1e-10)
+    # integer rows holding +-127: scale 1, codes equal the values, so the INT8 attention
+    # equals the FP16 attention over the same rows bit for bit
+    rng = np.random.default_rng(116)
+    ki = rng.integers(-127, 128, size=(2, 30, 2, 64)).astype(np.float16)
+    vi = rng.integers(-127, 128, size=(2, 30, 2, 64)).astype(np.float16)
+    ki[..., 0] = 127
+    vi[..., 1] = -127
+    pool8 = np.zeros(oracle.int8_pool_bytes(L), np.uint8)
+    pool16 = np.zeros(oracle.fp16_pool_bytes(L), np.uint8)
+    for b in range(2):
+        oracle.int8_quantize_append(L, pool8, ki[b:b + 1, :lens[b]], vi[b:b + 1, :lens[b]], bt[b:b + 1],
+                                    np.array([0], np.int32))
+        oracle.fp16_append(L, pool16, ki[b:b + 1, :lens[b]], vi[b:b + 1, :lens[b]], bt[b:b + 1],
+                           np.array([0], np.int32))
+    a = oracle.int8_decode_attention(L, pool8, q, bt, np.array(lens, np.int32), 0.01)
+    f = oracle.fp16_decode_attention(L, pool16, q, bt, np.array(lens, np.int32), 0.01)
+    assert np.array_equal(a, f)
