@@ -239,6 +239,29 @@ int kvq_fp16_decode_attention(const kvq_cache_config *cfg, const void *pool16, c
                               float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * INT8 per-row cache (KVCacheQuantizer.quantize_int8 of the KV-cache optimisation page,
+ * section 3.1): one fp32 scale per (token, kv head) row, scale = amax / 127 (IEEE fp32
+ * division, at least 1e-8), code = clamp(round-half-even(x / scale), -128, 127) (fp32
+ * division), value = fp32(code * scale).  Same pages, block table and cfg as the INT4
+ * cache (group sizes unused): block (page, kv head) at (page * Hkv + h) * (2 P d + 8 P)
+ * bytes holds K codes P x d int8, V codes P x d int8, K scales P fp32, V scales P fp32.
+ * kvq_int8_pool_bytes: num_pages * Hkv * (2 P d + 8 P); 0 if cfg is invalid.
+ * kvq_int8_quantize_append: as kvq_quantize_append (head_dim a multiple of 4, <= 256).
+ * kvq_int8_decode_workspace_bytes / kvq_int8_decode_attention: as the INT4 calls of the
+ *   same names over the INT8 pool (head_dim 128, up to 8 query heads per kv head).
+ */
+size_t kvq_int8_pool_bytes(const kvq_cache_config *cfg);
+int kvq_int8_quantize_append(const kvq_cache_config *cfg, void *pool8, const void *k, const void *v,
+                             const int32_t *block_table, int32_t max_blocks, const int32_t *start_pos,
+                             int32_t batch, int32_t n_new, uint32_t *status, kvq_stream_t stream);
+size_t kvq_int8_decode_workspace_bytes(const kvq_cache_config *cfg, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_len);
+int kvq_int8_decode_attention(const kvq_cache_config *cfg, const void *pool8, const void *q,
+                              const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                              int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                              float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
  * Mixed-precision decode attention (section 8.3 of the INT4 state-machine page: quantize
  * the KV of old tokens to INT4 first, keep recent tokens in FP16).  For sequence b of
  * L = seq_lens[b] positions, positions [0, L - residual) are read from the INT4 pool

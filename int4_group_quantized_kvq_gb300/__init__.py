@@ -31,6 +31,10 @@ from .binding import (  # noqa: F401
     kvq_fp16_decode_attention,
     kvq_fp16_decode_workspace_bytes,
     kvq_fp16_pool_bytes,
+    kvq_int8_decode_attention,
+    kvq_int8_decode_workspace_bytes,
+    kvq_int8_pool_bytes,
+    kvq_int8_quantize_append,
     kvq_mixed_decode_attention,
     kvq_mixed_decode_workspace_bytes,
     new_fp16_workspace,

@@ -23,7 +23,8 @@ ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_
                "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_attention_window",
                "kvq_decode_step_window", "kvq_fp16_pool_bytes", "kvq_fp16_append", "kvq_dequantize_to_fp16_pool",
                "kvq_fp16_decode_workspace_bytes", "kvq_fp16_decode_attention", "kvq_mixed_decode_workspace_bytes",
-               "kvq_mixed_decode_attention")
+               "kvq_mixed_decode_attention", "kvq_int8_pool_bytes", "kvq_int8_quantize_append",
+               "kvq_int8_decode_workspace_bytes", "kvq_int8_decode_attention")
 
 
 class KvqError(RuntimeError):
@@ -91,6 +92,14 @@ def lib() -> C.CDLL:
         L.kvq_mixed_decode_attention.argtypes = [cfgp, P, P, I32, P, P, I32, I32, P, P, I32, I32, I32, I32, C.c_float,
                                                  P, P, SZ, P]
         L.kvq_mixed_decode_attention.restype = C.c_int
+        L.kvq_int8_pool_bytes.argtypes = [cfgp]
+        L.kvq_int8_pool_bytes.restype = SZ
+        L.kvq_int8_quantize_append.argtypes = [cfgp, P, P, P, P, I32, P, I32, I32, P, P]
+        L.kvq_int8_quantize_append.restype = C.c_int
+        L.kvq_int8_decode_workspace_bytes.argtypes = [cfgp, I32, I32, I32]
+        L.kvq_int8_decode_workspace_bytes.restype = SZ
+        L.kvq_int8_decode_attention.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
+        L.kvq_int8_decode_attention.restype = C.c_int
         L.kvq_dequantize.argtypes = [cfgp, P, P, I32, I32, I32, I32, P, P, I32, P, P]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_read_status.argtypes = [P, C.POINTER(C.c_uint32), P]
@@ -359,4 +368,46 @@ def kvq_mixed_decode_attention(cfg: CacheConfig, pool: torch.Tensor, block_table
         _dev(q, "q", torch.float16), _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), int(residual),
         float(softmax_scale), _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream(stream))
+    _check(rc)
+
+
+# ---------------------------------------------------------------------------
+# The INT8 per-row cache (one fp32 scale per token and kv head).
+# ---------------------------------------------------------------------------
+
+def kvq_int8_pool_bytes(cfg: CacheConfig) -> int:
+    return int(lib().kvq_int8_pool_bytes(C.byref(cfg)))
+
+
+def kvq_int8_quantize_append(cfg: CacheConfig, pool8: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                             block_table: torch.Tensor, start_pos: torch.Tensor, status: torch.Tensor | None = None,
+                             stream=None) -> None:
+    """Quantize fp16 rows k, v [B, n_new, Hkv, d] into the INT8 pool at start_pos[b] + t."""
+    B, n = int(k.shape[0]), int(k.shape[1])
+    rc = lib().kvq_int8_quantize_append(
+        C.byref(cfg), _dev(pool8, "pool8", torch.uint8), _dev(k, "k", torch.float16), _dev(v, "v", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(start_pos, "start_pos", torch.int32), B, n, None if status is None else _dev(status, "status"),
+        _stream(stream))
+    _check(rc)
+
+
+def kvq_int8_decode_workspace_bytes(cfg: CacheConfig, batch: int, num_q_heads: int, max_len: int) -> int:
+    n = int(lib().kvq_int8_decode_workspace_bytes(C.byref(cfg), batch, num_q_heads, max_len))
+    if n == 0:
+        raise KvqError(KVQ_EINVAL, kvq_last_error())
+    return n
+
+
+def kvq_int8_decode_attention(cfg: CacheConfig, pool8: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
+                              seq_lens: torch.Tensor, max_len: int, softmax_scale: float, out: torch.Tensor,
+                              workspace: torch.Tensor, stream=None) -> None:
+    """Decode attention over the INT8 per-row cache; arguments as kvq_decode_attention."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_int8_decode_attention(
+        C.byref(cfg), _dev(pool8, "pool8", torch.uint8), _dev(q, "q", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
+        _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
     _check(rc)

@@ -8,11 +8,11 @@ namespace kvq {
 namespace decode {
 namespace {
 
-template <int R, bool WIN>
+template <int R, bool WIN, bool I8>
 cudaError_t fp16_smem_attr(size_t smem) {
     static std::atomic<long long> granted{-1};
     if (static_cast<long long>(smem) <= granted.load(std::memory_order_acquire)) return cudaSuccess;
-    const cudaError_t err = cudaFuncSetAttribute(decode_fp16_kernel<128, R, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t err = cudaFuncSetAttribute(decode_fp16_kernel<128, R, WIN, I8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -24,18 +24,18 @@ cudaError_t fp16_smem_attr(size_t smem) {
     return cudaSuccess;
 }
 
-template <int R, bool WIN>
+template <int R, bool WIN, bool I8>
 int fp16_occupancy(size_t smem) {
-    if (fp16_smem_attr<R, WIN>(smem) != cudaSuccess) return 0;
+    if (fp16_smem_attr<R, WIN, I8>(smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_fp16_kernel<128, R, WIN>, 128, smem) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_fp16_kernel<128, R, WIN, I8>, 128, smem) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-template <int R, bool WIN>
+template <int R, bool WIN, bool I8>
 cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     KParams p{};
     p.pool = a.pool;
@@ -58,13 +58,13 @@ cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s
     p.P = a.L.P;
     p.num_pages = a.num_pages;
     p.max_blocks = a.max_blocks;
-    p.block_bytes = 4 * a.L.P * a.L.d;
+    p.block_bytes = I8 ? 2 * a.L.P * a.L.d + 8 * a.L.P : 4 * a.L.P * a.L.d;
     p.unit_bytes = p.block_bytes;
     p.stages = plan.stages;
     p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
     p.lg_p = 0;
     while ((1 << p.lg_p) < a.L.P) ++p.lg_p;
-    cudaError_t err = fp16_smem_attr<R, WIN>(plan.smem_bytes);
+    cudaError_t err = fp16_smem_attr<R, WIN, I8>(plan.smem_bytes);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -76,7 +76,7 @@ cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, decode_fp16_kernel<128, R, WIN>, p);
+    err = cudaLaunchKernelEx(&cfg, decode_fp16_kernel<128, R, WIN, I8>, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -85,33 +85,35 @@ cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s
 }  // namespace decode
 
 // query heads per kv head r in 1..8, rounded up to 1, 2, 4 or 8; window instances when a
-// window is given
-template <bool WIN>
+// window is given; INT8 blocks for the INT8 cache
+template <bool WIN, bool I8>
 cudaError_t run_r(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {
     const int r = a.Hq / a.Hkv;
-    if (r <= 1) return decode::fp16_run<1, WIN>(a, plan, s);
-    if (r <= 2) return decode::fp16_run<2, WIN>(a, plan, s);
-    if (r <= 4) return decode::fp16_run<4, WIN>(a, plan, s);
-    if (r <= 8) return decode::fp16_run<8, WIN>(a, plan, s);
+    if (r <= 1) return decode::fp16_run<1, WIN, I8>(a, plan, s);
+    if (r <= 2) return decode::fp16_run<2, WIN, I8>(a, plan, s);
+    if (r <= 4) return decode::fp16_run<4, WIN, I8>(a, plan, s);
+    if (r <= 8) return decode::fp16_run<8, WIN, I8>(a, plan, s);
     return cudaErrorInvalidValue;
 }
-template <bool WIN>
+template <bool WIN, bool I8>
 int occ_r(const DecodeArgs& a, size_t smem) {
     const int r = a.Hq / a.Hkv;
-    if (r <= 1) return decode::fp16_occupancy<1, WIN>(smem);
-    if (r <= 2) return decode::fp16_occupancy<2, WIN>(smem);
-    if (r <= 4) return decode::fp16_occupancy<4, WIN>(smem);
-    if (r <= 8) return decode::fp16_occupancy<8, WIN>(smem);
+    if (r <= 1) return decode::fp16_occupancy<1, WIN, I8>(smem);
+    if (r <= 2) return decode::fp16_occupancy<2, WIN, I8>(smem);
+    if (r <= 4) return decode::fp16_occupancy<4, WIN, I8>(smem);
+    if (r <= 8) return decode::fp16_occupancy<8, WIN, I8>(smem);
     return 0;
 }
 
 cudaError_t decode_run_fp16(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {
-    return a.window > 0 ? run_r<true>(a, plan, s) : run_r<false>(a, plan, s);
+    if (a.int8) return a.window > 0 ? run_r<true, true>(a, plan, s) : run_r<false, true>(a, plan, s);
+    return a.window > 0 ? run_r<true, false>(a, plan, s) : run_r<false, false>(a, plan, s);
 }
 
 int decode_occupancy_fp16(const DecodeArgs& a, const DecodePlan& plan, size_t smem) {
     (void)plan;
-    return a.window > 0 ? occ_r<true>(a, smem) : occ_r<false>(a, smem);
+    if (a.int8) return a.window > 0 ? occ_r<true, true>(a, smem) : occ_r<false, true>(a, smem);
+    return a.window > 0 ? occ_r<true, false>(a, smem) : occ_r<false, false>(a, smem);
 }
 
 }  // namespace kvq

@@ -26,9 +26,35 @@
 namespace kvq {
 namespace decode {
 
+// One row of a staged block: this lane's 4 values (dimensions 4l .. 4l + 3) of row `row`
+// of K (is_v 0) or V (is_v 1).  FP16 blocks: K rows then V rows, P x D fp16 each.  INT8
+// blocks (the per-row codec of "AI inference tuning: KV Cache optimisation and memory
+// management" section 3.1): K codes P x D int8, V codes P x D int8, K scales P fp32, V
+// scales P fp32; a value is the fp32 product code * scale.
+template <bool I8, int D>
+__device__ __forceinline__ void block_row4(const uint8_t* blk, int P, int is_v, int row, int lane, float (&x)[4]) {
+    if constexpr (I8) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(blk + (is_v * P + row) * D + 4 * lane);
+        const float s = *reinterpret_cast<const float*>(blk + 2 * P * D + 4 * (is_v * P + row));
+        x[0] = static_cast<float>(static_cast<int8_t>(w & 0xffu)) * s;
+        x[1] = static_cast<float>(static_cast<int8_t>((w >> 8) & 0xffu)) * s;
+        x[2] = static_cast<float>(static_cast<int8_t>((w >> 16) & 0xffu)) * s;
+        x[3] = static_cast<float>(static_cast<int8_t>(w >> 24)) * s;
+    } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(blk + ((is_v * P + row) * D + 4 * lane) * 2);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+        x[0] = a.x;
+        x[1] = a.y;
+        x[2] = b.x;
+        x[3] = b.y;
+    }
+}
+
 // R: query heads per kv head, rounded up to 1, 2, 4 or 8.  WIN: the sequences list only
-// their window and sink pages (p.window > 0), as in decode_splitkv_kernel.
-template <int D, int R, bool WIN>
+// their window and sink pages (p.window > 0), as in decode_splitkv_kernel.  I8: INT8
+// per-row blocks instead of FP16 ones.
+template <int D, int R, bool WIN, bool I8 = false>
 __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
     static_assert(D == 128, "four dimensions per lane");
     constexpr int kWarps = 4;
@@ -208,8 +234,7 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
         for (int j = 0; j < cnt; ++j) {
             if (!failed && !__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * cst, cpar, kWaitLimitNs))) fail_here();
             if (!failed) {
-                const __half* kb = reinterpret_cast<const __half*>(ring + cst * ubytes);
-                const __half* vb = kb + p.P * D;
+                const uint8_t* blk = ring + cst * ubytes;
                 const int pg = pg0 + kWarps * j;
                 const int rp = WIN ? span_page(sspan, pg) : pg;  // the page (past a window gap)
                 for (int t0 = 0; t0 < p.P; t0 += T) {
@@ -222,9 +247,10 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
                     float a[R][T];
 #pragma unroll
                     for (int t = 0; t < T; ++t) {
-                        const uint2 w = *reinterpret_cast<const uint2*>(kb + (t0 + t) * D + 4 * lane);
-                        const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
-                        const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+                        float kx[4];
+                        block_row4<I8, D>(blk, p.P, 0, t0 + t, lane, kx);
+                        const float2 k0 = make_float2(kx[0], kx[1]);
+                        const float2 k1 = make_float2(kx[2], kx[3]);
 #pragma unroll
                         for (int s = 0; s < R; ++s)
                             a[s][t] = fmaf(qv[s][3], k1.y, fmaf(qv[s][2], k1.x, fmaf(qv[s][1], k0.y, qv[s][0] * k0.x)));
@@ -274,9 +300,10 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
                     // o += sum_tau p_tau v_tau
 #pragma unroll
                     for (int t = 0; t < T; ++t) {
-                        const uint2 w = *reinterpret_cast<const uint2*>(vb + (t0 + t) * D + 4 * lane);
-                        const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
-                        const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+                        float vx[4];
+                        block_row4<I8, D>(blk, p.P, 1, t0 + t, lane, vx);
+                        const float2 v0 = make_float2(vx[0], vx[1]);
+                        const float2 v1 = make_float2(vx[2], vx[3]);
 #pragma unroll
                         for (int s = 0; s < R; ++s) {
                             const float pt = __shfl_sync(0xffffffffu, pw[s], t << TSH);

@@ -96,7 +96,93 @@ __global__ void __launch_bounds__(256) dequantize_to_fp16_kernel(Fp16DequantArgs
     }
 }
 
+// INT8 per-row codec ("AI inference tuning: KV Cache optimisation and memory management"
+// section 3.1): rows k, v [B, n_new, Hkv, d] fp16 -> the INT8 pool at start_pos[b] + t.
+// One warp per K or V row, lane l on values 4l .. 4l + 3 (and 128 + 4l .. for d = 256):
+// scale = amax / 127 (IEEE division, floor 1e-8), code = clamp(rne(x / scale), -128, 127).
+// Block (page, kv head): K codes P x d int8, V codes P x d int8, K scales P fp32, V
+// scales P fp32.
+__global__ void __launch_bounds__(256) int8_quantize_kernel(Fp16AppendArgs a) {
+    const int lane = threadIdx.x & 31;
+    const long long rows = 2LL * a.B * a.n_new * a.Hkv;
+    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const long long block_bytes = 2LL * a.P * a.d + 8LL * a.P;
+    for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+         r += nwarps) {
+        const int is_v = static_cast<int>(r & 1);
+        const long long row = r >> 1;  // (b * n_new + t) * Hkv + h
+        const int h = static_cast<int>(row % a.Hkv);
+        const long long bt_ = row / a.Hkv;
+        const int t = static_cast<int>(bt_ % a.n_new);
+        const int b = static_cast<int>(bt_ / a.n_new);
+        const long long pos = static_cast<long long>(a.start_pos[b]) + t;
+        const long long pidx = pos >= 0 ? pos / a.P : -1;
+        if (pidx < 0 || pidx >= a.max_blocks) {
+            if (lane == 0 && is_v == 0) raise_flag(a.status, KVQ_FLAG_BAD_POSITION);
+            continue;
+        }
+        const int page = a.block_table[static_cast<long long>(b) * a.max_blocks + pidx];
+        if (page < 0 || page >= a.num_pages) {
+            if (lane == 0 && is_v == 0) raise_flag(a.status, KVQ_FLAG_BAD_PAGE);
+            continue;
+        }
+        const int slot = static_cast<int>(pos % a.P);
+        const __half* src = (is_v ? a.v : a.k) + row * a.d;
+        float x[2][4];
+        float amax = 0.f;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = lane + 32 * c2;  // 4-value chunk
+            if (4 * c < a.d) {
+                const uint2 w = reinterpret_cast<const uint2*>(src)[c];
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+                x[c2][0] = f0.x;
+                x[c2][1] = f0.y;
+                x[c2][2] = f1.x;
+                x[c2][3] = f1.y;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fabsf(x[c2][j]));
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        float sc = __fdiv_rn(amax, 127.0f);
+        if (sc < 1e-8f) sc = 1e-8f;
+        uint8_t* blk = a.pool16 + (static_cast<long long>(page) * a.Hkv + h) * block_bytes;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = lane + 32 * c2;
+            if (4 * c < a.d) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float q = rintf(__fdiv_rn(x[c2][j], sc));
+                    q = fminf(fmaxf(q, -128.f), 127.f);
+                    w |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xffu) << (8 * j);
+                }
+                *reinterpret_cast<uint32_t*>(blk + (static_cast<long long>(is_v) * a.P + slot) * a.d + 4 * c) = w;
+            }
+        }
+        if (lane == 0) *reinterpret_cast<float*>(blk + 2LL * a.P * a.d + 4LL * (is_v * a.P + slot)) = sc;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_int8_quantize_append(const Fp16AppendArgs& a, cudaStream_t stream) {
+    const long long rows = 2LL * a.B * a.n_new * a.Hkv;
+    if (rows == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long want = (rows + 7) / 8;
+    const long long grid = want < 8LL * sms ? want : 8LL * sms;
+    int8_quantize_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fp16_append(const Fp16AppendArgs& a, cudaStream_t stream) {
     const long long total = 2LL * a.B * a.n_new * a.Hkv * (a.d / 8);

@@ -109,8 +109,9 @@ int kvq_quantize_append(const kvq_cache_config* cfg, void* pool, const void* k, 
 }
 
 namespace {
+// codec: 0 the INT4 cache, 1 the FP16 cache, 2 the INT8 per-row cache
 size_t workspace_bytes_impl(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads, int32_t max_len,
-                            bool fp16) {
+                            int codec) {
     if (check_cfg(cfg) != KVQ_OK) return 0;
     if (batch < 1 || num_q_heads < 1 || max_len < 0 || num_q_heads % cfg->num_kv_heads) {
         fail(KVQ_EINVAL, "invalid batch / num_q_heads / max_len");
@@ -121,7 +122,8 @@ size_t workspace_bytes_impl(const kvq_cache_config* cfg, int32_t batch, int32_t 
     a.Hq = num_q_heads;
     a.Hkv = cfg->num_kv_heads;
     a.max_len = max_len;
-    a.fp16 = fp16;
+    a.fp16 = codec != 0;
+    a.int8 = codec == 2;
     a.L = kvq::block_layout(*cfg);
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
@@ -137,19 +139,24 @@ size_t workspace_bytes_impl(const kvq_cache_config* cfg, int32_t batch, int32_t 
 
 size_t kvq_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
                                   int32_t max_len) {
-    return workspace_bytes_impl(cfg, batch, num_q_heads, max_len, false);
+    return workspace_bytes_impl(cfg, batch, num_q_heads, max_len, 0);
 }
 
 size_t kvq_fp16_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
                                        int32_t max_len) {
-    return workspace_bytes_impl(cfg, batch, num_q_heads, max_len, true);
+    return workspace_bytes_impl(cfg, batch, num_q_heads, max_len, 1);
+}
+
+size_t kvq_int8_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_len) {
+    return workspace_bytes_impl(cfg, batch, num_q_heads, max_len, 2);
 }
 
 namespace {
 int decode_attention_impl(const kvq_cache_config* cfg, const void* pool, const void* q, const int32_t* block_table,
                           int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
                           int32_t max_len, float softmax_scale, int32_t window, int32_t sinks, float* out,
-                          void* workspace, size_t workspace_bytes, kvq_stream_t stream, bool fp16 = false) {
+                          void* workspace, size_t workspace_bytes, kvq_stream_t stream, int codec = 0) {
     if (int e = check_cfg(cfg)) return e;
     if (batch < 0 || num_q_heads < 1 || max_len < 0)
         return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
@@ -183,7 +190,8 @@ int decode_attention_impl(const kvq_cache_config* cfg, const void* pool, const v
     a.softmax_scale = softmax_scale;
     a.window = window;
     a.sinks = sinks;
-    a.fp16 = fp16;
+    a.fp16 = codec != 0;
+    a.int8 = codec == 2;
     a.L = kvq::block_layout(*cfg);
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
@@ -275,7 +283,15 @@ int kvq_fp16_decode_attention(const kvq_cache_config* cfg, const void* pool16, c
                               int32_t num_q_heads, int32_t max_len, float softmax_scale, float* out, void* workspace,
                               size_t workspace_bytes, kvq_stream_t stream) {
     return decode_attention_impl(cfg, pool16, q, block_table, max_blocks, seq_lens, batch, num_q_heads, max_len,
-                                 softmax_scale, 0, 0, out, workspace, workspace_bytes, stream, true);
+                                 softmax_scale, 0, 0, out, workspace, workspace_bytes, stream, 1);
+}
+
+int kvq_int8_decode_attention(const kvq_cache_config* cfg, const void* pool8, const void* q,
+                              const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                              int32_t num_q_heads, int32_t max_len, float softmax_scale, float* out, void* workspace,
+                              size_t workspace_bytes, kvq_stream_t stream) {
+    return decode_attention_impl(cfg, pool8, q, block_table, max_blocks, seq_lens, batch, num_q_heads, max_len,
+                                 softmax_scale, 0, 0, out, workspace, workspace_bytes, stream, 2);
 }
 
 int kvq_decode_step(const kvq_cache_config* cfg, void* pool, const void* k_new, const void* v_new,
@@ -331,9 +347,17 @@ size_t kvq_fp16_pool_bytes(const kvq_cache_config* cfg) {
     return static_cast<size_t>(cfg->num_pages) * cfg->num_kv_heads * 4u * cfg->page_size * cfg->head_dim;
 }
 
-int kvq_fp16_append(const kvq_cache_config* cfg, void* pool16, const void* k, const void* v,
+size_t kvq_int8_pool_bytes(const kvq_cache_config* cfg) {
+    if (check_cfg(cfg) != KVQ_OK) return 0;
+    return static_cast<size_t>(cfg->num_pages) * cfg->num_kv_heads *
+           (2u * cfg->page_size * cfg->head_dim + 8u * cfg->page_size);
+}
+
+namespace {
+// rows into the FP16 cache unchanged, or quantized into the INT8 per-row cache
+int rows_append_impl(const kvq_cache_config* cfg, void* pool16, const void* k, const void* v,
                     const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
-                    int32_t n_new, uint32_t* status, kvq_stream_t stream) {
+                    int32_t n_new, uint32_t* status, kvq_stream_t stream, bool int8) {
     if (int e = check_cfg(cfg)) return e;
     if (batch < 0 || n_new < 0) return fail(KVQ_EINVAL, "batch %d / n_new %d negative", batch, n_new);
     if (batch == 0 || n_new == 0) return ok();
@@ -357,9 +381,28 @@ int kvq_fp16_append(const kvq_cache_config* cfg, void* pool16, const void* k, co
     a.d = cfg->head_dim;
     a.P = cfg->page_size;
     a.num_pages = cfg->num_pages;
-    cudaError_t e = kvq::launch_fp16_append(a, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "kvq_fp16_append launch");
+    if (int8 && (cfg->head_dim % 4 || cfg->head_dim > 256))
+        return fail(KVQ_EUNSUPPORTED, "the INT8 cache needs head_dim a multiple of 4, at most 256");
+    cudaError_t e = int8 ? kvq::launch_int8_quantize_append(a, reinterpret_cast<cudaStream_t>(stream))
+                         : kvq::launch_fp16_append(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, int8 ? "kvq_int8_quantize_append launch" : "kvq_fp16_append launch");
     return ok();
+}
+
+}  // namespace
+
+int kvq_fp16_append(const kvq_cache_config* cfg, void* pool16, const void* k, const void* v,
+                    const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
+                    int32_t n_new, uint32_t* status, kvq_stream_t stream) {
+    return rows_append_impl(cfg, pool16, k, v, block_table, max_blocks, start_pos, batch, n_new, status, stream,
+                            false);
+}
+
+int kvq_int8_quantize_append(const kvq_cache_config* cfg, void* pool8, const void* k, const void* v,
+                             const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
+                             int32_t n_new, uint32_t* status, kvq_stream_t stream) {
+    return rows_append_impl(cfg, pool8, k, v, block_table, max_blocks, start_pos, batch, n_new, status, stream,
+                            true);
 }
 
 int kvq_dequantize_to_fp16_pool(const kvq_cache_config* cfg, const void* pool, void* pool16,

@@ -112,8 +112,10 @@ struct DecodeArgs {
     // sliding window with sink tokens: the last `window` positions (0: all) and the first `sinks`
     int32_t window = 0;
     int32_t sinks = 0;
-    // attention over the FP16 cache instead of the INT4 one (the comparison's baseline)
+    // attention over the FP16 cache instead of the INT4 one (the comparison's baseline), or
+    // (with int8 also set) over the INT8 per-row cache; both take the CUDA-core kernel
     bool fp16 = false;
+    bool int8 = false;
     // attend seq_lens[b] - len_sub positions (the INT4 part of the mixed-precision decode)
     int32_t len_sub = 0;
     // status word (nullptr: the first word of the workspace)
@@ -141,6 +143,8 @@ struct Fp16DequantArgs {
     BlockLayout L;
 };
 cudaError_t launch_fp16_append(const Fp16AppendArgs& a, cudaStream_t stream);
+// INT8 per-row cache: quantize-append, arguments as for the FP16 append
+cudaError_t launch_int8_quantize_append(const Fp16AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_dequantize_to_fp16(const Fp16DequantArgs& a, long long max_pages, cudaStream_t stream);
 
 // Returns cudaErrorInvalidValue for a geometry no kernel instance covers.
