@@ -336,14 +336,16 @@ def run_kvq(args, world, rank, local):
 
     prefill(caches[0])
     # the comparison's FP16 cache holds the same fp16 history
-    pool16 = None
+    pool16 = pool8 = None
     if getattr(args, "compare", False):
         pool16 = torch.zeros(kvq.kvq_fp16_pool_bytes(cfg), dtype=torch.uint8, device=dev)
-        if same_ctx:
-            kvq.kvq_fp16_append(cfg, pool16, hist[0][0], hist[0][1], caches[0].block_table, zero)
-        else:
-            for b, (kb, vb) in enumerate(hist):
-                kvq.kvq_fp16_append(cfg, pool16, kb, vb, caches[0].block_table[b:b + 1], zero)
+        pool8 = torch.zeros(kvq.kvq_int8_pool_bytes(cfg), dtype=torch.uint8, device=dev)
+        for fn, pl in ((kvq.kvq_fp16_append, pool16), (kvq.kvq_int8_quantize_append, pool8)):
+            if same_ctx:
+                fn(cfg, pl, hist[0][0], hist[0][1], caches[0].block_table, zero)
+            else:
+                for b, (kb, vb) in enumerate(hist):
+                    fn(cfg, pl, kb, vb, caches[0].block_table[b:b + 1], zero)
     torch.cuda.synchronize()
     qt = []
     for _ in range(3):
@@ -366,6 +368,7 @@ def run_kvq(args, world, rank, local):
     v_new = torch.gather(v_all, 1, idx).contiguous()
     if pool16 is not None:  # the new token, as the INT4 step appends it
         kvq.kvq_fp16_append(cfg, pool16, k_new, v_new, caches[0].block_table, pos)
+        kvq.kvq_int8_quantize_append(cfg, pool8, k_new, v_new, caches[0].block_table, pos)
     del k_all, v_all, hist
     torch.cuda.empty_cache()
     seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
@@ -494,6 +497,13 @@ def run_kvq(args, world, rank, local):
             kvq.kvq_mixed_decode_attention(cfg16, caches[0].pool, bt0, pool16, bt0, cfg16.num_pages, q, seq_lens,
                                            wl.max_len, R, scale, out16, wsm, stream=stream)
 
+        ws8 = torch.zeros(kvq.kvq_int8_decode_workspace_bytes(cfg16, wl.B, wl.Hq, wl.max_len), dtype=torch.uint8,
+                          device=dev)
+
+        def int8_attend():
+            kvq.kvq_int8_decode_attention(cfg16, pool8, q, bt0, seq_lens, wl.max_len, scale, out16, ws8, stream=stream)
+
+        t8 = per_call(int8_attend)
         t16 = per_call(fp16_attend)
         tdq = per_call(deq_then_attend)
         tmx = per_call(mixed_attend)
@@ -505,12 +515,15 @@ def run_kvq(args, world, rank, local):
             "int4_dequant_then_attend_us": tdq * 1e6,
             "int4_fused_us": decode_s * 1e6,
             "mixed_int4_fp16_last128_us": tmx * 1e6,
+            "int8_per_row_us": t8 * 1e6,
+            "int8_bytes": (2 * wl.d + 8) * sum(wl.seq_lens) * wl.Hkv,
             "fp16_bytes": fp16_bytes, "int4_bytes": wl.decode_bytes(),
             "fused_speedup_vs_fp16": t16 / decode_s, "fused_speedup_vs_dequant_then_attend": tdq / decode_s,
         }
         if rank == 0:
             print(f"[compare] fp16 {t16 * 1e6:.1f} us ({fp16_bytes / t16 / 1e9:.0f} GB/s), dequant+attend "
-                  f"{tdq * 1e6:.1f} us, int4 fused {decode_s * 1e6:.1f} us, mixed (last {R} fp16) {tmx * 1e6:.1f} us",
+                  f"{tdq * 1e6:.1f} us, int4 fused {decode_s * 1e6:.1f} us, mixed (last {R} fp16) {tmx * 1e6:.1f} us, "
+                  f"int8 {t8 * 1e6:.1f} us ({(2 * wl.d + 8) * sum(wl.seq_lens) * wl.Hkv / t8 / 1e9:.0f} GB/s)",
                   file=sys.stderr)
     # the step leaves the output of the last decode step in `out` for e2e and checks
     flags = max(c.flags() for c in caches)

@@ -34,12 +34,13 @@ namespace decode {
 template <bool I8, int D>
 __device__ __forceinline__ void block_row4(const uint8_t* blk, int P, int is_v, int row, int lane, float (&x)[4]) {
     if constexpr (I8) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(blk + (is_v * P + row) * D + 4 * lane);
+        // code c (int8) -> c + 128 in the low mantissa byte of 2^23: the float 2^23 + 128 + c,
+        // minus 2^23 + 128, is c exactly (one byte permute and one add per value)
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(blk + (is_v * P + row) * D + 4 * lane) ^ 0x80808080u;
         const float s = *reinterpret_cast<const float*>(blk + 2 * P * D + 4 * (is_v * P + row));
-        x[0] = static_cast<float>(static_cast<int8_t>(w & 0xffu)) * s;
-        x[1] = static_cast<float>(static_cast<int8_t>((w >> 8) & 0xffu)) * s;
-        x[2] = static_cast<float>(static_cast<int8_t>((w >> 16) & 0xffu)) * s;
-        x[3] = static_cast<float>(static_cast<int8_t>(w >> 24)) * s;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            x[j] = (__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + j)) - 8388736.0f) * s;
     } else {
         const uint2 w = *reinterpret_cast<const uint2*>(blk + ((is_v * P + row) * D + 4 * lane) * 2);
         const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
