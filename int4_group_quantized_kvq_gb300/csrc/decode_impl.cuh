@@ -974,213 +974,6 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     }
 }
 
-// ---------------------------------------------------------------------------
-// Combine: the warp partials of each (sequence, query head) row into its output.
-// ---------------------------------------------------------------------------
-// One source of partials: a decode grid's workspace region and how that grid listed
-// each sequence's pages and laid out its partials.
-struct CSource {
-    const float* ws_ml;
-    const float* ws_o;
-    const int32_t* ws_pre;  // the pages prefix the grid publishes (used above kCombineLocalB)
-    int32_t Hg, ns;         // head groups of the grid's units, query heads per unit
-    int32_t C, W;           // the grid's CTAs, and warps per CTA (partials per CTA and segment)
-    int32_t max_blocks, window, sinks, len_sub;  // as in KParams
-};
-
-struct CParams {
-    CSource src[2];
-    int32_t nsrc;  // 1, or 2 for the mixed-precision decode (INT4 history, FP16 recent tokens)
-    const int32_t* seq_lens;
-    float* out;
-    int32_t B, Hq, lg_p;
-};
-
-constexpr int kCombineMaxWarps = 16;
-constexpr int kCombineBatch = 8;      // partials loaded together by a warp
-constexpr int kCombineLocalB = 256;   // up to this batch the row metadata is computed before the wait
-
-// One CTA per output row (b, hq).  In source s the row's partials sit at W * (cf + seg) + j
-// for j < W * (cl - cf + 1), where CTAs cf..cl of that grid hold the units of segment
-// seg = (b, hq / ns); when some CTA slices are empty (fewer units than CTAs) their partials
-// do not exist.  Warp w of the CTA takes partials w, w + nw, ..., eight at a time, keeping
-// a running maximum M and sum L and an unnormalised output (lane l: dimensions 4l .. 4l + 3),
-// over the sources in turn; the warps' results are then merged with weights 2^(M_w - max M).
-// Sequences without positions have no partials and get zeros.  This is the split-KV
-// combine of flash decoding: out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
-template <int D>
-__global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams p) {
-    static_assert(D == 128, "one float4 per lane");
-    // the next decode call may start its set-up; it waits for this grid before it
-    // touches the workspace
-    asm volatile("griddepcontrol.launch_dependents;");
-    __shared__ float s_m[kCombineMaxWarps], s_l[kCombineMaxWarps];
-    __shared__ float4 s_o[kCombineMaxWarps][D / 4];
-    __shared__ int s_red[2][2][kCombineMaxWarps];
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int nw = blockDim.x >> 5;
-    const int b = static_cast<int>(blockIdx.x / p.Hq);
-    const int hq = static_cast<int>(blockIdx.x - static_cast<long long>(b) * p.Hq);
-
-    // Pages of sequence i as source s listed them, and the row's range of partials.
-    auto pages_of = [&](const CSource& s, int i) {
-        return seq_span(p.seq_lens[i] - s.len_sub, p.lg_p, s.max_blocks, s.window, s.sinks).np;
-    };
-    auto row_range = [&](const CSource& s, int pb_, int np_, int tot_, long long& cf_, long long& base_,
-                         long long& U_) {
-        const int hg = hq / s.ns;
-        U_ = static_cast<long long>(s.Hg) * tot_;
-        const long long sf = static_cast<long long>(s.Hg) * pb_ + static_cast<long long>(hg) * np_;
-        cf_ = slice_of(sf, U_, s.C);
-        const long long cl = slice_of(sf + np_ - 1, U_, s.C);
-        base_ = static_cast<long long>(s.W) * (cf_ + static_cast<long long>(b) * s.Hg + hg);
-        return s.W * static_cast<int>(cl - cf_ + 1);
-    };
-    int n[2] = {0, 0};
-    long long cf[2] = {0, 0}, base[2] = {0, 0}, U[2] = {1, 1};
-
-    // The row's pages prefix: for small batches from seq_lens (a read-only input) while
-    // the decode grids still run; else from the prefix each decode grid publishes.
-    const bool local = p.B <= kCombineLocalB;
-    if (local) {
-#pragma unroll
-        for (int si = 0; si < 2; ++si) {
-            if (si >= p.nsrc) break;
-            int before = 0, all = 0;
-            for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
-                const int n_i = pages_of(p.src[si], i);
-                all += n_i;
-                if (i < b) before += n_i;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                before += __shfl_xor_sync(0xffffffffu, before, off);
-                all += __shfl_xor_sync(0xffffffffu, all, off);
-            }
-            if (lane == 0) {
-                s_red[si][0][warp] = before;
-                s_red[si][1][warp] = all;
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int si = 0; si < 2; ++si) {
-            if (si >= p.nsrc) break;
-            int pb = 0, tot = 0;
-            for (int w = 0; w < nw; ++w) {
-                pb += s_red[si][0][w];
-                tot += s_red[si][1][w];
-            }
-            const int np = pages_of(p.src[si], b);
-            if (np > 0) n[si] = row_range(p.src[si], pb, np, tot, cf[si], base[si], U[si]);
-        }
-    }
-
-    // the partials (and the published prefixes) are written by the decode grids ahead of this one
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (!local) {
-#pragma unroll
-        for (int si = 0; si < 2; ++si) {
-            if (si >= p.nsrc) break;
-            const int32_t* pre = p.src[si].ws_pre;
-            const int pb = __ldcg(pre + b);
-            const int np = __ldcg(pre + b + 1) - pb;
-            const int tot = __ldcg(pre + p.B);
-            if (np > 0) n[si] = row_range(p.src[si], pb, np, tot, cf[si], base[si], U[si]);
-        }
-    }
-
-    float M = -INFINITY, L = 0.f;
-    float4 acc[4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) acc[a] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int si = 0; si < 2; ++si) {
-        if (si >= p.nsrc) break;
-        const CSource& s = p.src[si];
-        const int sl = hq - (hq / s.ns) * s.ns;
-        const bool dense = U[si] >= s.C;  // every CTA slice holds units
-        const long long stride_ml = static_cast<long long>(s.ns) * 2;
-        const long long stride_o = static_cast<long long>(s.ns) * D;
-        const float* ml0 = s.ws_ml + (base[si] * s.ns + sl) * 2;
-        const float* o0 = s.ws_o + (base[si] * s.ns + sl) * D + 4 * lane;
-        for (int j0 = warp; j0 < n[si]; j0 += kCombineBatch * nw) {
-            float2 ml[kCombineBatch];
-            float4 ov[kCombineBatch];
-#pragma unroll
-            for (int kk = 0; kk < kCombineBatch; ++kk) {
-                const int j = j0 + kk * nw;
-                bool have = j < n[si];
-                if (have && !dense) {
-                    const long long k = cf[si] + j / s.W;
-                    have = slice_start(k, U[si], s.C) < slice_start(k + 1, U[si], s.C);
-                }
-                if (have) {
-                    ml[kk] = __ldcg(reinterpret_cast<const float2*>(ml0 + j * stride_ml));
-                    ov[kk] = __ldcg(reinterpret_cast<const float4*>(o0 + j * stride_o));
-                } else {
-                    ml[kk] = make_float2(-INFINITY, 0.f);
-                    ov[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-            float mb = M;
-#pragma unroll
-            for (int kk = 0; kk < kCombineBatch; ++kk) mb = fmaxf(mb, ml[kk].x);
-            if (mb == -INFINITY) continue;  // only empty partials so far
-            if (mb > M) {  // a larger running maximum: rescale what has been summed
-                const float f = fast_exp2(M - mb);
-                L *= f;
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    acc[a].x *= f;
-                    acc[a].y *= f;
-                    acc[a].z *= f;
-                    acc[a].w *= f;
-                }
-                M = mb;
-            }
-#pragma unroll
-            for (int kk = 0; kk < kCombineBatch; ++kk) {
-                const float f = fast_exp2(ml[kk].x - M);
-                L = fmaf(f, ml[kk].y, L);
-                float4& A = acc[kk & 3];
-                A.x = fmaf(f, ov[kk].x, A.x);
-                A.y = fmaf(f, ov[kk].y, A.y);
-                A.z = fmaf(f, ov[kk].z, A.z);
-                A.w = fmaf(f, ov[kk].w, A.w);
-            }
-        }
-    }
-    if (lane == 0) {
-        s_m[warp] = M;
-        s_l[warp] = L;
-    }
-    s_o[warp][lane] = make_float4(acc[0].x + acc[1].x + acc[2].x + acc[3].x, acc[0].y + acc[1].y + acc[2].y + acc[3].y,
-                                  acc[0].z + acc[1].z + acc[2].z + acc[3].z, acc[0].w + acc[1].w + acc[2].w + acc[3].w);
-    __syncthreads();
-    if (warp == 0) {
-        float Mx = -INFINITY;
-        for (int w = 0; w < nw; ++w) Mx = fmaxf(Mx, s_m[w]);
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-        float Ls = 0.f;
-        if (Mx != -INFINITY) {
-            for (int w = 0; w < nw; ++w) {
-                const float f = fast_exp2(s_m[w] - Mx);
-                const float4 ow = s_o[w][lane];
-                Ls = fmaf(f, s_l[w], Ls);
-                O.x = fmaf(f, ow.x, O.x);
-                O.y = fmaf(f, ow.y, O.y);
-                O.z = fmaf(f, ow.z, O.z);
-                O.w = fmaf(f, ow.w, O.w);
-            }
-        }
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-        reinterpret_cast<float4*>(p.out + (static_cast<long long>(b) * p.Hq + hq) * D)[lane] =
-            make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
-    }
-}
-
 // Raise the kernel's dynamic shared-memory limit once to the largest size asked for,
 // so repeated calls (and calls under stream capture) only launch.
 template <int D, int GK, int GV, int HK, int HS, bool WIN>
