@@ -557,38 +557,42 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         }
 
         // -------- online softmax over the step's positions (per slot, lanes with the same c) --------
-        float mn[HS];
-        bool grow = false;
+        // The slot's maximum over the step is reduced across lanes only when some lane holds a
+        // score above the running maximum; otherwise the reduced value could not raise it, and
+        // the running maximum stays as it is (most steps once a segment is under way).
+        float cm[HS];
+        bool up = false;
 #pragma unroll
         for (int s = 0; s < HS; ++s) {
-            float cm = fmaxf(z[0][s][0], z[0][s][1]);
+            cm[s] = fmaxf(z[0][s][0], z[0][s][1]);
 #pragma unroll
-            for (int X = 1; X < TG; ++X) cm = fmaxf(cm, fmaxf(z[X][s][0], z[X][s][1]));
-            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
-            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
-            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
-            mn[s] = fmaxf(m[s], cm);
-            grow |= mn[s] > m[s];
+            for (int X = 1; X < TG; ++X) cm[s] = fmaxf(cm[s], fmaxf(z[X][s][0], z[X][s][1]));
+            up |= cm[s] > m[s];
         }
-        if (__any_sync(0xffffffffu, grow)) {
+        if (__any_sync(0xffffffffu, up)) {
 #pragma unroll
             for (int s = 0; s < HS; ++s) {
-                const float alpha = fast_exp2(m[s] - mn[s]);
+                float r = cm[s];
+                r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, 4));
+                r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, 8));
+                r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, 16));
+                const float mn = fmaxf(m[s], r);
+                const float alpha = fast_exp2(m[s] - mn);
                 l[s] *= alpha;
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) o[mt][s][e] *= alpha;
+                m[s] = mn;
             }
         }
         float pr[TG][HS][2];
 #pragma unroll
         for (int s = 0; s < HS; ++s) {
-            m[s] = mn[s];
 #pragma unroll
             for (int X = 0; X < TG; ++X) {
-                pr[X][s][0] = fast_exp2(z[X][s][0] - mn[s]);
-                pr[X][s][1] = fast_exp2(z[X][s][1] - mn[s]);
+                pr[X][s][0] = fast_exp2(z[X][s][0] - m[s]);
+                pr[X][s][1] = fast_exp2(z[X][s][1] - m[s]);
                 l[s] += pr[X][s][0] + pr[X][s][1];
             }
         }
