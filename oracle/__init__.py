@@ -85,6 +85,24 @@ def lib() -> C.CDLL:
         L.kvq_oracle_int8_decode_attention.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
                                                        C.c_int, C.c_int, C.c_double, C.c_void_p] + [C.c_int] * 4
         L.kvq_oracle_int8_decode_attention.restype = C.c_int
+        L.kvq_oracle_lloyd_max_normal.argtypes = [C.c_int, C.c_void_p, C.c_void_p]
+        L.kvq_oracle_lloyd_max_normal.restype = C.c_int
+        L.kvq_oracle_wht_f32.argtypes = [C.c_void_p, C.c_int]
+        L.kvq_oracle_wht_f32.restype = None
+        L.kvq_oracle_wht4_block_bytes.argtypes = [C.c_int, C.c_int]
+        L.kvq_oracle_wht4_block_bytes.restype = C.c_size_t
+        L.kvq_oracle_wht4_tables.argtypes = [C.c_void_p, C.c_void_p]
+        L.kvq_oracle_wht4_tables.restype = None
+        L.kvq_oracle_wht4_quantize_row.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
+        L.kvq_oracle_wht4_quantize_row.restype = C.c_int
+        L.kvq_oracle_wht4_quantize_append.argtypes = [C.c_void_p] * 4 + [C.c_int, C.c_void_p] + [C.c_int] * 6
+        L.kvq_oracle_wht4_quantize_append.restype = C.c_int
+        L.kvq_oracle_wht4_dequantize.argtypes = [C.c_void_p, C.c_void_p] + [C.c_int] * 4 + [C.c_void_p] * 2 + \
+            [C.c_int] * 4
+        L.kvq_oracle_wht4_dequantize.restype = C.c_int
+        L.kvq_oracle_wht4_decode_attention.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
+                                                       C.c_int, C.c_int, C.c_double, C.c_void_p] + [C.c_int] * 4
+        L.kvq_oracle_wht4_decode_attention.restype = C.c_int
         _lib = L
     return _lib
 
@@ -341,4 +359,86 @@ def int8_decode_attention(L: Layout, pool8: np.ndarray, q: np.ndarray, block_tab
     rc = lib().kvq_oracle_int8_decode_attention(_ptr(pool8), _ptr(q), _ptr(bt), int(bt.shape[1]), _ptr(sl), B, Hq,
                                                 float(softmax_scale), _ptr(out), L.Hkv, L.d, L.P, L.num_pages)
     _check(rc, "int8_decode_attention")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The rotated 4-bit codec ("LARQL KV cache engines", engine three: Walsh-Hadamard
+# rotation, Lloyd-Max codebook; the reading is written out in kvq_oracle.c).
+# ---------------------------------------------------------------------------
+def lloyd_max_normal(bits: int) -> tuple[np.ndarray, np.ndarray]:
+    """Lloyd-Max levels (2^bits, ascending) and thresholds (2^bits - 1) of N(0, 1), fp64."""
+    n = 1 << bits
+    lv = np.zeros(n, np.float64)
+    tb = np.zeros(n - 1, np.float64)
+    it = lib().kvq_oracle_lloyd_max_normal(bits, _ptr(lv), _ptr(tb))
+    if it < 0:
+        raise ValueError("bits out of range")
+    return lv, tb
+
+
+def wht_f32(y: np.ndarray) -> np.ndarray:
+    """The fast Walsh-Hadamard transform (unnormalised, stage order h = 1, 2, ..) in fp32."""
+    out = np.ascontiguousarray(y, dtype=np.float32).copy()
+    lib().kvq_oracle_wht_f32(_ptr(out), int(out.size))
+    return out
+
+
+def wht4_tables() -> tuple[np.ndarray, np.ndarray]:
+    """fp32 levels (16) and thresholds (15) of the 4-bit codec."""
+    c = np.zeros(16, np.float32)
+    t = np.zeros(15, np.float32)
+    lib().kvq_oracle_wht4_tables(_ptr(c), _ptr(t))
+    return c, t
+
+
+def wht4_block_bytes(head_dim: int, page_size: int) -> int:
+    return int(lib().kvq_oracle_wht4_block_bytes(head_dim, page_size))
+
+
+def wht4_pool_bytes(L: Layout) -> int:
+    return L.num_pages * L.Hkv * wht4_block_bytes(L.d, L.P)
+
+
+def wht4_quantize_row(x_f16: np.ndarray) -> tuple[np.ndarray, float]:
+    """One fp16 row of 128 -> (64 code bytes, fp32 sigma)."""
+    x = np.ascontiguousarray(x_f16, dtype=np.float16)
+    codes = np.zeros(x.size // 2, np.uint8)
+    s = np.zeros(1, np.float32)
+    _check(lib().kvq_oracle_wht4_quantize_row(_ptr(x), int(x.size), _ptr(codes), _ptr(s)), "wht4_quantize_row")
+    return codes, float(s[0])
+
+
+def wht4_quantize_append(L: Layout, pool: np.ndarray, k: np.ndarray, v: np.ndarray, block_table: np.ndarray,
+                         start_pos: np.ndarray) -> None:
+    k = np.ascontiguousarray(k, dtype=np.float16)
+    v = np.ascontiguousarray(v, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sp = np.ascontiguousarray(start_pos, dtype=np.int32)
+    rc = lib().kvq_oracle_wht4_quantize_append(_ptr(pool), _ptr(k), _ptr(v), _ptr(bt), int(bt.shape[1]), _ptr(sp),
+                                               int(k.shape[0]), int(k.shape[1]), L.Hkv, L.d, L.P, L.num_pages)
+    _check(rc, "wht4_quantize_append")
+
+
+def wht4_dequantize(L: Layout, pool: np.ndarray, block_table: np.ndarray, b: int, start: int,
+                    n: int) -> tuple[np.ndarray, np.ndarray]:
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    ok = np.zeros((n, L.Hkv, L.d), np.float32)
+    ov = np.zeros((n, L.Hkv, L.d), np.float32)
+    rc = lib().kvq_oracle_wht4_dequantize(_ptr(pool), _ptr(bt), int(bt.shape[1]), b, start, n, _ptr(ok), _ptr(ov),
+                                          L.Hkv, L.d, L.P, L.num_pages)
+    _check(rc, "wht4_dequantize")
+    return ok, ov
+
+
+def wht4_decode_attention(L: Layout, pool: np.ndarray, q: np.ndarray, block_table: np.ndarray,
+                          seq_lens: np.ndarray, softmax_scale: float) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    out = np.zeros((B, Hq, L.d), np.float64)
+    rc = lib().kvq_oracle_wht4_decode_attention(_ptr(pool), _ptr(q), _ptr(bt), int(bt.shape[1]), _ptr(sl), B, Hq,
+                                                float(softmax_scale), _ptr(out), L.Hkv, L.d, L.P, L.num_pages)
+    _check(rc, "wht4_decode_attention")
     return out

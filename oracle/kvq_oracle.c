@@ -740,3 +740,268 @@ int kvq_oracle_int8_decode_attention(const uint8_t *pool8, const uint16_t *q, co
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The rotated 4-bit codec ([L] "LARQL KV cache engines", engine three,      */
+/* codec/turbo-quant: each K or V row of a head is rotated by a Walsh-       */
+/* Hadamard transform and quantized with a Lloyd-Max codebook to 3 or 4     */
+/* bits; head_dim must be a power of two; approximate, per-row cosine       */
+/* about 0.9954 at 4 bits).  The page names the two steps only; the reading */
+/* written out here (and restated independently by the CUDA library):       */
+/*  - x_i = fp32(fp16 input), d = 128;                                       */
+/*  - y = H x, H the unnormalised Sylvester-order Walsh-Hadamard matrix,     */
+/*    computed by the fast transform: stages h = 1, 2, 4, .., d/2, each pair */
+/*    (i, i+h) with (i & h) == 0 becoming (y_i + y_{i+h}, y_i - y_{i+h}),    */
+/*    one fp32 rounding per addition;                                        */
+/*  - sigma = sqrt(sum x_i^2) = the RMS of y (H H = d I), the squares and    */
+/*    sums rounded to fp32 in a fixed tree: 32 partial sums of 4 elements    */
+/*    ((x0^2 + x1^2) + (x2^2 + x3^2)) for elements 4l .. 4l+3, then for      */
+/*    off = 16, 8, 4, 2, 1 every partial l becomes s_l + s_{l xor off};     */
+/*  - u_i = y_i / sigma (fp32 division); the code of u_i is the number of   */
+/*    thresholds T_1 < .. < T_15 with u_i >= T_j, T_j = fp32 of the midpoint */
+/*    of Lloyd-Max levels j-1 and j (fp64) for the standard normal, 16      */
+/*    levels; an all-zero row (sigma = 0) takes codes 0;                    */
+/*  - stored: the codes as nibbles (element 2j in the low nibble of byte j) */
+/*    and sigma as fp32;                                                     */
+/*  - dequantized: x^ = H (sigma * c) / d, c_j = fp32 of level j.            */
+/* Block (page, kv head), index page*Hkv + h, P*(d + 8) bytes: K codes      */
+/* P x d/2, V codes P x d/2, K sigma P fp32, V sigma P fp32.                 */
+/* ------------------------------------------------------------------------ */
+
+static double std_normal_pdf(double t) {
+    if (isinf(t)) return 0.0;
+    return exp(-0.5 * t * t) / sqrt(2.0 * 3.14159265358979323846);
+}
+static double std_normal_cdf(double t) {
+    if (isinf(t)) return t > 0 ? 1.0 : 0.0;
+    return 0.5 * erfc(-t / sqrt(2.0));
+}
+
+/* Lloyd-Max quantizer of the standard normal with 2^bits levels (bits 1..5),
+ * by Lloyd's alternation: the thresholds are the midpoints of adjacent levels,
+ * each level the mean of the normal restricted to its cell,
+ *   L_j = (pdf(T_j) - pdf(T_{j+1})) / (cdf(T_{j+1}) - cdf(T_j)),
+ * iterated from evenly spaced levels until no level moves by more than
+ * 1e-15.  The normal law is symmetric, and so is its quantizer: the levels are
+ * then made exactly antisymmetric (level n-1-j set to (L_{n-1-j} - L_j) / 2 and
+ * level j to its negation), which puts the middle threshold at exactly 0.
+ * levels[2^bits] ascending; thresholds[2^bits - 1], thresholds[j-1] between
+ * levels j-1 and j.  Returns the iteration count, or -1. */
+int kvq_oracle_lloyd_max_normal(int bits, double *levels, double *thresholds) {
+    if (bits < 1 || bits > 5) return -1;
+    int n = 1 << bits;
+    double lv[32], tb[33];
+    for (int j = 0; j < n; ++j) lv[j] = -3.0 + 6.0 * (j + 0.5) / n;
+    int it;
+    for (it = 1; it <= 200000; ++it) {
+        tb[0] = -INFINITY;
+        tb[n] = INFINITY;
+        for (int j = 1; j < n; ++j) tb[j] = 0.5 * (lv[j - 1] + lv[j]);
+        double moved = 0.0;
+        for (int j = 0; j < n; ++j) {
+            double mass = std_normal_cdf(tb[j + 1]) - std_normal_cdf(tb[j]);
+            double nl = (std_normal_pdf(tb[j]) - std_normal_pdf(tb[j + 1])) / mass;
+            double dj = fabs(nl - lv[j]);
+            if (dj > moved) moved = dj;
+            lv[j] = nl;
+        }
+        if (moved <= 1e-15) break;
+    }
+    for (int j = 0; j < n / 2; ++j) {
+        double a = 0.5 * (lv[n - 1 - j] - lv[j]);
+        lv[j] = -a;
+        lv[n - 1 - j] = a;
+    }
+    for (int j = 0; j < n; ++j) levels[j] = lv[j];
+    for (int j = 1; j < n; ++j) thresholds[j - 1] = 0.5 * (lv[j - 1] + lv[j]);
+    return it;
+}
+
+/* The fast Walsh-Hadamard transform in place, fp32, stage order h = 1, 2, .. */
+void kvq_oracle_wht_f32(float *y, int d) {
+    for (int h = 1; h < d; h <<= 1)
+        for (int i = 0; i < d; ++i)
+            if ((i & h) == 0) {
+                float a = y[i], b = y[i + h];
+                y[i] = a + b;
+                y[i + h] = a - b;
+            }
+}
+
+/* The same transform in fp64. */
+static void wht_f64(double *y, int d) {
+    for (int h = 1; h < d; h <<= 1)
+        for (int i = 0; i < d; ++i)
+            if ((i & h) == 0) {
+                double a = y[i], b = y[i + h];
+                y[i] = a + b;
+                y[i + h] = a - b;
+            }
+}
+
+size_t kvq_oracle_wht4_block_bytes(int head_dim, int page_size) {
+    if (head_dim <= 0 || page_size <= 0) return 0;
+    return (size_t)page_size * ((size_t)head_dim + 8);
+}
+
+/* fp32 codebook of the 4-bit codec: levels c_j and thresholds T_j */
+static void wht4_tables(float *c, float *T) {
+    static int ready = 0;
+    static float cs[16], ts[15];
+    if (!ready) {
+        double lv[16], tb[15];
+        kvq_oracle_lloyd_max_normal(4, lv, tb);
+        for (int j = 0; j < 16; ++j) cs[j] = (float)lv[j];
+        for (int j = 0; j < 15; ++j) ts[j] = (float)tb[j];
+        ready = 1;
+    }
+    memcpy(c, cs, sizeof cs);
+    memcpy(T, ts, sizeof ts);
+}
+
+void kvq_oracle_wht4_tables(float *levels16, float *thresholds15) { wht4_tables(levels16, thresholds15); }
+
+/* one row of d = 128 fp16 values -> d/2 code bytes and sigma */
+int kvq_oracle_wht4_quantize_row(const uint16_t *x, int d, uint8_t *codes, float *sigma_out) {
+    if (d != 128) return ORACLE_EINVAL;
+    float c[16], T[15], y[128], s[32];
+    wht4_tables(c, T);
+    for (int i = 0; i < d; ++i) y[i] = kvq_oracle_f16_to_f32(x[i]);
+    for (int l = 0; l < 32; ++l) {
+        float a0 = y[4 * l] * y[4 * l], a1 = y[4 * l + 1] * y[4 * l + 1];
+        float a2 = y[4 * l + 2] * y[4 * l + 2], a3 = y[4 * l + 3] * y[4 * l + 3];
+        s[l] = (a0 + a1) + (a2 + a3);
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+        float t[32];
+        for (int l = 0; l < 32; ++l) t[l] = s[l] + s[l ^ off];
+        memcpy(s, t, sizeof t);
+    }
+    float sigma = sqrtf(s[0]);
+    kvq_oracle_wht_f32(y, d);
+    memset(codes, 0, (size_t)d / 2);
+    for (int i = 0; i < d; ++i) {
+        int code = 0;
+        if (sigma > 0.0f) {
+            float u = y[i] / sigma;
+            for (int j = 0; j < 15; ++j) code += u >= T[j];
+        }
+        codes[i / 2] |= (uint8_t)(code << (4 * (i & 1)));
+    }
+    *sigma_out = sigma;
+    return ORACLE_OK;
+}
+
+/* x^ = H (sigma * c[code]) / d in fp64 */
+static void wht4_dequant_row_f64(const uint8_t *codes, float sigma, int d, double *out) {
+    float c[16], T[15];
+    wht4_tables(c, T);
+    for (int i = 0; i < d; ++i) {
+        int code = (codes[i / 2] >> (4 * (i & 1))) & 15;
+        out[i] = (double)(sigma * c[code]);
+    }
+    wht_f64(out, d);
+    for (int i = 0; i < d; ++i) out[i] /= d;
+}
+
+static uint8_t *wht4_block(uint8_t *pool, int Hkv, int d, int P, int page, int h) {
+    return pool + ((size_t)page * (size_t)Hkv + (size_t)h) * kvq_oracle_wht4_block_bytes(d, P);
+}
+
+int kvq_oracle_wht4_quantize_append(uint8_t *pool, const uint16_t *k, const uint16_t *v, const int32_t *block_table,
+                                    int max_blocks, const int32_t *start_pos, int B, int n_new, int Hkv, int d, int P,
+                                    int num_pages) {
+    if (Hkv <= 0 || d != 128 || P <= 0 || B < 0 || n_new < 0) return ORACLE_EINVAL;
+    uint8_t codes[64];
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < n_new; ++t) {
+            long pos = (long)start_pos[b] + t;
+            if (pos < 0 || pos / P >= max_blocks) return ORACLE_ERANGE;
+            int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(pos / P)];
+            if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+            int slot = (int)(pos % P);
+            for (int h = 0; h < Hkv; ++h) {
+                size_t src = (((size_t)b * (size_t)n_new + (size_t)t) * (size_t)Hkv + (size_t)h) * (size_t)d;
+                uint8_t *blk = wht4_block(pool, Hkv, d, P, page, h);
+                float sk, sv;
+                kvq_oracle_wht4_quantize_row(k + src, d, codes, &sk);
+                memcpy(blk + (size_t)slot * (size_t)(d / 2), codes, (size_t)d / 2);
+                kvq_oracle_wht4_quantize_row(v + src, d, codes, &sv);
+                memcpy(blk + ((size_t)P + (size_t)slot) * (size_t)(d / 2), codes, (size_t)d / 2);
+                put_f32(blk + (size_t)P * (size_t)d + (size_t)4 * (size_t)slot, sk);
+                put_f32(blk + (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot), sv);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Dequantize positions [start, start+n) of sequence b (fp64 rounded to fp32). */
+int kvq_oracle_wht4_dequantize(const uint8_t *pool, const int32_t *block_table, int max_blocks, int b, int start,
+                               int n, float *out_k, float *out_v, int Hkv, int d, int P, int num_pages) {
+    if (Hkv <= 0 || d != 128 || P <= 0 || start < 0 || n < 0) return ORACLE_EINVAL;
+    double r[128];
+    for (int t = 0; t < n; ++t) {
+        long pos = (long)start + t;
+        if (pos / P >= max_blocks) return ORACLE_ERANGE;
+        int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(pos / P)];
+        if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+        int slot = (int)(pos % P);
+        for (int h = 0; h < Hkv; ++h) {
+            const uint8_t *blk = wht4_block((uint8_t *)pool, Hkv, d, P, page, h);
+            size_t off = ((size_t)t * (size_t)Hkv + (size_t)h) * (size_t)d;
+            wht4_dequant_row_f64(blk + (size_t)slot * (size_t)(d / 2), get_f32(blk + (size_t)P * (size_t)d + (size_t)4 * (size_t)slot), d, r);
+            for (int i = 0; i < d; ++i) out_k[off + i] = (float)r[i];
+            wht4_dequant_row_f64(blk + ((size_t)P + (size_t)slot) * (size_t)(d / 2),
+                                 get_f32(blk + (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot)), d, r);
+            for (int i = 0; i < d; ++i) out_v[off + i] = (float)r[i];
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Decode attention over the rotated 4-bit cache, in fp64 ([M] section 3.2) over the
+ * dequantized rows x^ = H (sigma * c) / d. */
+int kvq_oracle_wht4_decode_attention(const uint8_t *pool, const uint16_t *q, const int32_t *block_table,
+                                     int max_blocks, const int32_t *seq_lens, int B, int Hq, double softmax_scale,
+                                     double *out, int Hkv, int d, int P, int num_pages) {
+    if (Hkv <= 0 || d != 128 || P <= 0 || Hq <= 0 || Hq % Hkv) return ORACLE_EINVAL;
+    int grp = Hq / Hkv;
+    double rk[128], rv[128];
+    for (int b = 0; b < B; ++b) {
+        int len = seq_lens[b];
+        if (len < 0 || (len + P - 1) / P > max_blocks) return ORACLE_ERANGE;
+        for (int hq = 0; hq < Hq; ++hq) {
+            int kvh = hq / grp;
+            const uint16_t *qrow = q + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            double *o = out + ((size_t)b * (size_t)Hq + (size_t)hq) * (size_t)d;
+            for (int i = 0; i < d; ++i) o[i] = 0.0;
+            if (len == 0) continue;
+            double top = -INFINITY, den = 0.0;
+            for (int pass = 0; pass < 2; ++pass) {
+                for (int t = 0; t < len; ++t) {
+                    int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];
+                    if (page < 0 || page >= num_pages) return ORACLE_ERANGE;
+                    const uint8_t *blk = wht4_block((uint8_t *)pool, Hkv, d, P, page, kvh);
+                    int slot = t % P;
+                    wht4_dequant_row_f64(blk + (size_t)slot * (size_t)(d / 2),
+                                         get_f32(blk + (size_t)P * (size_t)d + (size_t)4 * (size_t)slot), d, rk);
+                    double z = 0.0;
+                    for (int i = 0; i < d; ++i) z += kvq_oracle_f16_to_f64(qrow[i]) * rk[i];
+                    z *= softmax_scale;
+                    if (pass == 0) {
+                        if (z > top) top = z;
+                        continue;
+                    }
+                    wht4_dequant_row_f64(blk + ((size_t)P + (size_t)slot) * (size_t)(d / 2),
+                                         get_f32(blk + (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot)), d, rv);
+                    double e = exp(z - top);
+                    den += e;
+                    for (int i = 0; i < d; ++i) o[i] += e * rv[i];
+                }
+            }
+            for (int i = 0; i < d; ++i) o[i] /= den;
+        }
+    }
+    return ORACLE_OK;
+}

@@ -65,6 +65,26 @@ MUTANTS = [
     ("int8_attention_gqa_modulo", "int kh = hq / per;", "int kh = hq % Hkv;"),
     ("last_token_dropped", "for (int t = 0; t < len; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk",
      "for (int t = 0; t < len - 1; ++t) {\n                int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(t / P)];\n                uint8_t *blk"),
+    # the rotated 4-bit codec
+    ("wht_f32_butterfly_sign", "float a = y[i], b = y[i + h];\n                y[i] = a + b;\n                y[i + h] = a - b;",
+     "float a = y[i], b = y[i + h];\n                y[i] = a + b;\n                y[i + h] = b - a;"),
+    ("wht_f64_butterfly_sign", "double a = y[i], b = y[i + h];\n                y[i] = a + b;\n                y[i + h] = a - b;",
+     "double a = y[i], b = y[i + h];\n                y[i] = a + b;\n                y[i + h] = b - a;"),
+    ("wht_stage_skipped", "    for (int h = 1; h < d; h <<= 1)\n        for (int i = 0; i < d; ++i)\n            if ((i & h) == 0) {\n                float a",
+     "    for (int h = 2; h < d; h <<= 1)\n        for (int i = 0; i < d; ++i)\n            if ((i & h) == 0) {\n                float a"),
+    ("wht4_sigma_rms_of_x", "float sigma = sqrtf(s[0]);", "float sigma = sqrtf(s[0] / 128.0f);"),
+    ("wht4_threshold_strict", "for (int j = 0; j < 15; ++j) code += u >= T[j];", "for (int j = 0; j < 15; ++j) code += u > T[j];"),
+    ("wht4_nibbles_swapped", "codes[i / 2] |= (uint8_t)(code << (4 * (i & 1)));", "codes[i / 2] |= (uint8_t)(code << (4 * (1 - (i & 1))));"),
+    ("wht4_no_division_by_d", "    wht_f64(out, d);\n    for (int i = 0; i < d; ++i) out[i] /= d;", "    wht_f64(out, d);"),
+    ("lloyd_threshold_not_midpoint", "for (int j = 1; j < n; ++j) tb[j] = 0.5 * (lv[j - 1] + lv[j]);",
+     "for (int j = 1; j < n; ++j) tb[j] = 0.6 * lv[j - 1] + 0.4 * lv[j];"),
+    ("lloyd_centroid_sign", "double nl = (std_normal_pdf(tb[j]) - std_normal_pdf(tb[j + 1])) / mass;",
+     "double nl = (std_normal_pdf(tb[j + 1]) - std_normal_pdf(tb[j])) / mass;"),
+    ("wht4_attention_v_from_k", "wht4_dequant_row_f64(blk + ((size_t)P + (size_t)slot) * (size_t)(d / 2),\n                                         get_f32(blk + (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot)), d, rv);",
+     "wht4_dequant_row_f64(blk + (size_t)slot * (size_t)(d / 2),\n                                         get_f32(blk + (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot)), d, rv);"),
+    ("wht4_attention_gqa_modulo", "int kvh = hq / grp;", "int kvh = hq % Hkv;"),
+    ("wht4_sigma_slot_of_k_for_v", "put_f32(blk + (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot), sv);",
+     "put_f32(blk + (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot), sk);"),
 ]
 
 

@@ -815,3 +815,200 @@ def test_int8_attention_brute_force_and_exact_case():
     a = oracle.int8_decode_attention(L, pool8, q, bt, np.array(lens, np.int32), 0.01)
     f = oracle.fp16_decode_attention(L, pool16, q, bt, np.array(lens, np.int32), 0.01)
     assert np.array_equal(a, f)
+
+
+# ----------------------------------------------------------------------------
+# The rotated 4-bit codec ("LARQL KV cache engines", engine three codec/turbo-quant:
+# Walsh-Hadamard rotation, Lloyd-Max quantization, per-row cosine about 0.9954 at
+# 4 bits)
+# ----------------------------------------------------------------------------
+
+# J. Max, "Quantizing for minimum distortion", IRE Trans. Information Theory IT-6
+# (1960), table for the normal law: the positive output levels of the minimum mean
+# square error quantizer with 8 and 16 levels (four decimals) and its distortion.
+MAX_1960 = {
+    3: ([0.2451, 0.7560, 1.3440, 2.1520], 0.03455),
+    4: ([0.1284, 0.3881, 0.6568, 0.9424, 1.2562, 1.6180, 2.0690, 2.7326], 0.009497),
+}
+
+
+def _cell_stats(levels, thresholds):
+    """Mass, mean and distortion of N(0,1) per cell, by quadrature (independent of the oracle)."""
+    import scipy.integrate
+    import scipy.stats
+    edges = np.concatenate([[-np.inf], thresholds, [np.inf]])
+    pdf = scipy.stats.norm.pdf
+    mass, mean, dist = [], [], 0.0
+    for j, lv in enumerate(levels):
+        a, b = edges[j], edges[j + 1]
+        m = scipy.integrate.quad(pdf, a, b, epsabs=1e-14, epsrel=1e-13)[0]
+        mu = scipy.integrate.quad(lambda t: t * pdf(t), a, b, epsabs=1e-14, epsrel=1e-13)[0] / m
+        dist += scipy.integrate.quad(lambda t: (t - lv) ** 2 * pdf(t), a, b, epsabs=1e-14, epsrel=1e-13)[0]
+        mass.append(m)
+        mean.append(mu)
+    return np.array(mass), np.array(mean), dist
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_lloyd_max_matches_the_published_table(bits):
+    lv, tb = oracle.lloyd_max_normal(bits)
+    pos, mse = MAX_1960[bits]
+    n = 1 << bits
+    assert np.all(np.diff(lv) > 0)
+    np.testing.assert_allclose(lv[n // 2:], pos, atol=1.5e-4)
+    np.testing.assert_allclose(lv[:n // 2], -np.array(pos[::-1]), atol=1.5e-4)
+    _, _, dist = _cell_stats(lv, tb)
+    assert abs(dist - mse) <= 2e-3 * mse
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_lloyd_max_optimality_conditions(bits):
+    lv, tb = oracle.lloyd_max_normal(bits)
+    # nearest-neighbour condition: thresholds are the midpoints of adjacent levels
+    np.testing.assert_allclose(tb, 0.5 * (lv[:-1] + lv[1:]), rtol=0, atol=1e-15)
+    # centroid condition: every level is the mean of the normal law on its cell
+    _, mean, _ = _cell_stats(lv, tb)
+    np.testing.assert_allclose(lv, mean, rtol=1e-10, atol=1e-12)
+    # symmetric law, antisymmetric quantizer, the middle threshold exactly at 0
+    assert np.array_equal(lv, -lv[::-1]) and tb[len(tb) // 2] == 0.0
+
+
+def test_wht4_tables_are_the_codebook_in_fp32():
+    c, t = oracle.wht4_tables()
+    lv, tb = oracle.lloyd_max_normal(4)
+    assert np.array_equal(c, lv.astype(np.float32)) and np.array_equal(t, tb.astype(np.float32))
+    # every fp64 value lies well inside its fp32 rounding interval, so any implementation
+    # that reaches the fixed point to 1e-12 rounds it to the same fp32 value
+    for arr in (lv, tb[tb != 0]):
+        f = arr.astype(np.float32)
+        up = np.nextafter(f, np.float32(np.inf)).astype(np.float64)
+        dn = np.nextafter(f, np.float32(-np.inf)).astype(np.float64)
+        f = f.astype(np.float64)
+        margin = np.minimum(np.abs(arr - (f + up) / 2), np.abs(arr - (f + dn) / 2)) / np.abs(arr)
+        assert margin.min() > 1e-10
+
+
+def test_wht_is_the_hadamard_matrix():
+    import scipy.linalg
+    H = scipy.linalg.hadamard(128).astype(np.float64)  # Sylvester order
+    rng = np.random.default_rng(201)
+    # integer rows: every partial sum is exact in fp32, so the fast transform equals H x exactly
+    for _ in range(20):
+        x = rng.integers(-1000, 1001, size=128).astype(np.float32)
+        assert np.array_equal(oracle.wht_f32(x).astype(np.float64), H @ x.astype(np.float64))
+    x = rng.standard_normal(128).astype(np.float32)
+    y = oracle.wht_f32(x).astype(np.float64)
+    np.testing.assert_allclose(y, H @ x.astype(np.float64), rtol=0, atol=1e-5 * np.linalg.norm(x))
+    # H H = d I
+    np.testing.assert_allclose(oracle.wht_f32(oracle.wht_f32(x)), 128 * x, rtol=0, atol=1e-4)
+
+
+def test_wht4_worked_example():
+    # x = e_0 + e_1: (Hx)_i = 1 + H[i][1] = 2 (i even) or 0 (i odd); sigma = |x| = sqrt 2, so
+    # u = sqrt 2 = 1.41421 on even i and 0 on odd i.  The thresholds at or below sqrt 2 are the
+    # twelve up to (L_11 + L_12) / 2 = 1.0993 (the next one, (L_12 + L_13) / 2 = 1.4371, is above):
+    # code 12; u = 0 meets the middle threshold 0 itself: code 8.  Bytes: 12 | 8 << 4 = 0x8C.
+    x = np.zeros(128, np.float16)
+    x[:2] = 1.0
+    codes, s = oracle.wht4_quantize_row(x)
+    assert s == np.float32(np.sqrt(np.float32(2.0)))
+    assert np.all(codes == 0x8C)
+    # an all-zero row: sigma 0 and codes 0, which dequantize to zeros
+    codes, s = oracle.wht4_quantize_row(np.zeros(128, np.float16))
+    assert s == 0.0 and not codes.any()
+
+
+def test_wht4_codes_are_nearest_levels():
+    import scipy.linalg
+    H = scipy.linalg.hadamard(128).astype(np.float64)
+    lv, tb = oracle.lloyd_max_normal(4)
+    rng = np.random.default_rng(202)
+    for i in range(100):
+        x = (rng.standard_normal(128) * rng.uniform(0.01, 30)).astype(np.float16)
+        if i % 3 == 0:
+            x[rng.integers(0, 128, 3)] *= 20  # outlier channels
+        codes, s = oracle.wht4_quantize_row(x)
+        xd = x.astype(np.float64)
+        assert abs(s - np.linalg.norm(xd)) <= 2e-6 * np.linalg.norm(xd)
+        nib = np.stack([codes & 15, codes >> 4], axis=1).reshape(-1)  # element 2j in the low nibble
+        u = (H @ xd) / np.linalg.norm(xd)
+        best = np.argmin(np.abs(u[:, None] - lv[None, :]), axis=1)
+        near = np.min(np.abs(u[:, None] - tb[None, :]), axis=1) < 1e-5
+        assert np.array_equal(nib[~near], best[~near])
+
+
+def _wht4_case(seed, lens, Hkv=2, P=16, pages=10):
+    L = oracle.Layout(Hkv, 128, P, 64, 128, pages)
+    n = max(lens)
+    k = W.kv_tensor(seed, (len(lens), n, Hkv, 128), 20.0, W.outlier_channels(Hkv, 128, seed=seed + 1)).numpy()
+    v = W.kv_tensor(seed + 2, (len(lens), n, Hkv, 128)).numpy()
+    perm = np.random.default_rng(seed + 3).permutation(pages).astype(np.int32)
+    mb = (n + P - 1) // P
+    bt = np.full((len(lens), mb), -1, np.int32)
+    used = 0
+    for b, m in enumerate(lens):
+        np_ = (m + P - 1) // P
+        bt[b, :np_] = perm[used:used + np_]
+        used += np_
+    pool = np.zeros(oracle.wht4_pool_bytes(L), np.uint8)
+    for b, m in enumerate(lens):
+        oracle.wht4_quantize_append(L, pool, k[b:b + 1, :m], v[b:b + 1, :m], bt[b:b + 1], np.array([0], np.int32))
+    return L, pool, bt, k, v
+
+
+def test_wht4_layout_and_dequantize():
+    import scipy.linalg
+    H = scipy.linalg.hadamard(128).astype(np.float64)
+    c, _ = oracle.wht4_tables()
+    assert oracle.wht4_block_bytes(128, 16) == 16 * (128 + 8)
+    L, pool, bt, k, v = _wht4_case(211, [20])
+    blocks = pool.reshape(L.num_pages, L.Hkv, -1)
+    dk, dv = oracle.wht4_dequantize(L, pool, bt, 0, 0, 20)
+    for t in range(20):
+        for h in range(2):
+            blk = blocks[bt[0, t // 16], h]
+            s = t % 16
+            ck, sk = oracle.wht4_quantize_row(k[0, t, h])
+            cv, sv = oracle.wht4_quantize_row(v[0, t, h])
+            assert np.array_equal(blk[s * 64:(s + 1) * 64], ck)
+            assert np.array_equal(blk[(16 + s) * 64:(17 + s) * 64], cv)
+            assert blk[2048 + 4 * s:2052 + 4 * s].view(np.float32)[0] == np.float32(sk)
+            assert blk[2112 + 4 * s:2116 + 4 * s].view(np.float32)[0] == np.float32(sv)
+            for codes, sg, got in ((ck, sk, dk[t, h]), (cv, sv, dv[t, h])):
+                nib = np.stack([codes & 15, codes >> 4], axis=1).reshape(-1)
+                ref = H @ (np.float32(sg) * c[nib]).astype(np.float64) / 128
+                np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-7 * max(sg, 1e-30))
+
+
+def test_wht4_round_trip_cosine():
+    # rows of N(0, 1) values: after the rotation the coordinates over the row RMS are close to
+    # N(0, 1), so the per-row cosine is near sqrt(1 - D16), D16 = 0.009497 the Lloyd-Max
+    # distortion (0.99524); the page reports about 0.9954 at 4 bits
+    L, pool, bt, k, v = _wht4_case(212, [1000], Hkv=4, pages=63)
+    dk, dv = oracle.wht4_dequantize(L, pool, bt, 0, 0, 1000)
+    x = v[0, :1000].astype(np.float64)
+    xh = dv.astype(np.float64)
+    cos = (x * xh).sum(-1) / np.linalg.norm(x, axis=-1) / np.linalg.norm(xh, axis=-1)
+    assert 0.9945 <= cos.mean() <= 0.9960, cos.mean()
+    assert cos.min() > 0.985
+    rel_mse = ((x - xh) ** 2).sum() / (x ** 2).sum()
+    assert 0.0085 <= rel_mse <= 0.0105, rel_mse
+
+
+def test_wht4_attention_brute_force_and_exact_case():
+    lens = [37, 5]
+    L, pool, bt, k, v = _wht4_case(213, lens)
+    q = W.kv_tensor(214, (1, 2, 4, 128)).numpy()[0]
+    got = oracle.wht4_decode_attention(L, pool, q, bt, np.array(lens, np.int32), 0.3)
+    for b, n in enumerate(lens):
+        dk, dv = oracle.wht4_dequantize(L, pool, bt, b, 0, n)
+        for hq in range(4):
+            s_ = (dk[:, hq // 2].astype(np.float64) @ q[b, hq].astype(np.float64)) * 0.3
+            ref = scipy.special.softmax(s_) @ dv[:, hq // 2].astype(np.float64)
+            np.testing.assert_allclose(got[b, hq], ref, rtol=2e-6, atol=2e-7)
+    # one position: the output is that position's dequantized V row
+    got1 = oracle.wht4_decode_attention(L, pool, q, bt, np.array([1, 1], np.int32), 5.0)
+    for b in range(2):
+        _, dv = oracle.wht4_dequantize(L, pool, bt, b, 0, 1)
+        for hq in range(4):
+            np.testing.assert_allclose(got1[b, hq], dv[0, hq // 2].astype(np.float64), rtol=1e-6, atol=1e-7)
