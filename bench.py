@@ -284,6 +284,20 @@ def quality_report(dev, tokens: int = 4096, heads: int = 32, d: int = 128) -> di
                          "max_abs_err": float(err.max()), "max_err_over_scale": float(ratio),
                          "mse": float((err ** 2).mean())}
         rep[f"G{G}"] = out
+    # the rotated 4-bit codec (Walsh-Hadamard rotation, Lloyd-Max codebook) on the same rows
+    cfg = kvq.config(heads, d, P, 64, 128, npg)
+    pool = torch.zeros(kvq.kvq_wht4_pool_bytes(cfg), dtype=torch.uint8, device=dev)
+    kvq.kvq_wht4_quantize_append(cfg, pool, k, v, bt, torch.zeros(1, dtype=torch.int32, device=dev))
+    dk = torch.empty((tokens, heads, d), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+    kvq.kvq_wht4_dequantize(cfg, pool, bt, 0, 0, tokens, dk, dv)
+    out = {}
+    for name, x, xh in (("K", k[0].float(), dk), ("V", v[0].float(), dv)):
+        cos = torch.nn.functional.cosine_similarity(x.reshape(-1, d), xh.reshape(-1, d), dim=1)
+        err = (x - xh).abs()
+        out[name] = {"cos_mean": float(cos.mean()), "cos_min": float(cos.min()), "max_abs_err": float(err.max()),
+                     "mse": float((err ** 2).mean()), "rel_mse": float((err ** 2).sum() / (x ** 2).sum())}
+    rep["rotated_4bit"] = out
     rep["rows"] = f"{tokens} tokens x {heads} heads, d={d}, N(0,1) fp16; K with 4 x20 outlier channels per head"
     return rep
 
@@ -336,11 +350,13 @@ def run_kvq(args, world, rank, local):
 
     prefill(caches[0])
     # the comparison's FP16 cache holds the same fp16 history
-    pool16 = pool8 = None
+    pool16 = pool8 = pool4r = None
     if getattr(args, "compare", False):
         pool16 = torch.zeros(kvq.kvq_fp16_pool_bytes(cfg), dtype=torch.uint8, device=dev)
         pool8 = torch.zeros(kvq.kvq_int8_pool_bytes(cfg), dtype=torch.uint8, device=dev)
-        for fn, pl in ((kvq.kvq_fp16_append, pool16), (kvq.kvq_int8_quantize_append, pool8)):
+        pool4r = torch.zeros(kvq.kvq_wht4_pool_bytes(cfg), dtype=torch.uint8, device=dev)
+        for fn, pl in ((kvq.kvq_fp16_append, pool16), (kvq.kvq_int8_quantize_append, pool8),
+                       (kvq.kvq_wht4_quantize_append, pool4r)):
             if same_ctx:
                 fn(cfg, pl, hist[0][0], hist[0][1], caches[0].block_table, zero)
             else:
@@ -369,6 +385,7 @@ def run_kvq(args, world, rank, local):
     if pool16 is not None:  # the new token, as the INT4 step appends it
         kvq.kvq_fp16_append(cfg, pool16, k_new, v_new, caches[0].block_table, pos)
         kvq.kvq_int8_quantize_append(cfg, pool8, k_new, v_new, caches[0].block_table, pos)
+        kvq.kvq_wht4_quantize_append(cfg, pool4r, k_new, v_new, caches[0].block_table, pos)
     del k_all, v_all, hist
     torch.cuda.empty_cache()
     seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
@@ -503,6 +520,14 @@ def run_kvq(args, world, rank, local):
         def int8_attend():
             kvq.kvq_int8_decode_attention(cfg16, pool8, q, bt0, seq_lens, wl.max_len, scale, out16, ws8, stream=stream)
 
+        ws4r = torch.zeros(kvq.kvq_wht4_decode_workspace_bytes(cfg16, wl.B, wl.Hq, wl.max_len), dtype=torch.uint8,
+                           device=dev)
+
+        def wht4_attend():
+            kvq.kvq_wht4_decode_attention(cfg16, pool4r, q, bt0, seq_lens, wl.max_len, scale, out16, ws4r,
+                                          stream=stream)
+
+        t4r = per_call(wht4_attend)
         t8 = per_call(int8_attend)
         t16 = per_call(fp16_attend)
         tdq = per_call(deq_then_attend)
@@ -517,13 +542,16 @@ def run_kvq(args, world, rank, local):
             "mixed_int4_fp16_last128_us": tmx * 1e6,
             "int8_per_row_us": t8 * 1e6,
             "int8_bytes": (2 * wl.d + 8) * sum(wl.seq_lens) * wl.Hkv,
+            "rotated_4bit_us": t4r * 1e6,
+            "rotated_4bit_bytes": (wl.d + 8) * sum(wl.seq_lens) * wl.Hkv,
             "fp16_bytes": fp16_bytes, "int4_bytes": wl.decode_bytes(),
             "fused_speedup_vs_fp16": t16 / decode_s, "fused_speedup_vs_dequant_then_attend": tdq / decode_s,
         }
         if rank == 0:
             print(f"[compare] fp16 {t16 * 1e6:.1f} us ({fp16_bytes / t16 / 1e9:.0f} GB/s), dequant+attend "
                   f"{tdq * 1e6:.1f} us, int4 fused {decode_s * 1e6:.1f} us, mixed (last {R} fp16) {tmx * 1e6:.1f} us, "
-                  f"int8 {t8 * 1e6:.1f} us ({(2 * wl.d + 8) * sum(wl.seq_lens) * wl.Hkv / t8 / 1e9:.0f} GB/s)",
+                  f"int8 {t8 * 1e6:.1f} us ({(2 * wl.d + 8) * sum(wl.seq_lens) * wl.Hkv / t8 / 1e9:.0f} GB/s), "
+                  f"rotated 4-bit {t4r * 1e6:.1f} us ({(wl.d + 8) * sum(wl.seq_lens) * wl.Hkv / t4r / 1e9:.0f} GB/s)",
                   file=sys.stderr)
     # the step leaves the output of the last decode step in `out` for e2e and checks
     flags = max(c.flags() for c in caches)

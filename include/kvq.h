@@ -262,6 +262,50 @@ int kvq_int8_decode_attention(const kvq_cache_config *cfg, const void *pool8, co
                               float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * Rotated 4-bit cache ("LARQL KV cache engines", engine three codec/turbo-quant: each K
+ * or V row of a head is rotated by a Walsh-Hadamard transform and quantized with a
+ * Lloyd-Max codebook; head_dim a power of two; approximate, per-row cosine about 0.9954
+ * at 4 bits).  The page names the two steps only; this library reads them as:
+ *   y = H x (x the fp16 row as fp32, H the unnormalised Sylvester-order Walsh-Hadamard
+ *   matrix, fast transform with stages of span 1, 2, .., 64), sigma = sqrt(sum x_i^2)
+ *   (the RMS of y; squares summed as (x0^2+x1^2)+(x2^2+x3^2) over elements 4l..4l+3,
+ *   then across l by pairs at xor distances 16, 8, 4, 2, 1), code_i = the number of
+ *   thresholds T_j <= y_i / sigma, T the fp32 midpoints of the 16 Lloyd-Max levels of
+ *   the standard normal (sigma = 0: codes 0); every fp32 operation rounds once.
+ *   A row dequantizes to H (sigma * c_code) / 128, c the fp32 levels.
+ * Same pages, block table and cfg as the INT4 cache (group sizes unused; head_dim 128):
+ * block (page, kv head) at (page * Hkv + h) * P * (d + 8) bytes holds K codes P x d/2
+ * (element 2j in the low nibble of byte j), V codes P x d/2, K sigma P fp32, V sigma P
+ * fp32.
+ * kvq_wht4_codebook: writes the 16 fp32 levels (ascending) and the 15 fp32 thresholds to
+ *   host memory (either pointer may be NULL); host only, computed once.
+ * kvq_wht4_pool_bytes: num_pages * Hkv * P * (d + 8); 0 if cfg is invalid.
+ * kvq_wht4_quantize_append: as kvq_quantize_append, into this pool.
+ * kvq_wht4_dequantize: positions [start, start + n) of sequence b to fp32 out_k and
+ *   out_v [n, Hkv, 128] (device, 16-byte aligned); unmapped pages give zero rows and set
+ *   KVQ_FLAG_BAD_PAGE in *status (may be NULL).
+ * kvq_wht4_decode_workspace_bytes / kvq_wht4_decode_attention: as the INT4 calls of the
+ *   same names over this pool (head_dim 128, up to 8 query heads per kv head).  The
+ *   scores and the weighted sum are formed in the rotated domain (q is rotated once per
+ *   segment); each partial output is rotated back before the combine.
+ * Return codes as for the INT4 calls.
+ */
+void kvq_wht4_codebook(float *levels16, float *thresholds15);
+size_t kvq_wht4_pool_bytes(const kvq_cache_config *cfg);
+int kvq_wht4_quantize_append(const kvq_cache_config *cfg, void *pool4r, const void *k, const void *v,
+                             const int32_t *block_table, int32_t max_blocks, const int32_t *start_pos,
+                             int32_t batch, int32_t n_new, uint32_t *status, kvq_stream_t stream);
+int kvq_wht4_dequantize(const kvq_cache_config *cfg, const void *pool4r, const int32_t *block_table,
+                        int32_t max_blocks, int32_t b, int32_t start, int32_t n, float *out_k, float *out_v,
+                        uint32_t *status, kvq_stream_t stream);
+size_t kvq_wht4_decode_workspace_bytes(const kvq_cache_config *cfg, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_len);
+int kvq_wht4_decode_attention(const kvq_cache_config *cfg, const void *pool4r, const void *q,
+                              const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                              int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                              float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
  * Mixed-precision decode attention (section 8.3 of the INT4 state-machine page: quantize
  * the KV of old tokens to INT4 first, keep recent tokens in FP16).  For sequence b of
  * L = seq_lens[b] positions, positions [0, L - residual) are read from the INT4 pool

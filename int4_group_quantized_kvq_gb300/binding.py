@@ -24,7 +24,9 @@ ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_
                "kvq_decode_step_window", "kvq_fp16_pool_bytes", "kvq_fp16_append", "kvq_dequantize_to_fp16_pool",
                "kvq_fp16_decode_workspace_bytes", "kvq_fp16_decode_attention", "kvq_mixed_decode_workspace_bytes",
                "kvq_mixed_decode_attention", "kvq_int8_pool_bytes", "kvq_int8_quantize_append",
-               "kvq_int8_decode_workspace_bytes", "kvq_int8_decode_attention")
+               "kvq_int8_decode_workspace_bytes", "kvq_int8_decode_attention", "kvq_wht4_codebook",
+               "kvq_wht4_pool_bytes", "kvq_wht4_quantize_append", "kvq_wht4_dequantize",
+               "kvq_wht4_decode_workspace_bytes", "kvq_wht4_decode_attention")
 
 
 class KvqError(RuntimeError):
@@ -100,6 +102,18 @@ def lib() -> C.CDLL:
         L.kvq_int8_decode_workspace_bytes.restype = SZ
         L.kvq_int8_decode_attention.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
         L.kvq_int8_decode_attention.restype = C.c_int
+        L.kvq_wht4_codebook.argtypes = [P, P]
+        L.kvq_wht4_codebook.restype = None
+        L.kvq_wht4_pool_bytes.argtypes = [cfgp]
+        L.kvq_wht4_pool_bytes.restype = SZ
+        L.kvq_wht4_quantize_append.argtypes = [cfgp, P, P, P, P, I32, P, I32, I32, P, P]
+        L.kvq_wht4_quantize_append.restype = C.c_int
+        L.kvq_wht4_dequantize.argtypes = [cfgp, P, P, I32, I32, I32, I32, P, P, P, P]
+        L.kvq_wht4_dequantize.restype = C.c_int
+        L.kvq_wht4_decode_workspace_bytes.argtypes = [cfgp, I32, I32, I32]
+        L.kvq_wht4_decode_workspace_bytes.restype = SZ
+        L.kvq_wht4_decode_attention.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
+        L.kvq_wht4_decode_attention.restype = C.c_int
         L.kvq_dequantize.argtypes = [cfgp, P, P, I32, I32, I32, I32, P, P, I32, P, P]
         L.kvq_dequantize.restype = C.c_int
         L.kvq_read_status.argtypes = [P, C.POINTER(C.c_uint32), P]
@@ -406,6 +420,67 @@ def kvq_int8_decode_attention(cfg: CacheConfig, pool8: torch.Tensor, q: torch.Te
     B, Hq = int(q.shape[0]), int(q.shape[1])
     rc = lib().kvq_int8_decode_attention(
         C.byref(cfg), _dev(pool8, "pool8", torch.uint8), _dev(q, "q", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
+        _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(rc)
+
+
+# ---------------------------------------------------------------------------
+# The rotated 4-bit cache ("LARQL KV cache engines", engine three: Walsh-Hadamard
+# rotation and a Lloyd-Max codebook; layout and arithmetic in include/kvq.h)
+# ---------------------------------------------------------------------------
+def kvq_wht4_codebook() -> tuple[list[float], list[float]]:
+    """The library's fp32 codebook: 16 levels (ascending) and the 15 thresholds between them."""
+    lv = (C.c_float * 16)()
+    tb = (C.c_float * 15)()
+    lib().kvq_wht4_codebook(C.cast(lv, C.c_void_p), C.cast(tb, C.c_void_p))
+    return list(lv), list(tb)
+
+
+def kvq_wht4_pool_bytes(cfg: CacheConfig) -> int:
+    return int(lib().kvq_wht4_pool_bytes(C.byref(cfg)))
+
+
+def kvq_wht4_quantize_append(cfg: CacheConfig, pool: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                             block_table: torch.Tensor, start_pos: torch.Tensor, status: torch.Tensor | None = None,
+                             stream=None) -> None:
+    """Quantize fp16 rows k, v [B, n_new, Hkv, 128] into the rotated 4-bit pool at start_pos[b] + t."""
+    B, n = int(k.shape[0]), int(k.shape[1])
+    rc = lib().kvq_wht4_quantize_append(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(k, "k", torch.float16), _dev(v, "v", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(start_pos, "start_pos", torch.int32), B, n, None if status is None else _dev(status, "status"),
+        _stream(stream))
+    _check(rc)
+
+
+def kvq_wht4_dequantize(cfg: CacheConfig, pool: torch.Tensor, block_table: torch.Tensor, b: int, start: int, n: int,
+                        out_k: torch.Tensor, out_v: torch.Tensor, status: torch.Tensor | None = None,
+                        stream=None) -> None:
+    """Positions [start, start + n) of sequence b to fp32 out_k, out_v [n, Hkv, 128]."""
+    rc = lib().kvq_wht4_dequantize(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(block_table, "block_table", torch.int32),
+        int(block_table.shape[1]), int(b), int(start), int(n), _dev(out_k, "out_k", torch.float32),
+        _dev(out_v, "out_v", torch.float32), None if status is None else _dev(status, "status"), _stream(stream))
+    _check(rc)
+
+
+def kvq_wht4_decode_workspace_bytes(cfg: CacheConfig, batch: int, num_q_heads: int, max_len: int) -> int:
+    n = int(lib().kvq_wht4_decode_workspace_bytes(C.byref(cfg), batch, num_q_heads, max_len))
+    if n == 0:
+        raise KvqError(KVQ_EINVAL, kvq_last_error())
+    return n
+
+
+def kvq_wht4_decode_attention(cfg: CacheConfig, pool: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
+                              seq_lens: torch.Tensor, max_len: int, softmax_scale: float, out: torch.Tensor,
+                              workspace: torch.Tensor, stream=None) -> None:
+    """Decode attention over the rotated 4-bit cache; arguments as kvq_decode_attention."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_wht4_decode_attention(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(q, "q", torch.float16),
         _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
         _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
         _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),

@@ -19,6 +19,14 @@
 //    or (lane >> 2) (T = 8) in every lane;
 //  * the online softmax runs per query head on those lanes; each weight is then
 //    broadcast by a shuffle to the V accumulation.
+//
+// The same kernel serves the INT8 per-row cache and the rotated 4-bit cache (codec 1 and
+// 2): only the row reader differs, and for the rotated codec ("LARQL KV cache engines",
+// engine three; wht_codec.cu) the arithmetic runs in the rotated domain.  A row there is
+// x^ = H (sigma c) / d with H symmetric, so q . x^ = (H q / d) . (sigma c): each segment's
+// q is rotated once (and divided by d), the rows are read as sigma * c_code, and the
+// accumulated output sum_t p_t sigma_t c_t is rotated back (H / d) when the warp writes
+// its partial; the combine is linear and never sees the rotated domain.
 #pragma once
 
 #include "decode_impl.cuh"
@@ -26,14 +34,49 @@
 namespace kvq {
 namespace decode {
 
+// Parameters of the CUDA-core kernel: the split-KV kernel's, and the rotated codec's
+// codebook levels.
+struct FParams {
+    KParams p;
+    float lut[16];
+};
+
+// fp32 Walsh-Hadamard transform of a 128-vector held 4 per lane (lane l: elements 4l ..
+// 4l + 3): stages of span 1 and 2 inside the lane, then 4 .. 64 across lanes at xor
+// distances 1 .. 16, the lower element of each pair becoming a + b and the upper a - b.
+__device__ __forceinline__ void wht128_lane4(float (&y)[4], int lane) {
+    const float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
+    y[0] = t0 + t2;
+    y[2] = t0 - t2;
+    y[1] = t1 + t3;
+    y[3] = t1 - t3;
+#pragma unroll
+    for (int X = 1; X < 32; X <<= 1) {
+        const bool upper = (lane & X) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, y[j], X);
+            y[j] = upper ? other - y[j] : y[j] + other;
+        }
+    }
+}
+
 // One row of a staged block: this lane's 4 values (dimensions 4l .. 4l + 3) of row `row`
-// of K (is_v 0) or V (is_v 1).  FP16 blocks: K rows then V rows, P x D fp16 each.  INT8
-// blocks (the per-row codec of "AI inference tuning: KV Cache optimisation and memory
-// management" section 3.1): K codes P x D int8, V codes P x D int8, K scales P fp32, V
-// scales P fp32; a value is the fp32 product code * scale.
-template <bool I8, int D>
-__device__ __forceinline__ void block_row4(const uint8_t* blk, int P, int is_v, int row, int lane, float (&x)[4]) {
-    if constexpr (I8) {
+// of K (is_v 0) or V (is_v 1).  CODEC 0, FP16 blocks: K rows then V rows, P x D fp16
+// each.  CODEC 1, INT8 blocks (the per-row codec of "AI inference tuning: KV Cache
+// optimisation and memory management" section 3.1): K codes P x D int8, V codes P x D
+// int8, K scales P fp32, V scales P fp32; a value is the fp32 product code * scale.
+// CODEC 2, rotated 4-bit blocks: K codes P x D/2 (nibbles, element 2j low), V codes,
+// K sigma P fp32, V sigma P fp32; a value is sigma * lut[code], in the rotated domain.
+template <int CODEC, int D>
+__device__ __forceinline__ void block_row4(const uint8_t* blk, int P, int is_v, int row, int lane, float (&x)[4],
+                                           const float* lut) {
+    if constexpr (CODEC == 2) {
+        const uint32_t w = *reinterpret_cast<const uint16_t*>(blk + (is_v * P + row) * (D / 2) + 2 * lane);
+        const float s = *reinterpret_cast<const float*>(blk + P * D + 4 * (is_v * P + row));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = s * lut[(w >> (4 * j)) & 15u];
+    } else if constexpr (CODEC == 1) {
         // code c (int8) -> c + 128 in the low mantissa byte of 2^23: the float 2^23 + 128 + c,
         // minus 2^23 + 128, is c exactly (one byte permute and one add per value)
         const uint32_t w = *reinterpret_cast<const uint32_t*>(blk + (is_v * P + row) * D + 4 * lane) ^ 0x80808080u;
@@ -53,11 +96,12 @@ __device__ __forceinline__ void block_row4(const uint8_t* blk, int P, int is_v, 
 }
 
 // R: query heads per kv head, rounded up to 1, 2, 4 or 8.  WIN: the sequences list only
-// their window and sink pages (p.window > 0), as in decode_splitkv_kernel.  I8: INT8
-// per-row blocks instead of FP16 ones.
-template <int D, int R, bool WIN, bool I8 = false>
-__global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
+// their window and sink pages (p.window > 0), as in decode_splitkv_kernel.  CODEC: 0 FP16,
+// 1 INT8 per-row, 2 rotated 4-bit blocks.
+template <int D, int R, bool WIN, int CODEC = 0>
+__global__ void __launch_bounds__(128, 1) decode_fp16_kernel(const __grid_constant__ FParams f) {
     static_assert(D == 128, "four dimensions per lane");
+    const KParams& p = f.p;
     constexpr int kWarps = 4;
     constexpr int T = R == 8 ? 8 : 16;   // tokens per step
     constexpr int LG_T = R == 8 ? 3 : 4;
@@ -80,9 +124,11 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
     int32_t* aps = lens + p.B;
     const uint32_t qbar0 = smem_u32(&ctl->qbar[0]);
     const uint32_t qfree0 = smem_u32(&ctl->qfree[0]);
+    float* lut = reinterpret_cast<float*>(ctl->pad);  // the rotated codec's levels (64 of its 96 bytes)
 
     // read-only inputs only until griddepcontrol.wait (seq_lens, block table, q)
     if (warp == 0) page_prefix(p, pre, lens, aps, lane);
+    if (CODEC == 2 && threadIdx.x < 16) lut[threadIdx.x] = f.lut[threadIdx.x];
     if (threadIdx.x == 0) {
         mbar_init(qbar0, 1);
         mbar_init(qbar0 + 8, 1);
@@ -221,6 +267,15 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
                 qv[s][2] = f1.x * p.scale_log2;
                 qv[s][3] = f1.y * p.scale_log2;
             }
+            if constexpr (CODEC == 2) {
+                // scores against the rotated rows: (H q / d) . (sigma c)
+#pragma unroll
+                for (int s = 0; s < R; ++s) {
+                    wht128_lane4(qv[s], lane);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) qv[s][j] *= 1.0f / D;
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(qfree0 + 8 * (segk & 1));
@@ -249,7 +304,7 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
 #pragma unroll
                     for (int t = 0; t < T; ++t) {
                         float kx[4];
-                        block_row4<I8, D>(blk, p.P, 0, t0 + t, lane, kx);
+                        block_row4<CODEC, D>(blk, p.P, 0, t0 + t, lane, kx, lut);
                         const float2 k0 = make_float2(kx[0], kx[1]);
                         const float2 k1 = make_float2(kx[2], kx[3]);
 #pragma unroll
@@ -302,7 +357,7 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
 #pragma unroll
                     for (int t = 0; t < T; ++t) {
                         float vx[4];
-                        block_row4<I8, D>(blk, p.P, 1, t0 + t, lane, vx);
+                        block_row4<CODEC, D>(blk, p.P, 1, t0 + t, lane, vx, lut);
                         const float2 v0 = make_float2(vx[0], vx[1]);
                         const float2 v1 = make_float2(vx[2], vx[3]);
 #pragma unroll
@@ -335,6 +390,12 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(KParams p) {
             const bool mine = cnt > 0 && !failed;
 #pragma unroll
             for (int s = 0; s < R; ++s) {
+                if constexpr (CODEC == 2) {
+                    // back from the rotated domain: H o / d
+                    wht128_lane4(o[s], lane);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) o[s][j] *= 1.0f / D;
+                }
                 if (s < p.ns) {
                     if (lane == 0)
                         *reinterpret_cast<float2*>(p.ws_ml + (piece * p.ns + s) * 2) =

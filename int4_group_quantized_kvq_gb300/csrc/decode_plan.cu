@@ -60,6 +60,7 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     // the FP16 cache's unit is one page of one kv head: K and V rows, P x d fp16 each
     // (the INT8 cache's: K and V codes P x d each, then 2 P fp32 scales)
     const size_t unit = !a.fp16 ? static_cast<size_t>(a.L.bytes) * plan->hk
+                        : a.wht  ? static_cast<size_t>(a.L.P) * (a.L.d + 8)
                         : a.int8 ? static_cast<size_t>(2) * a.L.P * a.L.d + static_cast<size_t>(8) * a.L.P
                                  : static_cast<size_t>(4) * a.L.P * a.L.d;
     // a warp stages its partial (4 slots x d floats) in a unit buffer

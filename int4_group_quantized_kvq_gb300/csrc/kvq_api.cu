@@ -109,7 +109,8 @@ int kvq_quantize_append(const kvq_cache_config* cfg, void* pool, const void* k, 
 }
 
 namespace {
-// codec: 0 the INT4 cache, 1 the FP16 cache, 2 the INT8 per-row cache
+// codec: 0 the INT4 cache, 1 the FP16 cache, 2 the INT8 per-row cache, 3 the rotated
+// 4-bit cache
 size_t workspace_bytes_impl(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads, int32_t max_len,
                             int codec) {
     if (check_cfg(cfg) != KVQ_OK) return 0;
@@ -124,6 +125,7 @@ size_t workspace_bytes_impl(const kvq_cache_config* cfg, int32_t batch, int32_t 
     a.max_len = max_len;
     a.fp16 = codec != 0;
     a.int8 = codec == 2;
+    a.wht = codec == 3;
     a.L = kvq::block_layout(*cfg);
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
@@ -150,6 +152,11 @@ size_t kvq_fp16_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batc
 size_t kvq_int8_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
                                        int32_t max_len) {
     return workspace_bytes_impl(cfg, batch, num_q_heads, max_len, 2);
+}
+
+size_t kvq_wht4_decode_workspace_bytes(const kvq_cache_config* cfg, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_len) {
+    return workspace_bytes_impl(cfg, batch, num_q_heads, max_len, 3);
 }
 
 namespace {
@@ -192,6 +199,7 @@ int decode_attention_impl(const kvq_cache_config* cfg, const void* pool, const v
     a.sinks = sinks;
     a.fp16 = codec != 0;
     a.int8 = codec == 2;
+    a.wht = codec == 3;
     a.L = kvq::block_layout(*cfg);
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
@@ -294,6 +302,14 @@ int kvq_int8_decode_attention(const kvq_cache_config* cfg, const void* pool8, co
                                  softmax_scale, 0, 0, out, workspace, workspace_bytes, stream, 2);
 }
 
+int kvq_wht4_decode_attention(const kvq_cache_config* cfg, const void* pool4r, const void* q,
+                              const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                              int32_t num_q_heads, int32_t max_len, float softmax_scale, float* out, void* workspace,
+                              size_t workspace_bytes, kvq_stream_t stream) {
+    return decode_attention_impl(cfg, pool4r, q, block_table, max_blocks, seq_lens, batch, num_q_heads, max_len,
+                                 softmax_scale, 0, 0, out, workspace, workspace_bytes, stream, 3);
+}
+
 int kvq_decode_step(const kvq_cache_config* cfg, void* pool, const void* k_new, const void* v_new,
                     const int32_t* append_pos, const void* q, const int32_t* block_table, int32_t max_blocks,
                     const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
@@ -353,11 +369,23 @@ size_t kvq_int8_pool_bytes(const kvq_cache_config* cfg) {
            (2u * cfg->page_size * cfg->head_dim + 8u * cfg->page_size);
 }
 
+size_t kvq_wht4_pool_bytes(const kvq_cache_config* cfg) {
+    if (check_cfg(cfg) != KVQ_OK) return 0;
+    return static_cast<size_t>(cfg->num_pages) * cfg->num_kv_heads * cfg->page_size * (cfg->head_dim + 8u);
+}
+
+void kvq_wht4_codebook(float* levels16, float* thresholds15) {
+    const kvq::Wht4Codebook& cb = kvq::wht4_codebook();
+    for (int j = 0; j < 16 && levels16; ++j) levels16[j] = cb.levels[j];
+    for (int j = 0; j < 15 && thresholds15; ++j) thresholds15[j] = cb.thresholds[j];
+}
+
 namespace {
-// rows into the FP16 cache unchanged, or quantized into the INT8 per-row cache
+// rows into the FP16 cache unchanged (codec 1), or quantized into the INT8 per-row cache
+// (codec 2) or the rotated 4-bit cache (codec 3)
 int rows_append_impl(const kvq_cache_config* cfg, void* pool16, const void* k, const void* v,
                     const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
-                    int32_t n_new, uint32_t* status, kvq_stream_t stream, bool int8) {
+                    int32_t n_new, uint32_t* status, kvq_stream_t stream, int codec) {
     if (int e = check_cfg(cfg)) return e;
     if (batch < 0 || n_new < 0) return fail(KVQ_EINVAL, "batch %d / n_new %d negative", batch, n_new);
     if (batch == 0 || n_new == 0) return ok();
@@ -381,11 +409,17 @@ int rows_append_impl(const kvq_cache_config* cfg, void* pool16, const void* k, c
     a.d = cfg->head_dim;
     a.P = cfg->page_size;
     a.num_pages = cfg->num_pages;
-    if (int8 && (cfg->head_dim % 4 || cfg->head_dim > 256))
+    if (codec == 2 && (cfg->head_dim % 4 || cfg->head_dim > 256))
         return fail(KVQ_EUNSUPPORTED, "the INT8 cache needs head_dim a multiple of 4, at most 256");
-    cudaError_t e = int8 ? kvq::launch_int8_quantize_append(a, reinterpret_cast<cudaStream_t>(stream))
-                         : kvq::launch_fp16_append(a, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, int8 ? "kvq_int8_quantize_append launch" : "kvq_fp16_append launch");
+    if (codec == 3 && cfg->head_dim != 128) return fail(KVQ_EUNSUPPORTED, "the rotated 4-bit cache needs head_dim 128");
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = codec == 3   ? kvq::launch_wht4_quantize_append(a, st)
+                    : codec == 2 ? kvq::launch_int8_quantize_append(a, st)
+                                 : kvq::launch_fp16_append(a, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, codec == 3   ? "kvq_wht4_quantize_append launch"
+                            : codec == 2 ? "kvq_int8_quantize_append launch"
+                                         : "kvq_fp16_append launch");
     return ok();
 }
 
@@ -394,15 +428,39 @@ int rows_append_impl(const kvq_cache_config* cfg, void* pool16, const void* k, c
 int kvq_fp16_append(const kvq_cache_config* cfg, void* pool16, const void* k, const void* v,
                     const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
                     int32_t n_new, uint32_t* status, kvq_stream_t stream) {
-    return rows_append_impl(cfg, pool16, k, v, block_table, max_blocks, start_pos, batch, n_new, status, stream,
-                            false);
+    return rows_append_impl(cfg, pool16, k, v, block_table, max_blocks, start_pos, batch, n_new, status, stream, 1);
 }
 
 int kvq_int8_quantize_append(const kvq_cache_config* cfg, void* pool8, const void* k, const void* v,
                              const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
                              int32_t n_new, uint32_t* status, kvq_stream_t stream) {
-    return rows_append_impl(cfg, pool8, k, v, block_table, max_blocks, start_pos, batch, n_new, status, stream,
-                            true);
+    return rows_append_impl(cfg, pool8, k, v, block_table, max_blocks, start_pos, batch, n_new, status, stream, 2);
+}
+
+int kvq_wht4_quantize_append(const kvq_cache_config* cfg, void* pool4r, const void* k, const void* v,
+                             const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
+                             int32_t n_new, uint32_t* status, kvq_stream_t stream) {
+    return rows_append_impl(cfg, pool4r, k, v, block_table, max_blocks, start_pos, batch, n_new, status, stream, 3);
+}
+
+int kvq_wht4_dequantize(const kvq_cache_config* cfg, const void* pool4r, const int32_t* block_table,
+                        int32_t max_blocks, int32_t b, int32_t start, int32_t n, float* out_k, float* out_v,
+                        uint32_t* status, kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (cfg->head_dim != 128) return fail(KVQ_EUNSUPPORTED, "the rotated 4-bit cache needs head_dim 128");
+    if (b < 0 || start < 0 || n < 0) return fail(KVQ_EINVAL, "b %d, start %d, n %d", b, start, n);
+    if (n == 0) return ok();
+    if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
+    if (!pool4r || !block_table || !out_k || !out_v) return fail(KVQ_EINVAL, "NULL device pointer");
+    if (!aligned(pool4r, 16) || !aligned(out_k, 16) || !aligned(out_v, 16))
+        return fail(KVQ_EINVAL, "pool, out_k and out_v must be 16-byte aligned");
+    if (!aligned(block_table, 4) || (status && !aligned(status, 4)))
+        return fail(KVQ_EINVAL, "int32/uint32 arguments must be 4-byte aligned");
+    cudaError_t e = kvq::launch_wht4_dequantize(static_cast<const uint8_t*>(pool4r), block_table, max_blocks, b, start,
+                                                n, out_k, out_v, status, cfg->num_kv_heads, cfg->page_size,
+                                                cfg->num_pages, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_wht4_dequantize launch");
+    return ok();
 }
 
 int kvq_dequantize_to_fp16_pool(const kvq_cache_config* cfg, const void* pool, void* pool16,

@@ -113,9 +113,11 @@ struct DecodeArgs {
     int32_t window = 0;
     int32_t sinks = 0;
     // attention over the FP16 cache instead of the INT4 one (the comparison's baseline), or
-    // (with int8 also set) over the INT8 per-row cache; both take the CUDA-core kernel
+    // (with int8 or wht also set) over the INT8 per-row cache or the rotated 4-bit cache;
+    // all three take the CUDA-core kernel
     bool fp16 = false;
     bool int8 = false;
+    bool wht = false;
     // attend seq_lens[b] - len_sub positions (the INT4 part of the mixed-precision decode)
     int32_t len_sub = 0;
     // status word (nullptr: the first word of the workspace)
@@ -146,6 +148,20 @@ cudaError_t launch_fp16_append(const Fp16AppendArgs& a, cudaStream_t stream);
 // INT8 per-row cache: quantize-append, arguments as for the FP16 append
 cudaError_t launch_int8_quantize_append(const Fp16AppendArgs& a, cudaStream_t stream);
 cudaError_t launch_dequantize_to_fp16(const Fp16DequantArgs& a, long long max_pages, cudaStream_t stream);
+
+// The rotated 4-bit codec (wht_codec.cu): its fp32 codebook (the 16 Lloyd-Max levels of
+// the standard normal, ascending, and the 15 midpoints between them), computed once;
+// quantize-append with the FP16 append's arguments (pool16 the codec's pool, d = 128);
+// dequantization of positions [start, start + n) of sequence b to fp32 [n, Hkv, 128].
+struct Wht4Codebook {
+    float levels[16];
+    float thresholds[15];
+};
+const Wht4Codebook& wht4_codebook();
+cudaError_t launch_wht4_quantize_append(const Fp16AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_wht4_dequantize(const uint8_t* pool, const int32_t* block_table, int32_t max_blocks, int32_t b,
+                                   int32_t start, int32_t n, float* out_k, float* out_v, uint32_t* status,
+                                   int32_t Hkv, int32_t P, int32_t num_pages, cudaStream_t stream);
 
 // Returns cudaErrorInvalidValue for a geometry no kernel instance covers.
 cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan);

@@ -99,3 +99,14 @@ def test_null_and_misaligned_pointers_rejected_on_host(built):
 def test_version_string(built):
     import int4_group_quantized_kvq_gb300 as kvq
     assert "sm_103a" in kvq.kvq_version()
+
+
+def test_wht4_codebook_is_the_oracles():
+    # host code only: the library computes the rotated codec's Lloyd-Max codebook with its
+    # own routine; its fp32 levels and thresholds must equal the oracle's bit for bit
+    import numpy as np
+    import oracle
+    import int4_group_quantized_kvq_gb300 as kvq
+    lv, tb = kvq.kvq_wht4_codebook()
+    c, t = oracle.wht4_tables()
+    assert np.array_equal(np.array(lv, np.float32), c) and np.array_equal(np.array(tb, np.float32), t)
