@@ -555,12 +555,7 @@ def run_kvq(args, world, rank, local):
                   file=sys.stderr)
     # the step leaves the output of the last decode step in `out` for e2e and checks
     flags = max(c.flags() for c in caches)
-    if world > 1:
-        t = torch.tensor([t_local], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
-    else:
-        t_max = t_local
+    t_max = max_over_ranks(t_local, world, dev)
     step_s = t_max / K
 
     # ---- end to end through the public API from pinned host buffers ----
@@ -581,11 +576,7 @@ def run_kvq(args, world, rank, local):
         for i in range(n_e2e):
             caches[i % n_pools].decode_step_host(st, pos, seq_lens, stream=stream)
         stream.synchronize()
-        t_e2e = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
         h2d = st.host.numel() * 2
         d2h = st.out_host.numel() * 4
         e2e = {"value": world * n_e2e * step_bytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -656,6 +647,17 @@ def run_kvq(args, world, rank, local):
         res["cpu_baseline"] = time_oracle(wl, args.cpu_seconds)
         res["cpu_baseline"].pop("seconds_per_step", None)
     return res
+
+
+def max_over_ranks(seconds: float, world: int, device) -> float:
+    """The slowest rank's time: every rank contributes its own, all receive the maximum."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def run_reference(args, world, rank):

@@ -181,6 +181,26 @@ int kvq_decode_step(const kvq_cache_config *cfg, void *pool, const void *k_new, 
                     kvq_stream_t stream);
 
 /*
+ * kvq_decode_step from host memory, in one call: one host-to-device copy of the step's
+ * inputs, the step, one device-to-host copy of its output, all queued on `stream`
+ * (nothing waits; read host_out after the stream has passed the call).
+ *   host_in   host memory (pinned for an asynchronous copy) holding q [batch,
+ *             num_q_heads, head_dim] fp16, then k_new [batch, num_kv_heads, head_dim]
+ *             fp16, then v_new (same shape), back to back.
+ *   dev_in    device buffer of the same size, 16-byte aligned: the inputs' device copy,
+ *             from which the step reads q, k_new and v_new.
+ *   out       device fp32 [batch, num_q_heads, head_dim], as in kvq_decode_step.
+ *   host_out  host memory (pinned) of the same size: receives out.
+ *   other arguments as in kvq_decode_step.
+ * Returns as kvq_decode_step.
+ */
+int kvq_decode_step_host(const kvq_cache_config *cfg, void *pool, const void *host_in, void *dev_in,
+                         const int32_t *append_pos, const int32_t *block_table, int32_t max_blocks,
+                         const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len,
+                         float softmax_scale, float *out, void *host_out, void *workspace, size_t workspace_bytes,
+                         kvq_stream_t stream);
+
+/*
  * Decode attention and the decode step with a sliding window and sink tokens
  * (SlidingWindowAttention, section 3.2 of the KV-cache optimisation page): the query,
  * at the last position L - 1 of its sequence, attends to positions

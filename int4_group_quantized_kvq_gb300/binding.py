@@ -26,7 +26,7 @@ ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_
                "kvq_mixed_decode_attention", "kvq_int8_pool_bytes", "kvq_int8_quantize_append",
                "kvq_int8_decode_workspace_bytes", "kvq_int8_decode_attention", "kvq_wht4_codebook",
                "kvq_wht4_pool_bytes", "kvq_wht4_quantize_append", "kvq_wht4_dequantize",
-               "kvq_wht4_decode_workspace_bytes", "kvq_wht4_decode_attention")
+               "kvq_wht4_decode_workspace_bytes", "kvq_wht4_decode_attention", "kvq_decode_step_host")
 
 
 class KvqError(RuntimeError):
@@ -102,6 +102,8 @@ def lib() -> C.CDLL:
         L.kvq_int8_decode_workspace_bytes.restype = SZ
         L.kvq_int8_decode_attention.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
         L.kvq_int8_decode_attention.restype = C.c_int
+        L.kvq_decode_step_host.argtypes = [cfgp, P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, P, SZ, P]
+        L.kvq_decode_step_host.restype = C.c_int
         L.kvq_wht4_codebook.argtypes = [P, P]
         L.kvq_wht4_codebook.restype = None
         L.kvq_wht4_pool_bytes.argtypes = [cfgp]
@@ -485,4 +487,25 @@ def kvq_wht4_decode_attention(cfg: CacheConfig, pool: torch.Tensor, q: torch.Ten
         _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
         _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
         _stream(stream))
+    _check(rc)
+
+
+def kvq_decode_step_host(cfg: CacheConfig, pool: torch.Tensor, host_in: torch.Tensor, dev_in: torch.Tensor,
+                         append_pos: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor, batch: int,
+                         num_q_heads: int, max_len: int, softmax_scale: float, out: torch.Tensor,
+                         host_out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """The decode step from host memory in one call: host_in (pinned fp16 q, k_new, v_new back to back)
+    is copied to dev_in, the step runs, out is copied to host_out (pinned fp32)."""
+    if host_in.is_cuda or host_out.is_cuda:
+        raise ValueError("host_in and host_out must be host tensors")
+    if host_in.dtype != torch.float16 or host_out.dtype != torch.float32:
+        raise ValueError("host_in must be float16 and host_out float32")
+    if host_in.numel() != dev_in.numel() or host_out.numel() != out.numel():
+        raise ValueError("host and device buffers differ in size")
+    rc = lib().kvq_decode_step_host(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), host_in.data_ptr(), _dev(dev_in, "dev_in", torch.float16),
+        _dev(append_pos, "append_pos", torch.int32), _dev(block_table, "block_table", torch.int32),
+        int(block_table.shape[1]), _dev(seq_lens, "seq_lens", torch.int32), int(batch), int(num_q_heads),
+        int(max_len), float(softmax_scale), _dev(out, "out", torch.float32), host_out.data_ptr(),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(rc)

@@ -78,8 +78,13 @@ class PagedKVCache:
     def decode_step_host(self, staging: "HostStaging", append_pos, seq_lens, stream=None) -> None:
         """The decode step from pinned host memory: one H2D copy of the step's q, K and V (staged
         back to back), the step (the decode and combine launches), one D2H copy of the output.
-        All asynchronous on the step's stream."""
+        All asynchronous on the step's stream; without a window, one kvq_decode_step_host call."""
         s = torch.cuda.current_stream() if stream is None else stream
+        if self.window == 0:
+            B.kvq_decode_step_host(self.cfg, self.pool, staging.host, staging.dev, append_pos, self.block_table,
+                                   seq_lens, self.batch, self.num_q_heads, self.max_len, self.softmax_scale,
+                                   staging.out, staging.out_host, self.workspace, stream=s)
+            return
         with torch.cuda.stream(s):
             staging.dev.copy_(staging.host, non_blocking=True)
             self.decode_step(staging.q, staging.k_new, staging.v_new, append_pos, seq_lens, staging.out, stream=s)

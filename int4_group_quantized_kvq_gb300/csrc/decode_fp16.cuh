@@ -68,14 +68,15 @@ __device__ __forceinline__ void wht128_lane4(float (&y)[4], int lane) {
 // int8, K scales P fp32, V scales P fp32; a value is the fp32 product code * scale.
 // CODEC 2, rotated 4-bit blocks: K codes P x D/2 (nibbles, element 2j low), V codes,
 // K sigma P fp32, V sigma P fp32; a value is sigma * lut[code], in the rotated domain.
+// The reader returns lut[code] only: the row's sigma (row_sigma) multiplies the reduced
+// score and the softmax weight instead of every value.
 template <int CODEC, int D>
 __device__ __forceinline__ void block_row4(const uint8_t* blk, int P, int is_v, int row, int lane, float (&x)[4],
                                            const float* lut) {
     if constexpr (CODEC == 2) {
         const uint32_t w = *reinterpret_cast<const uint16_t*>(blk + (is_v * P + row) * (D / 2) + 2 * lane);
-        const float s = *reinterpret_cast<const float*>(blk + P * D + 4 * (is_v * P + row));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) x[j] = s * lut[(w >> (4 * j)) & 15u];
+        for (int j = 0; j < 4; ++j) x[j] = lut[(w >> (4 * j)) & 15u];
     } else if constexpr (CODEC == 1) {
         // code c (int8) -> c + 128 in the low mantissa byte of 2^23: the float 2^23 + 128 + c,
         // minus 2^23 + 128, is c exactly (one byte permute and one add per value)
@@ -93,6 +94,12 @@ __device__ __forceinline__ void block_row4(const uint8_t* blk, int P, int is_v, 
         x[2] = b.x;
         x[3] = b.y;
     }
+}
+
+// sigma of row `row` of K (is_v 0) or V (is_v 1) in a rotated 4-bit block
+template <int D>
+__device__ __forceinline__ float row_sigma(const uint8_t* blk, int P, int is_v, int row) {
+    return *reinterpret_cast<const float*>(blk + P * D + 4 * (is_v * P + row));
 }
 
 // R: query heads per kv head, rounded up to 1, 2, 4 or 8.  WIN: the sequences list only
@@ -299,6 +306,18 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(const __grid_consta
                     // a step wholly outside the window and the sinks is skipped, so every
                     // processed step holds an attended token
                     if (WIN && !(min(tpos + T, Leff) > wlo || tpos < p.sinks)) continue;
+                    // the attended tokens of the step (bit t); the others' V rows are skipped, since
+                    // slots past a sequence's end may hold any bit pattern, which a zero weight
+                    // would not cancel (0 * inf)
+                    uint32_t vmask = 0xffffffffu;
+                    if (!(tpos + T <= Leff && (!WIN || tpos >= wlo || tpos + T <= p.sinks))) {
+                        vmask = 0u;
+#pragma unroll
+                        for (int t = 0; t < T; ++t) {
+                            const int tt2 = tpos + t;
+                            if (tt2 < Leff && (!WIN || tt2 >= wlo || tt2 < p.sinks)) vmask |= 1u << t;
+                        }
+                    }
                     // partial dot products of this lane's 4 dimensions, T tokens, R heads
                     float a[R][T];
 #pragma unroll
@@ -331,6 +350,11 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(const __grid_consta
                     }
                     // online softmax per head on the token this lane holds
                     const int tau = lane >> TSH;
+                    if constexpr (CODEC == 2) {
+                        const float sk = row_sigma<D>(blk, p.P, 0, t0 + tau);
+#pragma unroll
+                        for (int s = 0; s < R; ++s) a[s][0] *= sk;
+                    }
                     const int tt = tpos + tau;
                     const bool valid = tt < Leff && (!WIN || tt >= wlo || tt < p.sinks);
                     float pw[R];
@@ -353,22 +377,37 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(const __grid_consta
                         o[s][2] *= alpha;
                         o[s][3] *= alpha;
                     }
-                    // o += sum_tau p_tau v_tau
+                    // o += sum_tau p_tau v_tau; a step with unattended tokens skips their rows
+                    // (MASKED), every other step runs without a test per token
+                    auto accumulate = [&](auto masked) {
+                        constexpr bool MASKED = decltype(masked)::value;
 #pragma unroll
-                    for (int t = 0; t < T; ++t) {
-                        float vx[4];
-                        block_row4<CODEC, D>(blk, p.P, 1, t0 + t, lane, vx, lut);
-                        const float2 v0 = make_float2(vx[0], vx[1]);
-                        const float2 v1 = make_float2(vx[2], vx[3]);
+                        for (int t = 0; t < T; ++t) {
+                            if (MASKED && !((vmask >> t) & 1u)) continue;
+                            float vx[4];
+                            block_row4<CODEC, D>(blk, p.P, 1, t0 + t, lane, vx, lut);
+                            // the rotated codec's row sigma goes into the weight (up to 4 query
+                            // heads per kv head) or into the values
+                            const float sv = CODEC == 2 ? row_sigma<D>(blk, p.P, 1, t0 + t) : 1.f;
+                            if (CODEC == 2 && R > 4) {
 #pragma unroll
-                        for (int s = 0; s < R; ++s) {
-                            const float pt = __shfl_sync(0xffffffffu, pw[s], t << TSH);
-                            o[s][0] = fmaf(pt, v0.x, o[s][0]);
-                            o[s][1] = fmaf(pt, v0.y, o[s][1]);
-                            o[s][2] = fmaf(pt, v1.x, o[s][2]);
-                            o[s][3] = fmaf(pt, v1.y, o[s][3]);
+                                for (int j = 0; j < 4; ++j) vx[j] *= sv;
+                            }
+                            const float2 v0 = make_float2(vx[0], vx[1]);
+                            const float2 v1 = make_float2(vx[2], vx[3]);
+#pragma unroll
+                            for (int s = 0; s < R; ++s) {
+                                float pt = __shfl_sync(0xffffffffu, pw[s], t << TSH);
+                                if (CODEC == 2 && R <= 4) pt *= sv;
+                                o[s][0] = fmaf(pt, v0.x, o[s][0]);
+                                o[s][1] = fmaf(pt, v0.y, o[s][1]);
+                                o[s][2] = fmaf(pt, v1.x, o[s][2]);
+                                o[s][3] = fmaf(pt, v1.y, o[s][3]);
+                            }
                         }
-                    }
+                    };
+                    if (vmask == 0xffffffffu) accumulate(std::false_type{});
+                    else accumulate(std::true_type{});
                 }
                 __syncwarp();
                 if (lane == 0) fence_proxy_async_smem();

@@ -318,6 +318,33 @@ int kvq_decode_step(const kvq_cache_config* cfg, void* pool, const void* k_new, 
                             num_q_heads, max_len, softmax_scale, 0, 0, out, workspace, workspace_bytes, stream);
 }
 
+int kvq_decode_step_host(const kvq_cache_config* cfg, void* pool, const void* host_in, void* dev_in,
+                         const int32_t* append_pos, const int32_t* block_table, int32_t max_blocks,
+                         const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len,
+                         float softmax_scale, float* out, void* host_out, void* workspace, size_t workspace_bytes,
+                         kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || num_q_heads < 1) return fail(KVQ_EINVAL, "batch %d, num_q_heads %d", batch, num_q_heads);
+    if (batch == 0) return ok();
+    if (!host_in || !dev_in || !host_out || !out) return fail(KVQ_EINVAL, "NULL buffer");
+    if (!aligned(dev_in, 16)) return fail(KVQ_EINVAL, "dev_in must be 16-byte aligned");
+    const size_t d = static_cast<size_t>(cfg->head_dim);
+    const size_t q_bytes = static_cast<size_t>(batch) * num_q_heads * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(batch) * cfg->num_kv_heads * d * 2;
+    const size_t out_bytes = static_cast<size_t>(batch) * num_q_heads * d * 4;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* din = static_cast<uint8_t*>(dev_in);
+    cudaError_t e = cudaMemcpyAsync(din, host_in, q_bytes + 2 * kv_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step_host input copy");
+    if (int rc = decode_step_impl(cfg, pool, din + q_bytes, din + q_bytes + kv_bytes, append_pos, din, block_table,
+                                  max_blocks, seq_lens, batch, num_q_heads, max_len, softmax_scale, 0, 0, out,
+                                  workspace, workspace_bytes, stream))
+        return rc;
+    e = cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step_host output copy");
+    return ok();
+}
+
 int kvq_decode_step_window(const kvq_cache_config* cfg, void* pool, const void* k_new, const void* v_new,
                            const int32_t* append_pos, const void* q, const int32_t* block_table, int32_t max_blocks,
                            const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len,
