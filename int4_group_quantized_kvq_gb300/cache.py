@@ -78,13 +78,8 @@ class PagedKVCache:
     def decode_step_host(self, staging: "HostStaging", append_pos, seq_lens, stream=None) -> None:
         """The decode step from pinned host memory: one H2D copy of the step's q, K and V (staged
         back to back), the step (the decode and combine launches), one D2H copy of the output.
-        All asynchronous on the step's stream; without a window, one kvq_decode_step_host call."""
+        All asynchronous on the step's stream.  (kvq_decode_step_host does the same in one C call.)"""
         s = torch.cuda.current_stream() if stream is None else stream
-        if self.window == 0:
-            B.kvq_decode_step_host(self.cfg, self.pool, staging.host, staging.dev, append_pos, self.block_table,
-                                   seq_lens, self.batch, self.num_q_heads, self.max_len, self.softmax_scale,
-                                   staging.out, staging.out_host, self.workspace, stream=s)
-            return
         with torch.cuda.stream(s):
             staging.dev.copy_(staging.host, non_blocking=True)
             self.decode_step(staging.q, staging.k_new, staging.v_new, append_pos, seq_lens, staging.out, stream=s)
@@ -116,3 +111,66 @@ class HostStaging:
         self.v_new = self.dev[nq + nk:].view(shk)
         self.out = torch.empty(shq, dtype=torch.float32, device=device)
         self.out_host = torch.empty(shq, dtype=torch.float32).pin_memory()
+
+
+class HostPipeline:
+    """Decode steps fed from pinned host memory with the copies overlapped with the kernels.
+
+    Two staging slots alternate.  Step i (slot i % 2) copies its inputs host-to-device on an
+    input copy stream, runs on the compute stream once that copy is done, and copies its
+    output device-to-host on an output copy stream once the step is done; so step i + 1's
+    inputs move while step i computes, and step i's output moves while step i + 1 computes.
+    Events keep each slot's device buffers from being overwritten while in use: a slot's
+    input copy waits for the step two back to have read that slot, and its step waits for
+    that step's output copy to have left the slot.  The host side is the caller's: fill
+    `slot(i)`'s host inputs before `step(i)` (for i >= 2, after `inputs_copied(i - 2)`),
+    and read its `out_host` after `done(i)` and before `step(i + 2)`."""
+
+    def __init__(self, cache: PagedKVCache, compute_stream=None):
+        self.cache = cache
+        dev = cache.device
+        self.slots = [HostStaging(cache.batch, cache.num_q_heads, cache.cfg.num_kv_heads, cache.cfg.head_dim, dev)
+                      for _ in range(2)]
+        self.compute = torch.cuda.Stream(device=dev) if compute_stream is None else compute_stream
+        self.copy_in = torch.cuda.Stream(device=dev)
+        self.copy_out = torch.cuda.Stream(device=dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_step = [torch.cuda.Event() for _ in range(2)]
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]
+        self.started = [False, False]
+
+    def slot(self, i: int) -> HostStaging:
+        return self.slots[i % 2]
+
+    def step(self, i: int, append_pos: torch.Tensor, seq_lens: torch.Tensor, cache: PagedKVCache | None = None) -> None:
+        """Step i on `cache` (default: the pipeline's), from slot(i)'s host inputs to its out_host."""
+        cache = self.cache if cache is None else cache
+        k = i % 2
+        st = self.slots[k]
+        if self.started[k]:
+            self.copy_in.wait_event(self.ev_step[k])   # step i - 2 has read this slot's inputs
+        with torch.cuda.stream(self.copy_in):
+            st.dev.copy_(st.host, non_blocking=True)
+            self.ev_in[k].record(self.copy_in)
+        self.compute.wait_event(self.ev_in[k])
+        if self.started[k]:
+            self.compute.wait_event(self.ev_out[k])   # step i - 2's output has left this slot
+        cache.decode_step(st.q, st.k_new, st.v_new, append_pos, seq_lens, st.out, stream=self.compute)
+        self.ev_step[k].record(self.compute)
+        self.copy_out.wait_event(self.ev_step[k])
+        with torch.cuda.stream(self.copy_out):
+            st.out_host.copy_(st.out, non_blocking=True)
+            self.ev_out[k].record(self.copy_out)
+        self.started[k] = True
+
+    def inputs_copied(self, i: int) -> torch.cuda.Event:
+        """The event after which step i's host inputs have been read (slot(i) may be refilled)."""
+        return self.ev_in[i % 2]
+
+    def done(self, i: int) -> torch.cuda.Event:
+        """The event after which step i's output is in slot(i).out_host (until step i + 2 is issued)."""
+        return self.ev_out[i % 2]
+
+    def synchronize(self) -> None:
+        for s in (self.copy_in, self.compute, self.copy_out):
+            s.synchronize()

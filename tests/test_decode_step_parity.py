@@ -196,3 +196,51 @@ def test_step_from_host_staging_matches_device_step(kvq):
     assert torch.equal(c1.pool, c2.pool)
     assert torch.equal(out1.cpu(), st.out_host)
     assert c1.flags() == 0 and c2.flags() == 0
+
+
+def test_host_pipeline_matches_sequential_steps(kvq):
+    """HostPipeline (double-buffered staging, copies on their own streams) gives every step's
+    output and the final pool bit for bit as the same steps run one after another on the
+    device; each step writes new rows into the same positions, so the order matters."""
+    from int4_group_quantized_kvq_gb300.cache import HostPipeline, PagedKVCache
+    case = Case(3, 16, 4, 128, [90, 33, 200], seed=37)
+    append_pos = [n - 1 for n in case.lens]
+    pool, _, _ = _setup(case, append_pos, 0x00)
+    cfg = case.cfg(kvq)
+    ap = torch.tensor(append_pos, dtype=torch.int32, device="cuda")
+    sl = torch.tensor(case.lens, dtype=torch.int32, device="cuda")
+    ref = PagedKVCache(cfg, case.block_table, case.Hq, max(case.lens), device="cuda",
+                       pool=torch.from_numpy(pool.copy()).cuda())
+    pc = PagedKVCache(cfg, case.block_table, case.Hq, max(case.lens), device="cuda",
+                      pool=torch.from_numpy(pool.copy()).cuda())
+    pipe = HostPipeline(pc)
+    n_steps = 7
+    g = torch.Generator().manual_seed(38)
+    ins = [(torch.randn(case.B, case.Hq, case.d, generator=g).half(),
+            torch.randn(case.B, case.Hkv, case.d, generator=g).half(),
+            torch.randn(case.B, case.Hkv, case.d, generator=g).half()) for _ in range(n_steps)]
+    want = []
+    for q, kn, vn in ins:
+        out = torch.empty((case.B, case.Hq, case.d), dtype=torch.float32, device="cuda")
+        ref.decode_step(q.cuda(), kn.cuda(), vn.cuda(), ap, sl, out)
+        want.append(out.cpu())
+    got = [None] * n_steps
+    for i, (q, kn, vn) in enumerate(ins):
+        if i >= 2:
+            pipe.done(i - 2).synchronize()
+            got[i - 2] = pipe.slot(i - 2).out_host.clone()
+            pipe.inputs_copied(i - 2).synchronize()
+        st = pipe.slot(i)
+        st.q_host.copy_(q)
+        st.k_host.copy_(kn)
+        st.v_host.copy_(vn)
+        pipe.step(i, ap, sl)
+    for i in (n_steps - 2, n_steps - 1):
+        pipe.done(i).synchronize()
+        got[i] = pipe.slot(i).out_host.clone()
+    pipe.synchronize()
+    torch.cuda.synchronize()
+    for i in range(n_steps):
+        assert torch.equal(got[i], want[i]), f"step {i}"
+    assert torch.equal(ref.pool, pc.pool)
+    assert ref.flags() == 0 and pc.flags() == 0
