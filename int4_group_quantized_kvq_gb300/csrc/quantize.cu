@@ -18,15 +18,79 @@
 namespace kvq {
 namespace {
 
-// Quantize one row job (a K or V row of one (sequence, token, kv head)) held as 8
+// The 16 values a lane holds (row values 16 tl .. 16 tl + 15, inside one group) as 16
+// nibbles (code + 8, element 2j low), low word first, and the group's fp16 scale.  The
+// codes are those of quant_lane8 (kvq_quant.cuh, which the decode step's fused append
+// uses), computed with fewer instructions for the common case:
+//  * y = x * rcp(s) plus 1.5 * 2^23 + 8 rounds y + 8 to an integer, ties to even (8 is
+//    even), whose low four bits are the nibble whenever the code needs no clamp;
+//  * a lane takes the slower path of quant_lane8's arithmetic (the exact half-integer
+//    check and the clamp) for all its values when one of them lies within 2^-10 of a
+//    half-integer or the group's largest |y| exceeds 7.49;
+//  * a NaN input or an infinite scale takes the IEEE division, as in quant_lane8.
+// LPR lanes hold a row; a group spans 1 << lg16 lanes.
+template <int LPR>
+__device__ __forceinline__ uint2 quant_lane16(const uint4 (&raw)[2], int lg16, __half& scale_out) {
+    float x[16];
+    uint32_t nanbits = 0;  // bit 15 or 31 set: a NaN half ((h & 0x7fff) > 0x7c00)
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint4 r4 = raw[w >> 2];
+        const uint32_t word = (w & 3) == 0 ? r4.x : (w & 3) == 1 ? r4.y : (w & 3) == 2 ? r4.z : r4.w;
+        nanbits |= ((word & 0x7fff7fffu) + 0x03ff03ffu) & 0x80008000u;
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&word));
+        x[2 * w] = f.x;
+        x[2 * w + 1] = f.y;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int off = 1; off < LPR; off <<= 1) {
+        const float other = __shfl_xor_sync(0xffffffffu, amax, off);
+        if (off < (1 << lg16)) amax = fmaxf(amax, other);
+    }
+    __half s16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
+    if ((__half_as_ushort(s16) & 0x7fffu) == 0) s16 = __ushort_as_half(0x3c00u);
+    const float s = __half2float(s16);
+    scale_out = s16;
+    if (nanbits != 0 || isinf(s)) {
+        uint2 out;
+        out.x = quant8(*reinterpret_cast<const float(*)[8]>(&x[0]), s, true);
+        out.y = quant8(*reinterpret_cast<const float(*)[8]>(&x[8]), s, true);
+        return out;
+    }
+    float rs;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rs) : "f"(s));
+    constexpr float kMagic8 = 12582920.0f;  // 1.5 * 2^23 + 8
+    bool slow = amax * rs > 7.49f;
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float y = x[i] * rs;
+        const float m = y + kMagic8;
+        slow |= fabsf(y - (m - kMagic8)) > 0.4990234375f;
+        const uint32_t nib = (__float_as_uint(m) & 0xFu) << (4 * (i & 7));
+        if (i < 8) lo |= nib;
+        else hi |= nib;
+    }
+    if (slow) {
+        lo = quant8(*reinterpret_cast<const float(*)[8]>(&x[0]), s, false);
+        hi = quant8(*reinterpret_cast<const float(*)[8]>(&x[8]), s, false);
+    }
+    return make_uint2(lo, hi);
+}
+
+// Quantize one row job (a K or V row of one (sequence, token, kv head)) held as 16
 // values per lane, and store its codes and scales.  Every lane of the warp calls this
 // together (the group maximum is a shuffle reduction); `active` marks real jobs.
 template <int D>
-__device__ __forceinline__ void quantize_row(const QuantizeArgs& a, uint4 raw, uint32_t job, bool active, int tl) {
+__device__ __forceinline__ void quantize_row(const QuantizeArgs& a, const uint4 (&raw)[2], uint32_t job, bool active,
+                                             int tl) {
     const int is_v = static_cast<int>(job & 1u);
-    const int lg = is_v ? a.lg_lanes_v : a.lg_lanes_k;  // log2 of the lanes per group
+    const int lg = (is_v ? a.lg_lanes_v : a.lg_lanes_k) - 1;  // log2 of the 16-value lanes per group
     __half s16;
-    const uint32_t word = quant_lane8<D / 8>(raw, lg, s16);
+    const uint2 words = quant_lane16<D / 16>(raw, lg, s16);
     if (!active) return;
 
     // destination: row = (b * n_new + t) * Hkv + h -> position, page, slot
@@ -49,27 +113,27 @@ __device__ __forceinline__ void quantize_row(const QuantizeArgs& a, uint4 raw, u
     const int slot = static_cast<int>(pos & ((1 << a.lg_p) - 1));
     uint8_t* blk = a.pool + (static_cast<long long>(page) * a.Hkv + h) * a.L.bytes;
     uint8_t* codes = blk + (is_v ? a.L.v_codes : 0) + slot * (D / 2);
-    reinterpret_cast<uint32_t*>(codes)[tl] = word;
+    reinterpret_cast<uint2*>(codes)[tl] = words;
     if ((tl & ((1 << lg) - 1)) == 0) {
-        const int ngroups = D >> (lg + 3);
+        const int ngroups = D >> (lg + 4);
         uint8_t* scales = blk + (is_v ? a.L.v_scales : a.L.k_scales) + slot * ngroups * 2;
         reinterpret_cast<__half*>(scales)[tl >> lg] = s16;
     }
 }
 
 // Work mapping: jobs are (row, K or V) pairs, K and V of a row adjacent.  A warp takes
-// TEAMS jobs at a time, U times over, loading all U x 16 bytes per lane before it
+// TEAMS jobs at a time, U times over, loading all U x 32 bytes per lane before it
 // computes, so enough loads are in flight to stream from HBM.  The job loop is
 // grid-strided over a grid of one wave of resident CTAs.
 template <int D, int U>
-__global__ void __launch_bounds__(256) quantize_append_kernel(QuantizeArgs a) {
+__global__ void __launch_bounds__(256, 4) quantize_append_kernel(QuantizeArgs a) {
     // A decode launched behind this kernel may start its own set-up now; it waits for this
     // grid to finish before it reads the pool.  This kernel itself may start before the
     // kernel ahead of it (a decode that reads the pool) has finished: it waits for it
     // before anything else.
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    constexpr int LPR = D / 8;            // lanes per row
+    constexpr int LPR = D / 16;           // lanes per row
     constexpr int TEAMS = 32 / LPR;       // row jobs per warp at a time
     const int lane = threadIdx.x & 31;
     const int team = lane / LPR;
@@ -78,14 +142,15 @@ __global__ void __launch_bounds__(256) quantize_append_kernel(QuantizeArgs a) {
     const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const uint32_t warps_total = gridDim.x * blockDim.x / 32;
     for (uint32_t base = warp_global * TEAMS * U; base < jobs; base += warps_total * TEAMS * U) {
-        uint4 raw[U];
+        uint4 raw[U][2];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const uint32_t job = base + u * TEAMS + team;
-            raw[u] = make_uint4(0, 0, 0, 0);
+            raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
             if (job < jobs) {
-                const __half* src = ((job & 1u) ? a.v : a.k) + static_cast<size_t>(job >> 1) * D + tl * 8;
-                raw[u] = __ldcs(reinterpret_cast<const uint4*>(src));  // read once: stream past the caches
+                const __half* src = ((job & 1u) ? a.v : a.k) + static_cast<size_t>(job >> 1) * D + tl * 16;
+                raw[u][0] = __ldcs(reinterpret_cast<const uint4*>(src));  // read once: stream past the caches
+                raw[u][1] = __ldcs(reinterpret_cast<const uint4*>(src) + 1);
             }
         }
 #pragma unroll
@@ -113,11 +178,11 @@ int quantize_ctas_per_sm() {
 
 template <int D>
 cudaError_t launch_q(const QuantizeArgs& a, cudaStream_t stream) {
-    constexpr int U = 4;
+    constexpr int U = 2;
     const long long jobs = 2LL * a.rows;
     if (jobs == 0) return cudaSuccess;
     constexpr int threads = 256;
-    constexpr int jobs_per_block = (threads / 32) * (32 / (D / 8)) * U;
+    constexpr int jobs_per_block = (threads / 32) * (32 / (D / 16)) * U;
     long long blocks = (jobs + jobs_per_block - 1) / jobs_per_block;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
