@@ -25,8 +25,12 @@ namespace {
 //  * y = x * rcp(s) plus 1.5 * 2^23 + 8 rounds y + 8 to an integer, ties to even (8 is
 //    even), whose low four bits are the nibble whenever the code needs no clamp;
 //  * a lane takes the slower path of quant_lane8's arithmetic (the exact half-integer
-//    check and the clamp) for all its values when one of them lies within 2^-10 of a
-//    half-integer or the group's largest |y| exceeds 7.49;
+//    check and the clamp) for all its values when one of them lies within 2^-16 of a
+//    half-integer or the group's largest |y| exceeds 7.49.  The band is safe: y is
+//    within 2^-17.7 of the quotient q for |q| < 16 (kvq_quant.cuh), and q is either a
+//    half-integer or more than 2^-13 from every one, so outside the band y and q round
+//    alike; and it is narrow, so a warp's 512 values rarely send it down the slower path
+//    (a 2^-10 band did for most warps);
 //  * a NaN input or an infinite scale takes the IEEE division, as in quant_lane8.
 // LPR lanes hold a row; a group spans 1 << lg16 lanes.
 template <int LPR>
@@ -69,7 +73,7 @@ __device__ __forceinline__ uint2 quant_lane16(const uint4 (&raw)[2], int lg16, _
     for (int i = 0; i < 16; ++i) {
         const float y = x[i] * rs;
         const float m = y + kMagic8;
-        slow |= fabsf(y - (m - kMagic8)) > 0.4990234375f;
+        slow |= fabsf(y - (m - kMagic8)) > 0.4999847412109375f;  // 1/2 - 2^-16
         const uint32_t nib = (__float_as_uint(m) & 0xFu) << (4 * (i & 7));
         if (i < 8) lo |= nib;
         else hi |= nib;
