@@ -31,17 +31,20 @@ namespace {
 //    half-integer or more than 2^-13 from every one, so outside the band y and q round
 //    alike; and it is narrow, so a warp's 512 values rarely send it down the slower path
 //    (a 2^-10 band did for most warps);
-//  * a NaN input or an infinite scale takes the IEEE division, as in quant_lane8.
+//  * a NaN input makes its |y - round(y)| NaN, and an infinite scale (from an infinite
+//    input) makes that input's y = inf * 0 = NaN, so both reach the slower path through
+//    the same test (written to hold for NaN); there they take the IEEE division, as in
+//    quant_lane8;
+//  * nibbles are paired into bytes by one shift and one bit select, and four bytes
+//    gathered into a word by three byte permutes.
 // LPR lanes hold a row; a group spans 1 << lg16 lanes.
 template <int LPR>
 __device__ __forceinline__ uint2 quant_lane16(const uint4 (&raw)[2], int lg16, __half& scale_out) {
     float x[16];
-    uint32_t nanbits = 0;  // bit 15 or 31 set: a NaN half ((h & 0x7fff) > 0x7c00)
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
         const uint4 r4 = raw[w >> 2];
         const uint32_t word = (w & 3) == 0 ? r4.x : (w & 3) == 1 ? r4.y : (w & 3) == 2 ? r4.z : r4.w;
-        nanbits |= ((word & 0x7fff7fffu) + 0x03ff03ffu) & 0x80008000u;
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&word));
         x[2 * w] = f.x;
         x[2 * w + 1] = f.y;
@@ -58,29 +61,28 @@ __device__ __forceinline__ uint2 quant_lane16(const uint4 (&raw)[2], int lg16, _
     if ((__half_as_ushort(s16) & 0x7fffu) == 0) s16 = __ushort_as_half(0x3c00u);
     const float s = __half2float(s16);
     scale_out = s16;
-    if (nanbits != 0 || isinf(s)) {
-        uint2 out;
-        out.x = quant8(*reinterpret_cast<const float(*)[8]>(&x[0]), s, true);
-        out.y = quant8(*reinterpret_cast<const float(*)[8]>(&x[8]), s, true);
-        return out;
-    }
     float rs;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rs) : "f"(s));
     constexpr float kMagic8 = 12582920.0f;  // 1.5 * 2^23 + 8
+    constexpr float kBand = 0.4999847412109375f;  // 1/2 - 2^-16
     bool slow = amax * rs > 7.49f;
-    uint32_t lo = 0, hi = 0;
+    uint32_t byt[8];  // byte j (low 8 bits): the nibbles of values 2j and 2j + 1
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float y = x[i] * rs;
-        const float m = y + kMagic8;
-        slow |= fabsf(y - (m - kMagic8)) > 0.4999847412109375f;  // 1/2 - 2^-16
-        const uint32_t nib = (__float_as_uint(m) & 0xFu) << (4 * (i & 7));
-        if (i < 8) lo |= nib;
-        else hi |= nib;
+    for (int j = 0; j < 8; ++j) {
+        const float y0 = x[2 * j] * rs, y1 = x[2 * j + 1] * rs;
+        const float m0 = y0 + kMagic8, m1 = y1 + kMagic8;
+        slow |= !(fabsf(y0 - (m0 - kMagic8)) <= kBand);
+        slow |= !(fabsf(y1 - (m1 - kMagic8)) <= kBand);
+        byt[j] = (__float_as_uint(m0) & 0xFu) | ((__float_as_uint(m1) << 4) & ~0xFu);
     }
+    uint32_t lo = prmt(prmt(byt[0], byt[1], 0x0040u), prmt(byt[2], byt[3], 0x0040u), 0x5410u);
+    uint32_t hi = prmt(prmt(byt[4], byt[5], 0x0040u), prmt(byt[6], byt[7], 0x0040u), 0x5410u);
     if (slow) {
-        lo = quant8(*reinterpret_cast<const float(*)[8]>(&x[0]), s, false);
-        hi = quant8(*reinterpret_cast<const float(*)[8]>(&x[8]), s, false);
+        bool plain = isinf(s);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) plain |= x[i] != x[i];
+        lo = quant8(*reinterpret_cast<const float(*)[8]>(&x[0]), s, plain);
+        hi = quant8(*reinterpret_cast<const float(*)[8]>(&x[8]), s, plain);
     }
     return make_uint2(lo, hi);
 }

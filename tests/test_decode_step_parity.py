@@ -244,3 +244,32 @@ def test_host_pipeline_matches_sequential_steps(kvq):
         assert torch.equal(got[i], want[i]), f"step {i}"
     assert torch.equal(ref.pool, pc.pool)
     assert ref.flags() == 0 and pc.flags() == 0
+
+
+def test_nonfinite_rows_pack_alike_in_both_quantizers(kvq):
+    """Rows holding NaN or +-inf (outside what the pages define) still get the same bytes from
+    the quantize-append kernel and from the decode step's fused append: a NaN value codes as 0,
+    the group scale comes from the other values, and an infinite value makes the scale infinite."""
+    case = Case(4, 8, 4, 128, [40, 17, 64, 3], seed=41)
+    append_pos = [n - 1 for n in case.lens]
+    pool, k_new, v_new = _setup(case, append_pos, 0x00)
+    k_new = k_new.copy()
+    v_new = v_new.copy()
+    k_new[0, 0, 5] = np.nan
+    k_new[1, 2, 70:74] = np.nan
+    v_new[2, 1, 3] = np.inf
+    v_new[3, 3, 100] = -np.inf
+    k_new[2, 3, :] = np.nan
+    cfg = case.cfg(kvq)
+    ap = torch.tensor(append_pos, dtype=torch.int32, device="cuda")
+    sl = torch.tensor(case.lens, dtype=torch.int32, device="cuda")
+    bt = case.block_table.cuda()
+    pa = torch.from_numpy(pool.copy()).cuda()
+    pb = torch.from_numpy(pool.copy()).cuda()
+    kn, vn = torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda()
+    kvq.kvq_quantize_append(cfg, pa, kn[:, None], vn[:, None], bt, ap)
+    ws = kvq.new_workspace(cfg, case.B, case.Hq, max(case.lens), device="cuda")
+    out = torch.empty((case.B, case.Hq, case.d), dtype=torch.float32, device="cuda")
+    kvq.kvq_decode_step(cfg, pb, kn, vn, ap, case.q.cuda(), bt, sl, max(case.lens), case.scale, out, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(pa, pb)
