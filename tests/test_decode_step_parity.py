@@ -273,3 +273,34 @@ def test_nonfinite_rows_pack_alike_in_both_quantizers(kvq):
     kvq.kvq_decode_step(cfg, pb, kn, vn, ap, case.q.cuda(), bt, sl, max(case.lens), case.scale, out, ws)
     torch.cuda.synchronize()
     assert torch.equal(pa, pb)
+
+
+def test_decode_step_host_call_matches_device_step(kvq):
+    """kvq_decode_step_host (host-to-device copy, the step, device-to-host copy, one C call) gives
+    the device step's pool and output bit for bit."""
+    from int4_group_quantized_kvq_gb300.cache import HostStaging
+    case = Case(3, 16, 4, 128, [90, 33, 200], seed=43)
+    append_pos = [n - 1 for n in case.lens]
+    pool, k_new, v_new = _setup(case, append_pos, 0x00)
+    cfg = case.cfg(kvq)
+    ap = torch.tensor(append_pos, dtype=torch.int32, device="cuda")
+    sl = torch.tensor(case.lens, dtype=torch.int32, device="cuda")
+    bt = case.block_table.cuda()
+    p1 = torch.from_numpy(pool.copy()).cuda()
+    p2 = torch.from_numpy(pool.copy()).cuda()
+    ml = max(case.lens)
+    out1 = torch.empty((case.B, case.Hq, case.d), dtype=torch.float32, device="cuda")
+    ws1 = kvq.new_workspace(cfg, case.B, case.Hq, ml, device="cuda")
+    kvq.kvq_decode_step(cfg, p1, torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda(), ap, case.q.cuda(), bt,
+                        sl, ml, case.scale, out1, ws1)
+    st = HostStaging(case.B, case.Hq, case.Hkv, case.d, device="cuda")
+    st.q_host.copy_(case.q)
+    st.k_host.copy_(torch.from_numpy(k_new))
+    st.v_host.copy_(torch.from_numpy(v_new))
+    ws2 = kvq.new_workspace(cfg, case.B, case.Hq, ml, device="cuda")
+    kvq.kvq_decode_step_host(cfg, p2, st.host, st.dev, ap, bt, sl, case.B, case.Hq, ml, case.scale, st.out, st.out_host,
+                             ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(p1, p2)
+    assert torch.equal(out1.cpu(), st.out_host)
+    assert kvq.kvq_read_status(ws1) == 0 and kvq.kvq_read_status(ws2) == 0
