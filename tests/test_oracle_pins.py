@@ -105,6 +105,17 @@ def test_fp16_kv_size_figures():
     for seq, gib in [(4096, 2.0), (8192, 4.0), (16384, 8.0), (32768, 16.0)]:
         assert oracle.fp16_kv_bytes(32, 32, 128, seq) / GiB == gib
         assert oracle.fp16_kv_bytes(32, 32, 128, seq) / 4 / GiB == gib / 4
+    # "LARQL KV cache engines", engines one and two: at 4096 positions of a 34-layer model with 4 KV heads of
+    # 256 kept as f32 rows (twice the fp16 bytes: 8 KiB per layer and position), the full cache holds
+    # 34 x 4096 rows and the window engine 29 sliding layers x 1024 rows plus 5 global layers x 4096:
+    # 1.06 GiB against 0.38 GiB
+    row_f32 = 2 * oracle.fp16_kv_bytes(1, 4, 256, 1)
+    assert row_f32 == 8 * 1024
+    full = 34 * 4096 * row_f32
+    window = (29 * 1024 + 5 * 4096) * row_f32
+    assert 34 * 4096 == 139264 and 29 * 1024 + 5 * 4096 == 50176
+    assert full / GiB == 1.0625 and round(window / GiB, 2) == 0.38
+    assert round(1 - window / full, 2) == 0.64  # the page's "-64%"
 
 
 # ----------------------------------------------------------------------------
