@@ -247,6 +247,34 @@ def time_oracle(wl, budget_s: float) -> dict:
             "seconds_per_step": per}
 
 
+def time_oracle_quantize(wl, budget_s: float) -> dict:
+    """The oracle's quantize-append as it stands, single-threaded, on a slice of the workload's history
+    (sequence 0, all KV heads, as many tokens as fit about budget_s seconds), over the bytes the GPU
+    quantize figure counts: fp16 K and V read, packed codes and scales written."""
+    import numpy as np
+    import oracle
+    import workloads as W
+    n_max = wl.seq_lens[0]
+    k = W.kv_tensor(W.SEED_K, (1, n_max, wl.Hkv, wl.d), 20.0, W.outlier_channels(wl.Hkv, wl.d)).numpy()
+    v = W.kv_tensor(W.SEED_V, (1, n_max, wl.Hkv, wl.d)).numpy()
+    npg = (n_max + wl.P - 1) // wl.P
+    L = oracle.Layout(wl.Hkv, wl.d, wl.P, wl.Gk, wl.Gv, npg)
+    pool = np.zeros(L.pool_bytes, np.uint8)
+    bt = np.arange(npg, dtype=np.int32).reshape(1, -1)
+    per_token = wl.Hkv * (2 * wl.d * 2 + wl.packed_bytes_per_token_head())
+    n = min(n_max, 64)
+    t0 = time.perf_counter()
+    oracle.quantize_append(L, pool, k[:, :n], v[:, :n], bt, np.zeros(1, np.int32))
+    per_tok_s = max((time.perf_counter() - t0) / n, 1e-9)
+    n = int(max(16, min(n_max, budget_s / per_tok_s)))
+    t0 = time.perf_counter()
+    oracle.quantize_append(L, pool, k[:, :n], v[:, :n], bt, np.zeros(1, np.int32))
+    t = time.perf_counter() - t0
+    return {"value": n * per_token / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{wl.name}: sequence 0, {n} of {n_max} tokens x {wl.Hkv} KV heads, K and V; "
+                      f"{t * 1e3:.0f} ms"}
+
+
 # ---------------------------------------------------------------------------
 # dequantization quality against the fp16 input
 # ---------------------------------------------------------------------------
@@ -660,6 +688,7 @@ def run_kvq(args, world, rank, local):
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = time_oracle(wl, args.cpu_seconds)
         res["cpu_baseline"].pop("seconds_per_step", None)
+        res["cpu_baseline"]["quantize"] = time_oracle_quantize(wl, 2.0)
     return res
 
 
