@@ -275,6 +275,30 @@ def test_dequantize_roundtrip_exact_on_grid():
         assert np.array_equal(hk, x[0]) and np.array_equal(hv, x[0])
 
 
+
+def test_quantize_store_read_roundtrip_mse_at_g32():
+    # "LLM long-context inference: managing the KV cache with an INT4 state machine", section 7.1: quantize at
+    # group size 32, write, read back, dequantize, and the MSE must stay under a threshold.  Here the write and
+    # the read go through the paged pool; the thresholds are the hard bound (|x - x^| <= s/2 gives MSE <= s^2/4)
+    # and, for Gaussian rows, the uniform rounding-error model s^2/12 to within 10%.
+    L = oracle.Layout(8, 128, 16, 32, 32, 64)
+    n = 1000
+    bt = np.arange(64, dtype=np.int32).reshape(1, -1)
+    for outl in (0.0, 20.0):
+        x = W.kv_tensor(301, (1, n, 8, 128), outl, W.outlier_channels(8, 128, seed=302) if outl else None).numpy()
+        pool = np.zeros(L.pool_bytes, np.uint8)
+        oracle.quantize_append(L, pool, x, x, bt, np.zeros(1, np.int32))
+        dk, dv = oracle.dequantize(L, pool, bt, 0, 0, n)
+        assert np.array_equal(dk, dv)
+        xd = x[0].astype(np.float64)
+        mse = ((dk.astype(np.float64) - xd) ** 2).mean()
+        step = np.abs(dk.astype(np.float64)).reshape(n, 8, 4, 32).max(-1) / 7.0
+        s2 = np.repeat(step ** 2, 32, axis=-1).reshape(n, 8, 128)
+        assert mse <= (s2 / 4).mean()
+        if outl == 0.0:
+            assert 0.9 <= mse / (s2 / 12).mean() <= 1.05
+            assert mse < 0.012  # under 1.2% of the rows' unit power
+
 @pytest.mark.parametrize("Gk,Gv", [(32, 64), (64, 128), (32, 32)])
 def test_dequantize_error_bound_per_group(Gk, Gv):
     """Each element comes back within half its own group's step amax_g / 7 (computed here from
