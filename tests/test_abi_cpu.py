@@ -110,3 +110,46 @@ def test_wht4_codebook_is_the_oracles():
     lv, tb = kvq.kvq_wht4_codebook()
     c, t = oracle.wht4_tables()
     assert np.array_equal(np.array(lv, np.float32), c) and np.array_equal(np.array(tb, np.float32), t)
+
+
+def test_codec_and_host_step_calls_reject_bad_arguments_on_host(built):
+    # the rotated 4-bit, INT8 and host-buffer calls check their arguments before touching the device
+    import int4_group_quantized_kvq_gb300 as kvq
+    L = kvq.lib()
+    cfg = kvq.config(8, 128, 16, 64, 128, 10)
+    cfg64 = kvq.config(8, 64, 16, 32, 64, 10)
+    bad = kvq.config(8, 128, 16, 64, 128, 10)
+    bad.page_size = 24
+    assert L.kvq_wht4_pool_bytes(C.byref(bad)) == 0 and L.kvq_int8_pool_bytes(C.byref(bad)) == 0
+    assert L.kvq_wht4_pool_bytes(C.byref(cfg)) == 10 * 8 * 16 * (128 + 8)
+    # quantize-append: NULL, misaligned, head_dim other than 128, nothing to do
+    assert L.kvq_wht4_quantize_append(C.byref(cfg), None, None, None, None, 4, None, 2, 1, None, None) == kvq.KVQ_EINVAL
+    assert L.kvq_wht4_quantize_append(C.byref(cfg), 0x1008, 0x2000, 0x3000, 0x4000, 4, 0x5000, 2, 1, None,
+                                      None) == kvq.KVQ_EINVAL
+    assert L.kvq_wht4_quantize_append(C.byref(cfg64), 0x1000, 0x2000, 0x3000, 0x4000, 4, 0x5000, 2, 1, None,
+                                      None) == kvq.KVQ_EUNSUPPORTED
+    assert L.kvq_wht4_quantize_append(C.byref(cfg), None, None, None, None, 4, None, 0, 1, None, None) == kvq.KVQ_OK
+    assert L.kvq_int8_quantize_append(C.byref(cfg), None, None, None, None, 4, None, 2, 1, None, None) == kvq.KVQ_EINVAL
+    # dequantize: head_dim, negative sequence, NULL, misaligned output, nothing to do
+    assert L.kvq_wht4_dequantize(C.byref(cfg64), 0x1000, 0x2000, 4, 0, 0, 4, 0x3000, 0x4000, None,
+                                 None) == kvq.KVQ_EUNSUPPORTED
+    assert L.kvq_wht4_dequantize(C.byref(cfg), 0x1000, 0x2000, 4, -1, 0, 4, 0x3000, 0x4000, None,
+                                 None) == kvq.KVQ_EINVAL
+    assert L.kvq_wht4_dequantize(C.byref(cfg), None, 0x2000, 4, 0, 0, 4, 0x3000, 0x4000, None, None) == kvq.KVQ_EINVAL
+    assert L.kvq_wht4_dequantize(C.byref(cfg), 0x1000, 0x2000, 4, 0, 0, 4, 0x3004, 0x4000, None,
+                                 None) == kvq.KVQ_EINVAL
+    assert L.kvq_wht4_dequantize(C.byref(cfg), None, None, 4, 0, 0, 0, None, None, None, None) == kvq.KVQ_OK
+    # decode attention over the codecs: more than 8 query heads per kv head, head_dim 64
+    for fn in (L.kvq_wht4_decode_attention, L.kvq_int8_decode_attention, L.kvq_fp16_decode_attention):
+        assert fn(C.byref(cfg), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 72, 10, 1.0, 0x5000, 0x6000, 1 << 20,
+                  None) == kvq.KVQ_EUNSUPPORTED
+        assert fn(C.byref(cfg64), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 8, 10, 1.0, 0x5000, 0x6000, 1 << 20,
+                  None) == kvq.KVQ_EUNSUPPORTED
+    # the host-buffer step: NULL buffers, a misaligned device copy, nothing to do
+    assert L.kvq_decode_step_host(C.byref(cfg), 0x1000, None, 0x2000, 0x3000, 0x4000, 4, 0x5000, 2, 8, 10, 1.0,
+                                  0x6000, 0x7000, 0x8000, 1 << 20, None) == kvq.KVQ_EINVAL
+    assert L.kvq_decode_step_host(C.byref(cfg), 0x1000, 0x9000, 0x2008, 0x3000, 0x4000, 4, 0x5000, 2, 8, 10, 1.0,
+                                  0x6000, 0x7000, 0x8000, 1 << 20, None) == kvq.KVQ_EINVAL
+    assert "aligned" in kvq.kvq_last_error()
+    assert L.kvq_decode_step_host(C.byref(cfg), None, None, None, None, None, 4, None, 0, 8, 10, 1.0, None, None,
+                                  None, 0, None) == kvq.KVQ_OK
