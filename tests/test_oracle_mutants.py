@@ -85,6 +85,21 @@ MUTANTS = [
     ("wht4_attention_gqa_modulo", "int kvh = hq / grp;", "int kvh = hq % Hkv;"),
     ("wht4_sigma_slot_of_k_for_v", "put_f32(blk + (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot), sv);",
      "put_f32(blk + (size_t)P * (size_t)d + (size_t)4 * ((size_t)P + (size_t)slot), sk);"),
+    ("attention_not_normalized", "o[i] += p * (double)rv[i];\n            }\n            for (int i = 0; i < d; ++i) o[i] /= l;",
+     "o[i] += p * (double)rv[i];\n            }"),
+    ("group_amax_signed",
+     "float a = fabsf(kvq_oracle_f16_to_f32(x[i]));\n        if (a > amax) amax = a;\n    }\n    float s32",
+     "float a = kvq_oracle_f16_to_f32(x[i]);\n        if (a > amax) amax = a;\n    }\n    float s32"),
+    ("int8_amax_signed",
+     "float a = fabsf(kvq_oracle_f16_to_f32(x[i]));\n        if (a > amax) amax = a;\n    }\n    float s = amax / 127.0f;",
+     "float a = kvq_oracle_f16_to_f32(x[i]);\n        if (a > amax) amax = a;\n    }\n    float s = amax / 127.0f;"),
+    ("int8_scale_floor_dropped", "    if (s < 1e-8f) s = 1e-8f;\n", ""),
+    ("dequant_fp16_v_from_k", "((uint16_t *)out_v)[off + i] = kvq_oracle_f32_to_f16(rv[i]);",
+     "((uint16_t *)out_v)[off + i] = kvq_oracle_f32_to_f16(rk[i]);"),
+    ("dequant_fp32_v_from_k", "((float *)out_v)[off + i] = rv[i];", "((float *)out_v)[off + i] = rk[i];"),
+    ("window_zero_hides_all", "if (window <= 0) return 1;", "if (window <= 0) return 0;"),
+    ("mixed_split_from_start", "int split = len - residual > 0 ? len - residual : 0;",
+     "int split = residual < len ? residual : len;"),
 ]
 
 
