@@ -100,6 +100,11 @@ MUTANTS = [
     ("window_zero_hides_all", "if (window <= 0) return 1;", "if (window <= 0) return 0;"),
     ("mixed_split_from_start", "int split = len - residual > 0 ? len - residual : 0;",
      "int split = residual < len ? residual : len;"),
+    ("f16_overflow_saturates", "if (e > 15) return (uint16_t)(sign | 0x7c00u);",
+     "if (e > 15) return (uint16_t)(sign | 0x7bffu);"),
+    ("f16_mantissa_carry_dropped", "if (m16 == 2048) { m16 = 1024; e += 1; }", "if (m16 == 2048) { m16 = 2047; }"),
+    ("f16_to_f64_subnormal_exponent", "v = ldexp((double)fr, -24);", "v = ldexp((double)fr, -25);"),
+    ("f16_nan_to_inf", "(ax > 0x7f800000u ? 0x0200u : 0u)", "0u"),
 ]
 
 

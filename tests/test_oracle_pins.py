@@ -68,6 +68,19 @@ def test_f32_to_f16_midpoints_and_random():
     assert bad.size == 0, f"{bad.size} mismatches, first {allv[bad[:5]]}: {ours[bad[:5]]} vs {ref[bad[:5]]}"
 
 
+def test_f32_to_f16_infinities_and_nans():
+    # IEEE 754 conversion: an infinity stays that infinity and a NaN stays a NaN (all-ones
+    # exponent, nonzero fraction) of the same sign; the NaN payload is not fixed by the
+    # standard, so only NaN-ness and sign are compared with numpy's cast
+    inf = np.array([np.inf, -np.inf, 3.4e38, -3.4e38], dtype=np.float32)
+    with np.errstate(over="ignore"):
+        assert np.array_equal(oracle.f32_to_f16_array(inf), inf.astype(np.float16).view(np.uint16))
+    nan_bits = np.array([0x7FC00000, 0x7F800001, 0x7FFFFFFF, 0xFFC00000, 0xFF800001, 0x7FA00000], dtype=np.uint32)
+    ours = oracle.f32_to_f16_array(nan_bits.view(np.float32))
+    assert np.all((ours & 0x7C00) == 0x7C00) and np.all((ours & 0x03FF) != 0)
+    assert np.array_equal(ours >> 15, (nan_bits >> 31).astype(ours.dtype))
+
+
 # ----------------------------------------------------------------------------
 # sizes
 # ----------------------------------------------------------------------------
