@@ -105,6 +105,17 @@ MUTANTS = [
     ("f16_mantissa_carry_dropped", "if (m16 == 2048) { m16 = 1024; e += 1; }", "if (m16 == 2048) { m16 = 2047; }"),
     ("f16_to_f64_subnormal_exponent", "v = ldexp((double)fr, -24);", "v = ldexp((double)fr, -25);"),
     ("f16_nan_to_inf", "(ax > 0x7f800000u ? 0x0200u : 0u)", "0u"),
+    ("append_token_offset_dropped",
+     "            long pos = (long)start_pos[b] + t;\n            if (pos < 0 || pos / P >= max_blocks) return ORACLE_ERANGE;\n            int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(pos / P)];\n            if (page < 0 || page >= num_pages) return ORACLE_ERANGE;\n            int slot = (int)(pos % P);\n            for (int h = 0; h < Hkv; ++h) {\n                size_t off = (((size_t)b * (size_t)n_new",
+     "            long pos = (long)start_pos[b];\n            if (pos < 0 || pos / P >= max_blocks) return ORACLE_ERANGE;\n            int page = block_table[(size_t)b * (size_t)max_blocks + (size_t)(pos / P)];\n            if (page < 0 || page >= num_pages) return ORACLE_ERANGE;\n            int slot = (int)(pos % P);\n            for (int h = 0; h < Hkv; ++h) {\n                size_t off = (((size_t)b * (size_t)n_new"),
+    ("dequant_start_ignored",
+     "    float rk[256], rv[256];\n    for (int t = 0; t < n; ++t) {\n        long pos = (long)start + t;",
+     "    float rk[256], rv[256];\n    for (int t = 0; t < n; ++t) {\n        long pos = (long)t;"),
+    ("lloyd_single_iteration", "        if (moved <= 1e-15) break;", "        if (moved <= 1e-15 || it >= 1) break;"),
+    ("lloyd_loose_tolerance", "        if (moved <= 1e-15) break;", "        if (moved <= 1e-6) break;"),
+    ("int8_v_scale_for_k", "rk[i] = (float)(int8_t)blk[(size_t)slot * (size_t)d + (size_t)i] * sk;",
+     "rk[i] = (float)(int8_t)blk[(size_t)slot * (size_t)d + (size_t)i] * sv;"),
+    ("lloyd_not_symmetrized", "        lv[j] = -a;\n        lv[n - 1 - j] = a;", "        (void)a;"),
 ]
 
 
