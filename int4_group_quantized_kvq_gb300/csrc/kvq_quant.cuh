@@ -20,8 +20,9 @@ namespace kvq {
 // X, S < 2048), q - (k + 1/2) = (2 X 2^(a-b) - (2k + 1) S) / (2 S), whose numerator is
 // a nonzero multiple of min(1, 2^(a-b)), and 2^(a-b) > S / 4096 whenever |q| >= 1/2.
 // The fp32 quotient the definition rounds is therefore on the same side of every
-// half-integer as q.  y = x * rs, with rs within 2 ulp of 1/s, is within 2^-18 of q for
-// |q| < 16 (the quotient never reaches 16 for finite input: the fp16 scale is at least
+// half-integer as q.  y = x * rs, with rs within 2 ulp of 1/s, is within
+// |q| (2^-22 + 2^-24) < 2^-17.6 of q for |q| < 16 (one reciprocal within 2 ulp, one
+// rounded product; the quotient never reaches 16 for finite input: the fp16 scale is at least
 // two thirds of amax / 7), so rounding y gives the same code unless y is within 2^-10
 // of a half-integer h; there the sign of x - h s, exact in one fma because h s has at
 // most 15 significant bits, decides, with ties to even.

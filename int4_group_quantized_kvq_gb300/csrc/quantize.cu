@@ -27,7 +27,7 @@ namespace {
 //  * a lane takes the slower path of quant_lane8's arithmetic (the exact half-integer
 //    check and the clamp) for all its values when one of them lies within 2^-16 of a
 //    half-integer or the group's largest |y| exceeds 7.49.  The band is safe: y is
-//    within 2^-17.7 of the quotient q for |q| < 16 (kvq_quant.cuh), and q is either a
+//    within 2^-17.6 of the quotient q for |q| < 16 (kvq_quant.cuh), and q is either a
 //    half-integer or more than 2^-13 from every one, so outside the band y and q round
 //    alike; and it is narrow, so a warp's 512 values rarely send it down the slower path
 //    (a 2^-10 band did for most warps);

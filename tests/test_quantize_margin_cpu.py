@@ -1,0 +1,47 @@
+"""The quantize kernel's fast path, checked on its arithmetic premise (no GPU needed).
+
+The kernel rounds y = x * rcp(s) to the nearest integer and sends a value down the
+exact path only when y lies within 2^-16 of a half-integer.  That is safe when the
+exact quotient q = x / s of two fp16 numbers is either a half-integer or more than
+2^-13 from every half-integer: y is within 2^-17.6 of q for |q| < 16 (a reciprocal
+within 2 ulp, relative error at most 2^-22, and one rounded product), so outside the band y and q
+round alike, and a true tie always lands inside the band.  This test checks that
+premise by brute force over every positive fp16 x and every normal fp16 scale s with
+x / s <= 7.5, in exact integer arithmetic.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _fp16_in_units_of_2_pow_minus_24() -> np.ndarray:
+    """Every positive finite fp16 value as an integer multiple of 2^-24 (index = bit pattern)."""
+    h = np.arange(1, 0x7C00, dtype=np.int64)
+    e, f = h >> 10, h & 0x3FF
+    return np.where(e == 0, f, (1024 + f) << np.maximum(e - 1, 0))
+
+
+def test_fp16_quotients_are_ties_or_clear_of_them():
+    X = _fp16_in_units_of_2_pow_minus_24()
+    assert X[-1] == 65504 * 2 ** 24 and X[0] == 1  # largest finite and smallest subnormal
+    normal_S = X[0x400 - 1:]  # bit patterns 0x0400 .. 0x7BFF
+    worst = np.inf
+    ties = 0
+    for c in range(0, normal_S.size, 512):
+        S = normal_S[c:c + 512, None]
+        Xs = X[None, :np.searchsorted(X, 15 * int(S[-1, 0]) // 2, side="right")]
+        ok = 2 * Xs <= 15 * S  # x / s <= 7.5: the range the fast path accepts
+        k = Xs // S
+        r = 2 * Xs - (2 * k + 1) * S  # q - (k + 1/2) = r / (2 S)
+        ties += int(np.count_nonzero(ok & (r == 0)))
+        off = ok & (r != 0)
+        # distance |r| / (2 S) must exceed 2^-13, i.e. 4096 |r| > S
+        assert np.all(4096 * np.abs(r[off]) > np.broadcast_to(S, r.shape)[off])
+        d = np.abs(r[off]) / (2.0 * np.broadcast_to(S, r.shape)[off])
+        if d.size:
+            worst = min(worst, float(d.min()))
+    assert ties > 0  # true ties occur (e.g. x = 2.5 s) and must take the exact path
+    assert worst > 2.0 ** -13
+    # the reciprocal-and-multiply error for |q| < 16 stays inside the gap to the band
+    err = 16 * (2.0 ** -22 + 2.0 ** -24 + 2.0 ** -46)
+    assert err < 2.0 ** -17.6 and err < 2.0 ** -16 and 2.0 ** -13 - err > 2.0 ** -16
