@@ -45,3 +45,17 @@ def test_fp16_quotients_are_ties_or_clear_of_them():
     # the reciprocal-and-multiply error for |q| < 16 stays inside the gap to the band
     err = 16 * (2.0 ** -22 + 2.0 ** -24 + 2.0 ** -46)
     assert err < 2.0 ** -17.6 and err < 2.0 ** -16 and 2.0 ** -13 - err > 2.0 ** -16
+
+
+def test_group_quotients_stay_below_16():
+    # the scale is fp16(fp32(amax) / 7) (1 when that rounds to zero), so for every finite
+    # fp16 amax the largest quotient amax / s of its group stays below 16; it exceeds 7
+    # only by the fp16 rounding of the scale, and only subnormal scales go far past 7.49
+    h = np.arange(1, 0x7C00, dtype=np.uint16)
+    amax = h.view(np.float16).astype(np.float32)
+    s = (amax / np.float32(7.0)).astype(np.float16).astype(np.float64)
+    s[s == 0] = 1.0
+    q = amax.astype(np.float64) / s
+    assert q.max() < 16
+    normal = s >= 2.0 ** -14
+    assert q[normal].max() <= 7 * (1 + 2.0 ** -11) and q.max() > 7.49  # the subnormal case needs the slow path
