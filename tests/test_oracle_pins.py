@@ -450,6 +450,42 @@ def test_attention_single_token_returns_its_value():
         assert np.array_equal(got[0, hq], dv[0, hq // 2].astype(np.float64))
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_split_combine_rule_reproduces_attention(seed):
+    # the split-KV merge: a segment of positions keeps its running maximum m, its sum
+    # l = sum exp(z - m) and its unnormalised output o = sum exp(z - m) v; segments merge
+    # as M = max m_i, out = sum exp(m_i - M) o_i / sum exp(m_i - M) l_i, an empty segment
+    # (m = -inf, l = 0) contributing nothing.  Over the oracle's dequantized cache this must
+    # give the oracle's attention, for any cut of the positions into segments.
+    L = oracle.Layout(2, 64, 16, 32, 64, 16)
+    lens = [150, 37]
+    pool, bt, _, _ = _build_cache(L, 2, lens, seed=41 + seed)
+    q = W.kv_tensor(W.SEED_Q + seed, (1, 2, 4, 64)).numpy()[0] * np.float16(4)  # sharp softmax
+    scale = 0.125
+    want = oracle.decode_attention(L, pool, q, bt, np.array(lens, np.int32), scale)
+    rng = np.random.default_rng(seed)
+    for b, n in enumerate(lens):
+        dk, dv = oracle.dequantize(L, pool, bt, b, 0, n)
+        cuts = np.sort(np.concatenate([[0, 0, n, n], rng.integers(0, n + 1, 6)]))  # repeats give empty segments
+        for hq in range(4):
+            k = dk[:, hq // 2].astype(np.float64)
+            v = dv[:, hq // 2].astype(np.float64)
+            z = (k @ q[b, hq].astype(np.float64)) * scale
+            parts = []
+            for a, e in zip(cuts[:-1], cuts[1:]):
+                if e == a:
+                    parts.append((-np.inf, 0.0, np.zeros(64)))
+                    continue
+                m = z[a:e].max()
+                w = np.exp(z[a:e] - m)
+                parts.append((m, w.sum(), w @ v[a:e]))
+            M = max(m for m, _, _ in parts)
+            num = sum(np.exp(m - M) * o for m, l, o in parts if l > 0)
+            den = sum(np.exp(m - M) * l for m, l, o in parts if l > 0)
+            got = num / den
+            assert np.abs(got - want[b, hq]).max() <= 1e-12 * max(1.0, np.abs(want[b, hq]).max())
+
+
 def test_attention_equal_keys_gives_mean_value():
     L = oracle.Layout(1, 64, 16, 32, 64, 4)
     n = 37
