@@ -1096,3 +1096,49 @@ def test_wht4_attention_brute_force_and_exact_case():
         _, dv = oracle.wht4_dequantize(L, pool, bt, b, 0, 1)
         for hq in range(4):
             np.testing.assert_allclose(got1[b, hq], dv[0, hq // 2].astype(np.float64), rtol=1e-6, atol=1e-7)
+
+
+def test_wht4_attention_in_the_rotated_domain():
+    # the decode kernel never forms a dequantized row: with x = H (sigma c) / d and H
+    # symmetric, q . x = (H q / d) . (sigma c), and sum_t p_t x_t = H (sum_t p_t sigma_t c_t) / d.
+    # Taken that way from the stored codes and norms, with each sigma * c rounded to fp32 as
+    # the dequantized row defines it, the scores and weighted sum give the oracle's attention
+    # to fp64 rounding; with sigma applied after the reduction, as the kernel does, they agree
+    # to the fp32 rounding of those products.
+    import scipy.linalg
+    H = scipy.linalg.hadamard(128).astype(np.float64)
+    levels, _ = oracle.wht4_tables()
+    lens = [45, 16]
+    L, pool, bt, _, _ = _wht4_case(215, lens)
+    q = W.kv_tensor(216, (1, 2, 4, 128)).numpy()[0]
+    scale = 0.2
+    want = oracle.wht4_decode_attention(L, pool, q, bt, np.array(lens, np.int32), scale)
+    blocks = pool.reshape(L.num_pages, L.Hkv, -1)
+    for b, n in enumerate(lens):
+        for hq in range(4):
+            h = hq // 2
+            qr = H @ q[b, hq].astype(np.float64) / 128
+            ck, cv, sk, sv = [], [], [], []
+            for t in range(n):
+                blk, s_ = blocks[bt[b, t // 16], h], t % 16
+                for base, out in ((s_ * 64, ck), ((16 + s_) * 64, cv)):
+                    by = blk[base:base + 64]
+                    out.append(levels[np.stack([by & 15, by >> 4], axis=1).reshape(-1)].astype(np.float64))
+                sk.append(float(blk[2048 + 4 * s_:2052 + 4 * s_].view(np.float32)[0]))
+                sv.append(float(blk[2112 + 4 * s_:2116 + 4 * s_].view(np.float32)[0]))
+            ck, cv = np.array(ck), np.array(cv)
+            sk, sv = np.array(sk)[:, None], np.array(sv)[:, None]
+            xk = (sk.astype(np.float32) * ck.astype(np.float32)).astype(np.float64)  # fp32 products
+            xv = (sv.astype(np.float32) * cv.astype(np.float32)).astype(np.float64)
+            p = scipy.special.softmax((xk @ qr) * scale)
+            np.testing.assert_allclose(H @ (p @ xv) / 128, want[b, hq], rtol=1e-9, atol=1e-12)
+            p = scipy.special.softmax(sk[:, 0] * (ck @ qr) * scale)
+            got = H @ ((p * sv[:, 0]) @ cv) / 128
+            # bound: each fp32 product is off by at most 2^-24 of itself, which moves an
+            # output element by at most 2^-24 mean|sigma c| through the transform, and a
+            # score by at most scale 2^-24 sum|H q / d| |sigma c|, which moves the
+            # softmax-weighted mean by at most 2 max|dz| max|x|
+            u = 2.0 ** -24
+            dz = scale * u * (np.abs(xk) @ np.abs(qr)).max()
+            bound = u * np.abs(xv).mean(1).max() + 2 * dz * np.abs(xv @ H / 128).max()
+            assert np.abs(got - want[b, hq]).max() <= bound
