@@ -24,8 +24,8 @@ namespace kvq {
 // |q| (2^-22 + 2^-24) < 2^-17.6 of q for |q| < 16 (one reciprocal within 2 ulp, one
 // rounded product; the quotient never reaches 16 for finite input: the fp16 scale is at least
 // two thirds of amax / 7), so rounding y gives the same code unless y is within 2^-10
-// of a half-integer h; there the sign of x - h s, exact in one fma because h s has at
-// most 15 significant bits, decides, with ties to even.
+// of a half-integer h; there the sign of x - h s decides, with ties to even.  One fma
+// rounds the exact x - h s once, which keeps its sign and its exact zeros.
 __device__ __forceinline__ int exact_code(float x, float s, float y) {
     const float h = floorf(y) + 0.5f;    // the half-integer next to y (when y is near one)
     const float r = fmaf(-h, s, x);      // sign of x - h s, exact
