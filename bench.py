@@ -19,6 +19,7 @@ workload, in the same metric.
 from __future__ import annotations
 
 import argparse
+import itertools
 import json
 import math
 import os
@@ -51,6 +52,8 @@ def parse_args():
                     help="also time the latency comparison: FP16 cache, INT4 dequantized then attended, INT4 fused")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-quality", action="store_true", help="skip the dequantization quality report")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the other decode workloads and the long-context prefill-quantize pass")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
     return ap.parse_args()
 
@@ -242,7 +245,7 @@ def time_oracle(wl, budget_s: float) -> dict:
         t_total += time.perf_counter() - t0
         reps += 1
     per = t_total / reps
-    return {"value": smp.bytes() / per / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": smp.bytes() / per / 1e9, "unit": "GB/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": smp.describe() + f"; {reps} repetitions, {per * 1e3:.1f} ms each",
             "seconds_per_step": per}
 
@@ -270,7 +273,7 @@ def time_oracle_quantize(wl, budget_s: float) -> dict:
     t0 = time.perf_counter()
     oracle.quantize_append(L, pool, k[:, :n], v[:, :n], bt, np.zeros(1, np.int32))
     t = time.perf_counter() - t0
-    return {"value": n * per_token / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": n * per_token / t / 1e9, "unit": "GB/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{wl.name}: sequence 0, {n} of {n_max} tokens x {wl.Hkv} KV heads, K and V; "
                       f"{t * 1e3:.0f} ms"}
 
@@ -362,19 +365,15 @@ def run_kvq(args, world, rank, local):
     n_pools = max(2, math.ceil(3 * l2 / pool_bytes))
 
     caches = [PagedKVCache(cfg, bt, wl.Hq, wl.max_len, device=dev)]
-    # prefill the first pool: each sequence's history (timed as the quantize throughput)
+    # prefill the first pool: each sequence's history in one call (timed as the quantize throughput)
     same_ctx = len(set(wl.ctx)) == 1
     zero = torch.zeros(wl.B if same_ctx else 1, dtype=torch.int32, device=dev)
     hist = [(k_all[:, :wl.ctx[0]].contiguous(), v_all[:, :wl.ctx[0]].contiguous())] if same_ctx else \
         [(k_all[b:b + 1, :c].contiguous(), v_all[b:b + 1, :c].contiguous()) for b, c in enumerate(wl.ctx)]
+    run_prefill = history_prefill(kvq, cfg, k_all, v_all, wl, dev)
 
     def prefill(cache):
-        if same_ctx:
-            cache.append(hist[0][0], hist[0][1], zero)
-        else:
-            for b, (kb, vb) in enumerate(hist):
-                kvq.kvq_quantize_append(cfg, cache.pool, kb, vb, cache.block_table[b:b + 1], zero,
-                                        status=cache.status)
+        run_prefill(cache.pool, cache.block_table, cache.status)
 
     prefill(caches[0])
     # the comparison's FP16 cache holds the same fp16 history
@@ -402,7 +401,8 @@ def run_kvq(args, world, rank, local):
     tok_hist = sum(wl.ctx)
     q_bytes = wl.Hkv * tok_hist * (2 * wl.d * 2 + wl.packed_bytes_per_token_head())
     quantize = {"gbs": q_bytes / min(qt) / 1e9, "tokens": tok_hist, "bytes": q_bytes,
-                "what": "prefill quantize of the whole history: fp16 K+V read, packed codes+scales written"}
+                "what": "prefill quantize of the whole history in one call: fp16 K+V read, packed codes+scales "
+                        "written"}
     for _ in range(n_pools - 1):
         caches.append(PagedKVCache(cfg, bt, wl.Hq, wl.max_len, device=dev, pool=caches[0].pool.clone()))
 
@@ -414,7 +414,7 @@ def run_kvq(args, world, rank, local):
         kvq.kvq_fp16_append(cfg, pool16, k_new, v_new, caches[0].block_table, pos)
         kvq.kvq_int8_quantize_append(cfg, pool8, k_new, v_new, caches[0].block_table, pos)
         kvq.kvq_wht4_quantize_append(cfg, pool4r, k_new, v_new, caches[0].block_table, pos)
-    del k_all, v_all, hist
+    del k_all, v_all, hist, run_prefill
     torch.cuda.empty_cache()
     seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
     out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.float32, device=dev)
@@ -685,10 +685,175 @@ def run_kvq(args, world, rank, local):
         res["comparison"] = comparison
     if not args.no_quality:
         res["quality"] = quality_report(dev)
+    if not args.no_sweep:
+        # the other workloads and the prefill-quantize pass, on rank 0's GPU, with their own clocks
+        del caches
+        torch.cuda.empty_cache()
+        sampler = ClockSampler(local)
+        sampler.start()
+        sweep = {"what": "decode_us: back-to-back kvq_decode_attention calls (split-KV decode) in CUDA graphs "
+                         "over rotated pools larger than L2; step_us: the same for kvq_decode_step (append of "
+                         "one token per sequence fused in); frac: packed decode bytes / decode_us against the "
+                         "measured HBM peak",
+                 "decode": decode_sweep(dev, stream, peaks, l2),
+                 "prefill_quantize": prefill_quantize_sweep(dev, stream, peaks)}
+        sweep["clocks"] = sampler.stop()
+        res["workloads"] = sweep
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = time_oracle(wl, args.cpu_seconds)
         res["cpu_baseline"].pop("seconds_per_step", None)
         res["cpu_baseline"]["quantize"] = time_oracle_quantize(wl, 2.0)
+    return res
+
+
+# ---------------------------------------------------------------------------
+# the other decode workloads and the long-context prefill-quantize pass, reported beside
+# the headline in the same JSON line
+# ---------------------------------------------------------------------------
+
+# GQA 8B-shaped, ragged continuous batching, and long context at the three group sizes
+SWEEP_DECODE = (("gqa8b", None), ("ragged", None), ("longctx", 32), ("longctx", 64), ("longctx", 128))
+
+
+def graph_per_call(fn, stream, calls: int = 50, reps: int = 4, warm: int = 3) -> float:
+    """Seconds per call of fn(i): `warm` eager calls, then a CUDA graph of `calls` back-to-back
+    calls replayed once untimed and `reps` times between two events on the launch stream."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(warm):
+            fn(i)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(calls):
+            fn(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    del g
+    return e0.elapsed_time(e1) * 1e-3 / (calls * reps)
+
+
+def history_prefill(kvq, cfg, k_all, v_all, wl, dev):
+    """A callable that quantizes each sequence's history (positions 0 .. ctx[b]-1) into a pool in
+    one call: kvq_quantize_append when every sequence has the same history, else the ragged
+    kvq_quantize_append_varlen over the histories packed back to back (built here, once)."""
+    import torch
+    zero = torch.zeros(wl.B, dtype=torch.int32, device=dev)
+    if len(set(wl.ctx)) == 1:
+        c = wl.ctx[0]
+        k_h, v_h = k_all[:, :c].contiguous(), v_all[:, :c].contiguous()
+
+        def run(pool, block_table, status, stream=None):
+            kvq.kvq_quantize_append(cfg, pool, k_h, v_h, block_table, zero, status=status, stream=stream)
+        return run
+    k_rows = torch.cat([k_all[b, :c] for b, c in enumerate(wl.ctx)]).contiguous()
+    v_rows = torch.cat([v_all[b, :c] for b, c in enumerate(wl.ctx)]).contiguous()
+    cu = torch.tensor([0] + list(itertools.accumulate(wl.ctx)), dtype=torch.int32, device=dev)
+
+    def run(pool, block_table, status, stream=None):
+        kvq.kvq_quantize_append_varlen(cfg, pool, k_rows, v_rows, block_table, zero, cu, status=status,
+                                       stream=stream)
+    return run
+
+
+def decode_sweep(dev, stream, peaks: dict, l2: int) -> dict:
+    """Per workload: the decode attention call and the decode step (append fused in), each timed as
+    back-to-back calls over rotated pool copies larger than L2."""
+    import torch
+
+    import int4_group_quantized_kvq_gb300 as kvq
+    import workloads as W
+    from int4_group_quantized_kvq_gb300.cache import PagedKVCache
+    res = {}
+    for name, G in SWEEP_DECODE:
+        wl = make_workload(name, G)
+        n_tok = max(wl.seq_lens)
+        oidx = W.outlier_channels(wl.Hkv, wl.d)
+        k_all = W.kv_tensor(W.SEED_K, (wl.B, n_tok, wl.Hkv, wl.d), 20.0, oidx, device=dev)
+        v_all = W.kv_tensor(W.SEED_V, (wl.B, n_tok, wl.Hkv, wl.d), device=dev)
+        q = W.kv_tensor(W.SEED_Q, (1, wl.B, wl.Hq, wl.d), device=dev)[0].contiguous()
+        cfg = kvq.config(wl.Hkv, wl.d, wl.P, wl.Gk, wl.Gv, wl.num_pages)
+        cache0 = PagedKVCache(cfg, wl.block_table(), wl.Hq, wl.max_len, device=dev)
+        history_prefill(kvq, cfg, k_all, v_all, wl, dev)(cache0.pool, cache0.block_table, cache0.status)
+        pos = torch.tensor(wl.ctx, dtype=torch.int32, device=dev)
+        idx = pos.long().view(-1, 1, 1, 1).expand(-1, 1, wl.Hkv, wl.d)
+        k_new = torch.gather(k_all, 1, idx).contiguous()
+        v_new = torch.gather(v_all, 1, idx).contiguous()
+        del k_all, v_all
+        pool_bytes = kvq.kvq_pool_bytes(cfg)
+        n_pools = max(2, math.ceil(3 * l2 / pool_bytes))
+        caches = [cache0] + [PagedKVCache(cfg, cache0.block_table, wl.Hq, wl.max_len, device=dev,
+                                          pool=cache0.pool.clone()) for _ in range(n_pools - 1)]
+        seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
+        out = torch.empty((wl.B, wl.Hq, wl.d), dtype=torch.float32, device=dev)
+        t_dec = graph_per_call(lambda i: caches[i % n_pools].attend(q, seq_lens, out, stream=stream), stream)
+        t_step = graph_per_call(lambda i: caches[i % n_pools].decode_step(q, k_new, v_new, pos, seq_lens, out,
+                                                                          stream=stream), stream)
+        torch.cuda.synchronize()
+        flags = max(c.flags() for c in caches)
+        gbs = wl.decode_bytes() / t_dec / 1e9
+        res[wl.name] = {
+            "batch": wl.B, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "group_k": wl.Gk, "group_v": wl.Gv,
+            "attended_tokens": sum(wl.seq_lens), "decode_bytes": wl.decode_bytes(),
+            "decode_us": t_dec * 1e6, "decode_gbs": gbs, "frac": gbs / peaks["hbm_gbs"],
+            "step_us": t_step * 1e6, "step_gbs": (wl.decode_bytes() + wl.append_bytes()) / t_step / 1e9,
+            "tokens_per_s": wl.B / t_step, "status_flags": flags,
+            "l2": f"{n_pools} rotated pool copies of {pool_bytes / 1e6:.1f} MB",
+        }
+        del caches, cache0, q, k_new, v_new, out
+        torch.cuda.empty_cache()
+    return res
+
+
+def prefill_quantize_sweep(dev, stream, peaks: dict, reps: int = 5) -> dict:
+    """The long-context prefill-quantize pass: 131072 tokens x 8 KV heads x 128, K and V, in one
+    kvq_quantize_append call into a permuted page pool, at K = V group sizes 32, 64 and 128.
+    Inputs (537 MB of fp16) and the pool exceed L2.  Bytes: fp16 K+V read, codes and scales written."""
+    import torch
+
+    import int4_group_quantized_kvq_gb300 as kvq
+    import workloads as W
+    res = {}
+    base = W.longctx(64)
+    n = base.ctx[0]
+    k = W.kv_tensor(W.SEED_K, (1, n, base.Hkv, base.d), 20.0, W.outlier_channels(base.Hkv, base.d), device=dev)
+    v = W.kv_tensor(W.SEED_V, (1, n, base.Hkv, base.d), device=dev)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    for G in (32, 64, 128):
+        wl = W.longctx(G)
+        cfg = kvq.config(wl.Hkv, wl.d, wl.P, wl.Gk, wl.Gv, wl.num_pages)
+        bt = wl.block_table().to(dev)
+        pool = torch.zeros(kvq.kvq_pool_bytes(cfg), dtype=torch.uint8, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                kvq.kvq_quantize_append(cfg, pool, k, v, bt, zero, status=status, stream=stream)
+        stream.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                kvq.kvq_quantize_append(cfg, pool, k, v, bt, zero, status=status, stream=stream)
+                e1.record(stream)
+            stream.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        nbytes = n * wl.Hkv * (2 * wl.d * 2 + wl.packed_bytes_per_token_head())
+        t = statistics.median(ts)
+        res[f"G{G}"] = {"tokens": n, "kv_heads": wl.Hkv, "head_dim": wl.d, "bytes": nbytes, "us": t * 1e6,
+                        "gbs": nbytes / t / 1e9, "frac": nbytes / t / 1e9 / peaks["hbm_gbs"],
+                        "best_us": min(ts) * 1e6, "status_flags": kvq.kvq_read_status(status)}
+        del pool
+    del k, v
+    torch.cuda.empty_cache()
     return res
 
 
@@ -733,7 +898,7 @@ def run_reference(args, world, rank):
         "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "sample": smp.describe()},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": smp.describe()},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle", "sample": smp.describe()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

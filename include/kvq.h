@@ -113,6 +113,30 @@ int kvq_quantize_append(const kvq_cache_config *cfg, void *pool, const void *k, 
                         int32_t batch, int32_t n_new, uint32_t *status, kvq_stream_t stream);
 
 /*
+ * Quantize-on-append of a ragged batch in one launch: the same quantization and storage
+ * as kvq_quantize_append (section 2.1 of the 4-bit page), with a different number of
+ * new tokens per sequence (the prefill of a continuous batch, section 3.1 of the
+ * KV-cache optimisation page).
+ *   k_rows, v_rows  device fp16 [total_rows, num_kv_heads, head_dim], contiguous,
+ *                   16-byte aligned: the new tokens of all sequences back to back.
+ *   cu_rows         device int32 [batch + 1]: sequence b owns rows cu_rows[b] ..
+ *                   cu_rows[b + 1] - 1 (cu_rows[0] = 0, non-decreasing,
+ *                   cu_rows[batch] = total_rows); its row cu_rows[b] + t goes to
+ *                   position start_pos[b] + t.
+ *   other arguments as in kvq_quantize_append.
+ * Each row goes to a sequence b in [0, batch) found by a binary search of
+ * cu_rows[0 .. batch - 1] (cu_rows[batch] is not read).  Offsets that break the rules
+ * above send rows to other sequences or positions but never make the kernel read or
+ * write outside its arguments: a position outside the block table is skipped and
+ * flagged as there.
+ * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED or KVQ_ECUDA.
+ */
+int kvq_quantize_append_varlen(const kvq_cache_config *cfg, void *pool, const void *k_rows,
+                               const void *v_rows, const int32_t *block_table, int32_t max_blocks,
+                               const int32_t *start_pos, const int32_t *cu_rows, int32_t batch,
+                               int32_t total_rows, uint32_t *status, kvq_stream_t stream);
+
+/*
  * Workspace bytes kvq_decode_attention needs for this shape on the current device
  * (it depends on the device's SM count).  0 if the arguments are invalid.
  */

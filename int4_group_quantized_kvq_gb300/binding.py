@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_PKG, "libkvq.so")
 KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE, KVQ_ECUDA = 0, 1, 2, 3, 4
 KVQ_FLAG_BAD_PAGE, KVQ_FLAG_BAD_POSITION, KVQ_FLAG_WAIT_TIMEOUT, KVQ_FLAG_STALE_WORKSPACE = 0x1, 0x2, 0x4, 0x8
 
-ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_decode_workspace_bytes",
+ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_quantize_append_varlen",
+               "kvq_decode_workspace_bytes",
                "kvq_decode_attention", "kvq_dequantize", "kvq_read_status", "kvq_last_error", "kvq_version",
                "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_attention_window",
                "kvq_decode_step_window", "kvq_fp16_pool_bytes", "kvq_fp16_append", "kvq_dequantize_to_fp16_pool",
@@ -65,6 +66,8 @@ def lib() -> C.CDLL:
         L.kvq_pool_bytes.restype = SZ
         L.kvq_quantize_append.argtypes = [cfgp, P, P, P, P, I32, P, I32, I32, P, P]
         L.kvq_quantize_append.restype = C.c_int
+        L.kvq_quantize_append_varlen.argtypes = [cfgp, P, P, P, P, I32, P, P, I32, I32, P, P]
+        L.kvq_quantize_append_varlen.restype = C.c_int
         L.kvq_decode_workspace_bytes.argtypes = [cfgp, I32, I32, I32]
         L.kvq_decode_workspace_bytes.restype = SZ
         L.kvq_decode_attention.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ, P]
@@ -159,6 +162,15 @@ def _dev(t: torch.Tensor, name: str, dtype: torch.dtype | None = None) -> int:
     return t.data_ptr()
 
 
+def _status(t: torch.Tensor) -> int:
+    """A device status word: the library writes or ORs 4 bytes into it."""
+    if not isinstance(t, torch.Tensor) or t.dtype not in (torch.int32, getattr(torch, "uint32", torch.int32)):
+        raise ValueError("status must be an int32 (or uint32) CUDA tensor")
+    if t.numel() < 1:
+        raise ValueError("status must hold at least one element")
+    return _dev(t, "status")
+
+
 def config(num_kv_heads: int, head_dim: int, page_size: int = 16, group_k: int = 64, group_v: int = 128,
            num_pages: int = 1) -> CacheConfig:
     return CacheConfig(num_kv_heads, head_dim, page_size, group_k, group_v, num_pages)
@@ -189,7 +201,25 @@ def kvq_quantize_append(cfg: CacheConfig, pool: torch.Tensor, k: torch.Tensor, v
         C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(k, "k", torch.float16), _dev(v, "v", torch.float16),
         _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
         _dev(start_pos, "start_pos", torch.int32), B, n_new,
-        None if status is None else _dev(status, "status"), _stream(stream))
+        None if status is None else _status(status), _stream(stream))
+    _check(rc)
+
+
+def kvq_quantize_append_varlen(cfg: CacheConfig, pool: torch.Tensor, k_rows: torch.Tensor, v_rows: torch.Tensor,
+                               block_table: torch.Tensor, start_pos: torch.Tensor, cu_rows: torch.Tensor,
+                               status: torch.Tensor | None = None, stream=None) -> None:
+    """k_rows, v_rows: fp16 [total_rows, Hkv, d], the sequences' new rows back to back; cu_rows int32 [B + 1]:
+    sequence b owns rows cu_rows[b] .. cu_rows[b + 1] - 1; start_pos int32 [B]."""
+    if k_rows.shape != v_rows.shape or k_rows.dim() != 3:
+        raise ValueError("k_rows and v_rows must both be [total_rows, Hkv, d]")
+    B = int(block_table.shape[0])
+    if cu_rows.dim() != 1 or int(cu_rows.shape[0]) != B + 1 or int(start_pos.shape[0]) != B:
+        raise ValueError("cu_rows must be [B + 1] and start_pos [B] for a block table of B rows")
+    rc = lib().kvq_quantize_append_varlen(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(k_rows, "k_rows", torch.float16),
+        _dev(v_rows, "v_rows", torch.float16), _dev(block_table, "block_table", torch.int32),
+        int(block_table.shape[1]), _dev(start_pos, "start_pos", torch.int32), _dev(cu_rows, "cu_rows", torch.int32),
+        B, int(k_rows.shape[0]), None if status is None else _status(status), _stream(stream))
     _check(rc)
 
 
@@ -272,7 +302,7 @@ def kvq_decode_attention_noalloc(cfg: CacheConfig, pool: torch.Tensor, q: torch.
         C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(q, "q", torch.float16),
         _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
         _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
-        _dev(out, "out", torch.float32), None if status is None else _dev(status, "status"), _stream(stream))
+        _dev(out, "out", torch.float32), None if status is None else _status(status), _stream(stream))
     _check(rc)
 
 
@@ -286,7 +316,7 @@ def kvq_dequantize(cfg: CacheConfig, pool: torch.Tensor, block_table: torch.Tens
     rc = lib().kvq_dequantize(
         C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(block_table, "block_table", torch.int32),
         int(block_table.shape[1]), b, start, n, _dev(out_k, "out_k"), _dev(out_v, "out_v"), out_dtype,
-        None if status is None else _dev(status, "status"), _stream(stream))
+        None if status is None else _status(status), _stream(stream))
     _check(rc)
 
 
@@ -319,7 +349,7 @@ def kvq_fp16_append(cfg: CacheConfig, pool16: torch.Tensor, k: torch.Tensor, v: 
     rc = lib().kvq_fp16_append(
         C.byref(cfg), _dev(pool16, "pool16", torch.uint8), _dev(k, "k", torch.float16), _dev(v, "v", torch.float16),
         _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
-        _dev(start_pos, "start_pos", torch.int32), B, n, None if status is None else _dev(status, "status"),
+        _dev(start_pos, "start_pos", torch.int32), B, n, None if status is None else _status(status),
         _stream(stream))
     _check(rc)
 
@@ -332,7 +362,7 @@ def kvq_dequantize_to_fp16_pool(cfg: CacheConfig, pool: torch.Tensor, pool16: to
         C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(pool16, "pool16", torch.uint8),
         _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
         _dev(seq_lens, "seq_lens", torch.int32), int(seq_lens.shape[0]), int(max_len),
-        None if status is None else _dev(status, "status"), _stream(stream))
+        None if status is None else _status(status), _stream(stream))
     _check(rc)
 
 
@@ -403,7 +433,7 @@ def kvq_int8_quantize_append(cfg: CacheConfig, pool8: torch.Tensor, k: torch.Ten
     rc = lib().kvq_int8_quantize_append(
         C.byref(cfg), _dev(pool8, "pool8", torch.uint8), _dev(k, "k", torch.float16), _dev(v, "v", torch.float16),
         _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
-        _dev(start_pos, "start_pos", torch.int32), B, n, None if status is None else _dev(status, "status"),
+        _dev(start_pos, "start_pos", torch.int32), B, n, None if status is None else _status(status),
         _stream(stream))
     _check(rc)
 
@@ -453,7 +483,7 @@ def kvq_wht4_quantize_append(cfg: CacheConfig, pool: torch.Tensor, k: torch.Tens
     rc = lib().kvq_wht4_quantize_append(
         C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(k, "k", torch.float16), _dev(v, "v", torch.float16),
         _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
-        _dev(start_pos, "start_pos", torch.int32), B, n, None if status is None else _dev(status, "status"),
+        _dev(start_pos, "start_pos", torch.int32), B, n, None if status is None else _status(status),
         _stream(stream))
     _check(rc)
 
@@ -465,7 +495,7 @@ def kvq_wht4_dequantize(cfg: CacheConfig, pool: torch.Tensor, block_table: torch
     rc = lib().kvq_wht4_dequantize(
         C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(block_table, "block_table", torch.int32),
         int(block_table.shape[1]), int(b), int(start), int(n), _dev(out_k, "out_k", torch.float32),
-        _dev(out_v, "out_v", torch.float32), None if status is None else _dev(status, "status"), _stream(stream))
+        _dev(out_v, "out_v", torch.float32), None if status is None else _status(status), _stream(stream))
     _check(rc)
 
 

@@ -67,35 +67,40 @@ size_t kvq_pool_bytes(const kvq_cache_config* cfg) {
     return static_cast<size_t>(cfg->num_pages) * cfg->num_kv_heads * kvq::block_layout(*cfg).bytes;
 }
 
-int kvq_quantize_append(const kvq_cache_config* cfg, void* pool, const void* k, const void* v,
-                        const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
-                        int32_t n_new, uint32_t* status, kvq_stream_t stream) {
-    if (int e = check_cfg(cfg)) return e;
-    if (batch < 0 || n_new < 0) return fail(KVQ_EINVAL, "batch %d / n_new %d negative", batch, n_new);
-    if (batch == 0 || n_new == 0) return ok();
+}  // extern "C"
+
+namespace {
+// The quantize-append of both entry points: `tokens` rows of [Hkv, d] in k and v, owned by
+// the sequences as cu_rows says (nullptr: n_new each).
+int quantize_append_impl(const kvq_cache_config* cfg, void* pool, const void* k, const void* v,
+                         const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos,
+                         const int32_t* cu_rows, int32_t batch, int32_t n_new, int64_t tokens, uint32_t* status,
+                         kvq_stream_t stream, const char* name) {
     if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
     if (!pool || !k || !v || !block_table || !start_pos) return fail(KVQ_EINVAL, "NULL device pointer");
     if (!aligned(pool, 16) || !aligned(k, 16) || !aligned(v, 16))
         return fail(KVQ_EINVAL, "pool, k and v must be 16-byte aligned");
-    if (!aligned(block_table, 4) || !aligned(start_pos, 4) || (status && !aligned(status, 4)))
+    if (!aligned(block_table, 4) || !aligned(start_pos, 4) || (status && !aligned(status, 4)) ||
+        (cu_rows && !aligned(cu_rows, 4)))
         return fail(KVQ_EINVAL, "int32/uint32 arguments must be 4-byte aligned");
-    if (static_cast<int64_t>(batch) * n_new * cfg->num_kv_heads >= (int64_t{1} << 30))
-        return fail(KVQ_EINVAL, "batch * n_new * num_kv_heads must be below 2^30 per call");
+    if (tokens * cfg->num_kv_heads >= (int64_t{1} << 30))
+        return fail(KVQ_EINVAL, "tokens * num_kv_heads must be below 2^30 per call");
     kvq::QuantizeArgs a;
     a.pool = static_cast<uint8_t*>(pool);
     a.k = static_cast<const __half*>(k);
     a.v = static_cast<const __half*>(v);
     a.block_table = block_table;
     a.start_pos = start_pos;
+    a.cu_rows = cu_rows;
     a.status = status;
     a.max_blocks = max_blocks;
     a.B = batch;
     a.n_new = n_new;
     a.Hkv = cfg->num_kv_heads;
     a.num_pages = cfg->num_pages;
-    a.rows = static_cast<uint32_t>(batch) * static_cast<uint32_t>(n_new) * static_cast<uint32_t>(cfg->num_kv_heads);
+    a.rows = static_cast<uint32_t>(tokens) * static_cast<uint32_t>(cfg->num_kv_heads);
     a.div_h = kvq::make_fastdiv(static_cast<uint32_t>(cfg->num_kv_heads));
-    a.div_n = kvq::make_fastdiv(static_cast<uint32_t>(n_new));
+    a.div_n = kvq::make_fastdiv(static_cast<uint32_t>(n_new > 0 ? n_new : 1));
     a.lg_p = 0;
     while ((1 << a.lg_p) < cfg->page_size) ++a.lg_p;
     a.lg_lanes_k = 0;
@@ -104,8 +109,34 @@ int kvq_quantize_append(const kvq_cache_config* cfg, void* pool, const void* k, 
     while ((8 << a.lg_lanes_v) < cfg->group_v) ++a.lg_lanes_v;
     a.L = kvq::block_layout(*cfg);
     cudaError_t e = kvq::launch_quantize_append(a, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "kvq_quantize_append launch");
+    if (e != cudaSuccess) return cuda_fail(e, name);
     return ok();
+}
+}  // namespace
+
+extern "C" {
+
+int kvq_quantize_append(const kvq_cache_config* cfg, void* pool, const void* k, const void* v,
+                        const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos, int32_t batch,
+                        int32_t n_new, uint32_t* status, kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || n_new < 0) return fail(KVQ_EINVAL, "batch %d / n_new %d negative", batch, n_new);
+    if (batch == 0 || n_new == 0) return ok();
+    return quantize_append_impl(cfg, pool, k, v, block_table, max_blocks, start_pos, nullptr, batch, n_new,
+                                static_cast<int64_t>(batch) * n_new, status, stream, "kvq_quantize_append launch");
+}
+
+int kvq_quantize_append_varlen(const kvq_cache_config* cfg, void* pool, const void* k_rows, const void* v_rows,
+                               const int32_t* block_table, int32_t max_blocks, const int32_t* start_pos,
+                               const int32_t* cu_rows, int32_t batch, int32_t total_rows, uint32_t* status,
+                               kvq_stream_t stream) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || total_rows < 0)
+        return fail(KVQ_EINVAL, "batch %d / total_rows %d negative", batch, total_rows);
+    if (batch == 0 || total_rows == 0) return ok();
+    if (!cu_rows) return fail(KVQ_EINVAL, "NULL device pointer");
+    return quantize_append_impl(cfg, pool, k_rows, v_rows, block_table, max_blocks, start_pos, cu_rows, batch, 0,
+                                total_rows, status, stream, "kvq_quantize_append_varlen launch");
 }
 
 namespace {

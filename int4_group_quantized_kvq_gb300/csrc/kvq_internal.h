@@ -59,10 +59,13 @@ struct QuantizeArgs {
     const __half* v;
     const int32_t* block_table;
     const int32_t* start_pos;
+    // ragged batches: sequence b owns tokens cu_rows[b] .. cu_rows[b + 1] - 1 of the row
+    // arrays (nullptr: every sequence owns n_new tokens, sequence b from b * n_new)
+    const int32_t* cu_rows;
     uint32_t* status;
     int32_t max_blocks, B, n_new, Hkv, num_pages;
-    uint32_t rows;          // B * n_new * Hkv (< 2^30)
-    FastDiv div_h, div_n;   // by Hkv, by n_new
+    uint32_t rows;          // tokens * Hkv (< 2^30)
+    FastDiv div_h, div_n;   // by Hkv, by n_new (unused with cu_rows)
     int32_t lg_p;           // log2 page_size
     int32_t lg_lanes_k, lg_lanes_v;  // log2 of group_k / 8 and group_v / 8 (lanes of 8 values per group)
     BlockLayout L;

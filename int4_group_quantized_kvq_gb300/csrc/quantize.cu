@@ -18,6 +18,13 @@
 namespace kvq {
 namespace {
 
+// fp32(1/7).  For every fp16 value a >= 0 (subnormals and +inf included),
+// fp16_rne(a * kInv7) == fp16_rne(fp32_rn(a / 7)): the product and the IEEE quotient
+// may differ in the last fp32 bit, but never across an fp16 rounding boundary.  The
+// domain is 31,745 values and the CPU tests check every one of them, so one multiply
+// stands in for the division of the definition.
+constexpr float kInv7 = 0.142857149f;  // 0x3E124925
+
 // The 16 values a lane holds (row values 16 tl .. 16 tl + 15, inside one group) as 16
 // nibbles (code + 8, element 2j low), low word first, and the group's fp16 scale.  The
 // codes are those of quant_lane8 (kvq_quant.cuh, which the decode step's fused append
@@ -57,7 +64,7 @@ __device__ __forceinline__ uint2 quant_lane16(const uint4 (&raw)[2], int lg16, _
         const float other = __shfl_xor_sync(0xffffffffu, amax, off);
         if (off < (1 << lg16)) amax = fmaxf(amax, other);
     }
-    __half s16 = __float2half_rn(__fdiv_rn(amax, 7.0f));
+    __half s16 = __float2half_rn(amax * kInv7);
     if ((__half_as_ushort(s16) & 0x7fffu) == 0) s16 = __ushort_as_half(0x3c00u);
     const float s = __half2float(s16);
     scale_out = s16;
@@ -87,50 +94,50 @@ __device__ __forceinline__ uint2 quant_lane16(const uint4 (&raw)[2], int lg16, _
     return make_uint2(lo, hi);
 }
 
-// Quantize one row job (a K or V row of one (sequence, token, kv head)) held as 16
-// values per lane, and store its codes and scales.  Every lane of the warp calls this
-// together (the group maximum is a shuffle reduction); `active` marks real jobs.
-template <int D>
-__device__ __forceinline__ void quantize_row(const QuantizeArgs& a, const uint4 (&raw)[2], uint32_t job, bool active,
-                                             int tl) {
-    const int is_v = static_cast<int>(job & 1u);
-    const int lg = (is_v ? a.lg_lanes_v : a.lg_lanes_k) - 1;  // log2 of the 16-value lanes per group
-    __half s16;
-    const uint2 words = quant_lane16<D / 16>(raw, lg, s16);
-    if (!active) return;
-
-    // destination: row = (b * n_new + t) * Hkv + h -> position, page, slot
-    const uint32_t row = job >> 1;
-    const uint32_t bt = fast_div(row, a.div_h);
-    const int h = static_cast<int>(row - bt * static_cast<uint32_t>(a.Hkv));
-    const uint32_t b = fast_div(bt, a.div_n);
-    const int t = static_cast<int>(bt - b * static_cast<uint32_t>(a.n_new));
-    const long long pos = static_cast<long long>(a.start_pos[b]) + t;
+// Destination of one row (a (token, kv head) pair): the address of its (page, kv head)
+// block and its slot in the page, or block 0 when the row is skipped (its position or
+// page is out of range, which raises a flag).  Token tok belongs to sequence b: with
+// cu_rows the last b whose first token cu_rows[b] is <= tok, else tok / n_new.
+__device__ __forceinline__ unsigned long long row_dest(const QuantizeArgs& a, uint32_t row, int& slot) {
+    const uint32_t tok = fast_div(row, a.div_h);
+    const int h = static_cast<int>(row - tok * static_cast<uint32_t>(a.Hkv));
+    int b;
+    long long t;
+    if (a.cu_rows != nullptr) {
+        int lo = 0, hi = a.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(a.cu_rows + mid) <= static_cast<int>(tok)) lo = mid;
+            else hi = mid - 1;
+        }
+        b = lo;
+        t = static_cast<long long>(tok) - __ldg(a.cu_rows + b);
+    } else {
+        b = static_cast<int>(fast_div(tok, a.div_n));
+        t = static_cast<long long>(tok) - static_cast<long long>(b) * a.n_new;
+    }
+    const long long pos = static_cast<long long>(__ldg(a.start_pos + b)) + t;
     const long long pidx = pos >> a.lg_p;
     if (pos < 0 || pidx >= a.max_blocks) {
-        if (tl == 0) raise_flag(a.status, KVQ_FLAG_BAD_POSITION);
-        return;
+        raise_flag(a.status, KVQ_FLAG_BAD_POSITION);
+        return 0ull;
     }
-    const int page = a.block_table[static_cast<long long>(b) * a.max_blocks + pidx];
+    const int page = __ldg(a.block_table + static_cast<long long>(b) * a.max_blocks + pidx);
     if (page < 0 || page >= a.num_pages) {
-        if (tl == 0) raise_flag(a.status, KVQ_FLAG_BAD_PAGE);
-        return;
+        raise_flag(a.status, KVQ_FLAG_BAD_PAGE);
+        return 0ull;
     }
-    const int slot = static_cast<int>(pos & ((1 << a.lg_p) - 1));
-    uint8_t* blk = a.pool + (static_cast<long long>(page) * a.Hkv + h) * a.L.bytes;
-    uint8_t* codes = blk + (is_v ? a.L.v_codes : 0) + slot * (D / 2);
-    reinterpret_cast<uint2*>(codes)[tl] = words;
-    if ((tl & ((1 << lg) - 1)) == 0) {
-        const int ngroups = D >> (lg + 4);
-        uint8_t* scales = blk + (is_v ? a.L.v_scales : a.L.k_scales) + slot * ngroups * 2;
-        reinterpret_cast<__half*>(scales)[tl >> lg] = s16;
-    }
+    slot = static_cast<int>(pos & ((1 << a.lg_p) - 1));
+    return reinterpret_cast<unsigned long long>(a.pool + (static_cast<long long>(page) * a.Hkv + h) * a.L.bytes);
 }
 
-// Work mapping: jobs are (row, K or V) pairs, K and V of a row adjacent.  A warp takes
-// TEAMS jobs at a time, U times over, loading all U x 32 bytes per lane before it
-// computes, so enough loads are in flight to stream from HBM.  The job loop is
-// grid-strided over a grid of one wave of resident CTAs.
+// Work mapping.  Rows go to warps in blocks of 32; a job is the K or the V row of one row
+// (K and V of a row adjacent), held by a team of LPR = D / 16 lanes, 16 values a lane.
+// Lane l of the warp first works out where row l of the block goes (one block-table
+// lookup per row, shared by its K and V jobs and by the lanes of their teams through
+// shuffles), then the warp quantizes the block's 64 jobs TEAMS * U at a time, loading
+// all U x 32 bytes per lane before it computes, so enough loads are in flight to stream
+// from HBM.  The block loop is grid-strided over one wave of resident CTAs.
 template <int D, int U>
 __global__ void __launch_bounds__(256, 4) quantize_append_kernel(QuantizeArgs a) {
     // A decode launched behind this kernel may start its own set-up now; it waits for this
@@ -139,30 +146,53 @@ __global__ void __launch_bounds__(256, 4) quantize_append_kernel(QuantizeArgs a)
     // before anything else.
     asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    constexpr int LPR = D / 16;           // lanes per row
-    constexpr int TEAMS = 32 / LPR;       // row jobs per warp at a time
+    constexpr int LPR = D / 16;           // lanes per job
+    constexpr int TEAMS = 32 / LPR;       // jobs per warp at a time
+    constexpr int JPP = TEAMS * U;        // jobs per pass
+    constexpr int PASSES = 64 / JPP;      // passes over a block's 64 jobs
     const int lane = threadIdx.x & 31;
     const int team = lane / LPR;
     const int tl = lane % LPR;            // lane within the team
-    const uint32_t jobs = 2u * a.rows;
+    const uint32_t blocks = (a.rows + 31u) / 32u;
     const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const uint32_t warps_total = gridDim.x * blockDim.x / 32;
-    for (uint32_t base = warp_global * TEAMS * U; base < jobs; base += warps_total * TEAMS * U) {
-        uint4 raw[U][2];
+    for (uint32_t blk = warp_global; blk < blocks; blk += warps_total) {
+        const uint32_t row0 = blk * 32u;
+        int my_slot = 0;
+        const unsigned long long my_dst = row0 + lane < a.rows ? row_dest(a, row0 + lane, my_slot) : 0ull;
+#pragma unroll 1
+        for (int ps = 0; ps < PASSES; ++ps) {
+            uint4 raw[U][2];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t job = base + u * TEAMS + team;
-            raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
-            if (job < jobs) {
-                const __half* src = ((job & 1u) ? a.v : a.k) + static_cast<size_t>(job >> 1) * D + tl * 16;
-                raw[u][0] = __ldcs(reinterpret_cast<const uint4*>(src));  // read once: stream past the caches
-                raw[u][1] = __ldcs(reinterpret_cast<const uint4*>(src) + 1);
+            for (int u = 0; u < U; ++u) {
+                const int jl = ps * JPP + u * TEAMS + team;  // job within the block
+                const uint32_t row = row0 + static_cast<uint32_t>(jl >> 1);
+                raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+                if (row < a.rows) {
+                    const __half* src = ((jl & 1) ? a.v : a.k) + static_cast<size_t>(row) * D + tl * 16;
+                    raw[u][0] = __ldcs(reinterpret_cast<const uint4*>(src));  // read once: stream past the caches
+                    raw[u][1] = __ldcs(reinterpret_cast<const uint4*>(src) + 1);
+                }
             }
-        }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t job = base + u * TEAMS + team;
-            quantize_row<D>(a, raw[u], job, job < jobs, tl);
+            for (int u = 0; u < U; ++u) {
+                const int jl = ps * JPP + u * TEAMS + team;
+                const int is_v = jl & 1;
+                const int lg = (is_v ? a.lg_lanes_v : a.lg_lanes_k) - 1;  // log2 of the 16-value lanes per group
+                __half s16;
+                const uint2 words = quant_lane16<LPR>(raw[u], lg, s16);
+                const unsigned long long dst = __shfl_sync(0xffffffffu, my_dst, jl >> 1);
+                const int slot = __shfl_sync(0xffffffffu, my_slot, jl >> 1);
+                if (dst == 0ull) continue;  // past the end, or skipped and flagged
+                uint8_t* blkp = reinterpret_cast<uint8_t*>(dst);
+                uint8_t* codes = blkp + (is_v ? a.L.v_codes : 0) + slot * (D / 2);
+                reinterpret_cast<uint2*>(codes)[tl] = words;
+                if ((tl & ((1 << lg) - 1)) == 0) {
+                    const int ngroups = D >> (lg + 4);
+                    uint8_t* scales = blkp + (is_v ? a.L.v_scales : a.L.k_scales) + slot * ngroups * 2;
+                    reinterpret_cast<__half*>(scales)[tl >> lg] = s16;
+                }
+            }
         }
     }
 }
@@ -185,11 +215,10 @@ int quantize_ctas_per_sm() {
 template <int D>
 cudaError_t launch_q(const QuantizeArgs& a, cudaStream_t stream) {
     constexpr int U = 2;
-    const long long jobs = 2LL * a.rows;
-    if (jobs == 0) return cudaSuccess;
+    const long long blocks32 = (static_cast<long long>(a.rows) + 31) / 32;
+    if (blocks32 == 0) return cudaSuccess;
     constexpr int threads = 256;
-    constexpr int jobs_per_block = (threads / 32) * (32 / (D / 16)) * U;
-    long long blocks = (jobs + jobs_per_block - 1) / jobs_per_block;
+    long long blocks = (blocks32 + threads / 32 - 1) / (threads / 32);
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -59,3 +59,20 @@ def test_group_quotients_stay_below_16():
     assert q.max() < 16
     normal = s >= 2.0 ** -14
     assert q[normal].max() <= 7 * (1 + 2.0 ** -11) and q.max() > 7.49  # the subnormal case needs the slow path
+
+
+def test_scale_by_reciprocal_multiply_equals_the_division():
+    # The quantize kernel forms the scale as fp16_rne(amax * fp32(1/7)) instead of
+    # fp16_rne(fp32_rn(amax / 7)).  amax is a non-negative fp16 value, so checking every
+    # one of them (subnormals, the largest finite value and +inf included) proves the two
+    # equal; both sides use IEEE round-to-nearest fp32 arithmetic.
+    h = np.arange(0, 0x7C01, dtype=np.uint16)
+    amax = h.view(np.float16).astype(np.float32)
+    inv7 = np.array([0x3E124925], np.uint32).view(np.float32)[0]
+    assert inv7 == np.float32(1.0) / np.float32(7.0)
+    by_div = (amax / np.float32(7.0)).astype(np.float16).view(np.uint16)
+    by_mul = (amax * inv7).astype(np.float16).view(np.uint16)
+    assert np.array_equal(by_div, by_mul)
+    # the fp32 results themselves do differ for some amax: the equality is a property of
+    # the fp16 rounding, not of the fp32 arithmetic
+    assert np.any((amax / np.float32(7.0)) != (amax * inv7))

@@ -197,3 +197,106 @@ def test_dequantize_arbitrary_bytes(kvq):
     rk, rv = oracle.dequantize(L, pool_np, bt, 0, 0, 48)
     assert np.array_equal(ok.cpu().numpy().view(np.uint32), rk.view(np.uint32))
     assert np.array_equal(ov.cpu().numpy().view(np.uint32), rv.view(np.uint32))
+
+
+def _varlen_case(seed, counts, H, d, P, Gk, Gv):
+    """Sequences with `counts[b]` new rows each, appended at ragged start positions into a permuted pool."""
+    rng = np.random.default_rng(seed)
+    B = len(counts)
+    start = rng.integers(0, 3 * P, B).astype(np.int32)
+    per = (int(max(start)) + max(counts) + P - 1) // P + 1
+    npg = B * per + 3
+    L = oracle.Layout(H, d, P, Gk, Gv, npg)
+    bt = W.permutation(seed, npg).numpy()[:B * per].reshape(B, per).astype(np.int32)
+    total = int(sum(counts))
+    x_k = _hard_inputs((1, total, H, d), seed=seed + 1)[0]
+    x_v = _hard_inputs((1, total, H, d), seed=seed + 2)[0]
+    cu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return L, bt, start, cu, x_k, x_v
+
+
+@pytest.mark.parametrize("counts,H,d,P,Gk,Gv", [
+    ([5, 0, 37, 1, 16, 70], 4, 128, 16, 64, 128),
+    ([3, 129, 0, 0, 2], 8, 128, 32, 32, 32),
+    ([17, 1, 33], 3, 64, 16, 32, 64),
+    ([9, 40], 2, 256, 64, 128, 64),
+    ([1] * 40, 8, 128, 16, 64, 128),
+])
+def test_quantize_append_varlen_bitexact(kvq, counts, H, d, P, Gk, Gv):
+    """One ragged call equals the oracle appending each sequence's own rows at its start position."""
+    L, bt, start, cu, x_k, x_v = _varlen_case(sum(counts) + H + d, counts, H, d, P, Gk, Gv)
+    ref = np.full(L.pool_bytes, 0x6B, np.uint8)
+    for b in range(len(counts)):
+        if counts[b]:
+            oracle.quantize_append(L, ref, x_k[None, cu[b]:cu[b + 1]], x_v[None, cu[b]:cu[b + 1]], bt[b:b + 1],
+                                   start[b:b + 1])
+    cfg = kvq.config(H, d, P, Gk, Gv, L.num_pages)
+    pool = torch.full((kvq.kvq_pool_bytes(cfg),), 0x6B, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.kvq_quantize_append_varlen(cfg, pool, torch.from_numpy(x_k).cuda(), torch.from_numpy(x_v).cuda(),
+                                   torch.from_numpy(bt).cuda(), torch.from_numpy(start).cuda(),
+                                   torch.from_numpy(cu).cuda(), status=status)
+    assert kvq.kvq_read_status(status) == 0
+    got = pool.cpu().numpy()
+    diff = np.nonzero(got != ref)[0]
+    assert diff.size == 0, f"{diff.size} bytes differ, first at {diff[:8]}"
+
+
+def test_quantize_append_varlen_equals_fixed_count_call(kvq):
+    """With every sequence appending n rows, the ragged call writes what kvq_quantize_append writes."""
+    B, n, H, d, P = 4, 45, 8, 128, 16
+    L, bt, start, cu, x_k, x_v = _varlen_case(31, [n] * B, H, d, P, 64, 128)
+    cfg = kvq.config(H, d, P, 64, 128, L.num_pages)
+    pools = []
+    for ragged in (False, True):
+        pool = torch.full((kvq.kvq_pool_bytes(cfg),), 0x11, dtype=torch.uint8, device="cuda")
+        if ragged:
+            kvq.kvq_quantize_append_varlen(cfg, pool, torch.from_numpy(x_k).cuda(), torch.from_numpy(x_v).cuda(),
+                                           torch.from_numpy(bt).cuda(), torch.from_numpy(start).cuda(),
+                                           torch.from_numpy(cu).cuda())
+        else:
+            kvq.kvq_quantize_append(cfg, pool, torch.from_numpy(x_k.reshape(B, n, H, d)).cuda(),
+                                    torch.from_numpy(x_v.reshape(B, n, H, d)).cuda(), torch.from_numpy(bt).cuda(),
+                                    torch.from_numpy(start).cuda())
+        pools.append(pool.cpu().numpy())
+    assert np.array_equal(pools[0], pools[1])
+
+
+def test_quantize_append_varlen_bad_positions_are_flagged(kvq):
+    """A sequence whose positions leave its block table is skipped and flagged; the others are exact."""
+    H, d, P = 2, 128, 16
+    counts = [10, 12, 10]
+    L, bt, _, cu, x_k, x_v = _varlen_case(5, counts, H, d, P, 64, 128)
+    start = np.array([0, P + 3, 10 * P], np.int32)  # sequence 2 beyond its block table
+    cfg = kvq.config(H, d, P, 64, 128, L.num_pages)
+    pool = torch.full((kvq.kvq_pool_bytes(cfg),), 0x22, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.kvq_quantize_append_varlen(cfg, pool, torch.from_numpy(x_k).cuda(), torch.from_numpy(x_v).cuda(),
+                                   torch.from_numpy(bt).cuda(), torch.from_numpy(start).cuda(),
+                                   torch.from_numpy(cu).cuda(), status=status)
+    assert kvq.kvq_read_status(status) == kvq.KVQ_FLAG_BAD_POSITION
+    ref = np.full(L.pool_bytes, 0x22, np.uint8)
+    for b in (0, 1):
+        oracle.quantize_append(L, ref, x_k[None, cu[b]:cu[b + 1]], x_v[None, cu[b]:cu[b + 1]], bt[b:b + 1],
+                               start[b:b + 1])
+    assert np.array_equal(pool.cpu().numpy(), ref)
+
+
+def test_quantize_append_varlen_decreasing_offsets_stay_in_bounds(kvq):
+    """Offsets that decrease move rows to other sequences or positions, but every byte written
+    lies in a block of a page the block table names."""
+    H, d, P = 2, 128, 16
+    counts = [10, 10, 10]
+    L, bt, start, _, x_k, x_v = _varlen_case(6, counts, H, d, P, 64, 128)
+    cu = np.array([0, 25, 12, 30], np.int32)
+    cfg = kvq.config(H, d, P, 64, 128, L.num_pages)
+    pool = torch.full((kvq.kvq_pool_bytes(cfg),), 0x33, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.kvq_quantize_append_varlen(cfg, pool, torch.from_numpy(x_k).cuda(), torch.from_numpy(x_v).cuda(),
+                                   torch.from_numpy(bt).cuda(), torch.from_numpy(start).cuda(),
+                                   torch.from_numpy(cu).cuda(), status=status)
+    torch.cuda.synchronize()
+    changed = np.nonzero(pool.cpu().numpy() != 0x33)[0]
+    assert changed.size > 0
+    pages = set(bt[bt >= 0].tolist())
+    assert set((changed // (L.block_bytes * H)).tolist()) <= pages
