@@ -259,9 +259,12 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(const __grid_consta
                 raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
             issue_q(nb, nhg, segk + 1);
         }
+        // Every warp waits for the segment's q copy, units here or not: that copy is issued
+        // only once every warp has released the buffer two segments back, so no warp can
+        // arrive on a qfree barrier while the phase of two segments back is still open.
+        if (!failed && !__all_sync(0xffffffffu, mbar_wait(qbar0 + 8 * (segk & 1), (segk >> 1) & 1, kWaitLimitNs)))
+            fail_here();
         if (cnt > 0) {
-            if (!failed && !__all_sync(0xffffffffu, mbar_wait(qbar0 + 8 * (segk & 1), (segk >> 1) & 1, kWaitLimitNs)))
-                fail_here();
             const __half* qseg = qbuf + (segk & 1) * 8 * D;
 #pragma unroll
             for (int s = 0; s < R; ++s) {

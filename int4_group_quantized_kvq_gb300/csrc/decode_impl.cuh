@@ -744,6 +744,16 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                 raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
             issue_q(nb, nhg, segk + 1);
         }
+        // Every warp waits for the segment's q copy, units here or not: that copy is issued
+        // only once every warp has released the buffer two segments back, so no warp can
+        // arrive on a qfree barrier while the phase of two segments back is still open.
+        if (!failed && !__all_sync(0xffffffffu, mbar_wait(qbar0 + 8 * (segk & 1), (segk >> 1) & 1, kWaitLimitNs))) {
+            if (lane == 0) raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
+            failed = true;
+            f_st = cst;
+            f_par = cpar;
+            f_out = issued - consumed;
+        }
         if (cnt > 0) {
             // new (sequence, head group): q fragments and a fresh softmax state
             if constexpr (WIN) {
@@ -756,13 +766,6 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
             apg_seg = -1;
             if (aps[b] >= 0 && (WIN ? span_index(sspan, aps[b] >> p.lg_p) >= 0 : (aps[b] >> p.lg_p) < np))
                 apg_seg = aps[b] >> p.lg_p;
-            if (!failed && !__all_sync(0xffffffffu, mbar_wait(qbar0 + 8 * (segk & 1), (segk >> 1) & 1, kWaitLimitNs))) {
-                if (lane == 0) raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
-                failed = true;
-                f_st = cst;
-                f_par = cpar;
-                f_out = issued - consumed;
-            }
             const __half* qseg = qbuf + (segk & 1) * 8 * D;
 #pragma unroll
             for (int t = 0; t < NTQ; ++t) {

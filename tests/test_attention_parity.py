@@ -127,3 +127,16 @@ def test_workspace_reused_across_shapes_without_clearing(kvq):
         got, flags = gpu_decode(kvq, case, torch.from_numpy(pool_np).cuda(), ws=ws)
         assert flags == 0
         assert_attention_close(got, ref, what=f"reused workspace B{case.B}")
+
+
+def test_many_one_page_segments_per_cta(kvq):
+    # thousands of sequences of at most one page: a CTA's slice crosses dozens of segments
+    # and three of its four warps hold no unit of a given segment.  Those warps must not
+    # run two segments ahead on the double-buffered q barriers (a wait that timed out and a
+    # flagged, wrong result before the fix)
+    rng = np.random.default_rng(25)
+    case = Case(2100, 32, 16, 128, rng.integers(0, 7, size=2100).tolist(), seed=25, device="cuda")
+    pool_np = case.oracle_pool()
+    got, flags = gpu_decode(kvq, case, torch.from_numpy(pool_np).cuda())
+    assert flags == 0
+    assert_attention_close(got, case.oracle_attention(pool_np), what="B2100")

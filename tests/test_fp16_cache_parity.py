@@ -136,3 +136,16 @@ def test_dequantize_then_attend(kvq, Hq, Hkv):
     kvq.kvq_fp16_decode_attention(cfg, pool16, case.q.cuda(), bt, sl, max(case.lens), case.scale, out, ws)
     assert kvq.kvq_read_status(ws) == 0
     assert_attention_close(out.cpu().numpy(), ref, what="dequantize then attend")
+
+
+def test_fp16_many_one_page_segments_per_cta(kvq):
+    # the FP16 kernel's q barriers: thousands of one-page sequences, most warps without a unit
+    # in a given segment (they must not run two segments ahead)
+    rng = np.random.default_rng(27)
+    case = Case(2100, 32, 16, 128, rng.integers(0, 7, size=2100).tolist(), seed=27, device="cuda")
+    pool16 = _fp16_pool(case)
+    got, flags = _gpu_fp16_attention(kvq, case, pool16)
+    assert flags == 0
+    ref = oracle.fp16_decode_attention(case.layout, pool16, case.q.numpy(), case.block_table.numpy(),
+                                       np.array(case.lens, np.int32), case.scale)
+    assert_attention_close(got, ref, what="fp16 B2100")
