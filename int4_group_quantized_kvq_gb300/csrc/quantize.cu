@@ -28,22 +28,25 @@ constexpr float kInv7 = 0.142857149f;  // 0x3E124925
 // The 16 values a lane holds (row values 16 tl .. 16 tl + 15, inside one group) as 16
 // nibbles (code + 8, element 2j low), low word first, and the group's fp16 scale.  The
 // codes are those of quant_lane8 (kvq_quant.cuh, which the decode step's fused append
-// uses), computed with fewer instructions for the common case:
-//  * y = x * rcp(s) plus 1.5 * 2^23 + 8 rounds y + 8 to an integer, ties to even (8 is
-//    even), whose low four bits are the nibble whenever the code needs no clamp;
-//  * a lane takes the slower path of quant_lane8's arithmetic (the exact half-integer
-//    check and the clamp) for all its values when one of them lies within 2^-16 of a
-//    half-integer or the group's largest |y| exceeds 7.49.  The band is safe: y is
-//    within 2^-17.6 of the quotient q for |q| < 16 (kvq_quant.cuh), and q is either a
-//    half-integer or more than 2^-13 from every one, so outside the band y and q round
-//    alike; and it is narrow, so a warp's 512 values rarely send it down the slower path
-//    (a 2^-10 band did for most warps);
-//  * a NaN input makes its |y - round(y)| NaN, and an infinite scale (from an infinite
-//    input) makes that input's y = inf * 0 = NaN, so both reach the slower path through
-//    the same test (written to hold for NaN); there they take the IEEE division, as in
-//    quant_lane8;
-//  * nibbles are paired into bytes by one shift and one bit select, and four bytes
-//    gathered into a word by three byte permutes.
+// uses), computed with fewer instructions for the common case.  With rs = rcp(s), within
+// 2 ulp of 1/s, the exact product p = x rs is within |q| 2^-23 < 2^-19 of the quotient
+// q = x / s for |q| < 16 (kvq_quant.cuh shows the quotient stays below 16).
+//  * m = fma(x, rs, 1.5 * 2^23 + 8) rounds p + 8 to an integer once, ties to even (8 is
+//    even), so r = m - (1.5 * 2^23 + 8) is the integer nearest p, and the low four bits of
+//    m's bit pattern are the nibble r + 8 whenever the code needs no clamp;
+//  * e = fma(x, rs, -r) is p - r rounded once (|p - r| <= 1/2, so within 2^-26).  When
+//    |e| <= 1/2 - 2^-16 for all of the lane's values, q is within 1/2 - 2^-16 + 2^-26 +
+//    2^-19 < 1/2 of r, so r is the nearest integer to q and no tie is possible; otherwise
+//    (or when the group's largest |p| may exceed 7.49 and a clamp is possible) the lane takes
+//    the slower path of quant_lane8's arithmetic, the exact half-integer check and the clamp,
+//    for all its values.  The band is narrow: a warp's 512 values rarely send it there;
+//  * a NaN input makes its e NaN, and an infinite scale (from an infinite input) makes that
+//    input's e = inf * 0 = NaN, so both reach the slower path through the same test
+//    (written to hold for NaN); there they take the IEEE division, as in quant_lane8;
+//  * on the fast path a nibble n = r + 8 is in [1, 15] and m's bit pattern is 0x4B4000 << 8
+//    | n: bits 4 .. 21 are zero.  So m0 + 16 m1 holds the byte of two nibbles in its low 8
+//    bits with zeros above up to bit 21, b0 + 256 b1 holds two such bytes in its low 16 bits,
+//    and one byte permute joins two of those into the word (shift-adds, no masks).
 // LPR lanes hold a row; a group spans 1 << lg16 lanes.
 template <int LPR>
 __device__ __forceinline__ uint2 quant_lane16(const uint4 (&raw)[2], int lg16, __half& scale_out) {
@@ -73,17 +76,23 @@ __device__ __forceinline__ uint2 quant_lane16(const uint4 (&raw)[2], int lg16, _
     constexpr float kMagic8 = 12582920.0f;  // 1.5 * 2^23 + 8
     constexpr float kBand = 0.4999847412109375f;  // 1/2 - 2^-16
     bool slow = amax * rs > 7.49f;
-    uint32_t byt[8];  // byte j (low 8 bits): the nibbles of values 2j and 2j + 1
+    uint32_t m[16];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float y0 = x[2 * j] * rs, y1 = x[2 * j + 1] * rs;
-        const float m0 = y0 + kMagic8, m1 = y1 + kMagic8;
-        slow |= !(fabsf(y0 - (m0 - kMagic8)) <= kBand);
-        slow |= !(fabsf(y1 - (m1 - kMagic8)) <= kBand);
-        byt[j] = (__float_as_uint(m0) & 0xFu) | ((__float_as_uint(m1) << 4) & ~0xFu);
+    for (int i = 0; i < 16; ++i) {
+        const float mi = fmaf(x[i], rs, kMagic8);
+        const float e = fmaf(x[i], rs, kMagic8 - mi);  // kMagic8 - mi = -r exactly
+        slow |= !(fabsf(e) <= kBand);
+        m[i] = __float_as_uint(mi);
     }
-    uint32_t lo = prmt(prmt(byt[0], byt[1], 0x0040u), prmt(byt[2], byt[3], 0x0040u), 0x5410u);
-    uint32_t hi = prmt(prmt(byt[4], byt[5], 0x0040u), prmt(byt[6], byt[7], 0x0040u), 0x5410u);
+    uint32_t h[4];  // h[k]: the nibbles of values 4k .. 4k + 3 in its low 16 bits
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t b0 = m[4 * k] + 16u * m[4 * k + 1];
+        const uint32_t b1 = m[4 * k + 2] + 16u * m[4 * k + 3];
+        h[k] = b0 + 256u * b1;
+    }
+    uint32_t lo = prmt(h[0], h[1], 0x5410u);
+    uint32_t hi = prmt(h[2], h[3], 0x5410u);
     if (slow) {
         bool plain = isinf(s);
 #pragma unroll
@@ -135,11 +144,12 @@ __device__ __forceinline__ unsigned long long row_dest(const QuantizeArgs& a, ui
 // (K and V of a row adjacent), held by a team of LPR = D / 16 lanes, 16 values a lane.
 // Lane l of the warp first works out where row l of the block goes (one block-table
 // lookup per row, shared by its K and V jobs and by the lanes of their teams through
-// shuffles), then the warp quantizes the block's 64 jobs TEAMS * U at a time, loading
-// all U x 32 bytes per lane before it computes, so enough loads are in flight to stream
-// from HBM.  The block loop is grid-strided over one wave of resident CTAs.
-template <int D, int U>
-__global__ void __launch_bounds__(256, 4) quantize_append_kernel(QuantizeArgs a) {
+// shuffles), then the warp quantizes the block's 64 jobs TEAMS * U at a time.  A pass's
+// fp16 rows are loaded (all U x 32 bytes per lane) before it computes, and with PF the
+// next pass's rows are loaded before this pass computes, so enough loads are in flight to
+// stream from HBM.  The block loop is grid-strided over one wave of resident CTAs.
+template <int D, int U, bool PF, int MINB>
+__global__ void __launch_bounds__(256, MINB) quantize_append_kernel(QuantizeArgs a) {
     // A decode launched behind this kernel may start its own set-up now; it waits for this
     // grid to finish before it reads the pool.  This kernel itself may start before the
     // kernel ahead of it (a decode that reads the pool) has finished: it waits for it
@@ -156,23 +166,33 @@ __global__ void __launch_bounds__(256, 4) quantize_append_kernel(QuantizeArgs a)
     const uint32_t blocks = (a.rows + 31u) / 32u;
     const uint32_t warp_global = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const uint32_t warps_total = gridDim.x * blockDim.x / 32;
+    // the fp16 rows of pass ps of the block at row0
+    auto load = [&](uint32_t row0, int ps, uint4 (&raw)[U][2]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int jl = ps * JPP + u * TEAMS + team;  // job within the block
+            const uint32_t row = row0 + static_cast<uint32_t>(jl >> 1);
+            raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+            if (row < a.rows) {
+                const __half* src = ((jl & 1) ? a.v : a.k) + static_cast<size_t>(row) * D + tl * 16;
+                raw[u][0] = __ldcs(reinterpret_cast<const uint4*>(src));  // read once: stream past the caches
+                raw[u][1] = __ldcs(reinterpret_cast<const uint4*>(src) + 1);
+            }
+        }
+    };
     for (uint32_t blk = warp_global; blk < blocks; blk += warps_total) {
         const uint32_t row0 = blk * 32u;
         int my_slot = 0;
         const unsigned long long my_dst = row0 + lane < a.rows ? row_dest(a, row0 + lane, my_slot) : 0ull;
+        uint4 raw[U][2];
+        if (PF) load(row0, 0, raw);
 #pragma unroll 1
         for (int ps = 0; ps < PASSES; ++ps) {
-            uint4 raw[U][2];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int jl = ps * JPP + u * TEAMS + team;  // job within the block
-                const uint32_t row = row0 + static_cast<uint32_t>(jl >> 1);
-                raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
-                if (row < a.rows) {
-                    const __half* src = ((jl & 1) ? a.v : a.k) + static_cast<size_t>(row) * D + tl * 16;
-                    raw[u][0] = __ldcs(reinterpret_cast<const uint4*>(src));  // read once: stream past the caches
-                    raw[u][1] = __ldcs(reinterpret_cast<const uint4*>(src) + 1);
-                }
+            uint4 nxt[U][2];
+            if (PF) {
+                if (ps + 1 < PASSES) load(row0, ps + 1, nxt);
+            } else {
+                load(row0, ps, raw);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -193,17 +213,31 @@ __global__ void __launch_bounds__(256, 4) quantize_append_kernel(QuantizeArgs a)
                     reinterpret_cast<__half*>(scales)[tl >> lg] = s16;
                 }
             }
+            if (PF) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    raw[u][0] = nxt[u][0];
+                    raw[u][1] = nxt[u][1];
+                }
+            }
         }
     }
 }
 
+// The instance launched: jobs per lane per pass, next-pass prefetch, resident CTAs per SM
+// the register budget is set for.
+constexpr int kQuantU = 2;
+constexpr bool kQuantPrefetch = false;
+constexpr int kQuantMinBlocks = 3;
+
 // Resident 256-thread CTAs per SM of an instance, looked up once.
-template <int D, int U>
+template <int D>
 int quantize_ctas_per_sm() {
     static std::atomic<int> memo{0};
     int n = memo.load(std::memory_order_relaxed);
     if (n > 0) return n;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_append_kernel<D, U>, 256, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, quantize_append_kernel<D, kQuantU, kQuantPrefetch, kQuantMinBlocks>, 256, 0) != cudaSuccess ||
         n < 1) {
         cudaGetLastError();
         n = 1;
@@ -214,7 +248,6 @@ int quantize_ctas_per_sm() {
 
 template <int D>
 cudaError_t launch_q(const QuantizeArgs& a, cudaStream_t stream) {
-    constexpr int U = 2;
     const long long blocks32 = (static_cast<long long>(a.rows) + 31) / 32;
     if (blocks32 == 0) return cudaSuccess;
     constexpr int threads = 256;
@@ -222,7 +255,7 @@ cudaError_t launch_q(const QuantizeArgs& a, cudaStream_t stream) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long cap = static_cast<long long>(sms > 0 ? sms : 1) * quantize_ctas_per_sm<D, U>();
+    const long long cap = static_cast<long long>(sms > 0 ? sms : 1) * quantize_ctas_per_sm<D>();
     if (blocks > cap) blocks = cap;
     // programmatic dependent launch: the CTAs may become resident while the kernel ahead
     // drains; the kernel waits for it with griddepcontrol.wait before touching memory
@@ -236,7 +269,8 @@ cudaError_t launch_q(const QuantizeArgs& a, cudaStream_t stream) {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t err = cudaLaunchKernelEx(&cfg, quantize_append_kernel<D, U>, a);
+    const cudaError_t err =
+        cudaLaunchKernelEx(&cfg, quantize_append_kernel<D, kQuantU, kQuantPrefetch, kQuantMinBlocks>, a);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

@@ -45,6 +45,10 @@ def test_fp16_quotients_are_ties_or_clear_of_them():
     # the reciprocal-and-multiply error for |q| < 16 stays inside the gap to the band
     err = 16 * (2.0 ** -22 + 2.0 ** -24 + 2.0 ** -46)
     assert err < 2.0 ** -17.6 and err < 2.0 ** -16 and 2.0 ** -13 - err > 2.0 ** -16
+    # the quantize kernel's fused form: p = x * rcp(s) unrounded (rcp within 2 ulp) is within
+    # |q| 2^-23 < 2^-19 of q, and e = fma(x, rcp(s), -r) is p - r within 2^-26, so a fast-path
+    # value (|e| <= 1/2 - 2^-16) lies strictly nearer to r than 1/2: r is its code
+    assert 16 * 2.0 ** -23 <= 2.0 ** -19 and 0.5 - 2.0 ** -16 + 2.0 ** -26 + 2.0 ** -19 < 0.5
 
 
 def test_group_quotients_stay_below_16():
@@ -76,3 +80,19 @@ def test_scale_by_reciprocal_multiply_equals_the_division():
     # the fp32 results themselves do differ for some amax: the equality is a property of
     # the fp16 rounding, not of the fp32 arithmetic
     assert np.any((amax / np.float32(7.0)) != (amax * inv7))
+
+
+def test_nibble_packing_by_shift_adds():
+    # On the quantize kernel's fast path a nibble n in [1, 15] comes as the fp32 bit pattern of
+    # 1.5 * 2^23 + n, i.e. 0x4B400000 | n, with bits 4 .. 21 zero; the kernel joins four of them
+    # as (m0 + 16 m1) + 256 (m2 + 16 m3) modulo 2^32 and keeps the low 16 bits.  Every
+    # combination of four nibbles must land in place.
+    import itertools
+    import struct
+    pat = {n: struct.unpack("<I", struct.pack("<f", 12582912.0 + n))[0] for n in range(1, 16)}
+    assert all(pat[n] == (0x4B400000 | n) for n in pat)
+    for n0, n1, n2, n3 in itertools.product(range(1, 16), repeat=4):
+        b0 = (pat[n0] + 16 * pat[n1]) & 0xFFFFFFFF
+        b1 = (pat[n2] + 16 * pat[n3]) & 0xFFFFFFFF
+        h = (b0 + 256 * b1) & 0xFFFFFFFF
+        assert h & 0xFFFF == n0 | n1 << 4 | n2 << 8 | n3 << 12
