@@ -619,13 +619,15 @@ def run_kvq(args, world, rank, local):
         d2h = st0.out_host.numel() * 4
         e2e = {"value": world * n_e2e * step_bytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": t_e2e / n_e2e * 1e3,
-               "how": "HostPipeline: every step copies its q/K/V from pinned host memory (one H2D copy), runs the "
-                      "step (decode and combine launches) and copies its output to pinned host memory (one D2H "
-                      "copy); the copies run on their own streams, double-buffered, so step i+1's input copy and "
-                      "step i-1's output copy overlap step i's kernels; wall clock over all steps, synchronized "
-                      "at the end",
+               "how": "one kvq_decode_step_host_pipelined C-ABI call per step (HostPipeline): the call copies "
+                      "the step's q/K/V from pinned host memory (one H2D copy) on an input copy stream, runs the "
+                      "step (decode and combine launches) on the compute stream and copies its output to pinned "
+                      "host memory (one D2H copy) on an output copy stream; two staging slots alternate, so step "
+                      "i+1's input copy and step i-1's output copy overlap step i's kernels; wall clock over all "
+                      "steps, synchronized at the end",
                "serial": {"value": world * n_e2e * step_bytes / t_ser / 1e9, "ms_per_step": t_ser / n_e2e * 1e3,
-                          "how": "PagedKVCache.decode_step_host: copy in, step, copy out on one stream"}}
+                          "how": "one kvq_decode_step_host C-ABI call per step: copy in, step, copy out on one "
+                                 "stream"}}
 
     if rank != 0:
         return None

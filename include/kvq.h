@@ -60,9 +60,11 @@
 extern "C" {
 #endif
 
-/* A cudaStream_t, declared without the CUDA headers. */
+/* A cudaStream_t and a cudaEvent_t, declared without the CUDA headers. */
 struct CUstream_st;
 typedef struct CUstream_st *kvq_stream_t;
+struct CUevent_st;
+typedef struct CUevent_st *kvq_event_t;
 
 /* Cache geometry, shared by all calls on one pool. */
 typedef struct {
@@ -225,6 +227,34 @@ int kvq_decode_step_host(const kvq_cache_config *cfg, void *pool, const void *ho
                          kvq_stream_t stream);
 
 /*
+ * kvq_decode_step_host with its copies taken off the compute stream, so that from one call
+ * to the next the input copy of step i + 1 and the output copy of step i - 1 run while
+ * step i computes (the decode step of section 1.1 of the 4-bit page, fed from the host).
+ * The caller keeps two (or more) staging slots, each its own host_in, dev_in, out,
+ * host_out and three events, and gives consecutive calls alternate slots.  Per call:
+ *   copy_in   waits for events[1] (the step that last read this slot's dev_in), copies
+ *             host_in to dev_in, records events[0];
+ *   stream    waits for events[0] and events[2] (the output copy that last read this
+ *             slot's out), runs the step (as kvq_decode_step), records events[1];
+ *   copy_out  waits for events[1], copies out to host_out, records events[2].
+ *   stream, copy_in, copy_out  three distinct streams of the device.
+ *   events    the slot's three cudaEvent_t, created by the caller (an event never recorded
+ *             counts as complete, so a fresh slot needs no set-up); host_out holds the
+ *             step's output once events[2] completes, and host_in may be refilled once
+ *             events[0] completes.
+ *   other arguments as in kvq_decode_step_host.  Steps run in call order on `stream` and
+ *   share the workspace.
+ * Nothing is allocated and nothing waits on the host.
+ * Returns as kvq_decode_step.
+ */
+int kvq_decode_step_host_pipelined(const kvq_cache_config *cfg, void *pool, const void *host_in, void *dev_in,
+                                   const int32_t *append_pos, const int32_t *block_table, int32_t max_blocks,
+                                   const int32_t *seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len,
+                                   float softmax_scale, float *out, void *host_out, void *workspace,
+                                   size_t workspace_bytes, kvq_stream_t stream, kvq_stream_t copy_in,
+                                   kvq_stream_t copy_out, kvq_event_t events[3]);
+
+/*
  * Decode attention and the decode step with a sliding window and sink tokens
  * (SlidingWindowAttention, section 3.2 of the KV-cache optimisation page): the query,
  * at the last position L - 1 of its sequence, attends to positions
@@ -384,7 +414,10 @@ int kvq_mixed_decode_attention(const kvq_cache_config *cfg, const void *pool, co
  * the scratch lives in an 8 MiB array built into the library, which every GPU that
  * loads the library holds until the process exits.  No cudaMalloc, cudaFree or other
  * allocating call is made.
- *   status   device uint32 or NULL: receives this call's status flags.
+ *   status   device uint32 or NULL: receives this call's status flags, overwriting what
+ *            it held (unlike the other calls, which OR flags into their status word).
+ * The array used is the current device's: the stream and every buffer must belong to
+ * the current device (a q pointer on another device is rejected with KVQ_EINVAL).
  * The first call on a device looks up the array's address on that device; make that
  * first call before any stream capture.  All calls on a device share the array, so
  * calls whose work overlaps on the GPU (other streams or threads) race: serialize them.
@@ -396,6 +429,23 @@ int kvq_decode_attention_noalloc(const kvq_cache_config *cfg, const void *pool, 
                                  const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
                                  int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
                                  float *out, uint32_t *status, kvq_stream_t stream);
+
+/*
+ * A test of the decode kernel's bounded waits, for the test suite: kvq_decode_attention
+ * (same arguments) with every wait on a copy bounded by wait_limit_ns (in [1 us, 10 ms])
+ * instead of 250 ms, and each warp's first page copy announced to its mbarrier as 16
+ * bytes larger than it is, so the wait for it runs out.  The kernel then raises
+ * KVQ_FLAG_WAIT_TIMEOUT in the workspace status word, stops waiting, writes empty partial
+ * results (out is not the attention) and, before it leaves, completes the short phase
+ * with a 16-byte copy of its own and waits for every copy it issued.  Nothing faults or
+ * hangs; later calls run normally.  (No passage of the pages has a counterpart.)
+ * Returns as kvq_decode_attention, or KVQ_EINVAL for a limit outside the range.
+ */
+int kvq_test_decode_wait_timeout(const kvq_cache_config *cfg, const void *pool, const void *q,
+                                 const int32_t *block_table, int32_t max_blocks, const int32_t *seq_lens,
+                                 int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
+                                 float *out, void *workspace, size_t workspace_bytes, uint64_t wait_limit_ns,
+                                 kvq_stream_t stream);
 
 /*
  * Dequantize positions [start, start + n) of sequence b (section 2.1 of the 4-bit

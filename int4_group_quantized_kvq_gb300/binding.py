@@ -27,7 +27,8 @@ ABI_SYMBOLS = ("kvq_block_bytes", "kvq_pool_bytes", "kvq_quantize_append", "kvq_
                "kvq_mixed_decode_attention", "kvq_int8_pool_bytes", "kvq_int8_quantize_append",
                "kvq_int8_decode_workspace_bytes", "kvq_int8_decode_attention", "kvq_wht4_codebook",
                "kvq_wht4_pool_bytes", "kvq_wht4_quantize_append", "kvq_wht4_dequantize",
-               "kvq_wht4_decode_workspace_bytes", "kvq_wht4_decode_attention", "kvq_decode_step_host")
+               "kvq_wht4_decode_workspace_bytes", "kvq_wht4_decode_attention", "kvq_decode_step_host",
+               "kvq_decode_step_host_pipelined", "kvq_test_decode_wait_timeout")
 
 
 class KvqError(RuntimeError):
@@ -107,6 +108,12 @@ def lib() -> C.CDLL:
         L.kvq_int8_decode_attention.restype = C.c_int
         L.kvq_decode_step_host.argtypes = [cfgp, P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, P, SZ, P]
         L.kvq_decode_step_host.restype = C.c_int
+        L.kvq_decode_step_host_pipelined.argtypes = [cfgp, P, P, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, P,
+                                                     SZ, P, P, P, C.POINTER(C.c_void_p)]
+        L.kvq_decode_step_host_pipelined.restype = C.c_int
+        L.kvq_test_decode_wait_timeout.argtypes = [cfgp, P, P, P, I32, P, I32, I32, I32, C.c_float, P, P, SZ,
+                                                   C.c_uint64, P]
+        L.kvq_test_decode_wait_timeout.restype = C.c_int
         L.kvq_wht4_codebook.argtypes = [P, P]
         L.kvq_wht4_codebook.restype = None
         L.kvq_wht4_pool_bytes.argtypes = [cfgp]
@@ -538,4 +545,46 @@ def kvq_decode_step_host(cfg: CacheConfig, pool: torch.Tensor, host_in: torch.Te
         int(block_table.shape[1]), _dev(seq_lens, "seq_lens", torch.int32), int(batch), int(num_q_heads),
         int(max_len), float(softmax_scale), _dev(out, "out", torch.float32), host_out.data_ptr(),
         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(rc)
+
+
+def kvq_decode_step_host_pipelined(cfg: CacheConfig, pool: torch.Tensor, host_in: torch.Tensor, dev_in: torch.Tensor,
+                                   append_pos: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                                   batch: int, num_q_heads: int, max_len: int, softmax_scale: float, out: torch.Tensor,
+                                   host_out: torch.Tensor, workspace: torch.Tensor, stream, copy_in, copy_out,
+                                   events) -> None:
+    """kvq_decode_step_host with its copies on copy_in / copy_out: events are the staging slot's three
+    torch.cuda.Event objects (input copied, step done, output copied), each recorded at least once so
+    that it exists."""
+    if host_in.is_cuda or host_out.is_cuda:
+        raise ValueError("host_in and host_out must be host tensors")
+    if host_in.dtype != torch.float16 or host_out.dtype != torch.float32:
+        raise ValueError("host_in must be float16 and host_out float32")
+    if host_in.numel() != dev_in.numel() or host_out.numel() != out.numel():
+        raise ValueError("host and device buffers differ in size")
+    handles = (C.c_void_p * 3)(*[int(ev.cuda_event) for ev in events])
+    if not all(handles):
+        raise ValueError("each event must have been recorded once (torch creates events on first record)")
+    rc = lib().kvq_decode_step_host_pipelined(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), host_in.data_ptr(), _dev(dev_in, "dev_in", torch.float16),
+        _dev(append_pos, "append_pos", torch.int32), _dev(block_table, "block_table", torch.int32),
+        int(block_table.shape[1]), _dev(seq_lens, "seq_lens", torch.int32), int(batch), int(num_q_heads),
+        int(max_len), float(softmax_scale), _dev(out, "out", torch.float32), host_out.data_ptr(),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream), _stream(copy_in),
+        _stream(copy_out), handles)
+    _check(rc)
+
+
+def kvq_test_decode_wait_timeout(cfg: CacheConfig, pool: torch.Tensor, q: torch.Tensor, block_table: torch.Tensor,
+                                 seq_lens: torch.Tensor, max_len: int, softmax_scale: float, out: torch.Tensor,
+                                 workspace: torch.Tensor, wait_limit_ns: int, stream=None) -> None:
+    """The bounded-wait test of the decode kernel (the test suite's): its waits run out and it
+    raises KVQ_FLAG_WAIT_TIMEOUT in the workspace status word."""
+    B, Hq = int(q.shape[0]), int(q.shape[1])
+    rc = lib().kvq_test_decode_wait_timeout(
+        C.byref(cfg), _dev(pool, "pool", torch.uint8), _dev(q, "q", torch.float16),
+        _dev(block_table, "block_table", torch.int32), int(block_table.shape[1]),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, int(max_len), float(softmax_scale),
+        _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        int(wait_limit_ns), _stream(stream))
     _check(rc)

@@ -10,9 +10,10 @@ nothing) around the C ABI calls of a decode step:
 With ``window > 0`` the attention is restricted to the last ``window`` positions and
 the first ``sinks`` (``kvq_decode_attention_window`` / ``kvq_decode_step_window``).
 
-``decode_step_host`` is the same step driven from pinned host buffers (``HostStaging``):
-the step's q, K and V are copied in with one transfer and the output copied back, on
-the same stream.
+``decode_step_host`` is the same step driven from pinned host buffers (``HostStaging``)
+in one kvq_decode_step_host call: the step's q, K and V are copied in with one transfer
+and the output copied back, on the same stream; ``HostPipeline`` overlaps those copies
+with the neighbouring steps (kvq_decode_step_host_pipelined).
 """
 from __future__ import annotations
 
@@ -76,14 +77,14 @@ class PagedKVCache:
         self.attend(q, seq_lens, out, stream)
 
     def decode_step_host(self, staging: "HostStaging", append_pos, seq_lens, stream=None) -> None:
-        """The decode step from pinned host memory: one H2D copy of the step's q, K and V (staged
-        back to back), the step (the decode and combine launches), one D2H copy of the output.
-        All asynchronous on the step's stream.  (kvq_decode_step_host does the same in one C call.)"""
-        s = torch.cuda.current_stream() if stream is None else stream
-        with torch.cuda.stream(s):
-            staging.dev.copy_(staging.host, non_blocking=True)
-            self.decode_step(staging.q, staging.k_new, staging.v_new, append_pos, seq_lens, staging.out, stream=s)
-            staging.out_host.copy_(staging.out, non_blocking=True)
+        """The decode step from pinned host memory in one kvq_decode_step_host call: one H2D copy of
+        the step's q, K and V (staged back to back), the step, one D2H copy of the output, all
+        asynchronous on the step's stream."""
+        if self.window > 0:
+            raise ValueError("the host step attends to every position (no window)")
+        B.kvq_decode_step_host(self.cfg, self.pool, staging.host, staging.dev, append_pos, self.block_table, seq_lens,
+                               self.batch, self.num_q_heads, self.max_len, self.softmax_scale, staging.out,
+                               staging.out_host, self.workspace, stream=stream)
 
     def flags(self) -> int:
         """Status flags of the last calls (synchronizes)."""
@@ -114,17 +115,19 @@ class HostStaging:
 
 
 class HostPipeline:
-    """Decode steps fed from pinned host memory with the copies overlapped with the kernels.
+    """Decode steps fed from pinned host memory with the copies overlapped with the kernels:
+    one kvq_decode_step_host_pipelined call per step.
 
     Two staging slots alternate.  Step i (slot i % 2) copies its inputs host-to-device on an
     input copy stream, runs on the compute stream once that copy is done, and copies its
     output device-to-host on an output copy stream once the step is done; so step i + 1's
     inputs move while step i computes, and step i's output moves while step i + 1 computes.
-    Events keep each slot's device buffers from being overwritten while in use: a slot's
-    input copy waits for the step two back to have read that slot, and its step waits for
-    that step's output copy to have left the slot.  The host side is the caller's: fill
-    `slot(i)`'s host inputs before `step(i)` (for i >= 2, after `inputs_copied(i - 2)`),
-    and read its `out_host` after `done(i)` and before `step(i + 2)`."""
+    The slot's three events (input copied, step done, output copied) keep its device buffers
+    from being overwritten while in use: a slot's input copy waits for the step two back to
+    have read that slot, and its step waits for that step's output copy to have left the slot.
+    The host side is the caller's: fill `slot(i)`'s host inputs before `step(i)` (for i >= 2,
+    after `inputs_copied(i - 2)`), and read its `out_host` after `done(i)` and before
+    `step(i + 2)`."""
 
     def __init__(self, cache: PagedKVCache, compute_stream=None):
         self.cache = cache
@@ -134,10 +137,12 @@ class HostPipeline:
         self.compute = torch.cuda.Stream(device=dev) if compute_stream is None else compute_stream
         self.copy_in = torch.cuda.Stream(device=dev)
         self.copy_out = torch.cuda.Stream(device=dev)
-        self.ev_in = [torch.cuda.Event() for _ in range(2)]
-        self.ev_step = [torch.cuda.Event() for _ in range(2)]
-        self.ev_out = [torch.cuda.Event() for _ in range(2)]
-        self.started = [False, False]
+        # per slot: input copied, step done, output copied; recorded once so that they exist
+        self.events = [[torch.cuda.Event() for _ in range(3)] for _ in range(2)]
+        for evs in self.events:
+            for ev in evs:
+                ev.record(self.compute)
+        self.compute.synchronize()
 
     def slot(self, i: int) -> HostStaging:
         return self.slots[i % 2]
@@ -145,31 +150,21 @@ class HostPipeline:
     def step(self, i: int, append_pos: torch.Tensor, seq_lens: torch.Tensor, cache: PagedKVCache | None = None) -> None:
         """Step i on `cache` (default: the pipeline's), from slot(i)'s host inputs to its out_host."""
         cache = self.cache if cache is None else cache
-        k = i % 2
-        st = self.slots[k]
-        if self.started[k]:
-            self.copy_in.wait_event(self.ev_step[k])   # step i - 2 has read this slot's inputs
-        with torch.cuda.stream(self.copy_in):
-            st.dev.copy_(st.host, non_blocking=True)
-            self.ev_in[k].record(self.copy_in)
-        self.compute.wait_event(self.ev_in[k])
-        if self.started[k]:
-            self.compute.wait_event(self.ev_out[k])   # step i - 2's output has left this slot
-        cache.decode_step(st.q, st.k_new, st.v_new, append_pos, seq_lens, st.out, stream=self.compute)
-        self.ev_step[k].record(self.compute)
-        self.copy_out.wait_event(self.ev_step[k])
-        with torch.cuda.stream(self.copy_out):
-            st.out_host.copy_(st.out, non_blocking=True)
-            self.ev_out[k].record(self.copy_out)
-        self.started[k] = True
+        st = self.slots[i % 2]
+        if cache.window > 0:
+            raise ValueError("the pipelined host step attends to every position (no window)")
+        B.kvq_decode_step_host_pipelined(cache.cfg, cache.pool, st.host, st.dev, append_pos, cache.block_table,
+                                         seq_lens, cache.batch, cache.num_q_heads, cache.max_len,
+                                         cache.softmax_scale, st.out, st.out_host, cache.workspace, self.compute,
+                                         self.copy_in, self.copy_out, self.events[i % 2])
 
     def inputs_copied(self, i: int) -> torch.cuda.Event:
         """The event after which step i's host inputs have been read (slot(i) may be refilled)."""
-        return self.ev_in[i % 2]
+        return self.events[i % 2][0]
 
     def done(self, i: int) -> torch.cuda.Event:
         """The event after which step i's output is in slot(i).out_host (until step i + 2 is issued)."""
-        return self.ev_out[i % 2]
+        return self.events[i % 2][2]
 
     def synchronize(self) -> None:
         for s in (self.copy_in, self.compute, self.copy_out):

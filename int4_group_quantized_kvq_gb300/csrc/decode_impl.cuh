@@ -113,6 +113,11 @@ struct KParams {
     // positions attended: seq_lens[b] - len_sub (the INT4 part of the mixed-precision decode
     // stops len_sub positions short of the sequence's end; 0 otherwise)
     int32_t len_sub;
+    // bound of every wait on a copy, in ns; and a test of that bound: with withhold > 0 each
+    // warp announces its first page copy as `withhold` bytes larger than it is, so the wait
+    // for it runs out
+    uint64_t wait_ns;
+    uint32_t withhold;
 };
 
 // a / b for a >= 0, b > 0, with 32-bit division when both fit (the usual case).
@@ -440,6 +445,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     orphan_appends();
     {
         const int pro = nm < stages ? nm : stages;
+        if (p.withhold != 0 && lane == 0 && pro > 0) mbar_expect_tx(bar0, p.withhold);  // before the copy is issued
         for (int k = 0; k < pro; ++k) issue(k, k);
     }
 
@@ -702,6 +708,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     bool failed = false;  // a copy did not arrive in time: stop waiting, keep the barriers
     int f_st = 0, f_out = 0;  // where consumption stopped, and the copies still in flight then
     uint32_t f_par = 0;
+    int f_consumed = 0;   // units consumed when it stopped
     const bool p16 = p.P == 16;
 
     // q rows of a segment go to shared memory by a bulk copy issued one segment ahead
@@ -740,19 +747,20 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         if (threadIdx.x == 0 && sfirst + np < c1) {
             int nb = b, nhg = hg;
             next_seg(nb, nhg);
-            if (segk >= 1 && !mbar_wait(qfree0 + 8 * ((segk - 1) & 1), ((segk - 1) >> 1) & 1, kWaitLimitNs))
+            if (segk >= 1 && !mbar_wait(qfree0 + 8 * ((segk - 1) & 1), ((segk - 1) >> 1) & 1, p.wait_ns))
                 raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
             issue_q(nb, nhg, segk + 1);
         }
         // Every warp waits for the segment's q copy, units here or not: that copy is issued
         // only once every warp has released the buffer two segments back, so no warp can
         // arrive on a qfree barrier while the phase of two segments back is still open.
-        if (!failed && !__all_sync(0xffffffffu, mbar_wait(qbar0 + 8 * (segk & 1), (segk >> 1) & 1, kWaitLimitNs))) {
+        if (!failed && !__all_sync(0xffffffffu, mbar_wait(qbar0 + 8 * (segk & 1), (segk >> 1) & 1, p.wait_ns))) {
             if (lane == 0) raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
             failed = true;
             f_st = cst;
             f_par = cpar;
             f_out = issued - consumed;
+            f_consumed = consumed;
         }
         if (cnt > 0) {
             // new (sequence, head group): q fragments and a fresh softmax state
@@ -811,14 +819,15 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                 par1 ^= 1u;
             }
             if (!failed) {
-                bool ok = mbar_wait(bar0 + 8 * cst, cpar, kWaitLimitNs);
-                if (n == 2) ok = ok && mbar_wait(bar0 + 8 * st1, par1, kWaitLimitNs);
+                bool ok = mbar_wait(bar0 + 8 * cst, cpar, p.wait_ns);
+                if (n == 2) ok = ok && mbar_wait(bar0 + 8 * st1, par1, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     if (lane == 0) raise_flag(p.status, KVQ_FLAG_WAIT_TIMEOUT);
                     failed = true;
                     f_st = cst;
                     f_par = cpar;
                     f_out = issued - consumed;
+                    f_consumed = consumed;
                 }
             }
             if (!failed) {
@@ -965,14 +974,18 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     // wait failed) ----
     if (threadIdx.x == 0) {
         for (int k = segk - 2; k < segk; ++k)
-            if (k >= 0) mbar_wait(qbar0 + 8 * (k & 1), (k >> 1) & 1, kWaitLimitNs);
+            if (k >= 0) mbar_wait(qbar0 + 8 * (k & 1), (k >> 1) & 1, p.wait_ns);
     }
     // ---- after a failed wait: let the copies already issued land before leaving ----
     if (failed) {
+        // the withheld bytes of the first copy's phase, as a 16-byte copy of its own, so that
+        // the phase completes once both copies have landed
+        if (p.withhold != 0 && f_consumed == 0 && f_out > 0 && lane == 0)
+            bulk_g2s(ring0, p.pool, p.withhold, bar0);
         int st = f_st;
         uint32_t par = f_par;
         for (int k = 0; k < f_out; ++k) {
-            mbar_wait(bar0 + 8 * st, par, kWaitLimitNs);
+            mbar_wait(bar0 + 8 * st, par, p.wait_ns);
             if (++st == stages) {
                 st = 0;
                 par ^= 1u;
@@ -1034,6 +1047,8 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     p.ws_pre = reinterpret_cast<int32_t*>(a.workspace + plan.ws_pre_offset);
     p.status = a.status ? a.status : reinterpret_cast<uint32_t*>(a.workspace);
     p.len_sub = a.len_sub;
+    p.wait_ns = a.wait_ns != 0 ? a.wait_ns : kWaitLimitNs;
+    p.withhold = a.withhold_first_copy ? 16u : 0u;
     p.B = a.B;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;

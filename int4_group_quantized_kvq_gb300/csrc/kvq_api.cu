@@ -194,7 +194,8 @@ namespace {
 int decode_attention_impl(const kvq_cache_config* cfg, const void* pool, const void* q, const int32_t* block_table,
                           int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
                           int32_t max_len, float softmax_scale, int32_t window, int32_t sinks, float* out,
-                          void* workspace, size_t workspace_bytes, kvq_stream_t stream, int codec = 0) {
+                          void* workspace, size_t workspace_bytes, kvq_stream_t stream, int codec = 0,
+                          uint64_t test_wait_ns = 0) {
     if (int e = check_cfg(cfg)) return e;
     if (batch < 0 || num_q_heads < 1 || max_len < 0)
         return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
@@ -232,6 +233,10 @@ int decode_attention_impl(const kvq_cache_config* cfg, const void* pool, const v
     a.int8 = codec == 2;
     a.wht = codec == 3;
     a.L = kvq::block_layout(*cfg);
+    if (test_wait_ns != 0) {
+        a.wait_ns = test_wait_ns;
+        a.withhold_first_copy = true;
+    }
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
     if (e == cudaErrorInvalidValue) return fail(KVQ_EUNSUPPORTED, "no decode kernel for this shape");
@@ -308,6 +313,17 @@ int kvq_decode_attention(const kvq_cache_config* cfg, const void* pool, const vo
                                  softmax_scale, 0, 0, out, workspace, workspace_bytes, stream);
 }
 
+int kvq_test_decode_wait_timeout(const kvq_cache_config* cfg, const void* pool, const void* q,
+                                 const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                                 int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale, float* out,
+                                 void* workspace, size_t workspace_bytes, uint64_t wait_limit_ns,
+                                 kvq_stream_t stream) {
+    if (wait_limit_ns < 1000 || wait_limit_ns > 10000000)
+        return fail(KVQ_EINVAL, "wait_limit_ns %llu outside [1 us, 10 ms]", static_cast<unsigned long long>(wait_limit_ns));
+    return decode_attention_impl(cfg, pool, q, block_table, max_blocks, seq_lens, batch, num_q_heads, max_len,
+                                 softmax_scale, 0, 0, out, workspace, workspace_bytes, stream, 0, wait_limit_ns);
+}
+
 int kvq_decode_attention_window(const kvq_cache_config* cfg, const void* pool, const void* q,
                                 const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
                                 int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
@@ -373,6 +389,49 @@ int kvq_decode_step_host(const kvq_cache_config* cfg, void* pool, const void* ho
         return rc;
     e = cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step_host output copy");
+    return ok();
+}
+
+int kvq_decode_step_host_pipelined(const kvq_cache_config* cfg, void* pool, const void* host_in, void* dev_in,
+                                   const int32_t* append_pos, const int32_t* block_table, int32_t max_blocks,
+                                   const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len,
+                                   float softmax_scale, float* out, void* host_out, void* workspace,
+                                   size_t workspace_bytes, kvq_stream_t stream, kvq_stream_t copy_in,
+                                   kvq_stream_t copy_out, kvq_event_t events[3]) {
+    if (int e = check_cfg(cfg)) return e;
+    if (batch < 0 || num_q_heads < 1) return fail(KVQ_EINVAL, "batch %d, num_q_heads %d", batch, num_q_heads);
+    if (batch == 0) return ok();
+    if (!host_in || !dev_in || !host_out || !out || !events || !events[0] || !events[1] || !events[2])
+        return fail(KVQ_EINVAL, "NULL buffer or event");
+    if (!aligned(dev_in, 16)) return fail(KVQ_EINVAL, "dev_in must be 16-byte aligned");
+    if (stream == copy_in || stream == copy_out || copy_in == copy_out)
+        return fail(KVQ_EINVAL, "stream, copy_in and copy_out must be three distinct streams");
+    const size_t d = static_cast<size_t>(cfg->head_dim);
+    const size_t q_bytes = static_cast<size_t>(batch) * num_q_heads * d * 2;
+    const size_t kv_bytes = static_cast<size_t>(batch) * cfg->num_kv_heads * d * 2;
+    const size_t out_bytes = static_cast<size_t>(batch) * num_q_heads * d * 4;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const cudaStream_t ci = reinterpret_cast<cudaStream_t>(copy_in);
+    const cudaStream_t co = reinterpret_cast<cudaStream_t>(copy_out);
+    cudaEvent_t ev_in = reinterpret_cast<cudaEvent_t>(events[0]);
+    cudaEvent_t ev_step = reinterpret_cast<cudaEvent_t>(events[1]);
+    cudaEvent_t ev_out = reinterpret_cast<cudaEvent_t>(events[2]);
+    uint8_t* din = static_cast<uint8_t*>(dev_in);
+    cudaError_t e = cudaStreamWaitEvent(ci, ev_step, 0);  // the slot's last step has read dev_in
+    if (e == cudaSuccess) e = cudaMemcpyAsync(din, host_in, q_bytes + 2 * kv_bytes, cudaMemcpyHostToDevice, ci);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in, ci);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_in, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_out, 0);  // the slot's last output copy has read out
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step_host_pipelined input copy");
+    if (int rc = decode_step_impl(cfg, pool, din + q_bytes, din + q_bytes + kv_bytes, append_pos, din, block_table,
+                                  max_blocks, seq_lens, batch, num_q_heads, max_len, softmax_scale, 0, 0, out,
+                                  workspace, workspace_bytes, stream))
+        return rc;
+    e = cudaEventRecord(ev_step, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(co, ev_step, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, co);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out, co);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step_host_pipelined output copy");
     return ok();
 }
 
@@ -767,6 +826,22 @@ extern "C" int kvq_decode_attention_noalloc(const kvq_cache_config* cfg, const v
                     "this shape needs %zu bytes of scratch; the built-in scratch of kvq_decode_attention_noalloc "
                     "holds %zu bytes (use kvq_decode_attention with a workspace)",
                     plan.ws_bytes, kNoAllocScratchBytes);
+    // The scratch used is the current device's copy of the array: the arguments must live on
+    // that device (q stands for them), or the kernel would pair them with another GPU's array.
+    {
+        int cur = 0;
+        cudaPointerAttributes attr{};
+        e = cudaGetDevice(&cur);
+        if (e == cudaSuccess) e = cudaPointerGetAttributes(&attr, q);
+        if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention_noalloc device check");
+        if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+            return fail(KVQ_EINVAL, "kvq_decode_attention_noalloc: q is not device memory");
+        if (attr.device != cur)
+            return fail(KVQ_EINVAL,
+                        "kvq_decode_attention_noalloc: q is on device %d but device %d is current; make the device "
+                        "of the stream and the buffers current",
+                        attr.device, cur);
+    }
     void* scratch = nullptr;
     e = noalloc_scratch(&scratch);
     if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_attention_noalloc scratch lookup");

@@ -125,6 +125,10 @@ struct DecodeArgs {
     int32_t len_sub = 0;
     // status word (nullptr: the first word of the workspace)
     uint32_t* status = nullptr;
+    // bound of the INT4 kernel's waits on copies in ns (0: the default, 250 ms), and the test
+    // of that bound (each warp's first page copy announced 16 bytes larger than it is)
+    uint64_t wait_ns = 0;
+    bool withhold_first_copy = false;
 };
 
 // The FP16 cache of the latency comparison: block (page, kv head) holds K rows P x d fp16,

@@ -153,3 +153,14 @@ def test_codec_and_host_step_calls_reject_bad_arguments_on_host(built):
     assert "aligned" in kvq.kvq_last_error()
     assert L.kvq_decode_step_host(C.byref(cfg), None, None, None, None, None, 4, None, 0, 8, 10, 1.0, None, None,
                                   None, 0, None) == kvq.KVQ_OK
+    # the pipelined host-buffer step: missing events, streams that are not three distinct ones
+    ev = (C.c_void_p * 3)(0xA000, 0xB000, 0xC000)
+    no_ev = (C.c_void_p * 3)(0xA000, None, 0xC000)
+    args = (C.byref(cfg), 0x1000, 0x9000, 0x2000, 0x3000, 0x4000, 4, 0x5000, 2, 8, 10, 1.0, 0x6000, 0x7000, 0x8000,
+            1 << 20)
+    assert L.kvq_decode_step_host_pipelined(*args, 0x11, 0x22, 0x33, no_ev) == kvq.KVQ_EINVAL
+    assert L.kvq_decode_step_host_pipelined(*args, 0x11, 0x22, 0x22, ev) == kvq.KVQ_EINVAL
+    assert L.kvq_decode_step_host_pipelined(*args, 0x11, 0x11, 0x33, ev) == kvq.KVQ_EINVAL
+    assert "distinct" in kvq.kvq_last_error()
+    assert L.kvq_decode_step_host_pipelined(C.byref(cfg), None, None, None, None, None, 4, None, 0, 8, 10, 1.0, None,
+                                            None, None, 0, None, None, None, None) == kvq.KVQ_OK
