@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(256, MINB) quantize_append_kernel(QuantizeArgs
 // The instance launched: jobs per lane per pass, next-pass prefetch, resident CTAs per SM
 // the register budget is set for.
 constexpr int kQuantU = 2;
-constexpr bool kQuantPrefetch = false;
+constexpr bool kQuantPrefetch = true;
 constexpr int kQuantMinBlocks = 3;
 
 // Resident 256-thread CTAs per SM of an instance, looked up once.
