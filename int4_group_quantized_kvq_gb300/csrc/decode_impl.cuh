@@ -291,10 +291,14 @@ __device__ __noinline__ void append_rows(const KParams& p, const int32_t* aps, u
     }
 }
 
-template <int D, int GK, int GV, int HK, int HS, bool WIN>
+// P16: the pages hold 16 tokens (P == 16), so two one-head units, i.e. two pages, make a
+// step; the instances for larger pages (P16 false) take two 16-token chunks of one page.
+// Each instance carries only its own path, which keeps the loop's code small.
+template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16>
 __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_splitkv_kernel(KParams p) {
     static_assert(D == 128, "the fragment mapping below is written for head_dim 128");
     static_assert(HK == 1 || HS == 1, "several kv heads per unit only with one query head each");
+    static_assert(HK == 1 || P16, "four-head units only for 16-token pages");
     constexpr int NGK = D / GK;               // K groups per row
     constexpr int NGV = D / GV;               // V groups per row
     constexpr int KW = D / 32;                // K code words per thread per token row
@@ -709,7 +713,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     int f_st = 0, f_out = 0;  // where consumption stopped, and the copies still in flight then
     uint32_t f_par = 0;
     int f_consumed = 0;   // units consumed when it stopped
-    const bool p16 = p.P == 16;
+    constexpr bool p16 = P16;
 
     // q rows of a segment go to shared memory by a bulk copy issued one segment ahead
     // (thread 0); segment k of this CTA uses buffer k & 1 at phase (k >> 1) & 1
@@ -844,7 +848,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                 auto all_in = [&](int t, int w) { return t + w <= Leff && (!WIN || t >= wlo || t + w <= p.sinks); };
                 auto any_in = [&](int t, int w) { return !WIN || (min(t + w, Leff) > wlo || t < p.sinks); };
                 if constexpr (HK == 1) {
-                    if (p16) {
+                    if constexpr (P16) {
                         const int t0A = rA * 16, t0B = rB * 16;
                         const Step<TG> st = {{blkA, blkB}, {0, 0}, {t0A, t0B}, {true, n == 2}};
                         // (without a window, page B comes after page A, so B whole implies A whole)
@@ -996,11 +1000,11 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
 
 // Raise the kernel's dynamic shared-memory limit once to the largest size asked for,
 // so repeated calls (and calls under stream capture) only launch.
-template <int D, int GK, int GV, int HK, int HS, bool WIN>
+template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16>
 cudaError_t ensure_smem_attr(size_t smem) {
     static std::atomic<long long> granted{-1};
     if (static_cast<long long>(smem) <= granted.load(std::memory_order_acquire)) return cudaSuccess;
-    const cudaError_t err = cudaFuncSetAttribute(decode_splitkv_kernel<D, GK, GV, HK, HS, WIN>,
+    const cudaError_t err = cudaFuncSetAttribute(decode_splitkv_kernel<D, GK, GV, HK, HS, WIN, P16>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) cudaGetLastError();  // a refused size must not linger as the last error
     if (err == cudaSuccess) {
@@ -1013,7 +1017,7 @@ cudaError_t ensure_smem_attr(size_t smem) {
 
 // Resident CTAs per SM for a given shared-memory size, memoised per size (a few sizes
 // per shape are asked for; the slots fill once and later calls only read them).
-template <int D, int GK, int GV, int HK, int HS, bool WIN>
+template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16>
 int occupancy(size_t smem) {
     constexpr int kSlots = 32;
     static std::atomic<long long> memo[kSlots];  // (smem << 8) | ctas, 0 = empty
@@ -1022,9 +1026,9 @@ int occupancy(size_t smem) {
         if (m == 0) break;
         if ((m >> 8) == static_cast<long long>(smem)) return static_cast<int>(m & 0xff);
     }
-    if (ensure_smem_attr<D, GK, GV, HK, HS, WIN>(smem) != cudaSuccess) return 0;
+    if (ensure_smem_attr<D, GK, GV, HK, HS, WIN, P16>(smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN>, cta_warps<HS>() * 32,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN, P16>, cta_warps<HS>() * 32,
                                                       smem) != cudaSuccess)
         return 0;
     const long long entry = (static_cast<long long>(smem) << 8) | (n & 0xff);
@@ -1035,7 +1039,7 @@ int occupancy(size_t smem) {
     return n;
 }
 
-template <int D, int GK, int GV, int HK, int HS, bool WIN>
+template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16>
 cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     KParams p;
     p.pool = a.pool;
@@ -1077,7 +1081,7 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     while ((8 << p.lg_lk) < a.L.Gk) ++p.lg_lk;
     p.lg_lv = 0;
     while ((8 << p.lg_lv) < a.L.Gv) ++p.lg_lv;
-    cudaError_t err = ensure_smem_attr<D, GK, GV, HK, HS, WIN>(plan.smem_bytes);
+    cudaError_t err = ensure_smem_attr<D, GK, GV, HK, HS, WIN, P16>(plan.smem_bytes);
     if (err != cudaSuccess) return err;
     // The launch may start before the kernel ahead of it on the stream finishes
     // (programmatic dependent launch); the kernel waits with griddepcontrol.wait before
@@ -1092,7 +1096,7 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN>, p);
+    err = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN, P16>, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -1116,23 +1120,24 @@ int decode_occupancy_gk128_win(const DecodeArgs& a, const DecodePlan& plan, size
 
 }  // namespace kvq
 
-// Instantiates the dispatch for one K group size GK_ over GV in {32, 64, 128} and the
-// three unit shapes (HK, HS) in {(1, 1), (1, 2), (4, 1)}; W_ selects the window instances.
+// Instantiates the dispatch for one K group size GK_ over GV in {32, 64, 128}, the three
+// unit shapes (HK, HS) in {(1, 1), (1, 2), (4, 1)} and, for one-head units, 16-token
+// pages or larger ones; W_ selects the window instances.
+#define KVQ_DECODE_CASES(GK_, GV_, W_, CALL)                                                        \
+    case GV_ * 32 + 8 + 2 + 1: return CALL(128, GK_, GV_, 1, 1, W_, true);                          \
+    case GV_ * 32 + 8 + 2 + 0: return CALL(128, GK_, GV_, 1, 1, W_, false);                         \
+    case GV_ * 32 + 8 + 4 + 1: return CALL(128, GK_, GV_, 1, 2, W_, true);                          \
+    case GV_ * 32 + 8 + 4 + 0: return CALL(128, GK_, GV_, 1, 2, W_, false);                         \
+    case GV_ * 32 + 32 + 2 + 1: return CALL(128, GK_, GV_, 4, 1, W_, true);
 #define KVQ_DECODE_DISPATCH(GK_, W_, CALL, FAIL)                                                     \
-    switch (a.L.Gv * 16 + plan.hk * 4 + plan.hs) {                                                   \
-        case 32 * 16 + 4 + 1: return CALL(128, GK_, 32, 1, 1, W_);                                   \
-        case 32 * 16 + 4 + 2: return CALL(128, GK_, 32, 1, 2, W_);                                   \
-        case 32 * 16 + 16 + 1: return CALL(128, GK_, 32, 4, 1, W_);                                  \
-        case 64 * 16 + 4 + 1: return CALL(128, GK_, 64, 1, 1, W_);                                   \
-        case 64 * 16 + 4 + 2: return CALL(128, GK_, 64, 1, 2, W_);                                   \
-        case 64 * 16 + 16 + 1: return CALL(128, GK_, 64, 4, 1, W_);                                  \
-        case 128 * 16 + 4 + 1: return CALL(128, GK_, 128, 1, 1, W_);                                 \
-        case 128 * 16 + 4 + 2: return CALL(128, GK_, 128, 1, 2, W_);                                 \
-        case 128 * 16 + 16 + 1: return CALL(128, GK_, 128, 4, 1, W_);                                \
+    switch (a.L.Gv * 32 + plan.hk * 8 + plan.hs * 2 + (a.L.P == 16 ? 1 : 0)) {                       \
+        KVQ_DECODE_CASES(GK_, 32, W_, CALL)                                                          \
+        KVQ_DECODE_CASES(GK_, 64, W_, CALL)                                                          \
+        KVQ_DECODE_CASES(GK_, 128, W_, CALL)                                                         \
         default: return FAIL;                                                                        \
     }
-#define KVQ_DECODE_RUN(D_, GK_, GV_, HK_, HS_, W_) decode::run<D_, GK_, GV_, HK_, HS_, W_>(a, plan, s)
-#define KVQ_DECODE_OCC(D_, GK_, GV_, HK_, HS_, W_) decode::occupancy<D_, GK_, GV_, HK_, HS_, W_>(smem)
+#define KVQ_DECODE_RUN(D_, GK_, GV_, HK_, HS_, W_, P16_) decode::run<D_, GK_, GV_, HK_, HS_, W_, P16_>(a, plan, s)
+#define KVQ_DECODE_OCC(D_, GK_, GV_, HK_, HS_, W_, P16_) decode::occupancy<D_, GK_, GV_, HK_, HS_, W_, P16_>(smem)
 #define KVQ_DECODE_TU(GK_, W_, RUN_NAME, OCC_NAME)                                                   \
     namespace kvq {                                                                                  \
     cudaError_t RUN_NAME(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {              \
