@@ -609,25 +609,28 @@ def run_kvq(args, world, rank, local):
             sync()
             return max_over_ranks(time.perf_counter() - t0, world, dev)
 
-        # one step after another on one stream: copy in, step, copy out
+        # one kvq_decode_step_host call per step, on one stream; the staging slots alternate so that
+        # the host may refill one while the other is in use
+        t_e2e = timed(lambda i: caches[i % n_pools].decode_step_host(pipe.slots[i % 2], pos, seq_lens,
+                                                                     stream=stream), stream.synchronize)
+        # the same steps with the copies on their own streams (kvq_decode_step_host_pipelined)
+        t_pipe = timed(lambda i: pipe.step(i, pos, seq_lens, cache=caches[i % n_pools]), pipe.synchronize)
         st0 = pipe.slots[0]
-        t_ser = timed(lambda i: caches[i % n_pools].decode_step_host(st0, pos, seq_lens, stream=stream),
-                      stream.synchronize)
-        # the same steps with the copies on their own streams, overlapped with the neighbouring steps' kernels
-        t_e2e = timed(lambda i: pipe.step(i, pos, seq_lens, cache=caches[i % n_pools]), pipe.synchronize)
         h2d = st0.host.numel() * 2
         d2h = st0.out_host.numel() * 4
-        e2e = {"value": world * n_e2e * step_bytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": t_e2e / n_e2e * 1e3,
-               "how": "one kvq_decode_step_host_pipelined C-ABI call per step (HostPipeline): the call copies "
-                      "the step's q/K/V from pinned host memory (one H2D copy) on an input copy stream, runs the "
-                      "step (decode and combine launches) on the compute stream and copies its output to pinned "
-                      "host memory (one D2H copy) on an output copy stream; two staging slots alternate, so step "
-                      "i+1's input copy and step i-1's output copy overlap step i's kernels; wall clock over all "
-                      "steps, synchronized at the end",
-               "serial": {"value": world * n_e2e * step_bytes / t_ser / 1e9, "ms_per_step": t_ser / n_e2e * 1e3,
-                          "how": "one kvq_decode_step_host C-ABI call per step: copy in, step, copy out on one "
-                                 "stream"}}
+        e2e = {"value": world * n_e2e * step_bytes / t_pipe / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": t_pipe / n_e2e * 1e3,
+               "how": "one kvq_decode_step_host_pipelined C-ABI call per step (HostPipeline), from pinned host "
+                      "buffers: the call copies the step's q/K/V host-to-device (one cudaMemcpyAsync) on an input "
+                      "copy stream, runs the step (decode and combine launches) on the compute stream and copies "
+                      "its output device-to-host (one cudaMemcpyAsync) on an output copy stream, ordered by "
+                      "per-slot events; two staging slots alternate, so step i+1's input copy and step i-1's "
+                      "output copy overlap step i's kernels; wall clock over all steps, synchronized at the end",
+               "single_call": {"value": world * n_e2e * step_bytes / t_e2e / 1e9, "ms_per_step": t_e2e / n_e2e * 1e3,
+                               "how": "one kvq_decode_step_host C-ABI call per step on one stream: a copy kernel "
+                                      "reads the inputs from pinned host memory, the step runs, the combine also "
+                                      "writes the output to pinned host memory; one chain of programmatic "
+                                      "dependent launches"}}
 
     if rank != 0:
         return None

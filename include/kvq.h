@@ -207,17 +207,22 @@ int kvq_decode_step(const kvq_cache_config *cfg, void *pool, const void *k_new, 
                     kvq_stream_t stream);
 
 /*
- * kvq_decode_step from host memory, in one call: one host-to-device copy of the step's
- * inputs, the step, one device-to-host copy of its output, all queued on `stream`
- * (nothing waits; read host_out after the stream has passed the call).
- *   host_in   host memory (pinned for an asynchronous copy) holding q [batch,
- *             num_q_heads, head_dim] fp16, then k_new [batch, num_kv_heads, head_dim]
- *             fp16, then v_new (same shape), back to back.
+ * kvq_decode_step from host memory, in one call: the step's inputs moved from host_in to
+ * dev_in, the step, its output moved from out to host_out, all queued on `stream`
+ * (nothing waits; read host_out after the stream has passed the call).  When host_in and
+ * host_out are page-locked (cudaHostAlloc, cudaHostRegister) the kernels move the data
+ * themselves: a copy kernel reads host_in through its device address, and the kernel
+ * that writes out also writes host_out, so the step stays one chain of kernels launched
+ * behind each other (programmatic dependent launch).  Pageable memory takes one
+ * cudaMemcpyAsync each way instead.
+ *   host_in   host memory holding q [batch, num_q_heads, head_dim] fp16, then k_new
+ *             [batch, num_kv_heads, head_dim] fp16, then v_new (same shape), back to back.
  *   dev_in    device buffer of the same size, 16-byte aligned: the inputs' device copy,
  *             from which the step reads q, k_new and v_new.
  *   out       device fp32 [batch, num_q_heads, head_dim], as in kvq_decode_step.
- *   host_out  host memory (pinned) of the same size: receives out.
- *   other arguments as in kvq_decode_step.
+ *   host_out  host memory of the same size: receives out.
+ *   other arguments as in kvq_decode_step.  host_in may be refilled, and host_out read,
+ *   once the stream has passed the call.
  * Returns as kvq_decode_step.
  */
 int kvq_decode_step_host(const kvq_cache_config *cfg, void *pool, const void *host_in, void *dev_in,

@@ -26,6 +26,7 @@ struct CParams {
     int32_t nsrc;  // 1, or 2 for the mixed-precision decode (INT4 history, FP16 recent tokens)
     const int32_t* seq_lens;
     float* out;
+    float* out_host;  // device address of mapped pinned host memory that also receives out, or nullptr
     int32_t B, Hq, lg_p;
 };
 
@@ -207,8 +208,10 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
             }
         }
         const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-        reinterpret_cast<float4*>(p.out + (static_cast<long long>(b) * p.Hq + hq) * D)[lane] =
-            make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+        const float4 r = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+        const long long row = static_cast<long long>(b) * p.Hq + hq;
+        reinterpret_cast<float4*>(p.out + row * D)[lane] = r;
+        if (p.out_host != nullptr) reinterpret_cast<float4*>(p.out_host + row * D)[lane] = r;
     }
 }
 
@@ -269,6 +272,7 @@ cudaError_t launch_combine(const DecodeArgs& a, const DecodePlan& plan, cudaStre
     p.nsrc = 1;
     p.seq_lens = a.seq_lens;
     p.out = a.out;
+    p.out_host = a.out_host;
     p.B = a.B;
     p.Hq = a.Hq;
     p.lg_p = lg2(a.L.P);

@@ -118,6 +118,9 @@ struct KParams {
     // for it runs out
     uint64_t wait_ns;
     uint32_t withhold;
+    // q is written by the kernel ahead on the stream (the host-buffer step's copy kernel):
+    // read it only after griddepcontrol.wait
+    bool q_after_wait;
 };
 
 // a / b for a >= 0, b > 0, with 32-bit division when both fit (the usual case).
@@ -431,8 +434,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
         }
         ++issued;
     };
-    // the first segment's q rows (read-only input) can move before the wait
-    {
+    // the first segment's q rows (read-only input) can move before the wait, unless the kernel
+    // ahead on the stream writes them (q_after_wait)
+    auto issue_first_q = [&]() {
         int b0 = find_seq(pre, p.B, p.Hg, c0);
         const int np0 = pre[b0 + 1] - pre[b0];
         const int hg0 = static_cast<int>(div_nn(c0 - static_cast<long long>(p.Hg) * pre[b0], np0));
@@ -441,10 +445,12 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
             mbar_arrive_expect_tx(qbar0, qbytes0);
             bulk_g2s(smem_u32(qbuf), p.q + (static_cast<long long>(b0) * p.Hq + hg0 * p.ns) * D, qbytes0, qbar0);
         }
-    }
+    };
+    if (!p.q_after_wait) issue_first_q();
 
     // ---- from here on the pool, the output and the workspace are used ----
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.q_after_wait) issue_first_q();
     publish_prefix();
     orphan_appends();
     {
@@ -1053,6 +1059,7 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     p.len_sub = a.len_sub;
     p.wait_ns = a.wait_ns != 0 ? a.wait_ns : kWaitLimitNs;
     p.withhold = a.withhold_first_copy ? 16u : 0u;
+    p.q_after_wait = a.q_after_wait;
     p.B = a.B;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;

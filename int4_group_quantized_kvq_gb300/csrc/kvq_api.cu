@@ -53,6 +53,18 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(KVQ_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+// The device address of page-locked host memory (cudaHostAlloc / cudaHostRegister), or
+// nullptr for any other pointer (pageable host memory, device memory).
+void* mapped_host_address(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // not a pointer the runtime knows: no lingering error
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost) return nullptr;
+    return at.devicePointer;
+}
+
 }  // namespace
 
 extern "C" {
@@ -252,7 +264,7 @@ int decode_step_impl(const kvq_cache_config* cfg, void* pool, const void* k_new,
                      const int32_t* append_pos, const void* q, const int32_t* block_table, int32_t max_blocks,
                      const int32_t* seq_lens, int32_t batch, int32_t num_q_heads, int32_t max_len, float softmax_scale,
                      int32_t window, int32_t sinks, float* out, void* workspace, size_t workspace_bytes,
-                     kvq_stream_t stream) {
+                     kvq_stream_t stream, float* out_host = nullptr, bool q_after_wait = false) {
     if (int e = check_cfg(cfg)) return e;
     if (batch < 0 || num_q_heads < 1 || max_len < 0)
         return fail(KVQ_EINVAL, "batch %d, num_q_heads %d, max_len %d", batch, num_q_heads, max_len);
@@ -293,6 +305,8 @@ int decode_step_impl(const kvq_cache_config* cfg, void* pool, const void* k_new,
     a.pool_w = static_cast<uint8_t*>(pool);
     a.window = window;
     a.sinks = sinks;
+    a.out_host = out_host;
+    a.q_after_wait = q_after_wait;
     kvq::DecodePlan plan;
     cudaError_t e = kvq::plan_decode(a, &plan);
     if (e == cudaErrorInvalidValue) return fail(KVQ_EUNSUPPORTED, "no decode kernel for this shape");
@@ -378,17 +392,28 @@ int kvq_decode_step_host(const kvq_cache_config* cfg, void* pool, const void* ho
     const size_t d = static_cast<size_t>(cfg->head_dim);
     const size_t q_bytes = static_cast<size_t>(batch) * num_q_heads * d * 2;
     const size_t kv_bytes = static_cast<size_t>(batch) * cfg->num_kv_heads * d * 2;
+    const size_t in_bytes = q_bytes + 2 * kv_bytes;
     const size_t out_bytes = static_cast<size_t>(batch) * num_q_heads * d * 4;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* din = static_cast<uint8_t*>(dev_in);
-    cudaError_t e = cudaMemcpyAsync(din, host_in, q_bytes + 2 * kv_bytes, cudaMemcpyHostToDevice, st);
+    // Pinned host memory is read and written by the kernels themselves (through its device
+    // address), so the step stays one chain of kernels launched behind each other; pageable
+    // memory takes a copy on the stream.
+    const void* in_dev = mapped_host_address(host_in);
+    float* out_dev = static_cast<float*>(mapped_host_address(host_out));
+    if (!aligned(in_dev, 16) || in_bytes % 16) in_dev = nullptr;
+    if (!aligned(out_dev, 16)) out_dev = nullptr;
+    cudaError_t e = in_dev ? kvq::launch_stage_in(in_dev, din, in_bytes / 16, st)
+                           : cudaMemcpyAsync(din, host_in, in_bytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step_host input copy");
     if (int rc = decode_step_impl(cfg, pool, din + q_bytes, din + q_bytes + kv_bytes, append_pos, din, block_table,
                                   max_blocks, seq_lens, batch, num_q_heads, max_len, softmax_scale, 0, 0, out,
-                                  workspace, workspace_bytes, stream))
+                                  workspace, workspace_bytes, stream, out_dev, in_dev != nullptr))
         return rc;
-    e = cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step_host output copy");
+    if (!out_dev) {
+        e = cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_fail(e, "kvq_decode_step_host output copy");
+    }
     return ok();
 }
 

@@ -83,6 +83,11 @@ struct DequantArgs {
 };
 cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t stream);
 
+// Copy n16 16-byte words from src (device address of mapped pinned host memory) to dst on
+// the device, as a kernel launched with programmatic dependent launch: it reads src while
+// the kernel ahead of it on the stream finishes and writes dst only after that kernel has.
+cudaError_t launch_stage_in(const void* src, void* dst, size_t n16, cudaStream_t stream);
+
 // Decode attention: the persistent split-KV kernel with the split combine fused in.
 struct DecodePlan {
     int32_t hk;           // kv heads per unit of work (4 when Hq == Hkv, Hkv % 4 == 0, P == 16; else 1)
@@ -125,6 +130,12 @@ struct DecodeArgs {
     int32_t len_sub = 0;
     // status word (nullptr: the first word of the workspace)
     uint32_t* status = nullptr;
+    // device address of mapped pinned host memory the combine also writes the output to
+    // (the host-buffer decode step), or nullptr
+    float* out_host = nullptr;
+    // q (and the new rows) are written by the kernel just ahead on the stream, which lets
+    // this grid start early: the grid reads q only after griddepcontrol.wait
+    bool q_after_wait = false;
     // bound of the INT4 kernel's waits on copies in ns (0: the default, 250 ms), and the test
     // of that bound (each warp's first page copy announced 16 bytes larger than it is)
     uint64_t wait_ns = 0;

@@ -304,3 +304,37 @@ def test_decode_step_host_call_matches_device_step(kvq):
     assert torch.equal(p1, p2)
     assert torch.equal(out1.cpu(), st.out_host)
     assert kvq.kvq_read_status(ws1) == 0 and kvq.kvq_read_status(ws2) == 0
+
+
+def test_decode_step_host_call_from_pageable_memory(kvq):
+    """kvq_decode_step_host with pageable host buffers (the copies then go through cudaMemcpyAsync
+    instead of the kernels) gives the same pool and output as with pinned ones."""
+    from int4_group_quantized_kvq_gb300.cache import HostStaging
+    case = Case(2, 16, 4, 128, [77, 300], seed=44)
+    append_pos = [n - 1 for n in case.lens]
+    pool, k_new, v_new = _setup(case, append_pos, 0x00)
+    cfg = case.cfg(kvq)
+    ap = torch.tensor(append_pos, dtype=torch.int32, device="cuda")
+    sl = torch.tensor(case.lens, dtype=torch.int32, device="cuda")
+    bt = case.block_table.cuda()
+    ml = max(case.lens)
+    outs, pools = [], []
+    for pinned in (True, False):
+        st = HostStaging(case.B, case.Hq, case.Hkv, case.d, device="cuda")
+        host_in = st.host if pinned else st.host.clone()        # clone(): pageable
+        host_out = st.out_host if pinned else st.out_host.clone()
+        n = case.B * case.Hq * case.d
+        nk = case.B * case.Hkv * case.d
+        host_in[:n].copy_(case.q.reshape(-1))
+        host_in[n:n + nk].copy_(torch.from_numpy(k_new).reshape(-1))
+        host_in[n + nk:].copy_(torch.from_numpy(v_new).reshape(-1))
+        p = torch.from_numpy(pool.copy()).cuda()
+        ws = kvq.new_workspace(cfg, case.B, case.Hq, ml, device="cuda")
+        kvq.kvq_decode_step_host(cfg, p, host_in, st.dev, ap, bt, sl, case.B, case.Hq, ml, case.scale, st.out, host_out,
+                                 ws)
+        torch.cuda.synchronize()
+        assert kvq.kvq_read_status(ws) == 0
+        outs.append(host_out.clone())
+        pools.append(p)
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(pools[0], pools[1])
