@@ -69,7 +69,9 @@ typedef struct CUevent_st *kvq_event_t;
 /* Cache geometry, shared by all calls on one pool. */
 typedef struct {
     int32_t num_kv_heads; /* KV heads per layer (Hkv), >= 1                          */
-    int32_t head_dim;     /* d: 64, 128 or 256 (decode attention: 128)                */
+    int32_t head_dim;     /* d: 64, 128 or 256 (decode over the INT4 cache: all three,
+                             d = 256 with up to 4 query heads per KV head and group_k
+                             >= 64; over the other caches: 128)                      */
     int32_t page_size;    /* tokens per page: 16, 32 or 64                            */
     int32_t group_k;      /* K quantization group along head_dim: 32, 64 or 128 (<= d) */
     int32_t group_v;      /* V quantization group: 32, 64 or 128 (<= d)               */

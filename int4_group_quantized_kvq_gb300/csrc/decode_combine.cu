@@ -38,7 +38,8 @@ constexpr int kCombineLocalB = 256;   // up to this batch the row metadata is co
 // for j < W * (cl - cf + 1), where CTAs cf..cl of that grid hold the units of segment
 // seg = (b, hq / ns); when some CTA slices are empty (fewer units than CTAs) their partials
 // do not exist.  Warp w of the CTA takes partials w, w + nw, ..., eight at a time, keeping
-// a running maximum M and sum L and an unnormalised output (lane l: dimensions 4l .. 4l + 3),
+// a running maximum M and sum L and an unnormalised output (lane l: dimensions 4f .. 4f + 3
+// for f = l, l + 32, ... below D / 4),
 // over the sources in turn; the warps' results are then merged with weights 2^(M_w - max M).
 // Sequences without positions have no partials and get zeros.  This is the split-KV
 // combine of flash decoding: out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
@@ -46,7 +47,10 @@ constexpr int kCombineLocalB = 256;   // up to this batch the row metadata is co
 // carries no code for a second.
 template <int D, int NSRC>
 __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams p) {
-    static_assert(D == 128, "one float4 per lane");
+    static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
+    constexpr int NV = (D / 4 + 31) / 32;  // float4 of the row per lane
+    constexpr int NA = NV == 1 ? 4 : 2;    // independent sums per float4 (shorter fma chains)
+    auto lane_has = [](int lane, int v) { return D / 4 >= 32 || lane + 32 * v < D / 4; };
     // the next decode call may start its set-up; it waits for this grid before it
     // touches the workspace
     asm volatile("griddepcontrol.launch_dependents;");
@@ -125,9 +129,11 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
     }
 
     float M = -INFINITY, L = 0.f;
-    float4 acc[4];
+    float4 acc[NV][NA];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) acc[a] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int a = 0; a < NA; ++a) acc[v][a] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int si = 0; si < NSRC; ++si) {
         const CSource& s = p.src[si];
@@ -139,7 +145,7 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
         const float* o0 = s.ws_o + (base[si] * s.ns + sl) * D + 4 * lane;
         for (int j0 = warp; j0 < n[si]; j0 += kCombineBatch * nw) {
             float2 ml[kCombineBatch];
-            float4 ov[kCombineBatch];
+            float4 ov[kCombineBatch][NV];
 #pragma unroll
             for (int kk = 0; kk < kCombineBatch; ++kk) {
                 const int j = j0 + kk * nw;
@@ -148,13 +154,11 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
                     const long long k = cf[si] + j / s.W;
                     have = slice_start(k, U[si], s.C) < slice_start(k + 1, U[si], s.C);
                 }
-                if (have) {
-                    ml[kk] = __ldcg(reinterpret_cast<const float2*>(ml0 + j * stride_ml));
-                    ov[kk] = __ldcg(reinterpret_cast<const float4*>(o0 + j * stride_o));
-                } else {
-                    ml[kk] = make_float2(-INFINITY, 0.f);
-                    ov[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                ml[kk] = have ? __ldcg(reinterpret_cast<const float2*>(ml0 + j * stride_ml)) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    ov[kk][v] = have && lane_has(lane, v) ? __ldcg(reinterpret_cast<const float4*>(o0 + j * stride_o) + 32 * v)
+                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             float mb = M;
 #pragma unroll
@@ -164,23 +168,28 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
                 const float f = fast_exp2(M - mb);
                 L *= f;
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    acc[a].x *= f;
-                    acc[a].y *= f;
-                    acc[a].z *= f;
-                    acc[a].w *= f;
-                }
+                for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int a = 0; a < NA; ++a) {
+                        acc[v][a].x *= f;
+                        acc[v][a].y *= f;
+                        acc[v][a].z *= f;
+                        acc[v][a].w *= f;
+                    }
                 M = mb;
             }
 #pragma unroll
             for (int kk = 0; kk < kCombineBatch; ++kk) {
                 const float f = fast_exp2(ml[kk].x - M);
                 L = fmaf(f, ml[kk].y, L);
-                float4& A = acc[kk & 3];
-                A.x = fmaf(f, ov[kk].x, A.x);
-                A.y = fmaf(f, ov[kk].y, A.y);
-                A.z = fmaf(f, ov[kk].z, A.z);
-                A.w = fmaf(f, ov[kk].w, A.w);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    float4& A = acc[v][kk % NA];
+                    A.x = fmaf(f, ov[kk][v].x, A.x);
+                    A.y = fmaf(f, ov[kk][v].y, A.y);
+                    A.z = fmaf(f, ov[kk][v].z, A.z);
+                    A.w = fmaf(f, ov[kk][v].w, A.w);
+                }
             }
         }
     }
@@ -188,30 +197,46 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
         s_m[warp] = M;
         s_l[warp] = L;
     }
-    s_o[warp][lane] = make_float4(acc[0].x + acc[1].x + acc[2].x + acc[3].x, acc[0].y + acc[1].y + acc[2].y + acc[3].y,
-                                  acc[0].z + acc[1].z + acc[2].z + acc[3].z, acc[0].w + acc[1].w + acc[2].w + acc[3].w);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        float4 t = acc[v][0];
+#pragma unroll
+        for (int a = 1; a < NA; ++a) {
+            t.x += acc[v][a].x;
+            t.y += acc[v][a].y;
+            t.z += acc[v][a].z;
+            t.w += acc[v][a].w;
+        }
+        if (lane_has(lane, v)) s_o[warp][lane + 32 * v] = t;
+    }
     __syncthreads();
     if (warp == 0) {
         float Mx = -INFINITY;
         for (int w = 0; w < nw; ++w) Mx = fmaxf(Mx, s_m[w]);
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         float Ls = 0.f;
-        if (Mx != -INFINITY) {
-            for (int w = 0; w < nw; ++w) {
-                const float f = fast_exp2(s_m[w] - Mx);
-                const float4 ow = s_o[w][lane];
-                Ls = fmaf(f, s_l[w], Ls);
-                O.x = fmaf(f, ow.x, O.x);
-                O.y = fmaf(f, ow.y, O.y);
-                O.z = fmaf(f, ow.z, O.z);
-                O.w = fmaf(f, ow.w, O.w);
-            }
-        }
+        if (Mx != -INFINITY)
+            for (int w = 0; w < nw; ++w) Ls = fmaf(fast_exp2(s_m[w] - Mx), s_l[w], Ls);
         const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-        const float4 r = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
         const long long row = static_cast<long long>(b) * p.Hq + hq;
-        reinterpret_cast<float4*>(p.out + row * D)[lane] = r;
-        if (p.out_host != nullptr) reinterpret_cast<float4*>(p.out_host + row * D)[lane] = r;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            if (!lane_has(lane, v)) continue;
+            const int f4 = lane + 32 * v;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (Mx != -INFINITY) {
+                for (int w = 0; w < nw; ++w) {
+                    const float f = fast_exp2(s_m[w] - Mx);
+                    const float4 ow = s_o[w][f4];
+                    O.x = fmaf(f, ow.x, O.x);
+                    O.y = fmaf(f, ow.y, O.y);
+                    O.z = fmaf(f, ow.z, O.z);
+                    O.w = fmaf(f, ow.w, O.w);
+                }
+            }
+            const float4 r = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+            reinterpret_cast<float4*>(p.out + row * D)[f4] = r;
+            if (p.out_host != nullptr) reinterpret_cast<float4*>(p.out_host + row * D)[f4] = r;
+        }
     }
 }
 
@@ -236,7 +261,7 @@ decode::CSource source_of(const DecodeArgs& a, const DecodePlan& plan) {
     return s;
 }
 
-cudaError_t launch(const decode::CParams& p, int warps, cudaStream_t stream) {
+cudaError_t launch(const decode::CParams& p, int d, int warps, cudaStream_t stream) {
     const long long rows = static_cast<long long>(p.B) * p.Hq;
     if (rows <= 0) return cudaSuccess;
     if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -252,8 +277,12 @@ cudaError_t launch(const decode::CParams& p, int warps, cudaStream_t stream) {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err = p.nsrc == 2 ? cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 2>, p)
-                                  : cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 1>, p);
+    cudaError_t err;
+    if (p.nsrc == 2) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 2>, p);  // mixed: head_dim 128 only
+    else if (d == 64) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<64, 1>, p);
+    else if (d == 256) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<256, 1>, p);
+    else if (d == 128) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 1>, p);
+    else return cudaErrorInvalidValue;
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -276,7 +305,7 @@ cudaError_t launch_combine(const DecodeArgs& a, const DecodePlan& plan, cudaStre
     p.B = a.B;
     p.Hq = a.Hq;
     p.lg_p = lg2(a.L.P);
-    return launch(p, plan.combine_warps, stream);
+    return launch(p, a.L.d, plan.combine_warps, stream);
 }
 
 // The mixed-precision decode: the partials of the INT4 grid (a0, plan0) and of the FP16
@@ -293,7 +322,7 @@ cudaError_t launch_combine2(const DecodeArgs& a0, const DecodePlan& plan0, const
     p.Hq = a0.Hq;
     p.lg_p = lg2(a0.L.P);
     const int warps = std::max(plan0.combine_warps, plan1.combine_warps);
-    return launch(p, warps, stream);
+    return launch(p, a0.L.d, warps, stream);
 }
 
 }  // namespace kvq

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(const __grid_consta
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_all) + warp * stages;
     CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + ring_all + kWarps * stages * sizeof(uint64_t));
     __half* qbuf = reinterpret_cast<__half*>(ctl + 1);  // [2][8][D]
-    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(qbuf) + kQBufBytes);
+    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(qbuf) + q_buf_bytes<D>());
     int32_t* lens = pre + p.B + 1;
     int32_t* aps = lens + p.B;
     const uint32_t qbar0 = smem_u32(&ctl->qbar[0]);

@@ -2,4 +2,8 @@
 // with sink tokens.
 #include "decode_impl.cuh"
 
-KVQ_DECODE_TU(128, true, decode_run_gk128_win, decode_occupancy_gk128_win)
+#define KVQ_GK128_WIN_CASES(CALL)                        \
+    KVQ_DECODE_CASES(128, 128, 32, true, CALL)  \
+    KVQ_DECODE_CASES(128, 128, 64, true, CALL)  \
+    KVQ_DECODE_CASES(128, 128, 128, true, CALL)
+KVQ_DECODE_TU(KVQ_GK128_WIN_CASES, decode_run_gk128_win, decode_occupancy_gk128_win)

@@ -72,11 +72,11 @@ namespace decode {
 constexpr uint64_t kWaitLimitNs = 250000000ull;   // a page copy that takes 250 ms has failed
 
 // Warps per CTA, and resident CTAs per SM the register budget is tuned for: 3 (up to 168
-// registers) when a thread carries one query-head slot, 2 when it carries two.
+// registers) when a thread carries one query-head slot of head_dim <= 128, else 2.
 template <int HS>
 constexpr int cta_warps() { return 4; }
-template <int HS>
-constexpr int min_ctas() { return HS == 1 ? 3 : 2; }
+template <int HS, int D = 128>
+constexpr int min_ctas() { return HS == 1 && D <= 128 ? 3 : 2; }
 
 // CTA-wide bookkeeping in shared memory.
 struct CtaCtl {
@@ -85,7 +85,9 @@ struct CtaCtl {
     uint64_t pad[12];
 };
 static_assert(sizeof(CtaCtl) == 128, "the planner reserves 128 bytes");
-constexpr int kQBufBytes = 2 * 8 * 128 * 2;  // two buffers of up to 8 query-head rows of d = 128 fp16
+// two buffers of up to 8 query-head rows of head_dim D fp16
+template <int D>
+constexpr int q_buf_bytes() { return 2 * 8 * D * 2; }
 
 struct KParams {
     const uint8_t* pool;
@@ -254,37 +256,47 @@ struct Step {
 // Fused append of the decode step: quantize the new token's K and V rows of sequence sb,
 // head group shg (its HK heads) into page index pgu of the sequence, in the pool and,
 // when the page is staged in shared memory at sblk, in that copy too.  All lanes call
-// this: lanes 0..15 take the K row, 16..31 the V row, 8 values each (the same arithmetic
-// and bytes as the quantize-append kernel).  Out of line: it runs once per segment at
-// most, and inlined into the streaming loop its code would crowd the instruction cache.
+// this.  A row takes D / 8 lanes, 8 values each (the same arithmetic and bytes as the
+// quantize-append kernel): for D <= 128 the K row and the V row in one pass (lanes past
+// 2 D / 8 idle), for D = 256 one after the other.  Out of line: it runs once per segment
+// at most, and inlined into the streaming loop its code would crowd the instruction cache.
 template <int D, int HK>
 __device__ __noinline__ void append_rows(const KParams& p, const int32_t* aps, uint8_t* sblk, int sb, int shg,
                                          int pgu) {
+    constexpr int LPR = D / 8;                 // lanes per row
+    constexpr int ROWS = LPR <= 16 ? 2 : 1;    // rows per pass
     const int lane = threadIdx.x & 31;
     const int page = p.block_table[static_cast<long long>(sb) * p.max_blocks + pgu];
     const bool pvalid = page >= 0 && page < p.num_pages;  // else flagged where the page is looked up
     const int slot = aps[sb] & ((1 << p.lg_p) - 1);
-    const int half = lane >> 4;
-    const int tl = lane & 15;
-    const int lg = half ? p.lg_lv : p.lg_lk;
-    const int ng = D >> (lg + 3);
-    const int code_off = (half ? p.v_codes : 0) + slot * (D / 2) + tl * 4;
-    const int scale_off = (half ? p.v_scales : p.k_scales) + slot * ng * 2 + (tl >> lg) * 2;
-    const bool writes_scale = (tl & ((1 << lg) - 1)) == 0;
+    const int rsel = lane / LPR;               // this lane's row in the pass
+    const int tl = lane % LPR;                 // lane within the row
     for (int a = 0; a < HK; ++a) {
         const int h = shg * HK + a;
-        const uint4 raw = *reinterpret_cast<const uint4*>((half ? p.v_new : p.k_new) +
-                                                          (static_cast<long long>(sb) * p.Hkv + h) * D + tl * 8);
-        __half s16;
-        const uint32_t word = quant_lane8<D / 8>(raw, lg, s16);
-        if (pvalid) {
-            uint8_t* gb = p.pool_w + (static_cast<long long>(page) * p.Hkv + h) * p.block_bytes;
-            *reinterpret_cast<uint32_t*>(gb + code_off) = word;
-            if (writes_scale) *reinterpret_cast<__half*>(gb + scale_off) = s16;
-            if (sblk != nullptr) {
-                uint8_t* sa = sblk + a * p.block_bytes;
-                *reinterpret_cast<uint32_t*>(sa + code_off) = word;
-                if (writes_scale) *reinterpret_cast<__half*>(sa + scale_off) = s16;
+#pragma unroll
+        for (int pass = 0; pass < 2 / ROWS; ++pass) {
+            const int half = ROWS == 2 ? (rsel & 1) : pass;  // 0: the K row, 1: the V row
+            const bool active = ROWS == 2 ? rsel < 2 : true;
+            const int lg = half ? p.lg_lv : p.lg_lk;
+            const int ng = D >> (lg + 3);
+            const int code_off = (half ? p.v_codes : 0) + slot * (D / 2) + tl * 4;
+            const int scale_off = (half ? p.v_scales : p.k_scales) + slot * ng * 2 + (tl >> lg) * 2;
+            const bool writes_scale = (tl & ((1 << lg) - 1)) == 0;
+            uint4 raw = make_uint4(0, 0, 0, 0);
+            if (active)
+                raw = *reinterpret_cast<const uint4*>((half ? p.v_new : p.k_new) +
+                                                      (static_cast<long long>(sb) * p.Hkv + h) * D + tl * 8);
+            __half s16;
+            const uint32_t word = quant_lane8<LPR>(raw, lg, s16);
+            if (active && pvalid) {
+                uint8_t* gb = p.pool_w + (static_cast<long long>(page) * p.Hkv + h) * p.block_bytes;
+                *reinterpret_cast<uint32_t*>(gb + code_off) = word;
+                if (writes_scale) *reinterpret_cast<__half*>(gb + scale_off) = s16;
+                if (sblk != nullptr) {
+                    uint8_t* sa = sblk + a * p.block_bytes;
+                    *reinterpret_cast<uint32_t*>(sa + code_off) = word;
+                    if (writes_scale) *reinterpret_cast<__half*>(sa + scale_off) = s16;
+                }
             }
         }
     }
@@ -298,8 +310,9 @@ __device__ __noinline__ void append_rows(const KParams& p, const int32_t* aps, u
 // step; the instances for larger pages (P16 false) take two 16-token chunks of one page.
 // Each instance carries only its own path, which keeps the loop's code small.
 template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16>
-__global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_splitkv_kernel(KParams p) {
-    static_assert(D == 128, "the fragment mapping below is written for head_dim 128");
+__global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decode_splitkv_kernel(KParams p) {
+    static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
+    static_assert(D <= 128 || (HK == 1 && HS == 1), "head_dim 256: one-head units, up to 4 query heads each");
     static_assert(HK == 1 || HS == 1, "several kv heads per unit only with one query head each");
     static_assert(HK == 1 || P16, "four-head units only for 16-token pages");
     constexpr int NGK = D / GK;               // K groups per row
@@ -331,7 +344,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_all) + warp * stages;
     CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + ring_all + kWarps * stages * sizeof(uint64_t));
     __half* qbuf = reinterpret_cast<__half*>(ctl + 1);  // [2][8][D]
-    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(qbuf) + kQBufBytes);
+    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(qbuf) + q_buf_bytes<D>());
     int32_t* lens = pre + p.B + 1;
     int32_t* aps = lens + p.B;
     const uint32_t qbar0 = smem_u32(&ctl->qbar[0]);
@@ -508,10 +521,22 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
 #pragma unroll
                 for (int a = 0; a < HK; ++a) {
                     const uint8_t* kb = blk[X] + a * bbytes + chk[X] * 16 * ROW + k_off;
-                    const uint4 x0 = *reinterpret_cast<const uint4*>(kb);
-                    const uint4 x1 = *reinterpret_cast<const uint4*>(kb + 8 * ROW);
-                    kg[X][a][0] = x0.x; kg[X][a][1] = x0.y; kg[X][a][2] = x0.z; kg[X][a][3] = x0.w;
-                    kg8[X][a][0] = x1.x; kg8[X][a][1] = x1.y; kg8[X][a][2] = x1.z; kg8[X][a][3] = x1.w;
+                    if constexpr (KW == 2) {
+                        const uint2 x0 = *reinterpret_cast<const uint2*>(kb);
+                        const uint2 x1 = *reinterpret_cast<const uint2*>(kb + 8 * ROW);
+                        kg[X][a][0] = x0.x; kg[X][a][1] = x0.y;
+                        kg8[X][a][0] = x1.x; kg8[X][a][1] = x1.y;
+                    } else {
+#pragma unroll
+                        for (int w4 = 0; w4 < KW / 4; ++w4) {
+                            const uint4 x0 = *reinterpret_cast<const uint4*>(kb + 16 * w4);
+                            const uint4 x1 = *reinterpret_cast<const uint4*>(kb + 8 * ROW + 16 * w4);
+                            kg[X][a][4 * w4 + 0] = x0.x; kg[X][a][4 * w4 + 1] = x0.y;
+                            kg[X][a][4 * w4 + 2] = x0.z; kg[X][a][4 * w4 + 3] = x0.w;
+                            kg8[X][a][4 * w4 + 0] = x1.x; kg8[X][a][4 * w4 + 1] = x1.y;
+                            kg8[X][a][4 * w4 + 2] = x1.z; kg8[X][a][4 * w4 + 3] = x1.w;
+                        }
+                    }
 #pragma unroll
                     for (int t = 0; t < NTQ; ++t)
                         acc[X][a][t][0] = acc[X][a][t][1] = acc[X][a][t][2] = acc[X][a][t][3] = 0.f;
@@ -947,8 +972,10 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                         }
                     __syncwarp();
                     for (int k = 0; k < nsr; ++k)
-                        reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + 4 * s + k) * D)[lane] =
-                            reinterpret_cast<const float4*>(sbuf + k * D)[lane];
+#pragma unroll
+                        for (int f = lane; f < D / 4; f += 32)  // D / 4 float4 a row
+                            reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + 4 * s + k) * D)[f] =
+                                reinterpret_cast<const float4*>(sbuf + k * D)[f];
                     if (g == 0 && c < nsr)
                         *reinterpret_cast<float2*>(p.ws_ml + (piece * p.ns + 4 * s + c) * 2) = make_float2(m[s], lt[s]);
                     __syncwarp();
@@ -963,7 +990,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS>()) decode_s
                 if (lane < p.ns)
                     *reinterpret_cast<float2*>(p.ws_ml + (piece * p.ns + lane) * 2) = make_float2(-INFINITY, 0.f);
                 for (int k = 0; k < p.ns; ++k)
-                    reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + k) * D)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int f = lane; f < D / 4; f += 32)
+                        reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + k) * D)[f] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
 
@@ -1110,8 +1139,8 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
 
 }  // namespace decode
 
-// Per-K-group dispatch entry points, one per translation unit (the _win ones serve calls
-// with a sliding window).
+// Dispatch entry points, one per translation unit: per K group size for head_dim 128, per
+// head_dim for 64 and 256 (the _win ones serve calls with a sliding window).
 cudaError_t decode_run_gk32(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_gk64(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_gk128(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
@@ -1124,33 +1153,48 @@ cudaError_t decode_run_gk128_win(const DecodeArgs& a, const DecodePlan& plan, cu
 int decode_occupancy_gk32_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk64_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk128_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+cudaError_t decode_run_d64(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_d64_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_d256(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_d256_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+int decode_occupancy_d64(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_d64_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_d256(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_d256_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 
 }  // namespace kvq
 
-// Instantiates the dispatch for one K group size GK_ over GV in {32, 64, 128}, the three
-// unit shapes (HK, HS) in {(1, 1), (1, 2), (4, 1)} and, for one-head units, 16-token
-// pages or larger ones; W_ selects the window instances.
-#define KVQ_DECODE_CASES(GK_, GV_, W_, CALL)                                                        \
-    case GV_ * 32 + 8 + 2 + 1: return CALL(128, GK_, GV_, 1, 1, W_, true);                          \
-    case GV_ * 32 + 8 + 2 + 0: return CALL(128, GK_, GV_, 1, 1, W_, false);                         \
-    case GV_ * 32 + 8 + 4 + 1: return CALL(128, GK_, GV_, 1, 2, W_, true);                          \
-    case GV_ * 32 + 8 + 4 + 0: return CALL(128, GK_, GV_, 1, 2, W_, false);                         \
-    case GV_ * 32 + 32 + 2 + 1: return CALL(128, GK_, GV_, 4, 1, W_, true);
-#define KVQ_DECODE_DISPATCH(GK_, W_, CALL, FAIL)                                                     \
-    switch (a.L.Gv * 32 + plan.hk * 8 + plan.hs * 2 + (a.L.P == 16 ? 1 : 0)) {                       \
-        KVQ_DECODE_CASES(GK_, 32, W_, CALL)                                                          \
-        KVQ_DECODE_CASES(GK_, 64, W_, CALL)                                                          \
-        KVQ_DECODE_CASES(GK_, 128, W_, CALL)                                                         \
-        default: return FAIL;                                                                        \
-    }
+// Dispatch key of an instance: K and V group sizes, unit shape (HK kv heads, HS query-head
+// slots per thread) and whether pages hold 16 tokens.
+#define KVQ_DECODE_KEY(GK, GV, HK, HS, P16) (((GK) << 13) + (GV) * 32 + (HK) * 8 + (HS) * 2 + (P16))
+// The instances of one (head_dim D_, GK_, GV_): the three unit shapes (HK, HS) in
+// {(1, 1), (1, 2), (4, 1)} and, for one-head units, 16-token pages or larger ones; W_
+// selects the window instances.
+#define KVQ_DECODE_CASES(D_, GK_, GV_, W_, CALL)                                                    \
+    case KVQ_DECODE_KEY(GK_, GV_, 1, 1, 1): return CALL(D_, GK_, GV_, 1, 1, W_, true);              \
+    case KVQ_DECODE_KEY(GK_, GV_, 1, 1, 0): return CALL(D_, GK_, GV_, 1, 1, W_, false);             \
+    case KVQ_DECODE_KEY(GK_, GV_, 1, 2, 1): return CALL(D_, GK_, GV_, 1, 2, W_, true);              \
+    case KVQ_DECODE_KEY(GK_, GV_, 1, 2, 0): return CALL(D_, GK_, GV_, 1, 2, W_, false);             \
+    case KVQ_DECODE_KEY(GK_, GV_, 4, 1, 1): return CALL(D_, GK_, GV_, 4, 1, W_, true);
+// Head_dim 256: one-head units with one query-head slot per thread only.
+#define KVQ_DECODE_CASES_1H(D_, GK_, GV_, W_, CALL)                                                 \
+    case KVQ_DECODE_KEY(GK_, GV_, 1, 1, 1): return CALL(D_, GK_, GV_, 1, 1, W_, true);              \
+    case KVQ_DECODE_KEY(GK_, GV_, 1, 1, 0): return CALL(D_, GK_, GV_, 1, 1, W_, false);
 #define KVQ_DECODE_RUN(D_, GK_, GV_, HK_, HS_, W_, P16_) decode::run<D_, GK_, GV_, HK_, HS_, W_, P16_>(a, plan, s)
 #define KVQ_DECODE_OCC(D_, GK_, GV_, HK_, HS_, W_, P16_) decode::occupancy<D_, GK_, GV_, HK_, HS_, W_, P16_>(smem)
-#define KVQ_DECODE_TU(GK_, W_, RUN_NAME, OCC_NAME)                                                   \
+// One translation unit's entry points over the cases CASES(CALL) lists.
+#define KVQ_DECODE_TU(CASES, RUN_NAME, OCC_NAME)                                                     \
     namespace kvq {                                                                                  \
     cudaError_t RUN_NAME(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {              \
-        KVQ_DECODE_DISPATCH(GK_, W_, KVQ_DECODE_RUN, cudaErrorInvalidValue)                          \
+        switch (KVQ_DECODE_KEY(a.L.Gk, a.L.Gv, plan.hk, plan.hs, a.L.P == 16 ? 1 : 0)) {             \
+            CASES(KVQ_DECODE_RUN)                                                                    \
+            default: return cudaErrorInvalidValue;                                                   \
+        }                                                                                            \
     }                                                                                                \
     int OCC_NAME(const DecodeArgs& a, const DecodePlan& plan, size_t smem) {                         \
-        KVQ_DECODE_DISPATCH(GK_, W_, KVQ_DECODE_OCC, 0)                                              \
+        switch (KVQ_DECODE_KEY(a.L.Gk, a.L.Gv, plan.hk, plan.hs, a.L.P == 16 ? 1 : 0)) {             \
+            CASES(KVQ_DECODE_OCC)                                                                    \
+            default: return 0;                                                                       \
+        }                                                                                            \
     }                                                                                                \
     }

@@ -31,6 +31,14 @@ cudaError_t decode_run_gk128_win(const DecodeArgs& a, const DecodePlan& plan, cu
 int decode_occupancy_gk32_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk64_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 int decode_occupancy_gk128_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+cudaError_t decode_run_d64(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_d64_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_d256(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+cudaError_t decode_run_d256_win(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+int decode_occupancy_d64(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_d64_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_d256(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+int decode_occupancy_d256_win(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 cudaError_t launch_combine(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_fp16(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 int decode_occupancy_fp16(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
@@ -38,7 +46,6 @@ int decode_occupancy_fp16(const DecodeArgs& a, const DecodePlan& plan, size_t sm
 namespace {
 constexpr int kMaxStages = 8;           // deepest unit ring per warp
 constexpr size_t kMaxRingBytes = 8 * 2144;  // per warp: deeper rings gain nothing
-constexpr size_t kCtlBytes = 128 + 2 * 8 * 128 * 2;  // CTA bookkeeping and the two q buffers
 constexpr int kMinUnitsPerWarp = 2;
 constexpr size_t kAlign = 256;
 
@@ -46,14 +53,18 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
 cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
-    if (a.L.d != 128) return cudaErrorInvalidValue;
+    // the INT4 kernels take head_dim 64, 128 or 256 (256: up to 4 query heads per kv head);
+    // the other caches and the mixed decode head_dim 128
+    if (a.L.d != 128 && (a.fp16 || (a.L.d != 64 && a.L.d != 256))) return cudaErrorInvalidValue;
     if (a.L.P % 16 != 0) return cudaErrorInvalidValue;
     const int r = a.Hq / a.Hkv;
-    if (r < 1 || r > 8) return cudaErrorInvalidValue;
+    if (r < 1 || r > (a.L.d == 256 ? 4 : 8)) return cudaErrorInvalidValue;
     // four kv heads per unit for 16-token pages (a 4-block unit then stays near the size
     // of one larger page); larger pages are big enough copies on their own
-    plan->hk = (!a.fp16 && r == 1 && a.Hkv % 4 == 0 && a.L.P == 16) ? 4 : 1;
+    plan->hk = (!a.fp16 && r == 1 && a.Hkv % 4 == 0 && a.L.P == 16 && a.L.d <= 128) ? 4 : 1;
     plan->hs = (plan->hk == 1 && r > 4) ? 2 : 1;
+    // CTA bookkeeping (128 bytes) and the two q buffers of 8 rows of head_dim fp16
+    const size_t kCtlBytes = 128 + static_cast<size_t>(2) * 8 * a.L.d * 2;
     const int hg = a.Hkv / plan->hk;
     const int kWarpsPerCta = 4;  // the kernel's CTA size
     const int ns = plan->hk * r;
@@ -75,6 +86,8 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     auto occ_for = [&](size_t smem) {
         if (a.fp16) return decode_occupancy_fp16(a, *plan, smem);
         const bool w = a.window > 0;
+        if (a.L.d == 64) return w ? decode_occupancy_d64_win(a, *plan, smem) : decode_occupancy_d64(a, *plan, smem);
+        if (a.L.d == 256) return w ? decode_occupancy_d256_win(a, *plan, smem) : decode_occupancy_d256(a, *plan, smem);
         switch (a.L.Gk) {
             case 32: return w ? decode_occupancy_gk32_win(a, *plan, smem) : decode_occupancy_gk32(a, *plan, smem);
             case 64: return w ? decode_occupancy_gk64_win(a, *plan, smem) : decode_occupancy_gk64(a, *plan, smem);
@@ -134,6 +147,8 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
 cudaError_t launch_decode_grid(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     if (a.fp16) return decode_run_fp16(a, plan, stream);
     const bool w = a.window > 0;
+    if (a.L.d == 64) return w ? decode_run_d64_win(a, plan, stream) : decode_run_d64(a, plan, stream);
+    if (a.L.d == 256) return w ? decode_run_d256_win(a, plan, stream) : decode_run_d256(a, plan, stream);
     switch (a.L.Gk) {
         case 32: return w ? decode_run_gk32_win(a, plan, stream) : decode_run_gk32(a, plan, stream);
         case 64: return w ? decode_run_gk64_win(a, plan, stream) : decode_run_gk64(a, plan, stream);

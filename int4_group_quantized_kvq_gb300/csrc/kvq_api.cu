@@ -49,6 +49,19 @@ int check_cfg(const kvq_cache_config* c) {
     return KVQ_OK;
 }
 
+// Shapes the decode kernels take: the INT4 cache at head_dim 64, 128 or 256 (256: up to 4
+// query heads per kv head and K groups of 64 or 128, the register budget of one warp's
+// fragments); the other caches at head_dim 128.
+int check_decode_shape(const kvq_cache_config* c, int r, int codec) {
+    if (codec != 0 && c->head_dim != 128)
+        return fail(KVQ_EUNSUPPORTED, "decode attention over this cache supports head_dim 128");
+    if (c->head_dim == 256 && r > 4)
+        return fail(KVQ_EUNSUPPORTED, "head_dim 256: query heads per KV head %d > 4", r);
+    if (c->head_dim == 256 && c->group_k < 64)
+        return fail(KVQ_EUNSUPPORTED, "head_dim 256: group_k %d < 64", c->group_k);
+    return KVQ_OK;
+}
+
 int cuda_fail(cudaError_t e, const char* what) {
     return fail(KVQ_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
@@ -161,6 +174,7 @@ size_t workspace_bytes_impl(const kvq_cache_config* cfg, int32_t batch, int32_t 
         fail(KVQ_EINVAL, "invalid batch / num_q_heads / max_len");
         return 0;
     }
+    if (check_decode_shape(cfg, num_q_heads / cfg->num_kv_heads, codec) != KVQ_OK) return 0;
     kvq::DecodeArgs a{};
     a.B = batch;
     a.Hq = num_q_heads;
@@ -216,7 +230,7 @@ int decode_attention_impl(const kvq_cache_config* cfg, const void* pool, const v
         return fail(KVQ_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, cfg->num_kv_heads);
     if (num_q_heads / cfg->num_kv_heads > 8)
         return fail(KVQ_EUNSUPPORTED, "query heads per KV head %d > 8", num_q_heads / cfg->num_kv_heads);
-    if (cfg->head_dim != 128) return fail(KVQ_EUNSUPPORTED, "decode attention supports head_dim 128");
+    if (int e = check_decode_shape(cfg, num_q_heads / cfg->num_kv_heads, codec)) return e;
     if (batch > 4096) return fail(KVQ_EUNSUPPORTED, "batch %d > 4096", batch);
     if (batch == 0) return ok();
     if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
@@ -273,7 +287,7 @@ int decode_step_impl(const kvq_cache_config* cfg, void* pool, const void* k_new,
         return fail(KVQ_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, cfg->num_kv_heads);
     if (num_q_heads / cfg->num_kv_heads > 8)
         return fail(KVQ_EUNSUPPORTED, "query heads per KV head %d > 8", num_q_heads / cfg->num_kv_heads);
-    if (cfg->head_dim != 128) return fail(KVQ_EUNSUPPORTED, "the decode step supports head_dim 128");
+    if (int e = check_decode_shape(cfg, num_q_heads / cfg->num_kv_heads, 0)) return e;
     if (batch > 4096) return fail(KVQ_EUNSUPPORTED, "batch %d > 4096", batch);
     if (batch == 0) return ok();
     if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);
@@ -819,7 +833,7 @@ extern "C" int kvq_decode_attention_noalloc(const kvq_cache_config* cfg, const v
         return fail(KVQ_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, cfg->num_kv_heads);
     if (num_q_heads / cfg->num_kv_heads > 8)
         return fail(KVQ_EUNSUPPORTED, "query heads per KV head %d > 8", num_q_heads / cfg->num_kv_heads);
-    if (cfg->head_dim != 128) return fail(KVQ_EUNSUPPORTED, "decode attention supports head_dim 128");
+    if (int e = check_decode_shape(cfg, num_q_heads / cfg->num_kv_heads, 0)) return e;
     if (batch > 4096) return fail(KVQ_EUNSUPPORTED, "batch %d > 4096", batch);
     if (batch == 0) return ok();
     if (max_blocks < 1) return fail(KVQ_EINVAL, "max_blocks %d < 1", max_blocks);

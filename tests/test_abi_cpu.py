@@ -81,12 +81,18 @@ def test_null_and_misaligned_pointers_rejected_on_host(built):
     assert "aligned" in kvq.kvq_last_error()
     # nothing to do is not an error
     assert L.kvq_quantize_append(C.byref(cfg), None, None, None, None, 4, None, 0, 1, None, None) == kvq.KVQ_OK
-    # decode: ratio > 8, head_dim 64, misaligned workspace
+    # decode: ratio > 8; head_dim 256 with more than 4 query heads per kv head or K groups of
+    # 32; misaligned workspace
     assert L.kvq_decode_attention(C.byref(cfg), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 72, 10, 1.0, 0x5000,
                                   0x6000, 1 << 20, None) == kvq.KVQ_EUNSUPPORTED
-    cfg64 = kvq.config(8, 64, 16, 32, 64, 10)
-    assert L.kvq_decode_attention(C.byref(cfg64), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 8, 10, 1.0, 0x5000,
+    cfg256 = kvq.config(8, 256, 16, 64, 128, 10)
+    assert L.kvq_decode_attention(C.byref(cfg256), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 64, 10, 1.0, 0x5000,
                                   0x6000, 1 << 20, None) == kvq.KVQ_EUNSUPPORTED
+    assert "query heads" in kvq.kvq_last_error()
+    cfg256.group_k = 32
+    assert L.kvq_decode_step(C.byref(cfg256), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 4, 0x7000, 1, 8,
+                             10, 1.0, 0x8000, 0x9000, 1 << 20, None) == kvq.KVQ_EUNSUPPORTED
+    assert "group_k" in kvq.kvq_last_error()
     assert L.kvq_decode_attention(C.byref(cfg), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 8, 10, 1.0, 0x5000,
                                   0x6010, 1 << 20, None) == kvq.KVQ_EINVAL
     assert L.kvq_decode_attention(C.byref(cfg), 0x1000, 0x2000, 0x3000, 4, 0x4000, 1, 12, 10, 1.0, 0x5000,
