@@ -26,20 +26,26 @@
 //    bulk copies (the TMA engine, cp.async.bulk) that complete on per-stage mbarriers.
 //    Waits are bounded in time.
 //  * The arithmetic runs on the tensor cores (mma.sync m16n8k16, f16 inputs, f32
-//    accumulate): nibbles become exact f16 integers in two instructions per pair and
-//    the MMA does the multiply-accumulate.  For a 16-token chunk of one kv head:
+//    accumulate) and the MMA does the multiply-accumulate.  For a 16-token chunk of one
+//    kv head:
 //      scores  S[token, col] = K[token, :] . Qcol  with M = 16 tokens, N = 8 columns,
 //              K-dim = head_dim.  Column (slot, k-group) carries the slot's q masked to
 //              that group, so each group's partial dot product comes out separately
-//              and is scaled by its own fp16 scale afterwards (codes and q are exact in
-//              f16; products and sums are fp32).  With HK = 4 each kv head's chunk has
-//              its own accumulator and a thread keeps the one of its slot's head.
+//              and is scaled by its own fp16 scale afterwards.  A K nibble n enters the
+//              MMA as the f16 subnormal n * 2^-24, one mask per pair of nibbles (the
+//              high nibble of a byte as 16 n * 2^-24, its q column entries divided by
+//              16); the MMA gives 2^-24 sum_d n_d q_d exactly in fp32, and the code
+//              offset comes off per group: sum_d (n_d - 8) q_d = 2^24 S - 8 sum_d q_d,
+//              with sum_d q_d taken once per segment.  With HK = 4 each kv head's chunk
+//              has its own accumulator and a thread keeps the one of its slot's head.
 //      output  O^T[d, col] += V^T[d, token] . W[token, col] with M = 16 dims, N = 8
 //              columns (slot, hi|lo), K-dim = 16 tokens.  W = p * v_scale is split into
 //              an f16 high part and an f16 remainder, two columns of the same MMA, which
 //              keeps about 22 bits of the weight.  With HK = 4 the columns of the other
 //              heads' slots are zeroed for each head's MMA.  M-tiles never straddle a
-//              V group.
+//              V group.  V nibbles become exact f16 integers n - 8 in two instructions
+//              per pair: the offset cannot come off afterwards as for K, since there it
+//              would cancel against the sum of the weights over the whole segment.
 //    The score fragment of thread (g, c) holds tokens g, g+8 of slot c (+4), and the
 //    output fragment holds slot c (+4) too, so the softmax rescale is thread-local;
 //    only the weights are exchanged (four shuffles per chunk and V group).  With HK = 1
@@ -473,6 +479,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     }
 
     uint32_t qb[KSTEPS][NTQ][2];
+    float q8[NTQ][2];  // 8 * the sum of q over the group of this thread's score columns 2c, 2c + 1
     float m[HS], l[HS];
     float o[MT][HS][4];
     int Leff = 0;  // positions of the segment's sequence (clamped to its block table)
@@ -549,9 +556,12 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                     for (int X = 0; X < TG; ++X)
 #pragma unroll
                         for (int a = 0; a < HK; ++a) {
+                            // nibbles of bytes e and e + 2 as f16 subnormals: the low ones
+                            // n * 2^-24, the high ones 16 n * 2^-24
                             const uint32_t x = kg[X][a][wi] >> (8 * e);
                             const uint32_t y = kg8[X][a][wi] >> (8 * e);
-                            const uint32_t a0 = unpack_lo(x), a1 = unpack_lo(y), a2 = unpack_hi(x), a3 = unpack_hi(y);
+                            const uint32_t a0 = x & 0x000F000Fu, a1 = y & 0x000F000Fu;
+                            const uint32_t a2 = x & 0x00F000F0u, a3 = y & 0x00F000F0u;
 #pragma unroll
                             for (int t = 0; t < NTQ; ++t)
                                 mma_f16_16816(acc[X][a][t], a0, a1, a2, a3, qb[2 * wi + e][t][0], qb[2 * wi + e][t][1]);
@@ -584,9 +594,11 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 float z0 = 0.f, z1 = 0.f;
 #pragma unroll
                 for (int R = 0; R < NGK; ++R) {
+                    // the group's code dot product sum (n - 8) q = 2^24 S - 8 sum q
                     const int pi = s * NGK + R;
-                    z0 = fmaf(skg[R], sacc[pi >> 1][pi & 1], z0);
-                    z1 = fmaf(skg8[R], sacc[pi >> 1][2 + (pi & 1)], z1);
+                    const float qo = q8[pi >> 1][pi & 1];
+                    z0 = fmaf(skg[R], fmaf(sacc[pi >> 1][pi & 1], 16777216.0f, -qo), z0);
+                    z1 = fmaf(skg8[R], fmaf(sacc[pi >> 1][2 + (pi & 1)], 16777216.0f, -qo), z1);
                 }
                 z[X][s][0] = z0 * p.scale_log2;
                 z[X][s][1] = z1 * p.scale_log2;
@@ -818,16 +830,29 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 const int j = (g >> 1) + 4 * sigma;
                 const bool colv = sigma < HS && j < p.ns;
                 const __half* qrow = qseg + (colv ? j : 0) * D;
+                float qs = 0.f;  // this thread's part of the column's sum of q
 #pragma unroll
                 for (int wi = 0; wi < KW; ++wi) {
                     const int dbase = c * (D / 4) + 8 * wi;
                     uint4 w4 = make_uint4(0, 0, 0, 0);
                     if (colv && dbase / GK == R) w4 = *reinterpret_cast<const uint4*>(qrow + dbase);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&(&w4.x)[h]));
+                        qs += f.x + f.y;
+                    }
+                    // the entries meeting high nibbles (odd dimensions) are divided by 16
                     qb[2 * wi][t][0] = prmt(w4.x, w4.z, 0x5410u);
-                    qb[2 * wi][t][1] = prmt(w4.x, w4.z, 0x7632u);
+                    qb[2 * wi][t][1] = h2_mul(prmt(w4.x, w4.z, 0x7632u), 0x2C002C00u /* 1/16 */);
                     qb[2 * wi + 1][t][0] = prmt(w4.y, w4.w, 0x5410u);
-                    qb[2 * wi + 1][t][1] = prmt(w4.y, w4.w, 0x7632u);
+                    qb[2 * wi + 1][t][1] = h2_mul(prmt(w4.y, w4.w, 0x7632u), 0x2C002C00u);
                 }
+                // column g of n-tile t: its sum over the row group's four threads; this
+                // thread's score columns 2c and 2c + 1 are those of the threads with g = 2c, 2c + 1
+                qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+                qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+                q8[t][0] = 8.f * __shfl_sync(0xffffffffu, qs, 8 * c);
+                q8[t][1] = 8.f * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
             }
         }
         // this warp is done with the segment's q buffer (a warp with units here has waited
