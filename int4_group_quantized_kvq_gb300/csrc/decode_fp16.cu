@@ -59,7 +59,7 @@ cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s
     p.P = a.L.P;
     p.num_pages = a.num_pages;
     p.max_blocks = a.max_blocks;
-    p.block_bytes = CODEC == 2 ? a.L.P * (a.L.d + 8) : CODEC == 1 ? 2 * a.L.P * a.L.d + 8 * a.L.P : 4 * a.L.P * a.L.d;
+    p.block_bytes = CODEC == 2 ? a.L.P * (a.L.d + 8) : 4 * a.L.P * a.L.d;
     if (CODEC == 2) {
         const Wht4Codebook& cb = wht4_codebook();
         for (int j = 0; j < 16; ++j) fp.lut[j] = cb.levels[j];
@@ -90,7 +90,7 @@ cudaError_t fp16_run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s
 }  // namespace decode
 
 // query heads per kv head r in 1..8, rounded up to 1, 2, 4 or 8; window instances when a
-// window is given; INT8 blocks for the INT8 cache, rotated 4-bit blocks for that cache
+// window is given; rotated 4-bit blocks for that cache
 template <bool WIN, int CODEC>
 cudaError_t run_r(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {
     const int r = a.Hq / a.Hkv;
@@ -112,14 +112,12 @@ int occ_r(const DecodeArgs& a, size_t smem) {
 
 cudaError_t decode_run_fp16(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s) {
     if (a.wht) return a.window > 0 ? run_r<true, 2>(a, plan, s) : run_r<false, 2>(a, plan, s);
-    if (a.int8) return a.window > 0 ? run_r<true, 1>(a, plan, s) : run_r<false, 1>(a, plan, s);
     return a.window > 0 ? run_r<true, 0>(a, plan, s) : run_r<false, 0>(a, plan, s);
 }
 
 int decode_occupancy_fp16(const DecodeArgs& a, const DecodePlan& plan, size_t smem) {
     (void)plan;
     if (a.wht) return a.window > 0 ? occ_r<true, 2>(a, smem) : occ_r<false, 2>(a, smem);
-    if (a.int8) return a.window > 0 ? occ_r<true, 1>(a, smem) : occ_r<false, 1>(a, smem);
     return a.window > 0 ? occ_r<true, 0>(a, smem) : occ_r<false, 0>(a, smem);
 }
 

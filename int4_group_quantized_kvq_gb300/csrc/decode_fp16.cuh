@@ -20,9 +20,10 @@
 //  * the online softmax runs per query head on those lanes; each weight is then
 //    broadcast by a shuffle to the V accumulation.
 //
-// The same kernel serves the INT8 per-row cache and the rotated 4-bit cache (codec 1 and
-// 2): only the row reader differs, and for the rotated codec ("LARQL KV cache engines",
-// engine three; wht_codec.cu) the arithmetic runs in the rotated domain.  A row there is
+// The same kernel serves the rotated 4-bit cache (codec 2; the INT8 per-row cache runs on
+// the tensor-core kernel of decode_impl.cuh): only the row reader differs, and for the
+// rotated codec ("LARQL KV cache engines", engine three; wht_codec.cu) the arithmetic runs
+// in the rotated domain.  A row there is
 // x^ = H (sigma c) / d with H symmetric, so q . x^ = (H q / d) . (sigma c): each segment's
 // q is rotated once (and divided by d), the rows are read as sigma * c_code, and the
 // accumulated output sum_t p_t sigma_t c_t is rotated back (H / d) when the warp writes
@@ -63,10 +64,7 @@ __device__ __forceinline__ void wht128_lane4(float (&y)[4], int lane) {
 
 // One row of a staged block: this lane's 4 values (dimensions 4l .. 4l + 3) of row `row`
 // of K (is_v 0) or V (is_v 1).  CODEC 0, FP16 blocks: K rows then V rows, P x D fp16
-// each.  CODEC 1, INT8 blocks (the per-row codec of "AI inference tuning: KV Cache
-// optimisation and memory management" section 3.1): K codes P x D int8, V codes P x D
-// int8, K scales P fp32, V scales P fp32; a value is the fp32 product code * scale.
-// CODEC 2, rotated 4-bit blocks: K codes P x D/2 (nibbles, element 2j low), V codes,
+// each.  CODEC 2, rotated 4-bit blocks: K codes P x D/2 (nibbles, element 2j low), V codes,
 // K sigma P fp32, V sigma P fp32; a value is sigma * lut[code], in the rotated domain.
 // The reader returns lut[code] only: the row's sigma (row_sigma) multiplies the reduced
 // score and the softmax weight instead of every value.
@@ -77,14 +75,6 @@ __device__ __forceinline__ void block_row4(const uint8_t* blk, int P, int is_v, 
         const uint32_t w = *reinterpret_cast<const uint16_t*>(blk + (is_v * P + row) * (D / 2) + 2 * lane);
 #pragma unroll
         for (int j = 0; j < 4; ++j) x[j] = lut[(w >> (4 * j)) & 15u];
-    } else if constexpr (CODEC == 1) {
-        // code c (int8) -> c + 128 in the low mantissa byte of 2^23: the float 2^23 + 128 + c,
-        // minus 2^23 + 128, is c exactly (one byte permute and one add per value)
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(blk + (is_v * P + row) * D + 4 * lane) ^ 0x80808080u;
-        const float s = *reinterpret_cast<const float*>(blk + 2 * P * D + 4 * (is_v * P + row));
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            x[j] = (__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + j)) - 8388736.0f) * s;
     } else {
         const uint2 w = *reinterpret_cast<const uint2*>(blk + ((is_v * P + row) * D + 4 * lane) * 2);
         const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
@@ -104,10 +94,11 @@ __device__ __forceinline__ float row_sigma(const uint8_t* blk, int P, int is_v, 
 
 // R: query heads per kv head, rounded up to 1, 2, 4 or 8.  WIN: the sequences list only
 // their window and sink pages (p.window > 0), as in decode_splitkv_kernel.  CODEC: 0 FP16,
-// 1 INT8 per-row, 2 rotated 4-bit blocks.
+// 2 rotated 4-bit blocks.
 template <int D, int R, bool WIN, int CODEC = 0>
 __global__ void __launch_bounds__(128, 1) decode_fp16_kernel(const __grid_constant__ FParams f) {
     static_assert(D == 128, "four dimensions per lane");
+    static_assert(CODEC == 0 || CODEC == 2, "FP16 or rotated 4-bit blocks");
     const KParams& p = f.p;
     constexpr int kWarps = 4;
     constexpr int T = R == 8 ? 8 : 16;   // tokens per step

@@ -46,6 +46,10 @@
 //              V group.  V nibbles become exact f16 integers n - 8 in two instructions
 //              per pair: the offset cannot come off afterwards as for K, since there it
 //              would cancel against the sum of the weights over the whole segment.
+//    The INT8 per-row cache runs on the same kernel (CODEC 1): one-head units, one group
+//    per row with an fp32 scale, K codes entering the score MMA as the f16 subnormals
+//    (c + 128) * 2^-24 (one byte permute per pair, the offset removed per row as above)
+//    and V codes as exact f16 integers.
 //    The score fragment of thread (g, c) holds tokens g, g+8 of slot c (+4), and the
 //    output fragment holds slot c (+4) too, so the softmax rescale is thread-local;
 //    only the weights are exchanged (four shuffles per chunk and V group).  With HK = 1
@@ -312,23 +316,40 @@ __device__ __noinline__ void append_rows(const KParams& p, const int32_t* aps, u
     }
 }
 
+// Scale i of a run of per-token scales at p: fp16 (the INT4 cache's per group) or fp32
+// (the INT8 cache's per row).
+template <bool F32>
+__device__ __forceinline__ float load_scale(const uint8_t* p, int i) {
+    if constexpr (F32) return reinterpret_cast<const float*>(p)[i];
+    else return __half2float(reinterpret_cast<const __half*>(p)[i]);
+}
+
 // P16: the pages hold 16 tokens (P == 16), so two one-head units, i.e. two pages, make a
 // step; the instances for larger pages (P16 false) take two 16-token chunks of one page.
 // Each instance carries only its own path, which keeps the loop's code small.
-template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16>
+// CODEC 0: the INT4 cache (nibble codes, fp16 scales per group).  CODEC 1: the INT8
+// per-row cache ("AI inference tuning: KV Cache optimisation and memory management"
+// section 3.1): K codes P x D int8, V codes P x D int8, K scales P fp32, V scales P fp32
+// per block, a value being code * scale; it runs with one group per row (GK = GV = D) and
+// one-head units, and has no fused append.
+template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16, int CODEC = 0>
 __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decode_splitkv_kernel(KParams p) {
     static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
+    static_assert(CODEC == 0 || (CODEC == 1 && D == 128 && GK == D && GV == D && HK == 1), "INT8: d 128, rows");
     static_assert(D <= 128 || (HK == 1 && HS == 1), "head_dim 256: one-head units, up to 4 query heads each");
     static_assert(HK == 1 || HS == 1, "several kv heads per unit only with one query head each");
     static_assert(HK == 1 || P16, "four-head units only for 16-token pages");
     constexpr int NGK = D / GK;               // K groups per row
     constexpr int NGV = D / GV;               // V groups per row
-    constexpr int KW = D / 32;                // K code words per thread per token row
+    constexpr bool I8 = CODEC == 1;
+    constexpr int KW = I8 ? D / 16 : D / 32;  // K code words per thread per token row
     constexpr int KSTEPS = D / 16;            // MMA k-steps over head_dim
     constexpr int NTQ = (HS * NGK + 1) / 2;   // score n-tiles
     constexpr int VB = GV / 16;               // V code bytes per thread per group per row
     constexpr int MT = D / 16;                // output m-tiles
-    constexpr int ROW = D / 2;                // bytes of one token's codes
+    constexpr int ROW = I8 ? D : D / 2;       // bytes of one token's codes
+    constexpr int SB = I8 ? 4 : 2;            // bytes of one scale (fp32 per row, fp16 per group)
+    constexpr float kOff = I8 ? 128.f : 8.f;  // the offset of the codes entering the score MMA
     constexpr int TG = HK == 1 ? 2 : 1;       // 16-token chunks per step
     constexpr int kWarps = cta_warps<HS>();   // warps per CTA
     static_assert(NGV * VB == MT, "m-tiles cover head_dim");
@@ -400,7 +421,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 if (lane == 0) raise_flag(p.status, KVQ_FLAG_BAD_PAGE);
                 continue;
             }
-            append_rows<D, HK>(p, aps, nullptr, sb, shg, static_cast<int>(apg));
+            if constexpr (!I8) append_rows<D, HK>(p, aps, nullptr, sb, shg, static_cast<int>(apg));
         }
     };
 
@@ -479,7 +500,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     }
 
     uint32_t qb[KSTEPS][NTQ][2];
-    float q8[NTQ][2];  // 8 * the sum of q over the group of this thread's score columns 2c, 2c + 1
+    float q8[NTQ][2];  // kOff * the sum of q over the group of this thread's score columns 2c, 2c + 1
     float m[HS], l[HS];
     float o[MT][HS][4];
     int Leff = 0;  // positions of the segment's sequence (clamped to its block table)
@@ -491,10 +512,10 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     const int a_row = HK == 1 ? 0 : c;
     const int a_col = HK == 1 ? 0 : (g >> 1);
     // per-thread byte offsets inside a unit buffer (chunk 0)
-    const int k_off = g * ROW + c * (D / 8);
-    const int ks_off = a_row * bbytes + p.k_scales + g * NGK * 2;
-    const int vs_off = a_row * bbytes + p.v_scales + g * NGV * 2;
-    const int v_off = p.v_codes + c * ROW + g * VB;
+    const int k_off = g * ROW + c * (KW * 4);
+    const int ks_off = a_row * bbytes + p.k_scales + g * NGK * SB;
+    const int vs_off = a_row * bbytes + p.v_scales + g * NGV * SB;
+    const int v_off = p.v_codes + c * ROW + g * (I8 ? 16 : VB);
     const int src0 = 4 * c + (g >> 1);
     const int src1 = 4 * (c + 4) + (g >> 1);
     const bool want_lo = (g & 1) != 0;
@@ -548,24 +569,40 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                     for (int t = 0; t < NTQ; ++t)
                         acc[X][a][t][0] = acc[X][a][t][1] = acc[X][a][t][2] = acc[X][a][t][3] = 0.f;
                 }
+            if constexpr (I8) {
+                // word j of a row is k-step j: its bytes' codes c, as c + 128, become the f16
+                // subnormals (c + 128) * 2^-24 (bytes 0, 1 and bytes 2, 3 paired)
 #pragma unroll
-            for (int wi = 0; wi < KW; ++wi)
+                for (int j = 0; j < KW; ++j)
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
+                    for (int X = 0; X < TG; ++X) {
+                        const uint32_t x = kg[X][0][j] ^ 0x80808080u, y = kg8[X][0][j] ^ 0x80808080u;
+                        const uint32_t a0 = prmt(x, 0u, 0x5140u), a1 = prmt(y, 0u, 0x5140u);
+                        const uint32_t a2 = prmt(x, 0u, 0x7362u), a3 = prmt(y, 0u, 0x7362u);
 #pragma unroll
-                    for (int X = 0; X < TG; ++X)
+                        for (int t = 0; t < NTQ; ++t) mma_f16_16816(acc[X][0][t], a0, a1, a2, a3, qb[j][t][0], qb[j][t][1]);
+                    }
+            } else {
 #pragma unroll
-                        for (int a = 0; a < HK; ++a) {
-                            // nibbles of bytes e and e + 2 as f16 subnormals: the low ones
-                            // n * 2^-24, the high ones 16 n * 2^-24
-                            const uint32_t x = kg[X][a][wi] >> (8 * e);
-                            const uint32_t y = kg8[X][a][wi] >> (8 * e);
-                            const uint32_t a0 = x & 0x000F000Fu, a1 = y & 0x000F000Fu;
-                            const uint32_t a2 = x & 0x00F000F0u, a3 = y & 0x00F000F0u;
+                for (int wi = 0; wi < KW; ++wi)
 #pragma unroll
-                            for (int t = 0; t < NTQ; ++t)
-                                mma_f16_16816(acc[X][a][t], a0, a1, a2, a3, qb[2 * wi + e][t][0], qb[2 * wi + e][t][1]);
-                        }
+                    for (int e = 0; e < 2; ++e)
+#pragma unroll
+                        for (int X = 0; X < TG; ++X)
+#pragma unroll
+                            for (int a = 0; a < HK; ++a) {
+                                // nibbles of bytes e and e + 2 as f16 subnormals: the low ones
+                                // n * 2^-24, the high ones 16 n * 2^-24
+                                const uint32_t x = kg[X][a][wi] >> (8 * e);
+                                const uint32_t y = kg8[X][a][wi] >> (8 * e);
+                                const uint32_t a0 = x & 0x000F000Fu, a1 = y & 0x000F000Fu;
+                                const uint32_t a2 = x & 0x00F000F0u, a3 = y & 0x00F000F0u;
+#pragma unroll
+                                for (int t = 0; t < NTQ; ++t)
+                                    mma_f16_16816(acc[X][a][t], a0, a1, a2, a3, qb[2 * wi + e][t][0],
+                                                  qb[2 * wi + e][t][1]);
+                            }
+            }
         }
         float z[TG][HS][2];
 #pragma unroll
@@ -581,20 +618,19 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                     for (int a = 1; a < HK; ++a) v = a_row == a ? acc[X][a][t][k] : v;
                     sacc[t][k] = v;
                 }
-            const __half* s0 = reinterpret_cast<const __half*>(blk[X] + chk[X] * 16 * NGK * 2 + ks_off);
-            const __half* s1 = s0 + 8 * NGK;
+            const uint8_t* s0 = blk[X] + chk[X] * 16 * NGK * SB + ks_off;
             float skg[NGK], skg8[NGK];
 #pragma unroll
             for (int R = 0; R < NGK; ++R) {
-                skg[R] = __half2float(s0[R]);
-                skg8[R] = __half2float(s1[R]);
+                skg[R] = load_scale<I8>(s0, R);
+                skg8[R] = load_scale<I8>(s0, 8 * NGK + R);
             }
 #pragma unroll
             for (int s = 0; s < HS; ++s) {
                 float z0 = 0.f, z1 = 0.f;
 #pragma unroll
                 for (int R = 0; R < NGK; ++R) {
-                    // the group's code dot product sum (n - 8) q = 2^24 S - 8 sum q
+                    // the group's code dot product sum (n - off) q = 2^24 S - off sum q
                     const int pi = s * NGK + R;
                     const float qo = q8[pi >> 1][pi & 1];
                     z0 = fmaf(skg[R], fmaf(sacc[pi >> 1][pi & 1], 16777216.0f, -qo), z0);
@@ -654,13 +690,12 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
         uint32_t bv[TG][HS][NGV][2];
 #pragma unroll
         for (int X = 0; X < TG; ++X) {
-            const __half* s0 = reinterpret_cast<const __half*>(blk[X] + chk[X] * 16 * NGV * 2 + vs_off);
-            const __half* s1 = s0 + 8 * NGV;
+            const uint8_t* s0 = blk[X] + chk[X] * 16 * NGV * SB + vs_off;
             float svg[NGV], svg8[NGV];
 #pragma unroll
             for (int R = 0; R < NGV; ++R) {
-                svg[R] = __half2float(s0[R]);
-                svg8[R] = __half2float(s1[R]);
+                svg[R] = load_scale<I8>(s0, R);
+                svg8[R] = load_scale<I8>(s0, 8 * NGV + R);
             }
 #pragma unroll
             for (int s = 0; s < HS; ++s) {
@@ -698,6 +733,32 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                     for (int s = 0; s < HS; ++s) {
                         b0[s] = (HK == 1 || a_col == a) ? bv[X][s][R][0] : 0u;
                         b1[s] = (HK == 1 || a_col == a) ? bv[X][s][R][1] : 0u;
+                    }
+                    if constexpr (I8) {
+                        // this thread's 16 bytes of the rows of tokens c, c + 8, c + 4, c + 12;
+                        // m-tile mt takes bytes 2 mt (rows g) and 2 mt + 1 (rows g + 8), a code c
+                        // as the exact f16 integer (1024 + c + 128) - 1152
+                        const uint8_t* vcodes = blk[X] + chk[X] * 16 * ROW + v_off;
+                        const uint4 ta = *reinterpret_cast<const uint4*>(vcodes);
+                        const uint4 tb = *reinterpret_cast<const uint4*>(vcodes + 8 * ROW);
+                        const uint4 tc = *reinterpret_cast<const uint4*>(vcodes + 4 * ROW);
+                        const uint4 td = *reinterpret_cast<const uint4*>(vcodes + 12 * ROW);
+                        const uint32_t va[4] = {ta.x, ta.y, ta.z, ta.w}, vb[4] = {tb.x, tb.y, tb.z, tb.w};
+                        const uint32_t vc[4] = {tc.x, tc.y, tc.z, tc.w}, vd[4] = {td.x, td.y, td.z, td.w};
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            const uint32_t bo = 2u * static_cast<uint32_t>(mt % 2);
+                            const uint32_t sel = bo | ((bo + 4) << 4) | ((bo + 1) << 8) | ((bo + 5) << 12);
+                            const uint32_t tac = prmt(va[mt / 2], vb[mt / 2], sel) ^ 0x80808080u;  // tokens c, c+8
+                            const uint32_t tbd = prmt(vc[mt / 2], vd[mt / 2], sel) ^ 0x80808080u;  // c+4, c+12
+                            const uint32_t a0 = h2_sub(prmt(tac, 0x64646464u, 0x5140u), 0x64806480u);
+                            const uint32_t a1 = h2_sub(prmt(tac, 0x64646464u, 0x7362u), 0x64806480u);
+                            const uint32_t a2 = h2_sub(prmt(tbd, 0x64646464u, 0x5140u), 0x64806480u);
+                            const uint32_t a3 = h2_sub(prmt(tbd, 0x64646464u, 0x7362u), 0x64806480u);
+#pragma unroll
+                            for (int s = 0; s < HS; ++s) mma_f16_16816(o[mt][s], a0, a1, a2, a3, b0[s], b1[s]);
+                        }
+                        continue;
                     }
                     uint32_t va[(VB + 3) / 4], vb[(VB + 3) / 4], vc[(VB + 3) / 4], vd[(VB + 3) / 4];
                     const uint8_t* vcodes = blk[X] + a * bbytes + chk[X] * 16 * ROW + v_off + R * (GV / 2);
@@ -831,8 +892,21 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 const bool colv = sigma < HS && j < p.ns;
                 const __half* qrow = qseg + (colv ? j : 0) * D;
                 float qs = 0.f;  // this thread's part of the column's sum of q
+                if constexpr (I8) {
+                    // k-step j: dimensions c (D / 4) + 4 j .. + 3, in order
 #pragma unroll
-                for (int wi = 0; wi < KW; ++wi) {
+                    for (int j = 0; j < KW; ++j) {
+                        uint2 w2 = make_uint2(0, 0);
+                        if (colv) w2 = *reinterpret_cast<const uint2*>(qrow + c * (D / 4) + 4 * j);
+                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&w2.x));
+                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&w2.y));
+                        qs += f0.x + f0.y + f1.x + f1.y;
+                        qb[j][t][0] = w2.x;
+                        qb[j][t][1] = w2.y;
+                    }
+                }
+#pragma unroll
+                for (int wi = 0; wi < (I8 ? 0 : KW); ++wi) {
                     const int dbase = c * (D / 4) + 8 * wi;
                     uint4 w4 = make_uint4(0, 0, 0, 0);
                     if (colv && dbase / GK == R) w4 = *reinterpret_cast<const uint4*>(qrow + dbase);
@@ -851,8 +925,8 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 // thread's score columns 2c and 2c + 1 are those of the threads with g = 2c, 2c + 1
                 qs += __shfl_xor_sync(0xffffffffu, qs, 1);
                 qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-                q8[t][0] = 8.f * __shfl_sync(0xffffffffu, qs, 8 * c);
-                q8[t][1] = 8.f * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
+                q8[t][0] = kOff * __shfl_sync(0xffffffffu, qs, 8 * c);
+                q8[t][1] = kOff * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
             }
         }
         // this warp is done with the segment's q buffer (a warp with units here has waited
@@ -898,8 +972,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 const int rA = WIN ? span_page(sspan, pg) : pg;
                 const int rB = WIN ? span_page(sspan, pg + kWarps) : pg + kWarps;
                 // the page taking this step's appended token is patched before it is used
-                if (apg_seg >= 0 && (rA == apg_seg || (n == 2 && rB == apg_seg)))
-                    append_rows<D, HK>(p, aps, ring + (rA == apg_seg ? cst : st1) * ubytes, b, hg, apg_seg);
+                if constexpr (!I8)
+                    if (apg_seg >= 0 && (rA == apg_seg || (n == 2 && rB == apg_seg)))
+                        append_rows<D, HK>(p, aps, ring + (rA == apg_seg ? cst : st1) * ubytes, b, hg, apg_seg);
                 // every position of [t, t + w) attended, and some of it attended
                 auto all_in = [&](int t, int w) { return t + w <= Leff && (!WIN || t >= wlo || t + w <= p.sinks); };
                 auto any_in = [&](int t, int w) { return !WIN || (min(t + w, Leff) > wlo || t < p.sinks); };
@@ -1060,11 +1135,11 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
 
 // Raise the kernel's dynamic shared-memory limit once to the largest size asked for,
 // so repeated calls (and calls under stream capture) only launch.
-template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16>
+template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16, int CODEC = 0>
 cudaError_t ensure_smem_attr(size_t smem) {
     static std::atomic<long long> granted{-1};
     if (static_cast<long long>(smem) <= granted.load(std::memory_order_acquire)) return cudaSuccess;
-    const cudaError_t err = cudaFuncSetAttribute(decode_splitkv_kernel<D, GK, GV, HK, HS, WIN, P16>,
+    const cudaError_t err = cudaFuncSetAttribute(decode_splitkv_kernel<D, GK, GV, HK, HS, WIN, P16, CODEC>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) cudaGetLastError();  // a refused size must not linger as the last error
     if (err == cudaSuccess) {
@@ -1077,7 +1152,7 @@ cudaError_t ensure_smem_attr(size_t smem) {
 
 // Resident CTAs per SM for a given shared-memory size, memoised per size (a few sizes
 // per shape are asked for; the slots fill once and later calls only read them).
-template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16>
+template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16, int CODEC = 0>
 int occupancy(size_t smem) {
     constexpr int kSlots = 32;
     static std::atomic<long long> memo[kSlots];  // (smem << 8) | ctas, 0 = empty
@@ -1086,9 +1161,9 @@ int occupancy(size_t smem) {
         if (m == 0) break;
         if ((m >> 8) == static_cast<long long>(smem)) return static_cast<int>(m & 0xff);
     }
-    if (ensure_smem_attr<D, GK, GV, HK, HS, WIN, P16>(smem) != cudaSuccess) return 0;
+    if (ensure_smem_attr<D, GK, GV, HK, HS, WIN, P16, CODEC>(smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN, P16>, cta_warps<HS>() * 32,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN, P16, CODEC>, cta_warps<HS>() * 32,
                                                       smem) != cudaSuccess)
         return 0;
     const long long entry = (static_cast<long long>(smem) << 8) | (n & 0xff);
@@ -1099,7 +1174,7 @@ int occupancy(size_t smem) {
     return n;
 }
 
-template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16>
+template <int D, int GK, int GV, int HK, int HS, bool WIN, bool P16, int CODEC = 0>
 cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     KParams p;
     p.pool = a.pool;
@@ -1124,11 +1199,17 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     p.num_pages = a.num_pages;
     p.max_blocks = a.max_blocks;
     p.block_bytes = a.L.bytes;
-    p.unit_bytes = a.L.bytes * HK;
-    p.stages = plan.stages;
     p.v_codes = a.L.v_codes;
     p.k_scales = a.L.k_scales;
     p.v_scales = a.L.v_scales;
+    if (CODEC == 1) {  // the INT8 block: K codes, V codes (P x D bytes each), K and V scales (P fp32 each)
+        p.block_bytes = 2 * a.L.P * D + 8 * a.L.P;
+        p.v_codes = a.L.P * D;
+        p.k_scales = 2 * a.L.P * D;
+        p.v_scales = 2 * a.L.P * D + 4 * a.L.P;
+    }
+    p.unit_bytes = p.block_bytes * HK;
+    p.stages = plan.stages;
     p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
     p.k_new = a.k_new;
     p.v_new = a.v_new;
@@ -1142,7 +1223,7 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     while ((8 << p.lg_lk) < a.L.Gk) ++p.lg_lk;
     p.lg_lv = 0;
     while ((8 << p.lg_lv) < a.L.Gv) ++p.lg_lv;
-    cudaError_t err = ensure_smem_attr<D, GK, GV, HK, HS, WIN, P16>(plan.smem_bytes);
+    cudaError_t err = ensure_smem_attr<D, GK, GV, HK, HS, WIN, P16, CODEC>(plan.smem_bytes);
     if (err != cudaSuccess) return err;
     // The launch may start before the kernel ahead of it on the stream finishes
     // (programmatic dependent launch); the kernel waits with griddepcontrol.wait before
@@ -1157,7 +1238,7 @@ cudaError_t run(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN, P16>, p);
+    err = cudaLaunchKernelEx(&cfg, decode_splitkv_kernel<D, GK, GV, HK, HS, WIN, P16, CODEC>, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

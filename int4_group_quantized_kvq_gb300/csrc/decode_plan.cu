@@ -42,6 +42,8 @@ int decode_occupancy_d256_win(const DecodeArgs& a, const DecodePlan& plan, size_
 cudaError_t launch_combine(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 cudaError_t decode_run_fp16(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
 int decode_occupancy_fp16(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
+cudaError_t decode_run_int8(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t s);
+int decode_occupancy_int8(const DecodeArgs& a, const DecodePlan& plan, size_t smem);
 
 namespace {
 constexpr int kMaxStages = 8;           // deepest unit ring per warp
@@ -84,6 +86,7 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
                kCtlBytes + round_up(static_cast<size_t>(3 * a.B + 1) * 4, 16);
     };
     auto occ_for = [&](size_t smem) {
+        if (a.int8) return decode_occupancy_int8(a, *plan, smem);
         if (a.fp16) return decode_occupancy_fp16(a, *plan, smem);
         const bool w = a.window > 0;
         if (a.L.d == 64) return w ? decode_occupancy_d64_win(a, *plan, smem) : decode_occupancy_d64(a, *plan, smem);
@@ -145,6 +148,7 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
 }
 
 cudaError_t launch_decode_grid(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
+    if (a.int8) return decode_run_int8(a, plan, stream);
     if (a.fp16) return decode_run_fp16(a, plan, stream);
     const bool w = a.window > 0;
     if (a.L.d == 64) return w ? decode_run_d64_win(a, plan, stream) : decode_run_d64(a, plan, stream);
