@@ -258,20 +258,24 @@ def time_oracle_quantize(wl, budget_s: float) -> dict:
     import oracle
     import workloads as W
     n_max = wl.seq_lens[0]
-    k = W.kv_tensor(W.SEED_K, (1, n_max, wl.Hkv, wl.d), 20.0, W.outlier_channels(wl.Hkv, wl.d)).numpy()
-    v = W.kv_tensor(W.SEED_V, (1, n_max, wl.Hkv, wl.d)).numpy()
     npg = (n_max + wl.P - 1) // wl.P
     L = oracle.Layout(wl.Hkv, wl.d, wl.P, wl.Gk, wl.Gv, npg)
     pool = np.zeros(L.pool_bytes, np.uint8)
     bt = np.arange(npg, dtype=np.int32).reshape(1, -1)
     per_token = wl.Hkv * (2 * wl.d * 2 + wl.packed_bytes_per_token_head())
+
+    def rows(n):  # the first n tokens of sequence 0 (the generator is counter-indexed, so a prefix is exact)
+        k = W.kv_tensor(W.SEED_K, (1, n, wl.Hkv, wl.d), 20.0, W.outlier_channels(wl.Hkv, wl.d)).numpy()
+        return k, W.kv_tensor(W.SEED_V, (1, n, wl.Hkv, wl.d)).numpy()
     n = min(n_max, 64)
+    k, v = rows(n)
     t0 = time.perf_counter()
-    oracle.quantize_append(L, pool, k[:, :n], v[:, :n], bt, np.zeros(1, np.int32))
+    oracle.quantize_append(L, pool, k, v, bt, np.zeros(1, np.int32))
     per_tok_s = max((time.perf_counter() - t0) / n, 1e-9)
     n = int(max(16, min(n_max, budget_s / per_tok_s)))
+    k, v = rows(n)
     t0 = time.perf_counter()
-    oracle.quantize_append(L, pool, k[:, :n], v[:, :n], bt, np.zeros(1, np.int32))
+    oracle.quantize_append(L, pool, k, v, bt, np.zeros(1, np.int32))
     t = time.perf_counter() - t0
     return {"value": n * per_token / t / 1e9, "unit": "GB/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{wl.name}: sequence 0, {n} of {n_max} tokens x {wl.Hkv} KV heads, K and V; "
@@ -708,6 +712,16 @@ def run_kvq(args, world, rank, local):
         res["cpu_baseline"] = time_oracle(wl, args.cpu_seconds)
         res["cpu_baseline"].pop("seconds_per_step", None)
         res["cpu_baseline"]["quantize"] = time_oracle_quantize(wl, 2.0)
+        if not args.no_sweep:
+            # the oracle on the other configurations too, a short sample each
+            per_cfg = {}
+            for name, G in (("gqa8b", None), ("ragged", None), ("longctx", 64)):
+                w = make_workload(name, G)
+                per_cfg[w.name] = time_oracle(w, 1.0)
+                per_cfg[w.name].pop("seconds_per_step", None)
+            w5 = make_workload("longctx", 64)
+            per_cfg["prefill_quantize_" + w5.name] = time_oracle_quantize(w5, 1.0)
+            res["cpu_baseline"]["configs"] = per_cfg
     return res
 
 
