@@ -89,59 +89,144 @@ __device__ __forceinline__ void wht128(float (&y)[4], int lane) {
     }
 }
 
-// One warp per K or V row (rows in the order (b, t, h), K before V).
+// The row's codes for the 8 values a lane holds (row elements 8 tl .. 8 tl + 7, a team of
+// 16 lanes per row), and the row's sigma.  Every step is the oracle's, in its order:
+//  * sigma^2: squares summed in fours ((y0^2 + y1^2) + (y2^2 + y3^2), elements 4g .. 4g+3),
+//    then the 32 sums pairwise at index distances 16, 8, 4, 2, 1 -- here lane distances 8,
+//    4, 2, 1 for both of the lane's sums, then the lane's two sums;
+//  * the transform's stages of span 1, 2, 4 inside the lane and 8 .. 64 across lanes at xor
+//    distances 1 .. 8, the lower element of a pair becoming a + b and the upper a - b;
+//  * u = y / sigma (IEEE division), the code the number of thresholds <= u, found by a
+//    binary search over the 15 ascending thresholds (the same count as a linear scan, NaN
+//    counting none); no codes (all 0) when sigma is not positive.
+__device__ __forceinline__ uint32_t wht4_lane8(uint4 raw, const float* thr, int tl, float& sigma_out) {
+    float y[8];
+    {
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+            y[2 * k] = f.x;
+            y[2 * k + 1] = f.y;
+        }
+    }
+    float s0 = __fadd_rn(__fadd_rn(__fmul_rn(y[0], y[0]), __fmul_rn(y[1], y[1])),
+                         __fadd_rn(__fmul_rn(y[2], y[2]), __fmul_rn(y[3], y[3])));
+    float s1 = __fadd_rn(__fadd_rn(__fmul_rn(y[4], y[4]), __fmul_rn(y[5], y[5])),
+                         __fadd_rn(__fmul_rn(y[6], y[6]), __fmul_rn(y[7], y[7])));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) {
+        s0 = __fadd_rn(s0, __shfl_xor_sync(0xffffffffu, s0, off));
+        s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, off));
+    }
+    const float sigma = __fsqrt_rn(__fadd_rn(s0, s1));
+    sigma_out = sigma;
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if ((j & h) == 0) {
+                const float a = y[j], b = y[j + h];
+                y[j] = __fadd_rn(a, b);
+                y[j + h] = __fsub_rn(a, b);
+            }
+#pragma unroll
+    for (int X = 1; X < 16; X <<= 1) {
+        const bool upper = (tl & X) != 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, y[j], X);
+            y[j] = upper ? __fsub_rn(other, y[j]) : __fadd_rn(y[j], other);
+        }
+    }
+    uint32_t packed = 0;
+    if (sigma > 0.f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float u = __fdiv_rn(y[j], sigma);
+            int c = u >= thr[7] ? 8 : 0;
+            c += u >= thr[c + 3] ? 4 : 0;
+            c += u >= thr[c + 1] ? 2 : 0;
+            c += u >= thr[c] ? 1 : 0;
+            packed |= static_cast<uint32_t>(c) << (4 * j);
+        }
+    }
+    return packed;
+}
+
+// Work mapping as in the INT4 quantize kernel: rows (a token of one kv head, in the order
+// (b, t, h)) go to warps in blocks of 32, lane l looking up where row l goes; a job is the
+// K or the V row of a row, held by a team of 16 lanes, 8 values a lane; the warp takes a
+// block's 64 jobs four at a time, loading the next pass's rows before it computes.
 __global__ void __launch_bounds__(256) wht4_quantize_kernel(Wht4QuantArgs w) {
     const Fp16AppendArgs& a = w.a;
+    __shared__ float thr[16];
+    if (threadIdx.x < 15) thr[threadIdx.x] = w.thr[threadIdx.x];
+    __syncthreads();
+    constexpr int LPR = 16, TEAMS = 2, U = 2, JPP = TEAMS * U, PASSES = 64 / JPP;
     const int lane = threadIdx.x & 31;
-    const long long rows = 2LL * a.B * a.n_new * a.Hkv;
-    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const int team = lane / LPR;
+    const int tl = lane % LPR;
+    const long long rows = static_cast<long long>(a.B) * a.n_new * a.Hkv;
+    const long long blocks = (rows + 31) / 32;
     const long long block_bytes = static_cast<long long>(a.P) * (128 + 8);
-    for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-         r += nwarps) {
-        const int is_v = static_cast<int>(r & 1);
-        const long long row = r >> 1;  // (b * n_new + t) * Hkv + h
-        const int h = static_cast<int>(row % a.Hkv);
-        const long long bt_ = row / a.Hkv;
-        const int t = static_cast<int>(bt_ % a.n_new);
-        const int b = static_cast<int>(bt_ / a.n_new);
-        const long long pos = static_cast<long long>(a.start_pos[b]) + t;
-        const long long pidx = pos >= 0 ? pos / a.P : -1;
-        if (pidx < 0 || pidx >= a.max_blocks) {
-            if (lane == 0 && is_v == 0) raise_flag(a.status, KVQ_FLAG_BAD_POSITION);
-            continue;
+    const long long warp_global = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+    const long long warps_total = static_cast<long long>(gridDim.x) * blockDim.x / 32;
+    auto load = [&](long long row0, int ps, uint4 (&raw)[U]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int jl = ps * JPP + u * TEAMS + team;
+            const long long row = row0 + (jl >> 1);
+            raw[u] = make_uint4(0, 0, 0, 0);
+            if (row < rows) raw[u] = __ldcs(reinterpret_cast<const uint4*>(((jl & 1) ? a.v : a.k) + row * 128) + tl);
         }
-        const int page = a.block_table[static_cast<long long>(b) * a.max_blocks + pidx];
-        if (page < 0 || page >= a.num_pages) {
-            if (lane == 0 && is_v == 0) raise_flag(a.status, KVQ_FLAG_BAD_PAGE);
-            continue;
-        }
-        const int slot = static_cast<int>(pos % a.P);
-        const __half* src = (is_v ? a.v : a.k) + row * 128;
-        const uint2 raw = reinterpret_cast<const uint2*>(src)[lane];
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-        float y[4] = {f0.x, f0.y, f1.x, f1.y};
-        float ss = __fadd_rn(__fadd_rn(__fmul_rn(y[0], y[0]), __fmul_rn(y[1], y[1])),
-                             __fadd_rn(__fmul_rn(y[2], y[2]), __fmul_rn(y[3], y[3])));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
-        const float sigma = __fsqrt_rn(ss);
-        wht128(y, lane);
-        uint32_t packed = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            int code = 0;
-            if (sigma > 0.f) {
-                const float u = __fdiv_rn(y[j], sigma);
-#pragma unroll
-                for (int k = 0; k < 15; ++k) code += u >= w.thr[k] ? 1 : 0;
+    };
+    for (long long blk = warp_global; blk < blocks; blk += warps_total) {
+        const long long row0 = blk * 32;
+        unsigned long long my_dst = 0ull;  // the row's block, or 0 when past the end or skipped (flagged)
+        int my_slot = 0;
+        if (row0 + lane < rows) {
+            const long long row = row0 + lane;  // (b * n_new + t) * Hkv + h
+            const int h = static_cast<int>(row % a.Hkv);
+            const long long tok = row / a.Hkv;
+            const int b = static_cast<int>(tok / a.n_new);
+            const long long pos = static_cast<long long>(a.start_pos[b]) + (tok - static_cast<long long>(b) * a.n_new);
+            const long long pidx = pos >= 0 ? pos / a.P : -1;
+            if (pidx < 0 || pidx >= a.max_blocks) {
+                raise_flag(a.status, KVQ_FLAG_BAD_POSITION);
+            } else {
+                const int page = a.block_table[static_cast<long long>(b) * a.max_blocks + pidx];
+                if (page < 0 || page >= a.num_pages) {
+                    raise_flag(a.status, KVQ_FLAG_BAD_PAGE);
+                } else {
+                    my_slot = static_cast<int>(pos - pidx * a.P);
+                    my_dst = reinterpret_cast<unsigned long long>(a.pool16 +
+                                                                  (static_cast<long long>(page) * a.Hkv + h) * block_bytes);
+                }
             }
-            packed |= static_cast<uint32_t>(code) << (4 * j);
         }
-        uint8_t* blk = a.pool16 + (static_cast<long long>(page) * a.Hkv + h) * block_bytes;
-        *reinterpret_cast<uint16_t*>(blk + (static_cast<long long>(is_v) * a.P + slot) * 64 + 2 * lane) =
-            static_cast<uint16_t>(packed);
-        if (lane == 0) *reinterpret_cast<float*>(blk + 128LL * a.P + 4LL * (is_v * a.P + slot)) = sigma;
+        uint4 raw[U];
+        load(row0, 0, raw);
+#pragma unroll 1
+        for (int ps = 0; ps < PASSES; ++ps) {
+            uint4 nxt[U];
+            if (ps + 1 < PASSES) load(row0, ps + 1, nxt);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int jl = ps * JPP + u * TEAMS + team;
+                const int is_v = jl & 1;
+                float sigma;
+                const uint32_t codes = wht4_lane8(raw[u], thr, tl, sigma);
+                const unsigned long long dst = __shfl_sync(0xffffffffu, my_dst, jl >> 1);
+                const int slot = __shfl_sync(0xffffffffu, my_slot, jl >> 1);
+                if (dst == 0ull) continue;
+                uint8_t* blkp = reinterpret_cast<uint8_t*>(dst);
+                reinterpret_cast<uint32_t*>(blkp + (static_cast<long long>(is_v) * a.P + slot) * 64)[tl] = codes;
+                if (tl == 0) *reinterpret_cast<float*>(blkp + 128LL * a.P + 4LL * (is_v * a.P + slot)) = sigma;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) raw[u] = nxt[u];
+        }
     }
 }
 
@@ -209,7 +294,7 @@ const Wht4Codebook& wht4_codebook() {
 cudaError_t launch_wht4_quantize_append(const Fp16AppendArgs& a, cudaStream_t stream) {
     const long long rows = 2LL * a.B * a.n_new * a.Hkv;
     if (rows == 0) return cudaSuccess;
-    const int grid = resident_grid((rows + 7) / 8);
+    const int grid = resident_grid(((rows / 2 + 31) / 32 + 7) / 8);  // CTAs of 8 warps, blocks of 32 rows
     if (grid < 0) return cudaErrorUnknown;
     Wht4QuantArgs w;
     w.a = a;
