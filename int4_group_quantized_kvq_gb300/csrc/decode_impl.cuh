@@ -364,8 +364,15 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     const int g = lane >> 2;   // fragment row group
     const int c = lane & 3;    // thread in group
     const int stages = p.stages;
-    const int ubytes = p.unit_bytes;
-    const int bbytes = p.block_bytes;
+    // block layout: with 16-token pages it is fixed by the template (K codes, V codes, K
+    // scales, V scales, the block rounded up to 16 bytes), so offsets fold into the loads
+    constexpr int kVC = 16 * ROW, kKS = 32 * ROW, kVS = kKS + 16 * NGK * SB;
+    constexpr int kBB = (kVS + 16 * NGV * SB + 15) / 16 * 16;
+    const int bbytes = P16 ? kBB : p.block_bytes;
+    const int ubytes = P16 ? HK * kBB : p.unit_bytes;
+    const int l_vcodes = P16 ? kVC : p.v_codes;
+    const int l_kscales = P16 ? kKS : p.k_scales;
+    const int l_vscales = P16 ? kVS : p.v_scales;
     const size_t ring_all = static_cast<size_t>(kWarps) * stages * ubytes;
     uint8_t* ring = smem + static_cast<size_t>(warp) * stages * ubytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_all) + warp * stages;
@@ -513,9 +520,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     const int a_col = HK == 1 ? 0 : (g >> 1);
     // per-thread byte offsets inside a unit buffer (chunk 0)
     const int k_off = g * ROW + c * (KW * 4);
-    const int ks_off = a_row * bbytes + p.k_scales + g * NGK * SB;
-    const int vs_off = a_row * bbytes + p.v_scales + g * NGV * SB;
-    const int v_off = p.v_codes + c * ROW + g * (I8 ? 16 : VB);
+    const int ks_off = a_row * bbytes + l_kscales + g * NGK * SB;
+    const int vs_off = a_row * bbytes + l_vscales + g * NGV * SB;
+    const int v_off = l_vcodes + c * ROW + g * (I8 ? 16 : VB);
     const int src0 = 4 * c + (g >> 1);
     const int src1 = 4 * (c + 4) + (g >> 1);
     const bool want_lo = (g & 1) != 0;
