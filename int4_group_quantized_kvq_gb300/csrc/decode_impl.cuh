@@ -316,12 +316,33 @@ __device__ __noinline__ void append_rows(const KParams& p, const int32_t* aps, u
     }
 }
 
-// Scale i of a run of per-token scales at p: fp16 (the INT4 cache's per group) or fp32
-// (the INT8 cache's per row).
-template <bool F32>
-__device__ __forceinline__ float load_scale(const uint8_t* p, int i) {
-    if constexpr (F32) return reinterpret_cast<const float*>(p)[i];
-    else return __half2float(reinterpret_cast<const __half*>(p)[i]);
+// The N scales of a token row at p (fp16 per group for the INT4 cache, fp32 per row for
+// the INT8 cache) and those of the row 8 tokens further: fp16 pairs read as one word.
+template <bool F32, int N>
+__device__ __forceinline__ void load_scales(const uint8_t* p, float (&a)[N], float (&b)[N]) {
+    if constexpr (F32) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            a[i] = reinterpret_cast<const float*>(p)[i];
+            b[i] = reinterpret_cast<const float*>(p)[8 * N + i];
+        }
+    } else if constexpr (N % 2 == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
+            const float2 fa = __half22float2(reinterpret_cast<const __half2*>(p)[i / 2]);
+            const float2 fb = __half22float2(reinterpret_cast<const __half2*>(p)[(8 * N + i) / 2]);
+            a[i] = fa.x;
+            a[i + 1] = fa.y;
+            b[i] = fb.x;
+            b[i + 1] = fb.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            a[i] = __half2float(reinterpret_cast<const __half*>(p)[i]);
+            b[i] = __half2float(reinterpret_cast<const __half*>(p)[8 * N + i]);
+        }
+    }
 }
 
 // P16: the pages hold 16 tokens (P == 16), so two one-head units, i.e. two pages, make a
@@ -507,7 +528,9 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     }
 
     uint32_t qb[KSTEPS][NTQ][2];
-    float q8[NTQ][2];  // kOff * the sum of q over the group of this thread's score columns 2c, 2c + 1
+    float q8[NTQ][2];  // kOff * the sum of q over the group of this thread's score columns 2c, 2c + 1,
+                       // times softmax_scale * log2 e
+    const float s24 = 16777216.0f * p.scale_log2;  // 2^24 * softmax_scale * log2 e
     float m[HS], l[HS];
     float o[MT][HS][4];
     int Leff = 0;  // positions of the segment's sequence (clamped to its block table)
@@ -627,11 +650,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 }
             const uint8_t* s0 = blk[X] + chk[X] * 16 * NGK * SB + ks_off;
             float skg[NGK], skg8[NGK];
-#pragma unroll
-            for (int R = 0; R < NGK; ++R) {
-                skg[R] = load_scale<I8>(s0, R);
-                skg8[R] = load_scale<I8>(s0, 8 * NGK + R);
-            }
+            load_scales<I8, NGK>(s0, skg, skg8);
 #pragma unroll
             for (int s = 0; s < HS; ++s) {
                 float z0 = 0.f, z1 = 0.f;
@@ -639,12 +658,13 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 for (int R = 0; R < NGK; ++R) {
                     // the group's code dot product sum (n - off) q = 2^24 S - off sum q
                     const int pi = s * NGK + R;
+                    // (times softmax_scale * log2 e, folded into both terms)
                     const float qo = q8[pi >> 1][pi & 1];
-                    z0 = fmaf(skg[R], fmaf(sacc[pi >> 1][pi & 1], 16777216.0f, -qo), z0);
-                    z1 = fmaf(skg8[R], fmaf(sacc[pi >> 1][2 + (pi & 1)], 16777216.0f, -qo), z1);
+                    z0 = fmaf(skg[R], fmaf(sacc[pi >> 1][pi & 1], s24, -qo), z0);
+                    z1 = fmaf(skg8[R], fmaf(sacc[pi >> 1][2 + (pi & 1)], s24, -qo), z1);
                 }
-                z[X][s][0] = z0 * p.scale_log2;
-                z[X][s][1] = z1 * p.scale_log2;
+                z[X][s][0] = z0;
+                z[X][s][1] = z1;
                 if (MASKED) {
                     z[X][s][0] = vg[X] ? z[X][s][0] : -INFINITY;
                     z[X][s][1] = vg8[X] ? z[X][s][1] : -INFINITY;
@@ -699,11 +719,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
         for (int X = 0; X < TG; ++X) {
             const uint8_t* s0 = blk[X] + chk[X] * 16 * NGV * SB + vs_off;
             float svg[NGV], svg8[NGV];
-#pragma unroll
-            for (int R = 0; R < NGV; ++R) {
-                svg[R] = load_scale<I8>(s0, R);
-                svg8[R] = load_scale<I8>(s0, 8 * NGV + R);
-            }
+            load_scales<I8, NGV>(s0, svg, svg8);
 #pragma unroll
             for (int s = 0; s < HS; ++s) {
 #pragma unroll
@@ -932,8 +948,8 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 // thread's score columns 2c and 2c + 1 are those of the threads with g = 2c, 2c + 1
                 qs += __shfl_xor_sync(0xffffffffu, qs, 1);
                 qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-                q8[t][0] = kOff * __shfl_sync(0xffffffffu, qs, 8 * c);
-                q8[t][1] = kOff * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
+                q8[t][0] = (kOff * p.scale_log2) * __shfl_sync(0xffffffffu, qs, 8 * c);
+                q8[t][1] = (kOff * p.scale_log2) * __shfl_sync(0xffffffffu, qs, 8 * c + 4);
             }
         }
         // this warp is done with the segment's q buffer (a warp with units here has waited
