@@ -153,15 +153,16 @@ __device__ __forceinline__ uint4 int8_lane16(const uint4 (&raw)[2], float& scale
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rs) : "f"(s));
     constexpr float kMagic = 12582912.0f;          // 1.5 * 2^23
     constexpr float kBand = 0.4998779296875f;      // 1/2 - 2^-13
-    bool slow = false;
     uint32_t m[16];
+    float emax = 0.f;  // the largest |e|, NaN if any e is NaN
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const float mi = fmaf(x[i], rs, kMagic);
         const float e = fmaf(x[i], rs, kMagic - mi);  // kMagic - mi = -r exactly
-        slow |= !(fabsf(e) <= kBand);
+        emax = max_abs_nan(emax, e);
         m[i] = __float_as_uint(mi);
     }
+    const bool slow = !(emax <= kBand);
     if (slow) return int8_slow16(raw[0], raw[1], s);
     uint32_t w[4];
 #pragma unroll

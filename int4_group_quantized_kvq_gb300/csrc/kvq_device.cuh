@@ -147,6 +147,14 @@ __device__ __forceinline__ uint32_t unpack_hi(uint32_t w) {
     return h2_fma(lop3_and_or(w, 0x00F000F0u, 0x64006400u), 0x2C002C00u /* 1/16 */, 0xD480D480u /* -72 */);
 }
 
+// max(a, |b|), NaN when either is NaN (max.NaN), so one instruction can track both the
+// largest magnitude and any NaN among a run of values.
+__device__ __forceinline__ float max_abs_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(fabsf(b)));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));

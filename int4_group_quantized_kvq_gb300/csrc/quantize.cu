@@ -41,8 +41,10 @@ constexpr float kInv7 = 0.142857149f;  // 0x3E124925
 //    the slower path of quant_lane8's arithmetic, the exact half-integer check and the clamp,
 //    for all its values.  The band is narrow: a warp's 512 values rarely send it there;
 //  * a NaN input makes its e NaN, and an infinite scale (from an infinite input) makes that
-//    input's e = inf * 0 = NaN, so both reach the slower path through the same test
-//    (written to hold for NaN); there they take the IEEE division, as in quant_lane8;
+//    input's e = inf * 0 = NaN, so both reach the slower path through the same test: the
+//    lane's largest |e| is kept by a NaN-propagating maximum (one instruction a value) and
+//    the test is written to hold for NaN; there they take the IEEE division, as in
+//    quant_lane8;
 //  * on the fast path a nibble n = r + 8 is in [1, 15] and m's bit pattern is 0x4B4000 << 8
 //    | n: bits 4 .. 21 are zero.  So m0 + 16 m1 holds the byte of two nibbles in its low 8
 //    bits with zeros above up to bit 21, b0 + 256 b1 holds two such bytes in its low 16 bits,
@@ -75,15 +77,16 @@ __device__ __forceinline__ uint2 quant_lane16(const uint4 (&raw)[2], int lg16, _
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rs) : "f"(s));
     constexpr float kMagic8 = 12582920.0f;  // 1.5 * 2^23 + 8
     constexpr float kBand = 0.4999847412109375f;  // 1/2 - 2^-16
-    bool slow = amax * rs > 7.49f;
     uint32_t m[16];
+    float emax = 0.f;  // the largest |e|, NaN if any e is NaN
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const float mi = fmaf(x[i], rs, kMagic8);
         const float e = fmaf(x[i], rs, kMagic8 - mi);  // kMagic8 - mi = -r exactly
-        slow |= !(fabsf(e) <= kBand);
+        emax = max_abs_nan(emax, e);
         m[i] = __float_as_uint(mi);
     }
+    const bool slow = amax * rs > 7.49f || !(emax <= kBand);
     uint32_t h[4];  // h[k]: the nibbles of values 4k .. 4k + 3 in its low 16 bits
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
