@@ -130,14 +130,13 @@ __device__ __forceinline__ uint32_t wht4_lane8(uint4 raw, const float* thr, int 
                 y[j] = __fadd_rn(a, b);
                 y[j + h] = __fsub_rn(a, b);
             }
+    // across lanes: lower a + b, upper a - b, as other + sgn * mine with sgn = +-1 (one
+    // rounding of the exact sum, so the same value as the add or the subtract)
 #pragma unroll
     for (int X = 1; X < 16; X <<= 1) {
-        const bool upper = (tl & X) != 0;
+        const float sgn = (tl & X) != 0 ? -1.f : 1.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float other = __shfl_xor_sync(0xffffffffu, y[j], X);
-            y[j] = upper ? __fsub_rn(other, y[j]) : __fadd_rn(y[j], other);
-        }
+        for (int j = 0; j < 8; ++j) y[j] = fmaf(y[j], sgn, __shfl_xor_sync(0xffffffffu, y[j], X));
     }
     uint32_t packed = 0;
     if (sigma > 0.f) {
