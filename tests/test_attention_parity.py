@@ -140,3 +140,13 @@ def test_many_one_page_segments_per_cta(kvq):
     got, flags = gpu_decode(kvq, case, torch.from_numpy(pool_np).cuda())
     assert flags == 0
     assert_attention_close(got, case.oracle_attention(pool_np), what="B2100")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 4)])
+def test_extreme_k_codes(kvq, Hq, Hkv):
+    # K rows whose every code is +-7 (nibbles 1 and 15, the ends of the score's offset
+    # correction, 2^24 S - 8 sum q) and q rows of one sign, where the correction is largest
+    case = Case(2, Hq, Hkv, 128, [77, 40], seed=Hq + 130)
+    case.k = torch.where(case.k >= 0, 3.0, -3.0).half()
+    case.q = case.q.abs()
+    _run(kvq, case)

@@ -101,3 +101,26 @@ def test_int8_attention_long_and_ragged(kvq):
     _check_attention(kvq, Case(1, 32, 8, 128, [6000], seed=121))
     _check_attention(kvq, Case(33, 8, 2, 128, np.random.default_rng(122).integers(1, 700, size=33).tolist(),
                                seed=122))
+
+
+@pytest.mark.parametrize("P", [32, 64])
+def test_int8_attention_eight_heads_per_kv_head_large_pages(kvq, P):
+    # two query-head slots per thread (8 query heads per kv head) on pages taken two 16-token chunks at a time
+    _check_attention(kvq, Case(3, 16, 2, 128, [5 * P + 3, 1, 2 * P], P=P, seed=P + 123))
+
+
+def test_int8_attention_batch_over_the_local_prefix_limit(kvq):
+    # more than 256 sequences: the combine reads the pages prefix the decode grid publishes
+    lens = np.random.default_rng(124).integers(0, 90, size=300).tolist()
+    _check_attention(kvq, Case(300, 8, 8, 128, lens, seed=124), max_len=128)
+
+
+def test_int8_attention_extreme_codes(kvq):
+    # K rows whose first 64 codes are all +-127 (the ends of the score's offset-corrected
+    # range, codes + 128 as subnormals), a zero V row (floor scale) and a V row of one
+    # large value
+    case = Case(2, 8, 4, 128, [70, 33], seed=125)
+    case.k[:, :, :, :64] = torch.where(case.k[:, :, :, :64] > 0, 100.0, -100.0).half()
+    case.v[:, 5] = 0
+    case.v[:, 6, :, 3] = -7.0
+    _check_attention(kvq, case)
