@@ -165,7 +165,8 @@ size_t kvq_decode_workspace_bytes(const kvq_cache_config *cfg, int32_t batch, in
  *                 to read flags); the rest holds the split-KV partial results of the
  *                 call, written before they are read, so it needs no initialisation and
  *                 can serve any call whose shape needs no more bytes.
- * num_q_heads must be a multiple of num_kv_heads with a ratio of at most 8.
+ * num_q_heads must be a multiple of num_kv_heads with a ratio of at most 8 (at most 4 at
+ * head_dim 256, where group_k must be 64 or 128; KVQ_EUNSUPPORTED otherwise).
  * Two kernels run: the decode grid, which leaves one partial result per warp and
  * segment in the workspace, and a combine grid that merges them into out.
  * Launch overlap: both are launched with programmatic dependent launch.  While the
