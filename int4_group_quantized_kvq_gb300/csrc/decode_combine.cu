@@ -31,13 +31,12 @@ struct CParams {
 };
 
 constexpr int kCombineMaxWarps = 16;
-constexpr int kCombineBatch = 8;      // partials loaded together by a warp
 constexpr int kCombineLocalB = 256;   // up to this batch the row metadata is computed before the wait
 
 // One CTA per output row (b, hq).  In source s the row's partials sit at W * (cf + seg) + j
 // for j < W * (cl - cf + 1), where CTAs cf..cl of that grid hold the units of segment
 // seg = (b, hq / ns); when some CTA slices are empty (fewer units than CTAs) their partials
-// do not exist.  Warp w of the CTA takes partials w, w + nw, ..., eight at a time, keeping
+// do not exist.  Warp w of the CTA takes partials w, w + nw, ..., NB at a time, keeping
 // a running maximum M and sum L and an unnormalised output (lane l: dimensions 4f .. 4f + 3
 // for f = l, l + 32, ... below D / 4),
 // over the sources in turn; the warps' results are then merged with weights 2^(M_w - max M).
@@ -45,11 +44,18 @@ constexpr int kCombineLocalB = 256;   // up to this batch the row metadata is co
 // combine of flash decoding: out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
 // NSRC: sources of partials (p.nsrc), a template parameter so the one-source combine
 // carries no code for a second.
-template <int D, int NSRC>
-__global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams p) {
+// NB: partials a warp loads together.  8 for rows with many partials (up to 16 warps a
+// CTA, one CTA per SM is enough); 4 for the 4-warp CTAs of rows with few partials, held
+// to 64 registers so that 8 CTAs fit on an SM (6 at head_dim 256, whose rows need more):
+// a batch of many short rows (a thousand or more) then runs as one wave instead of
+// waiting for a second one.
+template <int D, int NSRC, int NB>
+__global__ void __launch_bounds__(NB == 8 ? kCombineMaxWarps * 32 : 128, NB == 8 ? 1 : (D == 256 ? 6 : 8))
+combine_kernel(CParams p) {
     static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
-    constexpr int NV = (D / 4 + 31) / 32;  // float4 of the row per lane
-    constexpr int NA = NV == 1 ? 4 : 2;    // independent sums per float4 (shorter fma chains)
+    static_assert(NB == 8 || NB == 4, "8 partials a batch, or 4 for the 4-warp CTAs");
+    constexpr int NV = (D / 4 + 31) / 32;                 // float4 of the row per lane
+    constexpr int NA = NB == 4 ? 1 : (NV == 1 ? 4 : 2);  // independent sums per float4 (shorter fma chains)
     auto lane_has = [](int lane, int v) { return D / 4 >= 32 || lane + 32 * v < D / 4; };
     // the next decode call may start its set-up; it waits for this grid before it
     // touches the workspace
@@ -143,11 +149,11 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
         const long long stride_o = static_cast<long long>(s.ns) * D;
         const float* ml0 = s.ws_ml + (base[si] * s.ns + sl) * 2;
         const float* o0 = s.ws_o + (base[si] * s.ns + sl) * D + 4 * lane;
-        for (int j0 = warp; j0 < n[si]; j0 += kCombineBatch * nw) {
-            float2 ml[kCombineBatch];
-            float4 ov[kCombineBatch][NV];
+        for (int j0 = warp; j0 < n[si]; j0 += NB * nw) {
+            float2 ml[NB];
+            float4 ov[NB][NV];
 #pragma unroll
-            for (int kk = 0; kk < kCombineBatch; ++kk) {
+            for (int kk = 0; kk < NB; ++kk) {
                 const int j = j0 + kk * nw;
                 bool have = j < n[si];
                 if (have && !dense) {
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
             }
             float mb = M;
 #pragma unroll
-            for (int kk = 0; kk < kCombineBatch; ++kk) mb = fmaxf(mb, ml[kk].x);
+            for (int kk = 0; kk < NB; ++kk) mb = fmaxf(mb, ml[kk].x);
             if (mb == -INFINITY) continue;  // only empty partials so far
             if (mb > M) {  // a larger running maximum: rescale what has been summed
                 const float f = fast_exp2(M - mb);
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kCombineMaxWarps * 32) combine_kernel(CParams 
                 M = mb;
             }
 #pragma unroll
-            for (int kk = 0; kk < kCombineBatch; ++kk) {
+            for (int kk = 0; kk < NB; ++kk) {
                 const float f = fast_exp2(ml[kk].x - M);
                 L = fmaf(f, ml[kk].y, L);
 #pragma unroll
@@ -278,10 +284,14 @@ cudaError_t launch(const decode::CParams& p, int d, int warps, cudaStream_t stre
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t err;
-    if (p.nsrc == 2) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 2>, p);  // mixed: head_dim 128 only
-    else if (d == 64) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<64, 1>, p);
-    else if (d == 256) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<256, 1>, p);
-    else if (d == 128) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 1>, p);
+    const bool few = warps == 4;  // rows of few partials: the 64-register instance
+    if (p.nsrc == 2) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 2, 8>, p);  // mixed: head_dim 128 only
+    else if (d == 64) err = few ? cudaLaunchKernelEx(&cfg, decode::combine_kernel<64, 1, 4>, p)
+                                : cudaLaunchKernelEx(&cfg, decode::combine_kernel<64, 1, 8>, p);
+    else if (d == 256) err = few ? cudaLaunchKernelEx(&cfg, decode::combine_kernel<256, 1, 4>, p)
+                                 : cudaLaunchKernelEx(&cfg, decode::combine_kernel<256, 1, 8>, p);
+    else if (d == 128) err = few ? cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 1, 4>, p)
+                                 : cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 1, 8>, p);
     else return cudaErrorInvalidValue;
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
