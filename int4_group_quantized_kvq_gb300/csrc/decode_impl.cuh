@@ -870,8 +870,6 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
         const long long fu = ua + (((c0 + warp - ua) % kWarps) + kWarps) % kWarps;  // my first unit here
         const int cnt = fu < ue ? static_cast<int>((ue - fu + kWarps - 1) / kWarps) : 0;
         const int pg0 = static_cast<int>(fu - sfirst);
-        int last_st = -1;   // stage of the last unit consumed in this segment
-        int held[2] = {-1, -1}, held_i[2] = {0, 0};  // stages whose refill waits for the partial
 
         // the next segment's q rows start moving now, into the buffer of segment segk - 1
         // once every warp has taken its fragments out of it
@@ -1033,24 +1031,12 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 }
             }
 
-            // ---- release the stages and refill them with the units `stages` ahead; the
-            // segment's last stage(s) are refilled after the merge below ----
-            const bool last = j + n == cnt;
-            last_st = n == 2 ? st1 : cst;
+            // ---- release the stages and refill them with the units `stages` ahead ----
             if (!failed) {
                 __syncwarp();
                 if (lane == 0) fence_proxy_async_smem();
-                if (!last) {
-                    if (consumed + stages < nm) issue(consumed + stages, cst);
-                    if (n == 2 && consumed + 1 + stages < nm) issue(consumed + 1 + stages, st1);
-                } else {
-                    held[0] = cst;
-                    held_i[0] = consumed + stages;
-                    if (n == 2) {
-                        held[1] = st1;
-                        held_i[1] = consumed + 1 + stages;
-                    }
-                }
+                if (consumed + stages < nm) issue(consumed + stages, cst);
+                if (n == 2 && consumed + 1 + stages < nm) issue(consumed + 1 + stages, st1);
             }
             consumed += n;
             cst = st1;
@@ -1078,36 +1064,31 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 lt[s] += __shfl_xor_sync(0xffffffffu, lt[s], 16);
             }
             if (cnt > 0 && !failed) {
-                // staged through the ring stage just consumed ([4][D] floats per round of
-                // four slots), then written out in rows of 512 bytes
-                float* sbuf = reinterpret_cast<float*>(ring + last_st * ubytes);
+                // straight from the accumulators: thread (g, c) holds dimensions dd, dd + 1 of
+                // slot c for each P.V tile; its VB tiles of a V group give it 2 VB consecutive
+                // floats and thread (g + 1, c) continues them, so every 32-byte sector of a row
+                // is written whole by one store instruction or by one thread's stores in a row.
+                // (Staging the rows through a ring stage for 16-byte stores kept that stage
+                // from being refilled until the partial was out: a gap in the ring at every
+                // segment end.)
 #pragma unroll
                 for (int s = 0; s < HS; ++s) {
                     const int nsr = min(4, p.ns - 4 * s);  // slots in this round
+                    if (c < nsr) {
+                        float* orow = p.ws_o + (piece * p.ns + 4 * s + c) * D;
 #pragma unroll
-                    for (int R = 0; R < NGV; ++R)
+                        for (int R = 0; R < NGV; ++R)
 #pragma unroll
-                        for (int jb = 0; jb < VB; ++jb) {
-                            const int mt = R * VB + jb;
-                            const int dd = 2 * (R * (GV / 2) + g * VB + jb);
-                            *reinterpret_cast<float2*>(sbuf + c * D + dd) =
-                                make_float2(o[mt][s][0] + o[mt][s][1], o[mt][s][2] + o[mt][s][3]);
-                        }
-                    __syncwarp();
-                    for (int k = 0; k < nsr; ++k)
-#pragma unroll
-                        for (int f = lane; f < D / 4; f += 32)  // D / 4 float4 a row
-                            reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + 4 * s + k) * D)[f] =
-                                reinterpret_cast<const float4*>(sbuf + k * D)[f];
+                            for (int jb = 0; jb < VB; ++jb) {
+                                const int mt = R * VB + jb;
+                                const int dd = 2 * (R * (GV / 2) + g * VB + jb);
+                                *reinterpret_cast<float2*>(orow + dd) =
+                                    make_float2(o[mt][s][0] + o[mt][s][1], o[mt][s][2] + o[mt][s][3]);
+                            }
+                    }
                     if (g == 0 && c < nsr)
                         *reinterpret_cast<float2*>(p.ws_ml + (piece * p.ns + 4 * s + c) * 2) = make_float2(m[s], lt[s]);
-                    __syncwarp();
                 }
-                fence_proxy_async_smem();  // the stage is refilled by the bulk copy engine next
-                __syncwarp();
-#pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    if (held[k] >= 0 && held_i[k] < nm) issue(held_i[k], held[k]);
             } else {
                 // no units of this segment here (or a failed wait): an empty partial
                 if (lane < p.ns)
