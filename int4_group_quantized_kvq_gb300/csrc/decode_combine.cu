@@ -44,15 +44,12 @@ constexpr int kCombineLocalB = 256;   // up to this batch the row metadata is co
 // combine of flash decoding: out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
 // NSRC: sources of partials (p.nsrc), a template parameter so the one-source combine
 // carries no code for a second.
-// NB: partials a warp loads together, 8 or 4.  The 4-partial instance is held to 64
-// registers (at head_dim 256 it may take more, which its rows need).  It serves two
-// kinds of rows:
-//  - rows of few partials (4-warp CTAs): 8 CTAs then fit on an SM, so a batch of a
-//    thousand or more short rows runs as one wave instead of waiting for a second;
-//  - rows of many partials (16-warp CTAs): at up to 128 registers such a CTA would hold
-//    a whole SM's register file and keep the next call's decode CTAs off that SM until
-//    it leaves; at 64 it holds half.
-// Rows of 8-warp CTAs (up to 64 partials) load 8 at a time, in one round.
+// NB: partials a warp loads together, 8 or 4.  The 4-partial instance, held to 64
+// registers (at head_dim 256 it may take more, which its rows need), serves the rows of
+// many partials (16-warp CTAs): at up to 128 registers such a CTA would hold a whole SM's
+// register file and keep the next call's decode CTAs off that SM until it leaves; at 64
+// it holds half.  Rows of 4- and 8-warp CTAs (up to 64 partials) load 8 at a time, in
+// one round.
 template <int D, int NSRC, int NB>
 __global__ void __launch_bounds__(kCombineMaxWarps * 32, NB == 8 || D == 256 ? 1 : 2)
 combine_kernel(CParams p) {
@@ -288,7 +285,7 @@ cudaError_t launch(const decode::CParams& p, int d, int warps, cudaStream_t stre
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t err;
-    const bool light = warps != 8;  // 4 or 16 warps: the 64-register instance
+    const bool light = warps == 16;  // the 64-register instance
     if (p.nsrc == 2) err = cudaLaunchKernelEx(&cfg, decode::combine_kernel<128, 2, 8>, p);  // mixed: head_dim 128 only
     else if (d == 64) err = light ? cudaLaunchKernelEx(&cfg, decode::combine_kernel<64, 1, 4>, p)
                                   : cudaLaunchKernelEx(&cfg, decode::combine_kernel<64, 1, 8>, p);
