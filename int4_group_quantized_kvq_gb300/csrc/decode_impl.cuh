@@ -95,9 +95,11 @@ struct CtaCtl {
     uint64_t pad[12];
 };
 static_assert(sizeof(CtaCtl) == 128, "the planner reserves 128 bytes");
-// two buffers of up to 8 query-head rows of head_dim D fp16
+// two buffers of kQRows rows of head_dim D fp16: a segment's query-head rows (up to 8)
+// and, in the decode step, its new token's K rows and V rows (2 HK; q rows + 2 HK <= 12)
+constexpr int kQRows = 12;
 template <int D>
-constexpr int q_buf_bytes() { return 2 * 8 * D * 2; }
+constexpr int q_buf_bytes() { return 2 * kQRows * D * 2; }
 
 struct KParams {
     const uint8_t* pool;
@@ -247,6 +249,47 @@ __device__ __forceinline__ const uint8_t* unit_block(const KParams& p, const int
     return p.pool + (static_cast<long long>(page) * p.Hkv + static_cast<long long>(hg) * HK) * p.block_bytes;
 }
 
+// The page (index in sequence sb's block-table row) taking the sequence's appended token
+// when this call streams that page, else -1: no append, or an append into a page the call
+// does not attend (those are written by the grid's spare warps).
+template <bool WIN>
+__device__ __forceinline__ int seg_append(const KParams& p, const int32_t* pre, const int32_t* lens,
+                                          const int32_t* aps, int sb) {
+    const int apos = aps[sb];
+    if (apos < 0) return -1;
+    const long long apg = static_cast<long long>(apos) >> p.lg_p;
+    if (apg >= p.max_blocks) return -1;
+    if (WIN)
+        return span_index(seq_span(lens[sb], p.lg_p, p.max_blocks, p.window, p.sinks), static_cast<int>(apg)) >= 0
+                   ? static_cast<int>(apg)
+                   : -1;
+    return apg < pre[sb + 1] - pre[sb] ? static_cast<int>(apg) : -1;
+}
+
+// unit_block for the INT4 kernel, as an integer whose bit 0 marks a bad page id (the
+// address is then page 0's, 16-byte aligned, and the flag is raised): the producer clears
+// the bit before the copy, the fused append skips such a page.
+template <bool WIN>
+__device__ __forceinline__ unsigned long long unit_addr_tagged(const KParams& p, const int32_t* pre,
+                                                               const int32_t* lens, long long u, int HK) {
+    const int b = find_seq(pre, p.B, p.Hg, u);
+    const long long rem = u - static_cast<long long>(p.Hg) * pre[b];
+    const int np = pre[b + 1] - pre[b];
+    const int hg = static_cast<int>(rem / np);
+    int pg = static_cast<int>(rem - static_cast<long long>(hg) * np);
+    if (WIN) pg = span_page(seq_span(lens[b], p.lg_p, p.max_blocks, p.window, p.sinks), pg);
+    int page = p.block_table[static_cast<long long>(b) * p.max_blocks + pg];
+    unsigned long long bad = 0;
+    if (page < 0 || page >= p.num_pages) {
+        raise_flag(p.status, KVQ_FLAG_BAD_PAGE);
+        page = 0;
+        bad = 1;
+    }
+    return reinterpret_cast<unsigned long long>(
+               p.pool + (static_cast<long long>(page) * p.Hkv + static_cast<long long>(hg) * HK) * p.block_bytes) |
+           bad;
+}
+
 // First unit of slice w of U units split over W slices.
 __device__ __forceinline__ long long slice_start(long long w, long long U, long long W) { return div_nn(w * U, W); }
 
@@ -263,26 +306,25 @@ struct Step {
     bool live[TG];
 };
 
-// Fused append of the decode step: quantize the new token's K and V rows of sequence sb,
-// head group shg (its HK heads) into page index pgu of the sequence, in the pool and,
-// when the page is staged in shared memory at sblk, in that copy too.  All lanes call
-// this.  A row takes D / 8 lanes, 8 values each (the same arithmetic and bytes as the
-// quantize-append kernel): for D <= 128 the K row and the V row in one pass (lanes past
-// 2 D / 8 idle), for D = 256 one after the other.  Out of line: it runs once per segment
-// at most, and inlined into the streaming loop its code would crowd the instruction cache.
+// Fused append of the decode step: quantize the new token's K rows (krows: HK rows of D
+// fp16, one per kv head of the unit) and V rows (vrows) into slot `slot` of the HK
+// consecutive blocks at gblk in the pool and, when the page is staged in shared memory at
+// sblk, into that copy too.  The rows are read through generic pointers: from global
+// memory for an append into a page the call does not stream, from the segment's q buffer
+// (where they were copied with q) for one it does.  All lanes call this.  A row takes
+// D / 8 lanes, 8 values each (the same arithmetic and bytes as the quantize-append
+// kernel): for D <= 128 the K row and the V row in one pass (lanes past 2 D / 8 idle), for
+// D = 256 one after the other.  Out of line: it runs once per segment at most, and inlined
+// into the streaming loop its code would crowd the instruction cache.
 template <int D, int HK>
-__device__ __noinline__ void append_rows(const KParams& p, const int32_t* aps, uint8_t* sblk, int sb, int shg,
-                                         int pgu) {
+__device__ __noinline__ void append_rows(const KParams& p, const __half* krows, const __half* vrows, uint8_t* gblk,
+                                         uint8_t* sblk, int slot) {
     constexpr int LPR = D / 8;                 // lanes per row
     constexpr int ROWS = LPR <= 16 ? 2 : 1;    // rows per pass
     const int lane = threadIdx.x & 31;
-    const int page = p.block_table[static_cast<long long>(sb) * p.max_blocks + pgu];
-    const bool pvalid = page >= 0 && page < p.num_pages;  // else flagged where the page is looked up
-    const int slot = aps[sb] & ((1 << p.lg_p) - 1);
     const int rsel = lane / LPR;               // this lane's row in the pass
     const int tl = lane % LPR;                 // lane within the row
     for (int a = 0; a < HK; ++a) {
-        const int h = shg * HK + a;
 #pragma unroll
         for (int pass = 0; pass < 2 / ROWS; ++pass) {
             const int half = ROWS == 2 ? (rsel & 1) : pass;  // 0: the K row, 1: the V row
@@ -293,13 +335,11 @@ __device__ __noinline__ void append_rows(const KParams& p, const int32_t* aps, u
             const int scale_off = (half ? p.v_scales : p.k_scales) + slot * ng * 2 + (tl >> lg) * 2;
             const bool writes_scale = (tl & ((1 << lg) - 1)) == 0;
             uint4 raw = make_uint4(0, 0, 0, 0);
-            if (active)
-                raw = *reinterpret_cast<const uint4*>((half ? p.v_new : p.k_new) +
-                                                      (static_cast<long long>(sb) * p.Hkv + h) * D + tl * 8);
+            if (active) raw = *reinterpret_cast<const uint4*>((half ? vrows : krows) + a * D + tl * 8);
             __half s16;
             const uint32_t word = quant_lane8<LPR>(raw, lg, s16);
-            if (active && pvalid) {
-                uint8_t* gb = p.pool_w + (static_cast<long long>(page) * p.Hkv + h) * p.block_bytes;
+            if (active) {
+                uint8_t* gb = gblk + a * p.block_bytes;
                 *reinterpret_cast<uint32_t*>(gb + code_off) = word;
                 if (writes_scale) *reinterpret_cast<__half*>(gb + scale_off) = s16;
                 if (sblk != nullptr) {
@@ -360,6 +400,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     static_assert(D <= 128 || (HK == 1 && HS == 1), "head_dim 256: one-head units, up to 4 query heads each");
     static_assert(HK == 1 || HS == 1, "several kv heads per unit only with one query head each");
     static_assert(HK == 1 || P16, "four-head units only for 16-token pages");
+    static_assert(4 * HS + 2 * HK <= kQRows, "q rows and the appended token's K and V rows fit a q buffer");
     constexpr int NGK = D / GK;               // K groups per row
     constexpr int NGV = D / GV;               // V groups per row
     constexpr bool I8 = CODEC == 1;
@@ -397,8 +438,10 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     const size_t ring_all = static_cast<size_t>(kWarps) * stages * ubytes;
     uint8_t* ring = smem + static_cast<size_t>(warp) * stages * ubytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_all) + warp * stages;
-    CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + ring_all + kWarps * stages * sizeof(uint64_t));
-    __half* qbuf = reinterpret_cast<__half*>(ctl + 1);  // [2][8][D]
+    // the (tagged) pool address of the unit each stage holds, kept for the fused append
+    unsigned long long* uaddr = reinterpret_cast<unsigned long long*>(smem + ring_all) + kWarps * stages + warp * stages;
+    CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + ring_all + 2 * kWarps * stages * sizeof(uint64_t));
+    __half* qbuf = reinterpret_cast<__half*>(ctl + 1);  // [2][kQRows][D]
     int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(qbuf) + q_buf_bytes<D>());
     int32_t* lens = pre + p.B + 1;
     int32_t* aps = lens + p.B;
@@ -449,7 +492,12 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 if (lane == 0) raise_flag(p.status, KVQ_FLAG_BAD_PAGE);
                 continue;
             }
-            if constexpr (!I8) append_rows<D, HK>(p, aps, nullptr, sb, shg, static_cast<int>(apg));
+            if constexpr (!I8) {
+                const long long row = static_cast<long long>(sb) * p.Hkv + static_cast<long long>(shg) * HK;
+                append_rows<D, HK>(p, p.k_new + row * D, p.v_new + row * D,
+                                   p.pool_w + (static_cast<long long>(page) * p.Hkv + shg * HK) * p.block_bytes,
+                                   nullptr, apos & ((1 << p.lg_p) - 1));
+            }
         }
     };
 
@@ -480,45 +528,60 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     // window's addresses are looked up one window ahead so their loads overlap work ----
     auto unit_of = [&](int i) { return c0 + warp + static_cast<long long>(kWarps) * i; };
     int wbase = 0;
-    unsigned long long waddr =
-        lane < nm ? reinterpret_cast<unsigned long long>(unit_block<WIN>(p, pre, lens, unit_of(lane), HK)) : 0ull;
-    unsigned long long wnext =
-        32 + lane < nm ? reinterpret_cast<unsigned long long>(unit_block<WIN>(p, pre, lens, unit_of(32 + lane), HK)) : 0ull;
+    unsigned long long waddr = lane < nm ? unit_addr_tagged<WIN>(p, pre, lens, unit_of(lane), HK) : 0ull;
+    unsigned long long wnext = 32 + lane < nm ? unit_addr_tagged<WIN>(p, pre, lens, unit_of(32 + lane), HK) : 0ull;
     int issued = 0;
     const uint64_t l2_stream = l2_policy_evict_first();  // pages are read once per call
     auto issue = [&](int i, int st) {  // this warp's unit i into stage st; i increases call by call
         if (i - wbase >= 32) {
             wbase += 32;
             waddr = wnext;
-            wnext = wbase + 32 + lane < nm
-                        ? reinterpret_cast<unsigned long long>(unit_block<WIN>(p, pre, lens, unit_of(wbase + 32 + lane), HK))
-                        : 0ull;
+            wnext = wbase + 32 + lane < nm ? unit_addr_tagged<WIN>(p, pre, lens, unit_of(wbase + 32 + lane), HK) : 0ull;
         }
         const unsigned long long src = __shfl_sync(0xffffffffu, waddr, i - wbase);
         if (lane == 0) {
+            uaddr[st] = src;
             const uint32_t bar = bar0 + 8 * st;
             mbar_arrive_expect_tx(bar, ubytes);
-            bulk_g2s_hint(ring0 + st * ubytes, reinterpret_cast<const void*>(src), ubytes, bar, l2_stream);
+            bulk_g2s_hint(ring0 + st * ubytes, reinterpret_cast<const void*>(src & ~1ull), ubytes, bar, l2_stream);
         }
         ++issued;
     };
+    // The q rows of segment (sb, shg) into q buffer k & 1 (thread 0), and in the decode step,
+    // when the segment's new token lands in a page this call streams, that token's K and V
+    // rows of the segment's HK kv heads after them (rows ns .. ns + 2 HK - 1): the warp that
+    // streams the page quantizes them from there, instead of loading them from global memory
+    // in the middle of the stream, where a load waits behind the SM's page copies in flight.
+    const uint32_t q_bytes = static_cast<uint32_t>(p.ns) * D * 2;
+    auto issue_q = [&](int sb, int shg, int k) {
+        const uint32_t bar = qbar0 + 8 * (k & 1);
+        __half* dst = qbuf + (k & 1) * kQRows * D;
+        const bool rows = !I8 && seg_append<WIN>(p, pre, lens, aps, sb) >= 0;
+        const uint32_t r_bytes = HK * D * 2;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, q_bytes + (rows ? 2 * r_bytes : 0));
+        bulk_g2s(smem_u32(dst), p.q + (static_cast<long long>(sb) * p.Hq + shg * p.ns) * D, q_bytes, bar);
+        if (rows) {
+            const long long row = static_cast<long long>(sb) * p.Hkv + static_cast<long long>(shg) * HK;
+            bulk_g2s(smem_u32(dst + p.ns * D), p.k_new + row * D, r_bytes, bar);
+            bulk_g2s(smem_u32(dst + (p.ns + HK) * D), p.v_new + row * D, r_bytes, bar);
+        }
+    };
     // the first segment's q rows (read-only input) can move before the wait, unless the kernel
-    // ahead on the stream writes them (q_after_wait)
+    // ahead on the stream writes them (q_after_wait) or the decode step appends (its K and V
+    // rows may be written by that kernel)
+    const bool q_late = p.q_after_wait || p.k_new != nullptr;
     auto issue_first_q = [&]() {
         int b0 = find_seq(pre, p.B, p.Hg, c0);
         const int np0 = pre[b0 + 1] - pre[b0];
         const int hg0 = static_cast<int>(div_nn(c0 - static_cast<long long>(p.Hg) * pre[b0], np0));
-        if (threadIdx.x == 0) {
-            const uint32_t qbytes0 = static_cast<uint32_t>(p.ns) * D * 2;
-            mbar_arrive_expect_tx(qbar0, qbytes0);
-            bulk_g2s(smem_u32(qbuf), p.q + (static_cast<long long>(b0) * p.Hq + hg0 * p.ns) * D, qbytes0, qbar0);
-        }
+        if (threadIdx.x == 0) issue_q(b0, hg0, 0);
     };
-    if (!p.q_after_wait) issue_first_q();
+    if (!q_late) issue_first_q();
 
     // ---- from here on the pool, the output and the workspace are used ----
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (p.q_after_wait) issue_first_q();
+    if (q_late) issue_first_q();
     publish_prefix();
     orphan_appends();
     {
@@ -843,15 +906,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     constexpr bool p16 = P16;
 
     // q rows of a segment go to shared memory by a bulk copy issued one segment ahead
-    // (thread 0); segment k of this CTA uses buffer k & 1 at phase (k >> 1) & 1
-    const uint32_t q_bytes = static_cast<uint32_t>(p.ns) * D * 2;
-    auto issue_q = [&](int sb, int shg, int k) {
-        const uint32_t bar = qbar0 + 8 * (k & 1);
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, q_bytes);
-        bulk_g2s(smem_u32(qbuf + (k & 1) * 8 * D), p.q + (static_cast<long long>(sb) * p.Hq + shg * p.ns) * D, q_bytes,
-                 bar);
-    };
+    // (thread 0, issue_q above); segment k of this CTA uses buffer k & 1 at phase (k >> 1) & 1
     // the segment after (sb, shg), skipping sequences without positions; sb == B when none
     auto next_seg = [&](int& sb, int& shg) {
         if (++shg == p.Hg) {
@@ -863,6 +918,8 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
     };
     int segk = 0;  // segments of this CTA started so far (segment 0's q copy is already issued)
     int apg_seg = -1;  // page index (within the segment's sequence) of its append, if streamed here
+    bool my_app = false;  // this warp streams that page: it keeps the q buffer (which holds the
+                          // token's K and V rows) until it has quantized them
 
     while (sfirst < c1) {
         const long long ua = sfirst > c0 ? sfirst : c0;
@@ -870,6 +927,7 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
         const long long fu = ua + (((c0 + warp - ua) % kWarps) + kWarps) % kWarps;  // my first unit here
         const int cnt = fu < ue ? static_cast<int>((ue - fu + kWarps - 1) / kWarps) : 0;
         const int pg0 = static_cast<int>(fu - sfirst);
+        my_app = false;
 
         // the next segment's q rows start moving now, into the buffer of segment segk - 1
         // once every warp has taken its fragments out of it
@@ -901,9 +959,15 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 Leff = min(lens[b], p.max_blocks * p.P);
             }
             apg_seg = -1;
-            if (aps[b] >= 0 && (WIN ? span_index(sspan, aps[b] >> p.lg_p) >= 0 : (aps[b] >> p.lg_p) < np))
-                apg_seg = aps[b] >> p.lg_p;
-            const __half* qseg = qbuf + (segk & 1) * 8 * D;
+            if constexpr (!I8) {
+                apg_seg = seg_append<WIN>(p, pre, lens, aps, b);
+                if (apg_seg >= 0) {
+                    // its unit, and whether it is one of this warp's (units fu, fu + kWarps, ... < ue)
+                    const long long u = sfirst + (WIN ? span_index(sspan, apg_seg) : apg_seg);
+                    my_app = u >= fu && u < ue && (u - fu) % kWarps == 0;
+                }
+            }
+            const __half* qseg = qbuf + (segk & 1) * kQRows * D;
 #pragma unroll
             for (int t = 0; t < NTQ; ++t) {
                 const int pi = 2 * t + (g & 1);
@@ -951,9 +1015,10 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
             }
         }
         // this warp is done with the segment's q buffer (a warp with units here has waited
-        // for its copy, so the buffer is only reused after the copy has landed)
+        // for its copy, so the buffer is only reused after the copy has landed); the warp
+        // that appends the segment's token releases it after the append
         __syncwarp();
-        if (lane == 0) mbar_arrive(qfree0 + 8 * (segk & 1));
+        if (lane == 0 && !my_app) mbar_arrive(qfree0 + 8 * (segk & 1));
 #pragma unroll
         for (int s = 0; s < HS; ++s) {
             m[s] = -INFINITY;
@@ -992,10 +1057,22 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                 // pages of the two units (list indices past a window gap skip it)
                 const int rA = WIN ? span_page(sspan, pg) : pg;
                 const int rB = WIN ? span_page(sspan, pg + kWarps) : pg + kWarps;
-                // the page taking this step's appended token is patched before it is used
+                // the page taking this step's appended token: the token is quantized from the
+                // rows copied with q, written to the pool (the unit's address was kept when its
+                // copy was issued) and patched into the staged copy before the page is used
                 if constexpr (!I8)
-                    if (apg_seg >= 0 && (rA == apg_seg || (n == 2 && rB == apg_seg)))
-                        append_rows<D, HK>(p, aps, ring + (rA == apg_seg ? cst : st1) * ubytes, b, hg, apg_seg);
+                    if (my_app && (rA == apg_seg || (n == 2 && rB == apg_seg))) {
+                        const int ast = rA == apg_seg ? cst : st1;
+                        const unsigned long long ga = uaddr[ast];
+                        const __half* arow = qbuf + (segk & 1) * kQRows * D + p.ns * D;
+                        if ((ga & 1ull) == 0)  // a bad page id: no append (flagged at its lookup)
+                            append_rows<D, HK>(p, arow, arow + HK * D,
+                                               p.pool_w + (ga - reinterpret_cast<unsigned long long>(p.pool)),
+                                               ring + ast * ubytes, aps[b] & ((1 << p.lg_p) - 1));
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(qfree0 + 8 * (segk & 1));
+                        my_app = false;
+                    }
                 // every position of [t, t + w) attended, and some of it attended
                 auto all_in = [&](int t, int w) { return t + w <= Leff && (!WIN || t >= wlo || t + w <= p.sinks); };
                 auto any_in = [&](int t, int w) { return !WIN || (min(t + w, Leff) > wlo || t < p.sinks); };
@@ -1098,6 +1175,13 @@ __global__ void __launch_bounds__(cta_warps<HS>() * 32, min_ctas<HS, D>()) decod
                     for (int f = lane; f < D / 4; f += 32)
                         reinterpret_cast<float4*>(p.ws_o + (piece * p.ns + k) * D)[f] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
+        }
+
+        // a warp that was to append but did not (a failed wait) releases the q buffer now
+        if (my_app) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qfree0 + 8 * (segk & 1));
+            my_app = false;
         }
 
         // ---- next segment ----

@@ -65,8 +65,9 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
     // of one larger page); larger pages are big enough copies on their own
     plan->hk = (!a.fp16 && r == 1 && a.Hkv % 4 == 0 && a.L.P == 16 && a.L.d <= 128) ? 4 : 1;
     plan->hs = (plan->hk == 1 && r > 4) ? 2 : 1;
-    // CTA bookkeeping (128 bytes) and the two q buffers of 8 rows of head_dim fp16
-    const size_t kCtlBytes = 128 + static_cast<size_t>(2) * 8 * a.L.d * 2;
+    // CTA bookkeeping (128 bytes) and the two q buffers of 12 rows of head_dim fp16 (the q
+    // rows of a segment and, in the decode step, the new token's K and V rows)
+    const size_t kCtlBytes = 128 + static_cast<size_t>(2) * 12 * a.L.d * 2;
     const int hg = a.Hkv / plan->hk;
     const int kWarpsPerCta = 4;  // the kernel's CTA size
     const int ns = plan->hk * r;
@@ -76,13 +77,11 @@ cudaError_t plan_decode(const DecodeArgs& a, DecodePlan* plan) {
                         : a.wht  ? static_cast<size_t>(a.L.P) * (a.L.d + 8)
                         : a.int8 ? static_cast<size_t>(2) * a.L.P * a.L.d + static_cast<size_t>(8) * a.L.P
                                  : static_cast<size_t>(4) * a.L.P * a.L.d;
-    // a warp stages its partial (4 slots x d floats) in a unit buffer
-    if (unit < static_cast<size_t>(4 * (a.L.d + 2)) * sizeof(float)) return cudaErrorInvalidValue;
-
     // Resident CTAs are limited by registers; give each warp as deep a ring of unit
     // buffers as the shared memory left at that occupancy allows.
+    // per warp and stage: the unit buffer, its mbarrier and the unit's pool address
     auto smem_for = [&](int st) {
-        return static_cast<size_t>(kWarpsPerCta) * st * unit + static_cast<size_t>(kWarpsPerCta) * st * 8 +
+        return static_cast<size_t>(kWarpsPerCta) * st * unit + static_cast<size_t>(kWarpsPerCta) * st * 16 +
                kCtlBytes + round_up(static_cast<size_t>(3 * a.B + 1) * 4, 16);
     };
     auto occ_for = [&](size_t smem) {
