@@ -201,6 +201,9 @@ int kvq_decode_attention(const kvq_cache_config *cfg, const void *pool, const vo
  * A position outside the block table or a bad page id skips that append and sets a
  * flag in the workspace status word.  Two sequences appending into the same slot
  * leave either one.
+ * Launch overlap as in kvq_decode_attention, except that q, k_new and v_new are read
+ * only after the kernel ahead on the stream has finished (append_pos, like seq_lens
+ * and block_table, may be read before).
  * Returns KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_EWORKSPACE or KVQ_ECUDA.
  */
 int kvq_decode_step(const kvq_cache_config *cfg, void *pool, const void *k_new, const void *v_new,
