@@ -8,7 +8,8 @@ attend.  Checked against the oracle on the same bytes:
     bit for bit, pool and output.
 Cases cover four-head and one-head units, 8 query heads per kv head, page sizes 16/32/64,
 every group size pair, ragged batches, one long sequence over many CTAs, appends into a
-page the attention does not reach, sequences without an append, and bad positions."""
+page the attention does not reach, sequences without an append, bad positions, and a bad
+page id in the page taking the new token."""
 from __future__ import annotations
 
 import numpy as np
@@ -140,6 +141,28 @@ def test_step_bad_position_flagged(kvq):
     # sequence 0 appends past its block table: skipped and flagged; sequence 1 is normal
     _run(kvq, case, append_pos=[max_pos + 5, 32], seq_lens=[64, 33], expect_flags=kvq.KVQ_FLAG_BAD_POSITION,
          compare_two_calls=False)
+
+
+@pytest.mark.parametrize("Hkv", [8, 2])
+def test_step_bad_page_of_the_append_flagged(kvq, Hkv):
+    # the page taking sequence 0's new token has a bad id in the block table: that append is
+    # skipped (no byte of the pool changes for it, page 0 included, which the kernel reads in
+    # the bad page's place) and flagged; sequence 1 steps as usual.  Hkv = 8: four-head units,
+    # Hkv = 2: one-head units with four query heads each.
+    case = Case(2, 8, Hkv, 128, [64, 33], seed=26 + Hkv)
+    append_pos, seq_lens = [63, 32], [64, 33]
+    pool, k_new, v_new = _setup(case, append_pos, 0x5A)
+    bt_ok = case.block_table.numpy().copy()
+    case.block_table[0, 63 // case.P] = case.num_pages + 5
+    L = case.layout
+    ref = pool.copy()
+    oracle.quantize_append(L, ref, k_new[1:2, None], v_new[1:2, None], bt_ok[1:2], np.array([32], np.int32))
+    got_pool, got_out, flags = _gpu_step(kvq, case, pool, k_new, v_new, append_pos, seq_lens)
+    assert flags == kvq.KVQ_FLAG_BAD_PAGE, f"status flags {flags:#x}"
+    diff = np.nonzero(got_pool != ref)[0]
+    assert diff.size == 0, f"{diff.size} pool bytes differ, first at {diff[:8]}"
+    out_ref = oracle.decode_attention(L, ref, case.q.numpy(), bt_ok, np.array(seq_lens, np.int32), case.scale)
+    assert_attention_close(got_out[1:], out_ref[1:], what=f"sequence 1 beside a bad append page, Hkv {Hkv}")
 
 
 def test_step_repeated_steps_match_oracle(kvq):
