@@ -57,13 +57,13 @@
 //    page): the two score chains interleave and one softmax reduction covers both.
 //  * Split combine.  At the end of each segment (sequence, head group) every warp writes
 //    its own partial (running max, running sum and unnormalised output per slot) to the
-//    workspace, staged through the ring stage it has just consumed; no warp waits for
-//    another, and nothing is counted or fenced on the streaming path, so a warp that
+//    workspace, straight from its accumulators; no warp waits for another, and nothing is counted or fenced on the streaming path, so a warp that
 //    finishes its part of a segment early keeps its copies in flight.  A second, small
 //    kernel, launched behind this one with programmatic dependent launch, merges the
 //    partials of each (sequence, query head) row and writes the output.  The two q
-//    buffers of a CTA are reused once every warp has taken its fragments out (an
-//    mbarrier with one arrival per warp), the only point where warps of a CTA meet.
+//    buffers of a CTA (which in the decode step also carry the new token's K and V rows)
+//    are reused once every warp has taken its fragments out (an mbarrier with one arrival
+//    per warp), the only point where warps of a CTA meet.
 #pragma once
 
 #include <cuda_fp16.h>
